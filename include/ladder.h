@@ -1,0 +1,221 @@
+/*
+ * ladder.h — C ABI of libladder.so: the forward pass of a Ladder Transformer
+ * (prefill and single-token decode) on one GB300 (sm_103a).
+ *
+ * What it computes.  A decoder of n_layers layers, each an attention module
+ * followed by a SwiGLU MLP module, numbered k = 1 .. 2*n_layers.  The residual
+ * stream starts at x_0 = E[token] and every module adds its output to it:
+ *     x_k = x_{k-1} + h_k( RMSNorm(x_in(k)) )
+ * In a standard layer x_in(k) = x_{k-1}.  In a ladder layer the module reads
+ * the stream from one module further back, x_in(k) = x_{k-2}, which is the
+ * staggered residual x_{i+1} = h_{i+1}(x_{i-1}) + x_i of "Ladder Residual:
+ * Parallelism-Aware Architecture for Accelerating Large Model Inference"
+ * (ICML 2025 paper notes, sections 研究背景与动机 "core idea" and 方法详解 /
+ * 关键设计 "staggered residual connection").  The hybrid model of the same
+ * notes (关键设计, "hybrid ladder adaptation") keeps the lower
+ * n_standard_layers standard.  Choices where the pages are silent:
+ *   - x_{-1} := x_0 (the first two ladder modules read the embedding);
+ *   - the first ladder module above a standard block reads x_b, b = 2 *
+ *     n_standard_layers (strict_boundary = 1 reads x_{b-1});
+ *   - module internals follow the Llama-3.1 base: pre-norm RMSNorm with eps
+ *     inside the square root, no biases, grouped-query attention where query
+ *     head h uses KV head h / (n_q_heads / n_kv_heads), rotary embedding on
+ *     interleaved pairs (2j, 2j+1) with angle p * theta^(-2j/head_dim);
+ *   - logits are those of each sequence's last position; the greedy token is
+ *     the argmax with the lowest index on ties.
+ *
+ * Precision.  Weights bf16; accumulation fp32; residual stream fp32; KV cache
+ * bf16; tensor-core operands (prefill) bf16, rounded to nearest even.
+ *
+ * Ownership.  The caller allocates every device buffer (weights, workspace, KV
+ * pool, block table, sequence lengths, outputs) and passes raw device
+ * pointers; the library never allocates device memory.  Weights are borrowed
+ * and must outlive the model.  Handles are host objects owned by the library
+ * and released by the matching *_destroy call.
+ *
+ * Streams.  Every device-side call is asynchronous on the stream given
+ * (a cudaStream_t, 0 = legacy default stream).  A model and its KV handle must
+ * not be used from two streams at once.
+ *
+ * Errors.  Every int-returning call returns LADDER_OK (0) or a negative code.
+ * Arguments are validated on the host before anything is launched, so a call
+ * that fails validation leaves device state untouched.  ladder_last_error()
+ * returns a thread-local message for the last failure.  Device-side checks
+ * (a token id >= vocab) never trap: the kernel records an error word that
+ * ladder_get_device_error() reads back.
+ */
+#ifndef LADDER_H
+#define LADDER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ladder_stream_t; /* same handle as cudaStream_t */
+typedef struct ladder_model ladder_model;
+typedef struct ladder_kv ladder_kv;
+
+enum {
+  LADDER_OK = 0,
+  LADDER_ERR_INVALID = -1,     /* bad argument (null, out of range, misaligned) */
+  LADDER_ERR_CUDA = -2,        /* a CUDA runtime call failed */
+  LADDER_ERR_CAPACITY = -3,    /* workspace, batch, sequence or KV capacity exceeded */
+  LADDER_ERR_UNSUPPORTED = -4  /* valid but not implemented (a shape or option) */
+};
+
+/* Residual schedule selected by ladder_set_mode. */
+enum {
+  LADDER_RESIDUAL_CONFIG = 0,   /* as configured: standard below n_standard_layers, ladder above */
+  LADDER_RESIDUAL_STANDARD = 1  /* every layer standard (the baseline model, same weights) */
+};
+
+/* Flags for ladder_set_mode. */
+enum {
+  LADDER_FLAG_DECODE_GRAPH = 1  /* capture each decode step shape in a CUDA graph and replay it */
+};
+
+/* Model dimensions and capacities.  All int32 fields must be positive unless
+ * stated.  Shape rules: d_model, n_q_heads*head_dim and ffn_dim multiples of
+ * 256; head_dim 64 or 128; n_q_heads a multiple of n_kv_heads with at most 8
+ * query heads per KV head; vocab even. */
+typedef struct {
+  int32_t n_layers;
+  int32_t n_standard_layers;  /* 0 .. n_layers: lower layers with the standard residual */
+  int32_t d_model;
+  int32_t n_q_heads;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t ffn_dim;
+  int32_t vocab;
+  float rope_theta;
+  float norm_eps;
+  int32_t tie_embeddings;     /* 1: lm_head is the embedding table */
+  int32_t rope_interleaved;   /* must be 1 (pairs (2j, 2j+1)) */
+  int32_t shard_k;            /* 1 = off; k > 1 splits each module into k shards summed on device */
+  int32_t page_size;          /* KV positions per page: 16, 32 or 64 */
+  int32_t max_batch;          /* sequences per call, <= 64 */
+  int32_t max_seq;            /* positions per sequence */
+  int32_t max_prefill_tokens; /* packed prompt tokens per prefill call */
+  int32_t strict_boundary;    /* 0: first ladder module reads x_b; 1: reads x_{b-1} */
+} ladder_config;
+
+/* Weights: bf16 device pointers, row-major [out_features, in_features] unless
+ * stated, 16-byte aligned.  Per-layer fields are HOST arrays of n_layers device
+ * pointers; the library copies the pointer values during ladder_create.
+ *   embed [vocab, d_model]; final_norm [d_model]; lm_head [vocab, d_model]
+ *   (ignored when tie_embeddings); attn_norm, mlp_norm [d_model];
+ *   wq [n_q_heads*head_dim, d_model]; wk, wv [n_kv_heads*head_dim, d_model];
+ *   wo [d_model, n_q_heads*head_dim]; w_gate, w_up [ffn_dim, d_model];
+ *   w_down [d_model, ffn_dim]. */
+typedef struct {
+  const void* embed;
+  const void* final_norm;
+  const void* lm_head;
+  const void* const* attn_norm;
+  const void* const* wq;
+  const void* const* wk;
+  const void* const* wv;
+  const void* const* wo;
+  const void* const* mlp_norm;
+  const void* const* w_gate;
+  const void* const* w_up;
+  const void* const* w_down;
+} ladder_weights;
+
+/* Sizes the caller must allocate: device workspace bytes for ladder_create and
+ * bytes of one KV page (all layers: n_layers * 2 * n_kv_heads * page_size *
+ * head_dim * 2).  Either output pointer may be NULL. */
+int ladder_query_sizes(const ladder_config* cfg, size_t* workspace_bytes, size_t* kv_page_bytes);
+
+/* Create a model over borrowed weights.  `workspace` is a device buffer of at
+ * least the queried size, 256-byte aligned, owned by the caller and reserved
+ * for this model until ladder_destroy.  Initialisation kernels (rotary tables)
+ * run on `stream`. */
+int ladder_create(const ladder_config* cfg, const ladder_weights* w, void* workspace,
+                  size_t workspace_bytes, ladder_stream_t stream, ladder_model** out);
+void ladder_destroy(ladder_model* m);
+
+/* Residual schedule (LADDER_RESIDUAL_*) and flags (LADDER_FLAG_*). */
+int ladder_set_mode(ladder_model* m, int residual_mode, int flags);
+
+/* Paged KV cache.  `pool` is a device buffer of num_pages * kv_page_bytes,
+ * 16-byte aligned, laid out bf16 [n_layers][num_pages][2 (K, V)][n_kv_heads]
+ * [page_size][head_dim]; keys are stored after rotation.  `block_table` is a
+ * device int32 [max_batch][max_pages_per_seq], `seq_lens` a device int32
+ * [max_batch]; both are caller-owned and written only by the library.
+ * Position p of sequence b lives in page block_table[b][p / page_size] at
+ * offset p % page_size. */
+int ladder_kv_create(ladder_model* m, void* pool, int32_t num_pages, int32_t max_pages_per_seq,
+                     int32_t* block_table, int32_t* seq_lens, ladder_kv** out);
+void ladder_kv_destroy(ladder_kv* kv);
+
+/* Assign pages: host_table is a HOST int32 [max_batch][max_pages_per_seq];
+ * entries are page ids in [0, num_pages) or -1 for "none".  Assigned pages of
+ * a sequence must be a prefix of its row, and no page may be assigned twice.
+ * Copies the table to the device block table on `stream`. */
+int ladder_kv_set_pages(ladder_kv* kv, const int32_t* host_table, ladder_stream_t stream);
+
+/* Set every sequence length to 0 (on the device, on `stream`, and in the
+ * library's host copy). */
+int ladder_kv_reset(ladder_kv* kv, ladder_stream_t stream);
+
+/* Host copy of the current length of sequence b, or -1 if b is out of range. */
+int32_t ladder_kv_seq_len(const ladder_kv* kv, int32_t b);
+
+/* Prefill B sequences from empty caches.  `tokens` is a device int32 array of
+ * the sum of host_lens packed sequence after sequence; `host_lens` a HOST int32
+ * [B].  Writes every position's K/V into the cache, sets seq_lens[b] =
+ * host_lens[b], and writes the last position's logits to `logits` (device fp32
+ * [B, vocab]) and, if `next_tok` is not NULL, the greedy tokens (device int32
+ * [B]).  Fails with LADDER_ERR_CAPACITY when a sequence exceeds its assigned
+ * pages or max_seq, or the packed total exceeds max_prefill_tokens. */
+int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tokens, const int32_t* host_lens,
+                   int32_t B, float* logits, int32_t* next_tok, ladder_stream_t stream);
+
+/* One decode step for sequences 0 .. B-1: token tokens[b] (device int32 [B])
+ * is placed at position seq_lens[b]; writes logits (device fp32 [B, vocab]),
+ * the greedy tokens to next_tok (device int32 [B], may equal `tokens`, may be
+ * NULL) and increments every seq_lens[b].  With LADDER_FLAG_DECODE_GRAPH the
+ * step is captured once per (B, pointer set) and replayed afterwards. */
+int ladder_decode_step(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int32_t B,
+                       float* logits, int32_t* next_tok, ladder_stream_t stream);
+
+/* Reads and clears the device error word (synchronises `stream`).  *code is 0
+ * when no kernel reported a problem; 1 = a token id was outside [0, vocab). */
+int ladder_get_device_error(ladder_model* m, ladder_stream_t stream, int32_t* code);
+
+/* Number of kernel launches the last prefill / decode call issued (a decode
+ * step replayed from a graph reports the launches inside the graph). */
+int32_t ladder_last_launch_count(const ladder_model* m);
+
+/* Kernel classes that the launch probe can time. */
+enum {
+  LADDER_PROBE_QKV = 0,     /* decode: RMSNorm + QKV GEMV + RoPE + KV write */
+  LADDER_PROBE_ATTN = 1,    /* decode: paged attention (split + combine) */
+  LADDER_PROBE_OUT = 2,     /* decode: O-projection GEMV + residual */
+  LADDER_PROBE_GATEUP = 3,  /* decode: RMSNorm + gate/up GEMV + SwiGLU */
+  LADDER_PROBE_DOWN = 4,    /* decode: down-projection GEMV + residual */
+  LADDER_PROBE_LMHEAD = 5   /* decode: final RMSNorm + lm_head GEMV */
+};
+
+/* Start timing every launch of one kernel class in the following eager
+ * (non-graph) decode steps: a CUDA event pair is recorded on the launching
+ * stream around each launch, up to max_launches (1 .. 65536).  Fails while
+ * LADDER_FLAG_DECODE_GRAPH is set. */
+int ladder_probe_begin(ladder_model* m, int kernel_class, int32_t max_launches);
+
+/* Stop timing: waits for the recorded events and returns how many launches
+ * were timed and the sum of their durations in milliseconds. */
+int ladder_probe_end(ladder_model* m, int32_t* launches, float* total_ms);
+
+/* Thread-local message describing the last failed call on this thread. */
+const char* ladder_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LADDER_H */

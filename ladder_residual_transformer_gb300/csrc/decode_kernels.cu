@@ -1,0 +1,552 @@
+// Decode-side kernels of the Ladder Transformer forward pass (one new token per
+// sequence, B <= 64 sequences).
+//
+// Decode is bound by HBM bandwidth: every step streams all layer weights once
+// and the KV cache of each sequence once.  The GEMV kernel therefore reads each
+// weight row with 128-bit non-allocating loads, coalesced across the warp, and
+// keeps several loads in flight per lane; the normalised input rows are staged
+// once per CTA in shared memory (fp32).  RMSNorm is fused into the GEMV
+// prologue, and RoPE + KV-cache write, SwiGLU, and the residual add into its
+// epilogues, so that the module's activations never make a round trip through
+// HBM.
+#include "internal.cuh"
+
+#include <math.h>
+
+namespace ladder {
+
+constexpr int GEMV_WARPS = 8;
+constexpr int GEMV_THREADS = GEMV_WARPS * 32;
+constexpr int GEMV_SMEM_FLOATS = 16384;  // 64 KB staged input per CTA
+
+// ---------------------------------------------------------------------------
+// Embedding gather: x[m, :] = float(E[tok[m], :]).  Out-of-range ids write a
+// zero row and set bit 0 of the error word.
+// ---------------------------------------------------------------------------
+__global__ void embed_kernel(const int* __restrict__ tok, const bf16* __restrict__ E, int d, int vocab,
+                             float* __restrict__ x, int* err) {
+  const int m = blockIdx.x;
+  const int t = tok[m];
+  const bool ok = (unsigned)t < (unsigned)vocab;
+  if (!ok && threadIdx.x == 0) atomicOr(err, 1);
+  const bf16* row = E + (size_t)(ok ? t : 0) * d;
+  float* out = x + (size_t)m * d;
+  for (int i = threadIdx.x * 8; i < d; i += blockDim.x * 8) {
+    uint4 v = ok ? *reinterpret_cast<const uint4*>(row + i) : make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<float4*>(out + i) = make_float4(bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y));
+    *reinterpret_cast<float4*>(out + i + 4) = make_float4(bf_lo(v.z), bf_hi(v.z), bf_lo(v.w), bf_hi(v.w));
+  }
+}
+
+cudaError_t launch_embed(const int* tok, int M, const bf16* E, int d, int vocab, float* x, int* err,
+                         cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  embed_kernel<<<M, 128, 0, s>>>(tok, E, d, vocab, x, err);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// GEMV: out[b, n] = sum_k W[n, k] * u[b, k] for B <= BT rows, fused prologue and
+// epilogue by mode.  u = x * rsqrt(mean(x^2) + eps) * g when a gain is given.
+//
+// Work unit ("task") = two weight rows computed together by one warp: a RoPE
+// pair (2j, 2j+1) for QKV, the matching gate and up rows for SwiGLU, or two
+// consecutive rows otherwise.  Lane l reads 16 bytes (8 bf16) at k = 8l + 256i.
+// Staged input layout per batch row: two planes [kc/8][4] holding elements
+// k%8 < 4 and k%8 >= 4, so that each lane's 16-byte shared-memory reads are
+// contiguous across the warp (no bank conflicts).
+// ---------------------------------------------------------------------------
+template <int BT>
+__device__ __forceinline__ void gemv_fma(const uint4& w, const float* __restrict__ u, int kc, int k,
+                                         float (&acc)[BT]) {
+  const float w0 = bf_lo(w.x), w1 = bf_hi(w.x), w2 = bf_lo(w.y), w3 = bf_hi(w.y);
+  const float w4 = bf_lo(w.z), w5 = bf_hi(w.z), w6 = bf_lo(w.w), w7 = bf_hi(w.w);
+  const int q = (k >> 3) << 2;
+#pragma unroll
+  for (int b = 0; b < BT; ++b) {
+    const float4 a = *reinterpret_cast<const float4*>(u + b * kc + q);
+    const float4 c = *reinterpret_cast<const float4*>(u + b * kc + (kc >> 1) + q);
+    float s = acc[b];
+    s = fmaf(w0, a.x, s);
+    s = fmaf(w1, a.y, s);
+    s = fmaf(w2, a.z, s);
+    s = fmaf(w3, a.w, s);
+    s = fmaf(w4, c.x, s);
+    s = fmaf(w5, c.y, s);
+    s = fmaf(w6, c.z, s);
+    s = fmaf(w7, c.w, s);
+    acc[b] = s;
+  }
+}
+
+template <int BT, int MODE>
+__global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) {
+  extern __shared__ float4 gemv_smem4[];
+  float* u = reinterpret_cast<float*>(gemv_smem4);
+  __shared__ float s_red[GEMV_WARPS][BT];
+  __shared__ float s_rms[BT];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int K = p.K;
+
+  // RMSNorm statistics of each input row, in a fixed order (identical in every CTA).
+  if (p.g != nullptr) {
+    float ss[BT];
+#pragma unroll
+    for (int b = 0; b < BT; ++b) ss[b] = 0.f;
+    for (int i = tid * 4; i < K; i += GEMV_THREADS * 4) {
+#pragma unroll
+      for (int b = 0; b < BT; ++b) {
+        if (b < p.B) {
+          const float4 v = *reinterpret_cast<const float4*>(p.x + (size_t)b * p.ldx + i);
+          ss[b] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+      const float t = warp_sum(ss[b]);
+      if (lane == 0) s_red[warp][b] = t;
+    }
+    __syncthreads();
+    if (tid < BT) {
+      float t = 0.f;
+      for (int w = 0; w < GEMV_WARPS; ++w) t += s_red[w][tid];
+      s_rms[tid] = rsqrtf(t / (float)K + p.eps);
+    }
+    __syncthreads();
+  }
+
+  const int total_warps = gridDim.x * GEMV_WARPS;
+  const int rounds = (p.n_tasks + total_warps - 1) / total_warps;
+  const bool single_chunk = p.kc >= K;
+
+  for (int r = 0; r < rounds; ++r) {
+    const int task = r * total_warps + blockIdx.x * GEMV_WARPS + warp;
+    const bool active = task < p.n_tasks;
+
+    // Which two weight rows this task reads.
+    const bf16* row0 = p.w0;
+    const bf16* row1 = p.w0;
+    int local = 0, kind = 0;  // QKV: kind 0 = q, 1 = k, 2 = v; local = row inside its matrix
+    if (active) {
+      if (MODE == GEMV_QKV) {
+        const int r0 = 2 * task;
+        if (r0 < p.nq_hd) {
+          local = r0; kind = 0; row0 = p.w0 + (size_t)local * K;
+        } else if (r0 < p.nq_hd + p.nkv_hd) {
+          local = r0 - p.nq_hd; kind = 1; row0 = p.w1 + (size_t)local * K;
+        } else {
+          local = r0 - p.nq_hd - p.nkv_hd; kind = 2; row0 = p.w2 + (size_t)local * K;
+        }
+        row1 = row0 + K;
+      } else if (MODE == GEMV_GATEUP) {
+        row0 = p.w0 + (size_t)task * K;
+        row1 = p.w1 + (size_t)task * K;
+      } else {
+        row0 = p.w0 + (size_t)(2 * task) * K;
+        row1 = row0 + K;
+      }
+    }
+
+    float a0[BT], a1[BT];
+#pragma unroll
+    for (int b = 0; b < BT; ++b) a0[b] = a1[b] = 0.f;
+
+    for (int k0 = 0; k0 < K; k0 += p.kc) {
+      const int kc = min(p.kc, K - k0);
+      if (!single_chunk || r == 0) {
+        __syncthreads();
+        // Stage the (normalised) input chunk in the two-plane layout.
+        for (int i = tid * 4; i < kc; i += GEMV_THREADS * 4) {
+          float4 gv = make_float4(1.f, 1.f, 1.f, 1.f);
+          if (p.g != nullptr) {
+            const uint2 graw = *reinterpret_cast<const uint2*>(p.g + k0 + i);
+            gv = make_float4(bf_lo(graw.x), bf_hi(graw.x), bf_lo(graw.y), bf_hi(graw.y));
+          }
+          const int dst = ((i & 4) ? (kc >> 1) : 0) + ((i >> 3) << 2);
+#pragma unroll
+          for (int b = 0; b < BT; ++b) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (b < p.B) {
+              v = *reinterpret_cast<const float4*>(p.x + (size_t)b * p.ldx + k0 + i);
+              const float sc = (p.g != nullptr) ? s_rms[b] : 1.f;
+              v.x *= sc * gv.x; v.y *= sc * gv.y; v.z *= sc * gv.z; v.w *= sc * gv.w;
+            }
+            *reinterpret_cast<float4*>(u + b * kc + dst) = v;
+          }
+        }
+        __syncthreads();
+      }
+      if (active) {
+        const bf16* p0 = row0 + k0;
+        const bf16* p1 = row1 + k0;
+        int k = lane * 8;
+        for (; k + 768 < kc; k += 1024) {
+          uint4 wa[4], wb[4];
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            wa[s] = ld_stream_u4(p0 + k + 256 * s);
+            wb[s] = ld_stream_u4(p1 + k + 256 * s);
+          }
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            gemv_fma<BT>(wa[s], u, kc, k + 256 * s, a0);
+            gemv_fma<BT>(wb[s], u, kc, k + 256 * s, a1);
+          }
+        }
+        for (; k < kc; k += 256) {
+          const uint4 wa = ld_stream_u4(p0 + k);
+          const uint4 wb = ld_stream_u4(p1 + k);
+          gemv_fma<BT>(wa, u, kc, k, a0);
+          gemv_fma<BT>(wb, u, kc, k, a1);
+        }
+      }
+    }
+
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+      a0[b] = warp_sum(a0[b]);
+      a1[b] = warp_sum(a1[b]);
+    }
+    if (!active) continue;
+
+    // Epilogue: lane b handles batch row b.
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+      if (lane != b || b >= p.B) continue;
+      const float v0 = a0[b], v1 = a1[b];
+      if (MODE == GEMV_QKV) {
+        const int hd = p.kv.head_dim;
+        const int pos = p.pos[b];
+        float r0 = v0, r1 = v1;
+        if (kind < 2) {
+          const int j = (local % hd) >> 1;
+          const float c = p.rope_cos[(size_t)pos * (hd >> 1) + j];
+          const float s = p.rope_sin[(size_t)pos * (hd >> 1) + j];
+          r0 = v0 * c - v1 * s;
+          r1 = v0 * s + v1 * c;
+        }
+        if (kind == 0) {
+          float* q = p.out + (size_t)b * p.ldo + local;
+          q[0] = r0;
+          q[1] = r1;
+        } else {
+          const int head = local / hd, dim = local % hd;
+          bf16* dst = p.kv.base + p.kv.slot(b, pos, kind - 1, head) + dim;
+          dst[0] = __float2bfloat16_rn(r0);
+          dst[1] = __float2bfloat16_rn(r1);
+        }
+      } else if (MODE == GEMV_GATEUP) {
+        p.out[(size_t)b * p.ldo + task] = silu_f(v0) * v1;
+      } else if (MODE == GEMV_RESID) {
+        const size_t n = 2 * (size_t)task;
+        p.out[(size_t)b * p.ldo + n] = p.x_res[(size_t)b * p.ldr + n] + v0;
+        p.out[(size_t)b * p.ldo + n + 1] = p.x_res[(size_t)b * p.ldr + n + 1] + v1;
+      } else {
+        const size_t n = 2 * (size_t)task;
+        p.out[(size_t)b * p.ldo + n] = v0;
+        p.out[(size_t)b * p.ldo + n + 1] = v1;
+      }
+    }
+  }
+}
+
+int gemv_chunk(int B, int K) {
+  const int bt = B <= 1 ? 1 : (B <= 2 ? 2 : 4);
+  int kc = GEMV_SMEM_FLOATS / bt;
+  kc -= kc % 256;
+  return K < kc ? K : kc;
+}
+
+template <int BT>
+static cudaError_t set_gemv_attrs() {
+  const int bytes = GEMV_SMEM_FLOATS * 4;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(gemv_kernel<BT, GEMV_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
+  if ((e = cudaFuncSetAttribute(gemv_kernel<BT, GEMV_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
+  if ((e = cudaFuncSetAttribute(gemv_kernel<BT, GEMV_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
+  return cudaFuncSetAttribute(gemv_kernel<BT, GEMV_LOGITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+cudaError_t gemv_configure() {
+  cudaError_t e;
+  if ((e = set_gemv_attrs<1>())) return e;
+  if ((e = set_gemv_attrs<2>())) return e;
+  return set_gemv_attrs<4>();
+}
+
+template <int BT>
+static void gemv_dispatch(const GemvParams& p, int mode, int grid, size_t smem, cudaStream_t s) {
+  switch (mode) {
+    case GEMV_QKV: gemv_kernel<BT, GEMV_QKV><<<grid, GEMV_THREADS, smem, s>>>(p); break;
+    case GEMV_GATEUP: gemv_kernel<BT, GEMV_GATEUP><<<grid, GEMV_THREADS, smem, s>>>(p); break;
+    case GEMV_RESID: gemv_kernel<BT, GEMV_RESID><<<grid, GEMV_THREADS, smem, s>>>(p); break;
+    default: gemv_kernel<BT, GEMV_LOGITS><<<grid, GEMV_THREADS, smem, s>>>(p); break;
+  }
+}
+
+// Batches larger than 4 run as consecutive chunks of at most 4 rows.
+cudaError_t launch_gemv(const GemvParams& p0, int mode, int num_sms, cudaStream_t s) {
+  for (int b0 = 0; b0 < p0.B; b0 += 4) {
+    GemvParams p = p0;
+    p.B = p0.B - b0 < 4 ? p0.B - b0 : 4;
+    p.x = p0.x + (size_t)b0 * p0.ldx;
+    p.out = p0.out + (size_t)b0 * p0.ldo;
+    if (p0.x_res) p.x_res = p0.x_res + (size_t)b0 * p0.ldr;
+    if (p0.pos) p.pos = p0.pos + b0;
+    if (p0.kv.block_table) p.kv.block_table = p0.kv.block_table + (size_t)b0 * p0.kv.max_pages;
+    const int bt = p.B <= 1 ? 1 : (p.B <= 2 ? 2 : 4);
+    p.kc = gemv_chunk(p.B, p.K);
+    const size_t smem = (size_t)bt * p.kc * sizeof(float);
+    int grid = (p.n_tasks + GEMV_WARPS - 1) / GEMV_WARPS;
+    const int cap = num_sms * 4;
+    if (grid > cap) grid = cap;
+    if (bt == 1) gemv_dispatch<1>(p, mode, grid, smem, s);
+    else if (bt == 2) gemv_dispatch<2>(p, mode, grid, smem, s);
+    else gemv_dispatch<4>(p, mode, grid, smem, s);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// ---------------------------------------------------------------------------
+// Decode attention over the paged cache, split along the context.
+// CTA (split, kv head, sequence): the G = n_q / n_kv query heads of the group
+// against keys [split * split_len, ...) of the sequence.  Thread t scores key t
+// for all G heads; each warp then normalises heads w, w+4 with warp-shuffle
+// max/sum reductions; finally thread (d, parity) accumulates P V for dim d.
+// Partial (max, sum, o) per split are merged by attn_combine_kernel.
+// ---------------------------------------------------------------------------
+constexpr int ATT_THREADS = 128;
+constexpr int ATT_MAXG = 8;
+
+template <int HD>
+__global__ void __launch_bounds__(ATT_THREADS) attn_decode_kernel(const AttnDecodeParams p) {
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int G = p.n_q / p.kv.n_kv;
+  const int ctx = p.seq_lens[b] + 1;
+  const int s0 = split * p.split_len;
+  const int s1 = min(ctx, s0 + p.split_len);
+  if (s0 >= s1) return;  // the combine step reads only splits below ctx
+  const int n = s1 - s0;
+
+  __shared__ float q_s[ATT_MAXG][HD];
+  __shared__ float p_s[ATT_MAXG][ATT_THREADS];
+  __shared__ float m_s[ATT_MAXG], l_s[ATT_MAXG];
+  constexpr int KP = ATT_THREADS / HD;
+  __shared__ float o_red[KP > 1 ? ATT_MAXG : 1][KP > 1 ? HD : 1];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const float* qg = p.q + (size_t)b * p.n_q * HD + (size_t)kvh * G * HD;
+  for (int i = tid; i < G * HD; i += ATT_THREADS) q_s[i / HD][i % HD] = qg[i];
+  __syncthreads();
+
+  float acc[ATT_MAXG];
+#pragma unroll
+  for (int h = 0; h < ATT_MAXG; ++h) acc[h] = 0.f;
+  if (tid < n) {
+    const bf16* krow = p.kv.base + p.kv.slot(b, s0 + tid, 0, kvh);
+#pragma unroll 4
+    for (int d = 0; d < HD; d += 8) {
+      const uint4 kw = *reinterpret_cast<const uint4*>(krow + d);
+      const float k0 = bf_lo(kw.x), k1 = bf_hi(kw.x), k2 = bf_lo(kw.y), k3 = bf_hi(kw.y);
+      const float k4 = bf_lo(kw.z), k5 = bf_hi(kw.z), k6 = bf_lo(kw.w), k7 = bf_hi(kw.w);
+#pragma unroll
+      for (int h = 0; h < ATT_MAXG; ++h) {
+        if (h < G) {
+          const float* qh = &q_s[h][d];
+          acc[h] += qh[0] * k0 + qh[1] * k1 + qh[2] * k2 + qh[3] * k3 + qh[4] * k4 + qh[5] * k5 +
+                    qh[6] * k6 + qh[7] * k7;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < ATT_MAXG; ++h)
+    if (h < G) p_s[h][tid] = tid < n ? acc[h] * p.scale : -INFINITY;
+  __syncthreads();
+
+  for (int h = warp; h < G; h += ATT_THREADS / 32) {
+    float v[4];
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[i] = p_s[h][lane + 32 * i];
+      m = fmaxf(m, v[i]);
+    }
+    m = warp_max(m);
+    float l = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float e = (v[i] == -INFINITY) ? 0.f : __expf(v[i] - m);
+      p_s[h][lane + 32 * i] = e;
+      l += e;
+    }
+    l = warp_sum(l);
+    if (lane == 0) {
+      m_s[h] = m;
+      l_s[h] = l;
+    }
+  }
+  __syncthreads();
+
+  const int d = tid % HD, kp = tid / HD;
+  float o[ATT_MAXG];
+#pragma unroll
+  for (int h = 0; h < ATT_MAXG; ++h) o[h] = 0.f;
+  for (int t = kp; t < n; t += KP) {
+    const bf16* vrow = p.kv.base + p.kv.slot(b, s0 + t, 1, kvh);
+    const float v = __bfloat162float(vrow[d]);
+#pragma unroll
+    for (int h = 0; h < ATT_MAXG; ++h)
+      if (h < G) o[h] += p_s[h][t] * v;
+  }
+  if (KP > 1) {
+    if (kp == 1) {
+#pragma unroll
+      for (int h = 0; h < ATT_MAXG; ++h)
+        if (h < G) o_red[h][d] = o[h];
+    }
+    __syncthreads();
+    if (kp != 0) return;
+#pragma unroll
+    for (int h = 0; h < ATT_MAXG; ++h)
+      if (h < G) o[h] += o_red[h][d];
+  }
+#pragma unroll
+  for (int h = 0; h < ATT_MAXG; ++h) {
+    if (h >= G) continue;
+    const size_t idx = ((size_t)b * p.n_q + (size_t)kvh * G + h) * p.nsplit + split;
+    p.part_o[idx * HD + d] = o[h];
+    if (d == 0) {
+      p.part_ml[idx * 2] = m_s[h];
+      p.part_ml[idx * 2 + 1] = l_s[h];
+    }
+  }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(HD) attn_combine_kernel(const AttnDecodeParams p) {
+  const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+  const int ctx = p.seq_lens[b] + 1;
+  int ns = (ctx + p.split_len - 1) / p.split_len;
+  if (ns > p.nsplit) ns = p.nsplit;
+  const size_t base = ((size_t)b * p.n_q + h) * p.nsplit;
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, p.part_ml[(base + s) * 2]);
+  float L = 0.f, acc = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const float m = p.part_ml[(base + s) * 2];
+    const float w = __expf(m - M);
+    L += w * p.part_ml[(base + s) * 2 + 1];
+    acc += w * p.part_o[(base + s) * HD + d];
+  }
+  p.out[(size_t)b * p.n_q * HD + (size_t)h * HD + d] = acc / L;
+}
+
+cudaError_t launch_attn_decode(const AttnDecodeParams& p, int B, int n_kv, int hd, cudaStream_t s) {
+  dim3 grid(p.nsplit, n_kv, B);
+  if (hd == 64) {
+    attn_decode_kernel<64><<<grid, ATT_THREADS, 0, s>>>(p);
+    attn_combine_kernel<64><<<dim3(p.n_q, B), 64, 0, s>>>(p);
+  } else {
+    attn_decode_kernel<128><<<grid, ATT_THREADS, 0, s>>>(p);
+    attn_combine_kernel<128><<<dim3(p.n_q, B), 128, 0, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Greedy token: argmax over the vocabulary, lowest index on ties, NaN ignored.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void better(float& bv, int& bi, float v, int i) {
+  if (v > bv || (v == bv && i < bi)) {
+    bv = v;
+    bi = i;
+  }
+}
+
+__global__ void __launch_bounds__(256) argmax_partial_kernel(const float* __restrict__ logits, int V,
+                                                             float* pv, int* pi, int nblk) {
+  const int b = blockIdx.y, blk = blockIdx.x;
+  const int chunk = (V + nblk - 1) / nblk;
+  const int lo = blk * chunk, hi = min(V, lo + chunk);
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) better(bv, bi, logits[(size_t)b * V + i], i);
+  __shared__ float sv[32];
+  __shared__ int si[32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    better(bv, bi, ov, oi);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    sv[warp] = bv;
+    si[warp] = bi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) better(bv, bi, sv[w], si[w]);
+    pv[b * nblk + blk] = bv;
+    pi[b * nblk + blk] = bi;
+  }
+}
+
+__global__ void argmax_final_kernel(const float* pv, const int* pi, int nblk, int* out) {
+  const int b = blockIdx.x, lane = threadIdx.x;
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int i = lane; i < nblk; i += 32) better(bv, bi, pv[b * nblk + i], pi[b * nblk + i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    better(bv, bi, ov, oi);
+  }
+  if (lane == 0) out[b] = bi == 0x7fffffff ? 0 : bi;
+}
+
+cudaError_t launch_argmax(const float* logits, int B, int V, float* part_v, int* part_i, int nblk,
+                          int* out, cudaStream_t s) {
+  argmax_partial_kernel<<<dim3(nblk, B), 256, 0, s>>>(logits, V, part_v, part_i, nblk);
+  argmax_final_kernel<<<B, 32, 0, s>>>(part_v, part_i, nblk, out);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Small bookkeeping kernels
+// ---------------------------------------------------------------------------
+__global__ void advance_kernel(int* seq_lens, int B) {
+  const int b = threadIdx.x;
+  if (b < B) seq_lens[b] += 1;
+}
+
+cudaError_t launch_advance(int* seq_lens, int B, cudaStream_t s) {
+  advance_kernel<<<1, 64, 0, s>>>(seq_lens, B);
+  return cudaGetLastError();
+}
+
+// cos/sin of p * theta^(-2j/hd), formed in double precision and rounded once.
+__global__ void rope_table_kernel(float* c, float* sn, int max_seq, int hd, double theta) {
+  const int half = hd / 2;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)max_seq * half) return;
+  const int p = (int)(idx / half), j = (int)(idx % half);
+  const double inv = pow(theta, -2.0 * (double)j / (double)hd);
+  const double a = (double)p * inv;
+  c[idx] = (float)cos(a);
+  sn[idx] = (float)sin(a);
+}
+
+cudaError_t launch_rope_tables(float* cos_t, float* sin_t, int max_seq, int hd, float theta,
+                               cudaStream_t s) {
+  const long long n = (long long)max_seq * (hd / 2);
+  rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(cos_t, sin_t, max_seq, hd, (double)theta);
+  return cudaGetLastError();
+}
+
+}  // namespace ladder

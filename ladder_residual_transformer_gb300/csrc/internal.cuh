@@ -1,0 +1,153 @@
+// Internal declarations shared by the CUDA translation units of libladder.so.
+// Nothing here is part of the public ABI (include/ladder.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+typedef __nv_bfloat16 bf16;
+
+namespace ladder {
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+__device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
+  // Weights are read exactly once per step: bypass L1 allocation.
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+
+// ---------------------------------------------------------------------------
+// Kernel parameter blocks
+// ---------------------------------------------------------------------------
+
+// Paged KV cache view of one layer: bf16 [num_pages][2][n_kv][page_size][head_dim].
+struct KvLayer {
+  bf16* base;
+  const int* block_table;  // [max_batch][max_pages]
+  int max_pages;
+  int page_size;
+  int n_kv;
+  int head_dim;
+  __device__ __forceinline__ size_t page_elems() const { return (size_t)2 * n_kv * page_size * head_dim; }
+  // element offset of (position p of sequence b, kv 0/1, head h, dim 0)
+  __device__ __forceinline__ size_t slot(int b, int p, int kv, int h) const {
+    int page = block_table[b * max_pages + p / page_size];
+    return (size_t)page * page_elems() + ((size_t)(kv * n_kv + h) * page_size + (p % page_size)) * head_dim;
+  }
+};
+
+enum GemvMode { GEMV_QKV = 0, GEMV_GATEUP = 1, GEMV_RESID = 2, GEMV_LOGITS = 3 };
+
+struct GemvParams {
+  const float* x;    // input rows [B][ldx] fp32
+  int ldx;
+  const bf16* g;     // RMSNorm gain [K], or nullptr for no norm
+  float eps;
+  int B, K;
+  const bf16* w0;    // QKV: wq, GATEUP: w_gate, RESID/LOGITS: w
+  const bf16* w1;    // QKV: wk, GATEUP: w_up
+  const bf16* w2;    // QKV: wv
+  int n_tasks;       // row pairs (QKV, RESID, LOGITS) or rows (GATEUP)
+  int kc;            // K chunk staged in shared memory (multiple of 256)
+  float* out;        // QKV: q [B][ldo]; GATEUP: act [B][ldo]; RESID: x_out; LOGITS: logits
+  int ldo;
+  const float* x_res;  // RESID: residual rows [B][ldr]
+  int ldr;
+  // QKV
+  int nq_hd, nkv_hd;
+  const float* rope_cos;  // [max_seq][head_dim / 2]
+  const float* rope_sin;
+  const int* pos;         // position of row b (the sequence length before this step)
+  KvLayer kv;
+};
+
+struct AttnDecodeParams {
+  const float* q;      // [B][n_q * hd] rotated queries
+  KvLayer kv;
+  const int* seq_lens;  // context of row b = seq_lens[b] + 1
+  int n_q;
+  int split_len;        // keys per split (multiple of page_size)
+  int nsplit;
+  float scale;
+  float* part_o;        // [B][n_q][nsplit][hd]
+  float* part_ml;       // [B][n_q][nsplit][2]
+  float* out;           // [B][n_q * hd]
+};
+
+enum GemmMode { GEMM_QKV = 0, GEMM_GATEUP = 1, GEMM_RESID = 2 };
+
+struct GemmParams {
+  const bf16* A;        // [M][K] activations
+  const bf16* w0;       // QKV: wq; GATEUP: w_gate; RESID: w
+  const bf16* w1;       // QKV: wk; GATEUP: w_up
+  const bf16* w2;       // QKV: wv
+  int M, N, K;
+  bf16* out_bf;         // QKV: q [M][ldo]; GATEUP: act [M][ldo]
+  float* out_f;         // RESID: x_out [M][ldo]
+  int ldo;
+  const float* x_res;   // RESID
+  // QKV
+  int nq_hd, nkv_hd;
+  const float* rope_cos;
+  const float* rope_sin;
+  const int* row_b;     // sequence of packed row m
+  const int* row_pos;   // position of packed row m
+  KvLayer kv;
+};
+
+struct AttnPrefillParams {
+  const bf16* q;        // [M][n_q * hd]
+  KvLayer kv;
+  const int* row_b;
+  const int* row_pos;
+  int M, n_q;
+  float scale;
+  bf16* out;            // [M][n_q * hd]
+};
+
+// ---------------------------------------------------------------------------
+// Launchers (each returns the cudaError_t of its launch)
+// ---------------------------------------------------------------------------
+cudaError_t launch_embed(const int* tok, int M, const bf16* E, int d, int vocab, float* x, int* err,
+                         cudaStream_t s);
+cudaError_t launch_gemv(const GemvParams& p, int mode, int num_sms, cudaStream_t s);
+cudaError_t gemv_configure();
+int gemv_chunk(int B, int K);
+cudaError_t launch_attn_decode(const AttnDecodeParams& p, int B, int n_kv, int hd, cudaStream_t s);
+cudaError_t launch_argmax(const float* logits, int B, int V, float* part_v, int* part_i, int nblk,
+                          int* out, cudaStream_t s);
+cudaError_t launch_advance(int* seq_lens, int B, cudaStream_t s);
+cudaError_t launch_rope_tables(float* cos_t, float* sin_t, int max_seq, int hd, float theta,
+                               cudaStream_t s);
+
+cudaError_t launch_rmsnorm_rows(const float* x, int M, int d, const bf16* g, float eps, bf16* out,
+                                cudaStream_t s);
+cudaError_t launch_gemm(const GemmParams& p, int mode, cudaStream_t s);
+cudaError_t launch_attn_prefill(const AttnPrefillParams& p, int hd, cudaStream_t s);
+cudaError_t launch_gather_rows(const float* x, int d, const int* rows, int B, float* out,
+                               cudaStream_t s);
+cudaError_t launch_set_lens(const int* lens, int B, int* seq_lens, cudaStream_t s);
+
+}  // namespace ladder

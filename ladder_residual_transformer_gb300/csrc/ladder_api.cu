@@ -1,0 +1,671 @@
+// Host side of libladder.so: argument validation, workspace plan, the module
+// schedule of the ladder residual, and the launch sequences of prefill and
+// decode.  See include/ladder.h for the contract of every entry point.
+#include "ladder.h"
+#include "internal.cuh"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+using namespace ladder;
+
+// ---------------------------------------------------------------------------
+// Errors
+// ---------------------------------------------------------------------------
+static thread_local std::string g_last_error;
+
+static int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+#define CUDA_TRY(expr)                                                                          \
+  do {                                                                                          \
+    cudaError_t e_ = (expr);                                                                    \
+    if (e_ != cudaSuccess) return fail(LADDER_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e_)); \
+  } while (0)
+
+// ---------------------------------------------------------------------------
+// Workspace plan
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kSplitLen = 128;      // keys per decode-attention split
+constexpr int kArgmaxBlocks = 64;   // partial argmax blocks per sequence
+
+struct Plan {
+  size_t x[3], xn, q, ao, act, part_o, part_ml, am_v, am_i, rope_cos, rope_sin, meta, xlast, err;
+  size_t total;
+  int m_max, nsplit_max;
+};
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+Plan make_plan(const ladder_config& c) {
+  Plan p{};
+  const size_t d = c.d_model, qd = (size_t)c.n_q_heads * c.head_dim, f = c.ffn_dim;
+  p.m_max = c.max_prefill_tokens > c.max_batch ? c.max_prefill_tokens : c.max_batch;
+  p.nsplit_max = (c.max_seq + kSplitLen - 1) / kSplitLen;
+  const size_t M = p.m_max, Bm = c.max_batch;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  for (int i = 0; i < 3; ++i) p.x[i] = take(M * d * 4);
+  p.xn = take(M * d * 2);
+  p.q = take(M * qd * 4);
+  p.ao = take(M * qd * 4);
+  p.act = take(std::max(M * f * 2, Bm * f * 4));
+  p.part_o = take(Bm * c.n_q_heads * (size_t)p.nsplit_max * c.head_dim * 4);
+  p.part_ml = take(Bm * c.n_q_heads * (size_t)p.nsplit_max * 2 * 4);
+  p.am_v = take(Bm * kArgmaxBlocks * 4);
+  p.am_i = take(Bm * kArgmaxBlocks * 4);
+  p.rope_cos = take((size_t)c.max_seq * (c.head_dim / 2) * 4);
+  p.rope_sin = take((size_t)c.max_seq * (c.head_dim / 2) * 4);
+  p.meta = take((2 * M + 2 * Bm) * 4);
+  p.xlast = take(Bm * d * 4);
+  p.err = take(256);
+  p.total = off;
+  return p;
+}
+
+int validate_config(const ladder_config* c) {
+  if (!c) return fail(LADDER_ERR_INVALID, "config is NULL");
+  if (c->n_layers <= 0 || c->n_standard_layers < 0 || c->n_standard_layers > c->n_layers)
+    return fail(LADDER_ERR_INVALID, "n_layers=%d n_standard_layers=%d out of range", c->n_layers, c->n_standard_layers);
+  if (c->d_model <= 0 || c->d_model % 256)
+    return fail(LADDER_ERR_INVALID, "d_model=%d must be a positive multiple of 256", c->d_model);
+  if (c->head_dim != 64 && c->head_dim != 128)
+    return fail(LADDER_ERR_UNSUPPORTED, "head_dim=%d: only 64 and 128 are supported", c->head_dim);
+  if (c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->n_q_heads % c->n_kv_heads)
+    return fail(LADDER_ERR_INVALID, "n_q_heads=%d must be a positive multiple of n_kv_heads=%d", c->n_q_heads, c->n_kv_heads);
+  if (c->n_q_heads / c->n_kv_heads > 8)
+    return fail(LADDER_ERR_UNSUPPORTED, "more than 8 query heads per KV head");
+  if ((c->n_q_heads * c->head_dim) % 256)
+    return fail(LADDER_ERR_INVALID, "n_q_heads*head_dim=%d must be a multiple of 256", c->n_q_heads * c->head_dim);
+  if (c->ffn_dim <= 0 || c->ffn_dim % 256)
+    return fail(LADDER_ERR_INVALID, "ffn_dim=%d must be a positive multiple of 256", c->ffn_dim);
+  if (c->vocab <= 0 || c->vocab % 2) return fail(LADDER_ERR_INVALID, "vocab=%d must be positive and even", c->vocab);
+  if (!(c->rope_theta > 1.0f) || !std::isfinite(c->rope_theta))
+    return fail(LADDER_ERR_INVALID, "rope_theta must be finite and > 1");
+  if (!(c->norm_eps > 0.0f) || !std::isfinite(c->norm_eps)) return fail(LADDER_ERR_INVALID, "norm_eps must be > 0");
+  if (c->rope_interleaved != 1)
+    return fail(LADDER_ERR_UNSUPPORTED, "only interleaved rotary pairs (rope_interleaved=1) are implemented");
+  if (c->shard_k != 1) return fail(LADDER_ERR_UNSUPPORTED, "shard_k=%d: shard mode is not built yet", c->shard_k);
+  if (c->page_size != 16 && c->page_size != 32 && c->page_size != 64)
+    return fail(LADDER_ERR_INVALID, "page_size=%d must be 16, 32 or 64", c->page_size);
+  if (c->max_batch <= 0 || c->max_batch > 64) return fail(LADDER_ERR_INVALID, "max_batch=%d must be in 1..64", c->max_batch);
+  if (c->max_seq <= 0 || c->max_seq > (1 << 20)) return fail(LADDER_ERR_INVALID, "max_seq=%d out of range", c->max_seq);
+  if (c->max_prefill_tokens <= 0) return fail(LADDER_ERR_INVALID, "max_prefill_tokens must be positive");
+  if (c->tie_embeddings != 0 && c->tie_embeddings != 1) return fail(LADDER_ERR_INVALID, "tie_embeddings must be 0 or 1");
+  if (c->strict_boundary != 0 && c->strict_boundary != 1) return fail(LADDER_ERR_INVALID, "strict_boundary must be 0 or 1");
+  return LADDER_OK;
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+struct LayerW {
+  const bf16 *attn_norm, *wq, *wk, *wv, *wo, *mlp_norm, *w_gate, *w_up, *w_down;
+};
+
+struct GraphEntry {
+  int B;
+  const int32_t* tok;
+  float* logits;
+  int32_t* next;
+  const ladder_kv* kv;
+  cudaGraphExec_t exec;
+  int launches;
+};
+
+}  // namespace
+
+struct ladder_model {
+  ladder_config cfg;
+  const bf16 *embed, *final_norm, *lm_head;
+  std::vector<LayerW> layers;
+  char* ws;
+  Plan plan;
+  int num_sms;
+  int residual_mode = LADDER_RESIDUAL_CONFIG;
+  int flags = 0;
+  int launches = 0;
+  std::vector<GraphEntry> graphs;
+  std::vector<int32_t> meta_host;
+  // launch probe
+  int probe_class = -1;
+  int probe_count = 0;
+  std::vector<cudaEvent_t> probe_events;  // start/stop pairs
+  bool capturing = false;
+
+  float* X(int i) { return reinterpret_cast<float*>(ws + plan.x[i % 3]); }
+  template <class T> T* at(size_t off) { return reinterpret_cast<T*>(ws + off); }
+  int* err() { return at<int>(plan.err); }
+
+  // Index j of the stream state x_j that module k (1-based) reads.
+  int input_index(int k) const {
+    const int layer = (k - 1) / 2;
+    const int nstd = residual_mode == LADDER_RESIDUAL_STANDARD ? cfg.n_layers : cfg.n_standard_layers;
+    if (layer < nstd) return k - 1;
+    if (cfg.strict_boundary) return k - 2 > 0 ? k - 2 : 0;
+    const int b = 2 * nstd;
+    return k - 2 > b ? k - 2 : b;
+  }
+
+  void drop_graphs() {
+    for (auto& g : graphs) cudaGraphExecDestroy(g.exec);
+    graphs.clear();
+  }
+  void drop_probe() {
+    for (auto e : probe_events) cudaEventDestroy(e);
+    probe_events.clear();
+    probe_class = -1;
+    probe_count = 0;
+  }
+  // Event pair around one launch of `cls` when the probe is armed for it.
+  cudaEvent_t probe_start(int cls, cudaStream_t s) {
+    if (cls != probe_class || capturing || 2 * (size_t)probe_count >= probe_events.size()) return nullptr;
+    cudaEvent_t e = probe_events[2 * probe_count];
+    cudaEventRecord(e, s);
+    return e;
+  }
+  void probe_stop(cudaEvent_t started, cudaStream_t s) {
+    if (!started) return;
+    cudaEventRecord(probe_events[2 * probe_count + 1], s);
+    ++probe_count;
+  }
+};
+
+struct ladder_kv {
+  ladder_model* m;
+  bf16* pool;
+  int num_pages, max_pages;
+  int32_t* block_table;
+  int32_t* seq_lens;
+  std::vector<int32_t> host_lens;
+  std::vector<int32_t> host_table;
+  std::vector<int32_t> pages_of;  // assigned pages per sequence
+
+  KvLayer layer(int l) const {
+    KvLayer v;
+    const ladder_config& c = m->cfg;
+    const size_t page_elems = (size_t)2 * c.n_kv_heads * c.page_size * c.head_dim;
+    v.base = pool + (size_t)l * num_pages * page_elems;
+    v.block_table = block_table;
+    v.max_pages = max_pages;
+    v.page_size = c.page_size;
+    v.n_kv = c.n_kv_heads;
+    v.head_dim = c.head_dim;
+    return v;
+  }
+  int capacity(int b) const {
+    const int cap = pages_of[b] * m->cfg.page_size;
+    return cap < m->cfg.max_seq ? cap : m->cfg.max_seq;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Entry points
+// ---------------------------------------------------------------------------
+extern "C" {
+
+const char* ladder_last_error(void) { return g_last_error.c_str(); }
+
+int ladder_query_sizes(const ladder_config* cfg, size_t* workspace_bytes, size_t* kv_page_bytes) {
+  int rc = validate_config(cfg);
+  if (rc) return rc;
+  if (workspace_bytes) *workspace_bytes = make_plan(*cfg).total;
+  if (kv_page_bytes)
+    *kv_page_bytes = (size_t)cfg->n_layers * 2 * cfg->n_kv_heads * cfg->page_size * cfg->head_dim * 2;
+  return LADDER_OK;
+}
+
+int ladder_create(const ladder_config* cfg, const ladder_weights* w, void* workspace, size_t workspace_bytes,
+                  ladder_stream_t stream, ladder_model** out) {
+  if (!out) return fail(LADDER_ERR_INVALID, "out is NULL");
+  *out = nullptr;
+  int rc = validate_config(cfg);
+  if (rc) return rc;
+  if (!w || !w->embed || !w->final_norm || (!cfg->tie_embeddings && !w->lm_head))
+    return fail(LADDER_ERR_INVALID, "missing global weight pointer");
+  if (!w->attn_norm || !w->wq || !w->wk || !w->wv || !w->wo || !w->mlp_norm || !w->w_gate || !w->w_up || !w->w_down)
+    return fail(LADDER_ERR_INVALID, "missing per-layer weight array");
+  Plan plan = make_plan(*cfg);
+  if (!workspace) return fail(LADDER_ERR_INVALID, "workspace is NULL");
+  if (!aligned(workspace, 256)) return fail(LADDER_ERR_INVALID, "workspace must be 256-byte aligned");
+  if (workspace_bytes < plan.total)
+    return fail(LADDER_ERR_CAPACITY, "workspace too small: %zu < %zu bytes", workspace_bytes, plan.total);
+
+  auto* m = new ladder_model();
+  m->cfg = *cfg;
+  m->embed = static_cast<const bf16*>(w->embed);
+  m->final_norm = static_cast<const bf16*>(w->final_norm);
+  m->lm_head = static_cast<const bf16*>(cfg->tie_embeddings ? w->embed : w->lm_head);
+  const void* globals[3] = {m->embed, m->final_norm, m->lm_head};
+  for (const void* p : globals)
+    if (!aligned(p, 16)) { delete m; return fail(LADDER_ERR_INVALID, "weights must be 16-byte aligned"); }
+  m->layers.resize(cfg->n_layers);
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    LayerW& L = m->layers[l];
+    L.attn_norm = static_cast<const bf16*>(w->attn_norm[l]);
+    L.wq = static_cast<const bf16*>(w->wq[l]);
+    L.wk = static_cast<const bf16*>(w->wk[l]);
+    L.wv = static_cast<const bf16*>(w->wv[l]);
+    L.wo = static_cast<const bf16*>(w->wo[l]);
+    L.mlp_norm = static_cast<const bf16*>(w->mlp_norm[l]);
+    L.w_gate = static_cast<const bf16*>(w->w_gate[l]);
+    L.w_up = static_cast<const bf16*>(w->w_up[l]);
+    L.w_down = static_cast<const bf16*>(w->w_down[l]);
+    const void* ps[9] = {L.attn_norm, L.wq, L.wk, L.wv, L.wo, L.mlp_norm, L.w_gate, L.w_up, L.w_down};
+    for (const void* p : ps)
+      if (!p || !aligned(p, 16)) { delete m; return fail(LADDER_ERR_INVALID, "layer %d: weight NULL or not 16-byte aligned", l); }
+  }
+  m->ws = static_cast<char*>(workspace);
+  m->plan = plan;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = gemv_configure();
+  if (e == cudaSuccess) e = cudaMemsetAsync(m->err(), 0, 256, stream);
+  if (e == cudaSuccess)
+    e = launch_rope_tables(m->at<float>(plan.rope_cos), m->at<float>(plan.rope_sin), cfg->max_seq, cfg->head_dim,
+                           cfg->rope_theta, stream);
+  if (e != cudaSuccess) {
+    delete m;
+    return fail(LADDER_ERR_CUDA, "ladder_create: %s", cudaGetErrorString(e));
+  }
+  *out = m;
+  return LADDER_OK;
+}
+
+void ladder_destroy(ladder_model* m) {
+  if (!m) return;
+  m->drop_graphs();
+  m->drop_probe();
+  delete m;
+}
+
+int ladder_set_mode(ladder_model* m, int residual_mode, int flags) {
+  if (!m) return fail(LADDER_ERR_INVALID, "model is NULL");
+  if (residual_mode != LADDER_RESIDUAL_CONFIG && residual_mode != LADDER_RESIDUAL_STANDARD)
+    return fail(LADDER_ERR_INVALID, "unknown residual mode %d", residual_mode);
+  if (flags & ~LADDER_FLAG_DECODE_GRAPH) return fail(LADDER_ERR_INVALID, "unknown flags 0x%x", flags);
+  if (residual_mode != m->residual_mode || flags != m->flags) m->drop_graphs();
+  m->residual_mode = residual_mode;
+  m->flags = flags;
+  return LADDER_OK;
+}
+
+int ladder_kv_create(ladder_model* m, void* pool, int32_t num_pages, int32_t max_pages_per_seq,
+                     int32_t* block_table, int32_t* seq_lens, ladder_kv** out) {
+  if (!out) return fail(LADDER_ERR_INVALID, "out is NULL");
+  *out = nullptr;
+  if (!m || !pool || !block_table || !seq_lens) return fail(LADDER_ERR_INVALID, "NULL argument");
+  if (!aligned(pool, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+    return fail(LADDER_ERR_INVALID, "pool must be 16-byte aligned");
+  if (num_pages <= 0 || max_pages_per_seq <= 0) return fail(LADDER_ERR_INVALID, "num_pages and max_pages_per_seq must be positive");
+  auto* kv = new ladder_kv();
+  kv->m = m;
+  kv->pool = static_cast<bf16*>(pool);
+  kv->num_pages = num_pages;
+  kv->max_pages = max_pages_per_seq;
+  kv->block_table = block_table;
+  kv->seq_lens = seq_lens;
+  kv->host_lens.assign(m->cfg.max_batch, 0);
+  kv->host_table.assign((size_t)m->cfg.max_batch * max_pages_per_seq, -1);
+  kv->pages_of.assign(m->cfg.max_batch, 0);
+  *out = kv;
+  return LADDER_OK;
+}
+
+void ladder_kv_destroy(ladder_kv* kv) {
+  if (!kv) return;
+  // graphs captured against this handle must not be replayed for another one
+  auto& gs = kv->m->graphs;
+  for (size_t i = 0; i < gs.size();) {
+    if (gs[i].kv == kv) {
+      cudaGraphExecDestroy(gs[i].exec);
+      gs.erase(gs.begin() + i);
+    } else {
+      ++i;
+    }
+  }
+  delete kv;
+}
+
+int ladder_kv_set_pages(ladder_kv* kv, const int32_t* host_table, ladder_stream_t stream) {
+  if (!kv || !host_table) return fail(LADDER_ERR_INVALID, "NULL argument");
+  const int Bm = kv->m->cfg.max_batch, P = kv->max_pages;
+  std::vector<char> used(kv->num_pages, 0);
+  std::vector<int32_t> pages(Bm, 0);
+  for (int b = 0; b < Bm; ++b) {
+    bool ended = false;
+    for (int i = 0; i < P; ++i) {
+      const int32_t pg = host_table[(size_t)b * P + i];
+      if (pg == -1) { ended = true; continue; }
+      if (ended) return fail(LADDER_ERR_INVALID, "sequence %d: assigned pages must be a prefix of its row", b);
+      if (pg < 0 || pg >= kv->num_pages) return fail(LADDER_ERR_INVALID, "sequence %d: page id %d out of range", b, pg);
+      if (used[pg]) return fail(LADDER_ERR_INVALID, "page %d assigned twice", pg);
+      used[pg] = 1;
+      pages[b] = i + 1;
+    }
+    if (pages[b] * kv->m->cfg.page_size < kv->host_lens[b])
+      return fail(LADDER_ERR_CAPACITY, "sequence %d: new pages hold fewer positions than its length", b);
+  }
+  cudaError_t e = cudaMemcpyAsync(kv->block_table, host_table, sizeof(int32_t) * (size_t)Bm * P,
+                                  cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return fail(LADDER_ERR_CUDA, "block table copy: %s", cudaGetErrorString(e));
+  // The copy from pageable memory is staged before cudaMemcpyAsync returns.
+  kv->host_table.assign(host_table, host_table + (size_t)Bm * P);
+  kv->pages_of = pages;
+  return LADDER_OK;
+}
+
+int ladder_kv_reset(ladder_kv* kv, ladder_stream_t stream) {
+  if (!kv) return fail(LADDER_ERR_INVALID, "kv is NULL");
+  CUDA_TRY(cudaMemsetAsync(kv->seq_lens, 0, sizeof(int32_t) * kv->m->cfg.max_batch, stream));
+  std::fill(kv->host_lens.begin(), kv->host_lens.end(), 0);
+  return LADDER_OK;
+}
+
+int32_t ladder_kv_seq_len(const ladder_kv* kv, int32_t b) {
+  if (!kv || b < 0 || b >= (int)kv->host_lens.size()) return -1;
+  return kv->host_lens[b];
+}
+
+int32_t ladder_last_launch_count(const ladder_model* m) { return m ? m->launches : -1; }
+
+int ladder_probe_begin(ladder_model* m, int kernel_class, int32_t max_launches) {
+  if (!m) return fail(LADDER_ERR_INVALID, "model is NULL");
+  if (kernel_class < LADDER_PROBE_QKV || kernel_class > LADDER_PROBE_LMHEAD)
+    return fail(LADDER_ERR_INVALID, "unknown kernel class %d", kernel_class);
+  if (max_launches < 1 || max_launches > 65536) return fail(LADDER_ERR_INVALID, "max_launches out of range");
+  if (m->flags & LADDER_FLAG_DECODE_GRAPH) return fail(LADDER_ERR_INVALID, "the probe times eager decode steps only");
+  m->drop_probe();
+  m->probe_events.resize(2 * (size_t)max_launches, nullptr);
+  for (auto& e : m->probe_events) {
+    cudaError_t err = cudaEventCreate(&e);
+    if (err != cudaSuccess) {
+      e = nullptr;
+      m->drop_probe();
+      return fail(LADDER_ERR_CUDA, "cudaEventCreate: %s", cudaGetErrorString(err));
+    }
+  }
+  m->probe_class = kernel_class;
+  return LADDER_OK;
+}
+
+int ladder_probe_end(ladder_model* m, int32_t* launches, float* total_ms) {
+  if (!m || !launches || !total_ms) return fail(LADDER_ERR_INVALID, "NULL argument");
+  float total = 0.f;
+  for (int i = 0; i < m->probe_count; ++i) {
+    float ms = 0.f;
+    cudaError_t e = cudaEventSynchronize(m->probe_events[2 * i + 1]);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, m->probe_events[2 * i], m->probe_events[2 * i + 1]);
+    if (e != cudaSuccess) {
+      m->drop_probe();
+      return fail(LADDER_ERR_CUDA, "probe events: %s", cudaGetErrorString(e));
+    }
+    total += ms;
+  }
+  *launches = m->probe_count;
+  *total_ms = total;
+  m->drop_probe();
+  return LADDER_OK;
+}
+
+int ladder_get_device_error(ladder_model* m, ladder_stream_t stream, int32_t* code) {
+  if (!m || !code) return fail(LADDER_ERR_INVALID, "NULL argument");
+  int32_t v = 0;
+  CUDA_TRY(cudaMemcpyAsync(&v, m->err(), sizeof(int32_t), cudaMemcpyDeviceToHost, stream));
+  CUDA_TRY(cudaStreamSynchronize(stream));
+  CUDA_TRY(cudaMemsetAsync(m->err(), 0, sizeof(int32_t), stream));
+  *code = v;
+  return LADDER_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Launch sequences
+// ---------------------------------------------------------------------------
+namespace {
+
+#define LAUNCH(expr, n)                                                                          \
+  do {                                                                                           \
+    cudaError_t e_ = (expr);                                                                     \
+    if (e_ != cudaSuccess) return fail(LADDER_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_)); \
+    m->launches += (n);                                                                          \
+  } while (0)
+
+int gemv_launches(int B) { return (B + 3) / 4; }
+
+// One decode step for sequences 0..B-1 (everything on `s`).
+int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B, float* logits,
+                   int32_t* next_tok, int nsplit, cudaStream_t s) {
+  const ladder_config& c = m->cfg;
+  const int d = c.d_model, qd = c.n_q_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim, f = c.ffn_dim;
+  const Plan& P = m->plan;
+  float* q = m->at<float>(P.q);
+  float* ao = m->at<float>(P.ao);
+  float* act = m->at<float>(P.act);
+
+  LAUNCH(launch_embed(tokens, B, m->embed, d, c.vocab, m->X(0), m->err(), s), 1);
+  for (int l = 0; l < c.n_layers; ++l) {
+    const LayerW& L = m->layers[l];
+    const KvLayer kvl = kv->layer(l);
+    // attention module k = 2l + 1
+    {
+      const int k = 2 * l + 1;
+      GemvParams g{};
+      g.x = m->X(m->input_index(k)); g.ldx = d; g.g = L.attn_norm; g.eps = c.norm_eps; g.B = B; g.K = d;
+      g.w0 = L.wq; g.w1 = L.wk; g.w2 = L.wv; g.n_tasks = (qd + 2 * kvd) / 2;
+      g.out = q; g.ldo = qd; g.nq_hd = qd; g.nkv_hd = kvd;
+      g.rope_cos = m->at<float>(P.rope_cos); g.rope_sin = m->at<float>(P.rope_sin);
+      g.pos = kv->seq_lens; g.kv = kvl;
+      cudaEvent_t pe = m->probe_start(LADDER_PROBE_QKV, s);
+      LAUNCH(launch_gemv(g, GEMV_QKV, m->num_sms, s), gemv_launches(B));
+      m->probe_stop(pe, s);
+
+      AttnDecodeParams a{};
+      a.q = q; a.kv = kvl; a.seq_lens = kv->seq_lens; a.n_q = c.n_q_heads; a.split_len = kSplitLen;
+      a.nsplit = nsplit; a.scale = 1.0f / sqrtf((float)c.head_dim);
+      a.part_o = m->at<float>(P.part_o); a.part_ml = m->at<float>(P.part_ml); a.out = ao;
+      pe = m->probe_start(LADDER_PROBE_ATTN, s);
+      LAUNCH(launch_attn_decode(a, B, c.n_kv_heads, c.head_dim, s), 2);
+      m->probe_stop(pe, s);
+
+      GemvParams o{};
+      o.x = ao; o.ldx = qd; o.g = nullptr; o.B = B; o.K = qd; o.w0 = L.wo; o.n_tasks = d / 2;
+      o.out = m->X(k); o.ldo = d; o.x_res = m->X(k - 1); o.ldr = d;
+      pe = m->probe_start(LADDER_PROBE_OUT, s);
+      LAUNCH(launch_gemv(o, GEMV_RESID, m->num_sms, s), gemv_launches(B));
+      m->probe_stop(pe, s);
+    }
+    // MLP module k = 2l + 2
+    {
+      const int k = 2 * l + 2;
+      GemvParams g{};
+      g.x = m->X(m->input_index(k)); g.ldx = d; g.g = L.mlp_norm; g.eps = c.norm_eps; g.B = B; g.K = d;
+      g.w0 = L.w_gate; g.w1 = L.w_up; g.n_tasks = f; g.out = act; g.ldo = f;
+      cudaEvent_t pe = m->probe_start(LADDER_PROBE_GATEUP, s);
+      LAUNCH(launch_gemv(g, GEMV_GATEUP, m->num_sms, s), gemv_launches(B));
+      m->probe_stop(pe, s);
+
+      GemvParams o{};
+      o.x = act; o.ldx = f; o.g = nullptr; o.B = B; o.K = f; o.w0 = L.w_down; o.n_tasks = d / 2;
+      o.out = m->X(k); o.ldo = d; o.x_res = m->X(k - 1); o.ldr = d;
+      pe = m->probe_start(LADDER_PROBE_DOWN, s);
+      LAUNCH(launch_gemv(o, GEMV_RESID, m->num_sms, s), gemv_launches(B));
+      m->probe_stop(pe, s);
+    }
+  }
+  GemvParams h{};
+  h.x = m->X(2 * c.n_layers); h.ldx = d; h.g = m->final_norm; h.eps = c.norm_eps; h.B = B; h.K = d;
+  h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.out = logits; h.ldo = c.vocab;
+  cudaEvent_t pe = m->probe_start(LADDER_PROBE_LMHEAD, s);
+  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->num_sms, s), gemv_launches(B));
+  m->probe_stop(pe, s);
+  if (next_tok)
+    LAUNCH(launch_argmax(logits, B, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i), kArgmaxBlocks, next_tok, s), 2);
+  LAUNCH(launch_advance(kv->seq_lens, B, s), 1);
+  return LADDER_OK;
+}
+
+}  // namespace
+
+extern "C" int ladder_decode_step(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int32_t B,
+                                  float* logits, int32_t* next_tok, ladder_stream_t stream) {
+  if (!m || !kv || !tokens || !logits) return fail(LADDER_ERR_INVALID, "NULL argument");
+  if (kv->m != m) return fail(LADDER_ERR_INVALID, "KV handle belongs to another model");
+  if (B <= 0 || B > m->cfg.max_batch) return fail(LADDER_ERR_INVALID, "B=%d out of range 1..%d", B, m->cfg.max_batch);
+  int max_ctx = 0;
+  for (int b = 0; b < B; ++b) {
+    if (kv->host_lens[b] + 1 > kv->capacity(b))
+      return fail(LADDER_ERR_CAPACITY, "sequence %d: position %d exceeds its KV capacity %d", b, kv->host_lens[b], kv->capacity(b));
+    if (kv->host_lens[b] + 1 > max_ctx) max_ctx = kv->host_lens[b] + 1;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool use_graph = (m->flags & LADDER_FLAG_DECODE_GRAPH) != 0;
+  if (use_graph && s == nullptr) return fail(LADDER_ERR_INVALID, "graph mode needs a non-default stream");
+  m->launches = 0;
+  if (!use_graph) {
+    const int nsplit = (max_ctx + kSplitLen - 1) / kSplitLen;
+    int rc = enqueue_decode(m, kv, tokens, B, logits, next_tok, nsplit, s);
+    if (rc) return rc;
+  } else {
+    GraphEntry* ge = nullptr;
+    for (auto& g : m->graphs)
+      if (g.B == B && g.tok == tokens && g.logits == logits && g.next == next_tok && g.kv == kv) ge = &g;
+    if (!ge) {
+      CUDA_TRY(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
+      m->capturing = true;
+      int rc = enqueue_decode(m, kv, tokens, B, logits, next_tok, m->plan.nsplit_max, s);
+      m->capturing = false;
+      cudaGraph_t graph = nullptr;
+      cudaError_t e = cudaStreamEndCapture(s, &graph);
+      if (rc) { if (graph) cudaGraphDestroy(graph); return rc; }
+      if (e != cudaSuccess) return fail(LADDER_ERR_CUDA, "graph capture: %s", cudaGetErrorString(e));
+      cudaGraphExec_t exec = nullptr;
+      e = cudaGraphInstantiate(&exec, graph, 0);
+      cudaGraphDestroy(graph);
+      if (e != cudaSuccess) return fail(LADDER_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e));
+      m->graphs.push_back(GraphEntry{B, tokens, logits, next_tok, kv, exec, m->launches});
+      ge = &m->graphs.back();
+    }
+    CUDA_TRY(cudaGraphLaunch(ge->exec, s));
+    m->launches = ge->launches;
+  }
+  for (int b = 0; b < B; ++b) kv->host_lens[b] += 1;
+  return LADDER_OK;
+}
+
+extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tokens, const int32_t* host_lens,
+                              int32_t B, float* logits, int32_t* next_tok, ladder_stream_t stream) {
+  if (!m || !kv || !tokens || !host_lens || !logits) return fail(LADDER_ERR_INVALID, "NULL argument");
+  if (kv->m != m) return fail(LADDER_ERR_INVALID, "KV handle belongs to another model");
+  const ladder_config& c = m->cfg;
+  if (B <= 0 || B > c.max_batch) return fail(LADDER_ERR_INVALID, "B=%d out of range 1..%d", B, c.max_batch);
+  long long total = 0;
+  for (int b = 0; b < B; ++b) {
+    if (host_lens[b] <= 0) return fail(LADDER_ERR_INVALID, "sequence %d: length %d must be positive", b, host_lens[b]);
+    if (kv->host_lens[b] != 0) return fail(LADDER_ERR_INVALID, "sequence %d is not empty: prefill starts from an empty cache", b);
+    if (host_lens[b] > kv->capacity(b))
+      return fail(LADDER_ERR_CAPACITY, "sequence %d: length %d exceeds its KV capacity %d", b, host_lens[b], kv->capacity(b));
+    total += host_lens[b];
+  }
+  if (total > c.max_prefill_tokens)
+    return fail(LADDER_ERR_CAPACITY, "%lld prompt tokens exceed max_prefill_tokens=%d", total, c.max_prefill_tokens);
+  const int M = (int)total;
+  const int Bm = c.max_batch;
+  const Plan& P = m->plan;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  // Row metadata: row_b[M_max], row_pos[M_max], lens[Bm], last_row[Bm].
+  std::vector<int32_t>& meta = m->meta_host;
+  meta.assign(2 * (size_t)P.m_max + 2 * Bm, 0);
+  int32_t* row_b = meta.data();
+  int32_t* row_pos = row_b + P.m_max;
+  int32_t* lens = row_pos + P.m_max;
+  int32_t* last = lens + Bm;
+  int mm = 0;
+  for (int b = 0; b < B; ++b) {
+    for (int t = 0; t < host_lens[b]; ++t, ++mm) {
+      row_b[mm] = b;
+      row_pos[mm] = t;
+    }
+    lens[b] = host_lens[b];
+    last[b] = mm - 1;
+  }
+  m->launches = 0;
+  int32_t* dmeta = m->at<int32_t>(P.meta);
+  CUDA_TRY(cudaMemcpyAsync(dmeta, meta.data(), meta.size() * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+  const int32_t* d_row_b = dmeta;
+  const int32_t* d_row_pos = dmeta + P.m_max;
+  const int32_t* d_lens = d_row_pos + P.m_max;
+  const int32_t* d_last = d_lens + Bm;
+
+  const int d = c.d_model, qd = c.n_q_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim, f = c.ffn_dim;
+  bf16* xn = m->at<bf16>(P.xn);
+  bf16* qb = m->at<bf16>(P.q);
+  bf16* aob = m->at<bf16>(P.ao);
+  bf16* actb = m->at<bf16>(P.act);
+
+  LAUNCH(launch_embed(tokens, M, m->embed, d, c.vocab, m->X(0), m->err(), s), 1);
+  for (int l = 0; l < c.n_layers; ++l) {
+    const LayerW& L = m->layers[l];
+    const KvLayer kvl = kv->layer(l);
+    {
+      const int k = 2 * l + 1;
+      LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.attn_norm, c.norm_eps, xn, s), 1);
+      GemmParams g{};
+      g.A = xn; g.w0 = L.wq; g.w1 = L.wk; g.w2 = L.wv; g.M = M; g.N = qd + 2 * kvd; g.K = d;
+      g.out_bf = qb; g.ldo = qd; g.nq_hd = qd; g.nkv_hd = kvd;
+      g.rope_cos = m->at<float>(P.rope_cos); g.rope_sin = m->at<float>(P.rope_sin);
+      g.row_b = d_row_b; g.row_pos = d_row_pos; g.kv = kvl;
+      LAUNCH(launch_gemm(g, GEMM_QKV, s), 1);
+
+      AttnPrefillParams a{};
+      a.q = qb; a.kv = kvl; a.row_b = d_row_b; a.row_pos = d_row_pos; a.M = M; a.n_q = c.n_q_heads;
+      a.scale = 1.0f / sqrtf((float)c.head_dim); a.out = aob;
+      LAUNCH(launch_attn_prefill(a, c.head_dim, s), 1);
+
+      GemmParams o{};
+      o.A = aob; o.w0 = L.wo; o.M = M; o.N = d; o.K = qd; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);
+      LAUNCH(launch_gemm(o, GEMM_RESID, s), 1);
+    }
+    {
+      const int k = 2 * l + 2;
+      LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.mlp_norm, c.norm_eps, xn, s), 1);
+      GemmParams g{};
+      g.A = xn; g.w0 = L.w_gate; g.w1 = L.w_up; g.M = M; g.N = f; g.K = d; g.out_bf = actb; g.ldo = f;
+      LAUNCH(launch_gemm(g, GEMM_GATEUP, s), 1);
+      GemmParams o{};
+      o.A = actb; o.w0 = L.w_down; o.M = M; o.N = d; o.K = f; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);
+      LAUNCH(launch_gemm(o, GEMM_RESID, s), 1);
+    }
+  }
+  float* xlast = m->at<float>(P.xlast);
+  LAUNCH(launch_gather_rows(m->X(2 * c.n_layers), d, d_last, B, xlast, s), 1);
+  GemvParams h{};
+  h.x = xlast; h.ldx = d; h.g = m->final_norm; h.eps = c.norm_eps; h.B = B; h.K = d;
+  h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.out = logits; h.ldo = c.vocab;
+  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->num_sms, s), gemv_launches(B));
+  if (next_tok)
+    LAUNCH(launch_argmax(logits, B, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i), kArgmaxBlocks, next_tok, s), 2);
+  LAUNCH(launch_set_lens(d_lens, B, kv->seq_lens, s), 1);
+  for (int b = 0; b < B; ++b) kv->host_lens[b] = host_lens[b];
+  return LADDER_OK;
+}

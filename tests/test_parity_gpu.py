@@ -1,0 +1,234 @@
+"""CUDA path vs the CPU oracle, element by element, on the same seeded inputs.
+
+All calls go through the C ABI (libladder.so) via the ctypes binding.
+Tolerance on logits: max-abs 3e-2 and relative L2 1e-2 against the fp32
+oracle (bf16 weights and KV cache, fp32 accumulation and residual stream).
+Integer work (positions, page slots, greedy tokens, lengths) is compared
+exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle.ladder_oracle as O
+from ladder_residual_transformer_gb300 import ladder, synth
+
+from gpu_common import (BF16_NAN, check_greedy, compare_logits, gpu_weights, make_model, oracle_weights,
+                        packed, prompts_for, small_dims)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    dims = small_dims()
+    return dims, gpu_weights(dims), oracle_weights(dims)
+
+
+def run_teacher_forced(model, prompts, feed, graph=False):
+    """Prefill then decode feeding feed[:, s]; returns logits [S+1, B, V] and greedy tokens."""
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        model.set_mode(graph=graph)
+        logits, nxt = model.prefill(packed(prompts), [len(p) for p in prompts])
+        out, toks = [logits.cpu().numpy()], [nxt.cpu().numpy()]
+        tok_dev = torch.empty(len(prompts), dtype=torch.int32, device="cuda")
+        lg = torch.empty(len(prompts), model.dims["vocab"], dtype=torch.float32, device="cuda")
+        nt = torch.empty(len(prompts), dtype=torch.int32, device="cuda")
+        for i in range(feed.shape[1]):
+            tok_dev.copy_(torch.from_numpy(feed[:, i].astype(np.int32)))
+            model.decode_step(tok_dev, lg, nt)
+            out.append(lg.cpu().numpy())
+            toks.append(nt.cpu().numpy())
+    s.synchronize()
+    return np.stack(out), np.stack(toks)
+
+
+def test_tiny_greedy_tokens_and_logits(tiny):
+    dims, gw, ow = tiny
+    prompts = prompts_for([16], dims["vocab"])
+    o_toks, o_logits, _ = O.greedy_generate(dims, ow, prompts, 8)
+    model = make_model(dims, gw, max_batch=1, max_seq=64)
+    g_logits, g_toks = run_teacher_forced(model, prompts, o_toks[:, :8])
+    errs = [compare_logits(g_logits[s], o_logits[s], f"step {s}")[0] for s in range(9)]
+    check_greedy(g_toks[:, 0], o_logits[:, 0], 2 * max(errs))
+    # free-running greedy generation on the device (token fed back without the host)
+    model.reset()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        _, nxt = model.prefill(packed(prompts), [16])
+        gen = [nxt.clone()]
+        for _ in range(8):
+            model.decode_step(nxt, next_tok=nxt)
+            gen.append(nxt.clone())
+    s.synchronize()
+    gen = torch.stack(gen).cpu().numpy()[:, 0]
+    srt = np.sort(o_logits[:, 0], axis=-1)
+    print("oracle top-2 margins", (srt[:, -1] - srt[:, -2]).round(6).tolist(), "max err", max(errs))
+    for s_, (a, b) in enumerate(zip(gen, o_toks[0])):
+        if a != b:  # only a near-tie may make the free run diverge, and then the rest follows a new prefix
+            check_greedy([a], [o_logits[s_, 0]], 2 * max(errs))
+            break
+
+
+def test_kv_cache_layout_is_bit_exact(tiny):
+    dims, gw, ow = tiny
+    page = 16
+    rng = np.random.default_rng(11)
+    model = make_model(dims, gw, max_batch=2, max_seq=64, page_size=page, kv_fill_bits=BF16_NAN,
+                       page_order=rng.permutation(2 * 4))
+    prompts = prompts_for([21, 9], dims["vocab"])
+    feed = np.stack([synth.tokens(5, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(2)])
+    run_teacher_forced(model, prompts, feed)
+    assert [model.seq_len(0), model.seq_len(1)] == [26, 14]
+    assert model.seq_lens.cpu().tolist()[:2] == [26, 14]
+    _, caches = O.teacher_forced_decode(dims, ow, prompts, feed)
+    pool = model.kv_view().float().cpu().numpy()
+    bits = model.kv_pool.view(torch.int16).cpu().numpy().view(np.uint16)
+    written = np.zeros(bits.shape, dtype=bool)
+    for b, cache in enumerate(caches):
+        for p in range(cache.length):
+            pg, off = O.kv_slot(model.host_table[b], p, page)
+            for l in range(dims["n_layers"]):
+                for kv, ref in ((0, cache.k[l]), (1, cache.v[l])):
+                    got = pool[l, pg, kv, :, off, :]
+                    want = ref[p]
+                    assert np.abs(got - want).max() <= 1e-2 * np.abs(want).max() + 1e-3, (b, p, l, kv)
+                    for h in range(dims["n_kv_heads"]):
+                        o = O.kv_pool_offset(dims["n_kv_heads"], dims["head_dim"], model.num_pages, page,
+                                             l, pg, kv, h, off)
+                        written[o:o + dims["head_dim"]] = True
+    # every slot the oracle does not fill still holds the poison bits, untouched
+    assert (bits[~written] == BF16_NAN).all()
+    assert not (bits[written] == BF16_NAN).any()
+
+
+def test_ragged_batch_prefill_and_decode(tiny):
+    dims, gw, ow = tiny
+    lens = [5, 70, 33, 1, 64, 17]
+    prompts = prompts_for(lens, dims["vocab"])
+    feed = np.stack([synth.tokens(3, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(len(lens))])
+    model = make_model(dims, gw, max_batch=6, max_seq=96, page_size=32)
+    g_logits, g_toks = run_teacher_forced(model, prompts, feed)
+    o_logits, _ = O.teacher_forced_decode(dims, ow, prompts, feed)
+    for s in range(4):
+        compare_logits(g_logits[s], o_logits[s], f"step {s}")
+    assert (g_toks[0] == O.argmax_lowest(o_logits[0])).mean() >= 5 / 6
+
+
+@pytest.mark.parametrize("nstd,strict", [(1, 0), (1, 1), (3, 0)])
+def test_hybrid_and_standard_layers(nstd, strict):
+    dims = small_dims(n_layers=3, n_standard_layers=nstd)
+    gw, ow = gpu_weights(dims), oracle_weights(dims)
+    prompts = prompts_for([12, 7], dims["vocab"])
+    feed = np.stack([synth.tokens(2, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(2)])
+    model = make_model(dims, gw, max_batch=2, max_seq=32, page_size=16, strict_boundary=strict)
+    g_logits, _ = run_teacher_forced(model, prompts, feed)
+    o_logits, _ = O.teacher_forced_decode(dims, ow, prompts, feed, strict_boundary=bool(strict))
+    for s in range(3):
+        compare_logits(g_logits[s], o_logits[s], f"nstd {nstd} strict {strict} step {s}")
+
+
+def test_standard_mode_switch_matches_standard_oracle(tiny):
+    dims, gw, _ = tiny
+    prompts = prompts_for([16], dims["vocab"])
+    feed = synth.tokens(3, dims["vocab"], seed=synth.DECODE_SEED)[None, :]
+    model = make_model(dims, gw, max_batch=1, max_seq=32)
+    model.set_mode(standard=True)
+    s = torch.cuda.Stream()
+    std_dims = dict(dims, n_standard_layers=dims["n_layers"])
+    o_logits, _ = O.teacher_forced_decode(std_dims, oracle_weights(std_dims), prompts, feed)
+    with torch.cuda.stream(s):
+        model.set_mode(standard=True)
+        lg, _ = model.prefill(packed(prompts), [16])
+        got = [lg.cpu().numpy()]
+        for i in range(3):
+            lg, _ = model.decode_step(torch.tensor(feed[:, i], dtype=torch.int32, device="cuda"))
+            got.append(lg.cpu().numpy())
+    for i in range(4):
+        compare_logits(got[i], o_logits[i], f"standard step {i}")
+    lad = O.teacher_forced_decode(dims, oracle_weights(dims), prompts, feed)[0]
+    assert np.abs(lad - o_logits).max() > 1e-3  # the two schedules really differ
+
+
+def _bits(name, layer, b):
+    return np.zeros_like(b) if name == "wo" else b
+
+
+def test_zero_wo_makes_ladder_equal_standard_bitwise():
+    dims = small_dims()
+    model = make_model(dims, gpu_weights(dims, transform=_bits), max_batch=1, max_seq=32)
+    prompts = prompts_for([16], dims["vocab"])
+    outs = []
+    for standard in (False, True):
+        model.reset()
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            model.set_mode(standard=standard)
+            lg, nt = model.prefill(packed(prompts), [16])
+            l2, _ = model.decode_step(nt)
+        s.synchronize()
+        outs.append((lg.cpu().numpy(), l2.cpu().numpy()))
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+
+
+def test_graph_replay_equals_eager_and_runs_are_deterministic(tiny):
+    dims, gw, _ = tiny
+    prompts = prompts_for([16, 40], dims["vocab"])
+    feed = np.stack([synth.tokens(6, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(2)])
+    results = []
+    for graph, order in ((False, None), (True, None), (False, np.random.default_rng(3).permutation(2 * 4))):
+        model = make_model(dims, gw, max_batch=2, max_seq=64, page_size=32, page_order=order)
+        results.append(run_teacher_forced(model, prompts, feed, graph=graph))
+        model.close()
+    for r in results[1:]:
+        assert np.array_equal(r[0], results[0][0]) and np.array_equal(r[1], results[0][1])
+
+
+def test_host_and_device_errors(tiny):
+    dims, gw, _ = tiny
+    model = make_model(dims, gw, max_batch=2, max_seq=32, page_size=16)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        # a token id outside the vocabulary is reported by the device error word
+        bad = torch.tensor([3, dims["vocab"] + 5], dtype=torch.int32, device="cuda")
+        model.prefill(bad, [1, 1])
+        assert model.device_error(s) == 1
+        assert model.device_error(s) == 0
+        # prefill on a non-empty sequence and lengths beyond capacity fail before any launch
+        with pytest.raises(ladder.LadderError) as e:
+            model.prefill(packed(prompts_for([4], dims["vocab"])), [4])
+        assert e.value.code == ladder.LADDER_ERR_INVALID
+        model.reset()
+        with pytest.raises(ladder.LadderError) as e:
+            model.prefill(packed(prompts_for([33], dims["vocab"])), [33])
+        assert e.value.code == ladder.LADDER_ERR_CAPACITY
+        model.prefill(packed(prompts_for([31], dims["vocab"])), [31])
+        tok = torch.tensor([1], dtype=torch.int32, device="cuda")
+        model.decode_step(tok)
+        assert model.seq_len(0) == 32
+        with pytest.raises(ladder.LadderError) as e:
+            model.decode_step(tok)
+        assert e.value.code == ladder.LADDER_ERR_CAPACITY
+        assert model.seq_len(0) == 32
+        with pytest.raises(ladder.LadderError):
+            model.decode_step(torch.zeros(3, dtype=torch.int32, device="cuda"))
+    s.synchronize()
+    assert model.seq_lens.cpu().tolist()[0] == 32
+
+
+@pytest.mark.slow
+def test_full_size_1p2b_prefill_and_decode():
+    """The 1.2B workload at its full prompt length, in the graph-replay launch
+    configuration the benchmark times, against the oracle on the same inputs."""
+    dims = dict(synth.PRESETS["1.2b"])
+    gw = gpu_weights(dims)
+    prompts = prompts_for([1024], dims["vocab"])
+    feed = synth.tokens(3, dims["vocab"], seed=synth.DECODE_SEED)[None, :]
+    model = make_model(dims, gw, max_batch=1, max_seq=1024 + 256, max_prefill_tokens=1024)
+    g_logits, g_toks = run_teacher_forced(model, prompts, feed, graph=True)
+    del gw, model
+    torch.cuda.empty_cache()
+    o_logits, _ = O.teacher_forced_decode(dims, O.synthetic_weights(dims), prompts, feed)
+    errs = [compare_logits(g_logits[s], o_logits[s], f"1.2B step {s}")[0] for s in range(4)]
+    check_greedy(g_toks[:, 0], o_logits[:, 0], 2 * max(errs))
