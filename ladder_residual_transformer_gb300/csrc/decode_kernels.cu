@@ -23,25 +23,28 @@ constexpr int GEMV_SMEM_FLOATS = 16384;  // 64 KB staged input per CTA
 // Embedding gather: x[m, :] = float(E[tok[m], :]).  Out-of-range ids write a
 // zero row and set bit 0 of the error word.
 // ---------------------------------------------------------------------------
-__global__ void embed_kernel(const int* __restrict__ tok, const bf16* __restrict__ E, int d, int vocab,
+template <typename WT>
+__global__ void embed_kernel(const int* __restrict__ tok, const WT* __restrict__ E, int d, int vocab,
                              float* __restrict__ x, int* err) {
+  using C = W16<WT>;
   const int m = blockIdx.x;
   const int t = tok[m];
   const bool ok = (unsigned)t < (unsigned)vocab;
   if (!ok && threadIdx.x == 0) atomicOr(err, 1);
-  const bf16* row = E + (size_t)(ok ? t : 0) * d;
+  const WT* row = E + (size_t)(ok ? t : 0) * d;
   float* out = x + (size_t)m * d;
   for (int i = threadIdx.x * 8; i < d; i += blockDim.x * 8) {
     uint4 v = ok ? *reinterpret_cast<const uint4*>(row + i) : make_uint4(0, 0, 0, 0);
-    *reinterpret_cast<float4*>(out + i) = make_float4(bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y));
-    *reinterpret_cast<float4*>(out + i + 4) = make_float4(bf_lo(v.z), bf_hi(v.z), bf_lo(v.w), bf_hi(v.w));
+    *reinterpret_cast<float4*>(out + i) = make_float4(C::lo(v.x), C::hi(v.x), C::lo(v.y), C::hi(v.y));
+    *reinterpret_cast<float4*>(out + i + 4) = make_float4(C::lo(v.z), C::hi(v.z), C::lo(v.w), C::hi(v.w));
   }
 }
 
-cudaError_t launch_embed(const int* tok, int M, const bf16* E, int d, int vocab, float* x, int* err,
+cudaError_t launch_embed(const int* tok, int M, const void* E, int wdt, int d, int vocab, float* x, int* err,
                          cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  embed_kernel<<<M, 128, 0, s>>>(tok, E, d, vocab, x, err);
+  if (wdt == WDT_F16) embed_kernel<f16><<<M, 128, 0, s>>>(tok, static_cast<const f16*>(E), d, vocab, x, err);
+  else embed_kernel<bf16><<<M, 128, 0, s>>>(tok, static_cast<const bf16*>(E), d, vocab, x, err);
   return cudaGetLastError();
 }
 
@@ -56,11 +59,12 @@ cudaError_t launch_embed(const int* tok, int M, const bf16* E, int d, int vocab,
 // k%8 < 4 and k%8 >= 4, so that each lane's 16-byte shared-memory reads are
 // contiguous across the warp (no bank conflicts).
 // ---------------------------------------------------------------------------
-template <int BT>
+template <typename WT, int BT>
 __device__ __forceinline__ void gemv_fma(const uint4& w, const float* __restrict__ u, int kc, int k,
                                          float (&acc)[BT]) {
-  const float w0 = bf_lo(w.x), w1 = bf_hi(w.x), w2 = bf_lo(w.y), w3 = bf_hi(w.y);
-  const float w4 = bf_lo(w.z), w5 = bf_hi(w.z), w6 = bf_lo(w.w), w7 = bf_hi(w.w);
+  using C = W16<WT>;
+  const float w0 = C::lo(w.x), w1 = C::hi(w.x), w2 = C::lo(w.y), w3 = C::hi(w.y);
+  const float w4 = C::lo(w.z), w5 = C::hi(w.z), w6 = C::lo(w.w), w7 = C::hi(w.w);
   const int q = (k >> 3) << 2;
 #pragma unroll
   for (int b = 0; b < BT; ++b) {
@@ -79,8 +83,13 @@ __device__ __forceinline__ void gemv_fma(const uint4& w, const float* __restrict
   }
 }
 
-template <int BT, int MODE>
+template <typename WT, int BT, int MODE>
 __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) {
+  using C = W16<WT>;
+  const WT* g = static_cast<const WT*>(p.g);
+  const WT* W0 = static_cast<const WT*>(p.w0);
+  const WT* W1 = static_cast<const WT*>(p.w1);
+  const WT* W2 = static_cast<const WT*>(p.w2);
   extern __shared__ float4 gemv_smem4[];
   float* u = reinterpret_cast<float*>(gemv_smem4);
   __shared__ float s_red[GEMV_WARPS][BT];
@@ -125,25 +134,25 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
     const bool active = task < p.n_tasks;
 
     // Which two weight rows this task reads.
-    const bf16* row0 = p.w0;
-    const bf16* row1 = p.w0;
+    const WT* row0 = W0;
+    const WT* row1 = W0;
     int local = 0, kind = 0;  // QKV: kind 0 = q, 1 = k, 2 = v; local = row inside its matrix
     if (active) {
       if (MODE == GEMV_QKV) {
         const int r0 = 2 * task;
         if (r0 < p.nq_hd) {
-          local = r0; kind = 0; row0 = p.w0 + (size_t)local * K;
+          local = r0; kind = 0; row0 = W0 + (size_t)local * K;
         } else if (r0 < p.nq_hd + p.nkv_hd) {
-          local = r0 - p.nq_hd; kind = 1; row0 = p.w1 + (size_t)local * K;
+          local = r0 - p.nq_hd; kind = 1; row0 = W1 + (size_t)local * K;
         } else {
-          local = r0 - p.nq_hd - p.nkv_hd; kind = 2; row0 = p.w2 + (size_t)local * K;
+          local = r0 - p.nq_hd - p.nkv_hd; kind = 2; row0 = W2 + (size_t)local * K;
         }
         row1 = row0 + K;
       } else if (MODE == GEMV_GATEUP) {
-        row0 = p.w0 + (size_t)task * K;
-        row1 = p.w1 + (size_t)task * K;
+        row0 = W0 + (size_t)task * K;
+        row1 = W1 + (size_t)task * K;
       } else {
-        row0 = p.w0 + (size_t)(2 * task) * K;
+        row0 = W0 + (size_t)(2 * task) * K;
         row1 = row0 + K;
       }
     }
@@ -159,9 +168,9 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
         // Stage the (normalised) input chunk in the two-plane layout.
         for (int i = tid * 4; i < kc; i += GEMV_THREADS * 4) {
           float4 gv = make_float4(1.f, 1.f, 1.f, 1.f);
-          if (p.g != nullptr) {
-            const uint2 graw = *reinterpret_cast<const uint2*>(p.g + k0 + i);
-            gv = make_float4(bf_lo(graw.x), bf_hi(graw.x), bf_lo(graw.y), bf_hi(graw.y));
+          if (g != nullptr) {
+            const uint2 graw = *reinterpret_cast<const uint2*>(g + k0 + i);
+            gv = make_float4(C::lo(graw.x), C::hi(graw.x), C::lo(graw.y), C::hi(graw.y));
           }
           const int dst = ((i & 4) ? (kc >> 1) : 0) + ((i >> 3) << 2);
 #pragma unroll
@@ -178,8 +187,8 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
         __syncthreads();
       }
       if (active) {
-        const bf16* p0 = row0 + k0;
-        const bf16* p1 = row1 + k0;
+        const WT* p0 = row0 + k0;
+        const WT* p1 = row1 + k0;
         int k = lane * 8;
         for (; k + 768 < kc; k += 1024) {
           uint4 wa[4], wb[4];
@@ -190,15 +199,15 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
           }
 #pragma unroll
           for (int s = 0; s < 4; ++s) {
-            gemv_fma<BT>(wa[s], u, kc, k + 256 * s, a0);
-            gemv_fma<BT>(wb[s], u, kc, k + 256 * s, a1);
+            gemv_fma<WT, BT>(wa[s], u, kc, k + 256 * s, a0);
+            gemv_fma<WT, BT>(wb[s], u, kc, k + 256 * s, a1);
           }
         }
         for (; k < kc; k += 256) {
           const uint4 wa = ld_stream_u4(p0 + k);
           const uint4 wb = ld_stream_u4(p1 + k);
-          gemv_fma<BT>(wa, u, kc, k, a0);
-          gemv_fma<BT>(wb, u, kc, k, a1);
+          gemv_fma<WT, BT>(wa, u, kc, k, a0);
+          gemv_fma<WT, BT>(wb, u, kc, k, a1);
         }
       }
     }
@@ -258,35 +267,45 @@ int gemv_chunk(int B, int K) {
   return K < kc ? K : kc;
 }
 
-template <int BT>
+template <typename WT, int BT>
 static cudaError_t set_gemv_attrs() {
   const int bytes = GEMV_SMEM_FLOATS * 4;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(gemv_kernel<BT, GEMV_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
-  if ((e = cudaFuncSetAttribute(gemv_kernel<BT, GEMV_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
-  if ((e = cudaFuncSetAttribute(gemv_kernel<BT, GEMV_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
-  return cudaFuncSetAttribute(gemv_kernel<BT, GEMV_LOGITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if ((e = cudaFuncSetAttribute(gemv_kernel<WT, BT, GEMV_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
+  if ((e = cudaFuncSetAttribute(gemv_kernel<WT, BT, GEMV_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
+  if ((e = cudaFuncSetAttribute(gemv_kernel<WT, BT, GEMV_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
+  return cudaFuncSetAttribute(gemv_kernel<WT, BT, GEMV_LOGITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 cudaError_t gemv_configure() {
   cudaError_t e;
-  if ((e = set_gemv_attrs<1>())) return e;
-  if ((e = set_gemv_attrs<2>())) return e;
-  return set_gemv_attrs<4>();
+  if ((e = set_gemv_attrs<bf16, 1>())) return e;
+  if ((e = set_gemv_attrs<bf16, 2>())) return e;
+  if ((e = set_gemv_attrs<bf16, 4>())) return e;
+  if ((e = set_gemv_attrs<f16, 1>())) return e;
+  if ((e = set_gemv_attrs<f16, 2>())) return e;
+  return set_gemv_attrs<f16, 4>();
 }
 
-template <int BT>
+template <typename WT, int BT>
 static void gemv_dispatch(const GemvParams& p, int mode, int grid, size_t smem, cudaStream_t s) {
   switch (mode) {
-    case GEMV_QKV: gemv_kernel<BT, GEMV_QKV><<<grid, GEMV_THREADS, smem, s>>>(p); break;
-    case GEMV_GATEUP: gemv_kernel<BT, GEMV_GATEUP><<<grid, GEMV_THREADS, smem, s>>>(p); break;
-    case GEMV_RESID: gemv_kernel<BT, GEMV_RESID><<<grid, GEMV_THREADS, smem, s>>>(p); break;
-    default: gemv_kernel<BT, GEMV_LOGITS><<<grid, GEMV_THREADS, smem, s>>>(p); break;
+    case GEMV_QKV: gemv_kernel<WT, BT, GEMV_QKV><<<grid, GEMV_THREADS, smem, s>>>(p); break;
+    case GEMV_GATEUP: gemv_kernel<WT, BT, GEMV_GATEUP><<<grid, GEMV_THREADS, smem, s>>>(p); break;
+    case GEMV_RESID: gemv_kernel<WT, BT, GEMV_RESID><<<grid, GEMV_THREADS, smem, s>>>(p); break;
+    default: gemv_kernel<WT, BT, GEMV_LOGITS><<<grid, GEMV_THREADS, smem, s>>>(p); break;
   }
 }
 
+template <typename WT>
+static void gemv_dispatch_bt(const GemvParams& p, int bt, int mode, int grid, size_t smem, cudaStream_t s) {
+  if (bt == 1) gemv_dispatch<WT, 1>(p, mode, grid, smem, s);
+  else if (bt == 2) gemv_dispatch<WT, 2>(p, mode, grid, smem, s);
+  else gemv_dispatch<WT, 4>(p, mode, grid, smem, s);
+}
+
 // Batches larger than 4 run as consecutive chunks of at most 4 rows.
-cudaError_t launch_gemv(const GemvParams& p0, int mode, int num_sms, cudaStream_t s) {
+cudaError_t launch_gemv(const GemvParams& p0, int mode, int wdt, int num_sms, cudaStream_t s) {
   for (int b0 = 0; b0 < p0.B; b0 += 4) {
     GemvParams p = p0;
     p.B = p0.B - b0 < 4 ? p0.B - b0 : 4;
@@ -301,9 +320,8 @@ cudaError_t launch_gemv(const GemvParams& p0, int mode, int num_sms, cudaStream_
     int grid = (p.n_tasks + GEMV_WARPS - 1) / GEMV_WARPS;
     const int cap = num_sms * 4;
     if (grid > cap) grid = cap;
-    if (bt == 1) gemv_dispatch<1>(p, mode, grid, smem, s);
-    else if (bt == 2) gemv_dispatch<2>(p, mode, grid, smem, s);
-    else gemv_dispatch<4>(p, mode, grid, smem, s);
+    if (wdt == WDT_F16) gemv_dispatch_bt<f16>(p, bt, mode, grid, smem, s);
+    else gemv_dispatch_bt<bf16>(p, bt, mode, grid, smem, s);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -19,6 +19,7 @@
 #include "internal.cuh"
 
 #include <cuda.h>
+#include <string.h>
 
 namespace ladder {
 
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
     tc_fence_after();
     if (!ok) {
       if (lane == 0) atomicOr(err, 2);
-    } else if (!*reinterpret_cast<volatile int*>(bail)) {
+    } else if (!__shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(bail), 0)) {
       const int m = m0 + warp * 32 + lane;
       const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
       if (MODE == GEMM_GATEUP) {

@@ -4,11 +4,40 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 typedef __nv_bfloat16 bf16;
+typedef __half f16;
 
 namespace ladder {
+
+// ---------------------------------------------------------------------------
+// 16-bit storage types of weights and tensor-core operands.  `lo`/`hi` widen
+// the first/second element of a packed pair; `pack` rounds two floats to
+// nearest even; `umma_fmt` is the operand format code of tcgen05 kind::f16.
+// ---------------------------------------------------------------------------
+enum WeightDtype { WDT_BF16 = 0, WDT_F16 = 1 };
+
+template <typename T> struct W16;
+template <> struct W16<bf16> {
+  static __device__ __forceinline__ float lo(uint32_t v) { return __uint_as_float(v << 16); }
+  static __device__ __forceinline__ float hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+  static __device__ __forceinline__ uint32_t pack(float a, float b) {
+    __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&t);
+  }
+  static constexpr uint32_t umma_fmt = 1;
+};
+template <> struct W16<f16> {
+  static __device__ __forceinline__ float lo(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xffffu))); }
+  static __device__ __forceinline__ float hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
+  static __device__ __forceinline__ uint32_t pack(float a, float b) {
+    __half2 t = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&t);
+  }
+  static constexpr uint32_t umma_fmt = 0;
+};
 
 // ---------------------------------------------------------------------------
 // Device helpers
@@ -63,12 +92,12 @@ enum GemvMode { GEMV_QKV = 0, GEMV_GATEUP = 1, GEMV_RESID = 2, GEMV_LOGITS = 3 }
 struct GemvParams {
   const float* x;    // input rows [B][ldx] fp32
   int ldx;
-  const bf16* g;     // RMSNorm gain [K], or nullptr for no norm
+  const void* g;     // RMSNorm gain [K] (weight dtype), or nullptr for no norm
   float eps;
   int B, K;
-  const bf16* w0;    // QKV: wq, GATEUP: w_gate, RESID/LOGITS: w
-  const bf16* w1;    // QKV: wk, GATEUP: w_up
-  const bf16* w2;    // QKV: wv
+  const void* w0;    // QKV: wq, GATEUP: w_gate, RESID/LOGITS: w (weight dtype)
+  const void* w1;    // QKV: wk, GATEUP: w_up
+  const void* w2;    // QKV: wv
   int n_tasks;       // row pairs (QKV, RESID, LOGITS) or rows (GATEUP)
   int kc;            // K chunk staged in shared memory (multiple of 256)
   float* out;        // QKV: q [B][ldo]; GATEUP: act [B][ldo]; RESID: x_out; LOGITS: logits
@@ -99,12 +128,8 @@ struct AttnDecodeParams {
 enum GemmMode { GEMM_QKV = 0, GEMM_GATEUP = 1, GEMM_RESID = 2 };
 
 struct GemmParams {
-  const bf16* A;        // [M][K] activations
-  const bf16* w0;       // QKV: wq; GATEUP: w_gate; RESID: w
-  const bf16* w1;       // QKV: wk; GATEUP: w_up
-  const bf16* w2;       // QKV: wv
   int M, N, K;
-  bf16* out_bf;         // QKV: q [M][ldo]; GATEUP: act [M][ldo]
+  void* out_h;          // QKV: q (bf16) [M][ldo]; GATEUP: act (weight dtype) [M][ldo]
   float* out_f;         // RESID: x_out [M][ldo]
   int ldo;
   const float* x_res;   // RESID
@@ -118,21 +143,21 @@ struct GemmParams {
 };
 
 struct AttnPrefillParams {
-  const bf16* q;        // [M][n_q * hd]
+  const bf16* q;        // [M][n_q * hd] rotated queries
   KvLayer kv;
-  const int* row_b;
-  const int* row_pos;
-  int M, n_q;
+  const int* seq_start; // first packed row of sequence b
+  const int* seq_len;   // length of sequence b
+  int n_q;
   float scale;
-  bf16* out;            // [M][n_q * hd]
+  void* out;            // [M][n_q * hd] in the weight dtype (operand of the O projection)
 };
 
 // ---------------------------------------------------------------------------
 // Launchers (each returns the cudaError_t of its launch)
 // ---------------------------------------------------------------------------
-cudaError_t launch_embed(const int* tok, int M, const bf16* E, int d, int vocab, float* x, int* err,
+cudaError_t launch_embed(const int* tok, int M, const void* E, int wdt, int d, int vocab, float* x, int* err,
                          cudaStream_t s);
-cudaError_t launch_gemv(const GemvParams& p, int mode, int num_sms, cudaStream_t s);
+cudaError_t launch_gemv(const GemvParams& p, int mode, int wdt, int num_sms, cudaStream_t s);
 cudaError_t gemv_configure();
 int gemv_chunk(int B, int K);
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, int B, int n_kv, int hd, cudaStream_t s);
@@ -142,10 +167,16 @@ cudaError_t launch_advance(int* seq_lens, int B, cudaStream_t s);
 cudaError_t launch_rope_tables(float* cos_t, float* sin_t, int max_seq, int hd, float theta,
                                cudaStream_t s);
 
-cudaError_t launch_rmsnorm_rows(const float* x, int M, int d, const bf16* g, float eps, bf16* out,
+cudaError_t launch_rmsnorm_rows(const float* x, int M, int d, const void* g, float eps, void* out, int wdt,
                                 cudaStream_t s);
-cudaError_t launch_gemm(const GemmParams& p, int mode, cudaStream_t s);
-cudaError_t launch_attn_prefill(const AttnPrefillParams& p, int hd, cudaStream_t s);
+// Tensor-core GEMM (tcgen05 + TMA).  Maps are CUtensorMap objects made by make_tma_map.
+bool make_tma_map(void* map_out, const void* base, uint64_t rows, uint64_t cols, int wdt);
+cudaError_t gemm_tc_configure();
+cudaError_t launch_gemm_tc(const void* a_map, const void* b0, const void* b1, const void* b2, const GemmParams& p,
+                           int mode, int wdt, int* err, cudaStream_t s);
+// Tensor-core causal attention for packed prefill rows (mma.sync, bf16 Q/K/V).
+cudaError_t attn_prefill_configure();
+cudaError_t launch_attn_prefill_tc(const AttnPrefillParams& p, int hd, int wdt, int B, int max_len, cudaStream_t s);
 cudaError_t launch_gather_rows(const float* x, int d, const int* rows, int B, float* out,
                                cudaStream_t s);
 cudaError_t launch_set_lens(const int* lens, int B, int* seq_lens, cudaStream_t s);

@@ -4,6 +4,8 @@
 #include "ladder.h"
 #include "internal.cuh"
 
+#include <cuda.h>
+
 #include <algorithm>
 #include <cmath>
 #include <cstdarg>
@@ -46,7 +48,7 @@ constexpr int kArgmaxBlocks = 64;   // partial argmax blocks per sequence
 struct Plan {
   size_t x[3], xn, q, ao, act, part_o, part_ml, am_v, am_i, rope_cos, rope_sin, meta, xlast, err;
   size_t total;
-  int m_max, nsplit_max;
+  int m_max, m_pad, nsplit_max;
 };
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -56,7 +58,8 @@ Plan make_plan(const ladder_config& c) {
   const size_t d = c.d_model, qd = (size_t)c.n_q_heads * c.head_dim, f = c.ffn_dim;
   p.m_max = c.max_prefill_tokens > c.max_batch ? c.max_prefill_tokens : c.max_batch;
   p.nsplit_max = (c.max_seq + kSplitLen - 1) / kSplitLen;
-  const size_t M = p.m_max, Bm = c.max_batch;
+  p.m_pad = (p.m_max + 127) / 128 * 128;  // tensor-core operands are read in 128-row tiles
+  const size_t M = p.m_max, Mp = p.m_pad, Bm = c.max_batch;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -64,10 +67,10 @@ Plan make_plan(const ladder_config& c) {
     return o;
   };
   for (int i = 0; i < 3; ++i) p.x[i] = take(M * d * 4);
-  p.xn = take(M * d * 2);
-  p.q = take(M * qd * 4);
-  p.ao = take(M * qd * 4);
-  p.act = take(std::max(M * f * 2, Bm * f * 4));
+  p.xn = take(Mp * d * 2);
+  p.q = take(std::max(M * qd * 2, Bm * qd * 4));
+  p.ao = take(std::max(Mp * qd * 2, Bm * qd * 4));
+  p.act = take(std::max(Mp * f * 2, Bm * f * 4));
   p.part_o = take(Bm * c.n_q_heads * (size_t)p.nsplit_max * c.head_dim * 4);
   p.part_ml = take(Bm * c.n_q_heads * (size_t)p.nsplit_max * 2 * 4);
   p.am_v = take(Bm * kArgmaxBlocks * 4);
@@ -120,6 +123,11 @@ struct LayerW {
   const bf16 *attn_norm, *wq, *wk, *wv, *wo, *mlp_norm, *w_gate, *w_up, *w_down;
 };
 
+// Tensor maps of one layer's weights for the prefill GEMMs.
+struct LayerMaps {
+  CUtensorMap wq, wk, wv, wo, gate, up, down;
+};
+
 struct GraphEntry {
   int B;
   const int32_t* tok;
@@ -136,6 +144,8 @@ struct ladder_model {
   ladder_config cfg;
   const bf16 *embed, *final_norm, *lm_head;
   std::vector<LayerW> layers;
+  std::vector<LayerMaps> maps;
+  CUtensorMap map_xn, map_ao, map_act;  // activation operands, m_pad rows
   char* ws;
   Plan plan;
   int num_sms;
@@ -274,10 +284,30 @@ int ladder_create(const ladder_config* cfg, const ladder_weights* w, void* works
   }
   m->ws = static_cast<char*>(workspace);
   m->plan = plan;
+  {
+    const ladder_config& c = *cfg;
+    const uint64_t d = c.d_model, qd = (uint64_t)c.n_q_heads * c.head_dim, kvd = (uint64_t)c.n_kv_heads * c.head_dim;
+    const uint64_t f = c.ffn_dim, Mp = plan.m_pad;
+    bool ok = make_tma_map(&m->map_xn, m->ws + plan.xn, Mp, d) && make_tma_map(&m->map_ao, m->ws + plan.ao, Mp, qd) &&
+              make_tma_map(&m->map_act, m->ws + plan.act, Mp, f);
+    m->maps.resize(c.n_layers);
+    for (int l = 0; ok && l < c.n_layers; ++l) {
+      const LayerW& L = m->layers[l];
+      LayerMaps& T = m->maps[l];
+      ok = make_tma_map(&T.wq, L.wq, qd, d) && make_tma_map(&T.wk, L.wk, kvd, d) && make_tma_map(&T.wv, L.wv, kvd, d) &&
+           make_tma_map(&T.wo, L.wo, d, qd) && make_tma_map(&T.gate, L.w_gate, f, d) &&
+           make_tma_map(&T.up, L.w_up, f, d) && make_tma_map(&T.down, L.w_down, d, f);
+    }
+    if (!ok) {
+      delete m;
+      return fail(LADDER_ERR_CUDA, "ladder_create: could not encode TMA tensor maps (driver entry point missing?)");
+    }
+  }
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess) e = gemv_configure();
+  if (e == cudaSuccess) e = gemm_tc_configure();
   if (e == cudaSuccess) e = cudaMemsetAsync(m->err(), 0, 256, stream);
   if (e == cudaSuccess)
     e = launch_rope_tables(m->at<float>(plan.rope_cos), m->at<float>(plan.rope_sin), cfg->max_seq, cfg->head_dim,
@@ -635,7 +665,8 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
       g.out_bf = qb; g.ldo = qd; g.nq_hd = qd; g.nkv_hd = kvd;
       g.rope_cos = m->at<float>(P.rope_cos); g.rope_sin = m->at<float>(P.rope_sin);
       g.row_b = d_row_b; g.row_pos = d_row_pos; g.kv = kvl;
-      LAUNCH(launch_gemm(g, GEMM_QKV, s), 1);
+      const LayerMaps& T = m->maps[l];
+      LAUNCH(launch_gemm_tc(&m->map_xn, &T.wq, &T.wk, &T.wv, g, GEMM_QKV, m->err(), s), 1);
 
       AttnPrefillParams a{};
       a.q = qb; a.kv = kvl; a.row_b = d_row_b; a.row_pos = d_row_pos; a.M = M; a.n_q = c.n_q_heads;
@@ -644,17 +675,18 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
 
       GemmParams o{};
       o.A = aob; o.w0 = L.wo; o.M = M; o.N = d; o.K = qd; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);
-      LAUNCH(launch_gemm(o, GEMM_RESID, s), 1);
+      LAUNCH(launch_gemm_tc(&m->map_ao, &T.wo, nullptr, nullptr, o, GEMM_RESID, m->err(), s), 1);
     }
     {
       const int k = 2 * l + 2;
       LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.mlp_norm, c.norm_eps, xn, s), 1);
       GemmParams g{};
       g.A = xn; g.w0 = L.w_gate; g.w1 = L.w_up; g.M = M; g.N = f; g.K = d; g.out_bf = actb; g.ldo = f;
-      LAUNCH(launch_gemm(g, GEMM_GATEUP, s), 1);
+      const LayerMaps& T = m->maps[l];
+      LAUNCH(launch_gemm_tc(&m->map_xn, &T.gate, &T.up, nullptr, g, GEMM_GATEUP, m->err(), s), 1);
       GemmParams o{};
       o.A = actb; o.w0 = L.w_down; o.M = M; o.N = d; o.K = f; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);
-      LAUNCH(launch_gemm(o, GEMM_RESID, s), 1);
+      LAUNCH(launch_gemm_tc(&m->map_act, &T.down, nullptr, nullptr, o, GEMM_RESID, m->err(), s), 1);
     }
   }
   float* xlast = m->at<float>(P.xlast);
