@@ -100,10 +100,18 @@ typedef struct {
   int32_t max_seq;            /* positions per sequence */
   int32_t max_prefill_tokens; /* packed prompt tokens per prefill call */
   int32_t strict_boundary;    /* 0: first ladder module reads x_b; 1: reads x_{b-1} */
+  int32_t weight_dtype;       /* storage of weights and prefill tensor-core operands:
+                                 LADDER_DTYPE_BF16 or LADDER_DTYPE_F16 */
 } ladder_config;
 
-/* Weights: bf16 device pointers, row-major [out_features, in_features] unless
- * stated, 16-byte aligned.  Per-layer fields are HOST arrays of n_layers device
+/* Weight storage types.  bf16-valued weights convert to fp16 exactly when
+ * 2^-17 <= |w| <= 65504; with LADDER_DTYPE_F16 the prefill GEMM operands
+ * (normalised activations, attention output, SwiGLU output) are fp16 as well,
+ * which carries 3 more mantissa bits than bf16.  The KV cache is bf16 in both. */
+enum { LADDER_DTYPE_BF16 = 0, LADDER_DTYPE_F16 = 1 };
+
+/* Weights: device pointers of the configured weight_dtype (bf16 or fp16),
+ * row-major [out_features, in_features] unless stated, 16-byte aligned.  Per-layer fields are HOST arrays of n_layers device
  * pointers; the library copies the pointer values during ladder_create.
  *   embed [vocab, d_model]; final_norm [d_model]; lm_head [vocab, d_model]
  *   (ignored when tie_embeddings); attn_norm, mlp_norm [d_model];

@@ -57,7 +57,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int HD>
+template <typename OT, int HD>
 __global__ void __launch_bounds__(FA_THREADS) attn_prefill_kernel(const AttnPrefillParams p) {
   constexpr int LD = HD + 8;  // padded row (elements): conflict-free ldmatrix
   constexpr int KT = HD / 16; // k-steps over the head dimension
@@ -67,7 +67,8 @@ __global__ void __launch_bounds__(FA_THREADS) attn_prefill_kernel(const AttnPref
   bf16* sK = sQ + FA_BM * LD;        // [2][FA_BN][LD]
   bf16* sV = sK + 2 * FA_BN * LD;    // [2][FA_BN][LD]
 
-  const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // The heaviest (last) query blocks of the causal triangle are scheduled first.
+  const int qb = gridDim.x - 1 - blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int T = p.seq_len[b];
   if (qb * FA_BM >= T) return;
   const int start = p.seq_start[b];
@@ -210,30 +211,42 @@ __global__ void __launch_bounds__(FA_THREADS) attn_prefill_kernel(const AttnPref
   for (int r = 0; r < 2; ++r) {
     const int pos = qpos0 + r * 8;
     if (pos >= T) continue;
-    bf16* dst = p.out + (size_t)(start + pos) * ldq + (size_t)h * HD + 2 * (lane & 3);
+    OT* dst = static_cast<OT*>(p.out) + (size_t)(start + pos) * ldq + (size_t)h * HD + 2 * (lane & 3);
     const float inv = r ? inv1 : inv0;
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      *reinterpret_cast<uint32_t*>(dst + j * 8) = pack_bf16(o[j][2 * r] * inv, o[j][2 * r + 1] * inv);
+      *reinterpret_cast<uint32_t*>(dst + j * 8) = W16<OT>::pack(o[j][2 * r] * inv, o[j][2 * r + 1] * inv);
     }
   }
 }
 
 size_t attn_prefill_smem(int hd) { return (size_t)(FA_BM + 4 * FA_BN) * (hd + 8) * sizeof(bf16); }
 
-cudaError_t attn_prefill_configure() {
-  cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <typename OT>
+static cudaError_t attn_prefill_configure_t() {
+  cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel<OT, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)attn_prefill_smem(64));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attn_prefill_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(attn_prefill_kernel<OT, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)attn_prefill_smem(128));
 }
 
-cudaError_t launch_attn_prefill_tc(const AttnPrefillParams& p, int hd, int B, int max_len, cudaStream_t s) {
+cudaError_t attn_prefill_configure() {
+  cudaError_t e = attn_prefill_configure_t<bf16>();
+  return e != cudaSuccess ? e : attn_prefill_configure_t<f16>();
+}
+
+template <typename OT>
+static void attn_prefill_dispatch(const AttnPrefillParams& p, int hd, dim3 grid, cudaStream_t s) {
+  if (hd == 64) attn_prefill_kernel<OT, 64><<<grid, FA_THREADS, attn_prefill_smem(64), s>>>(p);
+  else attn_prefill_kernel<OT, 128><<<grid, FA_THREADS, attn_prefill_smem(128), s>>>(p);
+}
+
+cudaError_t launch_attn_prefill_tc(const AttnPrefillParams& p, int hd, int wdt, int B, int max_len, cudaStream_t s) {
   if (max_len <= 0) return cudaSuccess;
   dim3 grid((max_len + FA_BM - 1) / FA_BM, p.n_q, B);
-  if (hd == 64) attn_prefill_kernel<64><<<grid, FA_THREADS, attn_prefill_smem(64), s>>>(p);
-  else attn_prefill_kernel<128><<<grid, FA_THREADS, attn_prefill_smem(128), s>>>(p);
+  if (wdt == WDT_F16) attn_prefill_dispatch<f16>(p, hd, grid, s);
+  else attn_prefill_dispatch<bf16>(p, hd, grid, s);
   return cudaGetLastError();
 }
 

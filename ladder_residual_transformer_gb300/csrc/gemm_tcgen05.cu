@@ -85,9 +85,10 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor of kind::f16: bf16 A and B, fp32 D, both K-major.
-__host__ __device__ constexpr uint32_t umma_idesc(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor of kind::f16: A and B of format `fmt` (0 = f16, 1 = bf16),
+// fp32 D, both K-major, M x N.
+__host__ __device__ constexpr uint32_t umma_idesc(int M, int N, uint32_t fmt) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -155,9 +156,10 @@ struct TcMaps {
   CUtensorMap b[3];
 };
 
-template <int MODE>
+template <typename WT, int MODE>
 __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_constant__ TcMaps maps,
                                                                 const GemmParams p, int* err) {
+  using C = W16<WT>;
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + TC_STAGES * TC_STAGE_BYTES);
@@ -218,7 +220,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
     }
   } else if (warp == 5) {
     if (lane == 0) {
-      constexpr uint32_t idesc = umma_idesc(TC_BM, TC_BN);
+      constexpr uint32_t idesc = umma_idesc(TC_BM, TC_BN, C::umma_fmt);
       for (int kb = 0; kb < nkb; ++kb) {
         const int s = kb % TC_STAGES;
         const uint32_t ph = (kb / TC_STAGES) & 1;
@@ -251,18 +253,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
           tmem_ld32(trow + c * 32, g);
           tmem_ld32(trow + 128 + c * 32, u);
           if (m < p.M) {
-            bf16* dst = p.out_bf + (size_t)m * p.ldo + tile_n * 128 + c * 32;
+            WT* dst = static_cast<WT*>(p.out_h) + (size_t)m * p.ldo + tile_n * 128 + c * 32;
 #pragma unroll
             for (int j = 0; j < 32; j += 8) {
               uint4 pk;
-              __nv_bfloat162 t0 = __floats2bfloat162_rn(silu_f(g[j]) * u[j], silu_f(g[j + 1]) * u[j + 1]);
-              __nv_bfloat162 t1 = __floats2bfloat162_rn(silu_f(g[j + 2]) * u[j + 2], silu_f(g[j + 3]) * u[j + 3]);
-              __nv_bfloat162 t2 = __floats2bfloat162_rn(silu_f(g[j + 4]) * u[j + 4], silu_f(g[j + 5]) * u[j + 5]);
-              __nv_bfloat162 t3 = __floats2bfloat162_rn(silu_f(g[j + 6]) * u[j + 6], silu_f(g[j + 7]) * u[j + 7]);
-              pk.x = *reinterpret_cast<uint32_t*>(&t0);
-              pk.y = *reinterpret_cast<uint32_t*>(&t1);
-              pk.z = *reinterpret_cast<uint32_t*>(&t2);
-              pk.w = *reinterpret_cast<uint32_t*>(&t3);
+              pk.x = C::pack(silu_f(g[j]) * u[j], silu_f(g[j + 1]) * u[j + 1]);
+              pk.y = C::pack(silu_f(g[j + 2]) * u[j + 2], silu_f(g[j + 3]) * u[j + 3]);
+              pk.z = C::pack(silu_f(g[j + 4]) * u[j + 4], silu_f(g[j + 5]) * u[j + 5]);
+              pk.w = C::pack(silu_f(g[j + 6]) * u[j + 6], silu_f(g[j + 7]) * u[j + 7]);
               *reinterpret_cast<uint4*>(dst + j) = pk;
             }
           }
@@ -290,6 +288,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
           tmem_ld32(trow + c * 32, v);
           int map, row;
           if (!b_half<GEMM_QKV>(p, tile_n, c >> 2, map, row) || m >= p.M) continue;
+          // q and the KV cache are bf16 whatever the weight type (the attention kernels read bf16)
           const int local = row + (c & 3) * 32;  // first column of the chunk inside its matrix
           const int head = local / hd, dim0 = local % hd;
           if (map < 2) {
@@ -303,7 +302,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
               v[j + 1] = a0 * sj + a1 * cj;
             }
           }
-          bf16* dst = map == 0 ? p.out_bf + (size_t)m * p.ldo + local
+          bf16* dst = map == 0 ? static_cast<bf16*>(p.out_h) + (size_t)m * p.ldo + local
                                : p.kv.base + p.kv.slot(b, pos, map - 1, head) + dim0;
 #pragma unroll
           for (int j = 0; j < 32; j += 8) {
@@ -350,29 +349,47 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Row-major bf16 [rows, cols] matrix, box of 128 rows x 64 columns, 128-byte swizzle.
-bool make_tma_map(void* map_out, const void* base, uint64_t rows, uint64_t cols) {
+// Row-major 16-bit [rows, cols] matrix, box of 128 rows x 64 columns, 128-byte swizzle.
+bool make_tma_map(void* map_out, const void* base, uint64_t rows, uint64_t cols, int wdt) {
   EncodeTiledFn fn = encode_fn();
   if (!fn || rows % 128 || cols % 64 || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
   cuuint32_t box[2] = {TC_BK, 128};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(reinterpret_cast<CUtensorMap*>(map_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+  const CUtensorMapDataType dt = wdt == WDT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = fn(reinterpret_cast<CUtensorMap*>(map_out), dt, 2, const_cast<void*>(base),
                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-cudaError_t gemm_tc_configure() {
+template <typename WT>
+static cudaError_t gemm_tc_configure_t() {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<GEMM_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<GEMM_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  return cudaFuncSetAttribute(gemm_tc_kernel<GEMM_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  return cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+}
+
+cudaError_t gemm_tc_configure() {
+  cudaError_t e = gemm_tc_configure_t<bf16>();
+  return e != cudaSuccess ? e : gemm_tc_configure_t<f16>();
+}
+
+template <typename WT>
+static void gemm_tc_dispatch(const TcMaps& maps, const GemmParams& p, int mode, int mt, int* err, cudaStream_t s) {
+  if (mode == GEMM_GATEUP) {
+    gemm_tc_kernel<WT, GEMM_GATEUP><<<dim3(p.N / 128, mt), TC_THREADS, TC_SMEM, s>>>(maps, p, err);
+  } else if (mode == GEMM_RESID) {
+    gemm_tc_kernel<WT, GEMM_RESID><<<dim3(p.N / TC_BN, mt), TC_THREADS, TC_SMEM, s>>>(maps, p, err);
+  } else {
+    gemm_tc_kernel<WT, GEMM_QKV><<<dim3((p.N + TC_BN - 1) / TC_BN, mt), TC_THREADS, TC_SMEM, s>>>(maps, p, err);
+  }
 }
 
 cudaError_t launch_gemm_tc(const void* a_map, const void* b0, const void* b1, const void* b2, const GemmParams& p,
-                           int mode, int* err, cudaStream_t s) {
+                           int mode, int wdt, int* err, cudaStream_t s) {
   if (p.M <= 0) return cudaSuccess;
   TcMaps maps;
   memcpy(&maps.a, a_map, sizeof(CUtensorMap));
@@ -380,13 +397,8 @@ cudaError_t launch_gemm_tc(const void* a_map, const void* b0, const void* b1, co
   memcpy(&maps.b[1], b1 ? b1 : b0, sizeof(CUtensorMap));
   memcpy(&maps.b[2], b2 ? b2 : b0, sizeof(CUtensorMap));
   const int mt = (p.M + TC_BM - 1) / TC_BM;
-  if (mode == GEMM_GATEUP) {
-    gemm_tc_kernel<GEMM_GATEUP><<<dim3(p.N / 128, mt), TC_THREADS, TC_SMEM, s>>>(maps, p, err);
-  } else if (mode == GEMM_RESID) {
-    gemm_tc_kernel<GEMM_RESID><<<dim3(p.N / TC_BN, mt), TC_THREADS, TC_SMEM, s>>>(maps, p, err);
-  } else {
-    gemm_tc_kernel<GEMM_QKV><<<dim3((p.N + TC_BN - 1) / TC_BN, mt), TC_THREADS, TC_SMEM, s>>>(maps, p, err);
-  }
+  if (wdt == WDT_F16) gemm_tc_dispatch<f16>(maps, p, mode, mt, err, s);
+  else gemm_tc_dispatch<bf16>(maps, p, mode, mt, err, s);
   return cudaGetLastError();
 }
 

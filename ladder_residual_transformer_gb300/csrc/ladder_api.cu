@@ -77,7 +77,7 @@ Plan make_plan(const ladder_config& c) {
   p.am_i = take(Bm * kArgmaxBlocks * 4);
   p.rope_cos = take((size_t)c.max_seq * (c.head_dim / 2) * 4);
   p.rope_sin = take((size_t)c.max_seq * (c.head_dim / 2) * 4);
-  p.meta = take((2 * M + 2 * Bm) * 4);
+  p.meta = take((2 * M + 3 * Bm) * 4);
   p.xlast = take(Bm * d * 4);
   p.err = take(256);
   p.total = off;
@@ -114,13 +114,15 @@ int validate_config(const ladder_config* c) {
   if (c->max_prefill_tokens <= 0) return fail(LADDER_ERR_INVALID, "max_prefill_tokens must be positive");
   if (c->tie_embeddings != 0 && c->tie_embeddings != 1) return fail(LADDER_ERR_INVALID, "tie_embeddings must be 0 or 1");
   if (c->strict_boundary != 0 && c->strict_boundary != 1) return fail(LADDER_ERR_INVALID, "strict_boundary must be 0 or 1");
+  if (c->weight_dtype != LADDER_DTYPE_BF16 && c->weight_dtype != LADDER_DTYPE_F16)
+    return fail(LADDER_ERR_INVALID, "weight_dtype=%d must be LADDER_DTYPE_BF16 or LADDER_DTYPE_F16", c->weight_dtype);
   return LADDER_OK;
 }
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 struct LayerW {
-  const bf16 *attn_norm, *wq, *wk, *wv, *wo, *mlp_norm, *w_gate, *w_up, *w_down;
+  const void *attn_norm, *wq, *wk, *wv, *wo, *mlp_norm, *w_gate, *w_up, *w_down;
 };
 
 // Tensor maps of one layer's weights for the prefill GEMMs.
@@ -142,7 +144,8 @@ struct GraphEntry {
 
 struct ladder_model {
   ladder_config cfg;
-  const bf16 *embed, *final_norm, *lm_head;
+  const void *embed, *final_norm, *lm_head;
+  int wdt;  // weight dtype
   std::vector<LayerW> layers;
   std::vector<LayerMaps> maps;
   CUtensorMap map_xn, map_ao, map_act;  // activation operands, m_pad rows
@@ -154,6 +157,12 @@ struct ladder_model {
   int launches = 0;
   std::vector<GraphEntry> graphs;
   std::vector<int32_t> meta_host;
+  // Second stream of the decode schedule (the MLP chain of ladder layers) and the
+  // events that order the two chains: one per stream buffer, recorded after the
+  // kernel that writes it, plus one to fork the second stream from the caller's.
+  cudaStream_t aux = nullptr;
+  cudaEvent_t ev_slot[3] = {nullptr, nullptr, nullptr};
+  cudaEvent_t ev_fork = nullptr;
   // launch probe
   int probe_class = -1;
   int probe_count = 0;
@@ -260,24 +269,25 @@ int ladder_create(const ladder_config* cfg, const ladder_weights* w, void* works
 
   auto* m = new ladder_model();
   m->cfg = *cfg;
-  m->embed = static_cast<const bf16*>(w->embed);
-  m->final_norm = static_cast<const bf16*>(w->final_norm);
-  m->lm_head = static_cast<const bf16*>(cfg->tie_embeddings ? w->embed : w->lm_head);
+  m->embed = w->embed;
+  m->final_norm = w->final_norm;
+  m->lm_head = cfg->tie_embeddings ? w->embed : w->lm_head;
+  m->wdt = cfg->weight_dtype;
   const void* globals[3] = {m->embed, m->final_norm, m->lm_head};
   for (const void* p : globals)
     if (!aligned(p, 16)) { delete m; return fail(LADDER_ERR_INVALID, "weights must be 16-byte aligned"); }
   m->layers.resize(cfg->n_layers);
   for (int l = 0; l < cfg->n_layers; ++l) {
     LayerW& L = m->layers[l];
-    L.attn_norm = static_cast<const bf16*>(w->attn_norm[l]);
-    L.wq = static_cast<const bf16*>(w->wq[l]);
-    L.wk = static_cast<const bf16*>(w->wk[l]);
-    L.wv = static_cast<const bf16*>(w->wv[l]);
-    L.wo = static_cast<const bf16*>(w->wo[l]);
-    L.mlp_norm = static_cast<const bf16*>(w->mlp_norm[l]);
-    L.w_gate = static_cast<const bf16*>(w->w_gate[l]);
-    L.w_up = static_cast<const bf16*>(w->w_up[l]);
-    L.w_down = static_cast<const bf16*>(w->w_down[l]);
+    L.attn_norm = w->attn_norm[l];
+    L.wq = w->wq[l];
+    L.wk = w->wk[l];
+    L.wv = w->wv[l];
+    L.wo = w->wo[l];
+    L.mlp_norm = w->mlp_norm[l];
+    L.w_gate = w->w_gate[l];
+    L.w_up = w->w_up[l];
+    L.w_down = w->w_down[l];
     const void* ps[9] = {L.attn_norm, L.wq, L.wk, L.wv, L.wo, L.mlp_norm, L.w_gate, L.w_up, L.w_down};
     for (const void* p : ps)
       if (!p || !aligned(p, 16)) { delete m; return fail(LADDER_ERR_INVALID, "layer %d: weight NULL or not 16-byte aligned", l); }
@@ -288,15 +298,18 @@ int ladder_create(const ladder_config* cfg, const ladder_weights* w, void* works
     const ladder_config& c = *cfg;
     const uint64_t d = c.d_model, qd = (uint64_t)c.n_q_heads * c.head_dim, kvd = (uint64_t)c.n_kv_heads * c.head_dim;
     const uint64_t f = c.ffn_dim, Mp = plan.m_pad;
-    bool ok = make_tma_map(&m->map_xn, m->ws + plan.xn, Mp, d) && make_tma_map(&m->map_ao, m->ws + plan.ao, Mp, qd) &&
-              make_tma_map(&m->map_act, m->ws + plan.act, Mp, f);
+    const int wdt = c.weight_dtype;
+    bool ok = make_tma_map(&m->map_xn, m->ws + plan.xn, Mp, d, wdt) &&
+              make_tma_map(&m->map_ao, m->ws + plan.ao, Mp, qd, wdt) &&
+              make_tma_map(&m->map_act, m->ws + plan.act, Mp, f, wdt);
     m->maps.resize(c.n_layers);
     for (int l = 0; ok && l < c.n_layers; ++l) {
       const LayerW& L = m->layers[l];
       LayerMaps& T = m->maps[l];
-      ok = make_tma_map(&T.wq, L.wq, qd, d) && make_tma_map(&T.wk, L.wk, kvd, d) && make_tma_map(&T.wv, L.wv, kvd, d) &&
-           make_tma_map(&T.wo, L.wo, d, qd) && make_tma_map(&T.gate, L.w_gate, f, d) &&
-           make_tma_map(&T.up, L.w_up, f, d) && make_tma_map(&T.down, L.w_down, d, f);
+      ok = make_tma_map(&T.wq, L.wq, qd, d, wdt) && make_tma_map(&T.wk, L.wk, kvd, d, wdt) &&
+           make_tma_map(&T.wv, L.wv, kvd, d, wdt) && make_tma_map(&T.wo, L.wo, d, qd, wdt) &&
+           make_tma_map(&T.gate, L.w_gate, f, d, wdt) && make_tma_map(&T.up, L.w_up, f, d, wdt) &&
+           make_tma_map(&T.down, L.w_down, d, f, wdt);
     }
     if (!ok) {
       delete m;
@@ -308,12 +321,16 @@ int ladder_create(const ladder_config* cfg, const ladder_weights* w, void* works
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess) e = gemv_configure();
   if (e == cudaSuccess) e = gemm_tc_configure();
+  if (e == cudaSuccess) e = attn_prefill_configure();
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&m->aux, cudaStreamNonBlocking);
+  for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&m->ev_slot[i], cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_fork, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaMemsetAsync(m->err(), 0, 256, stream);
   if (e == cudaSuccess)
     e = launch_rope_tables(m->at<float>(plan.rope_cos), m->at<float>(plan.rope_sin), cfg->max_seq, cfg->head_dim,
                            cfg->rope_theta, stream);
   if (e != cudaSuccess) {
-    delete m;
+    ladder_destroy(m);
     return fail(LADDER_ERR_CUDA, "ladder_create: %s", cudaGetErrorString(e));
   }
   *out = m;
@@ -324,6 +341,10 @@ void ladder_destroy(ladder_model* m) {
   if (!m) return;
   m->drop_graphs();
   m->drop_probe();
+  for (auto& e : m->ev_slot)
+    if (e) cudaEventDestroy(e);
+  if (m->ev_fork) cudaEventDestroy(m->ev_fork);
+  if (m->aux) cudaStreamDestroy(m->aux);
   delete m;
 }
 
@@ -482,7 +503,19 @@ namespace {
 
 int gemv_launches(int B) { return (B + 3) / 4; }
 
-// One decode step for sequences 0..B-1 (everything on `s`).
+// One decode step for sequences 0..B-1.
+//
+// Schedule.  In a ladder layer the attention module k reads x_{k-2} and the MLP
+// module k+1 reads x_{k-1}, so neither module's weight streaming waits for the
+// module just before it; only their residual adds (x_k = x_{k-1} + h_k) join
+// the two.  The attention chain runs on the caller's stream and the MLP chain of
+// ladder layers on a second stream; each stream buffer has an event recorded by
+// its writer, and a kernel that reads a buffer written on the other stream waits
+// on that event.  Standard layers (and the STANDARD residual mode) keep every
+// kernel on the caller's stream.  The three buffers hold x_k in buffer k mod 3;
+// the write-after-read order on a reused buffer follows from these read
+// dependencies (the module that overwrites x_{k-3} has already waited for a
+// buffer written after every reader of x_{k-3}).
 int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B, float* logits,
                    int32_t* next_tok, int nsplit, cudaStream_t s) {
   const ladder_config& c = m->cfg;
@@ -491,22 +524,47 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
   float* q = m->at<float>(P.q);
   float* ao = m->at<float>(P.ao);
   float* act = m->at<float>(P.act);
+  const int nstd = m->residual_mode == LADDER_RESIDUAL_STANDARD ? c.n_layers : c.n_standard_layers;
+  cudaStream_t streams[2] = {s, m->aux};
+  int writer[3] = {0, 0, 0};  // stream index that last wrote each buffer
+  bool forked = false;
+  auto use = [&](int buf, int si) -> int {  // make stream si wait for the writer of x buffer `buf`
+    const int b3 = buf % 3;
+    if (writer[b3] == si) return LADDER_OK;
+    if (si == 1 && !forked) {
+      CUDA_TRY(cudaEventRecord(m->ev_fork, s));
+      CUDA_TRY(cudaStreamWaitEvent(m->aux, m->ev_fork, 0));
+      forked = true;
+    }
+    CUDA_TRY(cudaStreamWaitEvent(streams[si], m->ev_slot[b3], 0));
+    return LADDER_OK;
+  };
+  auto wrote = [&](int buf, int si) -> int {
+    writer[buf % 3] = si;
+    CUDA_TRY(cudaEventRecord(m->ev_slot[buf % 3], streams[si]));
+    return LADDER_OK;
+  };
+  int rc;
 
-  LAUNCH(launch_embed(tokens, B, m->embed, d, c.vocab, m->X(0), m->err(), s), 1);
+  LAUNCH(launch_embed(tokens, B, m->embed, m->wdt, d, c.vocab, m->X(0), m->err(), s), 1);
+  if ((rc = wrote(0, 0))) return rc;
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerW& L = m->layers[l];
     const KvLayer kvl = kv->layer(l);
-    // attention module k = 2l + 1
+    const int mlp_stream = l < nstd ? 0 : 1;
+    // attention module k = 2l + 1 (caller's stream)
     {
       const int k = 2 * l + 1;
+      const int j = m->input_index(k);
+      if ((rc = use(j, 0))) return rc;
       GemvParams g{};
-      g.x = m->X(m->input_index(k)); g.ldx = d; g.g = L.attn_norm; g.eps = c.norm_eps; g.B = B; g.K = d;
+      g.x = m->X(j); g.ldx = d; g.g = L.attn_norm; g.eps = c.norm_eps; g.B = B; g.K = d;
       g.w0 = L.wq; g.w1 = L.wk; g.w2 = L.wv; g.n_tasks = (qd + 2 * kvd) / 2;
       g.out = q; g.ldo = qd; g.nq_hd = qd; g.nkv_hd = kvd;
       g.rope_cos = m->at<float>(P.rope_cos); g.rope_sin = m->at<float>(P.rope_sin);
       g.pos = kv->seq_lens; g.kv = kvl;
       cudaEvent_t pe = m->probe_start(LADDER_PROBE_QKV, s);
-      LAUNCH(launch_gemv(g, GEMV_QKV, m->num_sms, s), gemv_launches(B));
+      LAUNCH(launch_gemv(g, GEMV_QKV, m->wdt, m->num_sms, s), gemv_launches(B));
       m->probe_stop(pe, s);
 
       AttnDecodeParams a{};
@@ -517,36 +575,44 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       LAUNCH(launch_attn_decode(a, B, c.n_kv_heads, c.head_dim, s), 2);
       m->probe_stop(pe, s);
 
+      if ((rc = use(k - 1, 0))) return rc;
       GemvParams o{};
       o.x = ao; o.ldx = qd; o.g = nullptr; o.B = B; o.K = qd; o.w0 = L.wo; o.n_tasks = d / 2;
       o.out = m->X(k); o.ldo = d; o.x_res = m->X(k - 1); o.ldr = d;
       pe = m->probe_start(LADDER_PROBE_OUT, s);
-      LAUNCH(launch_gemv(o, GEMV_RESID, m->num_sms, s), gemv_launches(B));
+      LAUNCH(launch_gemv(o, GEMV_RESID, m->wdt, m->num_sms, s), gemv_launches(B));
       m->probe_stop(pe, s);
+      if ((rc = wrote(k, 0))) return rc;
     }
-    // MLP module k = 2l + 2
+    // MLP module k = 2l + 2 (second stream in ladder layers)
     {
       const int k = 2 * l + 2;
+      const int j = m->input_index(k);
+      cudaStream_t ms = streams[mlp_stream];
+      if ((rc = use(j, mlp_stream))) return rc;
       GemvParams g{};
-      g.x = m->X(m->input_index(k)); g.ldx = d; g.g = L.mlp_norm; g.eps = c.norm_eps; g.B = B; g.K = d;
+      g.x = m->X(j); g.ldx = d; g.g = L.mlp_norm; g.eps = c.norm_eps; g.B = B; g.K = d;
       g.w0 = L.w_gate; g.w1 = L.w_up; g.n_tasks = f; g.out = act; g.ldo = f;
-      cudaEvent_t pe = m->probe_start(LADDER_PROBE_GATEUP, s);
-      LAUNCH(launch_gemv(g, GEMV_GATEUP, m->num_sms, s), gemv_launches(B));
-      m->probe_stop(pe, s);
+      cudaEvent_t pe = m->probe_start(LADDER_PROBE_GATEUP, ms);
+      LAUNCH(launch_gemv(g, GEMV_GATEUP, m->wdt, m->num_sms, ms), gemv_launches(B));
+      m->probe_stop(pe, ms);
 
+      if ((rc = use(k - 1, mlp_stream))) return rc;
       GemvParams o{};
       o.x = act; o.ldx = f; o.g = nullptr; o.B = B; o.K = f; o.w0 = L.w_down; o.n_tasks = d / 2;
       o.out = m->X(k); o.ldo = d; o.x_res = m->X(k - 1); o.ldr = d;
-      pe = m->probe_start(LADDER_PROBE_DOWN, s);
-      LAUNCH(launch_gemv(o, GEMV_RESID, m->num_sms, s), gemv_launches(B));
-      m->probe_stop(pe, s);
+      pe = m->probe_start(LADDER_PROBE_DOWN, ms);
+      LAUNCH(launch_gemv(o, GEMV_RESID, m->wdt, m->num_sms, ms), gemv_launches(B));
+      m->probe_stop(pe, ms);
+      if ((rc = wrote(k, mlp_stream))) return rc;
     }
   }
+  if ((rc = use(2 * c.n_layers, 0))) return rc;
   GemvParams h{};
   h.x = m->X(2 * c.n_layers); h.ldx = d; h.g = m->final_norm; h.eps = c.norm_eps; h.B = B; h.K = d;
   h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.out = logits; h.ldo = c.vocab;
   cudaEvent_t pe = m->probe_start(LADDER_PROBE_LMHEAD, s);
-  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->num_sms, s), gemv_launches(B));
+  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s), gemv_launches(B));
   m->probe_stop(pe, s);
   if (next_tok)
     LAUNCH(launch_argmax(logits, B, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i), kArgmaxBlocks, next_tok, s), 2);
@@ -623,21 +689,24 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
   const Plan& P = m->plan;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  // Row metadata: row_b[M_max], row_pos[M_max], lens[Bm], last_row[Bm].
+  // Row metadata: row_b[M_max], row_pos[M_max], lens[Bm], last_row[Bm], start[Bm].
   std::vector<int32_t>& meta = m->meta_host;
-  meta.assign(2 * (size_t)P.m_max + 2 * Bm, 0);
+  meta.assign(2 * (size_t)P.m_max + 3 * Bm, 0);
   int32_t* row_b = meta.data();
   int32_t* row_pos = row_b + P.m_max;
   int32_t* lens = row_pos + P.m_max;
   int32_t* last = lens + Bm;
-  int mm = 0;
+  int32_t* start = last + Bm;
+  int mm = 0, max_len = 0;
   for (int b = 0; b < B; ++b) {
+    start[b] = mm;
     for (int t = 0; t < host_lens[b]; ++t, ++mm) {
       row_b[mm] = b;
       row_pos[mm] = t;
     }
     lens[b] = host_lens[b];
     last[b] = mm - 1;
+    if (host_lens[b] > max_len) max_len = host_lens[b];
   }
   m->launches = 0;
   int32_t* dmeta = m->at<int32_t>(P.meta);
@@ -646,47 +715,48 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
   const int32_t* d_row_pos = dmeta + P.m_max;
   const int32_t* d_lens = d_row_pos + P.m_max;
   const int32_t* d_last = d_lens + Bm;
+  const int32_t* d_start = d_last + Bm;
 
   const int d = c.d_model, qd = c.n_q_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim, f = c.ffn_dim;
-  bf16* xn = m->at<bf16>(P.xn);
-  bf16* qb = m->at<bf16>(P.q);
-  bf16* aob = m->at<bf16>(P.ao);
-  bf16* actb = m->at<bf16>(P.act);
+  const int wdt = m->wdt;
+  void* xn = m->ws + P.xn;    // normalised rows, weight dtype
+  void* qb = m->ws + P.q;     // rotated queries, bf16
+  void* aob = m->ws + P.ao;   // attention output, weight dtype
+  void* actb = m->ws + P.act; // SwiGLU output, weight dtype
 
-  LAUNCH(launch_embed(tokens, M, m->embed, d, c.vocab, m->X(0), m->err(), s), 1);
+  LAUNCH(launch_embed(tokens, M, m->embed, wdt, d, c.vocab, m->X(0), m->err(), s), 1);
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerW& L = m->layers[l];
+    const LayerMaps& T = m->maps[l];
     const KvLayer kvl = kv->layer(l);
     {
       const int k = 2 * l + 1;
-      LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.attn_norm, c.norm_eps, xn, s), 1);
+      LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.attn_norm, c.norm_eps, xn, wdt, s), 1);
       GemmParams g{};
-      g.A = xn; g.w0 = L.wq; g.w1 = L.wk; g.w2 = L.wv; g.M = M; g.N = qd + 2 * kvd; g.K = d;
-      g.out_bf = qb; g.ldo = qd; g.nq_hd = qd; g.nkv_hd = kvd;
+      g.M = M; g.N = qd + 2 * kvd; g.K = d;
+      g.out_h = qb; g.ldo = qd; g.nq_hd = qd; g.nkv_hd = kvd;
       g.rope_cos = m->at<float>(P.rope_cos); g.rope_sin = m->at<float>(P.rope_sin);
       g.row_b = d_row_b; g.row_pos = d_row_pos; g.kv = kvl;
-      const LayerMaps& T = m->maps[l];
-      LAUNCH(launch_gemm_tc(&m->map_xn, &T.wq, &T.wk, &T.wv, g, GEMM_QKV, m->err(), s), 1);
+      LAUNCH(launch_gemm_tc(&m->map_xn, &T.wq, &T.wk, &T.wv, g, GEMM_QKV, wdt, m->err(), s), 1);
 
       AttnPrefillParams a{};
-      a.q = qb; a.kv = kvl; a.row_b = d_row_b; a.row_pos = d_row_pos; a.M = M; a.n_q = c.n_q_heads;
-      a.scale = 1.0f / sqrtf((float)c.head_dim); a.out = aob;
-      LAUNCH(launch_attn_prefill(a, c.head_dim, s), 1);
+      a.q = static_cast<const bf16*>(qb); a.kv = kvl; a.seq_start = d_start; a.seq_len = d_lens;
+      a.n_q = c.n_q_heads; a.scale = 1.0f / sqrtf((float)c.head_dim); a.out = aob;
+      LAUNCH(launch_attn_prefill_tc(a, c.head_dim, wdt, B, max_len, s), 1);
 
       GemmParams o{};
-      o.A = aob; o.w0 = L.wo; o.M = M; o.N = d; o.K = qd; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);
-      LAUNCH(launch_gemm_tc(&m->map_ao, &T.wo, nullptr, nullptr, o, GEMM_RESID, m->err(), s), 1);
+      o.M = M; o.N = d; o.K = qd; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);
+      LAUNCH(launch_gemm_tc(&m->map_ao, &T.wo, nullptr, nullptr, o, GEMM_RESID, wdt, m->err(), s), 1);
     }
     {
       const int k = 2 * l + 2;
-      LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.mlp_norm, c.norm_eps, xn, s), 1);
+      LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.mlp_norm, c.norm_eps, xn, wdt, s), 1);
       GemmParams g{};
-      g.A = xn; g.w0 = L.w_gate; g.w1 = L.w_up; g.M = M; g.N = f; g.K = d; g.out_bf = actb; g.ldo = f;
-      const LayerMaps& T = m->maps[l];
-      LAUNCH(launch_gemm_tc(&m->map_xn, &T.gate, &T.up, nullptr, g, GEMM_GATEUP, m->err(), s), 1);
+      g.M = M; g.N = f; g.K = d; g.out_h = actb; g.ldo = f;
+      LAUNCH(launch_gemm_tc(&m->map_xn, &T.gate, &T.up, nullptr, g, GEMM_GATEUP, wdt, m->err(), s), 1);
       GemmParams o{};
-      o.A = actb; o.w0 = L.w_down; o.M = M; o.N = d; o.K = f; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);
-      LAUNCH(launch_gemm_tc(&m->map_act, &T.down, nullptr, nullptr, o, GEMM_RESID, m->err(), s), 1);
+      o.M = M; o.N = d; o.K = f; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);
+      LAUNCH(launch_gemm_tc(&m->map_act, &T.down, nullptr, nullptr, o, GEMM_RESID, wdt, m->err(), s), 1);
     }
   }
   float* xlast = m->at<float>(P.xlast);
@@ -694,7 +764,7 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
   GemvParams h{};
   h.x = xlast; h.ldx = d; h.g = m->final_norm; h.eps = c.norm_eps; h.B = B; h.K = d;
   h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.out = logits; h.ldo = c.vocab;
-  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->num_sms, s), gemv_launches(B));
+  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s), gemv_launches(B));
   if (next_tok)
     LAUNCH(launch_argmax(logits, B, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i), kArgmaxBlocks, next_tok, s), 2);
   LAUNCH(launch_set_lens(d_lens, B, kv->seq_lens, s), 1);

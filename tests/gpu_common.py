@@ -32,8 +32,8 @@ def oracle_weights(dims, transform=None, keep_layers=True):
     return O.synthetic_weights(dims, transform=transform, keep_layers=keep_layers)
 
 
-def gpu_weights(dims, transform=None):
-    return ladder.synthetic_weights(dims, device="cuda", transform=transform)
+def gpu_weights(dims, transform=None, dtype="fp16"):
+    return ladder.synthetic_weights(dims, device="cuda", transform=transform, dtype=dtype)
 
 
 def make_model(dims, weights=None, **kw):

@@ -71,6 +71,20 @@ def test_tiny_greedy_tokens_and_logits(tiny):
             break
 
 
+def test_bf16_weights_and_operands():
+    """The bf16 storage variant of every kernel against the oracle."""
+    dims = small_dims()
+    ow = oracle_weights(dims)
+    lens = [16, 70]
+    prompts = prompts_for(lens, dims["vocab"])
+    feed = np.stack([synth.tokens(3, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(2)])
+    model = make_model(dims, gpu_weights(dims, dtype="bf16"), max_batch=2, max_seq=96, page_size=32)
+    g_logits, g_toks = run_teacher_forced(model, prompts, feed, graph=True)
+    o_logits, _ = O.teacher_forced_decode(dims, ow, prompts, feed)
+    for s_ in range(4):
+        compare_logits(g_logits[s_], o_logits[s_], f"bf16 step {s_}")
+
+
 def test_kv_cache_layout_is_bit_exact(tiny):
     dims, gw, ow = tiny
     page = 16
