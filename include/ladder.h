@@ -219,6 +219,27 @@ int ladder_probe_begin(ladder_model* m, int kernel_class, int32_t max_launches);
  * were timed and the sum of their durations in milliseconds. */
 int ladder_probe_end(ladder_model* m, int32_t* launches, float* total_ms);
 
+/* Decode attention as a standalone operation: the split-context paged GQA
+ * attention that ladder_decode_step runs in every layer.  For each sequence b
+ * the query q[b] (device fp32 [B][n_q_heads*head_dim], already rotated) sits
+ * at position positions[b] (device int32 [B]) and attends causally over the
+ * cached positions 0 .. positions[b] of `kv_layer`, one layer of the pool:
+ * bf16 [num_pages][2][n_kv_heads][page_size][head_dim] addressed through
+ * block_table (device int32 [B][max_pages_per_seq]).  Query head h reads KV
+ * head h / (n_q_heads / n_kv_heads); scores are scaled by `scale`.  Writes
+ * out (device fp32 [B][n_q_heads*head_dim]).  `scratch` is a caller-owned
+ * device buffer of at least ladder_attention_decode_scratch_bytes(...) bytes,
+ * 16-byte aligned, for the per-split partial results; every positions[b]
+ * must be <= max_position (host int).  Same shape rules as the model
+ * (head_dim 64 or 128, at most 8 query heads per KV head, page_size 16, 32
+ * or 64). */
+size_t ladder_attention_decode_scratch_bytes(int32_t B, int32_t n_q_heads, int32_t head_dim, int32_t max_position);
+int ladder_attention_decode(const float* q, const void* kv_layer, const int32_t* block_table,
+                            int32_t max_pages_per_seq, const int32_t* positions, int32_t B, int32_t n_q_heads,
+                            int32_t n_kv_heads, int32_t head_dim, int32_t page_size, float scale,
+                            int32_t max_position, float* out, void* scratch, size_t scratch_bytes,
+                            ladder_stream_t stream);
+
 /* Thread-local message describing the last failed call on this thread. */
 const char* ladder_last_error(void);
 

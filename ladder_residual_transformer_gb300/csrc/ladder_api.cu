@@ -771,3 +771,69 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
   for (int b = 0; b < B; ++b) kv->host_lens[b] = host_lens[b];
   return LADDER_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Standalone decode attention
+// ---------------------------------------------------------------------------
+namespace {
+
+int check_attention_shape(int32_t B, int32_t n_q, int32_t n_kv, int32_t hd, int32_t page_size, int32_t max_position) {
+  if (B <= 0) return fail(LADDER_ERR_INVALID, "B=%d must be positive", B);
+  if (hd != 64 && hd != 128) return fail(LADDER_ERR_UNSUPPORTED, "head_dim=%d: only 64 and 128 are supported", hd);
+  if (n_q <= 0 || n_kv <= 0 || n_q % n_kv) return fail(LADDER_ERR_INVALID, "n_q_heads must be a multiple of n_kv_heads");
+  if (n_q / n_kv > 8) return fail(LADDER_ERR_UNSUPPORTED, "more than 8 query heads per KV head");
+  if (page_size != 16 && page_size != 32 && page_size != 64)
+    return fail(LADDER_ERR_INVALID, "page_size=%d must be 16, 32 or 64", page_size);
+  if (max_position < 0) return fail(LADDER_ERR_INVALID, "max_position must be >= 0");
+  return LADDER_OK;
+}
+
+size_t attention_scratch(int32_t B, int32_t n_q, int32_t hd, int32_t max_position) {
+  const size_t nsplit = ((size_t)max_position + 1 + kSplitLen - 1) / kSplitLen;
+  const size_t po = align_up((size_t)B * n_q * nsplit * hd * 4, 256);
+  return po + (size_t)B * n_q * nsplit * 2 * 4;
+}
+
+}  // namespace
+
+extern "C" size_t ladder_attention_decode_scratch_bytes(int32_t B, int32_t n_q_heads, int32_t head_dim,
+                                                        int32_t max_position) {
+  if (B <= 0 || n_q_heads <= 0 || head_dim <= 0 || max_position < 0) return 0;
+  return attention_scratch(B, n_q_heads, head_dim, max_position);
+}
+
+extern "C" int ladder_attention_decode(const float* q, const void* kv_layer, const int32_t* block_table,
+                                       int32_t max_pages_per_seq, const int32_t* positions, int32_t B,
+                                       int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t page_size,
+                                       float scale, int32_t max_position, float* out, void* scratch,
+                                       size_t scratch_bytes, ladder_stream_t stream) {
+  if (!q || !kv_layer || !block_table || !positions || !out || !scratch) return fail(LADDER_ERR_INVALID, "NULL argument");
+  int rc = check_attention_shape(B, n_q_heads, n_kv_heads, head_dim, page_size, max_position);
+  if (rc) return rc;
+  if (max_pages_per_seq <= 0 || (int64_t)max_pages_per_seq * page_size < (int64_t)max_position + 1)
+    return fail(LADDER_ERR_CAPACITY, "max_pages_per_seq * page_size must cover max_position + 1");
+  if (!aligned(q, 16) || !aligned(kv_layer, 16) || !aligned(out, 16) || !aligned(scratch, 16))
+    return fail(LADDER_ERR_INVALID, "q, kv_layer, out and scratch must be 16-byte aligned");
+  const size_t need = attention_scratch(B, n_q_heads, head_dim, max_position);
+  if (scratch_bytes < need) return fail(LADDER_ERR_CAPACITY, "scratch too small: %zu < %zu bytes", scratch_bytes, need);
+  AttnDecodeParams a{};
+  a.q = q;
+  a.kv.base = static_cast<bf16*>(const_cast<void*>(kv_layer));
+  a.kv.block_table = block_table;
+  a.kv.max_pages = max_pages_per_seq;
+  a.kv.page_size = page_size;
+  a.kv.n_kv = n_kv_heads;
+  a.kv.head_dim = head_dim;
+  a.seq_lens = positions;
+  a.n_q = n_q_heads;
+  a.split_len = kSplitLen;
+  a.nsplit = (max_position + 1 + kSplitLen - 1) / kSplitLen;
+  a.scale = scale;
+  a.part_o = static_cast<float*>(scratch);
+  a.part_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) +
+                                       align_up((size_t)B * n_q_heads * a.nsplit * head_dim * 4, 256));
+  a.out = out;
+  cudaError_t e = launch_attn_decode(a, B, n_kv_heads, head_dim, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(LADDER_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
+  return LADDER_OK;
+}

@@ -64,6 +64,9 @@ _SIGNATURES = {
     "ladder_last_launch_count": (_i32, [_vp]),
     "ladder_probe_begin": (_i32, [_vp, ctypes.c_int, _i32]),
     "ladder_probe_end": (_i32, [_vp, _pi32, ctypes.POINTER(_f32)]),
+    "ladder_attention_decode_scratch_bytes": (_sz, [_i32, _i32, _i32, _i32]),
+    "ladder_attention_decode": (_i32, [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp, _vp,
+                                       _sz, _vp]),
     "ladder_last_error": (ctypes.c_char_p, []),
 }
 
@@ -166,6 +169,26 @@ def synthetic_weights(dims: dict, device="cuda", seed: int = 0, transform=None, 
            "dtype": dtype}
     for l in range(dims["n_layers"]):
         out["layers"].append({k: upload(k, l) for k in synth.LAYER_KINDS})
+    return out
+
+
+def attention_decode(q: torch.Tensor, kv_layer: torch.Tensor, block_table: torch.Tensor, positions: torch.Tensor,
+                     n_kv_heads: int, head_dim: int, page_size: int, max_position: int, scale: float | None = None,
+                     out: torch.Tensor | None = None, scratch: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Standalone decode attention through the C ABI (see ladder_attention_decode)."""
+    B = positions.numel()
+    n_q = q.shape[-1] // head_dim
+    if scale is None:
+        scale = head_dim ** -0.5
+    if out is None:
+        out = torch.empty(B, n_q * head_dim, dtype=torch.float32, device=q.device)
+    need = lib().ladder_attention_decode_scratch_bytes(B, n_q, head_dim, max_position)
+    if scratch is None:
+        scratch = torch.empty(need, dtype=torch.uint8, device=q.device)
+    check(lib().ladder_attention_decode(q.data_ptr(), kv_layer.data_ptr(), block_table.data_ptr(),
+                                        block_table.shape[-1], positions.data_ptr(), B, n_q, n_kv_heads, head_dim,
+                                        page_size, scale, max_position, out.data_ptr(), scratch.data_ptr(),
+                                        scratch.numel() * scratch.element_size(), _stream_handle(stream)))
     return out
 
 
