@@ -240,6 +240,27 @@ int ladder_attention_decode(const float* q, const void* kv_layer, const int32_t*
                             int32_t max_position, float* out, void* scratch, size_t scratch_bytes,
                             ladder_stream_t stream);
 
+/* Decode attention that allocates nothing.  No counterpart on the pages: this
+ * is a library convenience.  Same arguments and result as
+ * ladder_attention_decode, minus the scratch buffer, for callers that cannot
+ * allocate device memory (code running while a CUDA graph is being captured,
+ * plugins whose host framework owns all device memory, loops that must not
+ * stall on an allocation).  The partials live in a file-scope device array of
+ * LADDER_STATIC_SCRATCH_BYTES bytes that every GPU running this code keeps
+ * until the process exits.  Calls whose partials need more than that fail with
+ * LADDER_ERR_CAPACITY (need = 256-byte-aligned B*n_q_heads*nsplit*head_dim*4
+ * plus B*n_q_heads*nsplit*8, nsplit = ceil((max_position+1)/128)).  The first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture.
+ * All calls share the one array: calls that can overlap on the GPU (on
+ * different streams, or from different threads) race on it and must be
+ * serialised by the caller. */
+#define LADDER_STATIC_SCRATCH_BYTES (8u << 20)
+int ladder_attention_decode_noalloc(const float* q, const void* kv_layer, const int32_t* block_table,
+                                    int32_t max_pages_per_seq, const int32_t* positions, int32_t B,
+                                    int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t page_size,
+                                    float scale, int32_t max_position, float* out, ladder_stream_t stream);
+
 /* Thread-local message describing the last failed call on this thread. */
 const char* ladder_last_error(void);
 

@@ -31,6 +31,11 @@ static int fail(int code, const char* fmt, ...) {
   return code;
 }
 
+namespace ladder {
+// Records `msg` as the last error of this thread and returns `code` (used by other translation units).
+int set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace ladder
+
 #define CUDA_TRY(expr)                                                                          \
   do {                                                                                          \
     cudaError_t e_ = (expr);                                                                    \

@@ -67,8 +67,12 @@ _SIGNATURES = {
     "ladder_attention_decode_scratch_bytes": (_sz, [_i32, _i32, _i32, _i32]),
     "ladder_attention_decode": (_i32, [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp, _vp,
                                        _sz, _vp]),
+    "ladder_attention_decode_noalloc": (_i32, [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _i32,
+                                               _vp, _vp]),
     "ladder_last_error": (ctypes.c_char_p, []),
 }
+
+STATIC_SCRATCH_BYTES = 8 << 20  # LADDER_STATIC_SCRATCH_BYTES
 
 PROBE_CLASSES = {"qkv": 0, "attn": 1, "out": 2, "gateup": 3, "down": 4, "lmhead": 5}
 
@@ -189,6 +193,22 @@ def attention_decode(q: torch.Tensor, kv_layer: torch.Tensor, block_table: torch
                                         block_table.shape[-1], positions.data_ptr(), B, n_q, n_kv_heads, head_dim,
                                         page_size, scale, max_position, out.data_ptr(), scratch.data_ptr(),
                                         scratch.numel() * scratch.element_size(), _stream_handle(stream)))
+    return out
+
+
+def attention_decode_noalloc(q: torch.Tensor, kv_layer: torch.Tensor, block_table: torch.Tensor,
+                             positions: torch.Tensor, n_kv_heads: int, head_dim: int, page_size: int,
+                             max_position: int, out: torch.Tensor, scale: float | None = None, stream=None):
+    """Decode attention through the entry point that allocates nothing
+    (ladder_attention_decode_noalloc): its scratch is a static device array."""
+    B = positions.numel()
+    n_q = q.shape[-1] // head_dim
+    if scale is None:
+        scale = head_dim ** -0.5
+    check(lib().ladder_attention_decode_noalloc(q.data_ptr(), kv_layer.data_ptr(), block_table.data_ptr(),
+                                                block_table.shape[-1], positions.data_ptr(), B, n_q, n_kv_heads,
+                                                head_dim, page_size, scale, max_position, out.data_ptr(),
+                                                _stream_handle(stream)))
     return out
 
 
