@@ -125,12 +125,18 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
     __syncthreads();
   }
 
-  const int total_warps = gridDim.x * GEMV_WARPS;
-  const int rounds = (p.n_tasks + total_warps - 1) / total_warps;
+  // Warp w works on task slot w / ks of this CTA and on K slice w % ks.
+  const int ks = p.ks;
+  const int tpc = GEMV_WARPS / ks;  // tasks per CTA per round
+  const int slot = warp / ks, kslice = warp % ks;
+  const int total_slots = gridDim.x * tpc;
+  const int rounds = (p.n_tasks + total_slots - 1) / total_slots;
   const bool single_chunk = p.kc >= K;
+  const int kspan = K / ks;  // single chunk when ks > 1
+  __shared__ float s_part[GEMV_WARPS][2][BT];
 
   for (int r = 0; r < rounds; ++r) {
-    const int task = r * total_warps + blockIdx.x * GEMV_WARPS + warp;
+    const int task = r * total_slots + blockIdx.x * tpc + slot;
     const bool active = task < p.n_tasks;
 
     // Which two weight rows this task reads.
@@ -189,8 +195,10 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
       if (active) {
         const WT* p0 = row0 + k0;
         const WT* p1 = row1 + k0;
-        int k = lane * 8;
-        for (; k + 768 < kc; k += 1024) {
+        const int kb = ks > 1 ? kslice * kspan : 0;
+        const int ke = ks > 1 ? kb + kspan : kc;
+        int k = kb + lane * 8;
+        for (; k + 768 < ke; k += 1024) {
           uint4 wa[4], wb[4];
 #pragma unroll
           for (int s = 0; s < 4; ++s) {
@@ -203,7 +211,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
             gemv_fma<WT, BT>(wb[s], u, kc, k + 256 * s, a1);
           }
         }
-        for (; k < kc; k += 256) {
+        for (; k < ke; k += 256) {
           const uint4 wa = ld_stream_u4(p0 + k);
           const uint4 wb = ld_stream_u4(p1 + k);
           gemv_fma<WT, BT>(wa, u, kc, k, a0);
@@ -216,6 +224,31 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
     for (int b = 0; b < BT; ++b) {
       a0[b] = warp_sum(a0[b]);
       a1[b] = warp_sum(a1[b]);
+    }
+    if (ks > 1) {
+      // combine the K slices of each task in a fixed order
+      if (lane == 0) {
+#pragma unroll
+        for (int b = 0; b < BT; ++b) {
+          s_part[warp][0][b] = a0[b];
+          s_part[warp][1][b] = a1[b];
+        }
+      }
+      __syncthreads();
+      if (kslice == 0) {
+#pragma unroll
+        for (int b = 0; b < BT; ++b) {
+          float t0 = 0.f, t1 = 0.f;
+          for (int i = 0; i < ks; ++i) {
+            t0 += s_part[warp + i][0][b];
+            t1 += s_part[warp + i][1][b];
+          }
+          a0[b] = t0;
+          a1[b] = t1;
+        }
+      }
+      __syncthreads();
+      if (kslice != 0) continue;
     }
     if (!active) continue;
 
@@ -317,8 +350,17 @@ cudaError_t launch_gemv(const GemvParams& p0, int mode, int wdt, int num_sms, cu
     const int bt = p.B <= 1 ? 1 : (p.B <= 2 ? 2 : 4);
     p.kc = gemv_chunk(p.B, p.K);
     const size_t smem = (size_t)bt * p.kc * sizeof(float);
-    int grid = (p.n_tasks + GEMV_WARPS - 1) / GEMV_WARPS;
-    const int cap = num_sms * 4;
+    // K split: the smallest that gives at least 1.5 CTAs per SM (more warps in
+    // flight for short, wide matrices) while each slice stays a multiple of 256.
+    p.ks = 1;
+    if (p.kc >= p.K) {
+      while (p.ks < GEMV_WARPS && (long long)p.n_tasks * p.ks < (long long)num_sms * 12 &&
+             (p.K / (2 * p.ks)) % 256 == 0)
+        p.ks *= 2;
+    }
+    const int tpc = GEMV_WARPS / p.ks;
+    int grid = (p.n_tasks + tpc - 1) / tpc;
+    const int cap = num_sms * 8;
     if (grid > cap) grid = cap;
     if (wdt == WDT_F16) gemv_dispatch_bt<f16>(p, bt, mode, grid, smem, s);
     else gemv_dispatch_bt<bf16>(p, bt, mode, grid, smem, s);
@@ -331,16 +373,35 @@ cudaError_t launch_gemv(const GemvParams& p0, int mode, int wdt, int num_sms, cu
 // ---------------------------------------------------------------------------
 // Decode attention over the paged cache, split along the context.
 // CTA (split, kv head, sequence): the G = n_q / n_kv query heads of the group
-// against keys [split * split_len, ...) of the sequence.  Thread t scores key t
-// for all G heads; each warp then normalises heads w, w+4 with warp-shuffle
-// max/sum reductions; finally thread (d, parity) accumulates P V for dim d.
-// Partial (max, sum, o) per split are merged by attn_combine_kernel.
+// against keys [split * split_len, ...) of the sequence.  The CTA first issues
+// every K and V load of its split at once (16-byte cp.async, coalesced along
+// each page's contiguous [page_size][head_dim] slab) into padded shared memory,
+// so the whole split is a single memory round trip.  Thread t then scores key t
+// for all G heads; each warp normalises heads w, w+4 with warp-shuffle max/sum
+// reductions; threads (dim pair, key group) accumulate P V.  Partial (max, sum,
+// o) per split are merged by attn_combine_kernel.
 // ---------------------------------------------------------------------------
 constexpr int ATT_THREADS = 128;
 constexpr int ATT_MAXG = 8;
+constexpr int ATT_SPLIT = 128;  // keys per split (= ATT_THREADS)
+
+__device__ __forceinline__ void att_cp16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
 
 template <int HD>
 __global__ void __launch_bounds__(ATT_THREADS) attn_decode_kernel(const AttnDecodeParams p) {
+  constexpr int LD = HD + 8;                 // padded bf16 row: conflict-free 16-byte reads
+  constexpr int KG = ATT_THREADS / (HD / 2);  // key groups in the P V phase
+  extern __shared__ uint4 att_dyn[];
+  bf16* sK = reinterpret_cast<bf16*>(att_dyn);  // [ATT_SPLIT][LD]
+  bf16* sV = sK + ATT_SPLIT * LD;              // [ATT_SPLIT][LD]
+  __shared__ __align__(16) float q_s[ATT_MAXG][HD];
+  __shared__ float p_s[ATT_MAXG][ATT_SPLIT];
+  __shared__ float m_s[ATT_MAXG], l_s[ATT_MAXG];
+  __shared__ float2 o_red[KG > 1 ? KG - 1 : 1][ATT_MAXG][HD / 2];
+
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int G = p.n_q / p.kv.n_kv;
   const int ctx = p.seq_lens[b] + 1;
@@ -348,23 +409,28 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_decode_kernel(const AttnDeco
   const int s1 = min(ctx, s0 + p.split_len);
   if (s0 >= s1) return;  // the combine step reads only splits below ctx
   const int n = s1 - s0;
-
-  __shared__ float q_s[ATT_MAXG][HD];
-  __shared__ float p_s[ATT_MAXG][ATT_THREADS];
-  __shared__ float m_s[ATT_MAXG], l_s[ATT_MAXG];
-  constexpr int KP = ATT_THREADS / HD;
-  __shared__ float o_red[KP > 1 ? ATT_MAXG : 1][KP > 1 ? HD : 1];
-
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // 1. all K/V loads of the split in flight at once
+  for (int c = tid; c < n * (HD / 8); c += ATT_THREADS) {
+    const int r = c / (HD / 8), d8 = (c % (HD / 8)) * 8;
+    const size_t kofs = p.kv.slot(b, s0 + r, 0, kvh) + d8;
+    const size_t vofs = kofs + (size_t)p.kv.n_kv * p.kv.page_size * HD;  // V slab follows the K slab of the page
+    att_cp16(sK + r * LD + d8, p.kv.base + kofs);
+    att_cp16(sV + r * LD + d8, p.kv.base + vofs);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
   const float* qg = p.q + (size_t)b * p.n_q * HD + (size_t)kvh * G * HD;
   for (int i = tid; i < G * HD; i += ATT_THREADS) q_s[i / HD][i % HD] = qg[i];
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
   __syncthreads();
 
+  // 2. scores: thread t <-> key s0 + t
   float acc[ATT_MAXG];
 #pragma unroll
   for (int h = 0; h < ATT_MAXG; ++h) acc[h] = 0.f;
   if (tid < n) {
-    const bf16* krow = p.kv.base + p.kv.slot(b, s0 + tid, 0, kvh);
+    const bf16* krow = sK + tid * LD;
 #pragma unroll 4
     for (int d = 0; d < HD; d += 8) {
       const uint4 kw = *reinterpret_cast<const uint4*>(krow + d);
@@ -373,9 +439,9 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_decode_kernel(const AttnDeco
 #pragma unroll
       for (int h = 0; h < ATT_MAXG; ++h) {
         if (h < G) {
-          const float* qh = &q_s[h][d];
-          acc[h] += qh[0] * k0 + qh[1] * k1 + qh[2] * k2 + qh[3] * k3 + qh[4] * k4 + qh[5] * k5 +
-                    qh[6] * k6 + qh[7] * k7;
+          const float4 qa = *reinterpret_cast<const float4*>(&q_s[h][d]);
+          const float4 qb = *reinterpret_cast<const float4*>(&q_s[h][d + 4]);
+          acc[h] += qa.x * k0 + qa.y * k1 + qa.z * k2 + qa.w * k3 + qb.x * k4 + qb.y * k5 + qb.z * k6 + qb.w * k7;
         }
       }
     }
@@ -385,6 +451,7 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_decode_kernel(const AttnDeco
     if (h < G) p_s[h][tid] = tid < n ? acc[h] * p.scale : -INFINITY;
   __syncthreads();
 
+  // 3. softmax statistics per head (warp w: heads w, w + 4)
   for (int h = warp; h < G; h += ATT_THREADS / 32) {
     float v[4];
     float m = -INFINITY;
@@ -409,35 +476,47 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_decode_kernel(const AttnDeco
   }
   __syncthreads();
 
-  const int d = tid % HD, kp = tid / HD;
-  float o[ATT_MAXG];
+  // 4. P V: thread (dim pair dp, key group kg) over keys kg, kg + KG, ...
+  const int dp = tid % (HD / 2), kg = tid / (HD / 2);
+  float2 o[ATT_MAXG];
 #pragma unroll
-  for (int h = 0; h < ATT_MAXG; ++h) o[h] = 0.f;
-  for (int t = kp; t < n; t += KP) {
-    const bf16* vrow = p.kv.base + p.kv.slot(b, s0 + t, 1, kvh);
-    const float v = __bfloat162float(vrow[d]);
+  for (int h = 0; h < ATT_MAXG; ++h) o[h] = make_float2(0.f, 0.f);
+  for (int t = kg; t < n; t += KG) {
+    const uint32_t vv = *reinterpret_cast<const uint32_t*>(sV + t * LD + 2 * dp);
+    const float v0 = bf_lo(vv), v1 = bf_hi(vv);
 #pragma unroll
-    for (int h = 0; h < ATT_MAXG; ++h)
-      if (h < G) o[h] += p_s[h][t] * v;
+    for (int h = 0; h < ATT_MAXG; ++h) {
+      if (h < G) {
+        const float pw = p_s[h][t];
+        o[h].x += pw * v0;
+        o[h].y += pw * v1;
+      }
+    }
   }
-  if (KP > 1) {
-    if (kp == 1) {
+  if (KG > 1) {
+    if (kg > 0) {
 #pragma unroll
       for (int h = 0; h < ATT_MAXG; ++h)
-        if (h < G) o_red[h][d] = o[h];
+        if (h < G) o_red[kg - 1][h][dp] = o[h];
     }
     __syncthreads();
-    if (kp != 0) return;
+    if (kg != 0) return;
+    for (int g2 = 0; g2 < KG - 1; ++g2) {
 #pragma unroll
-    for (int h = 0; h < ATT_MAXG; ++h)
-      if (h < G) o[h] += o_red[h][d];
+      for (int h = 0; h < ATT_MAXG; ++h) {
+        if (h < G) {
+          o[h].x += o_red[g2][h][dp].x;
+          o[h].y += o_red[g2][h][dp].y;
+        }
+      }
+    }
   }
 #pragma unroll
   for (int h = 0; h < ATT_MAXG; ++h) {
     if (h >= G) continue;
     const size_t idx = ((size_t)b * p.n_q + (size_t)kvh * G + h) * p.nsplit + split;
-    p.part_o[idx * HD + d] = o[h];
-    if (d == 0) {
+    *reinterpret_cast<float2*>(p.part_o + idx * HD + 2 * dp) = o[h];
+    if (dp == 0) {
       p.part_ml[idx * 2] = m_s[h];
       p.part_ml[idx * 2 + 1] = l_s[h];
     }
@@ -463,13 +542,34 @@ __global__ void __launch_bounds__(HD) attn_combine_kernel(const AttnDecodeParams
   p.out[(size_t)b * p.n_q * HD + (size_t)h * HD + d] = acc / L;
 }
 
+static constexpr size_t att_dyn_smem(int hd) { return (size_t)2 * ATT_SPLIT * (hd + 8) * sizeof(bf16); }
+
+// The K/V tiles need more than the default 48 KB of shared memory for head_dim
+// 128: raise the limit once per device before the first launch there.
+static cudaError_t attn_configure_current_device() {
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && configured[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(attn_decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)att_dyn_smem(64));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)att_dyn_smem(128));
+  if (e == cudaSuccess && dev >= 0 && dev < 64) configured[dev] = 1;
+  return e;
+}
+
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, int B, int n_kv, int hd, cudaStream_t s) {
+  if (p.split_len != ATT_SPLIT) return cudaErrorInvalidValue;
+  cudaError_t e = attn_configure_current_device();
+  if (e != cudaSuccess) return e;
   dim3 grid(p.nsplit, n_kv, B);
   if (hd == 64) {
-    attn_decode_kernel<64><<<grid, ATT_THREADS, 0, s>>>(p);
+    attn_decode_kernel<64><<<grid, ATT_THREADS, att_dyn_smem(64), s>>>(p);
     attn_combine_kernel<64><<<dim3(p.n_q, B), 64, 0, s>>>(p);
   } else {
-    attn_decode_kernel<128><<<grid, ATT_THREADS, 0, s>>>(p);
+    attn_decode_kernel<128><<<grid, ATT_THREADS, att_dyn_smem(128), s>>>(p);
     attn_combine_kernel<128><<<dim3(p.n_q, B), 128, 0, s>>>(p);
   }
   return cudaGetLastError();

@@ -77,13 +77,14 @@ struct KvLayer {
   const int* block_table;  // [max_batch][max_pages]
   int max_pages;
   int page_size;
+  int page_shift;  // log2(page_size)
   int n_kv;
   int head_dim;
   __device__ __forceinline__ size_t page_elems() const { return (size_t)2 * n_kv * page_size * head_dim; }
   // element offset of (position p of sequence b, kv 0/1, head h, dim 0)
   __device__ __forceinline__ size_t slot(int b, int p, int kv, int h) const {
-    int page = block_table[b * max_pages + p / page_size];
-    return (size_t)page * page_elems() + ((size_t)(kv * n_kv + h) * page_size + (p % page_size)) * head_dim;
+    const int page = block_table[b * max_pages + (p >> page_shift)];
+    return (size_t)page * page_elems() + ((size_t)(kv * n_kv + h) * page_size + (p & (page_size - 1))) * head_dim;
   }
 };
 
@@ -100,6 +101,7 @@ struct GemvParams {
   const void* w2;    // QKV: wv
   int n_tasks;       // row pairs (QKV, RESID, LOGITS) or rows (GATEUP)
   int kc;            // K chunk staged in shared memory (multiple of 256)
+  int ks;            // warps that split one task's K range (1, 2, 4, 8; > 1 only with a single chunk)
   float* out;        // QKV: q [B][ldo]; GATEUP: act [B][ldo]; RESID: x_out; LOGITS: logits
   int ldo;
   const float* x_res;  // RESID: residual rows [B][ldr]

@@ -230,6 +230,7 @@ struct ladder_kv {
     v.block_table = block_table;
     v.max_pages = max_pages;
     v.page_size = c.page_size;
+    v.page_shift = __builtin_ctz((unsigned)c.page_size);
     v.n_kv = c.n_kv_heads;
     v.head_dim = c.head_dim;
     return v;
@@ -827,6 +828,7 @@ extern "C" int ladder_attention_decode(const float* q, const void* kv_layer, con
   a.kv.block_table = block_table;
   a.kv.max_pages = max_pages_per_seq;
   a.kv.page_size = page_size;
+  a.kv.page_shift = __builtin_ctz((unsigned)page_size);
   a.kv.n_kv = n_kv_heads;
   a.kv.head_dim = head_dim;
   a.seq_lens = positions;

@@ -85,6 +85,22 @@ def test_bf16_weights_and_operands():
         compare_logits(g_logits[s_], o_logits[s_], f"bf16 step {s_}")
 
 
+@pytest.mark.parametrize("graph", [False, True])
+def test_medium_head_dim_128_and_split_k(graph):
+    """head_dim 128 in both attention kernels and the K-split GEMV path (d_model 1024)."""
+    dims = small_dims(d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=2048, vocab=2048,
+                      n_layers=2, n_standard_layers=0)
+    gw, ow = gpu_weights(dims), oracle_weights(dims)
+    lens = [100, 257, 3]
+    prompts = prompts_for(lens, dims["vocab"])
+    feed = np.stack([synth.tokens(3, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(3)])
+    model = make_model(dims, gw, max_batch=3, max_seq=320, page_size=64)
+    g_logits, _ = run_teacher_forced(model, prompts, feed, graph=graph)
+    o_logits, _ = O.teacher_forced_decode(dims, ow, prompts, feed)
+    for s_ in range(4):
+        compare_logits(g_logits[s_], o_logits[s_], f"medium step {s_}")
+
+
 def test_kv_cache_layout_is_bit_exact(tiny):
     dims, gw, ow = tiny
     page = 16
