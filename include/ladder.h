@@ -74,7 +74,8 @@ enum {
 
 /* Flags for ladder_set_mode. */
 enum {
-  LADDER_FLAG_DECODE_GRAPH = 1  /* capture each decode step shape in a CUDA graph and replay it */
+  LADDER_FLAG_DECODE_GRAPH = 1, /* capture each decode step shape in a CUDA graph and replay it */
+  LADDER_FLAG_NO_PDL = 2        /* launch decode kernels without programmatic dependent launch */
 };
 
 /* Model dimensions and capacities.  All int32 fields must be positive unless

@@ -67,6 +67,32 @@ __device__ __forceinline__ float warp_max(float v) {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
+// Programmatic dependent launch.  pdl_trigger lets the next kernel of the stream
+// start launching its CTAs; pdl_wait blocks until the previous kernel of the
+// stream has completed and its writes are visible.  Both are no-ops for a
+// kernel launched without the programmatic-serialization attribute.  Every
+// kernel launched with the attribute calls pdl_wait before it reads or writes
+// anything that an earlier kernel touches, so completion stays transitive.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// cudaLaunchKernelEx with the programmatic-serialization attribute when `pdl`.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                            Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // ---------------------------------------------------------------------------
 // Kernel parameter blocks
 // ---------------------------------------------------------------------------
@@ -100,8 +126,9 @@ struct GemvParams {
   const void* w1;    // QKV: wk, GATEUP: w_up
   const void* w2;    // QKV: wv
   int n_tasks;       // row pairs (QKV, RESID, LOGITS) or rows (GATEUP)
-  int kc;            // K chunk staged in shared memory (multiple of 256)
-  int ks;            // warps that split one task's K range (1, 2, 4, 8; > 1 only with a single chunk)
+  int kc;            // elements of K per streamed chunk (multiple of 256, divides K)
+  int nst;           // shared-memory ring stages
+  int* err;          // device error word (bit 2: pipeline wait timed out)
   float* out;        // QKV: q [B][ldo]; GATEUP: act [B][ldo]; RESID: x_out; LOGITS: logits
   int ldo;
   const float* x_res;  // RESID: residual rows [B][ldr]
@@ -158,14 +185,15 @@ struct AttnPrefillParams {
 // Launchers (each returns the cudaError_t of its launch)
 // ---------------------------------------------------------------------------
 cudaError_t launch_embed(const int* tok, int M, const void* E, int wdt, int d, int vocab, float* x, int* err,
-                         cudaStream_t s);
-cudaError_t launch_gemv(const GemvParams& p, int mode, int wdt, int num_sms, cudaStream_t s);
+                         cudaStream_t s, bool pdl = false);
+cudaError_t launch_gemv(const GemvParams& p, int mode, int wdt, int num_sms, cudaStream_t s, bool pdl = false);
 cudaError_t gemv_configure();
 int gemv_chunk(int B, int K);
-cudaError_t launch_attn_decode(const AttnDecodeParams& p, int B, int n_kv, int hd, cudaStream_t s);
+int gemv_launch_count(int B, int K);
+cudaError_t launch_attn_decode(const AttnDecodeParams& p, int B, int n_kv, int hd, cudaStream_t s, bool pdl = false);
 cudaError_t launch_argmax(const float* logits, int B, int V, float* part_v, int* part_i, int nblk,
-                          int* out, cudaStream_t s);
-cudaError_t launch_advance(int* seq_lens, int B, cudaStream_t s);
+                          int* out, cudaStream_t s, bool pdl = false);
+cudaError_t launch_advance(int* seq_lens, int B, cudaStream_t s, bool pdl = false);
 cudaError_t launch_rope_tables(float* cos_t, float* sin_t, int max_seq, int hd, float theta,
                                cudaStream_t s);
 

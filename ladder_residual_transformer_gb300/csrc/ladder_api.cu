@@ -358,7 +358,7 @@ int ladder_set_mode(ladder_model* m, int residual_mode, int flags) {
   if (!m) return fail(LADDER_ERR_INVALID, "model is NULL");
   if (residual_mode != LADDER_RESIDUAL_CONFIG && residual_mode != LADDER_RESIDUAL_STANDARD)
     return fail(LADDER_ERR_INVALID, "unknown residual mode %d", residual_mode);
-  if (flags & ~LADDER_FLAG_DECODE_GRAPH) return fail(LADDER_ERR_INVALID, "unknown flags 0x%x", flags);
+  if (flags & ~(LADDER_FLAG_DECODE_GRAPH | LADDER_FLAG_NO_PDL)) return fail(LADDER_ERR_INVALID, "unknown flags 0x%x", flags);
   if (residual_mode != m->residual_mode || flags != m->flags) m->drop_graphs();
   m->residual_mode = residual_mode;
   m->flags = flags;
@@ -507,7 +507,6 @@ namespace {
     m->launches += (n);                                                                          \
   } while (0)
 
-int gemv_launches(int B) { return (B + 3) / 4; }
 
 // One decode step for sequences 0..B-1.
 //
@@ -531,6 +530,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
   float* ao = m->at<float>(P.ao);
   float* act = m->at<float>(P.act);
   const int nstd = m->residual_mode == LADDER_RESIDUAL_STANDARD ? c.n_layers : c.n_standard_layers;
+  const bool pdl = !(m->flags & LADDER_FLAG_NO_PDL);
   cudaStream_t streams[2] = {s, m->aux};
   int writer[3] = {0, 0, 0};  // stream index that last wrote each buffer
   bool forked = false;
@@ -552,7 +552,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
   };
   int rc;
 
-  LAUNCH(launch_embed(tokens, B, m->embed, m->wdt, d, c.vocab, m->X(0), m->err(), s), 1);
+  LAUNCH(launch_embed(tokens, B, m->embed, m->wdt, d, c.vocab, m->X(0), m->err(), s, pdl), 1);
   if ((rc = wrote(0, 0))) return rc;
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerW& L = m->layers[l];
@@ -570,7 +570,8 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       g.rope_cos = m->at<float>(P.rope_cos); g.rope_sin = m->at<float>(P.rope_sin);
       g.pos = kv->seq_lens; g.kv = kvl;
       cudaEvent_t pe = m->probe_start(LADDER_PROBE_QKV, s);
-      LAUNCH(launch_gemv(g, GEMV_QKV, m->wdt, m->num_sms, s), gemv_launches(B));
+      g.err = m->err();
+      LAUNCH(launch_gemv(g, GEMV_QKV, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, g.K));
       m->probe_stop(pe, s);
 
       AttnDecodeParams a{};
@@ -578,7 +579,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       a.nsplit = nsplit; a.scale = 1.0f / sqrtf((float)c.head_dim);
       a.part_o = m->at<float>(P.part_o); a.part_ml = m->at<float>(P.part_ml); a.out = ao;
       pe = m->probe_start(LADDER_PROBE_ATTN, s);
-      LAUNCH(launch_attn_decode(a, B, c.n_kv_heads, c.head_dim, s), 2);
+      LAUNCH(launch_attn_decode(a, B, c.n_kv_heads, c.head_dim, s, pdl), 2);
       m->probe_stop(pe, s);
 
       if ((rc = use(k - 1, 0))) return rc;
@@ -586,7 +587,8 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       o.x = ao; o.ldx = qd; o.g = nullptr; o.B = B; o.K = qd; o.w0 = L.wo; o.n_tasks = d / 2;
       o.out = m->X(k); o.ldo = d; o.x_res = m->X(k - 1); o.ldr = d;
       pe = m->probe_start(LADDER_PROBE_OUT, s);
-      LAUNCH(launch_gemv(o, GEMV_RESID, m->wdt, m->num_sms, s), gemv_launches(B));
+      o.err = m->err();
+      LAUNCH(launch_gemv(o, GEMV_RESID, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, o.K));
       m->probe_stop(pe, s);
       if ((rc = wrote(k, 0))) return rc;
     }
@@ -600,7 +602,8 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       g.x = m->X(j); g.ldx = d; g.g = L.mlp_norm; g.eps = c.norm_eps; g.B = B; g.K = d;
       g.w0 = L.w_gate; g.w1 = L.w_up; g.n_tasks = f; g.out = act; g.ldo = f;
       cudaEvent_t pe = m->probe_start(LADDER_PROBE_GATEUP, ms);
-      LAUNCH(launch_gemv(g, GEMV_GATEUP, m->wdt, m->num_sms, ms), gemv_launches(B));
+      g.err = m->err();
+      LAUNCH(launch_gemv(g, GEMV_GATEUP, m->wdt, m->num_sms, ms, pdl), gemv_launch_count(B, g.K));
       m->probe_stop(pe, ms);
 
       if ((rc = use(k - 1, mlp_stream))) return rc;
@@ -608,7 +611,8 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       o.x = act; o.ldx = f; o.g = nullptr; o.B = B; o.K = f; o.w0 = L.w_down; o.n_tasks = d / 2;
       o.out = m->X(k); o.ldo = d; o.x_res = m->X(k - 1); o.ldr = d;
       pe = m->probe_start(LADDER_PROBE_DOWN, ms);
-      LAUNCH(launch_gemv(o, GEMV_RESID, m->wdt, m->num_sms, ms), gemv_launches(B));
+      o.err = m->err();
+      LAUNCH(launch_gemv(o, GEMV_RESID, m->wdt, m->num_sms, ms, pdl), gemv_launch_count(B, o.K));
       m->probe_stop(pe, ms);
       if ((rc = wrote(k, mlp_stream))) return rc;
     }
@@ -618,11 +622,12 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
   h.x = m->X(2 * c.n_layers); h.ldx = d; h.g = m->final_norm; h.eps = c.norm_eps; h.B = B; h.K = d;
   h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.out = logits; h.ldo = c.vocab;
   cudaEvent_t pe = m->probe_start(LADDER_PROBE_LMHEAD, s);
-  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s), gemv_launches(B));
+  h.err = m->err();
+  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, h.K));
   m->probe_stop(pe, s);
   if (next_tok)
-    LAUNCH(launch_argmax(logits, B, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i), kArgmaxBlocks, next_tok, s), 2);
-  LAUNCH(launch_advance(kv->seq_lens, B, s), 1);
+    LAUNCH(launch_argmax(logits, B, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i), kArgmaxBlocks, next_tok, s, pdl), 2);
+  LAUNCH(launch_advance(kv->seq_lens, B, s, pdl), 1);
   return LADDER_OK;
 }
 
@@ -770,7 +775,8 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
   GemvParams h{};
   h.x = xlast; h.ldx = d; h.g = m->final_norm; h.eps = c.norm_eps; h.B = B; h.K = d;
   h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.out = logits; h.ldo = c.vocab;
-  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s), gemv_launches(B));
+  h.err = m->err();
+  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s), gemv_launch_count(B, h.K));
   if (next_tok)
     LAUNCH(launch_argmax(logits, B, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i), kArgmaxBlocks, next_tok, s), 2);
   LAUNCH(launch_set_lens(d_lens, B, kv->seq_lens, s), 1);

@@ -28,6 +28,7 @@ LADDER_ERR_UNSUPPORTED = -4
 RESIDUAL_CONFIG = 0
 RESIDUAL_STANDARD = 1
 FLAG_DECODE_GRAPH = 1
+FLAG_NO_PDL = 2
 
 # Entry points declared in include/ladder.h, with (restype, argtypes).
 _vp, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
@@ -273,9 +274,9 @@ class LadderModel:
         return lib().ladder_kv_seq_len(self._kv, b)
 
     # -- modes -----------------------------------------------------------
-    def set_mode(self, standard: bool = False, graph: bool = False):
-        check(lib().ladder_set_mode(self._m, RESIDUAL_STANDARD if standard else RESIDUAL_CONFIG,
-                                    FLAG_DECODE_GRAPH if graph else 0))
+    def set_mode(self, standard: bool = False, graph: bool = False, pdl: bool = True):
+        flags = (FLAG_DECODE_GRAPH if graph else 0) | (0 if pdl else FLAG_NO_PDL)
+        check(lib().ladder_set_mode(self._m, RESIDUAL_STANDARD if standard else RESIDUAL_CONFIG, flags))
 
     # -- forward ---------------------------------------------------------
     def prefill(self, tokens: torch.Tensor, lens, logits: torch.Tensor | None = None,
