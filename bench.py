@@ -404,8 +404,8 @@ def main():
     ap.add_argument("--decode", type=int, default=None)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-prompt", type=int, default=256)
-    ap.add_argument("--cpu-decode", type=int, default=16)
+    ap.add_argument("--cpu-prompt", type=int, default=None, help="oracle sample prompt (default: the workload's)")
+    ap.add_argument("--cpu-decode", type=int, default=None, help="oracle sample decode steps (default: the workload's)")
     ap.add_argument("--ref-prompt", type=int, default=64)
     ap.add_argument("--ref-decode", type=int, default=4)
     args = ap.parse_args()
@@ -415,6 +415,10 @@ def main():
         args.prompt = run["prompt"]
     if args.decode is None:
         args.decode = run["decode_steps"]
+    if args.cpu_prompt is None:
+        args.cpu_prompt = args.prompt
+    if args.cpu_decode is None:
+        args.cpu_decode = args.decode
     out = run_reference(args, dims) if args.impl == "reference" else run_ours(args, dims)
     if out is not None:
         print(json.dumps(out), flush=True)

@@ -13,6 +13,10 @@
 //     whole tasks round-robin, wait for each chunk's stage, accumulate the two
 //     dot products in fp32 (lane l owns elements 8l + 256i of a chunk) and
 //     release the stage.
+// The ring is split into one sub-ring per consumer warp: every stage is filled
+// and drained by the same warp, in order, so a warp never waits on a stage
+// whose previous use belongs to another warp (an mbarrier parity wait only
+// distinguishes consecutive phases).
 // Weights depend on no earlier kernel, so the producer starts streaming at
 // launch; with programmatic dependent launch this overlaps the previous
 // kernel's tail.  Only the consumers wait (griddepcontrol.wait) before they
@@ -28,7 +32,7 @@ constexpr int SG_CONSUMERS = 4;
 constexpr int SG_THREADS = (SG_CONSUMERS + 1) * 32;
 constexpr int SG_MAX_STAGES = 16;
 constexpr int SG_RING_BYTES = 64 * 1024;
-constexpr int SG_MAX_CHUNK = 4096;  // elements of K per stage and row
+constexpr int SG_MAX_CHUNK = 2048;  // elements of K per stage and row
 constexpr int SG_SMEM_LIMIT = 226 * 1024;  // dynamic shared memory cap (leaves room for the static part)
 constexpr long long SG_WAIT_LIMIT = 4000000000LL;  // cycles (about 2 s)
 
@@ -167,32 +171,41 @@ __global__ void __launch_bounds__(SG_THREADS, 1) sgemv_kernel(const GemvParams p
   pdl_trigger();
 
   if (warp == SG_CONSUMERS) {
-    // ---------------- producer: stream weight chunks into the ring ----------------
+    // ---------------- producer: stream weight chunks into the sub-rings ----------------
     if (lane == 0) {
-      int issued = 0;
-      for (int i = 0; i < n_items; ++i) {
-        const int s = i % nst;
-        if (i >= nst && !sg_wait(&empty[s], ((i / nst) - 1) & 1)) {
-          atomicOr(p.err, 4);
-          break;
-        }
+      const int spw = nst / SG_CONSUMERS;  // stages per consumer warp
+      int cnt[SG_CONSUMERS] = {0, 0, 0, 0};  // chunks issued to each warp's sub-ring
+      bool ok = true;
+      for (int ti = 0; ok && ti < t1 - t0; ++ti) {
+        const int w = ti % SG_CONSUMERS;
         const WT *r0, *r1;
         int kind, local;
-        sg_rows<WT, MODE>(p, t0 + i / nch, r0, r1, kind, local);
-        const int c = i % nch;
-        uint8_t* dst = ring + (size_t)s * stage_bytes;
-        const uint32_t bar = sg_smem(&full[s]);
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(stage_bytes) : "memory");
-        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                     ::"r"(sg_smem(dst)), "l"(r0 + (size_t)c * kch), "r"(2 * kch), "r"(bar)
-                     : "memory");
-        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                     ::"r"(sg_smem(dst + 2 * kch)), "l"(r1 + (size_t)c * kch), "r"(2 * kch), "r"(bar)
-                     : "memory");
-        ++issued;
+        sg_rows<WT, MODE>(p, t0 + ti, r0, r1, kind, local);
+        for (int c = 0; c < nch; ++c) {
+          const int j = cnt[w];
+          const int s = w * spw + j % spw;
+          if (j >= spw && !sg_wait(&empty[s], ((j / spw) - 1) & 1)) {
+            atomicOr(p.err, 4);
+            ok = false;
+            break;
+          }
+          uint8_t* dst = ring + (size_t)s * stage_bytes;
+          const uint32_t bar = sg_smem(&full[s]);
+          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(stage_bytes)
+                       : "memory");
+          asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                       ::"r"(sg_smem(dst)), "l"(r0 + (size_t)c * kch), "r"(2 * kch), "r"(bar)
+                       : "memory");
+          asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                       ::"r"(sg_smem(dst + 2 * kch)), "l"(r1 + (size_t)c * kch), "r"(2 * kch), "r"(bar)
+                       : "memory");
+          cnt[w] = j + 1;
+        }
       }
       // no copy into this CTA's shared memory may be in flight when it exits
-      for (int i = issued - nst < 0 ? 0 : issued - nst; i < issued; ++i) sg_wait(&full[i % nst], (i / nst) & 1);
+      for (int w = 0; w < SG_CONSUMERS; ++w)
+        for (int j = cnt[w] - spw < 0 ? 0 : cnt[w] - spw; j < cnt[w]; ++j)
+          sg_wait(&full[w * spw + j % spw], (j / spw) & 1);
     }
     return;
   }
@@ -248,14 +261,15 @@ __global__ void __launch_bounds__(SG_THREADS, 1) sgemv_kernel(const GemvParams p
   asm volatile("bar.sync 1, %0;" ::"n"(SG_CONSUMERS * 32) : "memory");
 
   bool ok = true;
+  const int spw = nst / SG_CONSUMERS;
+  int j = 0;  // chunks consumed from this warp's sub-ring
   for (int t = t0 + warp; t < t1 && ok; t += SG_CONSUMERS) {
     float a0[BT], a1[BT];
 #pragma unroll
     for (int b = 0; b < BT; ++b) a0[b] = a1[b] = 0.f;
-    for (int c = 0; c < nch; ++c) {
-      const int i = (t - t0) * nch + c;
-      const int s = i % nst;
-      if (!sg_wait(&full[s], (i / nst) & 1)) {
+    for (int c = 0; c < nch; ++c, ++j) {
+      const int s = warp * spw + j % spw;
+      if (!sg_wait(&full[s], (j / spw) & 1)) {
         if (lane == 0) atomicOr(p.err, 4);
         ok = false;
         break;
@@ -305,7 +319,8 @@ static SgPlan sg_plan(int B, int K) {
   const int stage = 4 * pl.kch;
   pl.nst = SG_RING_BYTES / stage;
   if (pl.nst > SG_MAX_STAGES) pl.nst = SG_MAX_STAGES;
-  if (pl.nst < 2) pl.nst = 2;
+  pl.nst -= pl.nst % SG_CONSUMERS;             // whole sub-rings
+  if (pl.nst < 2 * SG_CONSUMERS) pl.nst = 2 * SG_CONSUMERS;  // two stages per warp at least
   // the staged input rows must fit next to the ring
   pl.bt = B <= 1 ? 1 : (B <= 2 ? 2 : 4);
   while (pl.bt > 1 && (size_t)pl.nst * stage + (size_t)pl.bt * K * 4 + 2 * SG_MAX_STAGES * 8 > (size_t)SG_SMEM_LIMIT)

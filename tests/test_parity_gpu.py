@@ -87,8 +87,8 @@ def test_bf16_weights_and_operands():
 
 @pytest.mark.parametrize("graph", [False, True])
 def test_medium_head_dim_128_and_split_k(graph):
-    """head_dim 128 in both attention kernels and the K-split GEMV path (d_model 1024)."""
-    dims = small_dims(d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=2048, vocab=2048,
+    """head_dim 128 in both attention kernels; the down projection (K = 3072) streams in two chunks."""
+    dims = small_dims(d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=3072, vocab=2048,
                       n_layers=2, n_standard_layers=0)
     gw, ow = gpu_weights(dims), oracle_weights(dims)
     lens = [100, 257, 3]
