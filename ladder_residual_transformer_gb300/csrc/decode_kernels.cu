@@ -1,12 +1,16 @@
 // Decode-side kernels of the Ladder Transformer forward pass (one new token per
 // sequence, B <= 64 sequences): embedding gather, paged split-context
 // attention and its combine step, greedy argmax, and small bookkeeping
-// kernels.  The weight-streaming GEMVs are in gemv_stream.cu.
+// kernels, and the weight-streaming GEMVs with their fused prologue/epilogues.
 #include "internal.cuh"
 
 #include <math.h>
 
 namespace ladder {
+
+constexpr int GEMV_WARPS = 8;
+constexpr int GEMV_THREADS = GEMV_WARPS * 32;
+constexpr int GEMV_SMEM_FLOATS = 16384;  // 64 KB staged input per CTA
 
 
 // ---------------------------------------------------------------------------
@@ -38,6 +42,379 @@ cudaError_t launch_embed(const int* tok, int M, const void* E, int wdt, int d, i
   if (wdt == WDT_F16)
     return launch_k(embed_kernel<f16>, dim3(M), dim3(128), 0, s, pdl, tok, static_cast<const f16*>(E), d, vocab, x, err);
   return launch_k(embed_kernel<bf16>, dim3(M), dim3(128), 0, s, pdl, tok, static_cast<const bf16*>(E), d, vocab, x, err);
+}
+
+// ---------------------------------------------------------------------------
+// GEMV: out[b, n] = sum_k W[n, k] * u[b, k] for B <= BT rows, fused prologue and
+// epilogue by mode.  u = x * rsqrt(mean(x^2) + eps) * g when a gain is given.
+//
+// Work unit ("task") = two weight rows computed together by one warp: a RoPE
+// pair (2j, 2j+1) for QKV, the matching gate and up rows for SwiGLU, or two
+// consecutive rows otherwise.  Lane l reads 16 bytes (8 bf16) at k = 8l + 256i.
+// Staged input layout per batch row: two planes [kc/8][4] holding elements
+// k%8 < 4 and k%8 >= 4, so that each lane's 16-byte shared-memory reads are
+// contiguous across the warp (no bank conflicts).
+// ---------------------------------------------------------------------------
+template <typename WT, int BT>
+__device__ __forceinline__ void gemv_fma(const uint4& w, const float* __restrict__ u, int kc, int k,
+                                         float (&acc)[BT]) {
+  using C = W16<WT>;
+  const float w0 = C::lo(w.x), w1 = C::hi(w.x), w2 = C::lo(w.y), w3 = C::hi(w.y);
+  const float w4 = C::lo(w.z), w5 = C::hi(w.z), w6 = C::lo(w.w), w7 = C::hi(w.w);
+  const int q = (k >> 3) << 2;
+#pragma unroll
+  for (int b = 0; b < BT; ++b) {
+    const float4 a = *reinterpret_cast<const float4*>(u + b * kc + q);
+    const float4 c = *reinterpret_cast<const float4*>(u + b * kc + (kc >> 1) + q);
+    float s = acc[b];
+    s = fmaf(w0, a.x, s);
+    s = fmaf(w1, a.y, s);
+    s = fmaf(w2, a.z, s);
+    s = fmaf(w3, a.w, s);
+    s = fmaf(w4, c.x, s);
+    s = fmaf(w5, c.y, s);
+    s = fmaf(w6, c.z, s);
+    s = fmaf(w7, c.w, s);
+    acc[b] = s;
+  }
+}
+
+template <typename WT, int BT, int MODE>
+__global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) {
+  using C = W16<WT>;
+  const WT* g = static_cast<const WT*>(p.g);
+  const WT* W0 = static_cast<const WT*>(p.w0);
+  const WT* W1 = static_cast<const WT*>(p.w1);
+  const WT* W2 = static_cast<const WT*>(p.w2);
+  extern __shared__ float4 gemv_smem4[];
+  float* u = reinterpret_cast<float*>(gemv_smem4);
+  __shared__ float s_red[GEMV_WARPS][BT];
+  __shared__ float s_rms[BT];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int K = p.K;
+  pdl_trigger();
+
+  // Weights depend on no earlier kernel: when every task of this CTA fits in
+  // one round of a single chunk, each warp requests the first 4 x 256 elements
+  // of both its rows before waiting for the previous kernel, so that their
+  // latency overlaps the previous kernel's tail.
+  const int ks_ = p.ks;
+  const int task0 = blockIdx.x * (GEMV_WARPS / ks_) + warp / ks_;
+  const bool one_round = p.kc >= K && (long long)gridDim.x * (GEMV_WARPS / ks_) >= p.n_tasks;
+  uint4 pre_a[4], pre_b[4];
+  int pre_k = -1;  // first k of the prefetched iteration, -1 if none
+  if (one_round && task0 < p.n_tasks) {
+    const WT* r0;
+    const WT* r1;
+    if (MODE == GEMV_QKV) {
+      const int q0 = 2 * task0;
+      r0 = q0 < p.nq_hd ? W0 + (size_t)q0 * K
+                        : (q0 < p.nq_hd + p.nkv_hd ? W1 + (size_t)(q0 - p.nq_hd) * K
+                                                   : W2 + (size_t)(q0 - p.nq_hd - p.nkv_hd) * K);
+      r1 = r0 + K;
+    } else if (MODE == GEMV_GATEUP) {
+      r0 = W0 + (size_t)task0 * K;
+      r1 = W1 + (size_t)task0 * K;
+    } else {
+      r0 = W0 + (size_t)(2 * task0) * K;
+      r1 = r0 + K;
+    }
+    const int kb = ks_ > 1 ? (warp % ks_) * (K / ks_) : 0;
+    const int ke = ks_ > 1 ? kb + K / ks_ : K;
+    const int k = kb + lane * 8;
+    if (k + 768 < ke) {
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        pre_a[s] = ld_stream_u4(r0 + k + 256 * s);
+        pre_b[s] = ld_stream_u4(r1 + k + 256 * s);
+      }
+      pre_k = k;
+    }
+  }
+  pdl_wait();
+
+  // RMSNorm statistics of each input row, in a fixed order (identical in every CTA).
+  if (p.g != nullptr) {
+    float ss[BT];
+#pragma unroll
+    for (int b = 0; b < BT; ++b) ss[b] = 0.f;
+    for (int i = tid * 4; i < K; i += GEMV_THREADS * 4) {
+#pragma unroll
+      for (int b = 0; b < BT; ++b) {
+        if (b < p.B) {
+          const float4 v = *reinterpret_cast<const float4*>(p.x + (size_t)b * p.ldx + i);
+          ss[b] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+      const float t = warp_sum(ss[b]);
+      if (lane == 0) s_red[warp][b] = t;
+    }
+    __syncthreads();
+    if (tid < BT) {
+      float t = 0.f;
+      for (int w = 0; w < GEMV_WARPS; ++w) t += s_red[w][tid];
+      s_rms[tid] = rsqrtf(t / (float)K + p.eps);
+    }
+    __syncthreads();
+  }
+
+  // Warp w works on task slot w / ks of this CTA and on K slice w % ks.
+  const int ks = p.ks;
+  const int tpc = GEMV_WARPS / ks;  // tasks per CTA per round
+  const int slot = warp / ks, kslice = warp % ks;
+  const int total_slots = gridDim.x * tpc;
+  const int rounds = (p.n_tasks + total_slots - 1) / total_slots;
+  const bool single_chunk = p.kc >= K;
+  const int kspan = K / ks;  // single chunk when ks > 1
+  __shared__ float s_part[GEMV_WARPS][2][BT];
+
+  for (int r = 0; r < rounds; ++r) {
+    const int task = r * total_slots + blockIdx.x * tpc + slot;
+    const bool active = task < p.n_tasks;
+
+    // Which two weight rows this task reads.
+    const WT* row0 = W0;
+    const WT* row1 = W0;
+    int local = 0, kind = 0;  // QKV: kind 0 = q, 1 = k, 2 = v; local = row inside its matrix
+    if (active) {
+      if (MODE == GEMV_QKV) {
+        const int r0 = 2 * task;
+        if (r0 < p.nq_hd) {
+          local = r0; kind = 0; row0 = W0 + (size_t)local * K;
+        } else if (r0 < p.nq_hd + p.nkv_hd) {
+          local = r0 - p.nq_hd; kind = 1; row0 = W1 + (size_t)local * K;
+        } else {
+          local = r0 - p.nq_hd - p.nkv_hd; kind = 2; row0 = W2 + (size_t)local * K;
+        }
+        row1 = row0 + K;
+      } else if (MODE == GEMV_GATEUP) {
+        row0 = W0 + (size_t)task * K;
+        row1 = W1 + (size_t)task * K;
+      } else {
+        row0 = W0 + (size_t)(2 * task) * K;
+        row1 = row0 + K;
+      }
+    }
+
+    float a0[BT], a1[BT];
+#pragma unroll
+    for (int b = 0; b < BT; ++b) a0[b] = a1[b] = 0.f;
+
+    for (int k0 = 0; k0 < K; k0 += p.kc) {
+      const int kc = min(p.kc, K - k0);
+      if (!single_chunk || r == 0) {
+        __syncthreads();
+        // Stage the (normalised) input chunk in the two-plane layout.
+        for (int i = tid * 4; i < kc; i += GEMV_THREADS * 4) {
+          float4 gv = make_float4(1.f, 1.f, 1.f, 1.f);
+          if (g != nullptr) {
+            const uint2 graw = *reinterpret_cast<const uint2*>(g + k0 + i);
+            gv = make_float4(C::lo(graw.x), C::hi(graw.x), C::lo(graw.y), C::hi(graw.y));
+          }
+          const int dst = ((i & 4) ? (kc >> 1) : 0) + ((i >> 3) << 2);
+#pragma unroll
+          for (int b = 0; b < BT; ++b) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (b < p.B) {
+              v = *reinterpret_cast<const float4*>(p.x + (size_t)b * p.ldx + k0 + i);
+              const float sc = (p.g != nullptr) ? s_rms[b] : 1.f;
+              v.x *= sc * gv.x; v.y *= sc * gv.y; v.z *= sc * gv.z; v.w *= sc * gv.w;
+            }
+            *reinterpret_cast<float4*>(u + b * kc + dst) = v;
+          }
+        }
+        __syncthreads();
+      }
+      if (active) {
+        const WT* p0 = row0 + k0;
+        const WT* p1 = row1 + k0;
+        const int kb = ks > 1 ? kslice * kspan : 0;
+        const int ke = ks > 1 ? kb + kspan : kc;
+        int k = kb + lane * 8;
+        if (r == 0 && k0 == 0 && pre_k == k) {  // consume the loads issued before pdl_wait
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            gemv_fma<WT, BT>(pre_a[s], u, kc, k + 256 * s, a0);
+            gemv_fma<WT, BT>(pre_b[s], u, kc, k + 256 * s, a1);
+          }
+          k += 1024;
+        }
+        for (; k + 768 < ke; k += 1024) {
+          uint4 wa[4], wb[4];
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            wa[s] = ld_stream_u4(p0 + k + 256 * s);
+            wb[s] = ld_stream_u4(p1 + k + 256 * s);
+          }
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            gemv_fma<WT, BT>(wa[s], u, kc, k + 256 * s, a0);
+            gemv_fma<WT, BT>(wb[s], u, kc, k + 256 * s, a1);
+          }
+        }
+        for (; k < ke; k += 256) {
+          const uint4 wa = ld_stream_u4(p0 + k);
+          const uint4 wb = ld_stream_u4(p1 + k);
+          gemv_fma<WT, BT>(wa, u, kc, k, a0);
+          gemv_fma<WT, BT>(wb, u, kc, k, a1);
+        }
+      }
+    }
+
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+      a0[b] = warp_sum(a0[b]);
+      a1[b] = warp_sum(a1[b]);
+    }
+    if (ks > 1) {
+      // combine the K slices of each task in a fixed order
+      if (lane == 0) {
+#pragma unroll
+        for (int b = 0; b < BT; ++b) {
+          s_part[warp][0][b] = a0[b];
+          s_part[warp][1][b] = a1[b];
+        }
+      }
+      __syncthreads();
+      if (kslice == 0) {
+#pragma unroll
+        for (int b = 0; b < BT; ++b) {
+          float t0 = 0.f, t1 = 0.f;
+          for (int i = 0; i < ks; ++i) {
+            t0 += s_part[warp + i][0][b];
+            t1 += s_part[warp + i][1][b];
+          }
+          a0[b] = t0;
+          a1[b] = t1;
+        }
+      }
+      __syncthreads();
+      if (kslice != 0) continue;
+    }
+    if (!active) continue;
+
+    // Epilogue: lane b handles batch row b.
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+      if (lane != b || b >= p.B) continue;
+      const float v0 = a0[b], v1 = a1[b];
+      if (MODE == GEMV_QKV) {
+        const int hd = p.kv.head_dim;
+        const int pos = p.pos[b];
+        float r0 = v0, r1 = v1;
+        if (kind < 2) {
+          const int j = (local % hd) >> 1;
+          const float c = p.rope_cos[(size_t)pos * (hd >> 1) + j];
+          const float s = p.rope_sin[(size_t)pos * (hd >> 1) + j];
+          r0 = v0 * c - v1 * s;
+          r1 = v0 * s + v1 * c;
+        }
+        if (kind == 0) {
+          float* q = p.out + (size_t)b * p.ldo + local;
+          q[0] = r0;
+          q[1] = r1;
+        } else {
+          const int head = local / hd, dim = local % hd;
+          bf16* dst = p.kv.base + p.kv.slot(b, pos, kind - 1, head) + dim;
+          dst[0] = __float2bfloat16_rn(r0);
+          dst[1] = __float2bfloat16_rn(r1);
+        }
+      } else if (MODE == GEMV_GATEUP) {
+        p.out[(size_t)b * p.ldo + task] = silu_f(v0) * v1;
+      } else if (MODE == GEMV_RESID) {
+        const size_t n = 2 * (size_t)task;
+        p.out[(size_t)b * p.ldo + n] = p.x_res[(size_t)b * p.ldr + n] + v0;
+        p.out[(size_t)b * p.ldo + n + 1] = p.x_res[(size_t)b * p.ldr + n + 1] + v1;
+      } else {
+        const size_t n = 2 * (size_t)task;
+        p.out[(size_t)b * p.ldo + n] = v0;
+        p.out[(size_t)b * p.ldo + n + 1] = v1;
+      }
+    }
+  }
+}
+
+int gemv_chunk(int B, int K) {
+  const int bt = B <= 1 ? 1 : (B <= 2 ? 2 : 4);
+  int kc = GEMV_SMEM_FLOATS / bt;
+  kc -= kc % 256;
+  return K < kc ? K : kc;
+}
+
+template <typename WT, int BT>
+static cudaError_t set_gemv_attrs() {
+  const int bytes = GEMV_SMEM_FLOATS * 4;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(gemv_kernel<WT, BT, GEMV_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
+  if ((e = cudaFuncSetAttribute(gemv_kernel<WT, BT, GEMV_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
+  if ((e = cudaFuncSetAttribute(gemv_kernel<WT, BT, GEMV_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
+  return cudaFuncSetAttribute(gemv_kernel<WT, BT, GEMV_LOGITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+cudaError_t gemv_configure() {
+  cudaError_t e;
+  if ((e = set_gemv_attrs<bf16, 1>())) return e;
+  if ((e = set_gemv_attrs<bf16, 2>())) return e;
+  if ((e = set_gemv_attrs<bf16, 4>())) return e;
+  if ((e = set_gemv_attrs<f16, 1>())) return e;
+  if ((e = set_gemv_attrs<f16, 2>())) return e;
+  return set_gemv_attrs<f16, 4>();
+}
+
+template <typename WT, int BT>
+static cudaError_t gemv_dispatch(const GemvParams& p, int mode, int grid, size_t smem, cudaStream_t s, bool pdl) {
+  const dim3 g(grid), b(GEMV_THREADS);
+  switch (mode) {
+    case GEMV_QKV: return launch_k(gemv_kernel<WT, BT, GEMV_QKV>, g, b, smem, s, pdl, p);
+    case GEMV_GATEUP: return launch_k(gemv_kernel<WT, BT, GEMV_GATEUP>, g, b, smem, s, pdl, p);
+    case GEMV_RESID: return launch_k(gemv_kernel<WT, BT, GEMV_RESID>, g, b, smem, s, pdl, p);
+    default: return launch_k(gemv_kernel<WT, BT, GEMV_LOGITS>, g, b, smem, s, pdl, p);
+  }
+}
+
+template <typename WT>
+static cudaError_t gemv_dispatch_bt(const GemvParams& p, int bt, int mode, int grid, size_t smem, cudaStream_t s,
+                                    bool pdl) {
+  if (bt == 1) return gemv_dispatch<WT, 1>(p, mode, grid, smem, s, pdl);
+  if (bt == 2) return gemv_dispatch<WT, 2>(p, mode, grid, smem, s, pdl);
+  return gemv_dispatch<WT, 4>(p, mode, grid, smem, s, pdl);
+}
+
+int gemv_launch_count(int B, int K) { return (B + 3) / 4; }
+
+// Batches larger than 4 run as consecutive chunks of at most 4 rows.
+cudaError_t launch_gemv(const GemvParams& p0, int mode, int wdt, int num_sms, cudaStream_t s, bool pdl) {
+  for (int b0 = 0; b0 < p0.B; b0 += 4) {
+    GemvParams p = p0;
+    p.B = p0.B - b0 < 4 ? p0.B - b0 : 4;
+    p.x = p0.x + (size_t)b0 * p0.ldx;
+    p.out = p0.out + (size_t)b0 * p0.ldo;
+    if (p0.x_res) p.x_res = p0.x_res + (size_t)b0 * p0.ldr;
+    if (p0.pos) p.pos = p0.pos + b0;
+    if (p0.kv.block_table) p.kv.block_table = p0.kv.block_table + (size_t)b0 * p0.kv.max_pages;
+    const int bt = p.B <= 1 ? 1 : (p.B <= 2 ? 2 : 4);
+    p.kc = gemv_chunk(p.B, p.K);
+    const size_t smem = (size_t)bt * p.kc * sizeof(float);
+    // K split: the smallest that gives at least 1.5 CTAs per SM (more warps in
+    // flight for short, wide matrices) while each slice stays a multiple of 256.
+    p.ks = 1;
+    if (p.kc >= p.K) {
+      while (p.ks < GEMV_WARPS && (long long)p.n_tasks * p.ks < (long long)num_sms * 12 &&
+             (p.K / (2 * p.ks)) % 256 == 0)
+        p.ks *= 2;
+    }
+    const int tpc = GEMV_WARPS / p.ks;
+    int grid = (p.n_tasks + tpc - 1) / tpc;
+    const int cap = num_sms * 8;
+    if (grid > cap) grid = cap;
+    cudaError_t e = wdt == WDT_F16 ? gemv_dispatch_bt<f16>(p, bt, mode, grid, smem, s, pdl)
+                                   : gemv_dispatch_bt<bf16>(p, bt, mode, grid, smem, s, pdl);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 // ---------------------------------------------------------------------------

@@ -2,16 +2,20 @@
 //   C[m, n] = sum_k A[m, k] * W[n, k],  A = bf16 activations [M, K],
 //   W = bf16 weights [N, K] (both K-major), fp32 accumulation in TMEM.
 //
-// One CTA computes a 128 x 256 tile with tcgen05.mma (cta_group::1, kind::f16,
-// M = 128, N = 256, K = 16 per instruction).  Warp roles:
+// Persistent CTAs (one per SM) loop over 128 x BN tiles (BN = 256, or 128 for
+// narrow matrices) with tcgen05.mma (cta_group::1, kind::f16, M = 128, N = BN,
+// K = 16 per instruction).  Warp roles:
 //   warp 4: one elected thread issues the TMA loads of A (128 x 64) and of the
 //           two 128-row halves of B (each half may come from a different
 //           weight matrix: q/k/v rows, or the gate and up rows of SwiGLU);
-//   warp 5: allocates 256 TMEM columns and one elected thread issues the MMAs,
-//           releasing each shared-memory stage with tcgen05.commit;
+//   warp 5: allocates 2 x BN TMEM columns (two accumulator buffers) and one
+//           elected thread issues the MMAs, releasing each shared-memory stage
+//           with tcgen05.commit and each finished accumulator to the epilogue;
 //   warps 0-3: epilogue, reading the accumulator with tcgen05.ld (warp w owns
 //           TMEM lanes 32w..32w+31, i.e. tile rows) and applying the fused
-//           RoPE + KV scatter, SwiGLU, or residual add.
+//           RoPE + KV scatter, SwiGLU, or residual add, then handing the
+//           accumulator buffer back, so the epilogue of one tile overlaps the
+//           main loop of the next.
 // Operands sit in shared memory in the 128-byte-swizzled K-major layout that
 // TMA writes and the MMA descriptors describe.  Every mbarrier wait is bounded
 // by a clock limit: on expiry the kernel sets bit 1 of the error word, stops
@@ -127,21 +131,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 }
 
 // ---------------------------------------------------------------------------
-// B-operand half selection: (tensor map index, first row) of tile half h.
-// Returns false when the half lies beyond N (QKV only) and must be ignored.
+// B-operand half selection: (tensor map index, first row) of 128-row half h of
+// N-tile `tile_n` (tiles are BN wide; GATEUP tiles are 128 outputs = gate half
+// + up half).  Returns false when the half lies beyond N and must be ignored.
 // ---------------------------------------------------------------------------
-template <int MODE>
+template <int MODE, int BN>
 __device__ __forceinline__ bool b_half(const GemmParams& p, int tile_n, int h, int& map, int& row) {
   if (MODE == GEMM_GATEUP) {
     map = h;
     row = tile_n * 128;
     return true;
   }
-  const int c = tile_n * TC_BN + h * 128;
+  const int c = tile_n * BN + h * 128;
   if (MODE == GEMM_RESID) {
     map = 0;
     row = c;
-    return true;
+    return c < p.N;
   }
   if (c < p.nq_hd) { map = 0; row = c; return true; }
   if (c < p.nq_hd + p.nkv_hd) { map = 1; row = c - p.nq_hd; return true; }
@@ -156,34 +161,47 @@ struct TcMaps {
   CUtensorMap b[3];
 };
 
-template <typename WT, int MODE>
+// Persistent CTA: tiles t = blockIdx.x + i * gridDim.x, tile t -> (m = t % m_tiles,
+// n = t / m_tiles) so that CTAs running together share the weight tile in L2.
+// The accumulator is double-buffered in TMEM (2 x BN columns): the MMA warp
+// fills buffer i & 1 while the epilogue warps drain the other one.
+template <typename WT, int MODE, int BN>
 __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_constant__ TcMaps maps,
-                                                                const GemmParams p, int* err) {
+                                                                const GemmParams p, int m_tiles, int n_tiles,
+                                                                int* err) {
   using C = W16<WT>;
+  constexpr int HALVES = BN / 128;
+  constexpr int STAGE = TC_A_BYTES + HALVES * TC_BH_BYTES;
+  constexpr int NST = (TC_SMEM - 1024 - 256) / STAGE;
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TC_STAGES * TC_STAGE_BYTES);
-  uint64_t* empty = full + TC_STAGES;
-  uint64_t* accum = empty + TC_STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * STAGE);
+  uint64_t* empty = full + NST;
+  uint64_t* tfull = empty + NST;   // [2] accumulator ready
+  uint64_t* tempty = tfull + 2;    // [2] accumulator drained
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   int* bail = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile_n = blockIdx.x, m0 = blockIdx.y * TC_BM;
   const int nkb = p.K / TC_BK;
+  const int total = m_tiles * n_tiles;
+  const int my_tiles = blockIdx.x < total ? (total - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < TC_STAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(accum, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);  // one arrival per epilogue warp
+    }
     *bail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 5) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(TC_BN)
+                 "r"(2 * BN)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -194,59 +212,82 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
 
   if (warp == 4) {
     if (lane == 0) {
-      int map0, row0, map1, row1;
-      b_half<MODE>(p, tile_n, 0, map0, row0);
-      if (!b_half<MODE>(p, tile_n, 1, map1, row1)) { map1 = map0; row1 = row0; }
-      int issued = 0;
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % TC_STAGES;
-        const uint32_t ph = (kb / TC_STAGES) & 1;
-        if (kb >= TC_STAGES && !mbar_wait(&empty[s], ph ^ 1)) {
-          atomicOr(err, 2);
-          *reinterpret_cast<volatile int*>(bail) = 1;
-          break;
+      int it = 0;  // running k-block index across tiles
+      bool ok = true;
+      for (int i = 0; ok && i < my_tiles; ++i) {
+        const int t = blockIdx.x + i * gridDim.x;
+        const int m0 = (t % m_tiles) * TC_BM, tn = t / m_tiles;
+        int map0, row0, map1 = 0, row1 = 0;
+        b_half<MODE, BN>(p, tn, 0, map0, row0);
+        if (HALVES == 2 && !b_half<MODE, BN>(p, tn, 1, map1, row1)) { map1 = map0; row1 = row0; }
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % NST;
+          const uint32_t ph = (it / NST) & 1;
+          if (it >= NST && !mbar_wait(&empty[s], ph ^ 1)) {
+            atomicOr(err, 2);
+            *reinterpret_cast<volatile int*>(bail) = 1;
+            ok = false;
+            break;
+          }
+          if (*reinterpret_cast<volatile int*>(bail)) { ok = false; break; }
+          uint8_t* st = smem + s * STAGE;
+          mbar_expect_tx(&full[s], STAGE);
+          tma_load_2d(st, &maps.a, kb * TC_BK, m0, &full[s]);
+          tma_load_2d(st + TC_A_BYTES, &maps.b[map0], kb * TC_BK, row0, &full[s]);
+          if (HALVES == 2) tma_load_2d(st + TC_A_BYTES + TC_BH_BYTES, &maps.b[map1], kb * TC_BK, row1, &full[s]);
         }
-        if (*reinterpret_cast<volatile int*>(bail)) break;
-        uint8_t* st = smem + s * TC_STAGE_BYTES;
-        mbar_expect_tx(&full[s], TC_STAGE_BYTES);
-        tma_load_2d(st, &maps.a, kb * TC_BK, m0, &full[s]);
-        tma_load_2d(st + TC_A_BYTES, &maps.b[map0], kb * TC_BK, row0, &full[s]);
-        tma_load_2d(st + TC_A_BYTES + TC_BH_BYTES, &maps.b[map1], kb * TC_BK, row1, &full[s]);
-        ++issued;
       }
       // Make sure no copy into this CTA's shared memory is still in flight.
-      for (int kb = issued - TC_STAGES < 0 ? 0 : issued - TC_STAGES; kb < issued; ++kb)
-        mbar_wait(&full[kb % TC_STAGES], (kb / TC_STAGES) & 1);
+      for (int k = it - NST < 0 ? 0 : it - NST; k < it; ++k) mbar_wait(&full[k % NST], (k / NST) & 1);
     }
   } else if (warp == 5) {
     if (lane == 0) {
-      constexpr uint32_t idesc = umma_idesc(TC_BM, TC_BN, C::umma_fmt);
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % TC_STAGES;
-        const uint32_t ph = (kb / TC_STAGES) & 1;
-        if (!mbar_wait(&full[s], ph)) {
+      constexpr uint32_t idesc = umma_idesc(TC_BM, BN, C::umma_fmt);
+      int it = 0;
+      bool ok = true;
+      for (int i = 0; ok && i < my_tiles; ++i) {
+        const int acc = i & 1;
+        if (i >= 2 && !mbar_wait(&tempty[acc], ((i >> 1) - 1) & 1)) {
           atomicOr(err, 2);
           *reinterpret_cast<volatile int*>(bail) = 1;
           break;
         }
         tc_fence_after();
-        const uint32_t a_base = smem_u32(smem + s * TC_STAGE_BYTES);
-        const uint32_t b_base = a_base + TC_A_BYTES;
+        const uint32_t d = tmem + acc * BN;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % NST;
+          const uint32_t ph = (it / NST) & 1;
+          if (!mbar_wait(&full[s], ph)) {
+            atomicOr(err, 2);
+            *reinterpret_cast<volatile int*>(bail) = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + s * STAGE);
+          const uint32_t b_base = a_base + TC_A_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < TC_BK / 16; ++kk)
-          umma_bf16(tmem, umma_desc(a_base + kk * 32), umma_desc(b_base + kk * 32), idesc, (kb | kk) != 0);
-        umma_commit(&empty[s]);
+          for (int kk = 0; kk < TC_BK / 16; ++kk)
+            umma_bf16(d, umma_desc(a_base + kk * 32), umma_desc(b_base + kk * 32), idesc, (kb | kk) != 0);
+          umma_commit(&empty[s]);
+        }
+        umma_commit(&tfull[acc]);  // also after a bail, so that the MMAs in flight finish first
       }
-      umma_commit(accum);  // also issued after a bail, so that the MMAs in flight finish first
     }
   } else {
-    const bool ok = mbar_wait(accum, 0);
-    tc_fence_after();
-    if (!ok) {
-      if (lane == 0) atomicOr(err, 2);
-    } else if (!__shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(bail), 0)) {
-      const int m = m0 + warp * 32 + lane;
-      const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    const int hd = p.kv.head_dim;
+    for (int i = 0; i < my_tiles; ++i) {
+      const int acc = i & 1;
+      const int t = blockIdx.x + i * gridDim.x;
+      const int m = (t % m_tiles) * TC_BM + warp * 32 + lane, tile_n = t / m_tiles;
+      const bool ok = mbar_wait(&tfull[acc], (i >> 1) & 1);
+      tc_fence_after();
+      if (!ok) {
+        if (lane == 0) atomicOr(err, 2);
+        break;
+      }
+      if (__shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(bail), 0)) break;
+      const uint32_t trow = tmem + acc * BN + ((uint32_t)(warp * 32) << 16);
       if (MODE == GEMM_GATEUP) {
         for (int c = 0; c < 4; ++c) {
           float g[32], u[32];
@@ -266,11 +307,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
           }
         }
       } else if (MODE == GEMM_RESID) {
-        for (int c = 0; c < TC_BN / 32; ++c) {
+        for (int c = 0; c < BN / 32; ++c) {
           float v[32];
           tmem_ld32(trow + c * 32, v);
-          if (m < p.M) {
-            const size_t off = (size_t)m * p.ldo + (size_t)tile_n * TC_BN + c * 32;
+          const int n0 = tile_n * BN + c * 32;
+          if (m < p.M && n0 < p.N) {
+            const size_t off = (size_t)m * p.ldo + n0;
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
               const float4 r = *reinterpret_cast<const float4*>(p.x_res + off + j);
@@ -280,14 +322,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
           }
         }
       } else {  // GEMM_QKV
-        const int hd = p.kv.head_dim;
         const int pos = m < p.M ? p.row_pos[m] : 0;
         const int b = m < p.M ? p.row_b[m] : 0;
-        for (int c = 0; c < TC_BN / 32; ++c) {
+        for (int c = 0; c < BN / 32; ++c) {
           float v[32];
           tmem_ld32(trow + c * 32, v);
           int map, row;
-          if (!b_half<GEMM_QKV>(p, tile_n, c >> 2, map, row) || m >= p.M) continue;
+          if (!b_half<GEMM_QKV, BN>(p, tile_n, c >> 2, map, row) || m >= p.M) continue;
           // q and the KV cache are bf16 whatever the weight type (the attention kernels read bf16)
           const int local = row + (c & 3) * 32;  // first column of the chunk inside its matrix
           const int head = local / hd, dim0 = local % hd;
@@ -319,13 +360,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
           }
         }
       }
+      // hand the accumulator buffer back to the MMA warp
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&tempty[acc])) : "memory");
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 5) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_BN) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * BN) : "memory");
   }
 }
 
@@ -367,9 +412,11 @@ bool make_tma_map(void* map_out, const void* base, uint64_t rows, uint64_t cols,
 template <typename WT>
 static cudaError_t gemm_tc_configure_t() {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  return cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_GATEUP, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  return cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
 }
 
 cudaError_t gemm_tc_configure() {
@@ -377,19 +424,32 @@ cudaError_t gemm_tc_configure() {
   return e != cudaSuccess ? e : gemm_tc_configure_t<f16>();
 }
 
+template <typename WT, int MODE, int BN>
+static cudaError_t gemm_tc_go(const TcMaps& maps, const GemmParams& p, int mt, int nt, int num_sms, int* err,
+                              cudaStream_t s) {
+  const int total = mt * nt;
+  const int grid = total < num_sms ? total : num_sms;
+  gemm_tc_kernel<WT, MODE, BN><<<grid, TC_THREADS, TC_SMEM, s>>>(maps, p, mt, nt, err);
+  return cudaGetLastError();
+}
+
+// 256-wide tiles unless that leaves most SMs idle (narrow N at small M).
 template <typename WT>
-static void gemm_tc_dispatch(const TcMaps& maps, const GemmParams& p, int mode, int mt, int* err, cudaStream_t s) {
-  if (mode == GEMM_GATEUP) {
-    gemm_tc_kernel<WT, GEMM_GATEUP><<<dim3(p.N / 128, mt), TC_THREADS, TC_SMEM, s>>>(maps, p, err);
-  } else if (mode == GEMM_RESID) {
-    gemm_tc_kernel<WT, GEMM_RESID><<<dim3(p.N / TC_BN, mt), TC_THREADS, TC_SMEM, s>>>(maps, p, err);
-  } else {
-    gemm_tc_kernel<WT, GEMM_QKV><<<dim3((p.N + TC_BN - 1) / TC_BN, mt), TC_THREADS, TC_SMEM, s>>>(maps, p, err);
+static cudaError_t gemm_tc_dispatch(const TcMaps& maps, const GemmParams& p, int mode, int mt, int num_sms, int* err,
+                                    cudaStream_t s) {
+  if (mode == GEMM_GATEUP) return gemm_tc_go<WT, GEMM_GATEUP, 256>(maps, p, mt, p.N / 128, num_sms, err, s);
+  const int nt256 = (p.N + 255) / 256;
+  const bool narrow = (long long)mt * nt256 * 4 < (long long)num_sms * 3;
+  if (mode == GEMM_RESID) {
+    if (narrow) return gemm_tc_go<WT, GEMM_RESID, 128>(maps, p, mt, (p.N + 127) / 128, num_sms, err, s);
+    return gemm_tc_go<WT, GEMM_RESID, 256>(maps, p, mt, nt256, num_sms, err, s);
   }
+  if (narrow) return gemm_tc_go<WT, GEMM_QKV, 128>(maps, p, mt, (p.N + 127) / 128, num_sms, err, s);
+  return gemm_tc_go<WT, GEMM_QKV, 256>(maps, p, mt, nt256, num_sms, err, s);
 }
 
 cudaError_t launch_gemm_tc(const void* a_map, const void* b0, const void* b1, const void* b2, const GemmParams& p,
-                           int mode, int wdt, int* err, cudaStream_t s) {
+                           int mode, int wdt, int num_sms, int* err, cudaStream_t s) {
   if (p.M <= 0) return cudaSuccess;
   TcMaps maps;
   memcpy(&maps.a, a_map, sizeof(CUtensorMap));
@@ -397,9 +457,8 @@ cudaError_t launch_gemm_tc(const void* a_map, const void* b0, const void* b1, co
   memcpy(&maps.b[1], b1 ? b1 : b0, sizeof(CUtensorMap));
   memcpy(&maps.b[2], b2 ? b2 : b0, sizeof(CUtensorMap));
   const int mt = (p.M + TC_BM - 1) / TC_BM;
-  if (wdt == WDT_F16) gemm_tc_dispatch<f16>(maps, p, mode, mt, err, s);
-  else gemm_tc_dispatch<bf16>(maps, p, mode, mt, err, s);
-  return cudaGetLastError();
+  return wdt == WDT_F16 ? gemm_tc_dispatch<f16>(maps, p, mode, mt, num_sms, err, s)
+                        : gemm_tc_dispatch<bf16>(maps, p, mode, mt, num_sms, err, s);
 }
 
 }  // namespace ladder

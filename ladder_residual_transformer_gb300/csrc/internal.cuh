@@ -126,9 +126,9 @@ struct GemvParams {
   const void* w1;    // QKV: wk, GATEUP: w_up
   const void* w2;    // QKV: wv
   int n_tasks;       // row pairs (QKV, RESID, LOGITS) or rows (GATEUP)
-  int kc;            // elements of K per streamed chunk (multiple of 256, divides K)
-  int nst;           // shared-memory ring stages
-  int* err;          // device error word (bit 2: pipeline wait timed out)
+  int kc;            // K chunk staged in shared memory (multiple of 256)
+  int ks;            // warps that split one task's K range (1, 2, 4, 8; > 1 only with a single chunk)
+  int* err;          // device error word
   float* out;        // QKV: q [B][ldo]; GATEUP: act [B][ldo]; RESID: x_out; LOGITS: logits
   int ldo;
   const float* x_res;  // RESID: residual rows [B][ldr]
@@ -203,7 +203,7 @@ cudaError_t launch_rmsnorm_rows(const float* x, int M, int d, const void* g, flo
 bool make_tma_map(void* map_out, const void* base, uint64_t rows, uint64_t cols, int wdt);
 cudaError_t gemm_tc_configure();
 cudaError_t launch_gemm_tc(const void* a_map, const void* b0, const void* b1, const void* b2, const GemmParams& p,
-                           int mode, int wdt, int* err, cudaStream_t s);
+                           int mode, int wdt, int num_sms, int* err, cudaStream_t s);
 // Tensor-core causal attention for packed prefill rows (mma.sync, bf16 Q/K/V).
 cudaError_t attn_prefill_configure();
 cudaError_t launch_attn_prefill_tc(const AttnPrefillParams& p, int hd, int wdt, int B, int max_len, cudaStream_t s);

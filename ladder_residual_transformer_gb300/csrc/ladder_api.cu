@@ -748,7 +748,7 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
       g.out_h = qb; g.ldo = qd; g.nq_hd = qd; g.nkv_hd = kvd;
       g.rope_cos = m->at<float>(P.rope_cos); g.rope_sin = m->at<float>(P.rope_sin);
       g.row_b = d_row_b; g.row_pos = d_row_pos; g.kv = kvl;
-      LAUNCH(launch_gemm_tc(&m->map_xn, &T.wq, &T.wk, &T.wv, g, GEMM_QKV, wdt, m->err(), s), 1);
+      LAUNCH(launch_gemm_tc(&m->map_xn, &T.wq, &T.wk, &T.wv, g, GEMM_QKV, wdt, m->num_sms, m->err(), s), 1);
 
       AttnPrefillParams a{};
       a.q = static_cast<const bf16*>(qb); a.kv = kvl; a.seq_start = d_start; a.seq_len = d_lens;
@@ -757,17 +757,17 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
 
       GemmParams o{};
       o.M = M; o.N = d; o.K = qd; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);
-      LAUNCH(launch_gemm_tc(&m->map_ao, &T.wo, nullptr, nullptr, o, GEMM_RESID, wdt, m->err(), s), 1);
+      LAUNCH(launch_gemm_tc(&m->map_ao, &T.wo, nullptr, nullptr, o, GEMM_RESID, wdt, m->num_sms, m->err(), s), 1);
     }
     {
       const int k = 2 * l + 2;
       LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.mlp_norm, c.norm_eps, xn, wdt, s), 1);
       GemmParams g{};
       g.M = M; g.N = f; g.K = d; g.out_h = actb; g.ldo = f;
-      LAUNCH(launch_gemm_tc(&m->map_xn, &T.gate, &T.up, nullptr, g, GEMM_GATEUP, wdt, m->err(), s), 1);
+      LAUNCH(launch_gemm_tc(&m->map_xn, &T.gate, &T.up, nullptr, g, GEMM_GATEUP, wdt, m->num_sms, m->err(), s), 1);
       GemmParams o{};
       o.M = M; o.N = d; o.K = f; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);
-      LAUNCH(launch_gemm_tc(&m->map_act, &T.down, nullptr, nullptr, o, GEMM_RESID, wdt, m->err(), s), 1);
+      LAUNCH(launch_gemm_tc(&m->map_act, &T.down, nullptr, nullptr, o, GEMM_RESID, wdt, m->num_sms, m->err(), s), 1);
     }
   }
   float* xlast = m->at<float>(P.xlast);
