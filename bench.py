@@ -288,7 +288,7 @@ def run_ours(args, dims):
         return n_pre + n_dec
 
     with torch.cuda.stream(stream):
-        model.set_mode(graph=True)
+        model.set_mode(graph=not args.eager, pdl=not args.no_pdl)
         for _ in range(args.warmup):
             step(record=False)
         stream.synchronize()
@@ -308,7 +308,7 @@ def run_ours(args, dims):
         clk = clocks.stop()
 
         # Dominant kernel: time each gate/up GEMV launch over one eager step's decode.
-        model.set_mode(graph=False)
+        model.set_mode(graph=False, pdl=not args.no_pdl)
         model.reset(stream)
         model.prefill(prompt_dev, lens, logits, tok, stream)
         model.probe_begin("gateup", args.decode * dims["n_layers"])
@@ -345,7 +345,7 @@ def run_ours(args, dims):
     e2e = None
     if not args.no_e2e:
         with torch.cuda.stream(stream):
-            model.set_mode(graph=True)
+            model.set_mode(graph=not args.eager, pdl=not args.no_pdl)
             model.generate(prompts, args.decode, stream)
             ts = []
             for _ in range(args.steps):
@@ -371,7 +371,8 @@ def run_ours(args, dims):
         "metric": METRIC, "value": decode_tps, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init weights, random tokens)",
-        "config": dict(workload_config(args, dims), parallelism=f"replicas x{world}"),
+        "config": dict(workload_config(args, dims), parallelism=f"replicas x{world}",
+                       decode_launch=("eager" if args.eager else "cuda graph") + (", no PDL" if args.no_pdl else ", PDL")),
         "decode": {"tok_s": decode_tps, "achieved_gbs": dec_gbs, "peak_gbs": peaks["hbm_gbs"],
                    "frac": dec_gbs / peaks["hbm_gbs"], "bytes_per_step": dec_bytes / args.decode},
         "prefill": {"value": prefill_tps, "unit": "tok/s", "ms": tot_pre / args.steps,
@@ -403,6 +404,8 @@ def main():
     ap.add_argument("--prompt", type=int, default=None)
     ap.add_argument("--decode", type=int, default=None)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-pdl", action="store_true", help="decode without programmatic dependent launch")
+    ap.add_argument("--eager", action="store_true", help="decode without CUDA-graph replay")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-prompt", type=int, default=None, help="oracle sample prompt (default: the workload's)")
     ap.add_argument("--cpu-decode", type=int, default=None, help="oracle sample decode steps (default: the workload's)")

@@ -95,7 +95,7 @@ typedef struct {
   float norm_eps;
   int32_t tie_embeddings;     /* 1: lm_head is the embedding table */
   int32_t rope_interleaved;   /* must be 1 (pairs (2j, 2j+1)) */
-  int32_t shard_k;            /* 1 = off; k > 1 splits each module into k shards summed on device */
+  int32_t shard_k;            /* 1 = off; 2, 4 or 8 = shard mode (see below) */
   int32_t page_size;          /* KV positions per page: 16, 32 or 64 */
   int32_t max_batch;          /* sequences per call, <= 64 */
   int32_t max_seq;            /* positions per sequence */
@@ -104,6 +104,18 @@ typedef struct {
   int32_t weight_dtype;       /* storage of weights and prefill tensor-core operands:
                                  LADDER_DTYPE_BF16 or LADDER_DTYPE_F16 */
 } ladder_config;
+
+/* Shard mode (shard_k = k > 1) stands in, on one GPU, for the tensor-parallel
+ * split of the Ladder Residual notes (关键设计: each module's output is an
+ * all-reduce of per-device partial sums).  In decode, the column-parallel
+ * projections (QKV, gate/up) are unchanged, and the row-parallel ones (O,
+ * down) produce k partial sums, one per block of n_q_heads/k heads or
+ * ffn_dim/k columns; a reduce kernel on a second stream adds them, in the
+ * fixed order 0..k-1, to the residual.  A ladder module does not wait for the
+ * previous module's reduce, so the reduce overlaps its GEMVs; a standard
+ * module waits for it.  Requires n_q_heads, n_kv_heads divisible by k and
+ * n_q_heads*head_dim/k, ffn_dim/k multiples of 256.  Prefill is unsharded (the
+ * same function, up to fp32 reassociation). */
 
 /* Weight storage types.  bf16-valued weights convert to fp16 exactly when
  * 2^-17 <= |w| <= 65504; with LADDER_DTYPE_F16 the prefill GEMM operands

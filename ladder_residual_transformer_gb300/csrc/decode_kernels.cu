@@ -95,40 +95,39 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
   pdl_trigger();
 
   // Weights depend on no earlier kernel: when every task of this CTA fits in
-  // one round of a single chunk, each warp requests the first 4 x 256 elements
-  // of both its rows before waiting for the previous kernel, so that their
-  // latency overlaps the previous kernel's tail.
-  const int ks_ = p.ks;
-  const int task0 = blockIdx.x * (GEMV_WARPS / ks_) + warp / ks_;
-  const bool one_round = p.kc >= K && (long long)gridDim.x * (GEMV_WARPS / ks_) >= p.n_tasks;
-  uint4 pre_a[4], pre_b[4];
-  int pre_k = -1;  // first k of the prefetched iteration, -1 if none
-  if (one_round && task0 < p.n_tasks) {
-    const WT* r0;
-    const WT* r1;
-    if (MODE == GEMV_QKV) {
-      const int q0 = 2 * task0;
-      r0 = q0 < p.nq_hd ? W0 + (size_t)q0 * K
-                        : (q0 < p.nq_hd + p.nkv_hd ? W1 + (size_t)(q0 - p.nq_hd) * K
-                                                   : W2 + (size_t)(q0 - p.nq_hd - p.nkv_hd) * K);
-      r1 = r0 + K;
-    } else if (MODE == GEMV_GATEUP) {
-      r0 = W0 + (size_t)task0 * K;
-      r1 = W1 + (size_t)task0 * K;
-    } else {
-      r0 = W0 + (size_t)(2 * task0) * K;
-      r1 = r0 + K;
-    }
-    const int kb = ks_ > 1 ? (warp % ks_) * (K / ks_) : 0;
-    const int ke = ks_ > 1 ? kb + K / ks_ : K;
-    const int k = kb + lane * 8;
-    if (k + 768 < ke) {
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        pre_a[s] = ld_stream_u4(r0 + k + 256 * s);
-        pre_b[s] = ld_stream_u4(r1 + k + 256 * s);
+  // one round of a single chunk, each warp asks L2 for its whole weight range
+  // before the RMSNorm prologue and before waiting for the previous kernel, so
+  // that the DRAM traffic overlaps both (no registers are held for it).
+  {
+    const int ks_ = p.ks;
+    const int task0 = blockIdx.x * (GEMV_WARPS / ks_) + warp / ks_;
+    const bool one_round = p.kc >= p.kfull && (long long)gridDim.x * (GEMV_WARPS / ks_) >= p.n_tasks;
+    if (one_round && task0 < p.n_tasks) {
+      const WT* r0;
+      const WT* r1;
+      if (MODE == GEMV_QKV) {
+        const int q0 = 2 * task0;
+        r0 = q0 < p.nq_hd ? W0 + (size_t)q0 * K
+                          : (q0 < p.nq_hd + p.nkv_hd ? W1 + (size_t)(q0 - p.nq_hd) * K
+                                                     : W2 + (size_t)(q0 - p.nq_hd - p.nkv_hd) * K);
+        r1 = r0 + K;
+      } else if (MODE == GEMV_GATEUP) {
+        r0 = W0 + (size_t)task0 * K;
+        r1 = W1 + (size_t)task0 * K;
+      } else if (MODE == GEMV_PARTIAL) {
+        r0 = W0 + (size_t)(2 * (task0 % p.shard_tasks)) * p.ldw + (size_t)(task0 / p.shard_tasks) * K;
+        r1 = r0 + p.ldw;
+      } else {
+        r0 = W0 + (size_t)(2 * task0) * K;
+        r1 = r0 + K;
       }
-      pre_k = k;
+      const int kb = ks_ > 1 ? (warp % ks_) * (K / ks_) : 0;
+      const int ke = ks_ > 1 ? kb + K / ks_ : K;
+      // one 128-byte line (64 elements) per lane per step
+      for (int k = kb + lane * 64; k < ke; k += 32 * 64) {
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(r0 + k));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(r1 + k));
+      }
     }
   }
   pdl_wait();
@@ -167,7 +166,8 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
   const int slot = warp / ks, kslice = warp % ks;
   const int total_slots = gridDim.x * tpc;
   const int rounds = (p.n_tasks + total_slots - 1) / total_slots;
-  const bool single_chunk = p.kc >= K;
+  const int KF = p.kfull;  // length of the staged input rows
+  const bool single_chunk = p.kc >= KF;
   const int kspan = K / ks;  // single chunk when ks > 1
   __shared__ float s_part[GEMV_WARPS][2][BT];
 
@@ -179,6 +179,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
     const WT* row0 = W0;
     const WT* row1 = W0;
     int local = 0, kind = 0;  // QKV: kind 0 = q, 1 = k, 2 = v; local = row inside its matrix
+    int koff = 0;             // PARTIAL: first input element of the task's shard
     if (active) {
       if (MODE == GEMV_QKV) {
         const int r0 = 2 * task;
@@ -193,6 +194,10 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
       } else if (MODE == GEMV_GATEUP) {
         row0 = W0 + (size_t)task * K;
         row1 = W1 + (size_t)task * K;
+      } else if (MODE == GEMV_PARTIAL) {
+        koff = (task / p.shard_tasks) * K;
+        row0 = W0 + (size_t)(2 * (task % p.shard_tasks)) * p.ldw + koff;
+        row1 = row0 + p.ldw;
       } else {
         row0 = W0 + (size_t)(2 * task) * K;
         row1 = row0 + K;
@@ -203,8 +208,8 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
 #pragma unroll
     for (int b = 0; b < BT; ++b) a0[b] = a1[b] = 0.f;
 
-    for (int k0 = 0; k0 < K; k0 += p.kc) {
-      const int kc = min(p.kc, K - k0);
+    for (int k0 = 0; k0 < KF; k0 += p.kc) {
+      const int kc = min(p.kc, KF - k0);
       if (!single_chunk || r == 0) {
         __syncthreads();
         // Stage the (normalised) input chunk in the two-plane layout.
@@ -229,19 +234,13 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
         __syncthreads();
       }
       if (active) {
+        // Weights: row + k0 + k; staged input: element koff + k (koff = 0 but for shard partials,
+        // which are single-chunk).
         const WT* p0 = row0 + k0;
         const WT* p1 = row1 + k0;
         const int kb = ks > 1 ? kslice * kspan : 0;
-        const int ke = ks > 1 ? kb + kspan : kc;
+        const int ke = ks > 1 ? kb + kspan : (MODE == GEMV_PARTIAL ? K : kc);
         int k = kb + lane * 8;
-        if (r == 0 && k0 == 0 && pre_k == k) {  // consume the loads issued before pdl_wait
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            gemv_fma<WT, BT>(pre_a[s], u, kc, k + 256 * s, a0);
-            gemv_fma<WT, BT>(pre_b[s], u, kc, k + 256 * s, a1);
-          }
-          k += 1024;
-        }
         for (; k + 768 < ke; k += 1024) {
           uint4 wa[4], wb[4];
 #pragma unroll
@@ -251,15 +250,15 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
           }
 #pragma unroll
           for (int s = 0; s < 4; ++s) {
-            gemv_fma<WT, BT>(wa[s], u, kc, k + 256 * s, a0);
-            gemv_fma<WT, BT>(wb[s], u, kc, k + 256 * s, a1);
+            gemv_fma<WT, BT>(wa[s], u, kc, koff + k + 256 * s, a0);
+            gemv_fma<WT, BT>(wb[s], u, kc, koff + k + 256 * s, a1);
           }
         }
         for (; k < ke; k += 256) {
           const uint4 wa = ld_stream_u4(p0 + k);
           const uint4 wb = ld_stream_u4(p1 + k);
-          gemv_fma<WT, BT>(wa, u, kc, k, a0);
-          gemv_fma<WT, BT>(wb, u, kc, k, a1);
+          gemv_fma<WT, BT>(wa, u, kc, koff + k, a0);
+          gemv_fma<WT, BT>(wb, u, kc, koff + k, a1);
         }
       }
     }
@@ -328,6 +327,11 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
         const size_t n = 2 * (size_t)task;
         p.out[(size_t)b * p.ldo + n] = p.x_res[(size_t)b * p.ldr + n] + v0;
         p.out[(size_t)b * p.ldo + n + 1] = p.x_res[(size_t)b * p.ldr + n + 1] + v1;
+      } else if (MODE == GEMV_PARTIAL) {
+        // out is [B][k][d]: shard s writes its partial sums at s * (2 * shard_tasks)
+        const size_t n = (size_t)(task / p.shard_tasks) * (2 * p.shard_tasks) + 2 * (size_t)(task % p.shard_tasks);
+        p.out[(size_t)b * p.ldo + n] = v0;
+        p.out[(size_t)b * p.ldo + n + 1] = v1;
       } else {
         const size_t n = 2 * (size_t)task;
         p.out[(size_t)b * p.ldo + n] = v0;
@@ -351,6 +355,7 @@ static cudaError_t set_gemv_attrs() {
   if ((e = cudaFuncSetAttribute(gemv_kernel<WT, BT, GEMV_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
   if ((e = cudaFuncSetAttribute(gemv_kernel<WT, BT, GEMV_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
   if ((e = cudaFuncSetAttribute(gemv_kernel<WT, BT, GEMV_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
+  if ((e = cudaFuncSetAttribute(gemv_kernel<WT, BT, GEMV_PARTIAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
   return cudaFuncSetAttribute(gemv_kernel<WT, BT, GEMV_LOGITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
@@ -371,6 +376,7 @@ static cudaError_t gemv_dispatch(const GemvParams& p, int mode, int grid, size_t
     case GEMV_QKV: return launch_k(gemv_kernel<WT, BT, GEMV_QKV>, g, b, smem, s, pdl, p);
     case GEMV_GATEUP: return launch_k(gemv_kernel<WT, BT, GEMV_GATEUP>, g, b, smem, s, pdl, p);
     case GEMV_RESID: return launch_k(gemv_kernel<WT, BT, GEMV_RESID>, g, b, smem, s, pdl, p);
+    case GEMV_PARTIAL: return launch_k(gemv_kernel<WT, BT, GEMV_PARTIAL>, g, b, smem, s, pdl, p);
     default: return launch_k(gemv_kernel<WT, BT, GEMV_LOGITS>, g, b, smem, s, pdl, p);
   }
 }
@@ -396,12 +402,18 @@ cudaError_t launch_gemv(const GemvParams& p0, int mode, int wdt, int num_sms, cu
     if (p0.pos) p.pos = p0.pos + b0;
     if (p0.kv.block_table) p.kv.block_table = p0.kv.block_table + (size_t)b0 * p0.kv.max_pages;
     const int bt = p.B <= 1 ? 1 : (p.B <= 2 ? 2 : 4);
-    p.kc = gemv_chunk(p.B, p.K);
+    if (mode != GEMV_PARTIAL) {
+      p.kfull = p.K;
+      p.ldw = p.K;
+      p.shard_tasks = p.n_tasks;
+    }
+    p.kc = gemv_chunk(p.B, p.kfull);
+    if (mode == GEMV_PARTIAL && p.kc < p.kfull) return cudaErrorInvalidValue;  // shard partials stage one chunk
     const size_t smem = (size_t)bt * p.kc * sizeof(float);
     // K split: the smallest that gives at least 1.5 CTAs per SM (more warps in
     // flight for short, wide matrices) while each slice stays a multiple of 256.
     p.ks = 1;
-    if (p.kc >= p.K) {
+    if (p.kc >= p.kfull) {
       while (p.ks < GEMV_WARPS && (long long)p.n_tasks * p.ks < (long long)num_sms * 12 &&
              (p.K / (2 * p.ks)) % 256 == 0)
         p.ks *= 2;
@@ -699,6 +711,31 @@ __global__ void advance_kernel(int* seq_lens, int B) {
   pdl_wait();
   const int b = threadIdx.x;
   if (b < B) seq_lens[b] += 1;
+}
+
+// x_out[b, n] = x_res[b, n] + sum_s part[b][s][n] (fixed order): the on-device
+// stand-in for the all-reduce of tensor parallelism in shard mode.
+__global__ void shard_reduce_kernel(const float* __restrict__ part, int k, int d, const float* __restrict__ x_res,
+                                    float* __restrict__ x_out) {
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.y;
+  const int n = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (n >= d) return;
+  float4 acc = *reinterpret_cast<const float4*>(x_res + (size_t)b * d + n);
+  const float* pb = part + (size_t)b * k * d + n;
+  for (int s = 0; s < k; ++s) {
+    const float4 v = *reinterpret_cast<const float4*>(pb + (size_t)s * d);
+    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+  }
+  *reinterpret_cast<float4*>(x_out + (size_t)b * d + n) = acc;
+}
+
+cudaError_t launch_shard_reduce(const float* part, int k, int B, int d, const float* x_res, float* x_out,
+                                cudaStream_t s, bool pdl) {
+  const int threads = 128;
+  return launch_k(shard_reduce_kernel, dim3((d / 4 + threads - 1) / threads, B), dim3(threads), 0, s, pdl, part, k,
+                  d, x_res, x_out);
 }
 
 cudaError_t launch_advance(int* seq_lens, int B, cudaStream_t s, bool pdl) {

@@ -114,7 +114,7 @@ struct KvLayer {
   }
 };
 
-enum GemvMode { GEMV_QKV = 0, GEMV_GATEUP = 1, GEMV_RESID = 2, GEMV_LOGITS = 3 };
+enum GemvMode { GEMV_QKV = 0, GEMV_GATEUP = 1, GEMV_RESID = 2, GEMV_LOGITS = 3, GEMV_PARTIAL = 4 };
 
 struct GemvParams {
   const float* x;    // input rows [B][ldx] fp32
@@ -129,6 +129,10 @@ struct GemvParams {
   int kc;            // K chunk staged in shared memory (multiple of 256)
   int ks;            // warps that split one task's K range (1, 2, 4, 8; > 1 only with a single chunk)
   int* err;          // device error word
+  // Row-parallel shard partials (GEMV_PARTIAL): K is one shard's depth, kfull
+  // the whole input row, ldw the weight row stride; task t is row pair
+  // t % shard_tasks of shard t / shard_tasks.  Other modes: kfull = ldw = K.
+  int kfull, ldw, shard_tasks;
   float* out;        // QKV: q [B][ldo]; GATEUP: act [B][ldo]; RESID: x_out; LOGITS: logits
   int ldo;
   const float* x_res;  // RESID: residual rows [B][ldr]
@@ -210,5 +214,8 @@ cudaError_t launch_attn_prefill_tc(const AttnPrefillParams& p, int hd, int wdt, 
 cudaError_t launch_gather_rows(const float* x, int d, const int* rows, int B, float* out,
                                cudaStream_t s);
 cudaError_t launch_set_lens(const int* lens, int B, int* seq_lens, cudaStream_t s);
+// x_out[b, n] = x_res[b, n] + sum_{s < k} part[b][s][n], summed in the fixed order s = 0..k-1.
+cudaError_t launch_shard_reduce(const float* part, int k, int B, int d, const float* x_res, float* x_out,
+                                cudaStream_t s, bool pdl);
 
 }  // namespace ladder

@@ -51,7 +51,7 @@ constexpr int kSplitLen = 128;      // keys per decode-attention split
 constexpr int kArgmaxBlocks = 64;   // partial argmax blocks per sequence
 
 struct Plan {
-  size_t x[3], xn, q, ao, act, part_o, part_ml, am_v, am_i, rope_cos, rope_sin, meta, xlast, err;
+  size_t x[3], xn, q, ao, act, part_o, part_ml, am_v, am_i, rope_cos, rope_sin, meta, xlast, err, shard;
   size_t total;
   int m_max, m_pad, nsplit_max;
 };
@@ -85,6 +85,7 @@ Plan make_plan(const ladder_config& c) {
   p.meta = take((2 * M + 3 * Bm) * 4);
   p.xlast = take(Bm * d * 4);
   p.err = take(256);
+  p.shard = c.shard_k > 1 ? take(2 * Bm * c.shard_k * d * 4) : 0;  // double-buffered shard partials [B][k][d]
   p.total = off;
   return p;
 }
@@ -111,7 +112,17 @@ int validate_config(const ladder_config* c) {
   if (!(c->norm_eps > 0.0f) || !std::isfinite(c->norm_eps)) return fail(LADDER_ERR_INVALID, "norm_eps must be > 0");
   if (c->rope_interleaved != 1)
     return fail(LADDER_ERR_UNSUPPORTED, "only interleaved rotary pairs (rope_interleaved=1) are implemented");
-  if (c->shard_k != 1) return fail(LADDER_ERR_UNSUPPORTED, "shard_k=%d: shard mode is not built yet", c->shard_k);
+  if (c->shard_k != 1 && c->shard_k != 2 && c->shard_k != 4 && c->shard_k != 8)
+    return fail(LADDER_ERR_INVALID, "shard_k=%d must be 1, 2, 4 or 8", c->shard_k);
+  if (c->shard_k > 1) {
+    const int k = c->shard_k;
+    if (c->n_q_heads % k || c->n_kv_heads % k)
+      return fail(LADDER_ERR_INVALID, "shard_k=%d must divide n_q_heads and n_kv_heads", k);
+    if ((c->n_q_heads * c->head_dim / k) % 256 || (c->ffn_dim / k) % 256 || c->ffn_dim % k)
+      return fail(LADDER_ERR_UNSUPPORTED, "shard_k=%d: per-shard O and down depths must be multiples of 256", k);
+    if ((size_t)c->ffn_dim * 4 > 64 * 1024)
+      return fail(LADDER_ERR_UNSUPPORTED, "shard mode stages whole ffn rows: ffn_dim <= 16384 required");
+  }
   if (c->page_size != 16 && c->page_size != 32 && c->page_size != 64)
     return fail(LADDER_ERR_INVALID, "page_size=%d must be 16, 32 or 64", c->page_size);
   if (c->max_batch <= 0 || c->max_batch > 64) return fail(LADDER_ERR_INVALID, "max_batch=%d must be in 1..64", c->max_batch);
@@ -168,6 +179,7 @@ struct ladder_model {
   cudaStream_t aux = nullptr;
   cudaEvent_t ev_slot[3] = {nullptr, nullptr, nullptr};
   cudaEvent_t ev_fork = nullptr;
+  cudaEvent_t ev_part = nullptr;  // shard mode: partial sums of a module written
   // launch probe
   int probe_class = -1;
   int probe_count = 0;
@@ -331,6 +343,7 @@ int ladder_create(const ladder_config* cfg, const ladder_weights* w, void* works
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&m->aux, cudaStreamNonBlocking);
   for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&m->ev_slot[i], cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_part, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaMemsetAsync(m->err(), 0, 256, stream);
   if (e == cudaSuccess)
     e = launch_rope_tables(m->at<float>(plan.rope_cos), m->at<float>(plan.rope_sin), cfg->max_seq, cfg->head_dim,
@@ -350,6 +363,7 @@ void ladder_destroy(ladder_model* m) {
   for (auto& e : m->ev_slot)
     if (e) cudaEventDestroy(e);
   if (m->ev_fork) cudaEventDestroy(m->ev_fork);
+  if (m->ev_part) cudaEventDestroy(m->ev_part);
   if (m->aux) cudaStreamDestroy(m->aux);
   delete m;
 }
@@ -521,8 +535,92 @@ namespace {
 // the write-after-read order on a reused buffer follows from these read
 // dependencies (the module that overwrites x_{k-3} has already waited for a
 // buffer written after every reader of x_{k-3}).
+// Shard-mode decode step (shard_k > 1).  Every GEMV and attention kernel runs on
+// the caller's stream; the per-module reduce of the k partial sums runs on the
+// second stream.  A module's first kernel waits for the reduce that produced
+// its input, which in a ladder layer is the reduce of the module two back, so
+// the previous module's reduce overlaps this module's weight streaming; in a
+// standard layer it is the previous module's reduce, which serialises them.
+// The partial buffers alternate between modules; module k rewrites the buffer
+// of module k-2 only after its first kernel has waited for a reduce at least
+// as late as module k-2's.
+int enqueue_decode_shard(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B, float* logits,
+                         int32_t* next_tok, int nsplit, cudaStream_t s) {
+  const ladder_config& c = m->cfg;
+  const int d = c.d_model, qd = c.n_q_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim, f = c.ffn_dim;
+  const int ksh = c.shard_k;
+  const Plan& P = m->plan;
+  float* q = m->at<float>(P.q);
+  float* ao = m->at<float>(P.ao);
+  float* act = m->at<float>(P.act);
+  float* part = m->at<float>(P.shard);
+  const size_t part_stride = (size_t)B * ksh * d;
+  const bool pdl = !(m->flags & LADDER_FLAG_NO_PDL);
+  cudaStream_t rs = m->aux;
+  int writer[3] = {0, 0, 0};  // 0: caller's stream (embed), 1: reduce stream
+  auto use = [&](int buf) -> int {
+    if (writer[buf % 3] == 1) CUDA_TRY(cudaStreamWaitEvent(s, m->ev_slot[buf % 3], 0));
+    return LADDER_OK;
+  };
+
+  LAUNCH(launch_embed(tokens, B, m->embed, m->wdt, d, c.vocab, m->X(0), m->err(), s, pdl), 1);
+  CUDA_TRY(cudaEventRecord(m->ev_slot[0], s));
+  int rc;
+  for (int k = 1; k <= 2 * c.n_layers; ++k) {
+    const int l = (k - 1) / 2;
+    const LayerW& L = m->layers[l];
+    const int j = m->input_index(k);
+    if ((rc = use(j))) return rc;
+    float* pk = part + (size_t)(k & 1) * part_stride;
+    GemvParams o{};
+    if (k & 1) {  // attention module
+      const KvLayer kvl = kv->layer(l);
+      GemvParams g{};
+      g.x = m->X(j); g.ldx = d; g.g = L.attn_norm; g.eps = c.norm_eps; g.B = B; g.K = d;
+      g.w0 = L.wq; g.w1 = L.wk; g.w2 = L.wv; g.n_tasks = (qd + 2 * kvd) / 2;
+      g.out = q; g.ldo = qd; g.nq_hd = qd; g.nkv_hd = kvd;
+      g.rope_cos = m->at<float>(P.rope_cos); g.rope_sin = m->at<float>(P.rope_sin);
+      g.pos = kv->seq_lens; g.kv = kvl; g.err = m->err();
+      LAUNCH(launch_gemv(g, GEMV_QKV, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, g.K));
+      AttnDecodeParams a{};
+      a.q = q; a.kv = kvl; a.seq_lens = kv->seq_lens; a.n_q = c.n_q_heads; a.split_len = kSplitLen;
+      a.nsplit = nsplit; a.scale = 1.0f / sqrtf((float)c.head_dim);
+      a.part_o = m->at<float>(P.part_o); a.part_ml = m->at<float>(P.part_ml); a.out = ao;
+      LAUNCH(launch_attn_decode(a, B, c.n_kv_heads, c.head_dim, s, pdl), 2);
+      o.x = ao; o.ldx = qd; o.K = qd / ksh; o.kfull = qd; o.ldw = qd; o.w0 = L.wo;
+    } else {  // MLP module
+      GemvParams g{};
+      g.x = m->X(j); g.ldx = d; g.g = L.mlp_norm; g.eps = c.norm_eps; g.B = B; g.K = d;
+      g.w0 = L.w_gate; g.w1 = L.w_up; g.n_tasks = f; g.out = act; g.ldo = f; g.err = m->err();
+      LAUNCH(launch_gemv(g, GEMV_GATEUP, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, g.K));
+      o.x = act; o.ldx = f; o.K = f / ksh; o.kfull = f; o.ldw = f; o.w0 = L.w_down;
+    }
+    // row-parallel partial sums: shard sh uses input block sh and writes part[b][sh][:]
+    o.g = nullptr; o.B = B; o.shard_tasks = d / 2; o.n_tasks = ksh * (d / 2);
+    o.out = pk; o.ldo = ksh * d; o.err = m->err();
+    LAUNCH(launch_gemv(o, GEMV_PARTIAL, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, o.kfull));
+    CUDA_TRY(cudaEventRecord(m->ev_part, s));
+    // the "all-reduce": x_k = x_{k-1} + sum of the partials, on the second stream
+    CUDA_TRY(cudaStreamWaitEvent(rs, m->ev_part, 0));
+    if (writer[(k - 1) % 3] == 0) CUDA_TRY(cudaStreamWaitEvent(rs, m->ev_slot[(k - 1) % 3], 0));
+    LAUNCH(launch_shard_reduce(pk, ksh, B, d, m->X(k - 1), m->X(k), rs, pdl), 1);
+    CUDA_TRY(cudaEventRecord(m->ev_slot[k % 3], rs));
+    writer[k % 3] = 1;
+  }
+  if ((rc = use(2 * c.n_layers))) return rc;
+  GemvParams h{};
+  h.x = m->X(2 * c.n_layers); h.ldx = d; h.g = m->final_norm; h.eps = c.norm_eps; h.B = B; h.K = d;
+  h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.out = logits; h.ldo = c.vocab; h.err = m->err();
+  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, h.K));
+  if (next_tok)
+    LAUNCH(launch_argmax(logits, B, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i), kArgmaxBlocks, next_tok, s, pdl), 2);
+  LAUNCH(launch_advance(kv->seq_lens, B, s, pdl), 1);
+  return LADDER_OK;
+}
+
 int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B, float* logits,
                    int32_t* next_tok, int nsplit, cudaStream_t s) {
+  if (m->cfg.shard_k > 1) return enqueue_decode_shard(m, kv, tokens, B, logits, next_tok, nsplit, s);
   const ladder_config& c = m->cfg;
   const int d = c.d_model, qd = c.n_q_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim, f = c.ffn_dim;
   const Plan& P = m->plan;

@@ -222,11 +222,11 @@ class LadderModel:
 
     def __init__(self, dims: dict, weights: dict, *, max_batch: int, max_seq: int,
                  max_prefill_tokens: int | None = None, page_size: int = 64, strict_boundary: int = 0,
-                 page_order=None, kv_fill_bits: int | None = None, stream=None):
+                 page_order=None, kv_fill_bits: int | None = None, stream=None, shard_k: int = 1):
         self.dims = dict(dims)
         self.weights = weights
         self.cfg = make_config(dims, max_batch=max_batch, max_seq=max_seq, max_prefill_tokens=max_prefill_tokens,
-                               page_size=page_size, strict_boundary=strict_boundary,
+                               page_size=page_size, strict_boundary=strict_boundary, shard_k=shard_k,
                                dtype=weights.get("dtype", "bf16"))
         L = lib()
         ws_bytes, self.page_bytes = query_sizes(self.cfg)
@@ -277,6 +277,7 @@ class LadderModel:
     def set_mode(self, standard: bool = False, graph: bool = False, pdl: bool = True):
         flags = (FLAG_DECODE_GRAPH if graph else 0) | (0 if pdl else FLAG_NO_PDL)
         check(lib().ladder_set_mode(self._m, RESIDUAL_STANDARD if standard else RESIDUAL_CONFIG, flags))
+        self._standard = standard
 
     # -- forward ---------------------------------------------------------
     def prefill(self, tokens: torch.Tensor, lens, logits: torch.Tensor | None = None,

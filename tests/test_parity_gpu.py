@@ -25,11 +25,11 @@ def tiny():
     return dims, gpu_weights(dims), oracle_weights(dims)
 
 
-def run_teacher_forced(model, prompts, feed, graph=False):
+def run_teacher_forced(model, prompts, feed, graph=False, standard=None):
     """Prefill then decode feeding feed[:, s]; returns logits [S+1, B, V] and greedy tokens."""
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
-        model.set_mode(graph=graph)
+        model.set_mode(graph=graph, standard=getattr(model, "_standard", False) if standard is None else standard)
         logits, nxt = model.prefill(packed(prompts), [len(p) for p in prompts])
         out, toks = [logits.cpu().numpy()], [nxt.cpu().numpy()]
         tok_dev = torch.empty(len(prompts), dtype=torch.int32, device="cuda")
@@ -262,3 +262,35 @@ def test_full_size_1p2b_prefill_and_decode():
     o_logits, _ = O.teacher_forced_decode(dims, O.synthetic_weights(dims), prompts, feed)
     errs = [compare_logits(g_logits[s], o_logits[s], f"1.2B step {s}")[0] for s in range(4)]
     check_greedy(g_toks[:, 0], o_logits[:, 0], 2 * max(errs))
+
+
+@pytest.mark.parametrize("k,standard,graph", [(2, False, False), (2, True, True), (4, False, True), (4, True, False)])
+def test_shard_mode_matches_oracle(k, standard, graph):
+    """Shard mode: row-parallel partial sums reduced on a second stream (ladder or standard schedule)."""
+    if k == 2:
+        dims = small_dims(d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=3072, vocab=2048)
+    else:
+        dims = small_dims(d_model=1024, n_q_heads=16, n_kv_heads=4, head_dim=64, ffn_dim=4096, vocab=2048)
+    gw = gpu_weights(dims)
+    odims = dict(dims, n_standard_layers=dims["n_layers"]) if standard else dims
+    ow = oracle_weights(odims)
+    lens = [40, 9]
+    prompts = prompts_for(lens, dims["vocab"])
+    feed = np.stack([synth.tokens(4, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(2)])
+    model = make_model(dims, gw, max_batch=2, max_seq=64, page_size=32, shard_k=k)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        model.set_mode(standard=standard, graph=graph)
+    g_logits, _ = run_teacher_forced(model, prompts, feed, graph=graph)
+    o_logits, _ = O.teacher_forced_decode(odims, ow, prompts, feed)
+    for s_ in range(5):
+        compare_logits(g_logits[s_], o_logits[s_], f"shard k={k} standard={standard} step {s_}")
+
+
+def test_shard_config_is_validated():
+    dims = small_dims(d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=3072, vocab=2048)
+    gw = gpu_weights(dims)
+    for k, code in ((3, ladder.LADDER_ERR_INVALID), (4, ladder.LADDER_ERR_INVALID)):
+        with pytest.raises(ladder.LadderError) as e:
+            make_model(dims, gw, max_batch=1, max_seq=32, shard_k=k)
+        assert e.value.code == code
