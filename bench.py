@@ -262,8 +262,9 @@ def run_ours(args, dims):
     weights = ladder.synthetic_weights(dims, device=dev)
     B = args.batch
     lens = [args.prompt] * B
+    shard_k = synth.RUNS[args.workload].get("shard_k", 1) if args.shard_k is None else args.shard_k
     model = ladder.LadderModel(dims, weights, max_batch=B, max_seq=args.prompt + args.decode + 1,
-                               max_prefill_tokens=sum(lens))
+                               max_prefill_tokens=sum(lens), shard_k=shard_k)
     prompts = [synth.tokens(n, dims["vocab"], stream=b) for b, n in enumerate(lens)]
     prompt_dev = torch.from_numpy(np.concatenate(prompts).astype(np.int32)).to(dev)
     stream = torch.cuda.Stream(device=dev)
@@ -316,6 +317,24 @@ def run_ours(args, dims):
             model.decode_step(tok, logits, tok, stream)
         n_probe, probe_ms = model.probe_end()
         stream.synchronize()
+
+    # Shard mode: the same decode with the standard residual schedule, where each
+    # module waits for the previous module's reduce (the pages' comparison).
+    shard = None
+    if shard_k > 1:
+        std_ms = []
+        with torch.cuda.stream(stream):
+            model.set_mode(standard=True, graph=not args.eager, pdl=not args.no_pdl)
+            for i in range(args.warmup + args.steps):
+                step(record=True)
+                stream.synchronize()
+                if i >= args.warmup:
+                    std_ms.append(ev[1].elapsed_time(ev[2]))
+            model.set_mode(standard=False, graph=not args.eager, pdl=not args.no_pdl)
+        std_tps = B * args.decode * len(std_ms) / (sum(std_ms) / 1e3)
+        shard = {"k": shard_k, "ladder_decode_tok_s": B * args.decode * args.steps / (sum(dec_ms) / 1e3),
+                 "standard_decode_tok_s": std_tps,
+                 "note": "same weights and kernels; standard = every module waits for the previous module's reduce"}
 
     tot_pre, tot_dec = sum(pre_ms), sum(dec_ms)
     tot_pre, tot_dec = max_over_ranks([tot_pre, tot_dec], world, dev)
@@ -385,7 +404,7 @@ def run_ours(args, dims):
                      "timing": "CUDA events on the launching stream around each launch, one eager "
                                "step's decode right after the timed region"},
         "peaks": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'fallback 6.8 TB/s, 1.9 PF bf16'})",
-        "gpu_launches": launches, "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+        "gpu_launches": launches, "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "shard": shard,
         "wall_s": wall,
     }
     if rank == 0:
@@ -401,6 +420,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="1.2b", choices=sorted(synth.PRESETS))
     ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--shard-k", type=int, default=None, help="shard mode k (default: the workload's)")
     ap.add_argument("--prompt", type=int, default=None)
     ap.add_argument("--decode", type=int, default=None)
     ap.add_argument("--no-e2e", action="store_true")

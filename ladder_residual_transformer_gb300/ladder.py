@@ -133,47 +133,42 @@ def _stream_handle(stream) -> int:
     return stream.cuda_stream
 
 
-def synthetic_weights(dims: dict, device="cuda", seed: int = 0, transform=None, chunk: int = 1 << 26,
-                      dtype: str = "fp16") -> dict:
-    """Random-init weights of the seeded generator, uploaded tensor by tensor.
+def synthetic_weights(dims: dict, device="cuda", seed: int = 0, transform=None, dtype: str = "fp16") -> dict:
+    """Random-init weights of the seeded generator, produced on the device.
 
-    The generator yields bf16 values.  With dtype="fp16" each tensor is
-    converted on the device (round to nearest even), which is exact for
-    2^-17 <= |w| <= 65504, i.e. for all but a few hundredths of a percent of
-    N(0, 0.02) values, whose error is below 3e-8.
+    The device twin of the generator writes the same bf16 bits as the host code
+    (tests check this); with dtype="fp16" each tensor is then converted on the
+    device (round to nearest even), which is exact for 2^-17 <= |w| <= 65504,
+    i.e. for all but a few hundredths of a percent of N(0, 0.02) values, whose
+    error is below 3e-8.  ``transform(name, layer, np_bits) -> np_bits`` edits
+    a tensor's bf16 bits on the host first (small tensors only).
     Returns {"embed": T, "final_norm": T, "lm_head": T or None, "layers": [dict], "dtype": str}.
-    ``transform(name, layer, np_bits) -> np_bits`` may edit a tensor's bf16 bits first.
     """
     from . import synth
 
     tdt = {"bf16": torch.bfloat16, "fp16": torch.float16}[dtype]
-    pinned = torch.empty(chunk, dtype=torch.int16, pin_memory=True)
-    staging = pinned.numpy().view(np.uint16)
-    tmp = torch.empty(chunk, dtype=torch.int16, device=device)
+    stream = torch.cuda.current_stream(device)
 
-    def upload(name, layer):
+    def make(name, layer):
         shape = synth.tensor_shape(dims, name)
         n = int(np.prod(shape))
-        t = torch.empty(n, dtype=tdt, device=device)
-        bits = None
+        raw = torch.empty(n, dtype=torch.int16, device=device)
         if transform is not None:
             bits = np.ascontiguousarray(transform(name, layer, synth.gen_tensor(dims, name, layer, seed=seed)))
-        for off in range(0, n, chunk):
-            cnt = min(chunk, n - off)
-            if bits is None:
-                synth.gen_tensor(dims, name, layer, seed=seed, out=staging, offset=off, count=cnt)
-            else:
-                staging[:cnt] = bits[off:off + cnt]
-            tmp[:cnt].copy_(pinned[:cnt], non_blocking=True)
-            t[off:off + cnt].copy_(tmp[:cnt].view(torch.bfloat16))
-            torch.cuda.current_stream(device).synchronize()
+            raw.copy_(torch.from_numpy(bits.view(np.int16)))
+        elif name in synth.NORM_KINDS:
+            raw.fill_(0x3F80)
+        else:
+            synth.gen_tensor_device(dims, name, layer, raw.data_ptr(), seed=seed, stream_ptr=stream.cuda_stream)
+        t = raw.view(torch.bfloat16) if tdt == torch.bfloat16 else raw.view(torch.bfloat16).to(tdt)
         return t.view(shape)
 
-    out = {"embed": upload("embed", -1), "final_norm": upload("final_norm", -1),
-           "lm_head": None if dims.get("tie_embeddings") else upload("lm_head", -1), "layers": [],
+    out = {"embed": make("embed", -1), "final_norm": make("final_norm", -1),
+           "lm_head": None if dims.get("tie_embeddings") else make("lm_head", -1), "layers": [],
            "dtype": dtype}
     for l in range(dims["n_layers"]):
-        out["layers"].append({k: upload(k, l) for k in synth.LAYER_KINDS})
+        out["layers"].append({k: make(k, l) for k in synth.LAYER_KINDS})
+    torch.cuda.synchronize(device)
     return out
 
 

@@ -26,7 +26,10 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "synth.c")
 _LIB_PATH = os.path.join(_HERE, "libladder_synth.so")
+_CU_SRC = os.path.join(_HERE, "synth_cuda.cu")
+_CU_LIB_PATH = os.path.join(_HERE, "libladder_synth_cuda.so")
 _lib = None
+_cu_lib = None
 _lock = threading.Lock()
 
 
@@ -42,6 +45,33 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def build_cuda(force: bool = False) -> str:
+    """Compile the device twin of the generator (sm_103a)."""
+    if not force and os.path.exists(_CU_LIB_PATH) and os.path.getmtime(_CU_LIB_PATH) >= os.path.getmtime(_CU_SRC):
+        return _CU_LIB_PATH
+    import shutil
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_HERE)
+    os.close(fd)
+    cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-shared", "-Xcompiler", "-fPIC",
+           "-o", tmp, _CU_SRC]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _CU_LIB_PATH)
+    return _CU_LIB_PATH
+
+
+def _load_cuda():
+    global _cu_lib
+    with _lock:
+        if _cu_lib is None:
+            lib = ctypes.CDLL(build_cuda())
+            lib.synth_normal_bf16_device.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
+                                                     ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
+            lib.synth_normal_bf16_device.restype = ctypes.c_int
+            _cu_lib = lib
+    return _cu_lib
+
+
 def _load():
     global _lib
     with _lock:
@@ -50,12 +80,16 @@ def _load():
             u64, u32, f32 = ctypes.c_uint64, ctypes.c_uint32, ctypes.c_float
             lib.synth_normal_bf16.argtypes = [u64, u64, u64, u64, f32, ctypes.c_void_p]
             lib.synth_normal_bf16.restype = None
+            lib.synth_normal_f32.argtypes = [u64, u64, u64, u64, f32, ctypes.c_void_p]
+            lib.synth_normal_f32.restype = None
             lib.synth_tokens.argtypes = [u64, u64, u64, u64, u32, ctypes.c_void_p]
             lib.synth_tokens.restype = None
             lib.synth_mix64.argtypes = [u64]
             lib.synth_mix64.restype = u64
             lib.synth_normal_scale.argtypes = [f32]
             lib.synth_normal_scale.restype = f32
+            lib.synth_stream_key.argtypes = [u64, u64]
+            lib.synth_stream_key.restype = u64
             _lib = lib
     return _lib
 
@@ -140,6 +174,20 @@ def gen_tensor(dims: dict, name: str, layer: int = -1, seed: int = WEIGHT_SEED,
     return out[:count]
 
 
+def gen_tensor_f32(dims: dict, name: str, layer: int = -1, seed: int = WEIGHT_SEED) -> np.ndarray:
+    """The same values as gen_tensor, widened exactly to fp32, shaped like the tensor."""
+    if name == "lm_head" and dims.get("tie_embeddings"):
+        name = "embed"
+    shape = tensor_shape(dims, name)
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.float32)
+    if name in NORM_KINDS:
+        out[:] = 1.0
+    else:
+        _load().synth_normal_f32(seed, tensor_id(name, layer), 0, n, INIT_STD, out.ctypes.data)
+    return out.reshape(shape)
+
+
 def tokens(n: int, vocab: int, seed: int = PROMPT_SEED, stream: int = 0, offset: int = 0) -> np.ndarray:
     """n uniform token ids in [0, vocab) for sequence `stream`."""
     out = np.empty(n, dtype=np.int32)
@@ -169,4 +217,20 @@ def param_count(dims: dict) -> int:
         n += int(np.prod(tensor_shape(dims, "lm_head")))
     for name in LAYER_KINDS:
         n += dims["n_layers"] * int(np.prod(tensor_shape(dims, name)))
+    return n
+
+
+def gen_tensor_device(dims: dict, name: str, layer: int, out_ptr: int, seed: int = WEIGHT_SEED,
+                      stream_ptr: int = 0) -> int:
+    """Write the bf16 bits of a weight tensor into device memory at out_ptr
+    (the same bits as gen_tensor); returns the element count."""
+    if name == "lm_head" and dims.get("tie_embeddings"):
+        name = "embed"
+    n = int(np.prod(tensor_shape(dims, name)))
+    if name in NORM_KINDS:
+        raise ValueError("norm gains are constant; fill them directly")
+    key = int(_load().synth_stream_key(seed, tensor_id(name, layer)))
+    rc = _load_cuda().synth_normal_bf16_device(key, 0, n, normal_scale(INIT_STD), out_ptr, stream_ptr)
+    if rc != 0:
+        raise RuntimeError(f"device generator launch failed ({rc})")
     return n

@@ -73,6 +73,28 @@ void synth_normal_bf16(uint64_t seed, uint64_t tensor_id, uint64_t offset, uint6
   }
 }
 
+/* out[j] = fp32 value of the same sample as synth_normal_bf16 (exact widening of the bf16 bits). */
+void synth_normal_f32(uint64_t seed, uint64_t tensor_id, uint64_t offset, uint64_t n, float std, float* out) {
+  const uint64_t key = stream_key(seed, tensor_id);
+  const float scale = synth_normal_scale(std);
+  int64_t nn = (int64_t)n;
+#pragma omp parallel for schedule(static)
+  for (int64_t j = 0; j < nn; ++j) {
+    uint64_t i = offset + (uint64_t)j;
+    uint64_t h0 = mix64(key + 2 * i);
+    uint64_t h1 = mix64(key + 2 * i + 1);
+    int64_t s = 0;
+    for (int b = 0; b < 4; ++b) {
+      s += (int64_t)((h0 >> (16 * b)) & 0xFFFFu);
+      s += (int64_t)((h1 >> (16 * b)) & 0xFFFFu);
+    }
+    int32_t c = (int32_t)(s - 4 * 65535);
+    union { float f; uint32_t u; } v;
+    v.u = (uint32_t)f32_to_bf16_rne((float)c * scale) << 16;
+    out[j] = v.f;
+  }
+}
+
 /* out[j] = token number (offset + j) of stream `stream_id` under `seed`, in [0, vocab). */
 void synth_tokens(uint64_t seed, uint64_t stream_id, uint64_t offset, uint64_t n,
                   uint32_t vocab, int32_t* out) {
@@ -84,6 +106,9 @@ void synth_tokens(uint64_t seed, uint64_t stream_id, uint64_t offset, uint64_t n
     out[j] = (int32_t)(mix64(key + i) % (uint64_t)vocab);
   }
 }
+
+/* Stream key of (seed, tensor id), for the device twin of the generator. */
+uint64_t synth_stream_key(uint64_t seed, uint64_t tensor_id) { return stream_key(seed, tensor_id); }
 
 /* Plain SplitMix64 output function, exported so tests can check it against its definition. */
 uint64_t synth_mix64(uint64_t z) { return mix64(z); }

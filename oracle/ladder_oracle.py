@@ -126,8 +126,7 @@ def synthetic_weights(dims: dict, seed: int = synth.WEIGHT_SEED, dtype=np.float3
     modules with it).
     """
     def source(name, layer):
-        bits = synth.gen_tensor(dims, name, layer, seed=seed)
-        a = synth.bf16_bits_to_f32(bits).reshape(synth.tensor_shape(dims, name))
+        a = synth.gen_tensor_f32(dims, name, layer, seed=seed)
         if transform is not None:
             a = transform(name, layer, a)
         return a

@@ -65,3 +65,11 @@ def test_param_counts_match_named_sizes():
     assert abs(synth.param_count(synth.PRESETS["1.2b"]) / 1e9 - 1.236) < 0.01
     assert abs(synth.param_count(synth.PRESETS["8b-hybrid"]) / 1e9 - 8.03) < 0.01
     assert abs(synth.param_count(synth.PRESETS["70b"]) * 2 / 1e9 - 141.1) < 0.2
+
+
+def test_f32_widening_matches_bf16_bits():
+    dims = synth.PRESETS["tiny"]
+    for name, layer in (("wq", 1), ("embed", -1), ("mlp_norm", 0)):
+        a = synth.gen_tensor_f32(dims, name, layer)
+        b = synth.bf16_bits_to_f32(synth.gen_tensor(dims, name, layer)).reshape(a.shape)
+        assert np.array_equal(a, b)
