@@ -24,8 +24,9 @@
  *   - logits are those of each sequence's last position; the greedy token is
  *     the argmax with the lowest index on ties.
  *
- * Precision.  Weights bf16; accumulation fp32; residual stream fp32; KV cache
- * bf16; tensor-core operands (prefill) bf16, rounded to nearest even.
+ * Precision.  Weights, KV cache, queries and prefill tensor-core operands in
+ * one 16-bit type (weight_dtype: bf16, or fp16 holding bf16-valued weights
+ * exactly), rounded to nearest even; accumulation and residual stream fp32.
  *
  * Ownership.  The caller allocates every device buffer (weights, workspace, KV
  * pool, block table, sequence lengths, outputs) and passes raw device
@@ -117,10 +118,11 @@ typedef struct {
  * n_q_heads*head_dim/k, ffn_dim/k multiples of 256.  Prefill is unsharded (the
  * same function, up to fp32 reassociation). */
 
-/* Weight storage types.  bf16-valued weights convert to fp16 exactly when
- * 2^-17 <= |w| <= 65504; with LADDER_DTYPE_F16 the prefill GEMM operands
- * (normalised activations, attention output, SwiGLU output) are fp16 as well,
- * which carries 3 more mantissa bits than bf16.  The KV cache is bf16 in both. */
+/* Storage types.  bf16-valued weights convert to fp16 exactly when
+ * 2^-17 <= |w| <= 65504.  The KV cache, the prefill queries and the prefill
+ * tensor-core operands (normalised activations, attention output, SwiGLU
+ * output) use the same type as the weights; fp16 carries 3 more mantissa
+ * bits than bf16. */
 enum { LADDER_DTYPE_BF16 = 0, LADDER_DTYPE_F16 = 1 };
 
 /* Weights: device pointers of the configured weight_dtype (bf16 or fp16),
@@ -163,7 +165,7 @@ void ladder_destroy(ladder_model* m);
 int ladder_set_mode(ladder_model* m, int residual_mode, int flags);
 
 /* Paged KV cache.  `pool` is a device buffer of num_pages * kv_page_bytes,
- * 16-byte aligned, laid out bf16 [n_layers][num_pages][2 (K, V)][n_kv_heads]
+ * 16-byte aligned, laid out in the weight dtype [n_layers][num_pages][2 (K, V)][n_kv_heads]
  * [page_size][head_dim]; keys are stored after rotation.  `block_table` is a
  * device int32 [max_batch][max_pages_per_seq], `seq_lens` a device int32
  * [max_batch]; both are caller-owned and written only by the library.
@@ -237,7 +239,8 @@ int ladder_probe_end(ladder_model* m, int32_t* launches, float* total_ms);
  * the query q[b] (device fp32 [B][n_q_heads*head_dim], already rotated) sits
  * at position positions[b] (device int32 [B]) and attends causally over the
  * cached positions 0 .. positions[b] of `kv_layer`, one layer of the pool:
- * bf16 [num_pages][2][n_kv_heads][page_size][head_dim] addressed through
+ * [num_pages][2][n_kv_heads][page_size][head_dim] of kv_dtype
+ * (LADDER_DTYPE_BF16 or LADDER_DTYPE_F16), addressed through
  * block_table (device int32 [B][max_pages_per_seq]).  Query head h reads KV
  * head h / (n_q_heads / n_kv_heads); scores are scaled by `scale`.  Writes
  * out (device fp32 [B][n_q_heads*head_dim]).  `scratch` is a caller-owned
@@ -247,7 +250,7 @@ int ladder_probe_end(ladder_model* m, int32_t* launches, float* total_ms);
  * (head_dim 64 or 128, at most 8 query heads per KV head, page_size 16, 32
  * or 64). */
 size_t ladder_attention_decode_scratch_bytes(int32_t B, int32_t n_q_heads, int32_t head_dim, int32_t max_position);
-int ladder_attention_decode(const float* q, const void* kv_layer, const int32_t* block_table,
+int ladder_attention_decode(const float* q, const void* kv_layer, int32_t kv_dtype, const int32_t* block_table,
                             int32_t max_pages_per_seq, const int32_t* positions, int32_t B, int32_t n_q_heads,
                             int32_t n_kv_heads, int32_t head_dim, int32_t page_size, float scale,
                             int32_t max_position, float* out, void* scratch, size_t scratch_bytes,
@@ -269,10 +272,11 @@ int ladder_attention_decode(const float* q, const void* kv_layer, const int32_t*
  * different streams, or from different threads) race on it and must be
  * serialised by the caller. */
 #define LADDER_STATIC_SCRATCH_BYTES (8u << 20)
-int ladder_attention_decode_noalloc(const float* q, const void* kv_layer, const int32_t* block_table,
-                                    int32_t max_pages_per_seq, const int32_t* positions, int32_t B,
-                                    int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t page_size,
-                                    float scale, int32_t max_position, float* out, ladder_stream_t stream);
+int ladder_attention_decode_noalloc(const float* q, const void* kv_layer, int32_t kv_dtype,
+                                    const int32_t* block_table, int32_t max_pages_per_seq,
+                                    const int32_t* positions, int32_t B, int32_t n_q_heads, int32_t n_kv_heads,
+                                    int32_t head_dim, int32_t page_size, float scale, int32_t max_position,
+                                    float* out, ladder_stream_t stream);
 
 /* Thread-local message describing the last failed call on this thread. */
 const char* ladder_last_error(void);

@@ -56,11 +56,11 @@ size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 }  // namespace
 
-extern "C" int ladder_attention_decode_noalloc(const float* q, const void* kv_layer, const int32_t* block_table,
-                                               int32_t max_pages_per_seq, const int32_t* positions, int32_t B,
-                                               int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
-                                               int32_t page_size, float scale, int32_t max_position, float* out,
-                                               ladder_stream_t stream) {
+extern "C" int ladder_attention_decode_noalloc(const float* q, const void* kv_layer, int32_t kv_dtype,
+                                               const int32_t* block_table, int32_t max_pages_per_seq,
+                                               const int32_t* positions, int32_t B, int32_t n_q_heads,
+                                               int32_t n_kv_heads, int32_t head_dim, int32_t page_size, float scale,
+                                               int32_t max_position, float* out, ladder_stream_t stream) {
   if (B <= 0 || n_q_heads <= 0 || head_dim <= 0 || max_position < 0)
     return set_error(LADDER_ERR_INVALID, "B, n_q_heads, head_dim must be positive and max_position >= 0");
   const size_t nsplit = ((size_t)max_position + 1 + kSplitLen - 1) / kSplitLen;
@@ -78,6 +78,7 @@ extern "C" int ladder_attention_decode_noalloc(const float* q, const void* kv_la
   if (rc) return rc;
   // Every partial that the combine step reads is written earlier in the same
   // call, so nothing in the array has to start at zero.
-  return ladder_attention_decode(q, kv_layer, block_table, max_pages_per_seq, positions, B, n_q_heads, n_kv_heads,
-                                 head_dim, page_size, scale, max_position, out, scratch, kStaticScratchBytes, stream);
+  return ladder_attention_decode(q, kv_layer, kv_dtype, block_table, max_pages_per_seq, positions, B, n_q_heads,
+                                 n_kv_heads, head_dim, page_size, scale, max_position, out, scratch,
+                                 kStaticScratchBytes, stream);
 }

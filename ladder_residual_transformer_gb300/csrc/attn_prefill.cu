@@ -3,7 +3,7 @@
 // CTA = (64-query block, query head, sequence); four warps of 16 query rows.
 // Keys and values of the sequence are read from the paged KV cache (the QKV
 // GEMM epilogue has just written them) in 64-key tiles, double-buffered with
-// cp.async.  S = Q K^T and O += P V use mma.sync m16n8k16 (bf16 in, fp32
+// cp.async.  S = Q K^T and O += P V use mma.sync m16n8k16 (16-bit in, fp32
 // accumulate); the softmax is the online (running max / running sum) form in
 // fp32 registers, with the row reductions done by quad shuffles.  Only key
 // tiles at or below the diagonal are visited; the diagonal tile is masked.
@@ -43,34 +43,43 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t& r0, uint32_t& r1, uint32_t& 
                : "r"(fa_smem(p)));
 }
 
-__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+// D += A B for one m16n8k16 tile, 16-bit A and B of type T, fp32 accumulate.
+template <typename T>
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  if constexpr (W16<T>::umma_fmt == 1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-template <typename OT, int HD>
+// T: 16-bit type of q, K, V, P and the output (the weight dtype).
+template <typename T, int HD>
 __global__ void __launch_bounds__(FA_THREADS) attn_prefill_kernel(const AttnPrefillParams p) {
+  using C = W16<T>;
   constexpr int LD = HD + 8;  // padded row (elements): conflict-free ldmatrix
   constexpr int KT = HD / 16; // k-steps over the head dimension
   constexpr int NT = HD / 8;  // n-tiles of the output
   extern __shared__ uint4 fa_smem_raw[];
-  bf16* sQ = reinterpret_cast<bf16*>(fa_smem_raw);
-  bf16* sK = sQ + FA_BM * LD;        // [2][FA_BN][LD]
-  bf16* sV = sK + 2 * FA_BN * LD;    // [2][FA_BN][LD]
+  T* sQ = reinterpret_cast<T*>(fa_smem_raw);
+  T* sK = sQ + FA_BM * LD;        // [2][FA_BN][LD]
+  T* sV = sK + 2 * FA_BN * LD;    // [2][FA_BN][LD]
+  const T* qsrc = static_cast<const T*>(p.q);
+  const T* kvbase = static_cast<const T*>(p.kv.base);
 
   // The heaviest (last) query blocks of the causal triangle are scheduled first.
   const int qb = gridDim.x - 1 - blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int T = p.seq_len[b];
-  if (qb * FA_BM >= T) return;
+  const int Tn = p.seq_len[b];
+  if (qb * FA_BM >= Tn) return;
   const int start = p.seq_start[b];
   const int G = p.n_q / p.kv.n_kv, kvh = h / G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -80,19 +89,19 @@ __global__ void __launch_bounds__(FA_THREADS) attn_prefill_kernel(const AttnPref
   for (int c = tid; c < FA_BM * HD / 8; c += FA_THREADS) {
     const int r = c / (HD / 8), d8 = (c % (HD / 8)) * 8;
     const int pos = qb * FA_BM + r;
-    const bf16* src = p.q + (size_t)(start + (pos < T ? pos : 0)) * ldq + (size_t)h * HD + d8;
-    cp_async16(sQ + r * LD + d8, src, pos < T);
+    const T* src = qsrc + (size_t)(start + (pos < Tn ? pos : 0)) * ldq + (size_t)h * HD + d8;
+    cp_async16(sQ + r * LD + d8, src, pos < Tn);
   }
   auto load_kv = [&](int kb, int buf) {
-    bf16* dk = sK + buf * FA_BN * LD;
-    bf16* dv = sV + buf * FA_BN * LD;
+    T* dk = sK + buf * FA_BN * LD;
+    T* dv = sV + buf * FA_BN * LD;
     for (int c = tid; c < FA_BN * HD / 8; c += FA_THREADS) {
       const int r = c / (HD / 8), d8 = (c % (HD / 8)) * 8;
       const int key = kb * FA_BN + r;
-      const bool ok = key < T;
+      const bool ok = key < Tn;
       const int kk = ok ? key : 0;
-      cp_async16(dk + r * LD + d8, p.kv.base + p.kv.slot(b, kk, 0, kvh) + d8, ok);
-      cp_async16(dv + r * LD + d8, p.kv.base + p.kv.slot(b, kk, 1, kvh) + d8, ok);
+      cp_async16(dk + r * LD + d8, kvbase + p.kv.slot(b, kk, 0, kvh) + d8, ok);
+      cp_async16(dv + r * LD + d8, kvbase + p.kv.slot(b, kk, 1, kvh) + d8, ok);
     }
   };
   load_kv(0, 0);
@@ -117,12 +126,12 @@ __global__ void __launch_bounds__(FA_THREADS) attn_prefill_kernel(const AttnPref
 #pragma unroll
       for (int kt = 0; kt < KT; ++kt) {
         const int q = lane >> 3;
-        const bf16* a = sQ + (row0 + (q & 1) * 8 + (lane & 7)) * LD + kt * 16 + (q >> 1) * 8;
+        const T* a = sQ + (row0 + (q & 1) * 8 + (lane & 7)) * LD + kt * 16 + (q >> 1) * 8;
         ldsm_x4(qf[kt][0], qf[kt][1], qf[kt][2], qf[kt][3], a);
       }
     }
-    const bf16* K = sK + (kb & 1) * FA_BN * LD;
-    const bf16* V = sV + (kb & 1) * FA_BN * LD;
+    const T* K = sK + (kb & 1) * FA_BN * LD;
+    const T* V = sV + (kb & 1) * FA_BN * LD;
 
     // S = Q K^T for 16 rows x 64 keys (8 n-tiles of 8 keys)
     float s[8][4];
@@ -133,11 +142,11 @@ __global__ void __launch_bounds__(FA_THREADS) attn_prefill_kernel(const AttnPref
 #pragma unroll
       for (int j = 0; j < 8; j += 2) {
         const int q = lane >> 3;
-        const bf16* bp = K + ((j + (q >> 1)) * 8 + (lane & 7)) * LD + kt * 16 + (q & 1) * 8;
+        const T* bp = K + ((j + (q >> 1)) * 8 + (lane & 7)) * LD + kt * 16 + (q & 1) * 8;
         uint32_t b0, b1, b2, b3;
         ldsm_x4(b0, b1, b2, b3, bp);
-        mma_bf16(s[j], qf[kt][0], qf[kt][1], qf[kt][2], qf[kt][3], b0, b1);
-        mma_bf16(s[j + 1], qf[kt][0], qf[kt][1], qf[kt][2], qf[kt][3], b2, b3);
+        mma16816<T>(s[j], qf[kt][0], qf[kt][1], qf[kt][2], qf[kt][3], b0, b1);
+        mma16816<T>(s[j + 1], qf[kt][0], qf[kt][1], qf[kt][2], qf[kt][3], b2, b3);
       }
     }
     // causal mask on the diagonal tile, then the online softmax update
@@ -188,18 +197,18 @@ __global__ void __launch_bounds__(FA_THREADS) attn_prefill_kernel(const AttnPref
     // O += P V: keys in 4 k-steps of 16, output dims in NT n-tiles
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      const uint32_t a0 = pack_bf16(s[2 * t][0], s[2 * t][1]);
-      const uint32_t a1 = pack_bf16(s[2 * t][2], s[2 * t][3]);
-      const uint32_t a2 = pack_bf16(s[2 * t + 1][0], s[2 * t + 1][1]);
-      const uint32_t a3 = pack_bf16(s[2 * t + 1][2], s[2 * t + 1][3]);
+      const uint32_t a0 = C::pack(s[2 * t][0], s[2 * t][1]);
+      const uint32_t a1 = C::pack(s[2 * t][2], s[2 * t][3]);
+      const uint32_t a2 = C::pack(s[2 * t + 1][0], s[2 * t + 1][1]);
+      const uint32_t a3 = C::pack(s[2 * t + 1][2], s[2 * t + 1][3]);
 #pragma unroll
       for (int j = 0; j < NT; j += 2) {
         const int q = lane >> 3;
-        const bf16* vp = V + (t * 16 + (q & 1) * 8 + (lane & 7)) * LD + (j + (q >> 1)) * 8;
+        const T* vp = V + (t * 16 + (q & 1) * 8 + (lane & 7)) * LD + (j + (q >> 1)) * 8;
         uint32_t b0, b1, b2, b3;
         ldsm_x4_t(b0, b1, b2, b3, vp);
-        mma_bf16(o[j], a0, a1, a2, a3, b0, b1);
-        mma_bf16(o[j + 1], a0, a1, a2, a3, b2, b3);
+        mma16816<T>(o[j], a0, a1, a2, a3, b0, b1);
+        mma16816<T>(o[j + 1], a0, a1, a2, a3, b2, b3);
       }
     }
     __syncthreads();  // the buffer just read is refilled two tiles later
@@ -210,12 +219,12 @@ __global__ void __launch_bounds__(FA_THREADS) attn_prefill_kernel(const AttnPref
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     const int pos = qpos0 + r * 8;
-    if (pos >= T) continue;
-    OT* dst = static_cast<OT*>(p.out) + (size_t)(start + pos) * ldq + (size_t)h * HD + 2 * (lane & 3);
+    if (pos >= Tn) continue;
+    T* dst = static_cast<T*>(p.out) + (size_t)(start + pos) * ldq + (size_t)h * HD + 2 * (lane & 3);
     const float inv = r ? inv1 : inv0;
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      *reinterpret_cast<uint32_t*>(dst + j * 8) = W16<OT>::pack(o[j][2 * r] * inv, o[j][2 * r + 1] * inv);
+      *reinterpret_cast<uint32_t*>(dst + j * 8) = C::pack(o[j][2 * r] * inv, o[j][2 * r + 1] * inv);
     }
   }
 }

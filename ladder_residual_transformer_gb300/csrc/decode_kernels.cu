@@ -317,9 +317,8 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
           q[1] = r1;
         } else {
           const int head = local / hd, dim = local % hd;
-          bf16* dst = p.kv.base + p.kv.slot(b, pos, kind - 1, head) + dim;
-          dst[0] = __float2bfloat16_rn(r0);
-          dst[1] = __float2bfloat16_rn(r1);
+          WT* dst = static_cast<WT*>(p.kv.base) + p.kv.slot(b, pos, kind - 1, head) + dim;
+          *reinterpret_cast<uint32_t*>(dst) = C::pack(r0, r1);
         }
       } else if (MODE == GEMV_GATEUP) {
         p.out[(size_t)b * p.ldo + task] = silu_f(v0) * v1;
@@ -449,13 +448,15 @@ __device__ __forceinline__ void att_cp16(void* dst, const void* src) {
                : "memory");
 }
 
-template <int HD>
+template <typename KT, int HD>
 __global__ void __launch_bounds__(ATT_THREADS) attn_decode_kernel(const AttnDecodeParams p) {
-  constexpr int LD = HD + 8;                 // padded bf16 row: conflict-free 16-byte reads
+  using C = W16<KT>;
+  constexpr int LD = HD + 8;                 // padded 16-bit row: conflict-free 16-byte reads
   constexpr int KG = ATT_THREADS / (HD / 2);  // key groups in the P V phase
   extern __shared__ uint4 att_dyn[];
-  bf16* sK = reinterpret_cast<bf16*>(att_dyn);  // [ATT_SPLIT][LD]
-  bf16* sV = sK + ATT_SPLIT * LD;              // [ATT_SPLIT][LD]
+  KT* sK = reinterpret_cast<KT*>(att_dyn);  // [ATT_SPLIT][LD]
+  KT* sV = sK + ATT_SPLIT * LD;            // [ATT_SPLIT][LD]
+  const KT* kvbase = static_cast<const KT*>(p.kv.base);
   __shared__ __align__(16) float q_s[ATT_MAXG][HD];
   __shared__ float p_s[ATT_MAXG][ATT_SPLIT];
   __shared__ float m_s[ATT_MAXG], l_s[ATT_MAXG];
@@ -477,8 +478,8 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_decode_kernel(const AttnDeco
     const int r = c / (HD / 8), d8 = (c % (HD / 8)) * 8;
     const size_t kofs = p.kv.slot(b, s0 + r, 0, kvh) + d8;
     const size_t vofs = kofs + (size_t)p.kv.n_kv * p.kv.page_size * HD;  // V slab follows the K slab of the page
-    att_cp16(sK + r * LD + d8, p.kv.base + kofs);
-    att_cp16(sV + r * LD + d8, p.kv.base + vofs);
+    att_cp16(sK + r * LD + d8, kvbase + kofs);
+    att_cp16(sV + r * LD + d8, kvbase + vofs);
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
   const float* qg = p.q + (size_t)b * p.n_q * HD + (size_t)kvh * G * HD;
@@ -491,12 +492,12 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_decode_kernel(const AttnDeco
 #pragma unroll
   for (int h = 0; h < ATT_MAXG; ++h) acc[h] = 0.f;
   if (tid < n) {
-    const bf16* krow = sK + tid * LD;
+    const KT* krow = sK + tid * LD;
 #pragma unroll 4
     for (int d = 0; d < HD; d += 8) {
       const uint4 kw = *reinterpret_cast<const uint4*>(krow + d);
-      const float k0 = bf_lo(kw.x), k1 = bf_hi(kw.x), k2 = bf_lo(kw.y), k3 = bf_hi(kw.y);
-      const float k4 = bf_lo(kw.z), k5 = bf_hi(kw.z), k6 = bf_lo(kw.w), k7 = bf_hi(kw.w);
+      const float k0 = C::lo(kw.x), k1 = C::hi(kw.x), k2 = C::lo(kw.y), k3 = C::hi(kw.y);
+      const float k4 = C::lo(kw.z), k5 = C::hi(kw.z), k6 = C::lo(kw.w), k7 = C::hi(kw.w);
 #pragma unroll
       for (int h = 0; h < ATT_MAXG; ++h) {
         if (h < G) {
@@ -544,7 +545,7 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_decode_kernel(const AttnDeco
   for (int h = 0; h < ATT_MAXG; ++h) o[h] = make_float2(0.f, 0.f);
   for (int t = kg; t < n; t += KG) {
     const uint32_t vv = *reinterpret_cast<const uint32_t*>(sV + t * LD + 2 * dp);
-    const float v0 = bf_lo(vv), v1 = bf_hi(vv);
+    const float v0 = C::lo(vv), v1 = C::hi(vv);
 #pragma unroll
     for (int h = 0; h < ATT_MAXG; ++h) {
       if (h < G) {
@@ -615,27 +616,37 @@ static cudaError_t attn_configure_current_device() {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && configured[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(attn_decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)att_dyn_smem(64));
+  e = cudaFuncSetAttribute(attn_decode_kernel<bf16, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)att_dyn_smem(64));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_decode_kernel<bf16, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)att_dyn_smem(128));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_decode_kernel<f16, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)att_dyn_smem(64));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_decode_kernel<f16, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)att_dyn_smem(128));
   if (e == cudaSuccess && dev >= 0 && dev < 64) configured[dev] = 1;
   return e;
 }
 
-cudaError_t launch_attn_decode(const AttnDecodeParams& p, int B, int n_kv, int hd, cudaStream_t s, bool pdl) {
+template <typename KT, int HD>
+static cudaError_t attn_decode_go(const AttnDecodeParams& p, int B, int n_kv, cudaStream_t s, bool pdl) {
+  const dim3 grid(p.nsplit, n_kv, B);
+  cudaError_t e = launch_k(attn_decode_kernel<KT, HD>, grid, dim3(ATT_THREADS), att_dyn_smem(HD), s, pdl, p);
+  if (e == cudaSuccess) e = launch_k(attn_combine_kernel<HD>, dim3(p.n_q, B), dim3(HD), 0, s, pdl, p);
+  return e;
+}
+
+cudaError_t launch_attn_decode(const AttnDecodeParams& p, int B, int n_kv, int hd, int kv_dtype, cudaStream_t s,
+                               bool pdl) {
   if (p.split_len != ATT_SPLIT) return cudaErrorInvalidValue;
   cudaError_t e = attn_configure_current_device();
   if (e != cudaSuccess) return e;
-  const dim3 grid(p.nsplit, n_kv, B);
-  if (hd == 64) {
-    e = launch_k(attn_decode_kernel<64>, grid, dim3(ATT_THREADS), att_dyn_smem(64), s, pdl, p);
-    if (e == cudaSuccess) e = launch_k(attn_combine_kernel<64>, dim3(p.n_q, B), dim3(64), 0, s, pdl, p);
-  } else {
-    e = launch_k(attn_decode_kernel<128>, grid, dim3(ATT_THREADS), att_dyn_smem(128), s, pdl, p);
-    if (e == cudaSuccess) e = launch_k(attn_combine_kernel<128>, dim3(p.n_q, B), dim3(128), 0, s, pdl, p);
-  }
-  return e;
+  if (kv_dtype == WDT_F16)
+    return hd == 64 ? attn_decode_go<f16, 64>(p, B, n_kv, s, pdl) : attn_decode_go<f16, 128>(p, B, n_kv, s, pdl);
+  return hd == 64 ? attn_decode_go<bf16, 64>(p, B, n_kv, s, pdl) : attn_decode_go<bf16, 128>(p, B, n_kv, s, pdl);
 }
 
 // ---------------------------------------------------------------------------

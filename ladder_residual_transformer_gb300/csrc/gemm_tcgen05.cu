@@ -329,7 +329,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
           tmem_ld32(trow + c * 32, v);
           int map, row;
           if (!b_half<GEMM_QKV, BN>(p, tile_n, c >> 2, map, row) || m >= p.M) continue;
-          // q and the KV cache are bf16 whatever the weight type (the attention kernels read bf16)
           const int local = row + (c & 3) * 32;  // first column of the chunk inside its matrix
           const int head = local / hd, dim0 = local % hd;
           if (map < 2) {
@@ -343,19 +342,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
               v[j + 1] = a0 * sj + a1 * cj;
             }
           }
-          bf16* dst = map == 0 ? static_cast<bf16*>(p.out_h) + (size_t)m * p.ldo + local
-                               : p.kv.base + p.kv.slot(b, pos, map - 1, head) + dim0;
+          // q, K and V are stored in the weight dtype (the attention operands)
+          WT* dst = map == 0 ? static_cast<WT*>(p.out_h) + (size_t)m * p.ldo + local
+                             : static_cast<WT*>(p.kv.base) + p.kv.slot(b, pos, map - 1, head) + dim0;
 #pragma unroll
           for (int j = 0; j < 32; j += 8) {
             uint4 pk;
-            __nv_bfloat162 t0 = __floats2bfloat162_rn(v[j], v[j + 1]);
-            __nv_bfloat162 t1 = __floats2bfloat162_rn(v[j + 2], v[j + 3]);
-            __nv_bfloat162 t2 = __floats2bfloat162_rn(v[j + 4], v[j + 5]);
-            __nv_bfloat162 t3 = __floats2bfloat162_rn(v[j + 6], v[j + 7]);
-            pk.x = *reinterpret_cast<uint32_t*>(&t0);
-            pk.y = *reinterpret_cast<uint32_t*>(&t1);
-            pk.z = *reinterpret_cast<uint32_t*>(&t2);
-            pk.w = *reinterpret_cast<uint32_t*>(&t3);
+            pk.x = C::pack(v[j], v[j + 1]);
+            pk.y = C::pack(v[j + 2], v[j + 3]);
+            pk.z = C::pack(v[j + 4], v[j + 5]);
+            pk.w = C::pack(v[j + 6], v[j + 7]);
             *reinterpret_cast<uint4*>(dst + j) = pk;
           }
         }

@@ -97,9 +97,9 @@ inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_
 // Kernel parameter blocks
 // ---------------------------------------------------------------------------
 
-// Paged KV cache view of one layer: bf16 [num_pages][2][n_kv][page_size][head_dim].
+// Paged KV cache view of one layer: 16-bit (the weight dtype) [num_pages][2][n_kv][page_size][head_dim].
 struct KvLayer {
-  bf16* base;
+  void* base;
   const int* block_table;  // [max_batch][max_pages]
   int max_pages;
   int page_size;
@@ -162,7 +162,7 @@ enum GemmMode { GEMM_QKV = 0, GEMM_GATEUP = 1, GEMM_RESID = 2 };
 
 struct GemmParams {
   int M, N, K;
-  void* out_h;          // QKV: q (bf16) [M][ldo]; GATEUP: act (weight dtype) [M][ldo]
+  void* out_h;          // QKV: q [M][ldo]; GATEUP: act [M][ldo] (weight dtype)
   float* out_f;         // RESID: x_out [M][ldo]
   int ldo;
   const float* x_res;   // RESID
@@ -176,7 +176,7 @@ struct GemmParams {
 };
 
 struct AttnPrefillParams {
-  const bf16* q;        // [M][n_q * hd] rotated queries
+  const void* q;        // [M][n_q * hd] rotated queries (weight dtype, like the KV cache)
   KvLayer kv;
   const int* seq_start; // first packed row of sequence b
   const int* seq_len;   // length of sequence b
@@ -194,7 +194,8 @@ cudaError_t launch_gemv(const GemvParams& p, int mode, int wdt, int num_sms, cud
 cudaError_t gemv_configure();
 int gemv_chunk(int B, int K);
 int gemv_launch_count(int B, int K);
-cudaError_t launch_attn_decode(const AttnDecodeParams& p, int B, int n_kv, int hd, cudaStream_t s, bool pdl = false);
+cudaError_t launch_attn_decode(const AttnDecodeParams& p, int B, int n_kv, int hd, int kv_dtype, cudaStream_t s,
+                               bool pdl = false);
 cudaError_t launch_argmax(const float* logits, int B, int V, float* part_v, int* part_i, int nblk,
                           int* out, cudaStream_t s, bool pdl = false);
 cudaError_t launch_advance(int* seq_lens, int B, cudaStream_t s, bool pdl = false);

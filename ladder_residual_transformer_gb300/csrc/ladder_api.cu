@@ -226,7 +226,7 @@ struct ladder_model {
 
 struct ladder_kv {
   ladder_model* m;
-  bf16* pool;
+  char* pool;  // 16-bit elements of the weight dtype
   int num_pages, max_pages;
   int32_t* block_table;
   int32_t* seq_lens;
@@ -238,7 +238,7 @@ struct ladder_kv {
     KvLayer v;
     const ladder_config& c = m->cfg;
     const size_t page_elems = (size_t)2 * c.n_kv_heads * c.page_size * c.head_dim;
-    v.base = pool + (size_t)l * num_pages * page_elems;
+    v.base = pool + (size_t)l * num_pages * page_elems * 2;
     v.block_table = block_table;
     v.max_pages = max_pages;
     v.page_size = c.page_size;
@@ -389,7 +389,7 @@ int ladder_kv_create(ladder_model* m, void* pool, int32_t num_pages, int32_t max
   if (num_pages <= 0 || max_pages_per_seq <= 0) return fail(LADDER_ERR_INVALID, "num_pages and max_pages_per_seq must be positive");
   auto* kv = new ladder_kv();
   kv->m = m;
-  kv->pool = static_cast<bf16*>(pool);
+  kv->pool = static_cast<char*>(pool);
   kv->num_pages = num_pages;
   kv->max_pages = max_pages_per_seq;
   kv->block_table = block_table;
@@ -586,7 +586,7 @@ int enqueue_decode_shard(ladder_model* m, ladder_kv* kv, const int32_t* tokens, 
       a.q = q; a.kv = kvl; a.seq_lens = kv->seq_lens; a.n_q = c.n_q_heads; a.split_len = kSplitLen;
       a.nsplit = nsplit; a.scale = 1.0f / sqrtf((float)c.head_dim);
       a.part_o = m->at<float>(P.part_o); a.part_ml = m->at<float>(P.part_ml); a.out = ao;
-      LAUNCH(launch_attn_decode(a, B, c.n_kv_heads, c.head_dim, s, pdl), 2);
+      LAUNCH(launch_attn_decode(a, B, c.n_kv_heads, c.head_dim, m->wdt, s, pdl), 2);
       o.x = ao; o.ldx = qd; o.K = qd / ksh; o.kfull = qd; o.ldw = qd; o.w0 = L.wo;
     } else {  // MLP module
       GemvParams g{};
@@ -677,7 +677,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       a.nsplit = nsplit; a.scale = 1.0f / sqrtf((float)c.head_dim);
       a.part_o = m->at<float>(P.part_o); a.part_ml = m->at<float>(P.part_ml); a.out = ao;
       pe = m->probe_start(LADDER_PROBE_ATTN, s);
-      LAUNCH(launch_attn_decode(a, B, c.n_kv_heads, c.head_dim, s, pdl), 2);
+      LAUNCH(launch_attn_decode(a, B, c.n_kv_heads, c.head_dim, m->wdt, s, pdl), 2);
       m->probe_stop(pe, s);
 
       if ((rc = use(k - 1, 0))) return rc;
@@ -829,7 +829,7 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
   const int d = c.d_model, qd = c.n_q_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim, f = c.ffn_dim;
   const int wdt = m->wdt;
   void* xn = m->ws + P.xn;    // normalised rows, weight dtype
-  void* qb = m->ws + P.q;     // rotated queries, bf16
+  void* qb = m->ws + P.q;     // rotated queries, weight dtype
   void* aob = m->ws + P.ao;   // attention output, weight dtype
   void* actb = m->ws + P.act; // SwiGLU output, weight dtype
 
@@ -849,7 +849,7 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
       LAUNCH(launch_gemm_tc(&m->map_xn, &T.wq, &T.wk, &T.wv, g, GEMM_QKV, wdt, m->num_sms, m->err(), s), 1);
 
       AttnPrefillParams a{};
-      a.q = static_cast<const bf16*>(qb); a.kv = kvl; a.seq_start = d_start; a.seq_len = d_lens;
+      a.q = qb; a.kv = kvl; a.seq_start = d_start; a.seq_len = d_lens;
       a.n_q = c.n_q_heads; a.scale = 1.0f / sqrtf((float)c.head_dim); a.out = aob;
       LAUNCH(launch_attn_prefill_tc(a, c.head_dim, wdt, B, max_len, s), 1);
 
@@ -912,12 +912,13 @@ extern "C" size_t ladder_attention_decode_scratch_bytes(int32_t B, int32_t n_q_h
   return attention_scratch(B, n_q_heads, head_dim, max_position);
 }
 
-extern "C" int ladder_attention_decode(const float* q, const void* kv_layer, const int32_t* block_table,
-                                       int32_t max_pages_per_seq, const int32_t* positions, int32_t B,
-                                       int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t page_size,
-                                       float scale, int32_t max_position, float* out, void* scratch,
-                                       size_t scratch_bytes, ladder_stream_t stream) {
+extern "C" int ladder_attention_decode(const float* q, const void* kv_layer, int32_t kv_dtype,
+                                       const int32_t* block_table, int32_t max_pages_per_seq,
+                                       const int32_t* positions, int32_t B, int32_t n_q_heads, int32_t n_kv_heads,
+                                       int32_t head_dim, int32_t page_size, float scale, int32_t max_position,
+                                       float* out, void* scratch, size_t scratch_bytes, ladder_stream_t stream) {
   if (!q || !kv_layer || !block_table || !positions || !out || !scratch) return fail(LADDER_ERR_INVALID, "NULL argument");
+  if (kv_dtype != LADDER_DTYPE_BF16 && kv_dtype != LADDER_DTYPE_F16) return fail(LADDER_ERR_INVALID, "unknown kv_dtype %d", kv_dtype);
   int rc = check_attention_shape(B, n_q_heads, n_kv_heads, head_dim, page_size, max_position);
   if (rc) return rc;
   if (max_pages_per_seq <= 0 || (int64_t)max_pages_per_seq * page_size < (int64_t)max_position + 1)
@@ -928,7 +929,7 @@ extern "C" int ladder_attention_decode(const float* q, const void* kv_layer, con
   if (scratch_bytes < need) return fail(LADDER_ERR_CAPACITY, "scratch too small: %zu < %zu bytes", scratch_bytes, need);
   AttnDecodeParams a{};
   a.q = q;
-  a.kv.base = static_cast<bf16*>(const_cast<void*>(kv_layer));
+  a.kv.base = const_cast<void*>(kv_layer);
   a.kv.block_table = block_table;
   a.kv.max_pages = max_pages_per_seq;
   a.kv.page_size = page_size;
@@ -944,7 +945,7 @@ extern "C" int ladder_attention_decode(const float* q, const void* kv_layer, con
   a.part_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) +
                                        align_up((size_t)B * n_q_heads * a.nsplit * head_dim * 4, 256));
   a.out = out;
-  cudaError_t e = launch_attn_decode(a, B, n_kv_heads, head_dim, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_attn_decode(a, B, n_kv_heads, head_dim, kv_dtype, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(LADDER_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
   return LADDER_OK;
 }

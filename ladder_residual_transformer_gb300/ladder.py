@@ -66,10 +66,10 @@ _SIGNATURES = {
     "ladder_probe_begin": (_i32, [_vp, ctypes.c_int, _i32]),
     "ladder_probe_end": (_i32, [_vp, _pi32, ctypes.POINTER(_f32)]),
     "ladder_attention_decode_scratch_bytes": (_sz, [_i32, _i32, _i32, _i32]),
-    "ladder_attention_decode": (_i32, [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp, _vp,
-                                       _sz, _vp]),
-    "ladder_attention_decode_noalloc": (_i32, [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _i32,
-                                               _vp, _vp]),
+    "ladder_attention_decode": (_i32, [_vp, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _i32,
+                                       _vp, _vp, _sz, _vp]),
+    "ladder_attention_decode_noalloc": (_i32, [_vp, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _f32,
+                                               _i32, _vp, _vp]),
     "ladder_last_error": (ctypes.c_char_p, []),
 }
 
@@ -172,6 +172,11 @@ def synthetic_weights(dims: dict, device="cuda", seed: int = 0, transform=None, 
     return out
 
 
+def _kv_dtype(t: torch.Tensor) -> int:
+    """C-ABI code of a KV tensor's 16-bit type (int16 views count as bf16)."""
+    return DTYPES["fp16"] if t.dtype == torch.float16 else DTYPES["bf16"]
+
+
 def attention_decode(q: torch.Tensor, kv_layer: torch.Tensor, block_table: torch.Tensor, positions: torch.Tensor,
                      n_kv_heads: int, head_dim: int, page_size: int, max_position: int, scale: float | None = None,
                      out: torch.Tensor | None = None, scratch: torch.Tensor | None = None, stream=None) -> torch.Tensor:
@@ -185,7 +190,7 @@ def attention_decode(q: torch.Tensor, kv_layer: torch.Tensor, block_table: torch
     need = lib().ladder_attention_decode_scratch_bytes(B, n_q, head_dim, max_position)
     if scratch is None:
         scratch = torch.empty(need, dtype=torch.uint8, device=q.device)
-    check(lib().ladder_attention_decode(q.data_ptr(), kv_layer.data_ptr(), block_table.data_ptr(),
+    check(lib().ladder_attention_decode(q.data_ptr(), kv_layer.data_ptr(), _kv_dtype(kv_layer), block_table.data_ptr(),
                                         block_table.shape[-1], positions.data_ptr(), B, n_q, n_kv_heads, head_dim,
                                         page_size, scale, max_position, out.data_ptr(), scratch.data_ptr(),
                                         scratch.numel() * scratch.element_size(), _stream_handle(stream)))
@@ -201,7 +206,8 @@ def attention_decode_noalloc(q: torch.Tensor, kv_layer: torch.Tensor, block_tabl
     n_q = q.shape[-1] // head_dim
     if scale is None:
         scale = head_dim ** -0.5
-    check(lib().ladder_attention_decode_noalloc(q.data_ptr(), kv_layer.data_ptr(), block_table.data_ptr(),
+    check(lib().ladder_attention_decode_noalloc(q.data_ptr(), kv_layer.data_ptr(), _kv_dtype(kv_layer),
+                                                block_table.data_ptr(),
                                                 block_table.shape[-1], positions.data_ptr(), B, n_q, n_kv_heads,
                                                 head_dim, page_size, scale, max_position, out.data_ptr(),
                                                 _stream_handle(stream)))
@@ -352,10 +358,11 @@ class LadderModel:
         return lib().ladder_last_launch_count(self._m)
 
     def kv_view(self) -> torch.Tensor:
-        """The pool as bf16 [n_layers][num_pages][2][n_kv][page_size][head_dim]."""
+        """The pool in its 16-bit type, [n_layers][num_pages][2][n_kv][page_size][head_dim]."""
         d = self.dims
-        return self.kv_pool.view(torch.bfloat16).view(d["n_layers"], self.num_pages, 2, d["n_kv_heads"],
-                                                      self.page_size, d["head_dim"])
+        t = torch.float16 if self.cfg.weight_dtype == DTYPES["fp16"] else torch.bfloat16
+        return self.kv_pool.view(t).view(d["n_layers"], self.num_pages, 2, d["n_kv_heads"], self.page_size,
+                                         d["head_dim"])
 
     def close(self):
         L = lib()
