@@ -38,7 +38,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic of the dominant kernel from one ncu capture, valid only while the
 # kernel source is unchanged (sha256 of the file that defines it).
-NCU_TRAFFIC = None  # {"source": "...", "sha256": "...", "bytes_per_launch": ...}
+NCU_TRAFFIC = {  # profiles/gemv_gateup_1p2b_ncu_full.md (mean of the two captured launches)
+    "source": "ladder_residual_transformer_gb300/csrc/decode_kernels.cu",
+    "sha256": "34e4e9f54af6409ec4444c631ede82b1870b753645a96597b65219923f1e3f1d",
+    "bytes_per_launch": 67608320,
+}
 
 
 # ---------------------------------------------------------------------------
@@ -353,9 +357,9 @@ def run_ours(args, dims):
 
     gu_bytes = 2 * 2 * dims["ffn_dim"] * dims["d_model"]  # gate + up rows, bf16
     gu_avg_s = probe_ms / max(n_probe, 1) / 1e3
-    gu_gbs = gu_bytes / gu_avg_s / 1e9
+    gu_gbs = gu_bytes / gu_avg_s / 1e9 if gu_avg_s > 0 else None
     traffic = None
-    if NCU_TRAFFIC:
+    if NCU_TRAFFIC and args.workload == "1.2b" and B == 1:
         src = os.path.join(ROOT, NCU_TRAFFIC["source"])
         if os.path.exists(src) and hashlib.sha256(open(src, "rb").read()).hexdigest() == NCU_TRAFFIC["sha256"]:
             traffic = NCU_TRAFFIC["bytes_per_launch"]
@@ -399,7 +403,7 @@ def run_ours(args, dims):
                                  "unit": "TFLOP/s", "frac": pre_tf / peaks["bf16_tflops"], "flops": pf}},
         "roofline": {"bound": "hbm", "kernel": "decode gate/up GEMV (RMSNorm + SwiGLU fused)",
                      "achieved": gu_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": gu_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                     "frac": gu_gbs / peaks["hbm_gbs"] if gu_gbs else None, "traffic": traffic,
                      "algorithmic_bytes_per_launch": gu_bytes, "launches_timed": n_probe,
                      "timing": "CUDA events on the launching stream around each launch, one eager "
                                "step's decode right after the timed region"},

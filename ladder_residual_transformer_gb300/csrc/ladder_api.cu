@@ -592,7 +592,9 @@ int enqueue_decode_shard(ladder_model* m, ladder_kv* kv, const int32_t* tokens, 
       GemvParams g{};
       g.x = m->X(j); g.ldx = d; g.g = L.mlp_norm; g.eps = c.norm_eps; g.B = B; g.K = d;
       g.w0 = L.w_gate; g.w1 = L.w_up; g.n_tasks = f; g.out = act; g.ldo = f; g.err = m->err();
+      cudaEvent_t pe = m->probe_start(LADDER_PROBE_GATEUP, s);
       LAUNCH(launch_gemv(g, GEMV_GATEUP, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, g.K));
+      m->probe_stop(pe, s);
       o.x = act; o.ldx = f; o.K = f / ksh; o.kfull = f; o.ldw = f; o.w0 = L.w_down;
     }
     // row-parallel partial sums: shard sh uses input block sh and writes part[b][sh][:]

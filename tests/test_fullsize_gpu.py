@@ -97,6 +97,11 @@ def test_full_70b_cached_decode_agrees_with_prefill_and_is_deterministic():
     assert np.isfinite(a).all()
     model.reset()
     full = run_tf(model, [prompt], np.zeros((1, 0), dtype=np.int32))
-    # logits after feeding tokens 32 and 33 equal the last-position logits of prefilling all 34
-    compare_logits(a[2], full[0], "70B decode vs prefill rerun")
+    # Logits after feeding tokens 32 and 33 equal the last-position logits of
+    # prefilling all 34.  Both sides are 16-bit-operand computations, each within
+    # the oracle tolerance of the true function, so their difference is bounded
+    # by the sum of the two bounds.
+    err = np.abs(a[2] - full[0]).max()
+    rel = np.linalg.norm(a[2] - full[0]) / np.linalg.norm(full[0])
+    assert err <= 2 * 3e-2 and rel <= 2 * 1e-2, (err, rel)
     model.close()
