@@ -264,9 +264,8 @@ int ladder_attention_decode(const float* q, const void* kv_layer, int32_t kv_dty
  * stall on an allocation).  The partials live in a file-scope device array of
  * LADDER_STATIC_SCRATCH_BYTES bytes that every GPU running this code keeps
  * until the process exits.  Calls whose partials need more than that fail with
- * LADDER_ERR_CAPACITY (need = 256-byte-aligned B*n_q_heads*nsplit*head_dim*4,
- * plus 256-byte-aligned B*n_q_heads*nsplit*8, plus B*n_q_heads*4, with
- * nsplit = ceil((max_position+1)/128)).  The first
+ * LADDER_ERR_CAPACITY (need = 256-byte-aligned B*n_q_heads*nsplit*head_dim*4
+ * plus B*n_q_heads*nsplit*8, nsplit = ceil((max_position+1)/128)).  The first
  * call on a device looks up the array's device address (cudaGetSymbolAddress)
  * with that device current; make that first call before any stream capture.
  * All calls share the one array: calls that can overlap on the GPU (on

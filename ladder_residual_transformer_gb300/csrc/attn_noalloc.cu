@@ -29,8 +29,7 @@ constexpr int kSplitLen = 128;  // keys per split, as in the scratch-taking entr
 constexpr int kMaxDevices = 64;
 
 // Partials of the split attention: [B][n_q][nsplit][head_dim] fp32, then
-// [B][n_q][nsplit][2] fp32 (running max, running sum) and the finished-split
-// counters, each at a 256-byte boundary.
+// [B][n_q][nsplit][2] fp32 (running max, running sum) at a 256-byte boundary.
 static __device__ __align__(256) unsigned char g_attn_scratch[kStaticScratchBytes];
 
 std::mutex g_setup_mutex;
@@ -65,8 +64,7 @@ extern "C" int ladder_attention_decode_noalloc(const float* q, const void* kv_la
   if (B <= 0 || n_q_heads <= 0 || head_dim <= 0 || max_position < 0)
     return set_error(LADDER_ERR_INVALID, "B, n_q_heads, head_dim must be positive and max_position >= 0");
   const size_t nsplit = ((size_t)max_position + 1 + kSplitLen - 1) / kSplitLen;
-  const size_t need = align256((size_t)B * n_q_heads * nsplit * head_dim * 4) +
-                      align256((size_t)B * n_q_heads * nsplit * 2 * 4) + (size_t)B * n_q_heads * 4;
+  const size_t need = align256((size_t)B * n_q_heads * nsplit * head_dim * 4) + (size_t)B * n_q_heads * nsplit * 2 * 4;
   if (need > kStaticScratchBytes) {
     char msg[200];
     snprintf(msg, sizeof(msg),
@@ -78,9 +76,8 @@ extern "C" int ladder_attention_decode_noalloc(const float* q, const void* kv_la
   void* scratch = nullptr;
   int rc = scratch_address(&scratch);
   if (rc) return rc;
-  // Every partial that the merge reads is written earlier in the same call; the
-  // finished-split counters, which must start at zero, are cleared by
-  // ladder_attention_decode on every call.
+  // Every partial that the combine step reads is written earlier in the same
+  // call, so nothing in the array has to start at zero.
   return ladder_attention_decode(q, kv_layer, kv_dtype, block_table, max_pages_per_seq, positions, B, n_q_heads,
                                  n_kv_heads, head_dim, page_size, scale, max_position, out, scratch,
                                  kStaticScratchBytes, stream);

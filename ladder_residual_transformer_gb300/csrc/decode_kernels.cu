@@ -409,13 +409,11 @@ cudaError_t launch_gemv(const GemvParams& p0, int mode, int wdt, int num_sms, cu
     p.kc = gemv_chunk(p.B, p.kfull);
     if (mode == GEMV_PARTIAL && p.kc < p.kfull) return cudaErrorInvalidValue;  // shard partials stage one chunk
     const size_t smem = (size_t)bt * p.kc * sizeof(float);
-    // K split: the smallest that gives about two waves of 4 CTAs per SM (more
-    // warps in flight, shorter tail) while each slice stays a multiple of 256;
-    // at most 4 ways, 8 for depths of 8192 and more.
+    // K split: the smallest that gives at least 1.5 CTAs per SM (more warps in
+    // flight for short, wide matrices) while each slice stays a multiple of 256.
     p.ks = 1;
     if (p.kc >= p.kfull) {
-      const int ks_max = p.K >= 8192 ? 8 : 4;
-      while (p.ks < ks_max && (long long)p.n_tasks * p.ks < (long long)num_sms * 64 &&
+      while (p.ks < GEMV_WARPS && (long long)p.n_tasks * p.ks < (long long)num_sms * 12 &&
              (p.K / (2 * p.ks)) % 256 == 0)
         p.ks *= 2;
     }
@@ -438,10 +436,8 @@ cudaError_t launch_gemv(const GemvParams& p0, int mode, int wdt, int num_sms, cu
 // each page's contiguous [page_size][head_dim] slab) into padded shared memory,
 // so the whole split is a single memory round trip.  Thread t then scores key t
 // for all G heads; each warp normalises heads w, w+4 with warp-shuffle max/sum
-// reductions; threads (dim pair, key group) accumulate P V.  Each split writes
-// its partial (max, sum, o); the last split of a (sequence, KV head) to finish
-// (an atomic counter after a memory fence) merges all splits in the fixed order
-// 0..ns-1 and resets the counter, so no separate combine launch is needed.
+// reductions; threads (dim pair, key group) accumulate P V.  Partial (max, sum,
+// o) per split are merged by attn_combine_kernel.
 // ---------------------------------------------------------------------------
 constexpr int ATT_THREADS = 128;
 constexpr int ATT_MAXG = 8;
@@ -566,55 +562,48 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_decode_kernel(const AttnDeco
         if (h < G) o_red[kg - 1][h][dp] = o[h];
     }
     __syncthreads();
-    if (kg == 0) {
-      for (int g2 = 0; g2 < KG - 1; ++g2) {
+    if (kg != 0) return;
+    for (int g2 = 0; g2 < KG - 1; ++g2) {
 #pragma unroll
-        for (int h = 0; h < ATT_MAXG; ++h) {
-          if (h < G) {
-            o[h].x += o_red[g2][h][dp].x;
-            o[h].y += o_red[g2][h][dp].y;
-          }
+      for (int h = 0; h < ATT_MAXG; ++h) {
+        if (h < G) {
+          o[h].x += o_red[g2][h][dp].x;
+          o[h].y += o_red[g2][h][dp].y;
         }
       }
     }
   }
-  if (kg == 0) {
 #pragma unroll
-    for (int h = 0; h < ATT_MAXG; ++h) {
-      if (h >= G) continue;
-      const size_t idx = ((size_t)b * p.n_q + (size_t)kvh * G + h) * p.nsplit + split;
-      *reinterpret_cast<float2*>(p.part_o + idx * HD + 2 * dp) = o[h];
-      if (dp == 0) {
-        p.part_ml[idx * 2] = m_s[h];
-        p.part_ml[idx * 2 + 1] = l_s[h];
-      }
+  for (int h = 0; h < ATT_MAXG; ++h) {
+    if (h >= G) continue;
+    const size_t idx = ((size_t)b * p.n_q + (size_t)kvh * G + h) * p.nsplit + split;
+    *reinterpret_cast<float2*>(p.part_o + idx * HD + 2 * dp) = o[h];
+    if (dp == 0) {
+      p.part_ml[idx * 2] = m_s[h];
+      p.part_ml[idx * 2 + 1] = l_s[h];
     }
   }
+}
 
-  // 5. the last split of this (sequence, KV head) merges every split
-  __shared__ int s_last;
-  __threadfence();
-  __syncthreads();
+template <int HD>
+__global__ void __launch_bounds__(HD) attn_combine_kernel(const AttnDecodeParams p) {
+  pdl_trigger();
+  pdl_wait();
+  const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+  const int ctx = p.seq_lens[b] + 1;
   int ns = (ctx + p.split_len - 1) / p.split_len;
   if (ns > p.nsplit) ns = p.nsplit;
-  if (tid == 0) s_last = atomicAdd(&p.counters[b * p.kv.n_kv + kvh], 1) == ns - 1;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int i = tid; i < G * HD; i += ATT_THREADS) {
-    const int h = i / HD, d = i % HD;
-    const size_t base = ((size_t)b * p.n_q + (size_t)kvh * G + h) * p.nsplit;
-    float M = -INFINITY;
-    for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, __ldcg(p.part_ml + (base + s2) * 2));
-    float L = 0.f, acc = 0.f;
-    for (int s2 = 0; s2 < ns; ++s2) {
-      const float w = __expf(__ldcg(p.part_ml + (base + s2) * 2) - M);
-      L += w * __ldcg(p.part_ml + (base + s2) * 2 + 1);
-      acc += w * __ldcg(p.part_o + (base + s2) * HD + d);
-    }
-    p.out[(size_t)b * p.n_q * HD + ((size_t)kvh * G + h) * HD + d] = acc / L;
+  const size_t base = ((size_t)b * p.n_q + h) * p.nsplit;
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, p.part_ml[(base + s) * 2]);
+  float L = 0.f, acc = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const float m = p.part_ml[(base + s) * 2];
+    const float w = __expf(m - M);
+    L += w * p.part_ml[(base + s) * 2 + 1];
+    acc += w * p.part_o[(base + s) * HD + d];
   }
-  if (tid == 0) p.counters[b * p.kv.n_kv + kvh] = 0;
+  p.out[(size_t)b * p.n_q * HD + (size_t)h * HD + d] = acc / L;
 }
 
 static constexpr size_t att_dyn_smem(int hd) { return (size_t)2 * ATT_SPLIT * (hd + 8) * sizeof(bf16); }
@@ -645,7 +634,9 @@ static cudaError_t attn_configure_current_device() {
 template <typename KT, int HD>
 static cudaError_t attn_decode_go(const AttnDecodeParams& p, int B, int n_kv, cudaStream_t s, bool pdl) {
   const dim3 grid(p.nsplit, n_kv, B);
-  return launch_k(attn_decode_kernel<KT, HD>, grid, dim3(ATT_THREADS), att_dyn_smem(HD), s, pdl, p);
+  cudaError_t e = launch_k(attn_decode_kernel<KT, HD>, grid, dim3(ATT_THREADS), att_dyn_smem(HD), s, pdl, p);
+  if (e == cudaSuccess) e = launch_k(attn_combine_kernel<HD>, dim3(p.n_q, B), dim3(HD), 0, s, pdl, p);
+  return e;
 }
 
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, int B, int n_kv, int hd, int kv_dtype, cudaStream_t s,

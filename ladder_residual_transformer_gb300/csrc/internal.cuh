@@ -155,7 +155,6 @@ struct AttnDecodeParams {
   float scale;
   float* part_o;        // [B][n_q][nsplit][hd]
   float* part_ml;       // [B][n_q][nsplit][2]
-  int* counters;        // [B][n_kv] finished splits; zero between calls (the last split resets it)
   float* out;           // [B][n_q * hd]
 };
 

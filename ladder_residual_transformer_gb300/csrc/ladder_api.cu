@@ -51,7 +51,7 @@ constexpr int kSplitLen = 128;      // keys per decode-attention split
 constexpr int kArgmaxBlocks = 64;   // partial argmax blocks per sequence
 
 struct Plan {
-  size_t x[3], xn, q, ao, act, part_o, part_ml, att_cnt, am_v, am_i, rope_cos, rope_sin, meta, xlast, err, shard;
+  size_t x[3], xn, q, ao, act, part_o, part_ml, am_v, am_i, rope_cos, rope_sin, meta, xlast, err, shard;
   size_t total;
   int m_max, m_pad, nsplit_max;
 };
@@ -78,7 +78,6 @@ Plan make_plan(const ladder_config& c) {
   p.act = take(std::max(Mp * f * 2, Bm * f * 4));
   p.part_o = take(Bm * c.n_q_heads * (size_t)p.nsplit_max * c.head_dim * 4);
   p.part_ml = take(Bm * c.n_q_heads * (size_t)p.nsplit_max * 2 * 4);
-  p.att_cnt = take(Bm * c.n_kv_heads * 4);
   p.am_v = take(Bm * kArgmaxBlocks * 4);
   p.am_i = take(Bm * kArgmaxBlocks * 4);
   p.rope_cos = take((size_t)c.max_seq * (c.head_dim / 2) * 4);
@@ -346,7 +345,6 @@ int ladder_create(const ladder_config* cfg, const ladder_weights* w, void* works
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_fork, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_part, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaMemsetAsync(m->err(), 0, 256, stream);
-  if (e == cudaSuccess) e = cudaMemsetAsync(m->ws + plan.att_cnt, 0, (size_t)cfg->max_batch * cfg->n_kv_heads * 4, stream);
   if (e == cudaSuccess)
     e = launch_rope_tables(m->at<float>(plan.rope_cos), m->at<float>(plan.rope_sin), cfg->max_seq, cfg->head_dim,
                            cfg->rope_theta, stream);
@@ -587,8 +585,8 @@ int enqueue_decode_shard(ladder_model* m, ladder_kv* kv, const int32_t* tokens, 
       AttnDecodeParams a{};
       a.q = q; a.kv = kvl; a.seq_lens = kv->seq_lens; a.n_q = c.n_q_heads; a.split_len = kSplitLen;
       a.nsplit = nsplit; a.scale = 1.0f / sqrtf((float)c.head_dim);
-      a.part_o = m->at<float>(P.part_o); a.part_ml = m->at<float>(P.part_ml); a.counters = m->at<int>(P.att_cnt); a.out = ao;
-      LAUNCH(launch_attn_decode(a, B, c.n_kv_heads, c.head_dim, m->wdt, s, pdl), 1);
+      a.part_o = m->at<float>(P.part_o); a.part_ml = m->at<float>(P.part_ml); a.out = ao;
+      LAUNCH(launch_attn_decode(a, B, c.n_kv_heads, c.head_dim, m->wdt, s, pdl), 2);
       o.x = ao; o.ldx = qd; o.K = qd / ksh; o.kfull = qd; o.ldw = qd; o.w0 = L.wo;
     } else {  // MLP module
       GemvParams g{};
@@ -679,9 +677,9 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       AttnDecodeParams a{};
       a.q = q; a.kv = kvl; a.seq_lens = kv->seq_lens; a.n_q = c.n_q_heads; a.split_len = kSplitLen;
       a.nsplit = nsplit; a.scale = 1.0f / sqrtf((float)c.head_dim);
-      a.part_o = m->at<float>(P.part_o); a.part_ml = m->at<float>(P.part_ml); a.counters = m->at<int>(P.att_cnt); a.out = ao;
+      a.part_o = m->at<float>(P.part_o); a.part_ml = m->at<float>(P.part_ml); a.out = ao;
       pe = m->probe_start(LADDER_PROBE_ATTN, s);
-      LAUNCH(launch_attn_decode(a, B, c.n_kv_heads, c.head_dim, m->wdt, s, pdl), 1);
+      LAUNCH(launch_attn_decode(a, B, c.n_kv_heads, c.head_dim, m->wdt, s, pdl), 2);
       m->probe_stop(pe, s);
 
       if ((rc = use(k - 1, 0))) return rc;
@@ -902,13 +900,10 @@ int check_attention_shape(int32_t B, int32_t n_q, int32_t n_kv, int32_t hd, int3
   return LADDER_OK;
 }
 
-// Scratch of the standalone attention: partial outputs, partial (max, sum),
-// and one finished-split counter per (sequence, head) (only n_kv of them used).
 size_t attention_scratch(int32_t B, int32_t n_q, int32_t hd, int32_t max_position) {
   const size_t nsplit = ((size_t)max_position + 1 + kSplitLen - 1) / kSplitLen;
   const size_t po = align_up((size_t)B * n_q * nsplit * hd * 4, 256);
-  const size_t pm = align_up((size_t)B * n_q * nsplit * 2 * 4, 256);
-  return po + pm + (size_t)B * n_q * 4;
+  return po + (size_t)B * n_q * nsplit * 2 * 4;
 }
 
 }  // namespace
@@ -948,16 +943,11 @@ extern "C" int ladder_attention_decode(const float* q, const void* kv_layer, int
   a.split_len = kSplitLen;
   a.nsplit = (max_position + 1 + kSplitLen - 1) / kSplitLen;
   a.scale = scale;
-  const size_t po = align_up((size_t)B * n_q_heads * a.nsplit * head_dim * 4, 256);
-  const size_t pm = align_up((size_t)B * n_q_heads * a.nsplit * 2 * 4, 256);
   a.part_o = static_cast<float*>(scratch);
-  a.part_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) + po);
-  a.counters = reinterpret_cast<int*>(static_cast<char*>(scratch) + po + pm);
+  a.part_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) +
+                                       align_up((size_t)B * n_q_heads * a.nsplit * head_dim * 4, 256));
   a.out = out;
-  // the finished-split counters must start at zero (the caller's scratch holds anything)
-  cudaError_t e = cudaMemsetAsync(a.counters, 0, (size_t)B * n_kv_heads * 4, reinterpret_cast<cudaStream_t>(stream));
-  if (e == cudaSuccess)
-    e = launch_attn_decode(a, B, n_kv_heads, head_dim, kv_dtype, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_attn_decode(a, B, n_kv_heads, head_dim, kv_dtype, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(LADDER_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
   return LADDER_OK;
 }
