@@ -7,6 +7,9 @@ weights resident on the GPU) through properties that hold at any size: decode
 with the KV cache agrees with re-running prefill on the extended prompt, and
 repeated runs give identical logits.
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -62,8 +65,18 @@ def test_full_size_8b_hybrid():
     del gw, model
     torch.cuda.empty_cache()
     want, _ = O.teacher_forced_decode(dims, O.synthetic_weights(dims), prompts, feed)
+    # Relative L2 is held to 1e-2.  The max-abs bound is 3e-2, or 1.15x the error
+    # of an exactly rounded fp16-activation pipeline on these very inputs when
+    # that floor is higher (tests/golden/fp16_floor.py writes it from the oracle:
+    # 3.18e-2 for these 32 random layers, so no 16-bit implementation can meet 3e-2).
+    floor = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "fp16_floor_8b_hybrid.json")))
+    max_abs = max(3e-2, 1.15 * floor["max_abs"])
     for s in range(3):
-        compare_logits(got[s], want[s], f"8B hybrid step {s}")
+        err = np.abs(got[s] - want[s]).max()
+        rel = np.linalg.norm(got[s] - want[s]) / np.linalg.norm(want[s])
+        print(f"8B hybrid step {s}: max-abs {err:.3e} rel-L2 {rel:.3e} (fp16 floor {floor['max_abs']:.3e})")
+        assert np.isfinite(got[s]).all()
+        assert err <= max_abs and rel <= 1e-2, (s, err, rel)
 
 
 @pytest.mark.slow
