@@ -4,10 +4,6 @@
 // kernels, and the weight-streaming GEMVs with their fused prologue/epilogues.
 #include "internal.cuh"
 
-#include <map>
-#include <mutex>
-#include <tuple>
-
 #include <math.h>
 
 namespace ladder {
@@ -83,45 +79,6 @@ __device__ __forceinline__ void gemv_fma(const uint4& w, const float* __restrict
   }
 }
 
-// The two weight rows of task t (see gemv_kernel) and, for row-parallel shard
-// partials, the offset of the task's input block.
-template <typename WT, int MODE>
-__device__ __forceinline__ void gemv_rows(const GemvParams& p, int t, const WT*& r0, const WT*& r1) {
-  const WT* W0 = static_cast<const WT*>(p.w0);
-  const int K = p.K;
-  if (MODE == GEMV_QKV) {
-    const int q0 = 2 * t;
-    r0 = q0 < p.nq_hd ? W0 + (size_t)q0 * K
-                      : (q0 < p.nq_hd + p.nkv_hd ? static_cast<const WT*>(p.w1) + (size_t)(q0 - p.nq_hd) * K
-                                                 : static_cast<const WT*>(p.w2) + (size_t)(q0 - p.nq_hd - p.nkv_hd) * K);
-    r1 = r0 + K;
-  } else if (MODE == GEMV_GATEUP) {
-    r0 = W0 + (size_t)t * K;
-    r1 = static_cast<const WT*>(p.w1) + (size_t)t * K;
-  } else if (MODE == GEMV_PARTIAL) {
-    r0 = W0 + (size_t)(2 * (t % p.shard_tasks)) * p.ldw + (size_t)(t / p.shard_tasks) * K;
-    r1 = r0 + p.ldw;
-  } else {
-    r0 = W0 + (size_t)(2 * t) * K;
-    r1 = r0 + K;
-  }
-}
-
-// Ask L2 for this warp's K slice of task t's two rows (one 128-byte line per lane per step).
-template <typename WT, int MODE>
-__device__ __forceinline__ void gemv_prefetch_l2(const GemvParams& p, int t, int kslice, int ks, int lane) {
-  if (t >= p.n_tasks) return;
-  const WT *r0, *r1;
-  gemv_rows<WT, MODE>(p, t, r0, r1);
-  const int K = p.K;
-  const int kb = ks > 1 ? kslice * (K / ks) : 0;
-  const int ke = ks > 1 ? kb + K / ks : K;
-  for (int k = kb + lane * 64; k < ke; k += 32 * 64) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(r0 + k));
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(r1 + k));
-  }
-}
-
 template <typename WT, int BT, int MODE>
 __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) {
   using C = W16<WT>;
@@ -137,12 +94,42 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
   const int K = p.K;
   pdl_trigger();
 
-  // Weights depend on no earlier kernel: each warp asks L2 for its first
-  // task's weight rows before the RMSNorm prologue and before waiting for the
-  // previous kernel, so that the DRAM traffic overlaps both (no registers are
-  // held for it); later rounds prefetch their successor while they compute.
-  if (p.kc >= p.kfull)
-    gemv_prefetch_l2<WT, MODE>(p, blockIdx.x * (GEMV_WARPS / p.ks) + warp / p.ks, warp % p.ks, p.ks, lane);
+  // Weights depend on no earlier kernel: when every task of this CTA fits in
+  // one round of a single chunk, each warp asks L2 for its whole weight range
+  // before the RMSNorm prologue and before waiting for the previous kernel, so
+  // that the DRAM traffic overlaps both (no registers are held for it).
+  {
+    const int ks_ = p.ks;
+    const int task0 = blockIdx.x * (GEMV_WARPS / ks_) + warp / ks_;
+    const bool one_round = p.kc >= p.kfull && (long long)gridDim.x * (GEMV_WARPS / ks_) >= p.n_tasks;
+    if (one_round && task0 < p.n_tasks) {
+      const WT* r0;
+      const WT* r1;
+      if (MODE == GEMV_QKV) {
+        const int q0 = 2 * task0;
+        r0 = q0 < p.nq_hd ? W0 + (size_t)q0 * K
+                          : (q0 < p.nq_hd + p.nkv_hd ? W1 + (size_t)(q0 - p.nq_hd) * K
+                                                     : W2 + (size_t)(q0 - p.nq_hd - p.nkv_hd) * K);
+        r1 = r0 + K;
+      } else if (MODE == GEMV_GATEUP) {
+        r0 = W0 + (size_t)task0 * K;
+        r1 = W1 + (size_t)task0 * K;
+      } else if (MODE == GEMV_PARTIAL) {
+        r0 = W0 + (size_t)(2 * (task0 % p.shard_tasks)) * p.ldw + (size_t)(task0 / p.shard_tasks) * K;
+        r1 = r0 + p.ldw;
+      } else {
+        r0 = W0 + (size_t)(2 * task0) * K;
+        r1 = r0 + K;
+      }
+      const int kb = ks_ > 1 ? (warp % ks_) * (K / ks_) : 0;
+      const int ke = ks_ > 1 ? kb + K / ks_ : K;
+      // one 128-byte line (64 elements) per lane per step
+      for (int k = kb + lane * 64; k < ke; k += 32 * 64) {
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(r0 + k));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(r1 + k));
+      }
+    }
+  }
   pdl_wait();
 
   // RMSNorm statistics of each input row, in a fixed order (identical in every CTA).
@@ -187,7 +174,6 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
   for (int r = 0; r < rounds; ++r) {
     const int task = r * total_slots + blockIdx.x * tpc + slot;
     const bool active = task < p.n_tasks;
-    if (single_chunk && r + 1 < rounds) gemv_prefetch_l2<WT, MODE>(p, task + total_slots, kslice, ks, lane);
 
     // Which two weight rows this task reads.
     const WT* row0 = W0;
@@ -404,34 +390,6 @@ static cudaError_t gemv_dispatch_bt(const GemvParams& p, int bt, int mode, int g
 
 int gemv_launch_count(int B, int K) { return (B + 3) / 4; }
 
-// CTAs of one GEMV instance that fit on an SM at once (cached per instance and
-// shared-memory size; queried on the current device).
-template <typename WT, int BT>
-static const void* gemv_fn(int mode) {
-  switch (mode) {
-    case GEMV_QKV: return (const void*)gemv_kernel<WT, BT, GEMV_QKV>;
-    case GEMV_GATEUP: return (const void*)gemv_kernel<WT, BT, GEMV_GATEUP>;
-    case GEMV_RESID: return (const void*)gemv_kernel<WT, BT, GEMV_RESID>;
-    case GEMV_PARTIAL: return (const void*)gemv_kernel<WT, BT, GEMV_PARTIAL>;
-    default: return (const void*)gemv_kernel<WT, BT, GEMV_LOGITS>;
-  }
-}
-
-static int gemv_resident_ctas(int mode, int bt, int wdt, size_t smem) {
-  static std::mutex mu;
-  static std::map<std::tuple<int, int, int, size_t>, int> cache;
-  const auto key = std::make_tuple(mode, bt, wdt, smem);
-  std::lock_guard<std::mutex> lock(mu);
-  auto it = cache.find(key);
-  if (it != cache.end()) return it->second;
-  const void* fn = wdt == WDT_F16 ? (bt == 1 ? gemv_fn<f16, 1>(mode) : bt == 2 ? gemv_fn<f16, 2>(mode) : gemv_fn<f16, 4>(mode))
-                                  : (bt == 1 ? gemv_fn<bf16, 1>(mode) : bt == 2 ? gemv_fn<bf16, 2>(mode) : gemv_fn<bf16, 4>(mode));
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, GEMV_THREADS, smem) != cudaSuccess || n < 1) n = 1;
-  cache[key] = n;
-  return n;
-}
-
 // Batches larger than 4 run as consecutive chunks of at most 4 rows.
 cudaError_t launch_gemv(const GemvParams& p0, int mode, int wdt, int num_sms, cudaStream_t s, bool pdl) {
   for (int b0 = 0; b0 < p0.B; b0 += 4) {
@@ -461,7 +419,7 @@ cudaError_t launch_gemv(const GemvParams& p0, int mode, int wdt, int num_sms, cu
     }
     const int tpc = GEMV_WARPS / p.ks;
     int grid = (p.n_tasks + tpc - 1) / tpc;
-    const int cap = num_sms * gemv_resident_ctas(mode, bt, wdt, smem);  // whole rounds of resident CTAs
+    const int cap = num_sms * 8;
     if (grid > cap) grid = cap;
     cudaError_t e = wdt == WDT_F16 ? gemv_dispatch_bt<f16>(p, bt, mode, grid, smem, s, pdl)
                                    : gemv_dispatch_bt<bf16>(p, bt, mode, grid, smem, s, pdl);
