@@ -21,114 +21,28 @@
 // by a clock limit: on expiry the kernel sets bit 1 of the error word, stops
 // issuing work, and still frees its TMEM before returning.
 #include "internal.cuh"
+#include "tcgen05.cuh"
 
 #include <cuda.h>
 #include <string.h>
 
 namespace ladder {
 
-constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_STAGES = 4;
+constexpr int TC_BM = 128, TC_BK = 64;
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;   // 16 KB
 constexpr int TC_BH_BYTES = 128 * TC_BK * 2;    // one 128-row half of B, 16 KB
-constexpr int TC_STAGE_BYTES = TC_A_BYTES + 2 * TC_BH_BYTES;
-constexpr int TC_SMEM = TC_STAGES * TC_STAGE_BYTES + 1024 + 256;
+// Shared memory for the stage ring: 7 stages of 32 KB at BN = 128, 4 of 48 KB at BN = 256.
+constexpr int TC_SMEM = 7 * (TC_A_BYTES + TC_BH_BYTES) + 1024 + 256;
 constexpr int TC_THREADS = 192;
 constexpr long long TC_WAIT_LIMIT = 4000000000LL;  // cycles (about 2 s)
 
-// ---------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-
-// Wait for the phase of parity `parity` to complete; false after the clock limit.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  const uint32_t addr = smem_u32(bar);
-  const long long start = clock64();
-  while (true) {
-    uint32_t done;
-    asm volatile(
-        "{\n.reg .pred p;\n"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        "selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(done)
-        : "r"(addr), "r"(parity)
-        : "memory");
-    if (done) return true;
-    if (clock64() - start > TC_WAIT_LIMIT) return false;
-  }
+  return mbar_wait(bar, parity, TC_WAIT_LIMIT);
 }
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c_inner, int c_row,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c_inner), "r"(c_row), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart (stride byte offset), descriptor version 1.
-__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)1 << 16;            // leading byte offset (unused for swizzled K-major)
-  d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset
-  d |= (uint64_t)1 << 46;            // version
-  d |= (uint64_t)2 << 61;            // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor of kind::f16: A and B of format `fmt` (0 = f16, 1 = bf16),
-// fp32 D, both K-major, M x N.
-__host__ __device__ constexpr uint32_t umma_idesc(int M, int N, uint32_t fmt) {
-  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n.reg .pred p;\n"
-      "setp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
-      ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
+// K-major operand tile in the 128-byte-swizzled layout that TMA writes: 8-row
+// groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) { return umma_desc_sw128(saddr, 16, 1024); }
 
 // ---------------------------------------------------------------------------
 // B-operand half selection: (tensor map index, first row) of 128-row half h of
@@ -268,7 +182,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
           const uint32_t b_base = a_base + TC_A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < TC_BK / 16; ++kk)
-            umma_bf16(d, umma_desc(a_base + kk * 32), umma_desc(b_base + kk * 32), idesc, (kb | kk) != 0);
+            umma_f16(d, umma_desc(a_base + kk * 32), umma_desc(b_base + kk * 32), idesc, (kb | kk) != 0);
           umma_commit(&empty[s]);
         }
         umma_commit(&tfull[acc]);  // also after a bail, so that the MMAs in flight finish first
@@ -402,6 +316,22 @@ bool make_tma_map(void* map_out, const void* base, uint64_t rows, uint64_t cols,
   CUresult r = fn(reinterpret_cast<CUtensorMap*>(map_out), dt, 2, const_cast<void*>(base),
                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// One layer of the paged KV pool viewed as [pages * 2 * n_kv][page_size][hd]
+// 16-bit elements; box = 64 elements x page_size slots x 1, 128-byte swizzle.
+bool make_kv_tma_map(void* map_out, const void* base, uint64_t num_pages, int n_kv, int page_size, int hd, int wdt) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || hd % 64 || page_size < 8 || page_size > 256 || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)page_size, num_pages * 2 * (cuuint64_t)n_kv};
+  cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)page_size * hd * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)page_size, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt = wdt == WDT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = fn(reinterpret_cast<CUtensorMap*>(map_out), dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

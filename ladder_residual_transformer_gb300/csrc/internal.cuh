@@ -176,7 +176,7 @@ struct GemmParams {
 };
 
 struct AttnPrefillParams {
-  const void* q;        // [M][n_q * hd] rotated queries (weight dtype, like the KV cache)
+  const void* q;        // [M][n_q * hd] rotated queries (weight dtype, like the KV cache); read through a tensor map
   KvLayer kv;
   const int* seq_start; // first packed row of sequence b
   const int* seq_len;   // length of sequence b
@@ -206,12 +206,17 @@ cudaError_t launch_rmsnorm_rows(const float* x, int M, int d, const void* g, flo
                                 cudaStream_t s);
 // Tensor-core GEMM (tcgen05 + TMA).  Maps are CUtensorMap objects made by make_tma_map.
 bool make_tma_map(void* map_out, const void* base, uint64_t rows, uint64_t cols, int wdt);
+// One layer of the paged KV pool as a 3-D map (see gemm_tcgen05.cu).
+bool make_kv_tma_map(void* map_out, const void* base, uint64_t num_pages, int n_kv, int page_size, int hd, int wdt);
 cudaError_t gemm_tc_configure();
 cudaError_t launch_gemm_tc(const void* a_map, const void* b0, const void* b1, const void* b2, const GemmParams& p,
                            int mode, int wdt, int num_sms, int* err, cudaStream_t s);
 // Tensor-core causal attention for packed prefill rows (mma.sync, bf16 Q/K/V).
-cudaError_t attn_prefill_configure();
-cudaError_t launch_attn_prefill_tc(const AttnPrefillParams& p, int hd, int wdt, int B, int max_len, cudaStream_t s);
+// Prefill attention on tcgen05: q_map = make_tma_map of the query rows, kv_map =
+// make_kv_tma_map of the layer; head_dim 64 or 128.
+cudaError_t attn_prefill_tcgen05_configure();
+cudaError_t launch_attn_prefill_tcgen05(const void* q_map, const void* kv_map, const AttnPrefillParams& p, int hd,
+                                        int wdt, int B, int max_len, int* err, cudaStream_t s);
 cudaError_t launch_gather_rows(const float* x, int d, const int* rows, int B, float* out,
                                cudaStream_t s);
 cudaError_t launch_set_lens(const int* lens, int B, int* seq_lens, cudaStream_t s);

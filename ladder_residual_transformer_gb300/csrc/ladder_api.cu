@@ -73,7 +73,7 @@ Plan make_plan(const ladder_config& c) {
   };
   for (int i = 0; i < 3; ++i) p.x[i] = take(M * d * 4);
   p.xn = take(Mp * d * 2);
-  p.q = take(std::max(M * qd * 2, Bm * qd * 4));
+  p.q = take(std::max(Mp * qd * 2, Bm * qd * 4));
   p.ao = take(std::max(Mp * qd * 2, Bm * qd * 4));
   p.act = take(std::max(Mp * f * 2, Bm * f * 4));
   p.part_o = take(Bm * c.n_q_heads * (size_t)p.nsplit_max * c.head_dim * 4);
@@ -165,6 +165,7 @@ struct ladder_model {
   std::vector<LayerW> layers;
   std::vector<LayerMaps> maps;
   CUtensorMap map_xn, map_ao, map_act;  // activation operands, m_pad rows
+  CUtensorMap map_q;  // rotated queries [m_pad][n_q * hd], the prefill attention operand
   char* ws;
   Plan plan;
   int num_sms;
@@ -233,6 +234,7 @@ struct ladder_kv {
   std::vector<int32_t> host_lens;
   std::vector<int32_t> host_table;
   std::vector<int32_t> pages_of;  // assigned pages per sequence
+  std::vector<CUtensorMap> maps;   // per layer: the pool as a 3-D TMA map
 
   KvLayer layer(int l) const {
     KvLayer v;
@@ -319,7 +321,8 @@ int ladder_create(const ladder_config* cfg, const ladder_weights* w, void* works
     const int wdt = c.weight_dtype;
     bool ok = make_tma_map(&m->map_xn, m->ws + plan.xn, Mp, d, wdt) &&
               make_tma_map(&m->map_ao, m->ws + plan.ao, Mp, qd, wdt) &&
-              make_tma_map(&m->map_act, m->ws + plan.act, Mp, f, wdt);
+              make_tma_map(&m->map_act, m->ws + plan.act, Mp, f, wdt) &&
+              make_tma_map(&m->map_q, m->ws + plan.q, Mp, qd, wdt);
     m->maps.resize(c.n_layers);
     for (int l = 0; ok && l < c.n_layers; ++l) {
       const LayerW& L = m->layers[l];
@@ -339,7 +342,7 @@ int ladder_create(const ladder_config* cfg, const ladder_weights* w, void* works
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess) e = gemv_configure();
   if (e == cudaSuccess) e = gemm_tc_configure();
-  if (e == cudaSuccess) e = attn_prefill_configure();
+  if (e == cudaSuccess) e = attn_prefill_tcgen05_configure();
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&m->aux, cudaStreamNonBlocking);
   for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&m->ev_slot[i], cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_fork, cudaEventDisableTiming);
@@ -397,6 +400,15 @@ int ladder_kv_create(ladder_model* m, void* pool, int32_t num_pages, int32_t max
   kv->host_lens.assign(m->cfg.max_batch, 0);
   kv->host_table.assign((size_t)m->cfg.max_batch * max_pages_per_seq, -1);
   kv->pages_of.assign(m->cfg.max_batch, 0);
+  const ladder_config& c = m->cfg;
+  kv->maps.resize(c.n_layers);
+  for (int l = 0; l < c.n_layers; ++l) {
+    if (!make_kv_tma_map(&kv->maps[l], kv->layer(l).base, num_pages, c.n_kv_heads, c.page_size, c.head_dim,
+                         m->wdt)) {
+      delete kv;
+      return fail(LADDER_ERR_CUDA, "ladder_kv_create: could not encode the KV pool tensor map");
+    }
+  }
   *out = kv;
   return LADDER_OK;
 }
@@ -853,7 +865,7 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
       AttnPrefillParams a{};
       a.q = qb; a.kv = kvl; a.seq_start = d_start; a.seq_len = d_lens;
       a.n_q = c.n_q_heads; a.scale = 1.0f / sqrtf((float)c.head_dim); a.out = aob;
-      LAUNCH(launch_attn_prefill_tc(a, c.head_dim, wdt, B, max_len, s), 1);
+      LAUNCH(launch_attn_prefill_tcgen05(&m->map_q, &kv->maps[l], a, c.head_dim, wdt, B, max_len, m->err(), s), 1);
 
       GemmParams o{};
       o.M = M; o.N = d; o.K = qd; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);

@@ -1,6 +1,6 @@
 // Prefill-side helper kernels: RMSNorm of the stream rows into the 16-bit
 // operand of the next tensor-core GEMM, and small gathers.  The projection
-// GEMMs are in gemm_tcgen05.cu and the causal attention in attn_prefill.cu.
+// GEMMs are in gemm_tcgen05.cu and the causal attention in attn_prefill_tcgen05.cu.
 #include "internal.cuh"
 
 #include <math.h>
