@@ -14,9 +14,10 @@
 //
 // Warp roles (192 threads):
 //   warps 0-3  softmax + epilogue, thread r owns query row r (TMEM lane r);
-//   warp 4     one thread issues the TMA copies: the Q tile once, then K and V
-//              tiles page by page from the paged KV cache into a ring of
-//              stages (3-D tensor map over [page*2*n_kv + kv*n_kv + head][slot][dim]);
+//   warp 4     issues the TMA copies: the Q tile once, then K and V tiles
+//              page by page from the paged KV cache into a ring of stages
+//              (3-D tensor map over [page*2*n_kv + kv*n_kv + head][slot][dim]),
+//              one lane per page of the tile;
 //   warp 5     allocates TMEM (S double buffer + O) and one thread issues the
 //              MMAs: S_{j+1} is issued before PV_j so that the tensor cores
 //              compute the next scores while the softmax warps work on P_j.
@@ -123,36 +124,48 @@ __global__ void __launch_bounds__(FT_THREADS, 1)
   const uint32_t tmem_o = tmem + 256;
 
   if (warp == 4) {
+    // Lane c < nch issues the K and V boxes of page chunk c of the tile; the
+    // page ids of tile j + 1 are read while tile j's stage is awaited, so the
+    // block-table latency stays off the copy path.
+    const int ps = p.kv.page_size, cpt = FT_BN / ps;
+    const int npg = (Tn + ps - 1) / ps;  // pages holding the sequence
+    const int* btr = p.kv.block_table + (size_t)b * p.kv.max_pages;
     if (lane == 0) {
-      const int ps = p.kv.page_size;
       mbar_expect_tx(q_full, NB * FT_BLK);
       for (int c = 0; c < NB; ++c)
         tma_load_2d(smem + L::Q_OFF + c * FT_BLK, &maps.q, h * HD + c * 64, start + qb * FT_BM, q_full);
-      int j = 0;
-      for (; j < n_kb; ++j) {
-        const int s = j % ST;
-        if (j >= ST && !mbar_wait(&kv_empty[s], ((j / ST) - 1) & 1, FT_WAIT_LIMIT)) {
-          atomicOr(err, 2);
-          *bail = 1;
-        }
-        if (*bail) break;
-        const int key0 = j * FT_BN;
-        int nch = (Tn - key0 + ps - 1) / ps;
-        if (nch > FT_BN / ps) nch = FT_BN / ps;
-        mbar_expect_tx(&kv_full[s], (uint32_t)(nch * ps * 128 * NB * 2));
-        uint8_t* kdst = smem + L::KV_OFF + s * L::STAGE_BYTES;
+    }
+    int pg = lane < cpt && lane < npg ? btr[lane] : 0;
+    int j = 0;
+    for (; j < n_kb; ++j) {
+      const int s = j % ST;
+      const int nidx = (j + 1) * cpt + lane;
+      const int pg_next = j + 1 < n_kb && lane < cpt && nidx < npg ? btr[nidx] : 0;
+      bool ok = j < ST || mbar_wait(&kv_empty[s], ((j / ST) - 1) & 1, FT_WAIT_LIMIT);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok && lane == 0) {
+        atomicOr(err, 2);
+        *bail = 1;
+      }
+      if (__shfl_sync(0xffffffffu, (int)(!ok || *bail), 0)) break;
+      const int key0 = j * FT_BN;
+      int nch = (Tn - key0 + ps - 1) / ps;
+      if (nch > cpt) nch = cpt;
+      if (lane == 0) mbar_expect_tx(&kv_full[s], (uint32_t)(nch * ps * 128 * NB * 2));
+      __syncwarp();
+      if (lane < nch) {
+        uint8_t* kdst = smem + L::KV_OFF + s * L::STAGE_BYTES + lane * ps * 128;
         uint8_t* vdst = kdst + NB * FT_BLK;
-        const int* bt = p.kv.block_table + (size_t)b * p.kv.max_pages + key0 / ps;
-        for (int c = 0; c < nch; ++c) {
-          const int page = bt[c];
-          const int zk = (page * 2) * p.kv.n_kv + kvh, zv = zk + p.kv.n_kv;
-          for (int blk = 0; blk < NB; ++blk) {
-            tma_load_3d(kdst + blk * FT_BLK + c * ps * 128, &maps.kv, blk * 64, 0, zk, &kv_full[s]);
-            tma_load_3d(vdst + blk * FT_BLK + c * ps * 128, &maps.kv, blk * 64, 0, zv, &kv_full[s]);
-          }
+        const int zk = (pg * 2) * p.kv.n_kv + kvh, zv = zk + p.kv.n_kv;
+        for (int blk = 0; blk < NB; ++blk) {
+          tma_load_3d(kdst + blk * FT_BLK, &maps.kv, blk * 64, 0, zk, &kv_full[s]);
+          tma_load_3d(vdst + blk * FT_BLK, &maps.kv, blk * 64, 0, zv, &kv_full[s]);
         }
       }
-      // No copy into this CTA's shared memory may be in flight at exit.
+      pg = pg_next;
+    }
+    // No copy into this CTA's shared memory may be in flight at exit.
+    if (lane == 0) {
       mbar_wait(q_full, 0, FT_WAIT_LIMIT);
       for (int k = j - ST < 0 ? 0 : j - ST; k < j; ++k) mbar_wait(&kv_full[k % ST], (k / ST) & 1, FT_WAIT_LIMIT);
     }
@@ -222,13 +235,7 @@ __global__ void __launch_bounds__(FT_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       float sv[FT_BN];
-#pragma unroll
-      for (int c = 0; c < FT_BN / 32; ++c) {
-        float t[32];
-        tmem_ld32(tmem + lane_base + sb * FT_BN + c * 32, t);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) sv[c * 32 + e] = t[e];
-      }
+      tmem_ld128(tmem + lane_base + sb * FT_BN, sv);
       // S buffer sb may be overwritten by S_{j+2}
       tc_fence_before();
       __syncwarp();
@@ -240,9 +247,14 @@ __global__ void __launch_bounds__(FT_THREADS, 1)
         for (int e = 0; e < FT_BN; ++e)
           if (key0 + e > lim) sv[e] = -INFINITY;
       }
-      float mx = sv[0];
+      // row maximum: eight independent chains, then a tree
+      float m8[8];
 #pragma unroll
-      for (int e = 1; e < FT_BN; ++e) mx = fmaxf(mx, sv[e]);
+      for (int e = 0; e < 8; ++e) m8[e] = sv[e];
+#pragma unroll
+      for (int e = 8; e < FT_BN; ++e) m8[e & 7] = fmaxf(m8[e & 7], sv[e]);
+      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       const float mt = mx * sl2;
       bool rescale = false;
       float corr = 1.f;
@@ -261,14 +273,14 @@ __global__ void __launch_bounds__(FT_THREADS, 1)
         if (!ok) break;
       }
       uint8_t* prow = smem + L::P_OFF + pb * L::P_BYTES + r * 128;
-      float rs = 0.f;
+      float r8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c8 = 0; c8 < FT_BN / 8; ++c8) {
         float pv[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           pv[e] = ex2_approx(fmaf(sv[c8 * 8 + e], sl2, -m_ref));
-          rs += pv[e];
+          r8[e] += pv[e];
         }
         uint4 pk;
         pk.x = C::pack(pv[0], pv[1]);
@@ -278,6 +290,7 @@ __global__ void __launch_bounds__(FT_THREADS, 1)
         const int blk = c8 >> 3, chunk = c8 & 7;
         *reinterpret_cast<uint4*>(prow + blk * FT_BLK + ((chunk ^ (r & 7)) << 4)) = pk;
       }
+      const float rs = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
       l_sum += rs;
       // keys past the sequence end: zero their V rows (the MMA multiplies them by P = 0)
       if (j == n_kb - 1 && Tn - key0 < FT_BN) {

@@ -79,6 +79,85 @@ __device__ __forceinline__ void gemv_fma(const uint4& w, const float* __restrict
   }
 }
 
+// The two weight rows of GEMV task `task` (see the task definition above); for
+// QKV also which matrix (kind 0 = q, 1 = k, 2 = v) and the first row inside it.
+template <typename WT, int MODE>
+__device__ __forceinline__ void gemv_task_rows(const GemvParams& p, int task, const WT*& row0, const WT*& row1,
+                                               int& kind, int& local, int& koff) {
+  const WT* W0 = static_cast<const WT*>(p.w0);
+  const WT* W1 = static_cast<const WT*>(p.w1);
+  const WT* W2 = static_cast<const WT*>(p.w2);
+  const int K = p.K;
+  kind = 0;
+  local = 0;
+  koff = 0;
+  if (MODE == GEMV_QKV) {
+    const int r0 = 2 * task;
+    if (r0 < p.nq_hd) {
+      local = r0; kind = 0; row0 = W0 + (size_t)local * K;
+    } else if (r0 < p.nq_hd + p.nkv_hd) {
+      local = r0 - p.nq_hd; kind = 1; row0 = W1 + (size_t)local * K;
+    } else {
+      local = r0 - p.nq_hd - p.nkv_hd; kind = 2; row0 = W2 + (size_t)local * K;
+    }
+    row1 = row0 + K;
+  } else if (MODE == GEMV_GATEUP) {
+    row0 = W0 + (size_t)task * K;
+    row1 = W1 + (size_t)task * K;
+  } else if (MODE == GEMV_PARTIAL) {
+    koff = (task / p.shard_tasks) * K;
+    row0 = W0 + (size_t)(2 * (task % p.shard_tasks)) * p.ldw + koff;
+    row1 = row0 + p.ldw;
+  } else {
+    row0 = W0 + (size_t)(2 * task) * K;
+    row1 = row0 + K;
+  }
+}
+
+// Epilogue of task `task` for batch row b: (v0, v1) are the dot products of its
+// two weight rows.
+template <typename WT, int MODE>
+__device__ __forceinline__ void gemv_store(const GemvParams& p, int task, int b, int kind, int local, float v0,
+                                           float v1) {
+  using C = W16<WT>;
+  if (MODE == GEMV_QKV) {
+    const int hd = p.kv.head_dim;
+    const int pos = p.pos[b];
+    float r0 = v0, r1 = v1;
+    if (kind < 2) {
+      const int j = (local % hd) >> 1;
+      const float c = p.rope_cos[(size_t)pos * (hd >> 1) + j];
+      const float s = p.rope_sin[(size_t)pos * (hd >> 1) + j];
+      r0 = v0 * c - v1 * s;
+      r1 = v0 * s + v1 * c;
+    }
+    if (kind == 0) {
+      float* q = p.out + (size_t)b * p.ldo + local;
+      q[0] = r0;
+      q[1] = r1;
+    } else {
+      const int head = local / hd, dim = local % hd;
+      WT* dst = static_cast<WT*>(p.kv.base) + p.kv.slot(b, pos, kind - 1, head) + dim;
+      *reinterpret_cast<uint32_t*>(dst) = C::pack(r0, r1);
+    }
+  } else if (MODE == GEMV_GATEUP) {
+    p.out[(size_t)b * p.ldo + task] = silu_f(v0) * v1;
+  } else if (MODE == GEMV_RESID) {
+    const size_t n = 2 * (size_t)task;
+    p.out[(size_t)b * p.ldo + n] = p.x_res[(size_t)b * p.ldr + n] + v0;
+    p.out[(size_t)b * p.ldo + n + 1] = p.x_res[(size_t)b * p.ldr + n + 1] + v1;
+  } else if (MODE == GEMV_PARTIAL) {
+    // out is [B][k][d]: shard s writes its partial sums at s * (2 * shard_tasks)
+    const size_t n = (size_t)(task / p.shard_tasks) * (2 * p.shard_tasks) + 2 * (size_t)(task % p.shard_tasks);
+    p.out[(size_t)b * p.ldo + n] = v0;
+    p.out[(size_t)b * p.ldo + n + 1] = v1;
+  } else {
+    const size_t n = 2 * (size_t)task;
+    p.out[(size_t)b * p.ldo + n] = v0;
+    p.out[(size_t)b * p.ldo + n + 1] = v1;
+  }
+}
+
 template <typename WT, int BT, int MODE>
 __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) {
   using C = W16<WT>;
@@ -180,29 +259,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
     const WT* row1 = W0;
     int local = 0, kind = 0;  // QKV: kind 0 = q, 1 = k, 2 = v; local = row inside its matrix
     int koff = 0;             // PARTIAL: first input element of the task's shard
-    if (active) {
-      if (MODE == GEMV_QKV) {
-        const int r0 = 2 * task;
-        if (r0 < p.nq_hd) {
-          local = r0; kind = 0; row0 = W0 + (size_t)local * K;
-        } else if (r0 < p.nq_hd + p.nkv_hd) {
-          local = r0 - p.nq_hd; kind = 1; row0 = W1 + (size_t)local * K;
-        } else {
-          local = r0 - p.nq_hd - p.nkv_hd; kind = 2; row0 = W2 + (size_t)local * K;
-        }
-        row1 = row0 + K;
-      } else if (MODE == GEMV_GATEUP) {
-        row0 = W0 + (size_t)task * K;
-        row1 = W1 + (size_t)task * K;
-      } else if (MODE == GEMV_PARTIAL) {
-        koff = (task / p.shard_tasks) * K;
-        row0 = W0 + (size_t)(2 * (task % p.shard_tasks)) * p.ldw + koff;
-        row1 = row0 + p.ldw;
-      } else {
-        row0 = W0 + (size_t)(2 * task) * K;
-        row1 = row0 + K;
-      }
-    }
+    if (active) gemv_task_rows<WT, MODE>(p, task, row0, row1, kind, local, koff);
 
     float a0[BT], a1[BT];
 #pragma unroll
@@ -299,45 +356,249 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
 #pragma unroll
     for (int b = 0; b < BT; ++b) {
       if (lane != b || b >= p.B) continue;
-      const float v0 = a0[b], v1 = a1[b];
-      if (MODE == GEMV_QKV) {
-        const int hd = p.kv.head_dim;
-        const int pos = p.pos[b];
-        float r0 = v0, r1 = v1;
-        if (kind < 2) {
-          const int j = (local % hd) >> 1;
-          const float c = p.rope_cos[(size_t)pos * (hd >> 1) + j];
-          const float s = p.rope_sin[(size_t)pos * (hd >> 1) + j];
-          r0 = v0 * c - v1 * s;
-          r1 = v0 * s + v1 * c;
-        }
-        if (kind == 0) {
-          float* q = p.out + (size_t)b * p.ldo + local;
-          q[0] = r0;
-          q[1] = r1;
-        } else {
-          const int head = local / hd, dim = local % hd;
-          WT* dst = static_cast<WT*>(p.kv.base) + p.kv.slot(b, pos, kind - 1, head) + dim;
-          *reinterpret_cast<uint32_t*>(dst) = C::pack(r0, r1);
-        }
-      } else if (MODE == GEMV_GATEUP) {
-        p.out[(size_t)b * p.ldo + task] = silu_f(v0) * v1;
-      } else if (MODE == GEMV_RESID) {
-        const size_t n = 2 * (size_t)task;
-        p.out[(size_t)b * p.ldo + n] = p.x_res[(size_t)b * p.ldr + n] + v0;
-        p.out[(size_t)b * p.ldo + n + 1] = p.x_res[(size_t)b * p.ldr + n + 1] + v1;
-      } else if (MODE == GEMV_PARTIAL) {
-        // out is [B][k][d]: shard s writes its partial sums at s * (2 * shard_tasks)
-        const size_t n = (size_t)(task / p.shard_tasks) * (2 * p.shard_tasks) + 2 * (size_t)(task % p.shard_tasks);
-        p.out[(size_t)b * p.ldo + n] = v0;
-        p.out[(size_t)b * p.ldo + n + 1] = v1;
-      } else {
-        const size_t n = 2 * (size_t)task;
-        p.out[(size_t)b * p.ldo + n] = v0;
-        p.out[(size_t)b * p.ldo + n + 1] = v1;
-      }
+      gemv_store<WT, MODE>(p, task, b, kind, local, a0[b], a1[b]);
     }
   }
+}
+
+// ---------------------------------------------------------------------------
+// Batched decode projection, 5..16 rows, on the tensor cores.  The GEMV above
+// streams every weight byte once per 4 rows; here mma.sync m16n8k16 takes the
+// weights as the M = 16 operand and the batch as N (two 8-wide tiles), so each
+// weight byte is streamed once for all 16 rows.
+//
+// Warp task = 8 GEMV tasks (row pairs): MMA row g < 8 is the first row of pair g,
+// row g + 8 its second, so lane (g, t) ends up holding both values of pair g for
+// batch rows 2t, 2t+1 (+8) and the GEMV epilogue applies unchanged.
+// K is permuted inside each 32-element block so that lane (g, t) reads the 16
+// contiguous bytes k = 8t..8t+7 of its two weight rows and of each staged
+// input row: element 8t + 4c + {0,1,2,3} plays logical column {2t, 2t+1, 2t+8,
+// 2t+9} of MMA k-block c.  A permutation of K applied to both operands leaves
+// every dot product unchanged.
+// The normalised inputs are staged in shared memory as 16-bit values (the
+// operand type of the MMA) in chunks of GM_KCH columns, rows padded by 16 bytes
+// so that the 16-byte reads of a warp are conflict-free.  Short matrices split K
+// across up to 8 warps, combined in a fixed order.
+// ---------------------------------------------------------------------------
+constexpr int GM_KCH = 2048;             // staged input columns per chunk
+constexpr int GM_LD = GM_KCH + 8;        // padded row length (elements)
+constexpr int GM_SMEM = 16 * GM_LD * 2;  // 16 rows of 16-bit values
+
+template <typename T>
+__device__ __forceinline__ void mma16816_f32(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+  if constexpr (W16<T>::umma_fmt == 1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
+template <typename WT, int MODE>
+__global__ void __launch_bounds__(GEMV_THREADS) gemv_mma_kernel(const GemvParams p) {
+  using C = W16<WT>;
+  const WT* g = static_cast<const WT*>(p.g);
+  extern __shared__ float4 gm_smem4[];
+  WT* xs = reinterpret_cast<WT*>(gm_smem4);  // [16][GM_LD] staged inputs
+  __shared__ float s_red[GEMV_WARPS][16];
+  __shared__ float s_rms[16];
+  __shared__ float s_part[GEMV_WARPS][8][32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gi = lane >> 2, ti = lane & 3;
+  const int K = p.K;
+  pdl_trigger();
+  pdl_wait();
+
+  // RMSNorm statistics of each input row, in a fixed order (identical in every CTA).
+  if (p.g != nullptr) {
+    float ss[16];
+#pragma unroll
+    for (int b = 0; b < 16; ++b) ss[b] = 0.f;
+    for (int i = tid * 4; i < K; i += GEMV_THREADS * 4) {
+#pragma unroll
+      for (int b = 0; b < 16; ++b) {
+        if (b < p.B) {
+          const float4 v = *reinterpret_cast<const float4*>(p.x + (size_t)b * p.ldx + i);
+          ss[b] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < 16; ++b) {
+      const float t = warp_sum(ss[b]);
+      if (lane == 0) s_red[warp][b] = t;
+    }
+    __syncthreads();
+    if (tid < 16) {
+      float t = 0.f;
+      for (int w = 0; w < GEMV_WARPS; ++w) t += s_red[w][tid];
+      s_rms[tid] = rsqrtf(t / (float)K + p.eps);
+    }
+    __syncthreads();
+  }
+
+  const int ks = p.ks;
+  const int tpc = GEMV_WARPS / ks;  // warp tasks per CTA per round
+  const int slot = warp / ks, kslice = warp % ks;
+  const int n_wtasks = (p.n_tasks + 7) / 8;
+  const int total_slots = gridDim.x * tpc;
+  const int rounds = (n_wtasks + total_slots - 1) / total_slots;
+  const bool single_chunk = K <= GM_KCH;
+
+  for (int r = 0; r < rounds; ++r) {
+    const int wtask = r * total_slots + blockIdx.x * tpc + slot;
+    const int task = wtask * 8 + gi;  // the row pair of this lane
+    const bool lane_active = wtask < n_wtasks && task < p.n_tasks;
+    const WT* row0;
+    const WT* row1;
+    int kind, local, koff;
+    gemv_task_rows<WT, MODE>(p, lane_active ? task : 0, row0, row1, kind, local, koff);
+
+    float acc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+
+    for (int k0 = 0; k0 < K; k0 += GM_KCH) {
+      const int kc = min(GM_KCH, K - k0);
+      if (!single_chunk || r == 0) {
+        __syncthreads();
+        // Stage rows 0..15 of the normalised input chunk as 16-bit values (zero rows past B).
+        for (int i = tid; i < 16 * (kc / 8); i += GEMV_THREADS) {
+          const int b = i / (kc / 8), k8 = (i % (kc / 8)) * 8;
+          uint4 pk = make_uint4(0, 0, 0, 0);
+          if (b < p.B) {
+            const float* src = p.x + (size_t)b * p.ldx + k0 + k8;
+            const float4 v0 = *reinterpret_cast<const float4*>(src);
+            const float4 v1 = *reinterpret_cast<const float4*>(src + 4);
+            float sc[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+            if (g != nullptr) {
+              const uint4 graw = *reinterpret_cast<const uint4*>(g + k0 + k8);
+              const float rm = s_rms[b];
+              sc[0] = rm * C::lo(graw.x); sc[1] = rm * C::hi(graw.x);
+              sc[2] = rm * C::lo(graw.y); sc[3] = rm * C::hi(graw.y);
+              sc[4] = rm * C::lo(graw.z); sc[5] = rm * C::hi(graw.z);
+              sc[6] = rm * C::lo(graw.w); sc[7] = rm * C::hi(graw.w);
+            }
+            pk.x = C::pack(v0.x * sc[0], v0.y * sc[1]);
+            pk.y = C::pack(v0.z * sc[2], v0.w * sc[3]);
+            pk.z = C::pack(v1.x * sc[4], v1.y * sc[5]);
+            pk.w = C::pack(v1.z * sc[6], v1.w * sc[7]);
+          }
+          *reinterpret_cast<uint4*>(xs + b * GM_LD + k8) = pk;
+        }
+        __syncthreads();
+      }
+      if (wtask < n_wtasks) {
+        const int span = kc / ks;  // multiple of 32 (kc % 256 == 0, ks <= 8)
+        const int kb = kslice * span;
+        const WT* p0 = row0 + k0 + kb + 8 * ti;
+        const WT* p1 = row1 + k0 + kb + 8 * ti;
+        const WT* x0 = xs + gi * GM_LD + kb + 8 * ti;        // batch row gi (n tile 0)
+        const WT* x1 = xs + (gi + 8) * GM_LD + kb + 8 * ti;  // batch row gi + 8 (n tile 1)
+        int k = 0;
+        for (; k + 96 < span; k += 128) {
+          uint4 wa[4], wb[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            wa[u] = ld_stream_u4(p0 + k + 32 * u);
+            wb[u] = ld_stream_u4(p1 + k + 32 * u);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint4 xa = *reinterpret_cast<const uint4*>(x0 + k + 32 * u);
+            const uint4 xb = *reinterpret_cast<const uint4*>(x1 + k + 32 * u);
+            mma16816_f32<WT>(acc[0], wa[u].x, wb[u].x, wa[u].y, wb[u].y, xa.x, xa.y);
+            mma16816_f32<WT>(acc[0], wa[u].z, wb[u].z, wa[u].w, wb[u].w, xa.z, xa.w);
+            mma16816_f32<WT>(acc[1], wa[u].x, wb[u].x, wa[u].y, wb[u].y, xb.x, xb.y);
+            mma16816_f32<WT>(acc[1], wa[u].z, wb[u].z, wa[u].w, wb[u].w, xb.z, xb.w);
+          }
+        }
+        for (; k < span; k += 32) {
+          const uint4 wa = ld_stream_u4(p0 + k), wb = ld_stream_u4(p1 + k);
+          const uint4 xa = *reinterpret_cast<const uint4*>(x0 + k);
+          const uint4 xb = *reinterpret_cast<const uint4*>(x1 + k);
+          mma16816_f32<WT>(acc[0], wa.x, wb.x, wa.y, wb.y, xa.x, xa.y);
+          mma16816_f32<WT>(acc[0], wa.z, wb.z, wa.w, wb.w, xa.z, xa.w);
+          mma16816_f32<WT>(acc[1], wa.x, wb.x, wa.y, wb.y, xb.x, xb.y);
+          mma16816_f32<WT>(acc[1], wa.z, wb.z, wa.w, wb.w, xb.z, xb.w);
+        }
+      }
+    }
+
+    if (ks > 1) {
+      // combine the K slices of each warp task in a fixed order
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s_part[warp][nt * 4 + e][lane] = acc[nt][e];
+      __syncthreads();
+      if (kslice == 0) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float t = 0.f;
+            for (int i = 0; i < ks; ++i) t += s_part[warp + i][nt * 4 + e][lane];
+            acc[nt][e] = t;
+          }
+      }
+      __syncthreads();
+      if (kslice != 0) continue;
+    }
+    if (!lane_active) continue;
+    // lane (gi, ti): pair gi, batch rows nt * 8 + 2 ti + e; first row in acc[nt][e], second in acc[nt][2 + e]
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int b = nt * 8 + 2 * ti + e;
+        if (b < p.B) gemv_store<WT, MODE>(p, task, b, kind, local, acc[nt][e], acc[nt][2 + e]);
+      }
+  }
+}
+
+template <typename WT>
+static cudaError_t set_gemv_mma_attrs() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(gemv_mma_kernel<WT, GEMV_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemv_mma_kernel<WT, GEMV_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemv_mma_kernel<WT, GEMV_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM))) return e;
+  return cudaFuncSetAttribute(gemv_mma_kernel<WT, GEMV_LOGITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM);
+}
+
+template <typename WT>
+static cudaError_t gemv_mma_dispatch(const GemvParams& p, int mode, int grid, cudaStream_t s, bool pdl) {
+  const dim3 g(grid), b(GEMV_THREADS);
+  switch (mode) {
+    case GEMV_QKV: return launch_k(gemv_mma_kernel<WT, GEMV_QKV>, g, b, (size_t)GM_SMEM, s, pdl, p);
+    case GEMV_GATEUP: return launch_k(gemv_mma_kernel<WT, GEMV_GATEUP>, g, b, (size_t)GM_SMEM, s, pdl, p);
+    case GEMV_RESID: return launch_k(gemv_mma_kernel<WT, GEMV_RESID>, g, b, (size_t)GM_SMEM, s, pdl, p);
+    default: return launch_k(gemv_mma_kernel<WT, GEMV_LOGITS>, g, b, (size_t)GM_SMEM, s, pdl, p);
+  }
+}
+
+// Rows b0 .. b0 + 15 (at most) of a batched projection on the tensor cores.
+static cudaError_t launch_gemv_mma(GemvParams p, int mode, int wdt, int num_sms, cudaStream_t s, bool pdl) {
+  const int n_wtasks = (p.n_tasks + 7) / 8;
+  // K split: the smallest that gives about 12 warps per SM, each slice a multiple of 32 in every chunk
+  p.ks = 1;
+  const int kc0 = p.K < GM_KCH ? p.K : GM_KCH;
+  while (p.ks < GEMV_WARPS && (long long)n_wtasks * p.ks < (long long)num_sms * 12 && (kc0 / (2 * p.ks)) % 32 == 0 &&
+         (p.K % GM_KCH) % (2 * p.ks * 32) == 0)
+    p.ks *= 2;
+  const int tpc = GEMV_WARPS / p.ks;
+  int grid = (n_wtasks + tpc - 1) / tpc;
+  const int cap = num_sms * 3;
+  if (grid > cap) grid = cap;
+  return wdt == WDT_F16 ? gemv_mma_dispatch<f16>(p, mode, grid, s, pdl) : gemv_mma_dispatch<bf16>(p, mode, grid, s, pdl);
 }
 
 int gemv_chunk(int B, int K) {
@@ -365,7 +626,9 @@ cudaError_t gemv_configure() {
   if ((e = set_gemv_attrs<bf16, 4>())) return e;
   if ((e = set_gemv_attrs<f16, 1>())) return e;
   if ((e = set_gemv_attrs<f16, 2>())) return e;
-  return set_gemv_attrs<f16, 4>();
+  if ((e = set_gemv_attrs<f16, 4>())) return e;
+  if ((e = set_gemv_mma_attrs<bf16>())) return e;
+  return set_gemv_mma_attrs<f16>();
 }
 
 template <typename WT, int BT>
@@ -388,10 +651,32 @@ static cudaError_t gemv_dispatch_bt(const GemvParams& p, int bt, int mode, int g
   return gemv_dispatch<WT, 4>(p, mode, grid, smem, s, pdl);
 }
 
-int gemv_launch_count(int B, int K) { return (B + 3) / 4; }
+// Batches of 1..4 rows run on the CUDA-core GEMV; larger batches run on the
+// tensor-core kernel in chunks of 16 rows (shard partials stay on the GEMV, in
+// chunks of 4).
+static bool gemv_use_mma(int B, int mode) { return B > 4 && mode != GEMV_PARTIAL; }
+
+int gemv_launch_count(int B, int K, int mode) { return gemv_use_mma(B, mode) ? (B + 15) / 16 : (B + 3) / 4; }
 
 // Batches larger than 4 run as consecutive chunks of at most 4 rows.
 cudaError_t launch_gemv(const GemvParams& p0, int mode, int wdt, int num_sms, cudaStream_t s, bool pdl) {
+  if (gemv_use_mma(p0.B, mode)) {
+    for (int b0 = 0; b0 < p0.B; b0 += 16) {
+      GemvParams p = p0;
+      p.B = p0.B - b0 < 16 ? p0.B - b0 : 16;
+      p.x = p0.x + (size_t)b0 * p0.ldx;
+      p.out = p0.out + (size_t)b0 * p0.ldo;
+      if (p0.x_res) p.x_res = p0.x_res + (size_t)b0 * p0.ldr;
+      if (p0.pos) p.pos = p0.pos + b0;
+      if (p0.kv.block_table) p.kv.block_table = p0.kv.block_table + (size_t)b0 * p0.kv.max_pages;
+      p.kfull = p.K;
+      p.ldw = p.K;
+      p.shard_tasks = p.n_tasks;
+      cudaError_t e = launch_gemv_mma(p, mode, wdt, num_sms, s, pdl);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
   for (int b0 = 0; b0 < p0.B; b0 += 4) {
     GemvParams p = p0;
     p.B = p0.B - b0 < 4 ? p0.B - b0 : 4;

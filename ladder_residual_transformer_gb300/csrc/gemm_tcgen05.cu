@@ -5,15 +5,18 @@
 // Persistent CTAs (one per SM) loop over 128 x BN tiles (BN = 256, or 128 for
 // narrow matrices) with tcgen05.mma (cta_group::1, kind::f16, M = 128, N = BN,
 // K = 16 per instruction).  Warp roles:
-//   warp 4: one elected thread issues the TMA loads of A (128 x 64) and of the
+//   warp 4: one elected thread issues the TMA loads of A (128 rows) and of the
 //           two 128-row halves of B (each half may come from a different
-//           weight matrix: q/k/v rows, or the gate and up rows of SwiGLU);
+//           weight matrix: q/k/v rows, or the gate and up rows of SwiGLU),
+//           K = 64 (BN = 256) or 128 (BN = 128) per stage;
 //   warp 5: allocates 2 x BN TMEM columns (two accumulator buffers) and one
 //           elected thread issues the MMAs, releasing each shared-memory stage
 //           with tcgen05.commit and each finished accumulator to the epilogue;
 //   warps 0-3: epilogue, reading the accumulator with tcgen05.ld (warp w owns
-//           TMEM lanes 32w..32w+31, i.e. tile rows) and applying the fused
-//           RoPE + KV scatter, SwiGLU, or residual add, then handing the
+//           TMEM lanes 32w..32w+31, i.e. tile rows), transposing each 32x32
+//           block through shared memory so that every global load and store
+//           of a warp covers a contiguous row segment, and applying the fused
+//           RoPE + KV scatter, SwiGLU, or residual add; then it hands the
 //           accumulator buffer back, so the epilogue of one tile overlaps the
 //           main loop of the next.
 // Operands sit in shared memory in the 128-byte-swizzled K-major layout that
@@ -28,11 +31,19 @@
 
 namespace ladder {
 
-constexpr int TC_BM = 128, TC_BK = 64;
-constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;   // 16 KB
-constexpr int TC_BH_BYTES = 128 * TC_BK * 2;    // one 128-row half of B, 16 KB
-// Shared memory for the stage ring: 7 stages of 32 KB at BN = 128, 4 of 48 KB at BN = 256.
-constexpr int TC_SMEM = 7 * (TC_A_BYTES + TC_BH_BYTES) + 1024 + 256;
+// A stage holds K = 64 * KC of each operand as KC 64-element (128-byte) chunks,
+// loaded by one 3-D TMA box per operand ([chunk][row][64]): KC = 2 makes every
+// row of a box a 256-byte contiguous run of global memory, which the 128-wide
+// tiles need to keep the tensor cores fed; 256-wide tiles use KC = 1 and a
+// deeper ring.
+constexpr int TC_BM = 128;
+constexpr int TC_CHUNK = 128 * 64 * 2;  // one 128-row x 64-element chunk, 16 KB
+// Stage ring: 3 stages of 64 KB at BN = 128 (KC = 2), 4 of 48 KB at BN = 256 (KC = 1).
+constexpr int TC_RING = 3 * 4 * TC_CHUNK;
+// Epilogue staging: per epilogue warp one 32 x 32 fp32 block, rows padded to 33.
+constexpr int TC_EP_LD = 33;
+constexpr int TC_EP_BYTES = 4 * 32 * TC_EP_LD * 4;
+constexpr int TC_SMEM = TC_RING + TC_EP_BYTES + 1024 + 256;
 constexpr int TC_THREADS = 192;
 constexpr long long TC_WAIT_LIMIT = 4000000000LL;  // cycles (about 2 s)
 
@@ -79,17 +90,21 @@ struct TcMaps {
 // n = t / m_tiles) so that CTAs running together share the weight tile in L2.
 // The accumulator is double-buffered in TMEM (2 x BN columns): the MMA warp
 // fills buffer i & 1 while the epilogue warps drain the other one.
-template <typename WT, int MODE, int BN>
+template <typename WT, int MODE, int BN, int KC>
 __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_constant__ TcMaps maps,
                                                                 const GemmParams p, int m_tiles, int n_tiles,
                                                                 int* err) {
   using C = W16<WT>;
   constexpr int HALVES = BN / 128;
-  constexpr int STAGE = TC_A_BYTES + HALVES * TC_BH_BYTES;
-  constexpr int NST = (TC_SMEM - 1024 - 256) / STAGE;
+  constexpr int BK = 64 * KC;
+  constexpr int A_BYTES = KC * TC_CHUNK;   // 128 rows of A
+  constexpr int BH_BYTES = KC * TC_CHUNK;  // one 128-row half of B
+  constexpr int STAGE = A_BYTES + HALVES * BH_BYTES;
+  constexpr int NST = TC_RING / STAGE;
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * STAGE);
+  float* ep_all = reinterpret_cast<float*>(smem + TC_RING);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TC_RING + TC_EP_BYTES);
   uint64_t* empty = full + NST;
   uint64_t* tfull = empty + NST;   // [2] accumulator ready
   uint64_t* tempty = tfull + 2;    // [2] accumulator drained
@@ -97,7 +112,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
   int* bail = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nkb = p.K / TC_BK;
+  const int nkb = p.K / BK;
   const int total = m_tiles * n_tiles;
   const int my_tiles = blockIdx.x < total ? (total - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
@@ -146,9 +161,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
           if (*reinterpret_cast<volatile int*>(bail)) { ok = false; break; }
           uint8_t* st = smem + s * STAGE;
           mbar_expect_tx(&full[s], STAGE);
-          tma_load_2d(st, &maps.a, kb * TC_BK, m0, &full[s]);
-          tma_load_2d(st + TC_A_BYTES, &maps.b[map0], kb * TC_BK, row0, &full[s]);
-          if (HALVES == 2) tma_load_2d(st + TC_A_BYTES + TC_BH_BYTES, &maps.b[map1], kb * TC_BK, row1, &full[s]);
+          tma_load_3d(st, &maps.a, 0, m0, kb * KC, &full[s]);
+          tma_load_3d(st + A_BYTES, &maps.b[map0], 0, row0, kb * KC, &full[s]);
+          if (HALVES == 2) tma_load_3d(st + A_BYTES + BH_BYTES, &maps.b[map1], 0, row1, kb * KC, &full[s]);
         }
       }
       // Make sure no copy into this CTA's shared memory is still in flight.
@@ -156,7 +171,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
     }
   } else if (warp == 5) {
     if (lane == 0) {
-      constexpr uint32_t idesc = umma_idesc(TC_BM, BN, C::umma_fmt);
+      // KC = 1: the two B halves are contiguous, one N = BN MMA per k step.
+      // KC = 2: each half is its own [chunk][row] box, one N = 128 MMA per half.
+      constexpr int MMA_N = KC == 1 ? BN : 128;
+      constexpr int MMAS = KC == 1 ? 1 : HALVES;
+      constexpr uint32_t idesc = umma_idesc(TC_BM, MMA_N, C::umma_fmt);
       int it = 0;
       bool ok = true;
       for (int i = 0; ok && i < my_tiles; ++i) {
@@ -179,21 +198,43 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
           }
           tc_fence_after();
           const uint32_t a_base = smem_u32(smem + s * STAGE);
-          const uint32_t b_base = a_base + TC_A_BYTES;
+          const uint32_t b_base = a_base + A_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < TC_BK / 16; ++kk)
-            umma_f16(d, umma_desc(a_base + kk * 32), umma_desc(b_base + kk * 32), idesc, (kb | kk) != 0);
+          for (int c = 0; c < KC; ++c)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+              for (int hh = 0; hh < MMAS; ++hh)
+                umma_f16(d + hh * 128, umma_desc(a_base + c * TC_CHUNK + kk * 32),
+                         umma_desc(b_base + hh * BH_BYTES + c * TC_CHUNK + kk * 32), idesc, (kb | c | kk) != 0);
           umma_commit(&empty[s]);
         }
         umma_commit(&tfull[acc]);  // also after a bail, so that the MMAs in flight finish first
       }
     }
   } else {
+    // Epilogue warp w owns tile rows 32w .. 32w + 31 (its TMEM lanes).  Each
+    // 32-column chunk is read from TMEM row-wise (lane = row), staged in shared
+    // memory and read back column-wise, so that global loads and stores of a
+    // warp instruction cover whole row segments instead of 32 different rows.
     const int hd = p.kv.head_dim;
+    float* ep = ep_all + warp * 32 * TC_EP_LD;
+    const int cp = 2 * (lane & 15), rsub = lane >> 4;  // 16-bit outputs: column pair, row parity
     for (int i = 0; i < my_tiles; ++i) {
       const int acc = i & 1;
       const int t = blockIdx.x + i * gridDim.x;
-      const int m = (t % m_tiles) * TC_BM + warp * 32 + lane, tile_n = t / m_tiles;
+      const int mrow0 = (t % m_tiles) * TC_BM + warp * 32, tile_n = t / m_tiles;
+      // Row metadata of this lane's row (QKV), fetched before the accumulator is
+      // awaited: position and the element offset of its slot in the paged cache
+      // (page base + slot * hd; the kv / head term is added per column).
+      int my_pos = 0;
+      long long my_slot = 0;
+      if (MODE == GEMM_QKV && mrow0 + lane < p.M) {
+        my_pos = p.row_pos[mrow0 + lane];
+        const int bb = p.row_b[mrow0 + lane];
+        const int page = p.kv.block_table[bb * p.kv.max_pages + (my_pos >> p.kv.page_shift)];
+        my_slot = (long long)page * (long long)p.kv.page_elems() + (long long)(my_pos & (p.kv.page_size - 1)) * hd;
+      }
       const bool ok = mbar_wait(&tfull[acc], (i >> 1) & 1);
       tc_fence_after();
       if (!ok) {
@@ -202,72 +243,87 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
       }
       if (__shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(bail), 0)) break;
       const uint32_t trow = tmem + acc * BN + ((uint32_t)(warp * 32) << 16);
+      auto stage = [&](const float (&v)[32]) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ep[lane * TC_EP_LD + j] = v[j];
+        __syncwarp();
+      };
       if (MODE == GEMM_GATEUP) {
         for (int c = 0; c < 4; ++c) {
-          float g[32], u[32];
-          tmem_ld32(trow + c * 32, g);
-          tmem_ld32(trow + 128 + c * 32, u);
-          if (m < p.M) {
-            WT* dst = static_cast<WT*>(p.out_h) + (size_t)m * p.ldo + tile_n * 128 + c * 32;
+          float gv[32], uv[32];
+          tmem_ld32(trow + c * 32, gv);
+          tmem_ld32(trow + 128 + c * 32, uv);
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              uint4 pk;
-              pk.x = C::pack(silu_f(g[j]) * u[j], silu_f(g[j + 1]) * u[j + 1]);
-              pk.y = C::pack(silu_f(g[j + 2]) * u[j + 2], silu_f(g[j + 3]) * u[j + 3]);
-              pk.z = C::pack(silu_f(g[j + 4]) * u[j + 4], silu_f(g[j + 5]) * u[j + 5]);
-              pk.w = C::pack(silu_f(g[j + 6]) * u[j + 6], silu_f(g[j + 7]) * u[j + 7]);
-              *reinterpret_cast<uint4*>(dst + j) = pk;
-            }
+          for (int j = 0; j < 32; ++j) gv[j] = silu_f(gv[j]) * uv[j];
+          stage(gv);
+          WT* dst = static_cast<WT*>(p.out_h) + tile_n * 128 + c * 32 + cp;
+#pragma unroll
+          for (int r2 = 0; r2 < 16; ++r2) {
+            const int r = 2 * r2 + rsub, m = mrow0 + r;
+            if (m < p.M)
+              *reinterpret_cast<uint32_t*>(dst + (size_t)m * p.ldo) =
+                  C::pack(ep[r * TC_EP_LD + cp], ep[r * TC_EP_LD + cp + 1]);
           }
+          __syncwarp();
         }
       } else if (MODE == GEMM_RESID) {
         for (int c = 0; c < BN / 32; ++c) {
+          const int n0 = tile_n * BN + c * 32;
+          if (n0 >= p.N) break;
           float v[32];
           tmem_ld32(trow + c * 32, v);
-          const int n0 = tile_n * BN + c * 32;
-          if (m < p.M && n0 < p.N) {
-            const size_t off = (size_t)m * p.ldo + n0;
+          // the 32 residual values of this lane's column, all loads in flight at once
+          float xr[32];
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-              const float4 r = *reinterpret_cast<const float4*>(p.x_res + off + j);
-              *reinterpret_cast<float4*>(p.out_f + off + j) =
-                  make_float4(r.x + v[j], r.y + v[j + 1], r.z + v[j + 2], r.w + v[j + 3]);
-            }
+          for (int r = 0; r < 32; ++r) {
+            const int m = mrow0 + r;
+            xr[r] = m < p.M ? p.x_res[(size_t)m * p.ldo + n0 + lane] : 0.f;
           }
+          stage(v);
+#pragma unroll
+          for (int r = 0; r < 32; ++r) {
+            const int m = mrow0 + r;
+            if (m < p.M) p.out_f[(size_t)m * p.ldo + n0 + lane] = xr[r] + ep[r * TC_EP_LD + lane];
+          }
+          __syncwarp();
         }
       } else {  // GEMM_QKV
-        const int pos = m < p.M ? p.row_pos[m] : 0;
-        const int b = m < p.M ? p.row_b[m] : 0;
         for (int c = 0; c < BN / 32; ++c) {
+          int map, row;
+          if (!b_half<GEMM_QKV, BN>(p, tile_n, c >> 2, map, row)) break;
           float v[32];
           tmem_ld32(trow + c * 32, v);
-          int map, row;
-          if (!b_half<GEMM_QKV, BN>(p, tile_n, c >> 2, map, row) || m >= p.M) continue;
-          const int local = row + (c & 3) * 32;  // first column of the chunk inside its matrix
-          const int head = local / hd, dim0 = local % hd;
-          if (map < 2) {
-            const float* cs = p.rope_cos + (size_t)pos * (hd >> 1) + (dim0 >> 1);
-            const float* sn = p.rope_sin + (size_t)pos * (hd >> 1) + (dim0 >> 1);
+          const int col = row + (c & 3) * 32 + cp;  // column inside its matrix (even: a RoPE pair)
+          const int head = col / hd, dim = col % hd;
+          // rotation of each of this lane's 16 rows, all table loads in flight at once
+          float cs[16], sn[16];
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              const float cj = cs[j >> 1], sj = sn[j >> 1];
-              const float a0 = v[j], a1 = v[j + 1];
-              v[j] = a0 * cj - a1 * sj;
-              v[j + 1] = a0 * sj + a1 * cj;
+          for (int r2 = 0; r2 < 16; ++r2) {
+            const int r = 2 * r2 + rsub;
+            const int pos = __shfl_sync(0xffffffffu, my_pos, r);
+            cs[r2] = 1.f;
+            sn[r2] = 0.f;
+            if (map < 2 && mrow0 + r < p.M) {
+              const size_t tj = (size_t)pos * (hd >> 1) + (dim >> 1);
+              cs[r2] = p.rope_cos[tj];
+              sn[r2] = p.rope_sin[tj];
             }
           }
-          // q, K and V are stored in the weight dtype (the attention operands)
-          WT* dst = map == 0 ? static_cast<WT*>(p.out_h) + (size_t)m * p.ldo + local
-                             : static_cast<WT*>(p.kv.base) + p.kv.slot(b, pos, map - 1, head) + dim0;
+          stage(v);
+          const long long kvoff = (long long)((map - 1) * p.kv.n_kv + head) * p.kv.page_size * hd + dim;
 #pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            uint4 pk;
-            pk.x = C::pack(v[j], v[j + 1]);
-            pk.y = C::pack(v[j + 2], v[j + 3]);
-            pk.z = C::pack(v[j + 4], v[j + 5]);
-            pk.w = C::pack(v[j + 6], v[j + 7]);
-            *reinterpret_cast<uint4*>(dst + j) = pk;
+          for (int r2 = 0; r2 < 16; ++r2) {
+            const int r = 2 * r2 + rsub, m = mrow0 + r;
+            const long long slot = __shfl_sync(0xffffffffu, my_slot, r);
+            const float a0 = ep[r * TC_EP_LD + cp], a1 = ep[r * TC_EP_LD + cp + 1];
+            const float r0 = a0 * cs[r2] - a1 * sn[r2], r1 = a0 * sn[r2] + a1 * cs[r2];
+            if (m >= p.M) continue;
+            // q, K and V are stored in the weight dtype (the attention operands)
+            WT* dst = map == 0 ? static_cast<WT*>(p.out_h) + (size_t)m * p.ldo + col
+                               : static_cast<WT*>(p.kv.base) + slot + kvoff;
+            *reinterpret_cast<uint32_t*>(dst) = C::pack(r0, r1);
           }
+          __syncwarp();
         }
       }
       // hand the accumulator buffer back to the MMA warp
@@ -310,13 +366,33 @@ bool make_tma_map(void* map_out, const void* base, uint64_t rows, uint64_t cols,
   if (!fn || rows % 128 || cols % 64 || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {TC_BK, 128};
+  cuuint32_t box[2] = {64, 128};
   cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType dt = wdt == WDT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUresult r = fn(reinterpret_cast<CUtensorMap*>(map_out), dt, 2, const_cast<void*>(base),
                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// GEMM operand: row-major 16-bit [rows, cols] viewed as [cols / 64][rows][64]
+// (dimension order x = element in chunk, y = row, z = 64-element chunk), with a
+// box of 64 x 128 rows x KC chunks (KC = 1 and 2), 128-byte swizzle.
+bool make_tma_operand(TmaOperand* out, const void* base, uint64_t rows, uint64_t cols, int wdt) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows % 128 || cols % 128 || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
+  const CUtensorMapDataType dt = wdt == WDT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  for (int kc = 1; kc <= 2; ++kc) {
+    cuuint64_t dims[3] = {64, rows, cols / 64};
+    cuuint64_t strides[2] = {cols * 2, 128};
+    cuuint32_t box[3] = {64, 128, (cuuint32_t)kc};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(&out->box[kc - 1], dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+  }
+  return true;
 }
 
 // One layer of the paged KV pool viewed as [pages * 2 * n_kv][page_size][hd]
@@ -338,11 +414,11 @@ bool make_kv_tma_map(void* map_out, const void* base, uint64_t num_pages, int n_
 template <typename WT>
 static cudaError_t gemm_tc_configure_t() {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_GATEUP, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  return cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 256, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 128, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_GATEUP, 256, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 256, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  return cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 128, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
 }
 
 cudaError_t gemm_tc_configure() {
@@ -350,41 +426,42 @@ cudaError_t gemm_tc_configure() {
   return e != cudaSuccess ? e : gemm_tc_configure_t<f16>();
 }
 
+// Tile width BN with its box depth: 256-wide tiles take 1-chunk boxes, 128-wide 2-chunk boxes.
 template <typename WT, int MODE, int BN>
-static cudaError_t gemm_tc_go(const TcMaps& maps, const GemmParams& p, int mt, int nt, int num_sms, int* err,
-                              cudaStream_t s) {
+static cudaError_t gemm_tc_go(const TmaOperand* a, const TmaOperand* const* b, const GemmParams& p, int mt, int nt,
+                              int num_sms, int* err, cudaStream_t s) {
+  constexpr int KC = BN == 256 ? 1 : 2;
+  TcMaps maps;
+  memcpy(&maps.a, &a->box[KC - 1], sizeof(CUtensorMap));
+  for (int i = 0; i < 3; ++i) memcpy(&maps.b[i], &(b[i] ? b[i] : b[0])->box[KC - 1], sizeof(CUtensorMap));
   const int total = mt * nt;
   const int grid = total < num_sms ? total : num_sms;
-  gemm_tc_kernel<WT, MODE, BN><<<grid, TC_THREADS, TC_SMEM, s>>>(maps, p, mt, nt, err);
+  gemm_tc_kernel<WT, MODE, BN, KC><<<grid, TC_THREADS, TC_SMEM, s>>>(maps, p, mt, nt, err);
   return cudaGetLastError();
 }
 
 // 256-wide tiles unless that leaves most SMs idle (narrow N at small M).
 template <typename WT>
-static cudaError_t gemm_tc_dispatch(const TcMaps& maps, const GemmParams& p, int mode, int mt, int num_sms, int* err,
-                                    cudaStream_t s) {
-  if (mode == GEMM_GATEUP) return gemm_tc_go<WT, GEMM_GATEUP, 256>(maps, p, mt, p.N / 128, num_sms, err, s);
+static cudaError_t gemm_tc_dispatch(const TmaOperand* a, const TmaOperand* const* b, const GemmParams& p, int mode,
+                                    int mt, int num_sms, int* err, cudaStream_t s) {
+  if (mode == GEMM_GATEUP) return gemm_tc_go<WT, GEMM_GATEUP, 256>(a, b, p, mt, p.N / 128, num_sms, err, s);
   const int nt256 = (p.N + 255) / 256;
   const bool narrow = (long long)mt * nt256 * 4 < (long long)num_sms * 3;
   if (mode == GEMM_RESID) {
-    if (narrow) return gemm_tc_go<WT, GEMM_RESID, 128>(maps, p, mt, (p.N + 127) / 128, num_sms, err, s);
-    return gemm_tc_go<WT, GEMM_RESID, 256>(maps, p, mt, nt256, num_sms, err, s);
+    if (narrow) return gemm_tc_go<WT, GEMM_RESID, 128>(a, b, p, mt, (p.N + 127) / 128, num_sms, err, s);
+    return gemm_tc_go<WT, GEMM_RESID, 256>(a, b, p, mt, nt256, num_sms, err, s);
   }
-  if (narrow) return gemm_tc_go<WT, GEMM_QKV, 128>(maps, p, mt, (p.N + 127) / 128, num_sms, err, s);
-  return gemm_tc_go<WT, GEMM_QKV, 256>(maps, p, mt, nt256, num_sms, err, s);
+  if (narrow) return gemm_tc_go<WT, GEMM_QKV, 128>(a, b, p, mt, (p.N + 127) / 128, num_sms, err, s);
+  return gemm_tc_go<WT, GEMM_QKV, 256>(a, b, p, mt, nt256, num_sms, err, s);
 }
 
-cudaError_t launch_gemm_tc(const void* a_map, const void* b0, const void* b1, const void* b2, const GemmParams& p,
-                           int mode, int wdt, int num_sms, int* err, cudaStream_t s) {
+cudaError_t launch_gemm_tc(const TmaOperand* a, const TmaOperand* b0, const TmaOperand* b1, const TmaOperand* b2,
+                           const GemmParams& p, int mode, int wdt, int num_sms, int* err, cudaStream_t s) {
   if (p.M <= 0) return cudaSuccess;
-  TcMaps maps;
-  memcpy(&maps.a, a_map, sizeof(CUtensorMap));
-  memcpy(&maps.b[0], b0, sizeof(CUtensorMap));
-  memcpy(&maps.b[1], b1 ? b1 : b0, sizeof(CUtensorMap));
-  memcpy(&maps.b[2], b2 ? b2 : b0, sizeof(CUtensorMap));
+  const TmaOperand* b[3] = {b0, b1, b2};
   const int mt = (p.M + TC_BM - 1) / TC_BM;
-  return wdt == WDT_F16 ? gemm_tc_dispatch<f16>(maps, p, mode, mt, num_sms, err, s)
-                        : gemm_tc_dispatch<bf16>(maps, p, mode, mt, num_sms, err, s);
+  return wdt == WDT_F16 ? gemm_tc_dispatch<f16>(a, b, p, mode, mt, num_sms, err, s)
+                        : gemm_tc_dispatch<bf16>(a, b, p, mode, mt, num_sms, err, s);
 }
 
 }  // namespace ladder

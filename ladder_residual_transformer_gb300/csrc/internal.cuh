@@ -2,6 +2,7 @@
 // Nothing here is part of the public ABI (include/ladder.h).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -193,7 +194,7 @@ cudaError_t launch_embed(const int* tok, int M, const void* E, int wdt, int d, i
 cudaError_t launch_gemv(const GemvParams& p, int mode, int wdt, int num_sms, cudaStream_t s, bool pdl = false);
 cudaError_t gemv_configure();
 int gemv_chunk(int B, int K);
-int gemv_launch_count(int B, int K);
+int gemv_launch_count(int B, int K, int mode);
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, int B, int n_kv, int hd, int kv_dtype, cudaStream_t s,
                                bool pdl = false);
 cudaError_t launch_argmax(const float* logits, int B, int V, float* part_v, int* part_i, int nblk,
@@ -205,12 +206,19 @@ cudaError_t launch_rope_tables(float* cos_t, float* sin_t, int max_seq, int hd, 
 cudaError_t launch_rmsnorm_rows(const float* x, int M, int d, const void* g, float eps, void* out, int wdt,
                                 cudaStream_t s);
 // Tensor-core GEMM (tcgen05 + TMA).  Maps are CUtensorMap objects made by make_tma_map.
+// 2-D map of a row-major [rows, cols] 16-bit matrix, box 64 columns x 128 rows.
 bool make_tma_map(void* map_out, const void* base, uint64_t rows, uint64_t cols, int wdt);
+// GEMM operand: the same matrix as 3-D [cols / 64][rows][64], with boxes of
+// 128 rows x 1 and x 2 chunks (box[0], box[1]).
+struct TmaOperand {
+  CUtensorMap box[2];
+};
+bool make_tma_operand(TmaOperand* out, const void* base, uint64_t rows, uint64_t cols, int wdt);
 // One layer of the paged KV pool as a 3-D map (see gemm_tcgen05.cu).
 bool make_kv_tma_map(void* map_out, const void* base, uint64_t num_pages, int n_kv, int page_size, int hd, int wdt);
 cudaError_t gemm_tc_configure();
-cudaError_t launch_gemm_tc(const void* a_map, const void* b0, const void* b1, const void* b2, const GemmParams& p,
-                           int mode, int wdt, int num_sms, int* err, cudaStream_t s);
+cudaError_t launch_gemm_tc(const TmaOperand* a, const TmaOperand* b0, const TmaOperand* b1, const TmaOperand* b2,
+                           const GemmParams& p, int mode, int wdt, int num_sms, int* err, cudaStream_t s);
 // Tensor-core causal attention for packed prefill rows (mma.sync, bf16 Q/K/V).
 // Prefill attention on tcgen05: q_map = make_tma_map of the query rows, kv_map =
 // make_kv_tma_map of the layer; head_dim 64 or 128.

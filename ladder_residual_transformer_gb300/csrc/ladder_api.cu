@@ -143,7 +143,7 @@ struct LayerW {
 
 // Tensor maps of one layer's weights for the prefill GEMMs.
 struct LayerMaps {
-  CUtensorMap wq, wk, wv, wo, gate, up, down;
+  TmaOperand wq, wk, wv, wo, gate, up, down;
 };
 
 struct GraphEntry {
@@ -164,7 +164,7 @@ struct ladder_model {
   int wdt;  // weight dtype
   std::vector<LayerW> layers;
   std::vector<LayerMaps> maps;
-  CUtensorMap map_xn, map_ao, map_act;  // activation operands, m_pad rows
+  TmaOperand map_xn, map_ao, map_act;  // activation operands, m_pad rows
   CUtensorMap map_q;  // rotated queries [m_pad][n_q * hd], the prefill attention operand
   char* ws;
   Plan plan;
@@ -319,18 +319,18 @@ int ladder_create(const ladder_config* cfg, const ladder_weights* w, void* works
     const uint64_t d = c.d_model, qd = (uint64_t)c.n_q_heads * c.head_dim, kvd = (uint64_t)c.n_kv_heads * c.head_dim;
     const uint64_t f = c.ffn_dim, Mp = plan.m_pad;
     const int wdt = c.weight_dtype;
-    bool ok = make_tma_map(&m->map_xn, m->ws + plan.xn, Mp, d, wdt) &&
-              make_tma_map(&m->map_ao, m->ws + plan.ao, Mp, qd, wdt) &&
-              make_tma_map(&m->map_act, m->ws + plan.act, Mp, f, wdt) &&
+    bool ok = make_tma_operand(&m->map_xn, m->ws + plan.xn, Mp, d, wdt) &&
+              make_tma_operand(&m->map_ao, m->ws + plan.ao, Mp, qd, wdt) &&
+              make_tma_operand(&m->map_act, m->ws + plan.act, Mp, f, wdt) &&
               make_tma_map(&m->map_q, m->ws + plan.q, Mp, qd, wdt);
     m->maps.resize(c.n_layers);
     for (int l = 0; ok && l < c.n_layers; ++l) {
       const LayerW& L = m->layers[l];
       LayerMaps& T = m->maps[l];
-      ok = make_tma_map(&T.wq, L.wq, qd, d, wdt) && make_tma_map(&T.wk, L.wk, kvd, d, wdt) &&
-           make_tma_map(&T.wv, L.wv, kvd, d, wdt) && make_tma_map(&T.wo, L.wo, d, qd, wdt) &&
-           make_tma_map(&T.gate, L.w_gate, f, d, wdt) && make_tma_map(&T.up, L.w_up, f, d, wdt) &&
-           make_tma_map(&T.down, L.w_down, d, f, wdt);
+      ok = make_tma_operand(&T.wq, L.wq, qd, d, wdt) && make_tma_operand(&T.wk, L.wk, kvd, d, wdt) &&
+           make_tma_operand(&T.wv, L.wv, kvd, d, wdt) && make_tma_operand(&T.wo, L.wo, d, qd, wdt) &&
+           make_tma_operand(&T.gate, L.w_gate, f, d, wdt) && make_tma_operand(&T.up, L.w_up, f, d, wdt) &&
+           make_tma_operand(&T.down, L.w_down, d, f, wdt);
     }
     if (!ok) {
       delete m;
@@ -593,7 +593,7 @@ int enqueue_decode_shard(ladder_model* m, ladder_kv* kv, const int32_t* tokens, 
       g.out = q; g.ldo = qd; g.nq_hd = qd; g.nkv_hd = kvd;
       g.rope_cos = m->at<float>(P.rope_cos); g.rope_sin = m->at<float>(P.rope_sin);
       g.pos = kv->seq_lens; g.kv = kvl; g.err = m->err();
-      LAUNCH(launch_gemv(g, GEMV_QKV, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, g.K));
+      LAUNCH(launch_gemv(g, GEMV_QKV, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, g.K, GEMV_QKV));
       AttnDecodeParams a{};
       a.q = q; a.kv = kvl; a.seq_lens = kv->seq_lens; a.n_q = c.n_q_heads; a.split_len = kSplitLen;
       a.nsplit = nsplit; a.scale = 1.0f / sqrtf((float)c.head_dim);
@@ -605,14 +605,14 @@ int enqueue_decode_shard(ladder_model* m, ladder_kv* kv, const int32_t* tokens, 
       g.x = m->X(j); g.ldx = d; g.g = L.mlp_norm; g.eps = c.norm_eps; g.B = B; g.K = d;
       g.w0 = L.w_gate; g.w1 = L.w_up; g.n_tasks = f; g.out = act; g.ldo = f; g.err = m->err();
       cudaEvent_t pe = m->probe_start(LADDER_PROBE_GATEUP, s);
-      LAUNCH(launch_gemv(g, GEMV_GATEUP, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, g.K));
+      LAUNCH(launch_gemv(g, GEMV_GATEUP, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, g.K, GEMV_GATEUP));
       m->probe_stop(pe, s);
       o.x = act; o.ldx = f; o.K = f / ksh; o.kfull = f; o.ldw = f; o.w0 = L.w_down;
     }
     // row-parallel partial sums: shard sh uses input block sh and writes part[b][sh][:]
     o.g = nullptr; o.B = B; o.shard_tasks = d / 2; o.n_tasks = ksh * (d / 2);
     o.out = pk; o.ldo = ksh * d; o.err = m->err();
-    LAUNCH(launch_gemv(o, GEMV_PARTIAL, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, o.kfull));
+    LAUNCH(launch_gemv(o, GEMV_PARTIAL, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, o.kfull, GEMV_PARTIAL));
     CUDA_TRY(cudaEventRecord(m->ev_part, s));
     // the "all-reduce": x_k = x_{k-1} + sum of the partials, on the second stream
     CUDA_TRY(cudaStreamWaitEvent(rs, m->ev_part, 0));
@@ -625,7 +625,7 @@ int enqueue_decode_shard(ladder_model* m, ladder_kv* kv, const int32_t* tokens, 
   GemvParams h{};
   h.x = m->X(2 * c.n_layers); h.ldx = d; h.g = m->final_norm; h.eps = c.norm_eps; h.B = B; h.K = d;
   h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.out = logits; h.ldo = c.vocab; h.err = m->err();
-  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, h.K));
+  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, h.K, GEMV_LOGITS));
   if (next_tok)
     LAUNCH(launch_argmax(logits, B, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i), kArgmaxBlocks, next_tok, s, pdl), 2);
   LAUNCH(launch_advance(kv->seq_lens, B, s, pdl), 1);
@@ -683,7 +683,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       g.pos = kv->seq_lens; g.kv = kvl;
       cudaEvent_t pe = m->probe_start(LADDER_PROBE_QKV, s);
       g.err = m->err();
-      LAUNCH(launch_gemv(g, GEMV_QKV, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, g.K));
+      LAUNCH(launch_gemv(g, GEMV_QKV, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, g.K, GEMV_QKV));
       m->probe_stop(pe, s);
 
       AttnDecodeParams a{};
@@ -700,7 +700,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       o.out = m->X(k); o.ldo = d; o.x_res = m->X(k - 1); o.ldr = d;
       pe = m->probe_start(LADDER_PROBE_OUT, s);
       o.err = m->err();
-      LAUNCH(launch_gemv(o, GEMV_RESID, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, o.K));
+      LAUNCH(launch_gemv(o, GEMV_RESID, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, o.K, GEMV_RESID));
       m->probe_stop(pe, s);
       if ((rc = wrote(k, 0))) return rc;
     }
@@ -715,7 +715,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       g.w0 = L.w_gate; g.w1 = L.w_up; g.n_tasks = f; g.out = act; g.ldo = f;
       cudaEvent_t pe = m->probe_start(LADDER_PROBE_GATEUP, ms);
       g.err = m->err();
-      LAUNCH(launch_gemv(g, GEMV_GATEUP, m->wdt, m->num_sms, ms, pdl), gemv_launch_count(B, g.K));
+      LAUNCH(launch_gemv(g, GEMV_GATEUP, m->wdt, m->num_sms, ms, pdl), gemv_launch_count(B, g.K, GEMV_GATEUP));
       m->probe_stop(pe, ms);
 
       if ((rc = use(k - 1, mlp_stream))) return rc;
@@ -724,7 +724,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       o.out = m->X(k); o.ldo = d; o.x_res = m->X(k - 1); o.ldr = d;
       pe = m->probe_start(LADDER_PROBE_DOWN, ms);
       o.err = m->err();
-      LAUNCH(launch_gemv(o, GEMV_RESID, m->wdt, m->num_sms, ms, pdl), gemv_launch_count(B, o.K));
+      LAUNCH(launch_gemv(o, GEMV_RESID, m->wdt, m->num_sms, ms, pdl), gemv_launch_count(B, o.K, GEMV_RESID));
       m->probe_stop(pe, ms);
       if ((rc = wrote(k, mlp_stream))) return rc;
     }
@@ -735,7 +735,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
   h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.out = logits; h.ldo = c.vocab;
   cudaEvent_t pe = m->probe_start(LADDER_PROBE_LMHEAD, s);
   h.err = m->err();
-  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, h.K));
+  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, h.K, GEMV_LOGITS));
   m->probe_stop(pe, s);
   if (next_tok)
     LAUNCH(launch_argmax(logits, B, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i), kArgmaxBlocks, next_tok, s, pdl), 2);
@@ -888,7 +888,7 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
   h.x = xlast; h.ldx = d; h.g = m->final_norm; h.eps = c.norm_eps; h.B = B; h.K = d;
   h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.out = logits; h.ldo = c.vocab;
   h.err = m->err();
-  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s), gemv_launch_count(B, h.K));
+  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s), gemv_launch_count(B, h.K, GEMV_LOGITS));
   if (next_tok)
     LAUNCH(launch_argmax(logits, B, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i), kArgmaxBlocks, next_tok, s), 2);
   LAUNCH(launch_set_lens(d_lens, B, kv->seq_lens, s), 1);
