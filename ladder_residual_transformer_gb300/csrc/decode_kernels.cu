@@ -375,14 +375,17 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
 // input row: element 8t + 4c + {0,1,2,3} plays logical column {2t, 2t+1, 2t+8,
 // 2t+9} of MMA k-block c.  A permutation of K applied to both operands leaves
 // every dot product unchanged.
-// The normalised inputs are staged in shared memory as 16-bit values (the
-// operand type of the MMA) in chunks of GM_KCH columns, rows padded by 16 bytes
-// so that the 16-byte reads of a warp are conflict-free.  Short matrices split K
-// across up to 8 warps, combined in a fixed order.
+//
+// Split K across CTAs: CTA (group, slice) stages only its K slice of the 16
+// input rows (x * g as 16-bit values, rows padded by 16 bytes for
+// conflict-free reads) and the slice's sum of squares of each row, and each of
+// its 8 warps writes the 16 x 16 partial sums of one warp task.  The last CTA
+// of a group to finish (an atomic counter, reset after use) adds the slices in
+// a fixed order, applies the RMSNorm scale rsqrt(sum x^2 / K + eps) of each row
+// (a per-row factor, so it commutes with the dot products) and runs the
+// epilogue.  Each CTA thus reads a small slice of the inputs, not all of them.
 // ---------------------------------------------------------------------------
-constexpr int GM_KCH = 2048;             // staged input columns per chunk
-constexpr int GM_LD = GM_KCH + 8;        // padded row length (elements)
-constexpr int GM_SMEM = 16 * GM_LD * 2;  // 16 rows of 16-bit values
+constexpr int GM_KL_MAX = 2048;  // longest K slice (staged 16-bit columns)
 
 template <typename T>
 __device__ __forceinline__ void mma16816_f32(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -402,203 +405,207 @@ __device__ __forceinline__ void mma16816_f32(float (&c)[4], uint32_t a0, uint32_
   }
 }
 
+GemvSplitK gemv_splitk_shape(int n_tasks, int K) {
+  GemvSplitK sk;
+  sk.n_wtasks = (n_tasks + 7) / 8;
+  sk.n_groups = (sk.n_wtasks + GEMV_WARPS - 1) / GEMV_WARPS;
+  const int units = K / 256;  // K is a multiple of 256
+  int best = 0;
+  for (int ks = 1; ks <= units; ++ks) {
+    if (units % ks || K / ks > GM_KL_MAX) continue;
+    best = ks;  // the finest admissible split so far
+    if ((long long)sk.n_groups * ks >= 320) break;
+  }
+  sk.ksplit = best;
+  sk.kl = K / best;
+  return sk;
+}
+
+size_t gemv_splitk_bytes(int n_tasks, int K) {
+  const GemvSplitK sk = gemv_splitk_shape(n_tasks, K);
+  auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+  return up((size_t)sk.ksplit * sk.n_wtasks * 256 * 4) + up((size_t)sk.n_groups * sk.ksplit * 16 * 4) +
+         up((size_t)sk.n_groups * 4);
+}
+
 template <typename WT, int MODE>
-__global__ void __launch_bounds__(GEMV_THREADS) gemv_mma_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(GEMV_THREADS) gemv_splitk_kernel(const GemvParams p, int ksplit, int kl) {
   using C = W16<WT>;
   const WT* g = static_cast<const WT*>(p.g);
   extern __shared__ float4 gm_smem4[];
-  WT* xs = reinterpret_cast<WT*>(gm_smem4);  // [16][GM_LD] staged inputs
-  __shared__ float s_red[GEMV_WARPS][16];
+  WT* xs = reinterpret_cast<WT*>(gm_smem4);  // [16][kl + 8] staged inputs of this slice
+  __shared__ float s_ss[GEMV_WARPS][16];
   __shared__ float s_rms[16];
-  __shared__ float s_part[GEMV_WARPS][8][32];
+  __shared__ int s_last;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gi = lane >> 2, ti = lane & 3;
-  const int K = p.K;
+  const int gN = blockIdx.x, kS = blockIdx.y;
+  const int n_wtasks = (p.n_tasks + 7) / 8;
+  const int ld = kl + 8;
+  const int k0 = kS * kl;
+  const int wtask = gN * GEMV_WARPS + warp;
+  const int task = wtask * 8 + gi;  // the row pair of this lane
+  const bool lane_active = wtask < n_wtasks && task < p.n_tasks;
+  const WT* row0;
+  const WT* row1;
+  int kind, local, koff;
+  gemv_task_rows<WT, MODE>(p, lane_active ? task : 0, row0, row1, kind, local, koff);
   pdl_trigger();
+  // Weights depend on no earlier kernel: ask L2 for this warp's slab before waiting.
+  if (wtask < n_wtasks)
+    for (int k = lane * 64; k < kl; k += 32 * 64) {
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(row0 + k0 + k));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(row1 + k0 + k));
+    }
   pdl_wait();
 
-  // RMSNorm statistics of each input row, in a fixed order (identical in every CTA).
-  if (p.g != nullptr) {
-    float ss[16];
+  // 1. Stage x * g for rows 0..15 of this slice (zero rows past B) and the
+  //    slice's sum of squares of each row.  Item i = (row i / (kl/8), 8 columns);
+  //    kl / 8 is a multiple of 32, so a warp's items share one row.
+  s_ss[warp][lane & 15] = 0.f;
+  __syncwarp();
+  const int per_row = kl / 8;
+  for (int i = tid; i < 16 * per_row; i += GEMV_THREADS) {
+    const int b = i / per_row, k8 = (i % per_row) * 8;
+    uint4 pk = make_uint4(0, 0, 0, 0);
+    float sq = 0.f;
+    if (b < p.B) {
+      const float* src = p.x + (size_t)b * p.ldx + k0 + k8;
+      const float4 v0 = *reinterpret_cast<const float4*>(src);
+      const float4 v1 = *reinterpret_cast<const float4*>(src + 4);
+      sq = v0.x * v0.x + v0.y * v0.y + v0.z * v0.z + v0.w * v0.w + v1.x * v1.x + v1.y * v1.y + v1.z * v1.z +
+           v1.w * v1.w;
+      float sc[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+      if (g != nullptr) {
+        const uint4 graw = *reinterpret_cast<const uint4*>(g + k0 + k8);
+        sc[0] = C::lo(graw.x); sc[1] = C::hi(graw.x); sc[2] = C::lo(graw.y); sc[3] = C::hi(graw.y);
+        sc[4] = C::lo(graw.z); sc[5] = C::hi(graw.z); sc[6] = C::lo(graw.w); sc[7] = C::hi(graw.w);
+      }
+      pk.x = C::pack(v0.x * sc[0], v0.y * sc[1]);
+      pk.y = C::pack(v0.z * sc[2], v0.w * sc[3]);
+      pk.z = C::pack(v1.x * sc[4], v1.y * sc[5]);
+      pk.w = C::pack(v1.z * sc[6], v1.w * sc[7]);
+    }
+    *reinterpret_cast<uint4*>(xs + b * ld + k8) = pk;
+    sq = warp_sum(sq);
+    if (lane == 0) s_ss[warp][b] += sq;
+  }
+  __syncthreads();
+
+  // 2. Partial sums of this warp task over the slice.
+  float acc[2][4];
 #pragma unroll
-    for (int b = 0; b < 16; ++b) ss[b] = 0.f;
-    for (int i = tid * 4; i < K; i += GEMV_THREADS * 4) {
+  for (int nt = 0; nt < 2; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+  if (wtask < n_wtasks) {
+    const WT* p0 = row0 + k0 + 8 * ti;
+    const WT* p1 = row1 + k0 + 8 * ti;
+    const WT* x0 = xs + gi * ld + 8 * ti;        // batch row gi (n tile 0)
+    const WT* x1 = xs + (gi + 8) * ld + 8 * ti;  // batch row gi + 8 (n tile 1)
+    int k = 0;
+    for (; k + 96 < kl; k += 128) {
+      uint4 wa[4], wb[4];
 #pragma unroll
-      for (int b = 0; b < 16; ++b) {
-        if (b < p.B) {
-          const float4 v = *reinterpret_cast<const float4*>(p.x + (size_t)b * p.ldx + i);
-          ss[b] += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-        }
+      for (int u = 0; u < 4; ++u) {
+        wa[u] = ld_stream_u4(p0 + k + 32 * u);
+        wb[u] = ld_stream_u4(p1 + k + 32 * u);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint4 xa = *reinterpret_cast<const uint4*>(x0 + k + 32 * u);
+        const uint4 xb = *reinterpret_cast<const uint4*>(x1 + k + 32 * u);
+        mma16816_f32<WT>(acc[0], wa[u].x, wb[u].x, wa[u].y, wb[u].y, xa.x, xa.y);
+        mma16816_f32<WT>(acc[0], wa[u].z, wb[u].z, wa[u].w, wb[u].w, xa.z, xa.w);
+        mma16816_f32<WT>(acc[1], wa[u].x, wb[u].x, wa[u].y, wb[u].y, xb.x, xb.y);
+        mma16816_f32<WT>(acc[1], wa[u].z, wb[u].z, wa[u].w, wb[u].w, xb.z, xb.w);
       }
     }
-#pragma unroll
-    for (int b = 0; b < 16; ++b) {
-      const float t = warp_sum(ss[b]);
-      if (lane == 0) s_red[warp][b] = t;
+    for (; k < kl; k += 32) {
+      const uint4 wa = ld_stream_u4(p0 + k), wb = ld_stream_u4(p1 + k);
+      const uint4 xa = *reinterpret_cast<const uint4*>(x0 + k);
+      const uint4 xb = *reinterpret_cast<const uint4*>(x1 + k);
+      mma16816_f32<WT>(acc[0], wa.x, wb.x, wa.y, wb.y, xa.x, xa.y);
+      mma16816_f32<WT>(acc[0], wa.z, wb.z, wa.w, wb.w, xa.z, xa.w);
+      mma16816_f32<WT>(acc[1], wa.x, wb.x, wa.y, wb.y, xb.x, xb.y);
+      mma16816_f32<WT>(acc[1], wa.z, wb.z, wa.w, wb.w, xb.z, xb.w);
     }
-    __syncthreads();
-    if (tid < 16) {
+    float4* dst = reinterpret_cast<float4*>(p.sk_part + ((size_t)kS * n_wtasks + wtask) * 256 + lane * 8);
+    dst[0] = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+    dst[1] = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
+  }
+  if (tid < 16) {
+    float t = 0.f;
+    for (int w = 0; w < GEMV_WARPS; ++w) t += s_ss[w][tid];
+    p.sk_ss[((size_t)gN * ksplit + kS) * 16 + tid] = t;
+  }
+
+  // 3. The last CTA of the group combines the slices.
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(p.sk_count + gN, 1) == ksplit - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (tid < 16) {
+    float rm = 1.f;
+    if (g != nullptr) {
       float t = 0.f;
-      for (int w = 0; w < GEMV_WARPS; ++w) t += s_red[w][tid];
-      s_rms[tid] = rsqrtf(t / (float)K + p.eps);
+      for (int s2 = 0; s2 < ksplit; ++s2) t += __ldcg(p.sk_ss + ((size_t)gN * ksplit + s2) * 16 + tid);
+      rm = rsqrtf(t / (float)p.K + p.eps);
     }
-    __syncthreads();
+    s_rms[tid] = rm;
   }
-
-  const int ks = p.ks;
-  const int tpc = GEMV_WARPS / ks;  // warp tasks per CTA per round
-  const int slot = warp / ks, kslice = warp % ks;
-  const int n_wtasks = (p.n_tasks + 7) / 8;
-  const int total_slots = gridDim.x * tpc;
-  const int rounds = (n_wtasks + total_slots - 1) / total_slots;
-  const bool single_chunk = K <= GM_KCH;
-
-  for (int r = 0; r < rounds; ++r) {
-    const int wtask = r * total_slots + blockIdx.x * tpc + slot;
-    const int task = wtask * 8 + gi;  // the row pair of this lane
-    const bool lane_active = wtask < n_wtasks && task < p.n_tasks;
-    const WT* row0;
-    const WT* row1;
-    int kind, local, koff;
-    gemv_task_rows<WT, MODE>(p, lane_active ? task : 0, row0, row1, kind, local, koff);
-
-    float acc[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-
-    for (int k0 = 0; k0 < K; k0 += GM_KCH) {
-      const int kc = min(GM_KCH, K - k0);
-      if (!single_chunk || r == 0) {
-        __syncthreads();
-        // Stage rows 0..15 of the normalised input chunk as 16-bit values (zero rows past B).
-        for (int i = tid; i < 16 * (kc / 8); i += GEMV_THREADS) {
-          const int b = i / (kc / 8), k8 = (i % (kc / 8)) * 8;
-          uint4 pk = make_uint4(0, 0, 0, 0);
-          if (b < p.B) {
-            const float* src = p.x + (size_t)b * p.ldx + k0 + k8;
-            const float4 v0 = *reinterpret_cast<const float4*>(src);
-            const float4 v1 = *reinterpret_cast<const float4*>(src + 4);
-            float sc[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
-            if (g != nullptr) {
-              const uint4 graw = *reinterpret_cast<const uint4*>(g + k0 + k8);
-              const float rm = s_rms[b];
-              sc[0] = rm * C::lo(graw.x); sc[1] = rm * C::hi(graw.x);
-              sc[2] = rm * C::lo(graw.y); sc[3] = rm * C::hi(graw.y);
-              sc[4] = rm * C::lo(graw.z); sc[5] = rm * C::hi(graw.z);
-              sc[6] = rm * C::lo(graw.w); sc[7] = rm * C::hi(graw.w);
-            }
-            pk.x = C::pack(v0.x * sc[0], v0.y * sc[1]);
-            pk.y = C::pack(v0.z * sc[2], v0.w * sc[3]);
-            pk.z = C::pack(v1.x * sc[4], v1.y * sc[5]);
-            pk.w = C::pack(v1.z * sc[6], v1.w * sc[7]);
-          }
-          *reinterpret_cast<uint4*>(xs + b * GM_LD + k8) = pk;
-        }
-        __syncthreads();
-      }
-      if (wtask < n_wtasks) {
-        const int span = kc / ks;  // multiple of 32 (kc % 256 == 0, ks <= 8)
-        const int kb = kslice * span;
-        const WT* p0 = row0 + k0 + kb + 8 * ti;
-        const WT* p1 = row1 + k0 + kb + 8 * ti;
-        const WT* x0 = xs + gi * GM_LD + kb + 8 * ti;        // batch row gi (n tile 0)
-        const WT* x1 = xs + (gi + 8) * GM_LD + kb + 8 * ti;  // batch row gi + 8 (n tile 1)
-        int k = 0;
-        for (; k + 96 < span; k += 128) {
-          uint4 wa[4], wb[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            wa[u] = ld_stream_u4(p0 + k + 32 * u);
-            wb[u] = ld_stream_u4(p1 + k + 32 * u);
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint4 xa = *reinterpret_cast<const uint4*>(x0 + k + 32 * u);
-            const uint4 xb = *reinterpret_cast<const uint4*>(x1 + k + 32 * u);
-            mma16816_f32<WT>(acc[0], wa[u].x, wb[u].x, wa[u].y, wb[u].y, xa.x, xa.y);
-            mma16816_f32<WT>(acc[0], wa[u].z, wb[u].z, wa[u].w, wb[u].w, xa.z, xa.w);
-            mma16816_f32<WT>(acc[1], wa[u].x, wb[u].x, wa[u].y, wb[u].y, xb.x, xb.y);
-            mma16816_f32<WT>(acc[1], wa[u].z, wb[u].z, wa[u].w, wb[u].w, xb.z, xb.w);
-          }
-        }
-        for (; k < span; k += 32) {
-          const uint4 wa = ld_stream_u4(p0 + k), wb = ld_stream_u4(p1 + k);
-          const uint4 xa = *reinterpret_cast<const uint4*>(x0 + k);
-          const uint4 xb = *reinterpret_cast<const uint4*>(x1 + k);
-          mma16816_f32<WT>(acc[0], wa.x, wb.x, wa.y, wb.y, xa.x, xa.y);
-          mma16816_f32<WT>(acc[0], wa.z, wb.z, wa.w, wb.w, xa.z, xa.w);
-          mma16816_f32<WT>(acc[1], wa.x, wb.x, wa.y, wb.y, xb.x, xb.y);
-          mma16816_f32<WT>(acc[1], wa.z, wb.z, wa.w, wb.w, xb.z, xb.w);
-        }
-      }
-    }
-
-    if (ks > 1) {
-      // combine the K slices of each warp task in a fixed order
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) s_part[warp][nt * 4 + e][lane] = acc[nt][e];
-      __syncthreads();
-      if (kslice == 0) {
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float t = 0.f;
-            for (int i = 0; i < ks; ++i) t += s_part[warp + i][nt * 4 + e][lane];
-            acc[nt][e] = t;
-          }
-      }
-      __syncthreads();
-      if (kslice != 0) continue;
-    }
-    if (!lane_active) continue;
-    // lane (gi, ti): pair gi, batch rows nt * 8 + 2 ti + e; first row in acc[nt][e], second in acc[nt][2 + e]
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int b = nt * 8 + 2 * ti + e;
-        if (b < p.B) gemv_store<WT, MODE>(p, task, b, kind, local, acc[nt][e], acc[nt][2 + e]);
-      }
+  if (tid == 0) p.sk_count[gN] = 0;  // ready for the next launch
+  __syncthreads();
+  if (!lane_active) return;
+  float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int s2 = 0; s2 < ksplit; ++s2) {
+    const float4* src = reinterpret_cast<const float4*>(p.sk_part + ((size_t)s2 * n_wtasks + wtask) * 256 + lane * 8);
+    const float4 a = __ldcg(src), c = __ldcg(src + 1);
+    sum[0] += a.x; sum[1] += a.y; sum[2] += a.z; sum[3] += a.w;
+    sum[4] += c.x; sum[5] += c.y; sum[6] += c.z; sum[7] += c.w;
   }
+  // lane (gi, ti): pair gi, batch rows nt * 8 + 2 ti + e; first row in sum[4 nt + e], second in sum[4 nt + 2 + e]
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int b = nt * 8 + 2 * ti + e;
+      if (b < p.B)
+        gemv_store<WT, MODE>(p, task, b, kind, local, sum[4 * nt + e] * s_rms[b], sum[4 * nt + 2 + e] * s_rms[b]);
+    }
 }
 
 template <typename WT>
 static cudaError_t set_gemv_mma_attrs() {
+  const int bytes = 16 * (GM_KL_MAX + 8) * 2;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(gemv_mma_kernel<WT, GEMV_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM))) return e;
-  if ((e = cudaFuncSetAttribute(gemv_mma_kernel<WT, GEMV_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM))) return e;
-  if ((e = cudaFuncSetAttribute(gemv_mma_kernel<WT, GEMV_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM))) return e;
-  return cudaFuncSetAttribute(gemv_mma_kernel<WT, GEMV_LOGITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, GM_SMEM);
-}
-
-template <typename WT>
-static cudaError_t gemv_mma_dispatch(const GemvParams& p, int mode, int grid, cudaStream_t s, bool pdl) {
-  const dim3 g(grid), b(GEMV_THREADS);
-  switch (mode) {
-    case GEMV_QKV: return launch_k(gemv_mma_kernel<WT, GEMV_QKV>, g, b, (size_t)GM_SMEM, s, pdl, p);
-    case GEMV_GATEUP: return launch_k(gemv_mma_kernel<WT, GEMV_GATEUP>, g, b, (size_t)GM_SMEM, s, pdl, p);
-    case GEMV_RESID: return launch_k(gemv_mma_kernel<WT, GEMV_RESID>, g, b, (size_t)GM_SMEM, s, pdl, p);
-    default: return launch_k(gemv_mma_kernel<WT, GEMV_LOGITS>, g, b, (size_t)GM_SMEM, s, pdl, p);
-  }
+  if ((e = cudaFuncSetAttribute(gemv_splitk_kernel<WT, GEMV_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
+  if ((e = cudaFuncSetAttribute(gemv_splitk_kernel<WT, GEMV_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
+  if ((e = cudaFuncSetAttribute(gemv_splitk_kernel<WT, GEMV_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
+  return cudaFuncSetAttribute(gemv_splitk_kernel<WT, GEMV_LOGITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 // Rows b0 .. b0 + 15 (at most) of a batched projection on the tensor cores.
-static cudaError_t launch_gemv_mma(GemvParams p, int mode, int wdt, int num_sms, cudaStream_t s, bool pdl) {
-  const int n_wtasks = (p.n_tasks + 7) / 8;
-  // K split: the smallest that gives about 12 warps per SM, each slice a multiple of 32 in every chunk
-  p.ks = 1;
-  const int kc0 = p.K < GM_KCH ? p.K : GM_KCH;
-  while (p.ks < GEMV_WARPS && (long long)n_wtasks * p.ks < (long long)num_sms * 12 && (kc0 / (2 * p.ks)) % 32 == 0 &&
-         (p.K % GM_KCH) % (2 * p.ks * 32) == 0)
-    p.ks *= 2;
-  const int tpc = GEMV_WARPS / p.ks;
-  int grid = (n_wtasks + tpc - 1) / tpc;
-  const int cap = num_sms * 3;
-  if (grid > cap) grid = cap;
-  return wdt == WDT_F16 ? gemv_mma_dispatch<f16>(p, mode, grid, s, pdl) : gemv_mma_dispatch<bf16>(p, mode, grid, s, pdl);
+static cudaError_t launch_gemv_mma(GemvParams p, int mode, int wdt, cudaStream_t s, bool pdl) {
+  if (p.sk_part == nullptr || p.sk_ss == nullptr || p.sk_count == nullptr) return cudaErrorInvalidValue;
+  const GemvSplitK sk = gemv_splitk_shape(p.n_tasks, p.K);
+  const dim3 grid(sk.n_groups, sk.ksplit), block(GEMV_THREADS);
+  const size_t smem = (size_t)16 * (sk.kl + 8) * 2;
+  auto go = [&](auto kern) { return launch_k(kern, grid, block, smem, s, pdl, p, sk.ksplit, sk.kl); };
+  if (wdt == WDT_F16) {
+    switch (mode) {
+      case GEMV_QKV: return go(gemv_splitk_kernel<f16, GEMV_QKV>);
+      case GEMV_GATEUP: return go(gemv_splitk_kernel<f16, GEMV_GATEUP>);
+      case GEMV_RESID: return go(gemv_splitk_kernel<f16, GEMV_RESID>);
+      default: return go(gemv_splitk_kernel<f16, GEMV_LOGITS>);
+    }
+  }
+  switch (mode) {
+    case GEMV_QKV: return go(gemv_splitk_kernel<bf16, GEMV_QKV>);
+    case GEMV_GATEUP: return go(gemv_splitk_kernel<bf16, GEMV_GATEUP>);
+    case GEMV_RESID: return go(gemv_splitk_kernel<bf16, GEMV_RESID>);
+    default: return go(gemv_splitk_kernel<bf16, GEMV_LOGITS>);
+  }
 }
 
 int gemv_chunk(int B, int K) {
@@ -672,7 +679,7 @@ cudaError_t launch_gemv(const GemvParams& p0, int mode, int wdt, int num_sms, cu
       p.kfull = p.K;
       p.ldw = p.K;
       p.shard_tasks = p.n_tasks;
-      cudaError_t e = launch_gemv_mma(p, mode, wdt, num_sms, s, pdl);
+      cudaError_t e = launch_gemv_mma(p, mode, wdt, s, pdl);
       if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -922,6 +929,11 @@ static cudaError_t attn_decode_go(const AttnDecodeParams& p, int B, int n_kv, cu
   cudaError_t e = launch_k(attn_decode_kernel<KT, HD>, grid, dim3(ATT_THREADS), att_dyn_smem(HD), s, pdl, p);
   if (e == cudaSuccess) e = launch_k(attn_combine_kernel<HD>, dim3(p.n_q, B), dim3(HD), 0, s, pdl, p);
   return e;
+}
+
+cudaError_t launch_attn_combine(const AttnDecodeParams& p, int B, int hd, cudaStream_t s, bool pdl) {
+  if (hd == 64) return launch_k(attn_combine_kernel<64>, dim3(p.n_q, B), dim3(64), 0, s, pdl, p);
+  return launch_k(attn_combine_kernel<128>, dim3(p.n_q, B), dim3(128), 0, s, pdl, p);
 }
 
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, int B, int n_kv, int hd, int kv_dtype, cudaStream_t s,

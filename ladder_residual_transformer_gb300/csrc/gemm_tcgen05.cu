@@ -40,9 +40,12 @@ constexpr int TC_BM = 128;
 constexpr int TC_CHUNK = 128 * 64 * 2;  // one 128-row x 64-element chunk, 16 KB
 // Stage ring: 3 stages of 64 KB at BN = 128 (KC = 2), 4 of 48 KB at BN = 256 (KC = 1).
 constexpr int TC_RING = 3 * 4 * TC_CHUNK;
-// Epilogue staging: per epilogue warp one 32 x 32 fp32 block, rows padded to 33.
+// Epilogue buffers: per epilogue warp two 4 KB blocks (32 x 32 fp32, or 32 x 32
+// 16-bit values in the first half) that TMA fills and drains; the QKV epilogue
+// uses the same space as a 32 x 33 fp32 transpose block.
 constexpr int TC_EP_LD = 33;
-constexpr int TC_EP_BYTES = 4 * 32 * TC_EP_LD * 4;
+constexpr int TC_EP_WARP = 8192;
+constexpr int TC_EP_BYTES = 4 * TC_EP_WARP;
 constexpr int TC_SMEM = TC_RING + TC_EP_BYTES + 1024 + 256;
 constexpr int TC_THREADS = 192;
 constexpr long long TC_WAIT_LIMIT = 4000000000LL;  // cycles (about 2 s)
@@ -84,6 +87,8 @@ __device__ __forceinline__ bool b_half(const GemmParams& p, int tile_n, int h, i
 struct TcMaps {
   CUtensorMap a;
   CUtensorMap b[3];
+  CUtensorMap e_in;   // RESID: residual rows x_res (fp32, box 32 x 32, 128-byte swizzle)
+  CUtensorMap e_out;  // RESID: output rows (fp32, as e_in); GATEUP: SwiGLU rows (16-bit, box 32 x 32, 64-byte swizzle)
 };
 
 // Persistent CTA: tiles t = blockIdx.x + i * gridDim.x, tile t -> (m = t % m_tiles,
@@ -103,12 +108,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
   constexpr int NST = TC_RING / STAGE;
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
-  float* ep_all = reinterpret_cast<float*>(smem + TC_RING);
+  uint8_t* ep_all = smem + TC_RING;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + TC_RING + TC_EP_BYTES);
   uint64_t* empty = full + NST;
   uint64_t* tfull = empty + NST;   // [2] accumulator ready
   uint64_t* tempty = tfull + 2;    // [2] accumulator drained
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* ebar = tempty + 2;     // [4 warps][2] epilogue block loaded
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ebar + 8);
   int* bail = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -125,6 +131,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], 4);  // one arrival per epilogue warp
     }
+    for (int e = 0; e < 8; ++e) mbar_init(&ebar[e], 1);
     *bail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -164,6 +171,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
           tma_load_3d(st, &maps.a, 0, m0, kb * KC, &full[s]);
           tma_load_3d(st + A_BYTES, &maps.b[map0], 0, row0, kb * KC, &full[s]);
           if (HALVES == 2) tma_load_3d(st + A_BYTES + BH_BYTES, &maps.b[map1], 0, row1, kb * KC, &full[s]);
+          // The CTAs of a tile column read the same weight boxes at about the same
+          // time; for 128-wide tiles the first m tile asks L2 for them 2 * NST
+          // steps ahead, so that the ring's copies hit L2 instead of waiting on
+          // DRAM (measured: faster for 128-wide tiles, slower for the 256-wide
+          // gate/up tiles).
+          if (BN == 128 && m0 == 0 && kb + 2 * NST < nkb) {
+            tma_prefetch_3d(&maps.b[map0], 0, row0, (kb + 2 * NST) * KC);
+            if (HALVES == 2) tma_prefetch_3d(&maps.b[map1], 0, row1, (kb + 2 * NST) * KC);
+          }
         }
       }
       // Make sure no copy into this CTA's shared memory is still in flight.
@@ -213,12 +229,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
       }
     }
   } else {
-    // Epilogue warp w owns tile rows 32w .. 32w + 31 (its TMEM lanes).  Each
-    // 32-column chunk is read from TMEM row-wise (lane = row), staged in shared
-    // memory and read back column-wise, so that global loads and stores of a
-    // warp instruction cover whole row segments instead of 32 different rows.
+    // Epilogue warp w owns tile rows 32w .. 32w + 31 (its TMEM lanes; lane =
+    // row).  RESID and GATEUP move 32 x 32 blocks through TMA: the residual
+    // block is loaded before it is needed, lane r adds accumulator row r to
+    // row r of the block in shared memory, and a TMA store writes the block
+    // out.  QKV transposes each 32 x 32 block through shared memory so that
+    // a warp's global stores (q rows, paged K/V slots) are row segments.
     const int hd = p.kv.head_dim;
-    float* ep = ep_all + warp * 32 * TC_EP_LD;
+    uint8_t* ewarp = ep_all + warp * TC_EP_WARP;
+    float* ep = reinterpret_cast<float*>(ewarp);
+    uint64_t* eb = ebar + warp * 2;
+    constexpr int NCH = BN / 32;  // 32-column chunks of a tile
+    uint32_t nload[2] = {0, 0}, nwait[2] = {0, 0};  // loads issued / consumed per buffer (warp-uniform)
+    bool ep_ok = true;
     const int cp = 2 * (lane & 15), rsub = lane >> 4;  // 16-bit outputs: column pair, row parity
     for (int i = 0; i < my_tiles; ++i) {
       const int acc = i & 1;
@@ -235,10 +258,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
         const int page = p.kv.block_table[bb * p.kv.max_pages + (my_pos >> p.kv.page_shift)];
         my_slot = (long long)page * (long long)p.kv.page_elems() + (long long)(my_pos & (p.kv.page_size - 1)) * hd;
       }
+      if (MODE == GEMM_RESID) {
+        // the first two residual blocks of the tile, while its accumulator is computed
+        if (lane == 0) bulk_wait_read_all();  // the previous tile's stores have left the buffers
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          if (lane == 0) {
+            mbar_expect_tx(&eb[c], 4096);
+            tma_load_2d(ewarp + c * 4096, &maps.e_in, tile_n * BN + c * 32, mrow0, &eb[c]);
+          }
+          ++nload[c];
+        }
+      }
       const bool ok = mbar_wait(&tfull[acc], (i >> 1) & 1);
       tc_fence_after();
       if (!ok) {
         if (lane == 0) atomicOr(err, 2);
+        ep_ok = false;
         break;
       }
       if (__shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(bail), 0)) break;
@@ -250,43 +286,69 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
       };
       if (MODE == GEMM_GATEUP) {
         for (int c = 0; c < 4; ++c) {
+          uint8_t* buf = ewarp + (c & 1) * 4096;
+          // buffer c & 1 was last stored two chunks ago
+          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+          __syncwarp();
           float gv[32], uv[32];
           tmem_ld32(trow + c * 32, gv);
           tmem_ld32(trow + 128 + c * 32, uv);
+          uint32_t pk[16];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) gv[j] = silu_f(gv[j]) * uv[j];
-          stage(gv);
-          WT* dst = static_cast<WT*>(p.out_h) + tile_n * 128 + c * 32 + cp;
+          for (int j = 0; j < 16; ++j)
+            pk[j] = C::pack(silu_f(gv[2 * j]) * uv[2 * j], silu_f(gv[2 * j + 1]) * uv[2 * j + 1]);
+          // row lane, 64-byte rows, 16-byte chunk q at q ^ ((row >> 1) & 3) (64-byte swizzle)
+          uint4* rowp = reinterpret_cast<uint4*>(buf + lane * 64);
 #pragma unroll
-          for (int r2 = 0; r2 < 16; ++r2) {
-            const int r = 2 * r2 + rsub, m = mrow0 + r;
-            if (m < p.M)
-              *reinterpret_cast<uint32_t*>(dst + (size_t)m * p.ldo) =
-                  C::pack(ep[r * TC_EP_LD + cp], ep[r * TC_EP_LD + cp + 1]);
-          }
+          for (int q = 0; q < 4; ++q)
+            rowp[q ^ ((lane >> 1) & 3)] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          fence_proxy_async_smem();
           __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&maps.e_out, buf, tile_n * 128 + c * 32, mrow0);
+            bulk_commit();
+          }
         }
       } else if (MODE == GEMM_RESID) {
-        for (int c = 0; c < BN / 32; ++c) {
-          const int n0 = tile_n * BN + c * 32;
-          if (n0 >= p.N) break;
+        for (int c = 0; c < NCH; ++c) {
+          const int bi = c & 1;
+          float* buf = reinterpret_cast<float*>(ewarp + bi * 4096);
+          const bool okc = __all_sync(0xffffffffu, mbar_wait(&eb[bi], nwait[bi] & 1));
+          ++nwait[bi];
+          if (!okc) {
+            if (lane == 0) atomicOr(err, 2);
+            ep_ok = false;
+            break;
+          }
           float v[32];
           tmem_ld32(trow + c * 32, v);
-          // the 32 residual values of this lane's column, all loads in flight at once
-          float xr[32];
+          // row lane of the block: 16-byte chunk q at q ^ (row & 7) (128-byte swizzle)
+          float4* rowp = reinterpret_cast<float4*>(buf + lane * 32);
 #pragma unroll
-          for (int r = 0; r < 32; ++r) {
-            const int m = mrow0 + r;
-            xr[r] = m < p.M ? p.x_res[(size_t)m * p.ldo + n0 + lane] : 0.f;
+          for (int q = 0; q < 8; ++q) {
+            float4 xv = rowp[q ^ (lane & 7)];
+            xv.x += v[4 * q];
+            xv.y += v[4 * q + 1];
+            xv.z += v[4 * q + 2];
+            xv.w += v[4 * q + 3];
+            rowp[q ^ (lane & 7)] = xv;
           }
-          stage(v);
-#pragma unroll
-          for (int r = 0; r < 32; ++r) {
-            const int m = mrow0 + r;
-            if (m < p.M) p.out_f[(size_t)m * p.ldo + n0 + lane] = xr[r] + ep[r * TC_EP_LD + lane];
-          }
+          fence_proxy_async_smem();
           __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&maps.e_out, buf, tile_n * BN + c * 32, mrow0);
+            bulk_commit();
+          }
+          if (c + 2 < NCH) {
+            if (lane == 0) {
+              bulk_wait_read_all();  // the store above has read the buffer
+              mbar_expect_tx(&eb[bi], 4096);
+              tma_load_2d(buf, &maps.e_in, tile_n * BN + (c + 2) * 32, mrow0, &eb[bi]);
+            }
+            ++nload[bi];
+          }
         }
+        if (!ep_ok) break;
       } else {  // GEMM_QKV
         for (int c = 0; c < BN / 32; ++c) {
           int map, row;
@@ -331,6 +393,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&tempty[acc])) : "memory");
     }
+    // Nothing may be in flight into or out of shared memory at exit: outstanding
+    // block loads (only after an error) and the last block stores.
+    if (lane == 0) {
+      for (int bi = 0; bi < 2; ++bi)
+        for (; nwait[bi] < nload[bi]; ++nwait[bi]) mbar_wait(&eb[bi], nwait[bi] & 1);
+      bulk_wait_all();
+    }
+    (void)ep_ok;
   }
   tc_fence_before();
   __syncthreads();
@@ -395,6 +465,25 @@ bool make_tma_operand(TmaOperand* out, const void* base, uint64_t rows, uint64_t
   return true;
 }
 
+// Epilogue block map of a row-major [rows, cols] matrix: fp32 (elem_bytes 4,
+// 128-byte swizzle) or the weight dtype (elem_bytes 2, 64-byte swizzle), box of
+// 32 columns x 32 rows.  Stores outside [rows, cols] are dropped by the TMA.
+bool make_tma_map_epilogue(void* map_out, const void* base, uint64_t rows, uint64_t cols, int elem_bytes, int wdt) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || cols % 32 || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * (cuuint64_t)elem_bytes};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt = elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : wdt == WDT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle sw = elem_bytes == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  CUresult r = fn(reinterpret_cast<CUtensorMap*>(map_out), dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // One layer of the paged KV pool viewed as [pages * 2 * n_kv][page_size][hd]
 // 16-bit elements; box = 64 elements x page_size slots x 1, 128-byte swizzle.
 bool make_kv_tma_map(void* map_out, const void* base, uint64_t num_pages, int n_kv, int page_size, int hd, int wdt) {
@@ -428,12 +517,14 @@ cudaError_t gemm_tc_configure() {
 
 // Tile width BN with its box depth: 256-wide tiles take 1-chunk boxes, 128-wide 2-chunk boxes.
 template <typename WT, int MODE, int BN>
-static cudaError_t gemm_tc_go(const TmaOperand* a, const TmaOperand* const* b, const GemmParams& p, int mt, int nt,
-                              int num_sms, int* err, cudaStream_t s) {
+static cudaError_t gemm_tc_go(const TmaOperand* a, const TmaOperand* const* b, const void* const* e,
+                              const GemmParams& p, int mt, int nt, int num_sms, int* err, cudaStream_t s) {
   constexpr int KC = BN == 256 ? 1 : 2;
   TcMaps maps;
   memcpy(&maps.a, &a->box[KC - 1], sizeof(CUtensorMap));
   for (int i = 0; i < 3; ++i) memcpy(&maps.b[i], &(b[i] ? b[i] : b[0])->box[KC - 1], sizeof(CUtensorMap));
+  memcpy(&maps.e_in, e[0] ? e[0] : &maps.a, sizeof(CUtensorMap));
+  memcpy(&maps.e_out, e[1] ? e[1] : &maps.a, sizeof(CUtensorMap));
   const int total = mt * nt;
   const int grid = total < num_sms ? total : num_sms;
   gemm_tc_kernel<WT, MODE, BN, KC><<<grid, TC_THREADS, TC_SMEM, s>>>(maps, p, mt, nt, err);
@@ -442,26 +533,31 @@ static cudaError_t gemm_tc_go(const TmaOperand* a, const TmaOperand* const* b, c
 
 // 256-wide tiles unless that leaves most SMs idle (narrow N at small M).
 template <typename WT>
-static cudaError_t gemm_tc_dispatch(const TmaOperand* a, const TmaOperand* const* b, const GemmParams& p, int mode,
-                                    int mt, int num_sms, int* err, cudaStream_t s) {
-  if (mode == GEMM_GATEUP) return gemm_tc_go<WT, GEMM_GATEUP, 256>(a, b, p, mt, p.N / 128, num_sms, err, s);
+static cudaError_t gemm_tc_dispatch(const TmaOperand* a, const TmaOperand* const* b, const void* const* e,
+                                    const GemmParams& p, int mode, int mt, int num_sms, int* err, cudaStream_t s) {
+  if (mode == GEMM_GATEUP) return gemm_tc_go<WT, GEMM_GATEUP, 256>(a, b, e, p, mt, p.N / 128, num_sms, err, s);
   const int nt256 = (p.N + 255) / 256;
   const bool narrow = (long long)mt * nt256 * 4 < (long long)num_sms * 3;
   if (mode == GEMM_RESID) {
-    if (narrow) return gemm_tc_go<WT, GEMM_RESID, 128>(a, b, p, mt, (p.N + 127) / 128, num_sms, err, s);
-    return gemm_tc_go<WT, GEMM_RESID, 256>(a, b, p, mt, nt256, num_sms, err, s);
+    if (narrow) return gemm_tc_go<WT, GEMM_RESID, 128>(a, b, e, p, mt, (p.N + 127) / 128, num_sms, err, s);
+    return gemm_tc_go<WT, GEMM_RESID, 256>(a, b, e, p, mt, nt256, num_sms, err, s);
   }
-  if (narrow) return gemm_tc_go<WT, GEMM_QKV, 128>(a, b, p, mt, (p.N + 127) / 128, num_sms, err, s);
-  return gemm_tc_go<WT, GEMM_QKV, 256>(a, b, p, mt, nt256, num_sms, err, s);
+  if (narrow) return gemm_tc_go<WT, GEMM_QKV, 128>(a, b, e, p, mt, (p.N + 127) / 128, num_sms, err, s);
+  return gemm_tc_go<WT, GEMM_QKV, 256>(a, b, e, p, mt, nt256, num_sms, err, s);
 }
 
 cudaError_t launch_gemm_tc(const TmaOperand* a, const TmaOperand* b0, const TmaOperand* b1, const TmaOperand* b2,
-                           const GemmParams& p, int mode, int wdt, int num_sms, int* err, cudaStream_t s) {
+                           const void* e_in, const void* e_out, const GemmParams& p, int mode, int wdt, int num_sms,
+                           int* err, cudaStream_t s) {
   if (p.M <= 0) return cudaSuccess;
+  // RESID reads and writes its rows through the epilogue maps, GATEUP writes through e_out
+  if ((mode == GEMM_RESID && (!e_in || !e_out)) || (mode == GEMM_GATEUP && !e_out)) return cudaErrorInvalidValue;
+  if (mode == GEMM_RESID && p.N % 256) return cudaErrorInvalidValue;  // every 32-column block of a tile exists
   const TmaOperand* b[3] = {b0, b1, b2};
+  const void* e[2] = {e_in, e_out};
   const int mt = (p.M + TC_BM - 1) / TC_BM;
-  return wdt == WDT_F16 ? gemm_tc_dispatch<f16>(a, b, p, mode, mt, num_sms, err, s)
-                        : gemm_tc_dispatch<bf16>(a, b, p, mode, mt, num_sms, err, s);
+  return wdt == WDT_F16 ? gemm_tc_dispatch<f16>(a, b, e, p, mode, mt, num_sms, err, s)
+                        : gemm_tc_dispatch<bf16>(a, b, e, p, mode, mt, num_sms, err, s);
 }
 
 }  // namespace ladder

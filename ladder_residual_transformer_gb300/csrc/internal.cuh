@@ -144,7 +144,20 @@ struct GemvParams {
   const float* rope_sin;
   const int* pos;         // position of row b (the sequence length before this step)
   KvLayer kv;
+  // Batched rows (B > 4): split-K workspace of this projection (gemv_splitk_bytes
+  // bytes laid out as partial sums, per-slice sums of squares, group counters;
+  // counters zero before the first launch and left zero by every launch).
+  float* sk_part;
+  float* sk_ss;
+  int* sk_count;
 };
+
+// Split-K shape of a batched decode projection with n_tasks GEMV tasks and depth K.
+struct GemvSplitK {
+  int n_wtasks, n_groups, ksplit, kl;
+};
+GemvSplitK gemv_splitk_shape(int n_tasks, int K);
+size_t gemv_splitk_bytes(int n_tasks, int K);
 
 struct AttnDecodeParams {
   const float* q;      // [B][n_q * hd] rotated queries
@@ -197,6 +210,14 @@ int gemv_chunk(int B, int K);
 int gemv_launch_count(int B, int K, int mode);
 cudaError_t launch_attn_decode(const AttnDecodeParams& p, int B, int n_kv, int hd, int kv_dtype, cudaStream_t s,
                                bool pdl = false);
+// Merge of the per-split partials (part_o, part_ml) into out.
+cudaError_t launch_attn_combine(const AttnDecodeParams& p, int B, int hd, cudaStream_t s, bool pdl);
+// Decode attention on the tensor cores (mma.sync), K/V pages through the layer's
+// KV pool map (make_kv_tma_map); split_len 128, head_dim 64 or 128, up to 8 query
+// heads per KV head.  Launches the split kernel and the combine step.
+cudaError_t attn_decode_tc_configure();
+cudaError_t launch_attn_decode_tc(const void* kv_map, const AttnDecodeParams& p, int B, int n_kv, int hd, int wdt,
+                                  int* err, cudaStream_t s, bool pdl);
 cudaError_t launch_argmax(const float* logits, int B, int V, float* part_v, int* part_i, int nblk,
                           int* out, cudaStream_t s, bool pdl = false);
 cudaError_t launch_advance(int* seq_lens, int B, cudaStream_t s, bool pdl = false);
@@ -214,11 +235,16 @@ struct TmaOperand {
   CUtensorMap box[2];
 };
 bool make_tma_operand(TmaOperand* out, const void* base, uint64_t rows, uint64_t cols, int wdt);
+// Epilogue block map (box 32 x 32): fp32 rows (elem_bytes 4) or weight-dtype rows (2).
+bool make_tma_map_epilogue(void* map_out, const void* base, uint64_t rows, uint64_t cols, int elem_bytes, int wdt);
 // One layer of the paged KV pool as a 3-D map (see gemm_tcgen05.cu).
 bool make_kv_tma_map(void* map_out, const void* base, uint64_t num_pages, int n_kv, int page_size, int hd, int wdt);
 cudaError_t gemm_tc_configure();
+// e_in / e_out: make_tma_map_epilogue maps of the residual rows and the output
+// rows (RESID, fp32) or of the SwiGLU output rows (GATEUP e_out, weight dtype).
 cudaError_t launch_gemm_tc(const TmaOperand* a, const TmaOperand* b0, const TmaOperand* b1, const TmaOperand* b2,
-                           const GemmParams& p, int mode, int wdt, int num_sms, int* err, cudaStream_t s);
+                           const void* e_in, const void* e_out, const GemmParams& p, int mode, int wdt, int num_sms,
+                           int* err, cudaStream_t s);
 // Tensor-core causal attention for packed prefill rows (mma.sync, bf16 Q/K/V).
 // Prefill attention on tcgen05: q_map = make_tma_map of the query rows, kv_map =
 // make_kv_tma_map of the layer; head_dim 64 or 128.

@@ -50,8 +50,13 @@ namespace {
 constexpr int kSplitLen = 128;      // keys per decode-attention split
 constexpr int kArgmaxBlocks = 64;   // partial argmax blocks per sequence
 
+// Split-K workspace of the batched decode projections (B > 4), one region per
+// projection kind so that the two decode streams never share one.
+enum SplitKKind { SK_QKV = 0, SK_OUT = 1, SK_GATEUP = 2, SK_DOWN = 3, SK_LMHEAD = 4, SK_KINDS = 5 };
+
 struct Plan {
   size_t x[3], xn, q, ao, act, part_o, part_ml, am_v, am_i, rope_cos, rope_sin, meta, xlast, err, shard;
+  size_t sk[SK_KINDS], sk_bytes[SK_KINDS];
   size_t total;
   int m_max, m_pad, nsplit_max;
 };
@@ -86,6 +91,15 @@ Plan make_plan(const ladder_config& c) {
   p.xlast = take(Bm * d * 4);
   p.err = take(256);
   p.shard = c.shard_k > 1 ? take(2 * Bm * c.shard_k * d * 4) : 0;  // double-buffered shard partials [B][k][d]
+  if (c.max_batch > 4) {
+    const size_t kvd = (size_t)c.n_kv_heads * c.head_dim;
+    const int nt[SK_KINDS] = {(int)((qd + 2 * kvd) / 2), (int)(d / 2), (int)f, (int)(d / 2), c.vocab / 2};
+    const int kk[SK_KINDS] = {(int)d, (int)qd, (int)d, (int)f, (int)d};
+    for (int i = 0; i < SK_KINDS; ++i) {
+      p.sk_bytes[i] = gemv_splitk_bytes(nt[i], kk[i]);
+      p.sk[i] = take(p.sk_bytes[i]);
+    }
+  }
   p.total = off;
   return p;
 }
@@ -166,6 +180,8 @@ struct ladder_model {
   std::vector<LayerMaps> maps;
   TmaOperand map_xn, map_ao, map_act;  // activation operands, m_pad rows
   CUtensorMap map_q;  // rotated queries [m_pad][n_q * hd], the prefill attention operand
+  CUtensorMap map_x[3];   // stream buffers [m_max][d] fp32, epilogue blocks (prefill residual GEMMs)
+  CUtensorMap map_act_st; // SwiGLU rows [m_pad][ffn], epilogue blocks (prefill gate/up GEMM)
   char* ws;
   Plan plan;
   int num_sms;
@@ -190,6 +206,19 @@ struct ladder_model {
   float* X(int i) { return reinterpret_cast<float*>(ws + plan.x[i % 3]); }
   template <class T> T* at(size_t off) { return reinterpret_cast<T*>(ws + off); }
   int* err() { return at<int>(plan.err); }
+
+  // Point a batched decode projection at its split-K region (no-op when the
+  // model was created for at most 4 rows).
+  void splitk(GemvParams& g, int kind) {
+    if (!plan.sk_bytes[kind]) return;
+    const GemvSplitK sk = gemv_splitk_shape(g.n_tasks, g.K);
+    char* base = ws + plan.sk[kind];
+    size_t off = align_up((size_t)sk.ksplit * sk.n_wtasks * 256 * 4, 256);
+    g.sk_part = reinterpret_cast<float*>(base);
+    g.sk_ss = reinterpret_cast<float*>(base + off);
+    off += align_up((size_t)sk.n_groups * sk.ksplit * 16 * 4, 256);
+    g.sk_count = reinterpret_cast<int*>(base + off);
+  }
 
   // Index j of the stream state x_j that module k (1-based) reads.
   int input_index(int k) const {
@@ -322,7 +351,11 @@ int ladder_create(const ladder_config* cfg, const ladder_weights* w, void* works
     bool ok = make_tma_operand(&m->map_xn, m->ws + plan.xn, Mp, d, wdt) &&
               make_tma_operand(&m->map_ao, m->ws + plan.ao, Mp, qd, wdt) &&
               make_tma_operand(&m->map_act, m->ws + plan.act, Mp, f, wdt) &&
-              make_tma_map(&m->map_q, m->ws + plan.q, Mp, qd, wdt);
+              make_tma_map(&m->map_q, m->ws + plan.q, Mp, qd, wdt) &&
+              make_tma_map_epilogue(&m->map_x[0], m->ws + plan.x[0], plan.m_max, d, 4, wdt) &&
+              make_tma_map_epilogue(&m->map_x[1], m->ws + plan.x[1], plan.m_max, d, 4, wdt) &&
+              make_tma_map_epilogue(&m->map_x[2], m->ws + plan.x[2], plan.m_max, d, 4, wdt) &&
+              make_tma_map_epilogue(&m->map_act_st, m->ws + plan.act, Mp, f, 2, wdt);
     m->maps.resize(c.n_layers);
     for (int l = 0; ok && l < c.n_layers; ++l) {
       const LayerW& L = m->layers[l];
@@ -343,11 +376,14 @@ int ladder_create(const ladder_config* cfg, const ladder_weights* w, void* works
   if (e == cudaSuccess) e = gemv_configure();
   if (e == cudaSuccess) e = gemm_tc_configure();
   if (e == cudaSuccess) e = attn_prefill_tcgen05_configure();
+  if (e == cudaSuccess) e = attn_decode_tc_configure();
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&m->aux, cudaStreamNonBlocking);
   for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&m->ev_slot[i], cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_fork, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_part, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaMemsetAsync(m->err(), 0, 256, stream);
+  for (int i = 0; i < SK_KINDS && e == cudaSuccess; ++i)
+    if (plan.sk_bytes[i]) e = cudaMemsetAsync(m->ws + plan.sk[i], 0, plan.sk_bytes[i], stream);
   if (e == cudaSuccess)
     e = launch_rope_tables(m->at<float>(plan.rope_cos), m->at<float>(plan.rope_sin), cfg->max_seq, cfg->head_dim,
                            cfg->rope_theta, stream);
@@ -593,18 +629,20 @@ int enqueue_decode_shard(ladder_model* m, ladder_kv* kv, const int32_t* tokens, 
       g.out = q; g.ldo = qd; g.nq_hd = qd; g.nkv_hd = kvd;
       g.rope_cos = m->at<float>(P.rope_cos); g.rope_sin = m->at<float>(P.rope_sin);
       g.pos = kv->seq_lens; g.kv = kvl; g.err = m->err();
+      m->splitk(g, SK_QKV);
       LAUNCH(launch_gemv(g, GEMV_QKV, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, g.K, GEMV_QKV));
       AttnDecodeParams a{};
       a.q = q; a.kv = kvl; a.seq_lens = kv->seq_lens; a.n_q = c.n_q_heads; a.split_len = kSplitLen;
       a.nsplit = nsplit; a.scale = 1.0f / sqrtf((float)c.head_dim);
       a.part_o = m->at<float>(P.part_o); a.part_ml = m->at<float>(P.part_ml); a.out = ao;
-      LAUNCH(launch_attn_decode(a, B, c.n_kv_heads, c.head_dim, m->wdt, s, pdl), 2);
+      LAUNCH(launch_attn_decode_tc(&kv->maps[l], a, B, c.n_kv_heads, c.head_dim, m->wdt, m->err(), s, pdl), 2);
       o.x = ao; o.ldx = qd; o.K = qd / ksh; o.kfull = qd; o.ldw = qd; o.w0 = L.wo;
     } else {  // MLP module
       GemvParams g{};
       g.x = m->X(j); g.ldx = d; g.g = L.mlp_norm; g.eps = c.norm_eps; g.B = B; g.K = d;
       g.w0 = L.w_gate; g.w1 = L.w_up; g.n_tasks = f; g.out = act; g.ldo = f; g.err = m->err();
       cudaEvent_t pe = m->probe_start(LADDER_PROBE_GATEUP, s);
+      m->splitk(g, SK_GATEUP);
       LAUNCH(launch_gemv(g, GEMV_GATEUP, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, g.K, GEMV_GATEUP));
       m->probe_stop(pe, s);
       o.x = act; o.ldx = f; o.K = f / ksh; o.kfull = f; o.ldw = f; o.w0 = L.w_down;
@@ -625,6 +663,7 @@ int enqueue_decode_shard(ladder_model* m, ladder_kv* kv, const int32_t* tokens, 
   GemvParams h{};
   h.x = m->X(2 * c.n_layers); h.ldx = d; h.g = m->final_norm; h.eps = c.norm_eps; h.B = B; h.K = d;
   h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.out = logits; h.ldo = c.vocab; h.err = m->err();
+  m->splitk(h, SK_LMHEAD);
   LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, h.K, GEMV_LOGITS));
   if (next_tok)
     LAUNCH(launch_argmax(logits, B, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i), kArgmaxBlocks, next_tok, s, pdl), 2);
@@ -683,6 +722,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       g.pos = kv->seq_lens; g.kv = kvl;
       cudaEvent_t pe = m->probe_start(LADDER_PROBE_QKV, s);
       g.err = m->err();
+      m->splitk(g, SK_QKV);
       LAUNCH(launch_gemv(g, GEMV_QKV, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, g.K, GEMV_QKV));
       m->probe_stop(pe, s);
 
@@ -691,7 +731,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       a.nsplit = nsplit; a.scale = 1.0f / sqrtf((float)c.head_dim);
       a.part_o = m->at<float>(P.part_o); a.part_ml = m->at<float>(P.part_ml); a.out = ao;
       pe = m->probe_start(LADDER_PROBE_ATTN, s);
-      LAUNCH(launch_attn_decode(a, B, c.n_kv_heads, c.head_dim, m->wdt, s, pdl), 2);
+      LAUNCH(launch_attn_decode_tc(&kv->maps[l], a, B, c.n_kv_heads, c.head_dim, m->wdt, m->err(), s, pdl), 2);
       m->probe_stop(pe, s);
 
       if ((rc = use(k - 1, 0))) return rc;
@@ -700,6 +740,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       o.out = m->X(k); o.ldo = d; o.x_res = m->X(k - 1); o.ldr = d;
       pe = m->probe_start(LADDER_PROBE_OUT, s);
       o.err = m->err();
+      m->splitk(o, SK_OUT);
       LAUNCH(launch_gemv(o, GEMV_RESID, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, o.K, GEMV_RESID));
       m->probe_stop(pe, s);
       if ((rc = wrote(k, 0))) return rc;
@@ -715,6 +756,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       g.w0 = L.w_gate; g.w1 = L.w_up; g.n_tasks = f; g.out = act; g.ldo = f;
       cudaEvent_t pe = m->probe_start(LADDER_PROBE_GATEUP, ms);
       g.err = m->err();
+      m->splitk(g, SK_GATEUP);
       LAUNCH(launch_gemv(g, GEMV_GATEUP, m->wdt, m->num_sms, ms, pdl), gemv_launch_count(B, g.K, GEMV_GATEUP));
       m->probe_stop(pe, ms);
 
@@ -724,6 +766,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       o.out = m->X(k); o.ldo = d; o.x_res = m->X(k - 1); o.ldr = d;
       pe = m->probe_start(LADDER_PROBE_DOWN, ms);
       o.err = m->err();
+      m->splitk(o, SK_DOWN);
       LAUNCH(launch_gemv(o, GEMV_RESID, m->wdt, m->num_sms, ms, pdl), gemv_launch_count(B, o.K, GEMV_RESID));
       m->probe_stop(pe, ms);
       if ((rc = wrote(k, mlp_stream))) return rc;
@@ -735,6 +778,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
   h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.out = logits; h.ldo = c.vocab;
   cudaEvent_t pe = m->probe_start(LADDER_PROBE_LMHEAD, s);
   h.err = m->err();
+  m->splitk(h, SK_LMHEAD);
   LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, h.K, GEMV_LOGITS));
   m->probe_stop(pe, s);
   if (next_tok)
@@ -860,7 +904,7 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
       g.out_h = qb; g.ldo = qd; g.nq_hd = qd; g.nkv_hd = kvd;
       g.rope_cos = m->at<float>(P.rope_cos); g.rope_sin = m->at<float>(P.rope_sin);
       g.row_b = d_row_b; g.row_pos = d_row_pos; g.kv = kvl;
-      LAUNCH(launch_gemm_tc(&m->map_xn, &T.wq, &T.wk, &T.wv, g, GEMM_QKV, wdt, m->num_sms, m->err(), s), 1);
+      LAUNCH(launch_gemm_tc(&m->map_xn, &T.wq, &T.wk, &T.wv, nullptr, nullptr, g, GEMM_QKV, wdt, m->num_sms, m->err(), s), 1);
 
       AttnPrefillParams a{};
       a.q = qb; a.kv = kvl; a.seq_start = d_start; a.seq_len = d_lens;
@@ -869,17 +913,20 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
 
       GemmParams o{};
       o.M = M; o.N = d; o.K = qd; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);
-      LAUNCH(launch_gemm_tc(&m->map_ao, &T.wo, nullptr, nullptr, o, GEMM_RESID, wdt, m->num_sms, m->err(), s), 1);
+      LAUNCH(launch_gemm_tc(&m->map_ao, &T.wo, nullptr, nullptr, &m->map_x[(k - 1) % 3], &m->map_x[k % 3], o,
+                            GEMM_RESID, wdt, m->num_sms, m->err(), s), 1);
     }
     {
       const int k = 2 * l + 2;
       LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.mlp_norm, c.norm_eps, xn, wdt, s), 1);
       GemmParams g{};
       g.M = M; g.N = f; g.K = d; g.out_h = actb; g.ldo = f;
-      LAUNCH(launch_gemm_tc(&m->map_xn, &T.gate, &T.up, nullptr, g, GEMM_GATEUP, wdt, m->num_sms, m->err(), s), 1);
+      LAUNCH(launch_gemm_tc(&m->map_xn, &T.gate, &T.up, nullptr, nullptr, &m->map_act_st, g, GEMM_GATEUP, wdt,
+                            m->num_sms, m->err(), s), 1);
       GemmParams o{};
       o.M = M; o.N = d; o.K = f; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);
-      LAUNCH(launch_gemm_tc(&m->map_act, &T.down, nullptr, nullptr, o, GEMM_RESID, wdt, m->num_sms, m->err(), s), 1);
+      LAUNCH(launch_gemm_tc(&m->map_act, &T.down, nullptr, nullptr, &m->map_x[(k - 1) % 3], &m->map_x[k % 3], o,
+                            GEMM_RESID, wdt, m->num_sms, m->err(), s), 1);
     }
   }
   float* xlast = m->at<float>(P.xlast);
@@ -888,6 +935,7 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
   h.x = xlast; h.ldx = d; h.g = m->final_norm; h.eps = c.norm_eps; h.B = B; h.K = d;
   h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.out = logits; h.ldo = c.vocab;
   h.err = m->err();
+  m->splitk(h, SK_LMHEAD);
   LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s), gemv_launch_count(B, h.K, GEMV_LOGITS));
   if (next_tok)
     LAUNCH(launch_argmax(logits, B, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i), kArgmaxBlocks, next_tok, s), 2);
