@@ -38,10 +38,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic of the dominant kernel from one ncu capture, valid only while the
 # kernel source is unchanged (sha256 of the file that defines it).
-NCU_TRAFFIC = {  # profiles/gemv_gateup_1p2b_ncu_full.md (mean of the two captured launches)
+NCU_TRAFFIC = {  # profiles/gemv_gateup_1p2b_traffic.md (mean of the two captured launches)
     "source": "ladder_residual_transformer_gb300/csrc/decode_kernels.cu",
-    "sha256": "34e4e9f54af6409ec4444c631ede82b1870b753645a96597b65219923f1e3f1d",
-    "bytes_per_launch": 67608320,
+    "sha256": "34760af97f3022aa8d281dae24ae8a903b97f62206c59612ed7f9a4f240bc492",
+    "bytes_per_launch": 67295488,
 }
 
 
