@@ -95,7 +95,36 @@ struct TcMaps {
 // n = t / m_tiles) so that CTAs running together share the weight tile in L2.
 // The accumulator is double-buffered in TMEM (2 x BN columns): the MMA warp
 // fills buffer i & 1 while the epilogue warps drain the other one.
-template <typename WT, int MODE, int BN, int KC>
+//
+// PAIR = 1 (BN = 256): clusters of two CTAs compute 256 x 256 tiles with the
+// paired MMA (tcgen05 cta_group::2): each CTA holds the A rows of its own m
+// tile and one 128-row half of B, so a stage is 32 KB instead of 48 KB (6
+// stages instead of 4) and each SM's shared memory serves half as many B bytes
+// per MMA.  Both CTAs' copies signal the leader's full barrier; the leader
+// issues the M = 256 MMAs and commits to both CTAs' empty and accumulator-full
+// barriers; both CTAs' epilogue warps arrive on the leader's accumulator-empty
+// barrier.
+template <int PAIR>
+__device__ __forceinline__ int gemm_tile_count(int m_tiles, int n_tiles) {
+  const int units = PAIR ? (m_tiles / 2) * n_tiles : m_tiles * n_tiles;
+  const int id = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+  const int nid = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
+  return id < units ? (units - 1 - id) / nid + 1 : 0;
+}
+template <int PAIR>
+__device__ __forceinline__ void gemm_tile(int i, int m_tiles, uint32_t crank, int& m_tile, int& tile_n) {
+  if (PAIR) {
+    const int u = (int)blockIdx.x / 2 + i * ((int)gridDim.x / 2), mp = m_tiles / 2;
+    m_tile = 2 * (u % mp) + (int)crank;
+    tile_n = u / mp;
+  } else {
+    const int t = blockIdx.x + i * gridDim.x;
+    m_tile = t % m_tiles;
+    tile_n = t / m_tiles;
+  }
+}
+
+template <typename WT, int MODE, int BN, int KC, int PAIR>
 __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_constant__ TcMaps maps,
                                                                 const GemmParams p, int m_tiles, int n_tiles,
                                                                 int* err) {
@@ -104,8 +133,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
   constexpr int BK = 64 * KC;
   constexpr int A_BYTES = KC * TC_CHUNK;   // 128 rows of A
   constexpr int BH_BYTES = KC * TC_CHUNK;  // one 128-row half of B
-  constexpr int STAGE = A_BYTES + HALVES * BH_BYTES;
+  constexpr int HB = PAIR ? 1 : HALVES;  // B halves held by this CTA
+  constexpr int STAGE = A_BYTES + HB * BH_BYTES;
   constexpr int NST = TC_RING / STAGE;
+  static_assert(!PAIR || (BN == 256 && KC == 1), "paired tiles are 256 x 256 with one-chunk stages");
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ep_all = smem + TC_RING;
@@ -119,8 +150,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = p.K / BK;
-  const int total = m_tiles * n_tiles;
-  const int my_tiles = blockIdx.x < total ? (total - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const int my_tiles = gemm_tile_count<PAIR>(m_tiles, n_tiles);
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0;
+  const bool leader = crank == 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
@@ -129,20 +161,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);  // one arrival per epilogue warp
+      mbar_init(&tempty[a], PAIR ? 8 : 4);  // one arrival per epilogue warp (of both CTAs)
     }
     for (int e = 0; e < 8; ++e) mbar_init(&ebar[e], 1);
     *bail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 5) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(2 * BN)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if (PAIR) {  // one warp of each CTA of the pair allocates collectively
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                   "r"(2 * BN)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                   "r"(2 * BN)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR) cluster_sync_all();  // the leader's barriers exist before the peer signals them
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -151,8 +191,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
       int it = 0;  // running k-block index across tiles
       bool ok = true;
       for (int i = 0; ok && i < my_tiles; ++i) {
-        const int t = blockIdx.x + i * gridDim.x;
-        const int m0 = (t % m_tiles) * TC_BM, tn = t / m_tiles;
+        int mt_, tn;
+        gemm_tile<PAIR>(i, m_tiles, crank, mt_, tn);
+        const int m0 = mt_ * TC_BM;
         int map0, row0, map1 = 0, row1 = 0;
         b_half<MODE, BN>(p, tn, 0, map0, row0);
         if (HALVES == 2 && !b_half<MODE, BN>(p, tn, 1, map1, row1)) { map1 = map0; row1 = row0; }
@@ -167,6 +208,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
           }
           if (*reinterpret_cast<volatile int*>(bail)) { ok = false; break; }
           uint8_t* st = smem + s * STAGE;
+          if (PAIR) {
+            // this CTA's A rows and B half r; both signal the leader's full barrier
+            const uint32_t fb = smem_map_rank(&full[s], 0);
+            if (leader) mbar_expect_tx(&full[s], 2 * STAGE);
+            tma_load_3d_pair(st, &maps.a, 0, m0, kb * KC, fb);
+            if (crank == 0) tma_load_3d_pair(st + A_BYTES, &maps.b[map0], 0, row0, kb * KC, fb);
+            else tma_load_3d_pair(st + A_BYTES, &maps.b[map1], 0, row1, kb * KC, fb);
+            continue;
+          }
           mbar_expect_tx(&full[s], STAGE);
           tma_load_3d(st, &maps.a, 0, m0, kb * KC, &full[s]);
           tma_load_3d(st + A_BYTES, &maps.b[map0], 0, row0, kb * KC, &full[s]);
@@ -182,16 +232,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
           }
         }
       }
-      // Make sure no copy into this CTA's shared memory is still in flight.
-      for (int k = it - NST < 0 ? 0 : it - NST; k < it; ++k) mbar_wait(&full[k % NST], (k / NST) & 1);
+      // Make sure no copy into this CTA's shared memory is still in flight (the
+      // leader's full barriers also count the peer's copies; the peer's last
+      // copies have landed once the leader's MMAs consumed them, before the
+      // final cluster barrier).
+      if (leader)
+        for (int k = it - NST < 0 ? 0 : it - NST; k < it; ++k) mbar_wait(&full[k % NST], (k / NST) & 1);
     }
   } else if (warp == 5) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       // KC = 1: the two B halves are contiguous, one N = BN MMA per k step.
       // KC = 2: each half is its own [chunk][row] box, one N = 128 MMA per half.
+      // PAIR: one M = 256 paired MMA per k step.
       constexpr int MMA_N = KC == 1 ? BN : 128;
       constexpr int MMAS = KC == 1 ? 1 : HALVES;
-      constexpr uint32_t idesc = umma_idesc(TC_BM, MMA_N, C::umma_fmt);
+      constexpr uint32_t idesc = umma_idesc(PAIR ? 2 * TC_BM : TC_BM, MMA_N, C::umma_fmt);
       int it = 0;
       bool ok = true;
       for (int i = 0; ok && i < my_tiles; ++i) {
@@ -221,11 +276,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
             for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
               for (int hh = 0; hh < MMAS; ++hh)
-                umma_f16(d + hh * 128, umma_desc(a_base + c * TC_CHUNK + kk * 32),
-                         umma_desc(b_base + hh * BH_BYTES + c * TC_CHUNK + kk * 32), idesc, (kb | c | kk) != 0);
-          umma_commit(&empty[s]);
+                if (PAIR)
+                  umma_f16_pair(d, umma_desc(a_base + kk * 32), umma_desc(b_base + kk * 32), idesc, (kb | kk) != 0);
+                else
+                  umma_f16(d + hh * 128, umma_desc(a_base + c * TC_CHUNK + kk * 32),
+                           umma_desc(b_base + hh * BH_BYTES + c * TC_CHUNK + kk * 32), idesc, (kb | c | kk) != 0);
+          if (PAIR) umma_commit_pair(&empty[s], 3);
+          else umma_commit(&empty[s]);
         }
-        umma_commit(&tfull[acc]);  // also after a bail, so that the MMAs in flight finish first
+        // also after a bail, so that the MMAs in flight finish first
+        if (PAIR) umma_commit_pair(&tfull[acc], 3);
+        else umma_commit(&tfull[acc]);
       }
     }
   } else {
@@ -245,8 +306,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
     const int cp = 2 * (lane & 15), rsub = lane >> 4;  // 16-bit outputs: column pair, row parity
     for (int i = 0; i < my_tiles; ++i) {
       const int acc = i & 1;
-      const int t = blockIdx.x + i * gridDim.x;
-      const int mrow0 = (t % m_tiles) * TC_BM + warp * 32, tile_n = t / m_tiles;
+      int mt_, tile_n;
+      gemm_tile<PAIR>(i, m_tiles, crank, mt_, tile_n);
+      const int mrow0 = mt_ * TC_BM + warp * 32;
       // Row metadata of this lane's row (QKV), fetched before the accumulator is
       // awaited: position and the element offset of its slot in the paged cache
       // (page base + slot * hd; the kv / head term is added per column).
@@ -388,10 +450,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
           __syncwarp();
         }
       }
-      // hand the accumulator buffer back to the MMA warp
+      // hand the accumulator buffer back to the (leader's) MMA warp
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&tempty[acc])) : "memory");
+      if (lane == 0) {
+        if (PAIR) mbar_arrive_cluster(smem_map_rank(&tempty[acc], 0));
+        else asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&tempty[acc])) : "memory");
+      }
     }
     // Nothing may be in flight into or out of shared memory at exit: outstanding
     // block loads (only after an error) and the last block stores.
@@ -403,10 +468,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
     (void)ep_ok;
   }
   tc_fence_before();
-  __syncthreads();
+  // PAIR: neither CTA releases its TMEM or leaves while the leader's MMAs or the
+  // peer's copies may still touch it.
+  if (PAIR) cluster_sync_all();
+  else __syncthreads();
   if (warp == 5) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * BN) : "memory");
+    if (PAIR)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * BN) : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * BN) : "memory");
   }
 }
 
@@ -503,11 +574,14 @@ bool make_kv_tma_map(void* map_out, const void* base, uint64_t num_pages, int n_
 template <typename WT>
 static cudaError_t gemm_tc_configure_t() {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 256, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 128, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_GATEUP, 256, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 256, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  return cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 128, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 256, 1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 256, 1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 128, 2, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_GATEUP, 256, 1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_GATEUP, 256, 1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 256, 1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 256, 1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  return cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 128, 2, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
 }
 
 cudaError_t gemm_tc_configure() {
@@ -515,7 +589,9 @@ cudaError_t gemm_tc_configure() {
   return e != cudaSuccess ? e : gemm_tc_configure_t<f16>();
 }
 
-// Tile width BN with its box depth: 256-wide tiles take 1-chunk boxes, 128-wide 2-chunk boxes.
+// Tile width BN with its box depth: 256-wide tiles take 1-chunk boxes, 128-wide
+// 2-chunk boxes.  256-wide tiles with an even number of m tiles run as paired
+// 256 x 256 tiles on clusters of two CTAs, as many clusters as can be resident.
 template <typename WT, int MODE, int BN>
 static cudaError_t gemm_tc_go(const TmaOperand* a, const TmaOperand* const* b, const void* const* e,
                               const GemmParams& p, int mt, int nt, int num_sms, int* err, cudaStream_t s) {
@@ -525,9 +601,35 @@ static cudaError_t gemm_tc_go(const TmaOperand* a, const TmaOperand* const* b, c
   for (int i = 0; i < 3; ++i) memcpy(&maps.b[i], &(b[i] ? b[i] : b[0])->box[KC - 1], sizeof(CUtensorMap));
   memcpy(&maps.e_in, e[0] ? e[0] : &maps.a, sizeof(CUtensorMap));
   memcpy(&maps.e_out, e[1] ? e[1] : &maps.a, sizeof(CUtensorMap));
+  if constexpr (BN == 256) {
+    if (mt % 2 == 0) {
+      auto kern = gemm_tc_kernel<WT, MODE, BN, KC, 1>;
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.blockDim = dim3(TC_THREADS);
+      cfg.dynamicSmemBytes = TC_SMEM;
+      cfg.stream = s;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      static int resident = 0;  // clusters of this kernel that fit on the GPU at once
+      if (resident == 0) {
+        cfg.gridDim = dim3(2 * (num_sms / 2));
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = num_sms / 2;
+        resident = n;
+      }
+      const int units = (mt / 2) * nt;
+      cfg.gridDim = dim3(2 * (units < resident ? units : resident));
+      return cudaLaunchKernelEx(&cfg, kern, maps, p, mt, nt, err);
+    }
+  }
   const int total = mt * nt;
   const int grid = total < num_sms ? total : num_sms;
-  gemm_tc_kernel<WT, MODE, BN, KC><<<grid, TC_THREADS, TC_SMEM, s>>>(maps, p, mt, nt, err);
+  gemm_tc_kernel<WT, MODE, BN, KC, 0><<<grid, TC_THREADS, TC_SMEM, s>>>(maps, p, mt, nt, err);
   return cudaGetLastError();
 }
 

@@ -133,6 +133,23 @@ def test_kv_cache_layout_is_bit_exact(tiny):
     assert not (bits[written] == BF16_NAN).any()
 
 
+def test_paired_gemm_tiles_in_prefill():
+    """4096 packed prompt rows make every prefill projection use 256 x 256 tiles
+    computed by CTA pairs (the paired tcgen05 MMA): QKV with RoPE and the K/V
+    scatter, gate/up with SwiGLU, and both residual GEMMs."""
+    dims = small_dims(d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=2048, vocab=2048,
+                      n_layers=2, n_standard_layers=0)
+    gw, ow = gpu_weights(dims), oracle_weights(dims)
+    lens = [2048, 2048]
+    prompts = prompts_for(lens, dims["vocab"])
+    feed = np.stack([synth.tokens(1, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(2)])
+    model = make_model(dims, gw, max_batch=2, max_seq=2112, page_size=64)
+    g_logits, _ = run_teacher_forced(model, prompts, feed)
+    o_logits, _ = O.teacher_forced_decode(dims, ow, prompts, feed)
+    for s_ in range(2):
+        compare_logits(g_logits[s_], o_logits[s_], f"paired tiles step {s_}")
+
+
 @pytest.mark.parametrize("B", [16, 21])
 def test_batched_decode_on_tensor_cores(B):
     """Decode batches above 4 rows run on the mma.sync projection in chunks of 16
