@@ -419,35 +419,52 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
           tmem_ld32(trow + c * 32, v);
           const int col = row + (c & 3) * 32 + cp;  // column inside its matrix (even: a RoPE pair)
           const int head = col / hd, dim = col % hd;
-          // rotation of each of this lane's 16 rows, all table loads in flight at once
+          // Rotation of each of this lane's 16 rows, all table loads in flight at
+          // once (rows past M have position 0: in-bounds loads, no store).  The
+          // code below is branch-free per row so that the rows interleave.
           float cs[16], sn[16];
+          if (map < 2) {
+#pragma unroll
+            for (int r2 = 0; r2 < 16; ++r2) {
+              const int pos = __shfl_sync(0xffffffffu, my_pos, 2 * r2 + rsub);
+              const size_t tj = (size_t)pos * (hd >> 1) + (dim >> 1);
+              cs[r2] = __ldg(p.rope_cos + tj);
+              sn[r2] = __ldg(p.rope_sin + tj);
+            }
+          } else {
+#pragma unroll
+            for (int r2 = 0; r2 < 16; ++r2) {
+              cs[r2] = 1.f;
+              sn[r2] = 0.f;
+            }
+          }
+          long long off[16];
+#pragma unroll
+          for (int r2 = 0; r2 < 16; ++r2) {
+            const int m = mrow0 + 2 * r2 + rsub;
+            const long long slot = __shfl_sync(0xffffffffu, my_slot, 2 * r2 + rsub);
+            off[r2] = map == 0 ? (long long)m * p.ldo : slot;
+          }
+          stage(v);
+          float a[32];
 #pragma unroll
           for (int r2 = 0; r2 < 16; ++r2) {
             const int r = 2 * r2 + rsub;
-            const int pos = __shfl_sync(0xffffffffu, my_pos, r);
-            cs[r2] = 1.f;
-            sn[r2] = 0.f;
-            if (map < 2 && mrow0 + r < p.M) {
-              const size_t tj = (size_t)pos * (hd >> 1) + (dim >> 1);
-              cs[r2] = p.rope_cos[tj];
-              sn[r2] = p.rope_sin[tj];
-            }
-          }
-          stage(v);
-          const long long kvoff = (long long)((map - 1) * p.kv.n_kv + head) * p.kv.page_size * hd + dim;
-#pragma unroll
-          for (int r2 = 0; r2 < 16; ++r2) {
-            const int r = 2 * r2 + rsub, m = mrow0 + r;
-            const long long slot = __shfl_sync(0xffffffffu, my_slot, r);
-            const float a0 = ep[r * TC_EP_LD + cp], a1 = ep[r * TC_EP_LD + cp + 1];
-            const float r0 = a0 * cs[r2] - a1 * sn[r2], r1 = a0 * sn[r2] + a1 * cs[r2];
-            if (m >= p.M) continue;
-            // q, K and V are stored in the weight dtype (the attention operands)
-            WT* dst = map == 0 ? static_cast<WT*>(p.out_h) + (size_t)m * p.ldo + col
-                               : static_cast<WT*>(p.kv.base) + slot + kvoff;
-            *reinterpret_cast<uint32_t*>(dst) = C::pack(r0, r1);
+            a[2 * r2] = ep[r * TC_EP_LD + cp];
+            a[2 * r2 + 1] = ep[r * TC_EP_LD + cp + 1];
           }
           __syncwarp();
+          // q, K and V are stored in the weight dtype (the attention operands)
+          WT* base = map == 0 ? static_cast<WT*>(p.out_h) + col
+                              : static_cast<WT*>(p.kv.base) +
+                                    ((long long)((map - 1) * p.kv.n_kv + head) * p.kv.page_size * hd + dim);
+#pragma unroll
+          for (int r2 = 0; r2 < 16; ++r2) {
+            const float r0 = a[2 * r2] * cs[r2] - a[2 * r2 + 1] * sn[r2];
+            const float r1 = a[2 * r2] * sn[r2] + a[2 * r2 + 1] * cs[r2];
+            const uint32_t pk = C::pack(r0, r1);
+            if (mrow0 + 2 * r2 + rsub < p.M) *reinterpret_cast<uint32_t*>(base + off[r2]) = pk;
+          }
         }
       }
       // hand the accumulator buffer back to the (leader's) MMA warp

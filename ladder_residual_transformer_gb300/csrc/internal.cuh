@@ -66,7 +66,11 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+// silu(z) = z / (1 + e^-z) with the fast exponential and divide: straight-line
+// code (no slow-path branch), so that the independent evaluations of an
+// epilogue interleave.  For z below about -88, e^-z overflows and the result is
+// the correct limit 0.
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // Programmatic dependent launch.  pdl_trigger lets the next kernel of the stream
 // start launching its CTAs; pdl_wait blocks until the previous kernel of the

@@ -190,7 +190,7 @@ struct ladder_model {
   int launches = 0;
   std::vector<GraphEntry> graphs;
   std::vector<int32_t> meta_host;
-  // Second stream of the decode schedule (the MLP chain of ladder layers) and the
+  // Second stream of the decode schedule (the MLP chain of ladder layers; high priority) and the
   // events that order the two chains: one per stream buffer, recorded after the
   // kernel that writes it, plus one to fork the second stream from the caller's.
   cudaStream_t aux = nullptr;
@@ -377,7 +377,11 @@ int ladder_create(const ladder_config* cfg, const ladder_weights* w, void* works
   if (e == cudaSuccess) e = gemm_tc_configure();
   if (e == cudaSuccess) e = attn_prefill_tcgen05_configure();
   if (e == cudaSuccess) e = attn_decode_tc_configure();
-  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&m->aux, cudaStreamNonBlocking);
+  // The second stream carries the longer chain (the MLP modules of ladder layers, or
+  // the shard reduces), so its blocks are scheduled ahead of the caller's stream.
+  int prio_least = 0, prio_greatest = 0;
+  if (e == cudaSuccess) e = cudaDeviceGetStreamPriorityRange(&prio_least, &prio_greatest);
+  if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&m->aux, cudaStreamNonBlocking, prio_greatest);
   for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&m->ev_slot[i], cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_fork, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_part, cudaEventDisableTiming);
