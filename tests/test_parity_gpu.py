@@ -150,6 +150,23 @@ def test_paired_gemm_tiles_in_prefill():
         compare_logits(g_logits[s_], o_logits[s_], f"paired tiles step {s_}")
 
 
+def test_narrow_gemm_tiles_with_ragged_rows():
+    """450 packed rows (4 m tiles, the last one ragged) with narrow projections
+    (N = 768 and 512): QKV and both residual GEMMs take 128-wide tiles with
+    two-chunk boxes, the gate/up GEMM 256 x 256 tiles on CTA pairs."""
+    dims = small_dims(d_model=512, n_q_heads=8, n_kv_heads=2, head_dim=64, ffn_dim=1024, vocab=2048,
+                      n_layers=2, n_standard_layers=0)
+    gw, ow = gpu_weights(dims), oracle_weights(dims)
+    lens = [300, 150]
+    prompts = prompts_for(lens, dims["vocab"])
+    feed = np.stack([synth.tokens(1, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(2)])
+    model = make_model(dims, gw, max_batch=2, max_seq=320, page_size=64)
+    g_logits, _ = run_teacher_forced(model, prompts, feed)
+    o_logits, _ = O.teacher_forced_decode(dims, ow, prompts, feed)
+    for s_ in range(2):
+        compare_logits(g_logits[s_], o_logits[s_], f"paired narrow tiles step {s_}")
+
+
 @pytest.mark.parametrize("B", [16, 21])
 def test_batched_decode_on_tensor_cores(B):
     """Decode batches above 4 rows run on the mma.sync projection in chunks of 16
