@@ -43,6 +43,13 @@ Readings where the pages are silent (each one is a switch or a documented choice
   R5  GQA: query head h reads KV head h // (n_q_heads / n_kv_heads) (repeat_kv).
   R6  Prefill returns the logits of each sequence's last position; greedy
       decoding takes argmax with the lowest index on ties.
+  R7  The parallel-block model that [notes] compares against (the Parallel-70B
+      row of the 70B latency breakdown table, section 实验关键数据) is not spelt
+      out there; it is read as the usual parallel attention + MLP layer: both
+      modules of layer l read the layer input x_{2l}, each through its own
+      RMSNorm gain, and the stream still accumulates every module output
+      (x_{2l+1} = x_{2l} + A, x_{2l+2} = x_{2l+1} + M).  ``parallel=True``
+      applies it to every layer.
 
 Pins that tie this code to something other than itself live in
 tests/test_oracle_pins.py.
@@ -253,14 +260,18 @@ def mlp_module(lw: LayerWeights, u: np.ndarray) -> np.ndarray:
 # ---------------------------------------------------------------------------
 # The ladder schedule ([notes] 研究背景与动机, 方法详解, 关键设计; R1, R2)
 # ---------------------------------------------------------------------------
-def module_input_index(k: int, n_standard_layers: int, strict_boundary: bool = False) -> int:
+def module_input_index(k: int, n_standard_layers: int, strict_boundary: bool = False,
+                       parallel: bool = False) -> int:
     """Index j of the stream state x_j that module k (1-based) reads.
 
     Module k is the attention (k odd) or MLP (k even) of layer (k-1)//2.  In a
     standard layer it reads x_{k-1}; in a ladder layer it reads x_{k-2} (the
     staggered residual of [notes]), with x_{-1} := x_0 (R1) and the hybrid
-    boundary rule R2.
+    boundary rule R2.  With ``parallel`` every layer is a parallel block (R7):
+    both modules of layer l read x_{2l}.
     """
+    if parallel:
+        return k - 1 if k % 2 == 1 else k - 2
     layer = (k - 1) // 2
     if layer < n_standard_layers:
         return k - 1
@@ -271,7 +282,7 @@ def module_input_index(k: int, n_standard_layers: int, strict_boundary: bool = F
 
 def forward(dims: dict, W: OracleWeights, blocks: list[np.ndarray], caches: list[SeqCache],
             all_positions: bool = False, strict_boundary: bool = False,
-            return_stream: bool = False):
+            return_stream: bool = False, parallel: bool = False):
     """Run one block of new tokens per sequence through the model.
 
     blocks[b] holds the token ids that sequence b appends, at positions
@@ -291,7 +302,7 @@ def forward(dims: dict, W: OracleWeights, blocks: list[np.ndarray], caches: list
     for k in range(1, 2 * L + 1):
         layer = (k - 1) // 2
         lw = W.layer(layer)
-        j = module_input_index(k, nstd, strict_boundary)
+        j = module_input_index(k, nstd, strict_boundary, parallel)
         for b in range(len(blocks)):
             if len(blocks[b]) == 0:
                 hist[b].append(hist[b][-1])

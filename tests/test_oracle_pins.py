@@ -239,6 +239,64 @@ def test_cached_decode_equals_independent_unrolled_ladder():
 
 
 # ---------------------------------------------------------------------------
+# Parallel-block model (the comparison model of the pages' 70B table, read as
+# the usual parallel attention + MLP layer).
+# ---------------------------------------------------------------------------
+def ref_parallel_forward(dims, W, tokens):
+    """Textbook parallel layer: x <- x + Attn(n_a(x)) + MLP(n_m(x))."""
+    x = t(W.glob("embed"))[torch.as_tensor(tokens, dtype=torch.long)]
+    for l in range(dims["n_layers"]):
+        lw = W.layer(l)
+        x = x + ref_attention_module(dims, lw, x, len(tokens)) + ref_mlp_module(dims, lw, x)
+    return F.linear(ref_norm(x, t(W.glob("final_norm")), dims["norm_eps"]), t(W.glob("lm_head")))
+
+
+def test_parallel_block_matches_textbook_and_unrolled():
+    dims = small_dims(n_layers=3, n_standard_layers=0)
+    W = random_weights(dims, 11)
+    toks = np.array([3, 14, 15, 92, 65, 35, 89])
+    got = O.forward(dims, W, [toks], [O.SeqCache()], all_positions=True, parallel=True)[0]
+    close(got, ref_parallel_forward(dims, W, toks).numpy())
+    close(got, _unrolled(dims, W, toks, {1: 0, 2: 0, 3: 2, 4: 2, 5: 4, 6: 4}).numpy())
+    # it is neither the standard nor the ladder model
+    lad = O.forward(dims, W, [toks], [O.SeqCache()], all_positions=True)[0]
+    std = O.forward(dict(dims, n_standard_layers=3), W, [toks], [O.SeqCache()], all_positions=True)[0]
+    assert np.abs(got - lad).max() > 1e-3 and np.abs(got - std).max() > 1e-3
+
+
+def test_parallel_block_special_cases():
+    dims = dict(TINY)
+    toks = synth.tokens(16, dims["vocab"])
+    # one layer: the ladder layer above x_{-1} := x_0 is a parallel block, bitwise
+    one = dict(dims, n_layers=1)
+    W1 = O.synthetic_weights(one)
+    a = O.forward(one, W1, [toks], [O.SeqCache()], all_positions=True, parallel=True)[0]
+    b = O.forward(one, W1, [toks], [O.SeqCache()], all_positions=True)[0]
+    assert np.array_equal(a, b)
+    # a zero attention output or a zero MLP output makes the parallel block standard, bitwise
+    for kind in ("wo", "w_down"):
+        zero = lambda name, layer, arr, kind=kind: np.zeros_like(arr) if name == kind else arr
+        W = O.synthetic_weights(dims, transform=zero)
+        par = O.forward(dims, W, [toks], [O.SeqCache()], all_positions=True, parallel=True)[0]
+        std = O.forward(dict(dims, n_standard_layers=dims["n_layers"]), W, [toks], [O.SeqCache()],
+                        all_positions=True)[0]
+        assert np.array_equal(par, std), kind
+
+
+def test_parallel_cached_decode_equals_prefill_rerun():
+    dims = small_dims(n_layers=2, n_standard_layers=0)
+    W = random_weights(dims, 12)
+    toks = np.array([4, 8, 15, 16, 23, 42, 11, 19])
+    P = 4
+    logits, caches = O.prefill(dims, W, [toks[:P]], parallel=True)
+    rerun = O.forward(dims, W, [toks], [O.SeqCache()], all_positions=True, parallel=True)[0]
+    close(logits[0], rerun[P - 1], 1e-12)
+    for p in range(P, len(toks)):
+        step = O.decode_step(dims, W, toks[p:p + 1], caches, parallel=True)
+        close(step[0], rerun[p], 1e-12)
+
+
+# ---------------------------------------------------------------------------
 # Causality and batch independence
 # ---------------------------------------------------------------------------
 def test_causality_and_batch_independence():
@@ -347,6 +405,8 @@ def test_module_input_index_table():
     # hybrid with 2 standard layers (b = 4)
     assert [O.module_input_index(k, 2) for k in range(1, 9)] == [0, 1, 2, 3, 4, 4, 5, 6]
     assert [O.module_input_index(k, 2, True) for k in range(1, 9)] == [0, 1, 2, 3, 3, 4, 5, 6]
+    # parallel blocks: both modules of layer l read x_{2l}
+    assert [O.module_input_index(k, 0, parallel=True) for k in range(1, 7)] == [0, 0, 2, 2, 4, 4]
 
 
 def test_kv_slot_and_pool_offset():
