@@ -322,23 +322,38 @@ def run_ours(args, dims):
         n_probe, probe_ms = model.probe_end()
         stream.synchronize()
 
-    # Shard mode: the same decode with the standard residual schedule, where each
-    # module waits for the previous module's reduce (the pages' comparison).
-    shard = None
-    if shard_k > 1:
-        std_ms = []
+    # The same weights and kernels under the other residual schedules (the pages'
+    # comparison: standard, where every module waits for the previous one, and
+    # the parallel-block model), each timed like the configured schedule above.
+    def time_schedule(**mode):
+        d_ms, p_ms = [], []
         with torch.cuda.stream(stream):
-            model.set_mode(standard=True, graph=not args.eager, pdl=not args.no_pdl)
+            model.set_mode(graph=not args.eager, pdl=not args.no_pdl, **mode)
             for i in range(args.warmup + args.steps):
                 step(record=True)
                 stream.synchronize()
                 if i >= args.warmup:
-                    std_ms.append(ev[1].elapsed_time(ev[2]))
-            model.set_mode(standard=False, graph=not args.eager, pdl=not args.no_pdl)
-        std_tps = B * args.decode * len(std_ms) / (sum(std_ms) / 1e3)
-        shard = {"k": shard_k, "ladder_decode_tok_s": B * args.decode * args.steps / (sum(dec_ms) / 1e3),
-                 "standard_decode_tok_s": std_tps,
-                 "note": "same weights and kernels; standard = every module waits for the previous module's reduce"}
+                    p_ms.append(ev[0].elapsed_time(ev[1]))
+                    d_ms.append(ev[1].elapsed_time(ev[2]))
+            model.set_mode(graph=not args.eager, pdl=not args.no_pdl)
+        return {"decode_tok_s": B * args.decode * len(d_ms) / (sum(d_ms) / 1e3),
+                "prefill_ms": sum(p_ms) / len(p_ms)}
+
+    schedules = None
+    shard = None
+    if not args.no_schedules:
+        schedules = {"configured": {"decode_tok_s": B * args.decode * args.steps / (sum(dec_ms) / 1e3),
+                                    "prefill_ms": sum(pre_ms) / len(pre_ms)},
+                     "standard": time_schedule(standard=True),
+                     "parallel": time_schedule(parallel=True),
+                     "note": "same weights and kernels; configured = the workload's ladder/hybrid schedule; "
+                             "standard = every layer standard; parallel = every layer a parallel "
+                             "attention + MLP block"}
+        if shard_k > 1:
+            shard = {"k": shard_k, "ladder_decode_tok_s": schedules["configured"]["decode_tok_s"],
+                     "standard_decode_tok_s": schedules["standard"]["decode_tok_s"],
+                     "note": "same weights and kernels; standard = every module waits for the previous "
+                             "module's reduce"}
 
     tot_pre, tot_dec = sum(pre_ms), sum(dec_ms)
     tot_pre, tot_dec = max_over_ranks([tot_pre, tot_dec], world, dev)
@@ -409,6 +424,7 @@ def run_ours(args, dims):
                                "step's decode right after the timed region"},
         "peaks": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'fallback 6.8 TB/s, 1.9 PF bf16'})",
         "gpu_launches": launches, "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "shard": shard,
+        "schedules": schedules,
         "wall_s": wall,
     }
     if rank == 0:
@@ -431,6 +447,8 @@ def main():
     ap.add_argument("--no-pdl", action="store_true", help="decode without programmatic dependent launch")
     ap.add_argument("--eager", action="store_true", help="decode without CUDA-graph replay")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-schedules", action="store_true",
+                    help="skip timing the standard and parallel-block schedules on the same weights")
     ap.add_argument("--cpu-prompt", type=int, default=None, help="oracle sample prompt (default: the workload's)")
     ap.add_argument("--cpu-decode", type=int, default=None, help="oracle sample decode steps (default: the workload's)")
     ap.add_argument("--ref-prompt", type=int, default=64)

@@ -70,7 +70,13 @@ enum {
 /* Residual schedule selected by ladder_set_mode. */
 enum {
   LADDER_RESIDUAL_CONFIG = 0,   /* as configured: standard below n_standard_layers, ladder above */
-  LADDER_RESIDUAL_STANDARD = 1  /* every layer standard (the baseline model, same weights) */
+  LADDER_RESIDUAL_STANDARD = 1, /* every layer standard (the baseline model, same weights) */
+  LADDER_RESIDUAL_PARALLEL = 2  /* every layer a parallel block: the attention and the MLP of layer l
+                                   both read x_{2l}, each through its own RMSNorm gain, and the stream
+                                   accumulates both outputs (x_{2l+1} = x_{2l} + A, x_{2l+2} =
+                                   x_{2l+1} + M).  This is the plain reading of the Parallel-70B
+                                   comparison model in the notes' 70B latency table (section
+                                   实验关键数据), which the pages do not spell out. */
 };
 
 /* Flags for ladder_set_mode. */

@@ -222,6 +222,7 @@ struct ladder_model {
 
   // Index j of the stream state x_j that module k (1-based) reads.
   int input_index(int k) const {
+    if (residual_mode == LADDER_RESIDUAL_PARALLEL) return (k & 1) ? k - 1 : k - 2;
     const int layer = (k - 1) / 2;
     const int nstd = residual_mode == LADDER_RESIDUAL_STANDARD ? cfg.n_layers : cfg.n_standard_layers;
     if (layer < nstd) return k - 1;
@@ -413,7 +414,8 @@ void ladder_destroy(ladder_model* m) {
 
 int ladder_set_mode(ladder_model* m, int residual_mode, int flags) {
   if (!m) return fail(LADDER_ERR_INVALID, "model is NULL");
-  if (residual_mode != LADDER_RESIDUAL_CONFIG && residual_mode != LADDER_RESIDUAL_STANDARD)
+  if (residual_mode != LADDER_RESIDUAL_CONFIG && residual_mode != LADDER_RESIDUAL_STANDARD &&
+      residual_mode != LADDER_RESIDUAL_PARALLEL)
     return fail(LADDER_ERR_INVALID, "unknown residual mode %d", residual_mode);
   if (flags & ~(LADDER_FLAG_DECODE_GRAPH | LADDER_FLAG_NO_PDL)) return fail(LADDER_ERR_INVALID, "unknown flags 0x%x", flags);
   if (residual_mode != m->residual_mode || flags != m->flags) m->drop_graphs();
@@ -684,7 +686,11 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
   float* q = m->at<float>(P.q);
   float* ao = m->at<float>(P.ao);
   float* act = m->at<float>(P.act);
-  const int nstd = m->residual_mode == LADDER_RESIDUAL_STANDARD ? c.n_layers : c.n_standard_layers;
+  // layers below nstd run both modules on the caller's stream; above it the MLP
+  // module (which does not read the attention module's output) runs on the second
+  const int nstd = m->residual_mode == LADDER_RESIDUAL_STANDARD ? c.n_layers
+                   : m->residual_mode == LADDER_RESIDUAL_PARALLEL ? 0
+                                                                  : c.n_standard_layers;
   const bool pdl = !(m->flags & LADDER_FLAG_NO_PDL);
   cudaStream_t streams[2] = {s, m->aux};
   int writer[3] = {0, 0, 0};  // stream index that last wrote each buffer

@@ -27,6 +27,7 @@ LADDER_ERR_UNSUPPORTED = -4
 
 RESIDUAL_CONFIG = 0
 RESIDUAL_STANDARD = 1
+RESIDUAL_PARALLEL = 2
 FLAG_DECODE_GRAPH = 1
 FLAG_NO_PDL = 2
 
@@ -275,10 +276,17 @@ class LadderModel:
         return lib().ladder_kv_seq_len(self._kv, b)
 
     # -- modes -----------------------------------------------------------
-    def set_mode(self, standard: bool = False, graph: bool = False, pdl: bool = True):
+    def set_mode(self, standard: bool = False, graph: bool = False, pdl: bool = True, parallel: bool = False):
+        """Residual schedule: as configured (default), every layer standard
+        (``standard``), or every layer a parallel attention + MLP block
+        (``parallel``); decode launch flags."""
+        if standard and parallel:
+            raise ValueError("standard and parallel are exclusive")
         flags = (FLAG_DECODE_GRAPH if graph else 0) | (0 if pdl else FLAG_NO_PDL)
-        check(lib().ladder_set_mode(self._m, RESIDUAL_STANDARD if standard else RESIDUAL_CONFIG, flags))
+        mode = RESIDUAL_STANDARD if standard else RESIDUAL_PARALLEL if parallel else RESIDUAL_CONFIG
+        check(lib().ladder_set_mode(self._m, mode, flags))
         self._standard = standard
+        self._parallel = parallel
 
     # -- forward ---------------------------------------------------------
     def prefill(self, tokens: torch.Tensor, lens, logits: torch.Tensor | None = None,

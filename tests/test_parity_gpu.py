@@ -25,11 +25,12 @@ def tiny():
     return dims, gpu_weights(dims), oracle_weights(dims)
 
 
-def run_teacher_forced(model, prompts, feed, graph=False, standard=None):
+def run_teacher_forced(model, prompts, feed, graph=False, standard=None, parallel=None):
     """Prefill then decode feeding feed[:, s]; returns logits [S+1, B, V] and greedy tokens."""
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
-        model.set_mode(graph=graph, standard=getattr(model, "_standard", False) if standard is None else standard)
+        model.set_mode(graph=graph, standard=getattr(model, "_standard", False) if standard is None else standard,
+                       parallel=getattr(model, "_parallel", False) if parallel is None else parallel)
         logits, nxt = model.prefill(packed(prompts), [len(p) for p in prompts])
         out, toks = [logits.cpu().numpy()], [nxt.cpu().numpy()]
         tok_dev = torch.empty(len(prompts), dtype=torch.int32, device="cuda")
@@ -234,6 +235,58 @@ def test_standard_mode_switch_matches_standard_oracle(tiny):
         compare_logits(got[i], o_logits[i], f"standard step {i}")
     lad = O.teacher_forced_decode(dims, oracle_weights(dims), prompts, feed)[0]
     assert np.abs(lad - o_logits).max() > 1e-3  # the two schedules really differ
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_parallel_mode_matches_parallel_oracle(graph):
+    """Every layer a parallel block (both modules read the layer input), on a
+    hybrid-configured model: the mode overrides the configured schedule.  Two
+    ragged sequences, prefill and four decode steps, eager and graph replay."""
+    dims = small_dims(n_layers=3, n_standard_layers=1)
+    gw, ow = gpu_weights(dims), oracle_weights(dims)
+    prompts = prompts_for([37, 12], dims["vocab"])
+    feed = np.stack([synth.tokens(4, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(2)])
+    model = make_model(dims, gw, max_batch=2, max_seq=64, page_size=16)
+    g_logits, g_toks = run_teacher_forced(model, prompts, feed, graph=graph, parallel=True)
+    o_logits, _ = O.teacher_forced_decode(dims, ow, prompts, feed, parallel=True)
+    errs = [compare_logits(g_logits[s_], o_logits[s_], f"parallel step {s_}")[0] for s_ in range(5)]
+    for s_ in range(5):
+        check_greedy(g_toks[s_], o_logits[s_], 2 * max(errs))
+    lad = O.teacher_forced_decode(dims, ow, prompts, feed)[0]
+    assert np.abs(lad - o_logits).max() > 1e-3  # the schedules really differ
+
+
+def test_zero_wo_makes_parallel_equal_standard_bitwise():
+    """With W_o = 0 the attention adds nothing, so the MLP's input x_{2l} equals
+    x_{2l+1}: the parallel and standard schedules give the same bits."""
+    dims = small_dims()
+    model = make_model(dims, gpu_weights(dims, transform=_bits), max_batch=1, max_seq=32)
+    prompts = prompts_for([16], dims["vocab"])
+    outs = []
+    for parallel in (False, True):
+        model.reset()
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            model.set_mode(standard=not parallel, parallel=parallel)
+            lg, nt = model.prefill(packed(prompts), [16])
+            l2, _ = model.decode_step(nt)
+        s.synchronize()
+        outs.append((lg.cpu().numpy(), l2.cpu().numpy()))
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+
+
+def test_shard_mode_parallel_schedule():
+    """Shard mode (k = 2 row/column shards, reduce on the second stream) with
+    parallel blocks."""
+    dims = small_dims(d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=3072, vocab=2048)
+    gw, ow = gpu_weights(dims), oracle_weights(dims)
+    prompts = prompts_for([40, 9], dims["vocab"])
+    feed = np.stack([synth.tokens(4, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(2)])
+    model = make_model(dims, gw, max_batch=2, max_seq=64, page_size=32, shard_k=2)
+    g_logits, _ = run_teacher_forced(model, prompts, feed, graph=True, parallel=True)
+    o_logits, _ = O.teacher_forced_decode(dims, ow, prompts, feed, parallel=True)
+    for s_ in range(5):
+        compare_logits(g_logits[s_], o_logits[s_], f"shard parallel step {s_}")
 
 
 def _bits(name, layer, b):
