@@ -43,6 +43,16 @@ Readings where the pages are silent (each one is a switch or a documented choice
   R5  GQA: query head h reads KV head h // (n_q_heads / n_kv_heads) (repeat_kv).
   R6  Prefill returns the logits of each sequence's last position; greedy
       decoding takes argmax with the lowest index on ties.
+  R8  Sampling beyond greedy: [record] names the official benchmark's
+      logits_to_probs / multinomial_sample_one_no_sync / sample helpers (the
+      gpt-fast generation loop).  Read plainly: scale the logits by 1/T (T
+      clamped below at 1e-5), keep the logits at or above the k-th largest
+      (top_k <= 0 or >= V keeps all), normalise to probabilities p, and return
+      argmax_i p_i / q_i with q_i ~ Exp(1) drawn independently per vocabulary
+      entry (the "exponential race", a sample of p).  In the log domain this is
+      argmax_i l_i / T - ln(q_i).  The draws are not the pages': q_i = -ln u_i
+      with u_i from SplitMix64 counters keyed by (seed, batch row, position of
+      the sampled token), as written in ``sample_uniforms``.
   R7  The parallel-block model that [notes] compares against (the Parallel-70B
       row of the 70B latency breakdown table, section 实验关键数据) is not spelt
       out there; it is read as the usual parallel attention + MLP layer: both
@@ -68,7 +78,7 @@ __all__ = [
     "OracleWeights", "synthetic_weights", "SeqCache", "rmsnorm", "rope_tables", "apply_rope",
     "causal_gqa_attention", "attention_module", "mlp_module", "silu", "module_input_index",
     "forward", "prefill", "decode_step", "greedy_generate", "teacher_forced_decode",
-    "argmax_lowest", "kv_slot", "kv_pool_offset",
+    "argmax_lowest", "kv_slot", "kv_pool_offset", "splitmix64_mix", "sample_uniforms", "sample_token",
 ]
 
 
@@ -332,6 +342,63 @@ def forward(dims: dict, W: OracleWeights, blocks: list[np.ndarray], caches: list
 def argmax_lowest(logits: np.ndarray) -> np.ndarray:
     """Greedy token: index of the largest logit, the lowest index on ties (R6)."""
     return np.argmax(logits, axis=-1).astype(np.int32)
+
+
+# ---------------------------------------------------------------------------
+# Sampling (R8)
+# ---------------------------------------------------------------------------
+_M64 = (1 << 64) - 1
+SM64_GAMMA = 0x9E3779B97F4A7C15
+
+
+def splitmix64_mix(z):
+    """The SplitMix64 output function (Steele, Lea and Flood, "Fast splittable
+    pseudorandom number generators", OOPSLA 2014), on Python ints or uint64
+    arrays (arithmetic modulo 2^64)."""
+    if isinstance(z, np.ndarray):
+        with np.errstate(over="ignore"):
+            z = z.astype(np.uint64)
+            z = (z ^ (z >> np.uint64(30))) * np.uint64(0xBF58476D1CE4E5B9)
+            z = (z ^ (z >> np.uint64(27))) * np.uint64(0x94D049BB133111EB)
+            return z ^ (z >> np.uint64(31))
+    z &= _M64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & _M64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & _M64
+    return z ^ (z >> 31)
+
+
+def sample_uniforms(seed: int, row: int, pos: int, n: int) -> np.ndarray:
+    """u_i, i < n, for batch row `row` sampling the token at position `pos`:
+    key = mix(mix(seed + G (row + 1)) + G (pos + 1)), u_i = (top 23 bits of
+    mix(key + G (i + 1)) + 1/2) / 2^23, with G the SplitMix64 increment.  Every
+    u_i lies in (0, 1) and is exact in fp32 and fp64."""
+    k1 = splitmix64_mix((seed + SM64_GAMMA * (row + 1)) & _M64)
+    key = splitmix64_mix((k1 + SM64_GAMMA * (pos + 1)) & _M64)
+    with np.errstate(over="ignore"):
+        ctr = np.uint64(key) + np.uint64(SM64_GAMMA) * np.arange(1, n + 1, dtype=np.uint64)
+    h = splitmix64_mix(ctr)
+    return ((h >> np.uint64(41)).astype(np.float64) + 0.5) / float(1 << 23)
+
+
+def sample_token(logits_row: np.ndarray, temperature: float, top_k: int, seed: int, row: int, pos: int,
+                 return_scores: bool = False):
+    """Next token of one row by temperature / top-k sampling (R8); greedy when
+    temperature <= 0.  Scores l_i / T - ln(-ln u_i) in fp64, -inf outside the
+    top-k set; the lowest index wins ties."""
+    l = np.asarray(logits_row, dtype=np.float64)
+    V = l.shape[0]
+    if temperature <= 0:
+        tok = int(np.argmax(l))
+        return (tok, l) if return_scores else tok
+    T = max(float(temperature), 1e-5)
+    keep = np.ones(V, dtype=bool)
+    if 0 < top_k < V:
+        pivot = np.sort(l)[V - top_k]  # the k-th largest logit
+        keep = l >= pivot
+    u = sample_uniforms(seed, row, pos, V)
+    score = np.where(keep, l / T - np.log(-np.log(u)), -np.inf)
+    tok = int(np.argmax(score))
+    return (tok, score) if return_scores else tok
 
 
 def prefill(dims: dict, W: OracleWeights, prompts: list[np.ndarray], **kw):

@@ -448,3 +448,72 @@ def test_tiny_greedy_matches_golden():
     toks, logits, _ = O.greedy_generate(dims, O.synthetic_weights(dims), [synth.tokens(16, dims["vocab"])], 8)
     assert toks[0].tolist() == g["tokens"]
     assert np.allclose(logits[:, 0, :8], np.array(g["logits_head"]), atol=1e-5)
+
+
+# ---------------------------------------------------------------------------
+# Sampling (temperature / top-k exponential race)
+# ---------------------------------------------------------------------------
+def test_sampling_mix_matches_published_splitmix64():
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "splitmix64.json")))
+    gamma = int(g["gamma"], 16)
+    for i, want in enumerate(g["outputs_from_state_0"]):
+        z = ((i + 1) * gamma) & (2 ** 64 - 1)  # the generator's state after i + 1 steps
+        assert O.splitmix64_mix(z) == int(want, 16)
+        assert int(O.splitmix64_mix(np.array([z], dtype=np.uint64))[0]) == int(want, 16)
+
+
+def test_sampling_uniforms_are_exact_and_uniform():
+    u = O.sample_uniforms(seed=7, row=1, pos=33, n=200000)
+    assert u.min() > 0.0 and u.max() < 1.0
+    assert np.array_equal(u.astype(np.float32).astype(np.float64), u)  # exact in fp32
+    hist = np.histogram(u, bins=20, range=(0, 1))[0]
+    assert np.all(np.abs(hist / len(u) - 0.05) < 0.003)
+    # different rows and positions give different streams
+    assert not np.array_equal(u[:100], O.sample_uniforms(7, 2, 33, 100))
+    assert not np.array_equal(u[:100], O.sample_uniforms(7, 1, 34, 100))
+
+
+def _chi2(counts, probs):
+    n = counts.sum()
+    e = n * probs
+    m = e > 0
+    assert np.all(counts[~m] == 0)
+    return ((counts[m] - e[m]) ** 2 / e[m]).sum(), int(m.sum()) - 1
+
+
+@pytest.mark.parametrize("T,k", [(1.0, 0), (0.7, 4), (1.6, 2)])
+def test_sampling_distribution_is_softmax_of_the_top_k(T, k):
+    """Draws over many positions follow softmax(l / T) restricted to the k
+    largest logits: a chi-square test (threshold far in the tail, p ~ 1e-6),
+    which a sign flip of the noise, l * T for l / T or an off-by-one top-k set
+    all fail."""
+    l = np.array([1.2, -0.3, 0.8, 2.0, 0.0, -1.5, 0.5])
+    V = len(l)
+    N = 30000
+    counts = np.zeros(V)
+    for pos in range(N):
+        counts[O.sample_token(l, T, k, seed=5, row=0, pos=pos)] += 1
+    keep = np.ones(V, bool) if k <= 0 else l >= np.sort(l)[V - k]
+    p = np.where(keep, np.exp(l / T - (l / T).max()), 0.0)
+    p /= p.sum()
+    stat, dof = _chi2(counts, p)
+    # chi-square tail: dof <= 6 -> p = 1e-6 at about 35
+    assert stat < 35.0, (stat, dof, counts / N, p)
+
+
+def test_sampling_special_cases():
+    rng = np.random.default_rng(9)
+    l = rng.standard_normal(1000)
+    l[417] = 5.0
+    for pos in range(20):
+        assert O.sample_token(l, 1.0, 1, seed=3, row=2, pos=pos) == 417       # top-1 is greedy
+        assert O.sample_token(l, 1e-9, 0, seed=3, row=2, pos=pos) == 417      # T -> 0 is greedy
+        assert O.sample_token(l, 0.0, 50, seed=3, row=2, pos=pos) == 417      # T = 0: argmax
+        t = O.sample_token(l, 2.0, 10, seed=3, row=2, pos=pos)
+        assert l[t] >= np.sort(l)[-10]                                          # inside the top-10
+    # ties at the pivot: every logit equal to the k-th largest stays a candidate
+    l2 = np.array([3.0, 1.0, 1.0, 1.0, 0.0])
+    seen = {O.sample_token(l2, 5.0, 2, seed=1, row=0, pos=p) for p in range(400)}
+    assert seen == {0, 1, 2, 3}
