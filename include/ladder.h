@@ -170,6 +170,21 @@ void ladder_destroy(ladder_model* m);
 /* Residual schedule (LADDER_RESIDUAL_*) and flags (LADDER_FLAG_*). */
 int ladder_set_mode(ladder_model* m, int residual_mode, int flags);
 
+/* Next-token rule for the next_tok outputs of ladder_prefill and
+ * ladder_decode_step.  temperature <= 0 (the default): greedy argmax, lowest
+ * index on ties.  temperature > 0: temperature / top-k sampling, read from the
+ * generation helpers the paper's codewithpapers record names
+ * (logits_to_probs, multinomial_sample_one_no_sync, sample): the logits are
+ * scaled by 1 / max(temperature, 1e-5), those below the top_k-th largest are
+ * dropped (top_k <= 0 or >= vocab keeps all; logits equal to the top_k-th
+ * largest stay), and the token is argmax_i p_i / q_i with q_i ~ Exp(1): a
+ * sample of the softmax p of the kept logits (the "exponential race"), taken
+ * as argmax_i l_i / T - ln(-ln u_i).  The uniforms are SplitMix64 counters keyed
+ * by (seed, batch row, position of the sampled token): the same seed, batch
+ * and positions reproduce the same tokens.  The logits outputs are unchanged.
+ * Returns LADDER_ERR_INVALID for a NaN temperature. */
+int ladder_set_sampling(ladder_model* m, float temperature, int32_t top_k, uint64_t seed);
+
 /* Paged KV cache.  `pool` is a device buffer of num_pages * kv_page_bytes,
  * 16-byte aligned, laid out in the weight dtype [n_layers][num_pages][2 (K, V)][n_kv_heads]
  * [page_size][head_dim]; keys are stored after rotation.  `block_table` is a
@@ -283,6 +298,14 @@ int ladder_attention_decode_noalloc(const float* q, const void* kv_layer, int32_
                                     const int32_t* positions, int32_t B, int32_t n_q_heads, int32_t n_kv_heads,
                                     int32_t head_dim, int32_t page_size, float scale, int32_t max_position,
                                     float* out, ladder_stream_t stream);
+
+/* Standalone sampler (the kernel behind ladder_set_sampling), for callers with
+ * their own logits: logits is a device fp32 [B][V] row-major array, positions a
+ * device int32 [B] array; row b draws with position positions[b] + pos_offset.
+ * out is a device int32 [B] array.  temperature must be > 0 (greedy decoding
+ * is the model's argmax).  Asynchronous on `stream`; allocates nothing. */
+int ladder_sample(const float* logits, int32_t B, int32_t V, float temperature, int32_t top_k, uint64_t seed,
+                  const int32_t* positions, int32_t pos_offset, int32_t* out, ladder_stream_t stream);
 
 /* Thread-local message describing the last failed call on this thread. */
 const char* ladder_last_error(void);

@@ -222,6 +222,10 @@ cudaError_t launch_attn_combine(const AttnDecodeParams& p, int B, int hd, cudaSt
 cudaError_t attn_decode_tc_configure();
 cudaError_t launch_attn_decode_tc(const void* kv_map, const AttnDecodeParams& p, int B, int n_kv, int hd, int wdt,
                                   int* err, cudaStream_t s, bool pdl);
+// Temperature / top-k sampling of the next token (sample.cu); row b draws with
+// position pos[b] + pos_off.  temperature must be > 0.
+cudaError_t launch_sample(const float* logits, int B, int V, float temperature, int top_k, uint64_t seed,
+                          const int* pos, int pos_off, int* out, cudaStream_t s, bool pdl);
 cudaError_t launch_argmax(const float* logits, int B, int V, float* part_v, int* part_i, int nblk,
                           int* out, cudaStream_t s, bool pdl = false);
 cudaError_t launch_advance(int* seq_lens, int B, cudaStream_t s, bool pdl = false);

@@ -187,6 +187,10 @@ struct ladder_model {
   int num_sms;
   int residual_mode = LADDER_RESIDUAL_CONFIG;
   int flags = 0;
+  // next-token rule: greedy when samp_t <= 0, else temperature / top-k sampling
+  float samp_t = 0.f;
+  int samp_k = 0;
+  uint64_t samp_seed = 0;
   int launches = 0;
   std::vector<GraphEntry> graphs;
   std::vector<int32_t> meta_host;
@@ -421,6 +425,17 @@ int ladder_set_mode(ladder_model* m, int residual_mode, int flags) {
   if (residual_mode != m->residual_mode || flags != m->flags) m->drop_graphs();
   m->residual_mode = residual_mode;
   m->flags = flags;
+  return LADDER_OK;
+}
+
+int ladder_set_sampling(ladder_model* m, float temperature, int32_t top_k, uint64_t seed) {
+  if (!m) return fail(LADDER_ERR_INVALID, "model is NULL");
+  if (temperature != temperature) return fail(LADDER_ERR_INVALID, "temperature is NaN");
+  const float t = temperature > 0.f ? temperature : 0.f;
+  if (t != m->samp_t || top_k != m->samp_k || seed != m->samp_seed) m->drop_graphs();
+  m->samp_t = t;
+  m->samp_k = top_k;
+  m->samp_seed = seed;
   return LADDER_OK;
 }
 
@@ -671,7 +686,9 @@ int enqueue_decode_shard(ladder_model* m, ladder_kv* kv, const int32_t* tokens, 
   h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.out = logits; h.ldo = c.vocab; h.err = m->err();
   m->splitk(h, SK_LMHEAD);
   LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, h.K, GEMV_LOGITS));
-  if (next_tok)
+  if (next_tok && m->samp_t > 0.f)  // the sampled token takes position seq_lens[b] + 1
+    LAUNCH(launch_sample(logits, B, c.vocab, m->samp_t, m->samp_k, m->samp_seed, kv->seq_lens, 1, next_tok, s, pdl), 1);
+  else if (next_tok)
     LAUNCH(launch_argmax(logits, B, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i), kArgmaxBlocks, next_tok, s, pdl), 2);
   LAUNCH(launch_advance(kv->seq_lens, B, s, pdl), 1);
   return LADDER_OK;
@@ -791,7 +808,9 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
   m->splitk(h, SK_LMHEAD);
   LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, h.K, GEMV_LOGITS));
   m->probe_stop(pe, s);
-  if (next_tok)
+  if (next_tok && m->samp_t > 0.f)  // the sampled token takes position seq_lens[b] + 1
+    LAUNCH(launch_sample(logits, B, c.vocab, m->samp_t, m->samp_k, m->samp_seed, kv->seq_lens, 1, next_tok, s, pdl), 1);
+  else if (next_tok)
     LAUNCH(launch_argmax(logits, B, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i), kArgmaxBlocks, next_tok, s, pdl), 2);
   LAUNCH(launch_advance(kv->seq_lens, B, s, pdl), 1);
   return LADDER_OK;
@@ -947,10 +966,25 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
   h.err = m->err();
   m->splitk(h, SK_LMHEAD);
   LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s), gemv_launch_count(B, h.K, GEMV_LOGITS));
-  if (next_tok)
+  if (next_tok && m->samp_t > 0.f)  // the sampled token takes position T_b
+    LAUNCH(launch_sample(logits, B, c.vocab, m->samp_t, m->samp_k, m->samp_seed, d_lens, 0, next_tok, s, false), 1);
+  else if (next_tok)
     LAUNCH(launch_argmax(logits, B, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i), kArgmaxBlocks, next_tok, s), 2);
   LAUNCH(launch_set_lens(d_lens, B, kv->seq_lens, s), 1);
   for (int b = 0; b < B; ++b) kv->host_lens[b] = host_lens[b];
+  return LADDER_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Standalone sampler
+// ---------------------------------------------------------------------------
+int ladder_sample(const float* logits, int32_t B, int32_t V, float temperature, int32_t top_k, uint64_t seed,
+                  const int32_t* positions, int32_t pos_offset, int32_t* out, ladder_stream_t stream) {
+  if (!logits || !positions || !out) return fail(LADDER_ERR_INVALID, "ladder_sample: null pointer");
+  if (B < 1 || V < 1) return fail(LADDER_ERR_INVALID, "ladder_sample: B=%d V=%d", B, V);
+  if (!(temperature > 0.f)) return fail(LADDER_ERR_INVALID, "ladder_sample: temperature must be > 0");
+  CUDA_TRY(launch_sample(logits, B, V, temperature, top_k, seed, positions, pos_offset, out,
+                         reinterpret_cast<cudaStream_t>(stream), false));
   return LADDER_OK;
 }
 

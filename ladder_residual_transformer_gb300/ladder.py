@@ -71,6 +71,8 @@ _SIGNATURES = {
                                        _vp, _vp, _sz, _vp]),
     "ladder_attention_decode_noalloc": (_i32, [_vp, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _f32,
                                                _i32, _vp, _vp]),
+    "ladder_set_sampling": (_i32, [_vp, _f32, _i32, ctypes.c_uint64]),
+    "ladder_sample": (_i32, [_vp, _i32, _i32, _f32, _i32, ctypes.c_uint64, _vp, _i32, _vp, _vp]),
     "ladder_last_error": (ctypes.c_char_p, []),
 }
 
@@ -215,6 +217,18 @@ def attention_decode_noalloc(q: torch.Tensor, kv_layer: torch.Tensor, block_tabl
     return out
 
 
+def sample(logits: torch.Tensor, positions: torch.Tensor, temperature: float, top_k: int = 0, seed: int = 0,
+           pos_offset: int = 0, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Temperature / top-k sampling of each row of device fp32 logits [B, V]
+    through the C ABI (see ladder_sample); positions: device int32 [B]."""
+    B, V = logits.shape
+    if out is None:
+        out = torch.empty(B, dtype=torch.int32, device=logits.device)
+    check(lib().ladder_sample(logits.data_ptr(), B, V, float(temperature), int(top_k), int(seed) & (2 ** 64 - 1),
+                              positions.data_ptr(), int(pos_offset), out.data_ptr(), _stream_handle(stream)))
+    return out
+
+
 class LadderModel:
     """A model over device weights plus its paged KV cache, driven through the C ABI.
 
@@ -287,6 +301,12 @@ class LadderModel:
         check(lib().ladder_set_mode(self._m, mode, flags))
         self._standard = standard
         self._parallel = parallel
+
+    def set_sampling(self, temperature: float = 0.0, top_k: int = 0, seed: int = 0):
+        """Next-token rule of prefill / decode_step: greedy (temperature <= 0) or
+        temperature / top-k sampling with SplitMix64 draws keyed by seed, batch
+        row and position (see ladder_set_sampling)."""
+        check(lib().ladder_set_sampling(self._m, float(temperature), int(top_k), int(seed) & (2 ** 64 - 1)))
 
     # -- forward ---------------------------------------------------------
     def prefill(self, tokens: torch.Tensor, lens, logits: torch.Tensor | None = None,
