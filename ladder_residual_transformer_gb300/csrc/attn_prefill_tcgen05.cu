@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(FT_THREADS, 1)
   const int kvh = h / (p.n_q / p.kv.n_kv);
   const int n_kb = qb + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -122,6 +123,9 @@ __global__ void __launch_bounds__(FT_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tmem_o = tmem + 256;
+  // Launched early (programmatic dependent launch), the prologue above overlaps
+  // the previous kernel; no thread touches global memory before it completes.
+  pdl_wait();
 
   if (warp == 4) {
     // Lane c < nch issues the K and V boxes of page chunk c of the tile; the
@@ -384,26 +388,26 @@ cudaError_t attn_prefill_tcgen05_configure() {
 }
 
 template <typename T>
-static void ft_dispatch(const FtMaps& maps, const AttnPrefillParams& p, int hd, int nqb, int B, int* err,
-                        cudaStream_t s) {
+static cudaError_t ft_dispatch(const FtMaps& maps, const AttnPrefillParams& p, int hd, int nqb, int B, int* err,
+                               cudaStream_t s, bool pdl) {
   const unsigned grid = (unsigned)nqb * p.n_q * B;
   if (hd == 64)
-    attn_prefill_tcgen05_kernel<T, 64><<<grid, FT_THREADS, FtCfg<64>::SMEM, s>>>(maps, p, nqb, B, err);
-  else
-    attn_prefill_tcgen05_kernel<T, 128><<<grid, FT_THREADS, FtCfg<128>::SMEM, s>>>(maps, p, nqb, B, err);
+    return launch_k(attn_prefill_tcgen05_kernel<T, 64>, dim3(grid), dim3(FT_THREADS), (size_t)FtCfg<64>::SMEM, s, pdl,
+                    maps, p, nqb, B, err);
+  return launch_k(attn_prefill_tcgen05_kernel<T, 128>, dim3(grid), dim3(FT_THREADS), (size_t)FtCfg<128>::SMEM, s, pdl,
+                  maps, p, nqb, B, err);
 }
 
 cudaError_t launch_attn_prefill_tcgen05(const void* q_map, const void* kv_map, const AttnPrefillParams& p, int hd,
-                                        int wdt, int B, int max_len, int* err, cudaStream_t s) {
+                                        int wdt, int B, int max_len, int* err, cudaStream_t s, bool pdl) {
   if (max_len <= 0) return cudaSuccess;
   if (hd != 64 && hd != 128) return cudaErrorInvalidValue;
   FtMaps maps;
   memcpy(&maps.q, q_map, sizeof(CUtensorMap));
   memcpy(&maps.kv, kv_map, sizeof(CUtensorMap));
   const int nqb = (max_len + FT_BM - 1) / FT_BM;
-  if (wdt == WDT_F16) ft_dispatch<f16>(maps, p, hd, nqb, B, err, s);
-  else ft_dispatch<bf16>(maps, p, hd, nqb, B, err, s);
-  return cudaGetLastError();
+  return wdt == WDT_F16 ? ft_dispatch<f16>(maps, p, hd, nqb, B, err, s, pdl)
+                        : ft_dispatch<bf16>(maps, p, hd, nqb, B, err, s, pdl);
 }
 
 }  // namespace ladder

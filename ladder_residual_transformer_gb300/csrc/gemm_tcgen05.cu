@@ -48,6 +48,7 @@ constexpr int TC_EP_WARP = 8192;
 constexpr int TC_EP_BYTES = 4 * TC_EP_WARP;
 constexpr int TC_SMEM = TC_RING + TC_EP_BYTES + 1024 + 256;
 constexpr int TC_THREADS = 192;
+constexpr int TC_PAIR_KC = 1;  // 64-wide K chunks per stage of the paired 256 x 256 tiles
 constexpr long long TC_WAIT_LIMIT = 4000000000LL;  // cycles (about 2 s)
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
@@ -136,7 +137,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
   constexpr int HB = PAIR ? 1 : HALVES;  // B halves held by this CTA
   constexpr int STAGE = A_BYTES + HB * BH_BYTES;
   constexpr int NST = TC_RING / STAGE;
-  static_assert(!PAIR || (BN == 256 && KC == 1), "paired tiles are 256 x 256 with one-chunk stages");
+  static_assert(!PAIR || BN == 256, "paired tiles are 256 x 256");
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ep_all = smem + TC_RING;
@@ -151,6 +152,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = p.K / BK;
   const int my_tiles = gemm_tile_count<PAIR>(m_tiles, n_tiles);
+  pdl_trigger();
   const uint32_t crank = PAIR ? cluster_ctarank() : 0;
   const bool leader = crank == 0;
 
@@ -185,6 +187,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
   else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Launched early (programmatic dependent launch), the prologue above overlaps
+  // the previous kernel; no thread touches global memory before it completes.
+  pdl_wait();
 
   if (warp == 4) {
     if (lane == 0) {
@@ -244,8 +249,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
       // KC = 1: the two B halves are contiguous, one N = BN MMA per k step.
       // KC = 2: each half is its own [chunk][row] box, one N = 128 MMA per half.
       // PAIR: one M = 256 paired MMA per k step.
-      constexpr int MMA_N = KC == 1 ? BN : 128;
-      constexpr int MMAS = KC == 1 ? 1 : HALVES;
+      constexpr int MMA_N = (PAIR || KC == 1) ? BN : 128;
+      constexpr int MMAS = (PAIR || KC == 1) ? 1 : HALVES;
       constexpr uint32_t idesc = umma_idesc(PAIR ? 2 * TC_BM : TC_BM, MMA_N, C::umma_fmt);
       int it = 0;
       bool ok = true;
@@ -277,7 +282,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
 #pragma unroll
               for (int hh = 0; hh < MMAS; ++hh)
                 if (PAIR)
-                  umma_f16_pair(d, umma_desc(a_base + kk * 32), umma_desc(b_base + kk * 32), idesc, (kb | kk) != 0);
+                  umma_f16_pair(d, umma_desc(a_base + c * TC_CHUNK + kk * 32), umma_desc(b_base + c * TC_CHUNK + kk * 32),
+                                idesc, (kb | c | kk) != 0);
                 else
                   umma_f16(d + hh * 128, umma_desc(a_base + c * TC_CHUNK + kk * 32),
                            umma_desc(b_base + hh * BH_BYTES + c * TC_CHUNK + kk * 32), idesc, (kb | c | kk) != 0);
@@ -592,12 +598,12 @@ template <typename WT>
 static cudaError_t gemm_tc_configure_t() {
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 256, 1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 256, 1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 256, TC_PAIR_KC, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
   if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 128, 2, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
   if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_GATEUP, 256, 1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_GATEUP, 256, 1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_GATEUP, 256, TC_PAIR_KC, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
   if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 256, 1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 256, 1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 256, TC_PAIR_KC, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
   return cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 128, 2, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
 }
 
@@ -611,16 +617,17 @@ cudaError_t gemm_tc_configure() {
 // 256 x 256 tiles on clusters of two CTAs, as many clusters as can be resident.
 template <typename WT, int MODE, int BN>
 static cudaError_t gemm_tc_go(const TmaOperand* a, const TmaOperand* const* b, const void* const* e,
-                              const GemmParams& p, int mt, int nt, int num_sms, int* err, cudaStream_t s) {
+                              const GemmParams& p, int mt, int nt, int num_sms, int* err, cudaStream_t s, bool pdl) {
   constexpr int KC = BN == 256 ? 1 : 2;
+  constexpr int BOX = (BN == 256 ? TC_PAIR_KC : KC) - 1;  // paired tiles use TC_PAIR_KC-chunk boxes
   TcMaps maps;
-  memcpy(&maps.a, &a->box[KC - 1], sizeof(CUtensorMap));
-  for (int i = 0; i < 3; ++i) memcpy(&maps.b[i], &(b[i] ? b[i] : b[0])->box[KC - 1], sizeof(CUtensorMap));
-  memcpy(&maps.e_in, e[0] ? e[0] : &maps.a, sizeof(CUtensorMap));
-  memcpy(&maps.e_out, e[1] ? e[1] : &maps.a, sizeof(CUtensorMap));
+  memcpy(&maps.e_in, e[0] ? e[0] : &a->box[0], sizeof(CUtensorMap));
+  memcpy(&maps.e_out, e[1] ? e[1] : &a->box[0], sizeof(CUtensorMap));
   if constexpr (BN == 256) {
     if (mt % 2 == 0) {
-      auto kern = gemm_tc_kernel<WT, MODE, BN, KC, 1>;
+      memcpy(&maps.a, &a->box[BOX], sizeof(CUtensorMap));
+      for (int i = 0; i < 3; ++i) memcpy(&maps.b[i], &(b[i] ? b[i] : b[0])->box[BOX], sizeof(CUtensorMap));
+      auto kern = gemm_tc_kernel<WT, MODE, BN, TC_PAIR_KC, 1>;
       cudaLaunchConfig_t cfg = {};
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -641,33 +648,41 @@ static cudaError_t gemm_tc_go(const TmaOperand* a, const TmaOperand* const* b, c
       }
       const int units = (mt / 2) * nt;
       cfg.gridDim = dim3(2 * (units < resident ? units : resident));
+      cudaLaunchAttribute attr2[2] = {attr[0], {}};
+      attr2[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr2[1].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr2;
+      cfg.numAttrs = pdl ? 2 : 1;
       return cudaLaunchKernelEx(&cfg, kern, maps, p, mt, nt, err);
     }
   }
+  memcpy(&maps.a, &a->box[KC - 1], sizeof(CUtensorMap));
+  for (int i = 0; i < 3; ++i) memcpy(&maps.b[i], &(b[i] ? b[i] : b[0])->box[KC - 1], sizeof(CUtensorMap));
   const int total = mt * nt;
   const int grid = total < num_sms ? total : num_sms;
-  gemm_tc_kernel<WT, MODE, BN, KC, 0><<<grid, TC_THREADS, TC_SMEM, s>>>(maps, p, mt, nt, err);
-  return cudaGetLastError();
+  return launch_k(gemm_tc_kernel<WT, MODE, BN, KC, 0>, dim3(grid), dim3(TC_THREADS), (size_t)TC_SMEM, s, pdl, maps, p,
+                  mt, nt, err);
 }
 
 // 256-wide tiles unless that leaves most SMs idle (narrow N at small M).
 template <typename WT>
 static cudaError_t gemm_tc_dispatch(const TmaOperand* a, const TmaOperand* const* b, const void* const* e,
-                                    const GemmParams& p, int mode, int mt, int num_sms, int* err, cudaStream_t s) {
-  if (mode == GEMM_GATEUP) return gemm_tc_go<WT, GEMM_GATEUP, 256>(a, b, e, p, mt, p.N / 128, num_sms, err, s);
+                                    const GemmParams& p, int mode, int mt, int num_sms, int* err, cudaStream_t s,
+                                    bool pdl) {
+  if (mode == GEMM_GATEUP) return gemm_tc_go<WT, GEMM_GATEUP, 256>(a, b, e, p, mt, p.N / 128, num_sms, err, s, pdl);
   const int nt256 = (p.N + 255) / 256;
   const bool narrow = (long long)mt * nt256 * 4 < (long long)num_sms * 3;
   if (mode == GEMM_RESID) {
-    if (narrow) return gemm_tc_go<WT, GEMM_RESID, 128>(a, b, e, p, mt, (p.N + 127) / 128, num_sms, err, s);
-    return gemm_tc_go<WT, GEMM_RESID, 256>(a, b, e, p, mt, nt256, num_sms, err, s);
+    if (narrow) return gemm_tc_go<WT, GEMM_RESID, 128>(a, b, e, p, mt, (p.N + 127) / 128, num_sms, err, s, pdl);
+    return gemm_tc_go<WT, GEMM_RESID, 256>(a, b, e, p, mt, nt256, num_sms, err, s, pdl);
   }
-  if (narrow) return gemm_tc_go<WT, GEMM_QKV, 128>(a, b, e, p, mt, (p.N + 127) / 128, num_sms, err, s);
-  return gemm_tc_go<WT, GEMM_QKV, 256>(a, b, e, p, mt, nt256, num_sms, err, s);
+  if (narrow) return gemm_tc_go<WT, GEMM_QKV, 128>(a, b, e, p, mt, (p.N + 127) / 128, num_sms, err, s, pdl);
+  return gemm_tc_go<WT, GEMM_QKV, 256>(a, b, e, p, mt, nt256, num_sms, err, s, pdl);
 }
 
 cudaError_t launch_gemm_tc(const TmaOperand* a, const TmaOperand* b0, const TmaOperand* b1, const TmaOperand* b2,
                            const void* e_in, const void* e_out, const GemmParams& p, int mode, int wdt, int num_sms,
-                           int* err, cudaStream_t s) {
+                           int* err, cudaStream_t s, bool pdl) {
   if (p.M <= 0) return cudaSuccess;
   // RESID reads and writes its rows through the epilogue maps, GATEUP writes through e_out
   if ((mode == GEMM_RESID && (!e_in || !e_out)) || (mode == GEMM_GATEUP && !e_out)) return cudaErrorInvalidValue;
@@ -675,8 +690,8 @@ cudaError_t launch_gemm_tc(const TmaOperand* a, const TmaOperand* b0, const TmaO
   const TmaOperand* b[3] = {b0, b1, b2};
   const void* e[2] = {e_in, e_out};
   const int mt = (p.M + TC_BM - 1) / TC_BM;
-  return wdt == WDT_F16 ? gemm_tc_dispatch<f16>(a, b, e, p, mode, mt, num_sms, err, s)
-                        : gemm_tc_dispatch<bf16>(a, b, e, p, mode, mt, num_sms, err, s);
+  return wdt == WDT_F16 ? gemm_tc_dispatch<f16>(a, b, e, p, mode, mt, num_sms, err, s, pdl)
+                        : gemm_tc_dispatch<bf16>(a, b, e, p, mode, mt, num_sms, err, s, pdl);
 }
 
 }  // namespace ladder

@@ -232,8 +232,10 @@ cudaError_t launch_advance(int* seq_lens, int B, cudaStream_t s, bool pdl = fals
 cudaError_t launch_rope_tables(float* cos_t, float* sin_t, int max_seq, int hd, float theta,
                                cudaStream_t s);
 
+// Prefill launches take `pdl` (programmatic dependent launch); every kernel
+// launched with it waits for the previous kernel before touching its data.
 cudaError_t launch_rmsnorm_rows(const float* x, int M, int d, const void* g, float eps, void* out, int wdt,
-                                cudaStream_t s);
+                                cudaStream_t s, bool pdl = false);
 // Tensor-core GEMM (tcgen05 + TMA).  Maps are CUtensorMap objects made by make_tma_map.
 // 2-D map of a row-major [rows, cols] 16-bit matrix, box 64 columns x 128 rows.
 bool make_tma_map(void* map_out, const void* base, uint64_t rows, uint64_t cols, int wdt);
@@ -252,16 +254,16 @@ cudaError_t gemm_tc_configure();
 // rows (RESID, fp32) or of the SwiGLU output rows (GATEUP e_out, weight dtype).
 cudaError_t launch_gemm_tc(const TmaOperand* a, const TmaOperand* b0, const TmaOperand* b1, const TmaOperand* b2,
                            const void* e_in, const void* e_out, const GemmParams& p, int mode, int wdt, int num_sms,
-                           int* err, cudaStream_t s);
+                           int* err, cudaStream_t s, bool pdl = false);
 // Tensor-core causal attention for packed prefill rows (mma.sync, bf16 Q/K/V).
 // Prefill attention on tcgen05: q_map = make_tma_map of the query rows, kv_map =
 // make_kv_tma_map of the layer; head_dim 64 or 128.
 cudaError_t attn_prefill_tcgen05_configure();
 cudaError_t launch_attn_prefill_tcgen05(const void* q_map, const void* kv_map, const AttnPrefillParams& p, int hd,
-                                        int wdt, int B, int max_len, int* err, cudaStream_t s);
+                                        int wdt, int B, int max_len, int* err, cudaStream_t s, bool pdl = false);
 cudaError_t launch_gather_rows(const float* x, int d, const int* rows, int B, float* out,
-                               cudaStream_t s);
-cudaError_t launch_set_lens(const int* lens, int B, int* seq_lens, cudaStream_t s);
+                               cudaStream_t s, bool pdl = false);
+cudaError_t launch_set_lens(const int* lens, int B, int* seq_lens, cudaStream_t s, bool pdl = false);
 // x_out[b, n] = x_res[b, n] + sum_{s < k} part[b][s][n], summed in the fixed order s = 0..k-1.
 cudaError_t launch_shard_reduce(const float* part, int k, int B, int d, const float* x_res, float* x_out,
                                 cudaStream_t s, bool pdl);

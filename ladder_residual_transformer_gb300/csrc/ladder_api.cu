@@ -919,58 +919,61 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
   void* qb = m->ws + P.q;     // rotated queries, weight dtype
   void* aob = m->ws + P.ao;   // attention output, weight dtype
   void* actb = m->ws + P.act; // SwiGLU output, weight dtype
+  // Every prefill kernel waits for its predecessor before touching memory, so
+  // each one is launched early and its prologue overlaps the previous tail.
+  const bool pdl = !(m->flags & LADDER_FLAG_NO_PDL);
 
-  LAUNCH(launch_embed(tokens, M, m->embed, wdt, d, c.vocab, m->X(0), m->err(), s), 1);
+  LAUNCH(launch_embed(tokens, M, m->embed, wdt, d, c.vocab, m->X(0), m->err(), s, pdl), 1);
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerW& L = m->layers[l];
     const LayerMaps& T = m->maps[l];
     const KvLayer kvl = kv->layer(l);
     {
       const int k = 2 * l + 1;
-      LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.attn_norm, c.norm_eps, xn, wdt, s), 1);
+      LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.attn_norm, c.norm_eps, xn, wdt, s, pdl), 1);
       GemmParams g{};
       g.M = M; g.N = qd + 2 * kvd; g.K = d;
       g.out_h = qb; g.ldo = qd; g.nq_hd = qd; g.nkv_hd = kvd;
       g.rope_cos = m->at<float>(P.rope_cos); g.rope_sin = m->at<float>(P.rope_sin);
       g.row_b = d_row_b; g.row_pos = d_row_pos; g.kv = kvl;
-      LAUNCH(launch_gemm_tc(&m->map_xn, &T.wq, &T.wk, &T.wv, nullptr, nullptr, g, GEMM_QKV, wdt, m->num_sms, m->err(), s), 1);
+      LAUNCH(launch_gemm_tc(&m->map_xn, &T.wq, &T.wk, &T.wv, nullptr, nullptr, g, GEMM_QKV, wdt, m->num_sms, m->err(), s, pdl), 1);
 
       AttnPrefillParams a{};
       a.q = qb; a.kv = kvl; a.seq_start = d_start; a.seq_len = d_lens;
       a.n_q = c.n_q_heads; a.scale = 1.0f / sqrtf((float)c.head_dim); a.out = aob;
-      LAUNCH(launch_attn_prefill_tcgen05(&m->map_q, &kv->maps[l], a, c.head_dim, wdt, B, max_len, m->err(), s), 1);
+      LAUNCH(launch_attn_prefill_tcgen05(&m->map_q, &kv->maps[l], a, c.head_dim, wdt, B, max_len, m->err(), s, pdl), 1);
 
       GemmParams o{};
       o.M = M; o.N = d; o.K = qd; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);
       LAUNCH(launch_gemm_tc(&m->map_ao, &T.wo, nullptr, nullptr, &m->map_x[(k - 1) % 3], &m->map_x[k % 3], o,
-                            GEMM_RESID, wdt, m->num_sms, m->err(), s), 1);
+                            GEMM_RESID, wdt, m->num_sms, m->err(), s, pdl), 1);
     }
     {
       const int k = 2 * l + 2;
-      LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.mlp_norm, c.norm_eps, xn, wdt, s), 1);
+      LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.mlp_norm, c.norm_eps, xn, wdt, s, pdl), 1);
       GemmParams g{};
       g.M = M; g.N = f; g.K = d; g.out_h = actb; g.ldo = f;
       LAUNCH(launch_gemm_tc(&m->map_xn, &T.gate, &T.up, nullptr, nullptr, &m->map_act_st, g, GEMM_GATEUP, wdt,
-                            m->num_sms, m->err(), s), 1);
+                            m->num_sms, m->err(), s, pdl), 1);
       GemmParams o{};
       o.M = M; o.N = d; o.K = f; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);
       LAUNCH(launch_gemm_tc(&m->map_act, &T.down, nullptr, nullptr, &m->map_x[(k - 1) % 3], &m->map_x[k % 3], o,
-                            GEMM_RESID, wdt, m->num_sms, m->err(), s), 1);
+                            GEMM_RESID, wdt, m->num_sms, m->err(), s, pdl), 1);
     }
   }
   float* xlast = m->at<float>(P.xlast);
-  LAUNCH(launch_gather_rows(m->X(2 * c.n_layers), d, d_last, B, xlast, s), 1);
+  LAUNCH(launch_gather_rows(m->X(2 * c.n_layers), d, d_last, B, xlast, s, pdl), 1);
   GemvParams h{};
   h.x = xlast; h.ldx = d; h.g = m->final_norm; h.eps = c.norm_eps; h.B = B; h.K = d;
   h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.out = logits; h.ldo = c.vocab;
   h.err = m->err();
   m->splitk(h, SK_LMHEAD);
-  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s), gemv_launch_count(B, h.K, GEMV_LOGITS));
+  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, h.K, GEMV_LOGITS));
   if (next_tok && m->samp_t > 0.f)  // the sampled token takes position T_b
-    LAUNCH(launch_sample(logits, B, c.vocab, m->samp_t, m->samp_k, m->samp_seed, d_lens, 0, next_tok, s, false), 1);
+    LAUNCH(launch_sample(logits, B, c.vocab, m->samp_t, m->samp_k, m->samp_seed, d_lens, 0, next_tok, s, pdl), 1);
   else if (next_tok)
-    LAUNCH(launch_argmax(logits, B, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i), kArgmaxBlocks, next_tok, s), 2);
-  LAUNCH(launch_set_lens(d_lens, B, kv->seq_lens, s), 1);
+    LAUNCH(launch_argmax(logits, B, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i), kArgmaxBlocks, next_tok, s, pdl), 2);
+  LAUNCH(launch_set_lens(d_lens, B, kv->seq_lens, s, pdl), 1);
   for (int b = 0; b < B; ++b) kv->host_lens[b] = host_lens[b];
   return LADDER_OK;
 }

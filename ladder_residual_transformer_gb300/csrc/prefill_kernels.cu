@@ -16,6 +16,8 @@ __global__ void __launch_bounds__(256) rmsnorm_rows_kernel(const float* __restri
                                                             const WT* __restrict__ g, float eps,
                                                             WT* __restrict__ out) {
   using C = W16<WT>;
+  pdl_trigger();
+  pdl_wait();
   const int m = blockIdx.x, tid = threadIdx.x;
   const float* xr = x + (size_t)m * d;
   float ss = 0.f;
@@ -43,13 +45,13 @@ __global__ void __launch_bounds__(256) rmsnorm_rows_kernel(const float* __restri
 }
 
 cudaError_t launch_rmsnorm_rows(const float* x, int M, int d, const void* g, float eps, void* out, int wdt,
-                                cudaStream_t s) {
+                                cudaStream_t s, bool pdl) {
   if (M <= 0) return cudaSuccess;
   if (wdt == WDT_F16)
-    rmsnorm_rows_kernel<f16><<<M, 256, 0, s>>>(x, d, static_cast<const f16*>(g), eps, static_cast<f16*>(out));
-  else
-    rmsnorm_rows_kernel<bf16><<<M, 256, 0, s>>>(x, d, static_cast<const bf16*>(g), eps, static_cast<bf16*>(out));
-  return cudaGetLastError();
+    return launch_k(rmsnorm_rows_kernel<f16>, dim3(M), dim3(256), 0, s, pdl, x, d, static_cast<const f16*>(g), eps,
+                    static_cast<f16*>(out));
+  return launch_k(rmsnorm_rows_kernel<bf16>, dim3(M), dim3(256), 0, s, pdl, x, d, static_cast<const bf16*>(g), eps,
+                  static_cast<bf16*>(out));
 }
 
 // ---------------------------------------------------------------------------
@@ -57,25 +59,27 @@ cudaError_t launch_rmsnorm_rows(const float* x, int M, int d, const void* g, flo
 // ---------------------------------------------------------------------------
 __global__ void gather_rows_kernel(const float* __restrict__ x, int d, const int* __restrict__ rows,
                                    float* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x;
   const float* src = x + (size_t)rows[b] * d;
   for (int i = threadIdx.x * 4; i < d; i += blockDim.x * 4)
     *reinterpret_cast<float4*>(out + (size_t)b * d + i) = *reinterpret_cast<const float4*>(src + i);
 }
 
-cudaError_t launch_gather_rows(const float* x, int d, const int* rows, int B, float* out, cudaStream_t s) {
-  gather_rows_kernel<<<B, 256, 0, s>>>(x, d, rows, out);
-  return cudaGetLastError();
+cudaError_t launch_gather_rows(const float* x, int d, const int* rows, int B, float* out, cudaStream_t s, bool pdl) {
+  return launch_k(gather_rows_kernel, dim3(B), dim3(256), 0, s, pdl, x, d, rows, out);
 }
 
 __global__ void set_lens_kernel(const int* lens, int B, int* seq_lens) {
+  pdl_trigger();
+  pdl_wait();
   const int b = threadIdx.x;
   if (b < B) seq_lens[b] = lens[b];
 }
 
-cudaError_t launch_set_lens(const int* lens, int B, int* seq_lens, cudaStream_t s) {
-  set_lens_kernel<<<1, 64, 0, s>>>(lens, B, seq_lens);
-  return cudaGetLastError();
+cudaError_t launch_set_lens(const int* lens, int B, int* seq_lens, cudaStream_t s, bool pdl) {
+  return launch_k(set_lens_kernel, dim3(1), dim3(64), 0, s, pdl, lens, B, seq_lens);
 }
 
 }  // namespace ladder
