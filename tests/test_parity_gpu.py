@@ -168,6 +168,29 @@ def test_narrow_gemm_tiles_with_ragged_rows():
         compare_logits(g_logits[s_], o_logits[s_], f"paired narrow tiles step {s_}")
 
 
+def test_prefill_repeats_bitwise():
+    """500 packed rows (4 m tiles) and d = 1024 (narrow residual GEMMs, paired
+    gate/up tiles, two-stream-free prefill with programmatic dependent launch):
+    logits match the oracle, and repeated prefills give identical bits."""
+    dims = small_dims(d_model=1024, n_q_heads=16, n_kv_heads=4, head_dim=64, ffn_dim=4096, vocab=2048,
+                      n_layers=2, n_standard_layers=0)
+    gw, ow = gpu_weights(dims), oracle_weights(dims)
+    lens = [300, 200]
+    prompts = prompts_for(lens, dims["vocab"])
+    feed = np.stack([synth.tokens(1, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(2)])
+    model = make_model(dims, gw, max_batch=2, max_seq=320, page_size=64)
+    g_logits, _ = run_teacher_forced(model, prompts, feed)
+    o_logits, _ = O.teacher_forced_decode(dims, ow, prompts, feed)
+    for s_ in range(2):
+        compare_logits(g_logits[s_], o_logits[s_], f"4-tile prefill step {s_}")
+    runs = []
+    for _ in range(3):
+        model.reset()
+        runs.append(run_teacher_forced(model, prompts, feed)[0])
+    for r in runs:
+        assert np.array_equal(r, g_logits)
+
+
 @pytest.mark.parametrize("B", [16, 21])
 def test_batched_decode_on_tensor_cores(B):
     """Decode batches above 4 rows run on the mma.sync projection in chunks of 16
