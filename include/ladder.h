@@ -242,7 +242,8 @@ enum {
   LADDER_PROBE_OUT = 2,     /* decode: O-projection GEMV + residual */
   LADDER_PROBE_GATEUP = 3,  /* decode: RMSNorm + gate/up GEMV + SwiGLU */
   LADDER_PROBE_DOWN = 4,    /* decode: down-projection GEMV + residual */
-  LADDER_PROBE_LMHEAD = 5   /* decode: final RMSNorm + lm_head GEMV */
+  LADDER_PROBE_LMHEAD = 5,  /* decode: final RMSNorm + lm_head GEMV */
+  LADDER_PROBE_REDUCE = 6   /* decode, shard mode: the reduce of a module's partial sums */
 };
 
 /* Start timing every launch of one kernel class in the following eager
@@ -254,6 +255,22 @@ int ladder_probe_begin(ladder_model* m, int kernel_class, int32_t max_launches);
 /* Stop timing: waits for the recorded events and returns how many launches
  * were timed and the sum of their durations in milliseconds. */
 int ladder_probe_end(ladder_model* m, int32_t* launches, float* total_ms);
+
+/* Launch timeline of eager decode steps (a tracing aid; the pages have no
+ * counterpart).  ladder_timeline_begin arms it for up to max_launches launches
+ * (1 .. 65536) and records a reference event on `stream`; every launch of a
+ * probe class (LADDER_PROBE_*) in the following eager decode steps then records
+ * an event before and after it on the stream it runs on.  ladder_timeline_end
+ * waits for the events and writes, for the first min(recorded, capacity)
+ * launches in issue order, the stream (0 = the caller's, 1 = the model's second
+ * stream), the class, and the start and end in milliseconds after the
+ * reference event; *n receives that count.  The event records sit between
+ * kernels, so a launch cannot overlap the previous kernel of its own stream
+ * (programmatic dependent launch is defeated); overlap between the two streams
+ * is what the timeline shows.  Fails while LADDER_FLAG_DECODE_GRAPH is set. */
+int ladder_timeline_begin(ladder_model* m, int32_t max_launches, ladder_stream_t stream);
+int ladder_timeline_end(ladder_model* m, int32_t capacity, int32_t* n, int32_t* streams, int32_t* classes,
+                        float* start_ms, float* end_ms);
 
 /* Decode attention as a standalone operation: the split-context paged GQA
  * attention that ladder_decode_step runs in every layer.  For each sequence b

@@ -205,6 +205,12 @@ struct ladder_model {
   int probe_class = -1;
   int probe_count = 0;
   std::vector<cudaEvent_t> probe_events;  // start/stop pairs
+  // launch timeline: an event pair per launch on its stream, and a reference event
+  bool tl_on = false;
+  int tl_count = 0;
+  std::vector<cudaEvent_t> tl_events;  // start/stop pairs
+  std::vector<int> tl_stream, tl_class;
+  cudaEvent_t tl_ref = nullptr;
   bool capturing = false;
 
   float* X(int i) { return reinterpret_cast<float*>(ws + plan.x[i % 3]); }
@@ -245,17 +251,43 @@ struct ladder_model {
     probe_class = -1;
     probe_count = 0;
   }
-  // Event pair around one launch of `cls` when the probe is armed for it.
-  cudaEvent_t probe_start(int cls, cudaStream_t s) {
-    if (cls != probe_class || capturing || 2 * (size_t)probe_count >= probe_events.size()) return nullptr;
-    cudaEvent_t e = probe_events[2 * probe_count];
-    cudaEventRecord(e, s);
-    return e;
+  void drop_timeline() {
+    for (auto e : tl_events)
+      if (e) cudaEventDestroy(e);
+    if (tl_ref) cudaEventDestroy(tl_ref);
+    tl_events.clear();
+    tl_stream.clear();
+    tl_class.clear();
+    tl_ref = nullptr;
+    tl_on = false;
+    tl_count = 0;
   }
-  void probe_stop(cudaEvent_t started, cudaStream_t s) {
-    if (!started) return;
-    cudaEventRecord(probe_events[2 * probe_count + 1], s);
-    ++probe_count;
+  // Event pairs around one launch of `cls`: for the probe when it is armed for
+  // this class, for the timeline when it is armed.
+  struct Probe {
+    int probe = -1, tl = -1;
+  };
+  Probe probe_start(int cls, cudaStream_t s) {
+    Probe p;
+    if (capturing) return p;
+    if (cls == probe_class && 2 * (size_t)probe_count < probe_events.size()) {
+      p.probe = probe_count;
+      cudaEventRecord(probe_events[2 * probe_count], s);
+    }
+    if (tl_on && 2 * (size_t)tl_count < tl_events.size()) {
+      p.tl = tl_count++;
+      tl_stream[p.tl] = s == aux ? 1 : 0;
+      tl_class[p.tl] = cls;
+      cudaEventRecord(tl_events[2 * p.tl], s);
+    }
+    return p;
+  }
+  void probe_stop(Probe p, cudaStream_t s) {
+    if (p.probe >= 0) {
+      cudaEventRecord(probe_events[2 * p.probe + 1], s);
+      ++probe_count;
+    }
+    if (p.tl >= 0) cudaEventRecord(tl_events[2 * p.tl + 1], s);
   }
 };
 
@@ -408,6 +440,7 @@ void ladder_destroy(ladder_model* m) {
   if (!m) return;
   m->drop_graphs();
   m->drop_probe();
+  m->drop_timeline();
   for (auto& e : m->ev_slot)
     if (e) cudaEventDestroy(e);
   if (m->ev_fork) cudaEventDestroy(m->ev_fork);
@@ -529,7 +562,7 @@ int32_t ladder_last_launch_count(const ladder_model* m) { return m ? m->launches
 
 int ladder_probe_begin(ladder_model* m, int kernel_class, int32_t max_launches) {
   if (!m) return fail(LADDER_ERR_INVALID, "model is NULL");
-  if (kernel_class < LADDER_PROBE_QKV || kernel_class > LADDER_PROBE_LMHEAD)
+  if (kernel_class < LADDER_PROBE_QKV || kernel_class > LADDER_PROBE_REDUCE)
     return fail(LADDER_ERR_INVALID, "unknown kernel class %d", kernel_class);
   if (max_launches < 1 || max_launches > 65536) return fail(LADDER_ERR_INVALID, "max_launches out of range");
   if (m->flags & LADDER_FLAG_DECODE_GRAPH) return fail(LADDER_ERR_INVALID, "the probe times eager decode steps only");
@@ -544,6 +577,51 @@ int ladder_probe_begin(ladder_model* m, int kernel_class, int32_t max_launches) 
     }
   }
   m->probe_class = kernel_class;
+  return LADDER_OK;
+}
+
+int ladder_timeline_begin(ladder_model* m, int32_t max_launches, ladder_stream_t stream) {
+  if (!m) return fail(LADDER_ERR_INVALID, "model is NULL");
+  if (max_launches < 1 || max_launches > 65536) return fail(LADDER_ERR_INVALID, "max_launches out of range");
+  if (m->flags & LADDER_FLAG_DECODE_GRAPH) return fail(LADDER_ERR_INVALID, "the timeline records eager decode steps only");
+  m->drop_timeline();
+  m->tl_events.resize(2 * (size_t)max_launches, nullptr);
+  m->tl_stream.assign(max_launches, 0);
+  m->tl_class.assign(max_launches, 0);
+  cudaError_t err = cudaEventCreate(&m->tl_ref);
+  for (auto& e : m->tl_events)
+    if (err == cudaSuccess) err = cudaEventCreate(&e);
+  if (err == cudaSuccess) err = cudaEventRecord(m->tl_ref, reinterpret_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) {
+    m->drop_timeline();
+    return fail(LADDER_ERR_CUDA, "timeline events: %s", cudaGetErrorString(err));
+  }
+  m->tl_on = true;
+  return LADDER_OK;
+}
+
+int ladder_timeline_end(ladder_model* m, int32_t capacity, int32_t* n, int32_t* streams, int32_t* classes,
+                        float* start_ms, float* end_ms) {
+  if (!m || !n || (capacity > 0 && (!streams || !classes || !start_ms || !end_ms)))
+    return fail(LADDER_ERR_INVALID, "NULL argument");
+  if (!m->tl_on) return fail(LADDER_ERR_INVALID, "the timeline is not armed");
+  const int cnt = m->tl_count < capacity ? m->tl_count : capacity;
+  for (int i = 0; i < cnt; ++i) {
+    float t0 = 0.f, t1 = 0.f;
+    cudaError_t e = cudaEventSynchronize(m->tl_events[2 * i + 1]);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t0, m->tl_ref, m->tl_events[2 * i]);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t1, m->tl_ref, m->tl_events[2 * i + 1]);
+    if (e != cudaSuccess) {
+      m->drop_timeline();
+      return fail(LADDER_ERR_CUDA, "timeline events: %s", cudaGetErrorString(e));
+    }
+    streams[i] = m->tl_stream[i];
+    classes[i] = m->tl_class[i];
+    start_ms[i] = t0;
+    end_ms[i] = t1;
+  }
+  *n = cnt;
+  m->drop_timeline();
   return LADDER_OK;
 }
 
@@ -651,18 +729,22 @@ int enqueue_decode_shard(ladder_model* m, ladder_kv* kv, const int32_t* tokens, 
       g.rope_cos = m->at<float>(P.rope_cos); g.rope_sin = m->at<float>(P.rope_sin);
       g.pos = kv->seq_lens; g.kv = kvl; g.err = m->err();
       m->splitk(g, SK_QKV);
+      auto pq = m->probe_start(LADDER_PROBE_QKV, s);
       LAUNCH(launch_gemv(g, GEMV_QKV, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, g.K, GEMV_QKV));
+      m->probe_stop(pq, s);
       AttnDecodeParams a{};
       a.q = q; a.kv = kvl; a.seq_lens = kv->seq_lens; a.n_q = c.n_q_heads; a.split_len = kSplitLen;
       a.nsplit = nsplit; a.scale = 1.0f / sqrtf((float)c.head_dim);
       a.part_o = m->at<float>(P.part_o); a.part_ml = m->at<float>(P.part_ml); a.out = ao;
+      auto pa = m->probe_start(LADDER_PROBE_ATTN, s);
       LAUNCH(launch_attn_decode_tc(&kv->maps[l], a, B, c.n_kv_heads, c.head_dim, m->wdt, m->err(), s, pdl), 2);
+      m->probe_stop(pa, s);
       o.x = ao; o.ldx = qd; o.K = qd / ksh; o.kfull = qd; o.ldw = qd; o.w0 = L.wo;
     } else {  // MLP module
       GemvParams g{};
       g.x = m->X(j); g.ldx = d; g.g = L.mlp_norm; g.eps = c.norm_eps; g.B = B; g.K = d;
       g.w0 = L.w_gate; g.w1 = L.w_up; g.n_tasks = f; g.out = act; g.ldo = f; g.err = m->err();
-      cudaEvent_t pe = m->probe_start(LADDER_PROBE_GATEUP, s);
+      auto pe = m->probe_start(LADDER_PROBE_GATEUP, s);
       m->splitk(g, SK_GATEUP);
       LAUNCH(launch_gemv(g, GEMV_GATEUP, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, g.K, GEMV_GATEUP));
       m->probe_stop(pe, s);
@@ -671,12 +753,16 @@ int enqueue_decode_shard(ladder_model* m, ladder_kv* kv, const int32_t* tokens, 
     // row-parallel partial sums: shard sh uses input block sh and writes part[b][sh][:]
     o.g = nullptr; o.B = B; o.shard_tasks = d / 2; o.n_tasks = ksh * (d / 2);
     o.out = pk; o.ldo = ksh * d; o.err = m->err();
+    auto po = m->probe_start((k & 1) ? LADDER_PROBE_OUT : LADDER_PROBE_DOWN, s);
     LAUNCH(launch_gemv(o, GEMV_PARTIAL, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, o.kfull, GEMV_PARTIAL));
+    m->probe_stop(po, s);
     CUDA_TRY(cudaEventRecord(m->ev_part, s));
     // the "all-reduce": x_k = x_{k-1} + sum of the partials, on the second stream
     CUDA_TRY(cudaStreamWaitEvent(rs, m->ev_part, 0));
     if (writer[(k - 1) % 3] == 0) CUDA_TRY(cudaStreamWaitEvent(rs, m->ev_slot[(k - 1) % 3], 0));
+    auto pr = m->probe_start(LADDER_PROBE_REDUCE, rs);
     LAUNCH(launch_shard_reduce(pk, ksh, B, d, m->X(k - 1), m->X(k), rs, pdl), 1);
+    m->probe_stop(pr, rs);
     CUDA_TRY(cudaEventRecord(m->ev_slot[k % 3], rs));
     writer[k % 3] = 1;
   }
@@ -685,7 +771,9 @@ int enqueue_decode_shard(ladder_model* m, ladder_kv* kv, const int32_t* tokens, 
   h.x = m->X(2 * c.n_layers); h.ldx = d; h.g = m->final_norm; h.eps = c.norm_eps; h.B = B; h.K = d;
   h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.out = logits; h.ldo = c.vocab; h.err = m->err();
   m->splitk(h, SK_LMHEAD);
+  auto ph = m->probe_start(LADDER_PROBE_LMHEAD, s);
   LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, h.K, GEMV_LOGITS));
+  m->probe_stop(ph, s);
   if (next_tok && m->samp_t > 0.f)  // the sampled token takes position seq_lens[b] + 1
     LAUNCH(launch_sample(logits, B, c.vocab, m->samp_t, m->samp_k, m->samp_seed, kv->seq_lens, 1, next_tok, s, pdl), 1);
   else if (next_tok)
@@ -747,7 +835,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       g.out = q; g.ldo = qd; g.nq_hd = qd; g.nkv_hd = kvd;
       g.rope_cos = m->at<float>(P.rope_cos); g.rope_sin = m->at<float>(P.rope_sin);
       g.pos = kv->seq_lens; g.kv = kvl;
-      cudaEvent_t pe = m->probe_start(LADDER_PROBE_QKV, s);
+      auto pe = m->probe_start(LADDER_PROBE_QKV, s);
       g.err = m->err();
       m->splitk(g, SK_QKV);
       LAUNCH(launch_gemv(g, GEMV_QKV, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, g.K, GEMV_QKV));
@@ -781,7 +869,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       GemvParams g{};
       g.x = m->X(j); g.ldx = d; g.g = L.mlp_norm; g.eps = c.norm_eps; g.B = B; g.K = d;
       g.w0 = L.w_gate; g.w1 = L.w_up; g.n_tasks = f; g.out = act; g.ldo = f;
-      cudaEvent_t pe = m->probe_start(LADDER_PROBE_GATEUP, ms);
+      auto pe = m->probe_start(LADDER_PROBE_GATEUP, ms);
       g.err = m->err();
       m->splitk(g, SK_GATEUP);
       LAUNCH(launch_gemv(g, GEMV_GATEUP, m->wdt, m->num_sms, ms, pdl), gemv_launch_count(B, g.K, GEMV_GATEUP));
@@ -803,7 +891,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
   GemvParams h{};
   h.x = m->X(2 * c.n_layers); h.ldx = d; h.g = m->final_norm; h.eps = c.norm_eps; h.B = B; h.K = d;
   h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.out = logits; h.ldo = c.vocab;
-  cudaEvent_t pe = m->probe_start(LADDER_PROBE_LMHEAD, s);
+  auto pe = m->probe_start(LADDER_PROBE_LMHEAD, s);
   h.err = m->err();
   m->splitk(h, SK_LMHEAD);
   LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, h.K, GEMV_LOGITS));

@@ -71,6 +71,8 @@ _SIGNATURES = {
                                        _vp, _vp, _sz, _vp]),
     "ladder_attention_decode_noalloc": (_i32, [_vp, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _f32,
                                                _i32, _vp, _vp]),
+    "ladder_timeline_begin": (_i32, [_vp, _i32, _vp]),
+    "ladder_timeline_end": (_i32, [_vp, _i32, _pi32, _vp, _vp, _vp, _vp]),
     "ladder_set_sampling": (_i32, [_vp, _f32, _i32, ctypes.c_uint64]),
     "ladder_sample": (_i32, [_vp, _i32, _i32, _f32, _i32, ctypes.c_uint64, _vp, _i32, _vp, _vp]),
     "ladder_last_error": (ctypes.c_char_p, []),
@@ -78,7 +80,7 @@ _SIGNATURES = {
 
 STATIC_SCRATCH_BYTES = 8 << 20  # LADDER_STATIC_SCRATCH_BYTES
 
-PROBE_CLASSES = {"qkv": 0, "attn": 1, "out": 2, "gateup": 3, "down": 4, "lmhead": 5}
+PROBE_CLASSES = {"qkv": 0, "attn": 1, "out": 2, "gateup": 3, "down": 4, "lmhead": 5, "reduce": 6}
 
 
 def lib(build_if_missing: bool = True):
@@ -381,6 +383,24 @@ class LadderModel:
         n, ms = ctypes.c_int32(0), ctypes.c_float(0)
         check(lib().ladder_probe_end(self._m, ctypes.byref(n), ctypes.byref(ms)))
         return n.value, ms.value
+
+    def timeline_begin(self, max_launches: int, stream=None):
+        """Arm the launch timeline for the following eager decode steps."""
+        check(lib().ladder_timeline_begin(self._m, max_launches, _stream_handle(stream)))
+        self._tl_cap = max_launches
+
+    def timeline_end(self) -> list[tuple[int, str, float, float]]:
+        """(stream, class name, start ms, end ms) of each recorded launch, in issue order."""
+        cap = getattr(self, "_tl_cap", 0)
+        st = np.zeros(cap, np.int32)
+        cl = np.zeros(cap, np.int32)
+        t0 = np.zeros(cap, np.float32)
+        t1 = np.zeros(cap, np.float32)
+        n = ctypes.c_int32(0)
+        check(lib().ladder_timeline_end(self._m, cap, ctypes.byref(n), st.ctypes.data, cl.ctypes.data,
+                                        t0.ctypes.data, t1.ctypes.data))
+        names = {v: k for k, v in PROBE_CLASSES.items()}
+        return [(int(st[i]), names[int(cl[i])], float(t0[i]), float(t1[i])) for i in range(n.value)]
 
     def last_launch_count(self) -> int:
         return lib().ladder_last_launch_count(self._m)

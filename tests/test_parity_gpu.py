@@ -425,3 +425,39 @@ def test_shard_config_is_validated():
         with pytest.raises(ladder.LadderError) as e:
             make_model(dims, gw, max_batch=1, max_seq=32, shard_k=k)
         assert e.value.code == code
+
+
+@pytest.mark.parametrize("shard_k", [1, 2])
+def test_launch_timeline(shard_k):
+    """The launch timeline of one eager decode step: every projection,
+    attention and reduce launch is recorded once, on the stream the schedule
+    puts it on (ladder layers: MLP chain, or shard reduces, on the second
+    stream), with end >= start and issue order preserved per stream."""
+    dims = small_dims(d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=3072, vocab=2048)
+    model = make_model(dims, gpu_weights(dims), max_batch=1, max_seq=64, page_size=32, shard_k=shard_k)
+    s = torch.cuda.Stream()
+    tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(s):
+        model.set_mode(graph=False)
+        _, nt = model.prefill(packed(prompts_for([20], dims["vocab"])), [20])
+        model.timeline_begin(256, s)
+        model.decode_step(nt)
+        rows = model.timeline_end()
+    s.synchronize()
+    L = dims["n_layers"]
+    names = [r[1] for r in rows]
+    for cls in ("qkv", "attn", "out", "gateup", "down"):
+        assert names.count(cls) == L, (cls, names)
+    assert names.count("lmhead") == 1
+    assert names.count("reduce") == (2 * L if shard_k > 1 else 0)
+    for st, cls, t0, t1 in rows:
+        assert t1 >= t0 >= 0.0
+        if shard_k > 1:
+            assert st == (1 if cls == "reduce" else 0), (st, cls)
+        elif cls in ("gateup", "down"):
+            assert st == 1  # ladder layers: the MLP chain runs on the second stream
+        else:
+            assert st == 0
+    for stream_id in (0, 1):
+        starts = [t0 for st, _, t0, _ in rows if st == stream_id]
+        assert starts == sorted(starts)
