@@ -53,6 +53,16 @@ Readings where the pages are silent (each one is a switch or a documented choice
       argmax_i l_i / T - ln(q_i).  The draws are not the pages': q_i = -ln u_i
       with u_i from SplitMix64 counters keyed by (seed, batch row, position of
       the sampled token), as written in ``sample_uniforms``.
+  R9  Rotary frequency scaling: [record] names the official code's
+      apply_rope_scaling helper (Llama-3.1 checkpoints).  Read as the published
+      Llama-3.1 rule, written out in ``rope_inv_freq``: with wavelength
+      w_j = 2 pi / f_j, frequencies with w_j < L / high_freq_factor stay,
+      those with w_j > L / low_freq_factor are divided by `factor`, and those
+      in between are interpolated, f = (1 - s) f / factor + s f with
+      s = (L / w_j - low_freq_factor) / (high_freq_factor - low_freq_factor),
+      L = the original maximum position.  ``dims["rope_scaling"]`` (a dict of
+      factor, low_freq_factor, high_freq_factor, original_max_position)
+      switches it on; absent or None leaves the frequencies unscaled.
   R7  The parallel-block model that [notes] compares against (the Parallel-70B
       row of the 70B latency breakdown table, section 实验关键数据) is not spelt
       out there; it is read as the usual parallel attention + MLP layer: both
@@ -79,6 +89,7 @@ __all__ = [
     "causal_gqa_attention", "attention_module", "mlp_module", "silu", "module_input_index",
     "forward", "prefill", "decode_step", "greedy_generate", "teacher_forced_decode",
     "argmax_lowest", "kv_slot", "kv_pool_offset", "splitmix64_mix", "sample_uniforms", "sample_token",
+    "rope_inv_freq",
 ]
 
 
@@ -159,10 +170,32 @@ def rmsnorm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
     return x / np.sqrt(ms + x.dtype.type(eps)) * g
 
 
-def rope_tables(positions: np.ndarray, head_dim: int, theta: float, dtype) -> tuple[np.ndarray, np.ndarray]:
-    """cos and sin of phi[p, j] = p * theta^(-2j/hd), j < hd/2, formed in fp64 (R4)."""
+def rope_inv_freq(head_dim: int, theta: float, scaling: dict | None = None) -> np.ndarray:
+    """f_j = theta^(-2j/hd), j < hd/2, in fp64 (R4), then the frequency scaling of R9."""
     j = np.arange(head_dim // 2, dtype=np.float64)
-    inv_freq = float(theta) ** (-2.0 * j / head_dim)
+    f = float(theta) ** (-2.0 * j / head_dim)
+    if not scaling:
+        return f
+    factor = float(scaling["factor"])
+    low, high = float(scaling["low_freq_factor"]), float(scaling["high_freq_factor"])
+    L = float(scaling["original_max_position"])
+    out = np.empty_like(f)
+    for i, fj in enumerate(f):
+        w = 2.0 * math.pi / fj
+        if w < L / high:
+            out[i] = fj
+        elif w > L / low:
+            out[i] = fj / factor
+        else:
+            s = (L / w - low) / (high - low)
+            out[i] = (1.0 - s) * fj / factor + s * fj
+    return out
+
+
+def rope_tables(positions: np.ndarray, head_dim: int, theta: float, dtype,
+                scaling: dict | None = None) -> tuple[np.ndarray, np.ndarray]:
+    """cos and sin of phi[p, j] = p * f_j, j < hd/2, formed in fp64 (R4, R9)."""
+    inv_freq = rope_inv_freq(head_dim, theta, scaling)
     phi = np.asarray(positions, dtype=np.float64)[:, None] * inv_freq[None, :]
     return np.cos(phi).astype(dtype), np.sin(phi).astype(dtype)
 
@@ -243,7 +276,7 @@ def attention_module(dims: dict, lw: LayerWeights, u: np.ndarray, start: int,
     k = (u @ lw.wk.T).reshape(T, nkv, hd)
     v = (u @ lw.wv.T).reshape(T, nkv, hd)
     pos = np.arange(start, start + T)
-    cos, sin = rope_tables(pos, hd, dims["rope_theta"], u.dtype)
+    cos, sin = rope_tables(pos, hd, dims["rope_theta"], u.dtype, dims.get("rope_scaling"))
     inter = bool(dims.get("rope_interleaved", 1))
     q = apply_rope(q, cos, sin, inter)
     k = apply_rope(k, cos, sin, inter)

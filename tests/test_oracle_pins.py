@@ -517,3 +517,45 @@ def test_sampling_special_cases():
     l2 = np.array([3.0, 1.0, 1.0, 1.0, 0.0])
     seen = {O.sample_token(l2, 5.0, 2, seed=1, row=0, pos=p) for p in range(400)}
     assert seen == {0, 1, 2, 3}
+
+
+# ---------------------------------------------------------------------------
+# Rotary frequency scaling (Llama-3.1 rule)
+# ---------------------------------------------------------------------------
+SCALING = {"factor": 8.0, "low_freq_factor": 1.0, "high_freq_factor": 4.0, "original_max_position": 8192}
+
+
+def test_rope_scaling_regimes_and_continuity():
+    hd, theta = 128, 500000.0
+    f = O.rope_inv_freq(hd, theta)
+    g = O.rope_inv_freq(hd, theta, SCALING)
+    w = 2 * np.pi / f
+    L = SCALING["original_max_position"]
+    hi, lo = w < L / 4.0, w > L / 1.0
+    assert hi.any() and lo.any() and (~hi & ~lo).any()       # all three regimes occur at this shape
+    assert np.array_equal(g[hi], f[hi])                       # short wavelengths untouched
+    assert np.allclose(g[lo], f[lo] / 8.0, rtol=0, atol=0)    # long wavelengths divided by the factor
+    mid = ~hi & ~lo
+    # in between, the ratio g / f falls from 1 towards 1 / factor as the wavelength grows
+    r = g / f
+    assert np.all((r[mid] < 1.0) & (r[mid] > 1.0 / 8.0))
+    assert np.all(np.diff(r) <= 0)
+    # the interpolation weight is affine in 1 / wavelength: r = 1/8 + (7/8) s with
+    # s = (L / w - 1) / 3, so (r - 1/8) * w is affine in w ... checked through
+    # three mid-band points (collinearity of (1/w, r))
+    x, y = 1.0 / w[mid], r[mid]
+    if len(x) >= 3:
+        slope = (y[1:] - y[:-1]) / (x[1:] - x[:-1])
+        assert np.allclose(slope, slope[0], rtol=1e-9)
+    # scaled frequencies are still decreasing in j (wavelengths increasing)
+    assert np.all(np.diff(g) < 0)
+
+
+def test_rope_scaling_factor_one_is_identity():
+    hd, theta = 64, 10000.0
+    ident = dict(SCALING, factor=1.0)
+    assert np.allclose(O.rope_inv_freq(hd, theta, ident), O.rope_inv_freq(hd, theta), rtol=1e-15, atol=0)
+    # no scaling dict: exactly the unscaled angles
+    c0, s0 = O.rope_tables(np.arange(5), hd, theta, np.float64)
+    c1, s1 = O.rope_tables(np.arange(5), hd, theta, np.float64, None)
+    assert np.array_equal(c0, c1) and np.array_equal(s0, s1)
