@@ -110,6 +110,18 @@ typedef struct {
   int32_t strict_boundary;    /* 0: first ladder module reads x_b; 1: reads x_{b-1} */
   int32_t weight_dtype;       /* storage of weights and prefill tensor-core operands:
                                  LADDER_DTYPE_BF16 or LADDER_DTYPE_F16 */
+  /* Rotary frequency scaling (Llama-3.1 checkpoints; the official code's
+   * apply_rope_scaling, named in the paper's codewithpapers record).  Off when
+   * rope_scale_factor <= 1 (all four fields zero).  Otherwise, with f_j =
+   * rope_theta^(-2j/head_dim), wavelength w = 2 pi / f_j and L =
+   * rope_original_max_pos: f_j stays when w < L / rope_high_freq_factor, becomes
+   * f_j / rope_scale_factor when w > L / rope_low_freq_factor, and in between
+   * (1 - s) f_j / rope_scale_factor + s f_j with s = (L / w - low) / (high - low).
+   * Requires 0 < rope_low_freq_factor < rope_high_freq_factor and L > 0. */
+  float rope_scale_factor;
+  float rope_low_freq_factor;
+  float rope_high_freq_factor;
+  int32_t rope_original_max_pos;
 } ladder_config;
 
 /* Shard mode (shard_k = k > 1) stands in, on one GPU, for the tensor-parallel

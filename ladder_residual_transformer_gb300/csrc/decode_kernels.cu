@@ -1056,21 +1056,30 @@ cudaError_t launch_advance(int* seq_lens, int B, cudaStream_t s, bool pdl) {
 }
 
 // cos/sin of p * theta^(-2j/hd), formed in double precision and rounded once.
-__global__ void rope_table_kernel(float* c, float* sn, int max_seq, int hd, double theta) {
+__global__ void rope_table_kernel(float* c, float* sn, int max_seq, int hd, double theta, RopeScaling sc) {
   const int half = hd / 2;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (long long)max_seq * half) return;
   const int p = (int)(idx / half), j = (int)(idx % half);
-  const double inv = pow(theta, -2.0 * (double)j / (double)hd);
+  double inv = pow(theta, -2.0 * (double)j / (double)hd);
+  if (sc.factor > 1.0) {  // Llama-3.1 frequency scaling by wavelength band
+    const double w = 2.0 * 3.14159265358979323846 / inv, L = sc.original_max_pos;
+    if (w > L / sc.low_freq_factor) {
+      inv = inv / sc.factor;
+    } else if (w >= L / sc.high_freq_factor) {
+      const double s = (L / w - sc.low_freq_factor) / (sc.high_freq_factor - sc.low_freq_factor);
+      inv = (1.0 - s) * inv / sc.factor + s * inv;
+    }
+  }
   const double a = (double)p * inv;
   c[idx] = (float)cos(a);
   sn[idx] = (float)sin(a);
 }
 
-cudaError_t launch_rope_tables(float* cos_t, float* sin_t, int max_seq, int hd, float theta,
+cudaError_t launch_rope_tables(float* cos_t, float* sin_t, int max_seq, int hd, float theta, RopeScaling sc,
                                cudaStream_t s) {
   const long long n = (long long)max_seq * (hd / 2);
-  rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(cos_t, sin_t, max_seq, hd, (double)theta);
+  rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(cos_t, sin_t, max_seq, hd, (double)theta, sc);
   return cudaGetLastError();
 }
 

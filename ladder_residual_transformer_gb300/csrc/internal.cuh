@@ -229,7 +229,11 @@ cudaError_t launch_sample(const float* logits, int B, int V, float temperature, 
 cudaError_t launch_argmax(const float* logits, int B, int V, float* part_v, int* part_i, int nblk,
                           int* out, cudaStream_t s, bool pdl = false);
 cudaError_t launch_advance(int* seq_lens, int B, cudaStream_t s, bool pdl = false);
-cudaError_t launch_rope_tables(float* cos_t, float* sin_t, int max_seq, int hd, float theta,
+// Rotary frequency scaling by wavelength band (off when factor <= 1).
+struct RopeScaling {
+  double factor, low_freq_factor, high_freq_factor, original_max_pos;
+};
+cudaError_t launch_rope_tables(float* cos_t, float* sin_t, int max_seq, int hd, float theta, RopeScaling sc,
                                cudaStream_t s);
 
 // Prefill launches take `pdl` (programmatic dependent launch); every kernel

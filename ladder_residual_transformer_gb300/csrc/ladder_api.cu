@@ -123,6 +123,11 @@ int validate_config(const ladder_config* c) {
   if (c->vocab <= 0 || c->vocab % 2) return fail(LADDER_ERR_INVALID, "vocab=%d must be positive and even", c->vocab);
   if (!(c->rope_theta > 1.0f) || !std::isfinite(c->rope_theta))
     return fail(LADDER_ERR_INVALID, "rope_theta must be finite and > 1");
+  if (c->rope_scale_factor > 1.0f &&
+      (!std::isfinite(c->rope_scale_factor) || !(c->rope_low_freq_factor > 0.0f) ||
+       !(c->rope_high_freq_factor > c->rope_low_freq_factor) || !std::isfinite(c->rope_high_freq_factor) ||
+       c->rope_original_max_pos <= 0))
+    return fail(LADDER_ERR_INVALID, "rope scaling needs 0 < low_freq_factor < high_freq_factor and original_max_pos > 0");
   if (!(c->norm_eps > 0.0f) || !std::isfinite(c->norm_eps)) return fail(LADDER_ERR_INVALID, "norm_eps must be > 0");
   if (c->rope_interleaved != 1)
     return fail(LADDER_ERR_UNSUPPORTED, "only interleaved rotary pairs (rope_interleaved=1) are implemented");
@@ -427,7 +432,10 @@ int ladder_create(const ladder_config* cfg, const ladder_weights* w, void* works
     if (plan.sk_bytes[i]) e = cudaMemsetAsync(m->ws + plan.sk[i], 0, plan.sk_bytes[i], stream);
   if (e == cudaSuccess)
     e = launch_rope_tables(m->at<float>(plan.rope_cos), m->at<float>(plan.rope_sin), cfg->max_seq, cfg->head_dim,
-                           cfg->rope_theta, stream);
+                           cfg->rope_theta,
+                           RopeScaling{cfg->rope_scale_factor, cfg->rope_low_freq_factor, cfg->rope_high_freq_factor,
+                                       (double)cfg->rope_original_max_pos},
+                           stream);
   if (e != cudaSuccess) {
     ladder_destroy(m);
     return fail(LADDER_ERR_CUDA, "ladder_create: %s", cudaGetErrorString(e));

@@ -41,7 +41,9 @@ class Config(ctypes.Structure):
         "n_layers", "n_standard_layers", "d_model", "n_q_heads", "n_kv_heads", "head_dim", "ffn_dim", "vocab")] + [
         ("rope_theta", ctypes.c_float), ("norm_eps", ctypes.c_float)] + [(n, ctypes.c_int32) for n in (
             "tie_embeddings", "rope_interleaved", "shard_k", "page_size", "max_batch", "max_seq",
-            "max_prefill_tokens", "strict_boundary", "weight_dtype")]
+            "max_prefill_tokens", "strict_boundary", "weight_dtype")] + [
+        ("rope_scale_factor", ctypes.c_float), ("rope_low_freq_factor", ctypes.c_float),
+        ("rope_high_freq_factor", ctypes.c_float), ("rope_original_max_pos", ctypes.c_int32)]
 
 
 class Weights(ctypes.Structure):
@@ -123,7 +125,16 @@ def make_config(dims: dict, *, max_batch: int, max_seq: int, max_prefill_tokens:
         tie_embeddings=dims.get("tie_embeddings", 0), rope_interleaved=dims.get("rope_interleaved", 1),
         shard_k=shard_k, page_size=page_size, max_batch=max_batch, max_seq=max_seq,
         max_prefill_tokens=max_prefill_tokens if max_prefill_tokens is not None else max_batch * max_seq,
-        strict_boundary=strict_boundary, weight_dtype=DTYPES[dtype])
+        strict_boundary=strict_boundary, weight_dtype=DTYPES[dtype],
+        **_rope_scaling_fields(dims.get("rope_scaling")))
+
+
+def _rope_scaling_fields(sc: dict | None) -> dict:
+    if not sc:
+        return {}
+    return dict(rope_scale_factor=float(sc["factor"]), rope_low_freq_factor=float(sc["low_freq_factor"]),
+                rope_high_freq_factor=float(sc["high_freq_factor"]),
+                rope_original_max_pos=int(sc["original_max_position"]))
 
 
 def query_sizes(cfg: Config) -> tuple[int, int]:

@@ -28,7 +28,8 @@ def _oracle_weights_cached(key):
 
 def oracle_weights(dims, transform=None, keep_layers=True):
     if transform is None and keep_layers:
-        return _oracle_weights_cached(tuple(sorted(dims.items())))
+        # the weights depend on the shapes only (not on e.g. the rotary scaling)
+        return _oracle_weights_cached(tuple(sorted((k, v) for k, v in dims.items() if not isinstance(v, dict))))
     return O.synthetic_weights(dims, transform=transform, keep_layers=keep_layers)
 
 

@@ -65,6 +65,23 @@ def test_invalid_configs_are_rejected_on_the_host(field, value, code):
     assert ladder.lib().ladder_last_error()
 
 
+@pytest.mark.parametrize("fields", [
+    dict(rope_scale_factor=8.0, rope_low_freq_factor=4.0, rope_high_freq_factor=1.0, rope_original_max_pos=8192),
+    dict(rope_scale_factor=8.0, rope_low_freq_factor=0.0, rope_high_freq_factor=4.0, rope_original_max_pos=8192),
+    dict(rope_scale_factor=8.0, rope_low_freq_factor=1.0, rope_high_freq_factor=4.0, rope_original_max_pos=0),
+])
+def test_invalid_rope_scaling_is_rejected(fields):
+    with pytest.raises(ladder.LadderError) as e:
+        ladder.query_sizes(cfg(**fields))
+    assert e.value.code == ladder.LADDER_ERR_INVALID
+
+
+def test_rope_scaling_off_and_valid_configs_are_accepted():
+    ladder.query_sizes(cfg(rope_scale_factor=1.0))
+    ladder.query_sizes(cfg(rope_scale_factor=8.0, rope_low_freq_factor=1.0, rope_high_freq_factor=4.0,
+                           rope_original_max_pos=8192))
+
+
 def test_null_arguments_are_rejected_without_a_device():
     L = ladder.lib()
     out = ctypes.c_void_p()

@@ -461,3 +461,24 @@ def test_launch_timeline(shard_k):
     for stream_id in (0, 1):
         starts = [t0 for st, _, t0, _ in rows if st == stream_id]
         assert starts == sorted(starts)
+
+
+def test_rope_scaling_matches_oracle():
+    """Llama-3.1 rotary frequency scaling with the original context set so that
+    the tiny model's 32 frequencies fall in all three bands (kept, interpolated,
+    divided by the factor); prefill of two ragged prompts and three decode steps."""
+    sc = {"factor": 8.0, "low_freq_factor": 1.0, "high_freq_factor": 4.0, "original_max_position": 64}
+    dims = small_dims(rope_scaling=sc)
+    f = O.rope_inv_freq(dims["head_dim"], dims["rope_theta"])
+    w = 2 * np.pi / f
+    assert (w < 16).any() and (w > 64).any() and ((w >= 16) & (w <= 64)).any()
+    gw, ow = gpu_weights(dims), oracle_weights(dims)
+    prompts = prompts_for([40, 23], dims["vocab"])
+    feed = np.stack([synth.tokens(3, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(2)])
+    model = make_model(dims, gw, max_batch=2, max_seq=64, page_size=16)
+    g_logits, _ = run_teacher_forced(model, prompts, feed)
+    o_logits, _ = O.teacher_forced_decode(dims, ow, prompts, feed)
+    for s_ in range(4):
+        compare_logits(g_logits[s_], o_logits[s_], f"rope scaling step {s_}")
+    plain = O.teacher_forced_decode(dict(dims, rope_scaling=None), ow, prompts, feed)[0]
+    assert np.abs(plain - o_logits).max() > 1e-3  # the scaling changes the model
