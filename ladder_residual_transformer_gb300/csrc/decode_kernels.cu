@@ -386,6 +386,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
 // epilogue.  Each CTA thus reads a small slice of the inputs, not all of them.
 // ---------------------------------------------------------------------------
 constexpr int GM_KL_MAX = 2048;  // longest K slice (staged 16-bit columns)
+constexpr int GM_PF_AHEAD = 2;   // 128-column steps of weights requested ahead of use
 
 template <typename T>
 __device__ __forceinline__ void mma16816_f32(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -451,12 +452,16 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_splitk_kernel(const GemvPar
   int kind, local, koff;
   gemv_task_rows<WT, MODE>(p, lane_active ? task : 0, row0, row1, kind, local, koff);
   pdl_trigger();
-  // Weights depend on no earlier kernel: ask L2 for this warp's slab before waiting.
+  // Weights depend on no earlier kernel: the L2 is asked for the first
+  // GM_PF_AHEAD 128-column steps of this warp's rows before the wait, and for
+  // step i + GM_PF_AHEAD at step i (a window: the whole slab of a large matrix
+  // would not stay in L2 until it is read).  Lane (gi, ti) takes one of the
+  // four 128-byte lines of its row pair per step.
+  const WT* pf_row = (ti >> 1) ? row1 : row0;
+  const int pf_off = k0 + (ti & 1) * 64;
   if (wtask < n_wtasks)
-    for (int k = lane * 64; k < kl; k += 32 * 64) {
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(row0 + k0 + k));
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(row1 + k0 + k));
-    }
+    for (int i = 0; i < GM_PF_AHEAD && i * 128 < kl; ++i)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(pf_row + pf_off + i * 128));
   pdl_wait();
 
   // 1. Stage x * g for rows 0..15 of this slice (zero rows past B) and the
@@ -503,6 +508,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_splitk_kernel(const GemvPar
     const WT* x1 = xs + (gi + 8) * ld + 8 * ti;  // batch row gi + 8 (n tile 1)
     int k = 0;
     for (; k + 96 < kl; k += 128) {
+      if (k + GM_PF_AHEAD * 128 < kl) asm volatile("prefetch.global.L2 [%0];" ::"l"(pf_row + pf_off + k + GM_PF_AHEAD * 128));
       uint4 wa[4], wb[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
