@@ -447,6 +447,8 @@ def main():
     ap.add_argument("--no-pdl", action="store_true", help="decode without programmatic dependent launch")
     ap.add_argument("--eager", action="store_true", help="decode without CUDA-graph replay")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="cut the workload to this many layers (for kernel captures; the line names the count)")
     ap.add_argument("--no-schedules", action="store_true",
                     help="skip timing the standard and parallel-block schedules on the same weights")
     ap.add_argument("--cpu-prompt", type=int, default=None, help="oracle sample prompt (default: the workload's)")
@@ -455,6 +457,10 @@ def main():
     ap.add_argument("--ref-decode", type=int, default=4)
     args = ap.parse_args()
     dims = dict(synth.PRESETS[args.workload])
+    if args.layers:
+        # kernel captures on a shallow copy of the workload (every layer has the same shapes)
+        dims["n_layers"] = args.layers
+        dims["n_standard_layers"] = min(dims["n_standard_layers"], args.layers // 2)
     run = synth.RUNS[args.workload]
     if args.prompt is None:
         args.prompt = run["prompt"]
