@@ -40,8 +40,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel source is unchanged (sha256 of the file that defines it).
 NCU_TRAFFIC = {  # profiles/gemv_gateup_1p2b_traffic.md (mean of the two captured launches)
     "source": "ladder_residual_transformer_gb300/csrc/decode_kernels.cu",
-    "sha256": "7e5e7425c3d4e6e9aa964ce389a62821fe52ada7bfc9c44676086a02a1dbf9dd",
-    "bytes_per_launch": 67308672,
+    "sha256": "68c11402b3e9ee869e1b8d36051b2bca5f41863760ce8a3827319d1953c7d357",
+    "bytes_per_launch": 67294464,
 }
 
 
