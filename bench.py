@@ -40,8 +40,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel source is unchanged (sha256 of the file that defines it).
 NCU_TRAFFIC = {  # profiles/gemv_gateup_1p2b_traffic.md (mean of the two captured launches)
     "source": "ladder_residual_transformer_gb300/csrc/decode_kernels.cu",
-    "sha256": "68c11402b3e9ee869e1b8d36051b2bca5f41863760ce8a3827319d1953c7d357",
-    "bytes_per_launch": 67294464,
+    "sha256": "4b1c34c7aca74415b647445cc24c5b1a95a5f5f415b4969b59c76653d08455b1",
+    "bytes_per_launch": 67251712,
 }
 
 

@@ -893,10 +893,43 @@ __global__ void __launch_bounds__(HD) attn_combine_kernel(const AttnDecodeParams
   pdl_trigger();
   pdl_wait();
   const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+  const size_t base = ((size_t)b * p.n_q + h) * p.nsplit;
+  constexpr int CB = 16;
+  if (p.nsplit <= CB) {
+    // Every partial is requested at once, together with the length (one memory
+    // round trip); splits past the context are masked by selection, and the
+    // arithmetic is that of the loop below, in the same order.
+    float m[CB], l[CB], o[CB];
+#pragma unroll
+    for (int s = 0; s < CB; ++s) {
+      if (s < p.nsplit) {
+        m[s] = p.part_ml[(base + s) * 2];
+        l[s] = p.part_ml[(base + s) * 2 + 1];
+        o[s] = p.part_o[(base + s) * HD + d];
+      }
+    }
+    const int ctx = p.seq_lens[b] + 1;
+    int ns = (ctx + p.split_len - 1) / p.split_len;
+    if (ns > p.nsplit) ns = p.nsplit;
+    float M = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < CB; ++s)
+      if (s < ns) M = fmaxf(M, m[s]);
+    float L = 0.f, acc = 0.f;
+#pragma unroll
+    for (int s = 0; s < CB; ++s) {
+      if (s < ns) {
+        const float w = __expf(m[s] - M);
+        L += w * l[s];
+        acc += w * o[s];
+      }
+    }
+    p.out[(size_t)b * p.n_q * HD + (size_t)h * HD + d] = acc / L;
+    return;
+  }
   const int ctx = p.seq_lens[b] + 1;
   int ns = (ctx + p.split_len - 1) / p.split_len;
   if (ns > p.nsplit) ns = p.nsplit;
-  const size_t base = ((size_t)b * p.n_q + h) * p.nsplit;
   float M = -INFINITY;
   for (int s = 0; s < ns; ++s) M = fmaxf(M, p.part_ml[(base + s) * 2]);
   float L = 0.f, acc = 0.f;
