@@ -40,8 +40,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel source is unchanged (sha256 of the file that defines it).
 NCU_TRAFFIC = {  # profiles/gemv_gateup_1p2b_traffic.md (mean of the two captured launches)
     "source": "ladder_residual_transformer_gb300/csrc/decode_kernels.cu",
-    "sha256": "4b1c34c7aca74415b647445cc24c5b1a95a5f5f415b4969b59c76653d08455b1",
-    "bytes_per_launch": 67251712,
+    "sha256": "64a10bb4198afd08bbb2f08c6a701a9eee869507690fd652fcfb0c7ff7ffbffc",
+    "bytes_per_launch": 67258112,
 }
 
 

@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
 }
 
 // ---------------------------------------------------------------------------
-// Batched decode projection, 5..16 rows, on the tensor cores.  The GEMV above
+// Batched decode projection, 3..16 rows, on the tensor cores.  The GEMV above
 // streams every weight byte once per 4 rows; here mma.sync m16n8k16 takes the
 // weights as the M = 16 operand and the batch as N (two 8-wide tiles), so each
 // weight byte is streamed once for all 16 rows.
@@ -667,7 +667,10 @@ static cudaError_t gemv_dispatch_bt(const GemvParams& p, int bt, int mode, int g
 // Batches of 1..4 rows run on the CUDA-core GEMV; larger batches run on the
 // tensor-core kernel in chunks of 16 rows (shard partials stay on the GEMV, in
 // chunks of 4).
-static bool gemv_use_mma(int B, int mode) { return B > 4 && mode != GEMV_PARTIAL; }
+// From three rows on, the tensor-core projection (weights streamed once for up
+// to 16 rows) beats the GEMV's batch tile of 4 (8B hybrid, graph decode step:
+// B = 3 608 vs 561 tok/s, B = 4 814 vs 713; B = 2 stays on the GEMV, 498 vs 416).
+static bool gemv_use_mma(int B, int mode) { return B > 2 && mode != GEMV_PARTIAL; }
 
 int gemv_launch_count(int B, int K, int mode) { return gemv_use_mma(B, mode) ? (B + 15) / 16 : (B + 3) / 4; }
 

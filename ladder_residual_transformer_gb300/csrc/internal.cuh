@@ -148,7 +148,7 @@ struct GemvParams {
   const float* rope_sin;
   const int* pos;         // position of row b (the sequence length before this step)
   KvLayer kv;
-  // Batched rows (B > 4): split-K workspace of this projection (gemv_splitk_bytes
+  // Batched rows (B > 2): split-K workspace of this projection (gemv_splitk_bytes
   // bytes laid out as partial sums, per-slice sums of squares, group counters;
   // counters zero before the first launch and left zero by every launch).
   float* sk_part;

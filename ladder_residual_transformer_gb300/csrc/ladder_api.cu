@@ -50,7 +50,7 @@ namespace {
 constexpr int kSplitLen = 128;      // keys per decode-attention split
 constexpr int kArgmaxBlocks = 64;   // partial argmax blocks per sequence
 
-// Split-K workspace of the batched decode projections (B > 4), one region per
+// Split-K workspace of the batched decode projections (B > 2), one region per
 // projection kind so that the two decode streams never share one.
 enum SplitKKind { SK_QKV = 0, SK_OUT = 1, SK_GATEUP = 2, SK_DOWN = 3, SK_LMHEAD = 4, SK_KINDS = 5 };
 
@@ -91,7 +91,7 @@ Plan make_plan(const ladder_config& c) {
   p.xlast = take(Bm * d * 4);
   p.err = take(256);
   p.shard = c.shard_k > 1 ? take(2 * Bm * c.shard_k * d * 4) : 0;  // double-buffered shard partials [B][k][d]
-  if (c.max_batch > 4) {
+  if (c.max_batch > 2) {  // batched decode projections (3 rows and more) split K across CTAs
     const size_t kvd = (size_t)c.n_kv_heads * c.head_dim;
     const int nt[SK_KINDS] = {(int)((qd + 2 * kvd) / 2), (int)(d / 2), (int)f, (int)(d / 2), c.vocab / 2};
     const int kk[SK_KINDS] = {(int)d, (int)qd, (int)d, (int)f, (int)d};

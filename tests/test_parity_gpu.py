@@ -191,11 +191,11 @@ def test_prefill_repeats_bitwise():
         assert np.array_equal(r, g_logits)
 
 
-@pytest.mark.parametrize("B", [16, 21])
+@pytest.mark.parametrize("B", [3, 4, 16, 21])
 def test_batched_decode_on_tensor_cores(B):
-    """Decode batches above 4 rows run on the mma.sync projection in chunks of 16
-    rows (21 = 16 + 5); the down projection (K = 3072) stages its input in two
-    chunks, the QKV projection writes rotated K/V for every row."""
+    """Decode batches of 3 rows and more run on the mma.sync projection in chunks
+    of 16 rows (21 = 16 + 5); the down projection (K = 3072) stages its input in
+    two chunks, the QKV projection writes rotated K/V for every row."""
     dims = small_dims(d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=3072, vocab=2048,
                       n_layers=2, n_standard_layers=0)
     gw, ow = gpu_weights(dims), oracle_weights(dims)
