@@ -35,8 +35,12 @@
  * and released by the matching *_destroy call.
  *
  * Streams.  Every device-side call is asynchronous on the stream given
- * (a cudaStream_t, 0 = legacy default stream).  A model and its KV handle must
- * not be used from two streams at once.
+ * (a cudaStream_t, 0 = legacy default stream).  Prefill and decode also use a
+ * second stream owned by the model (the MLP chain of ladder layers, or the
+ * shard reduces), forked from and joined back into the given stream by events
+ * within the call, so all of a call's work is ordered before later work on the
+ * given stream.  A model and its KV handle must not be used from two streams
+ * at once.
  *
  * Errors.  Every int-returning call returns LADDER_OK (0) or a negative code.
  * Arguments are validated on the host before anything is launched, so a call
@@ -226,8 +230,9 @@ int32_t ladder_kv_seq_len(const ladder_kv* kv, int32_t b);
  * [B].  Writes every position's K/V into the cache, sets seq_lens[b] =
  * host_lens[b], and writes the last position's logits to `logits` (device fp32
  * [B, vocab]) and, if `next_tok` is not NULL, the greedy tokens (device int32
- * [B]).  Fails with LADDER_ERR_CAPACITY when a sequence exceeds its assigned
- * pages or max_seq, or the packed total exceeds max_prefill_tokens. */
+ * [B]) (or sampled ones, see ladder_set_sampling).  Fails with
+ * LADDER_ERR_CAPACITY when a sequence exceeds its assigned pages or max_seq,
+ * or the packed total exceeds max_prefill_tokens. */
 int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tokens, const int32_t* host_lens,
                    int32_t B, float* logits, int32_t* next_tok, ladder_stream_t stream);
 
