@@ -92,3 +92,11 @@ def test_null_arguments_are_rejected_without_a_device():
     assert L.ladder_prefill(None, None, None, None, 1, None, None, None) == ladder.LADDER_ERR_INVALID
     assert L.ladder_kv_seq_len(None, 0) == -1
     assert L.ladder_last_launch_count(None) == -1
+    # entry points added with the sampler, the schedules and the tracing aids
+    assert L.ladder_set_sampling(None, 1.0, 0, 0) == ladder.LADDER_ERR_INVALID
+    assert L.ladder_set_mode(None, 2, 0) == ladder.LADDER_ERR_INVALID
+    assert L.ladder_sample(None, 1, 10, 1.0, 0, 0, None, 0, None, None) == ladder.LADDER_ERR_INVALID
+    n = ctypes.c_int32(0)
+    assert L.ladder_timeline_begin(None, 16, None) == ladder.LADDER_ERR_INVALID
+    assert L.ladder_timeline_end(None, 0, ctypes.byref(n), None, None, None, None) == ladder.LADDER_ERR_INVALID
+    assert L.ladder_probe_begin(None, 0, 16) == ladder.LADDER_ERR_INVALID
