@@ -35,11 +35,11 @@
  * and released by the matching *_destroy call.
  *
  * Streams.  Every device-side call is asynchronous on the stream given
- * (a cudaStream_t, 0 = legacy default stream).  Prefill and decode also use a
- * second stream owned by the model (the MLP chain of ladder layers, or the
- * shard reduces), forked from and joined back into the given stream by events
- * within the call, so all of a call's work is ordered before later work on the
- * given stream.  A model and its KV handle must not be used from two streams
+ * (a cudaStream_t, 0 = legacy default stream).  Decode also uses a second
+ * stream owned by the model (the MLP chain of ladder layers, or the shard
+ * reduces), forked from and joined back into the given stream by events within
+ * the call, so all of a call's work is ordered before later work on the given
+ * stream.  A model and its KV handle must not be used from two streams
  * at once.
  *
  * Errors.  Every int-returning call returns LADDER_OK (0) or a negative code.

@@ -55,7 +55,7 @@ constexpr int kArgmaxBlocks = 64;   // partial argmax blocks per sequence
 enum SplitKKind { SK_QKV = 0, SK_OUT = 1, SK_GATEUP = 2, SK_DOWN = 3, SK_LMHEAD = 4, SK_KINDS = 5 };
 
 struct Plan {
-  size_t x[3], xn, xn2, q, ao, act, part_o, part_ml, am_v, am_i, rope_cos, rope_sin, meta, xlast, err, shard;
+  size_t x[3], xn, q, ao, act, part_o, part_ml, am_v, am_i, rope_cos, rope_sin, meta, xlast, err, shard;
   size_t sk[SK_KINDS], sk_bytes[SK_KINDS];
   size_t total;
   int m_max, m_pad, nsplit_max;
@@ -78,7 +78,6 @@ Plan make_plan(const ladder_config& c) {
   };
   for (int i = 0; i < 3; ++i) p.x[i] = take(M * d * 4);
   p.xn = take(Mp * d * 2);
-  p.xn2 = take(Mp * d * 2);  // the second prefill stream's normalised rows
   p.q = take(std::max(Mp * qd * 2, Bm * qd * 4));
   p.ao = take(std::max(Mp * qd * 2, Bm * qd * 4));
   p.act = take(std::max(Mp * f * 2, Bm * f * 4));
@@ -184,7 +183,7 @@ struct ladder_model {
   int wdt;  // weight dtype
   std::vector<LayerW> layers;
   std::vector<LayerMaps> maps;
-  TmaOperand map_xn, map_xn2, map_ao, map_act;  // activation operands, m_pad rows
+  TmaOperand map_xn, map_ao, map_act;  // activation operands, m_pad rows
   CUtensorMap map_q;  // rotated queries [m_pad][n_q * hd], the prefill attention operand
   CUtensorMap map_x[3];   // stream buffers [m_max][d] fp32, epilogue blocks (prefill residual GEMMs)
   CUtensorMap map_act_st; // SwiGLU rows [m_pad][ffn], epilogue blocks (prefill gate/up GEMM)
@@ -392,7 +391,6 @@ int ladder_create(const ladder_config* cfg, const ladder_weights* w, void* works
     const uint64_t f = c.ffn_dim, Mp = plan.m_pad;
     const int wdt = c.weight_dtype;
     bool ok = make_tma_operand(&m->map_xn, m->ws + plan.xn, Mp, d, wdt) &&
-              make_tma_operand(&m->map_xn2, m->ws + plan.xn2, Mp, d, wdt) &&
               make_tma_operand(&m->map_ao, m->ws + plan.ao, Mp, qd, wdt) &&
               make_tma_operand(&m->map_act, m->ws + plan.act, Mp, f, wdt) &&
               make_tma_map(&m->map_q, m->ws + plan.q, Mp, qd, wdt) &&
@@ -1013,6 +1011,7 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
 
   const int d = c.d_model, qd = c.n_q_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim, f = c.ffn_dim;
   const int wdt = m->wdt;
+  void* xn = m->ws + P.xn;    // normalised rows, weight dtype
   void* qb = m->ws + P.q;     // rotated queries, weight dtype
   void* aob = m->ws + P.ao;   // attention output, weight dtype
   void* actb = m->ws + P.act; // SwiGLU output, weight dtype
@@ -1020,86 +1019,44 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
   // each one is launched early and its prologue overlaps the previous tail.
   const bool pdl = !(m->flags & LADDER_FLAG_NO_PDL);
 
-  // Two streams, as in decode: the MLP modules of ladder layers run on the
-  // second stream (their input x_{k-2} does not wait for the attention module
-  // before them), each stream with its own normalised-row buffer; a kernel
-  // that reads a stream buffer written on the other stream waits for its event.
-  const int nstd = m->residual_mode == LADDER_RESIDUAL_STANDARD ? c.n_layers
-                   : m->residual_mode == LADDER_RESIDUAL_PARALLEL ? 0
-                                                                  : c.n_standard_layers;
-  cudaStream_t streams[2] = {s, m->aux};
-  void* xns[2] = {m->ws + P.xn, m->ws + P.xn2};
-  const TmaOperand* map_xns[2] = {&m->map_xn, &m->map_xn2};
-  int writer[3] = {0, 0, 0};
-  bool forked = false;
-  auto use = [&](int buf, int si) -> int {
-    const int b3 = buf % 3;
-    if (writer[b3] == si) return LADDER_OK;
-    if (si == 1 && !forked) {
-      CUDA_TRY(cudaEventRecord(m->ev_fork, s));
-      CUDA_TRY(cudaStreamWaitEvent(m->aux, m->ev_fork, 0));
-      forked = true;
-    }
-    CUDA_TRY(cudaStreamWaitEvent(streams[si], m->ev_slot[b3], 0));
-    return LADDER_OK;
-  };
-  auto wrote = [&](int buf, int si) -> int {
-    writer[buf % 3] = si;
-    CUDA_TRY(cudaEventRecord(m->ev_slot[buf % 3], streams[si]));
-    return LADDER_OK;
-  };
-  int rc;
-
   LAUNCH(launch_embed(tokens, M, m->embed, wdt, d, c.vocab, m->X(0), m->err(), s, pdl), 1);
-  if ((rc = wrote(0, 0))) return rc;
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerW& L = m->layers[l];
     const LayerMaps& T = m->maps[l];
     const KvLayer kvl = kv->layer(l);
     {
-      const int k = 2 * l + 1;  // attention module: caller's stream
-      const int j = m->input_index(k);
-      if ((rc = use(j, 0))) return rc;
-      LAUNCH(launch_rmsnorm_rows(m->X(j), M, d, L.attn_norm, c.norm_eps, xns[0], wdt, s, pdl), 1);
+      const int k = 2 * l + 1;
+      LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.attn_norm, c.norm_eps, xn, wdt, s, pdl), 1);
       GemmParams g{};
       g.M = M; g.N = qd + 2 * kvd; g.K = d;
       g.out_h = qb; g.ldo = qd; g.nq_hd = qd; g.nkv_hd = kvd;
       g.rope_cos = m->at<float>(P.rope_cos); g.rope_sin = m->at<float>(P.rope_sin);
       g.row_b = d_row_b; g.row_pos = d_row_pos; g.kv = kvl;
-      LAUNCH(launch_gemm_tc(map_xns[0], &T.wq, &T.wk, &T.wv, nullptr, nullptr, g, GEMM_QKV, wdt, m->num_sms, m->err(), s, pdl), 1);
+      LAUNCH(launch_gemm_tc(&m->map_xn, &T.wq, &T.wk, &T.wv, nullptr, nullptr, g, GEMM_QKV, wdt, m->num_sms, m->err(), s, pdl), 1);
 
       AttnPrefillParams a{};
       a.q = qb; a.kv = kvl; a.seq_start = d_start; a.seq_len = d_lens;
       a.n_q = c.n_q_heads; a.scale = 1.0f / sqrtf((float)c.head_dim); a.out = aob;
       LAUNCH(launch_attn_prefill_tcgen05(&m->map_q, &kv->maps[l], a, c.head_dim, wdt, B, max_len, m->err(), s, pdl), 1);
 
-      if ((rc = use(k - 1, 0))) return rc;
       GemmParams o{};
       o.M = M; o.N = d; o.K = qd; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);
       LAUNCH(launch_gemm_tc(&m->map_ao, &T.wo, nullptr, nullptr, &m->map_x[(k - 1) % 3], &m->map_x[k % 3], o,
                             GEMM_RESID, wdt, m->num_sms, m->err(), s, pdl), 1);
-      if ((rc = wrote(k, 0))) return rc;
     }
     {
-      const int k = 2 * l + 2;  // MLP module: second stream in ladder layers
-      const int si = l < nstd ? 0 : 1;
-      cudaStream_t ms = streams[si];
-      const int j = m->input_index(k);
-      if ((rc = use(j, si))) return rc;
-      LAUNCH(launch_rmsnorm_rows(m->X(j), M, d, L.mlp_norm, c.norm_eps, xns[si], wdt, ms, pdl), 1);
+      const int k = 2 * l + 2;
+      LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.mlp_norm, c.norm_eps, xn, wdt, s, pdl), 1);
       GemmParams g{};
       g.M = M; g.N = f; g.K = d; g.out_h = actb; g.ldo = f;
-      LAUNCH(launch_gemm_tc(map_xns[si], &T.gate, &T.up, nullptr, nullptr, &m->map_act_st, g, GEMM_GATEUP, wdt,
-                            m->num_sms, m->err(), ms, pdl), 1);
-      if ((rc = use(k - 1, si))) return rc;
+      LAUNCH(launch_gemm_tc(&m->map_xn, &T.gate, &T.up, nullptr, nullptr, &m->map_act_st, g, GEMM_GATEUP, wdt,
+                            m->num_sms, m->err(), s, pdl), 1);
       GemmParams o{};
       o.M = M; o.N = d; o.K = f; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);
       LAUNCH(launch_gemm_tc(&m->map_act, &T.down, nullptr, nullptr, &m->map_x[(k - 1) % 3], &m->map_x[k % 3], o,
-                            GEMM_RESID, wdt, m->num_sms, m->err(), ms, pdl), 1);
-      if ((rc = wrote(k, si))) return rc;
+                            GEMM_RESID, wdt, m->num_sms, m->err(), s, pdl), 1);
     }
   }
-  if ((rc = use(2 * c.n_layers, 0))) return rc;
   float* xlast = m->at<float>(P.xlast);
   LAUNCH(launch_gather_rows(m->X(2 * c.n_layers), d, d_last, B, xlast, s, pdl), 1);
   GemvParams h{};
