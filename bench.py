@@ -40,8 +40,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel source is unchanged (sha256 of the file that defines it).
 NCU_TRAFFIC = {  # profiles/gemv_gateup_1p2b_traffic.md (mean of the two captured launches)
     "source": "ladder_residual_transformer_gb300/csrc/decode_kernels.cu",
-    "sha256": "64a10bb4198afd08bbb2f08c6a701a9eee869507690fd652fcfb0c7ff7ffbffc",
-    "bytes_per_launch": 67258112,
+    "sha256": "9b1e41e127b124917a06d8b238fa1c5057abf915ac462157c3231eff74ea9e39",
+    "bytes_per_launch": 67253120,
 }
 
 
