@@ -73,7 +73,8 @@ def test_tiny_greedy_tokens_and_logits(tiny):
 
 
 def test_bf16_weights_and_operands():
-    """The bf16 storage variant of every kernel against the oracle."""
+    """The bf16 storage variant of the prefill kernels and the B <= 2 decode
+    kernels against the oracle (the batched projections: the next test)."""
     dims = small_dims()
     ow = oracle_weights(dims)
     lens = [16, 70]
@@ -84,6 +85,22 @@ def test_bf16_weights_and_operands():
     o_logits, _ = O.teacher_forced_decode(dims, ow, prompts, feed)
     for s_ in range(4):
         compare_logits(g_logits[s_], o_logits[s_], f"bf16 step {s_}")
+
+
+def test_bf16_batched_decode_on_tensor_cores():
+    """bf16 storage on the batched (mma.sync, split-K) decode projections: five
+    ragged sequences, prefill and three decode steps."""
+    dims = small_dims(d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=3072, vocab=2048,
+                      n_layers=2, n_standard_layers=0)
+    ow = oracle_weights(dims)
+    lens = [9, 40, 23, 3, 61]
+    prompts = prompts_for(lens, dims["vocab"])
+    feed = np.stack([synth.tokens(3, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(5)])
+    model = make_model(dims, gpu_weights(dims, dtype="bf16"), max_batch=5, max_seq=96, page_size=32)
+    g_logits, _ = run_teacher_forced(model, prompts, feed, graph=True)
+    o_logits, _ = O.teacher_forced_decode(dims, ow, prompts, feed)
+    for s_ in range(4):
+        compare_logits(g_logits[s_], o_logits[s_], f"bf16 batched step {s_}")
 
 
 @pytest.mark.parametrize("graph", [False, True])
