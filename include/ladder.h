@@ -86,7 +86,8 @@ enum {
 /* Flags for ladder_set_mode. */
 enum {
   LADDER_FLAG_DECODE_GRAPH = 1, /* capture each decode step shape in a CUDA graph and replay it */
-  LADDER_FLAG_NO_PDL = 2        /* launch decode kernels without programmatic dependent launch */
+  LADDER_FLAG_NO_PDL = 2,       /* launch decode kernels without programmatic dependent launch */
+  LADDER_FLAG_ALL_LOGITS = 4    /* prefill writes the logits of every position (a debugging aid) */
 };
 
 /* Model dimensions and capacities.  All int32 fields must be positive unless
@@ -232,15 +233,24 @@ int32_t ladder_kv_seq_len(const ladder_kv* kv, int32_t b);
  * [B, vocab]) and, if `next_tok` is not NULL, the greedy tokens (device int32
  * [B]) (or sampled ones, see ladder_set_sampling).  Fails with
  * LADDER_ERR_CAPACITY when a sequence exceeds its assigned pages or max_seq,
- * or the packed total exceeds max_prefill_tokens. */
+ * or the packed total exceeds max_prefill_tokens, and with LADDER_ERR_INVALID
+ * when B is outside 1 .. max_batch or a length is not positive (an empty batch
+ * or an empty prompt); every check runs before the first launch.
+ * With LADDER_FLAG_ALL_LOGITS set, `logits` receives one row per packed token
+ * instead ([sum of host_lens, vocab], in packing order: the lm_head runs over
+ * max_batch rows per launch) and next_tok the greedy token of each sequence's
+ * last row; sampling is not available in that mode (LADDER_ERR_UNSUPPORTED
+ * when a temperature is set and next_tok is not NULL). */
 int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tokens, const int32_t* host_lens,
                    int32_t B, float* logits, int32_t* next_tok, ladder_stream_t stream);
 
 /* One decode step for sequences 0 .. B-1: token tokens[b] (device int32 [B])
  * is placed at position seq_lens[b]; writes logits (device fp32 [B, vocab]),
  * the greedy tokens to next_tok (device int32 [B], may equal `tokens`, may be
- * NULL) and increments every seq_lens[b].  With LADDER_FLAG_DECODE_GRAPH the
- * step is captured once per (B, pointer set) and replayed afterwards. */
+ * NULL) and increments every seq_lens[b].  B outside 1 .. max_batch fails
+ * with LADDER_ERR_INVALID, a full sequence with LADDER_ERR_CAPACITY, before
+ * any launch.  With LADDER_FLAG_DECODE_GRAPH the step is captured once per
+ * (B, pointer set) and replayed afterwards. */
 int ladder_decode_step(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int32_t B,
                        float* logits, int32_t* next_tok, ladder_stream_t stream);
 

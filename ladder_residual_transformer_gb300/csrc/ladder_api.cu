@@ -462,7 +462,8 @@ int ladder_set_mode(ladder_model* m, int residual_mode, int flags) {
   if (residual_mode != LADDER_RESIDUAL_CONFIG && residual_mode != LADDER_RESIDUAL_STANDARD &&
       residual_mode != LADDER_RESIDUAL_PARALLEL)
     return fail(LADDER_ERR_INVALID, "unknown residual mode %d", residual_mode);
-  if (flags & ~(LADDER_FLAG_DECODE_GRAPH | LADDER_FLAG_NO_PDL)) return fail(LADDER_ERR_INVALID, "unknown flags 0x%x", flags);
+  if (flags & ~(LADDER_FLAG_DECODE_GRAPH | LADDER_FLAG_NO_PDL | LADDER_FLAG_ALL_LOGITS))
+    return fail(LADDER_ERR_INVALID, "unknown flags 0x%x", flags);
   if (residual_mode != m->residual_mode || flags != m->flags) m->drop_graphs();
   m->residual_mode = residual_mode;
   m->flags = flags;
@@ -976,6 +977,9 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
   }
   if (total > c.max_prefill_tokens)
     return fail(LADDER_ERR_CAPACITY, "%lld prompt tokens exceed max_prefill_tokens=%d", total, c.max_prefill_tokens);
+  const bool all_rows = (m->flags & LADDER_FLAG_ALL_LOGITS) != 0;
+  if (all_rows && next_tok && m->samp_t > 0.f)
+    return fail(LADDER_ERR_UNSUPPORTED, "sampling is not available with LADDER_FLAG_ALL_LOGITS");
   const int M = (int)total;
   const int Bm = c.max_batch;
   const Plan& P = m->plan;
@@ -1057,13 +1061,32 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
                             GEMM_RESID, wdt, m->num_sms, m->err(), s, pdl), 1);
     }
   }
-  float* xlast = m->at<float>(P.xlast);
-  LAUNCH(launch_gather_rows(m->X(2 * c.n_layers), d, d_last, B, xlast, s, pdl), 1);
   GemvParams h{};
-  h.x = xlast; h.ldx = d; h.g = m->final_norm; h.eps = c.norm_eps; h.B = B; h.K = d;
-  h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.out = logits; h.ldo = c.vocab;
+  h.ldx = d; h.g = m->final_norm; h.eps = c.norm_eps; h.K = d;
+  h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.ldo = c.vocab;
   h.err = m->err();
   m->splitk(h, SK_LMHEAD);
+  if (all_rows) {
+    // Every packed row, max_batch rows per launch (the row count the lm_head
+    // projection's workspace is planned for); then each sequence's last row.
+    for (int r0 = 0; r0 < M; r0 += Bm) {
+      GemvParams hc = h;
+      hc.x = m->X(2 * c.n_layers) + (size_t)r0 * d;
+      hc.B = M - r0 < Bm ? M - r0 : Bm;
+      hc.out = logits + (size_t)r0 * c.vocab;
+      LAUNCH(launch_gemv(hc, GEMV_LOGITS, m->wdt, m->num_sms, s, pdl), gemv_launch_count(hc.B, hc.K, GEMV_LOGITS));
+    }
+    if (next_tok)
+      for (int b = 0; b < B; ++b)
+        LAUNCH(launch_argmax(logits + (size_t)last[b] * c.vocab, 1, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i),
+                             kArgmaxBlocks, next_tok + b, s, pdl), 2);
+    LAUNCH(launch_set_lens(d_lens, B, kv->seq_lens, s, pdl), 1);
+    for (int b = 0; b < B; ++b) kv->host_lens[b] = host_lens[b];
+    return LADDER_OK;
+  }
+  float* xlast = m->at<float>(P.xlast);
+  LAUNCH(launch_gather_rows(m->X(2 * c.n_layers), d, d_last, B, xlast, s, pdl), 1);
+  h.x = xlast; h.B = B; h.out = logits;
   LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, h.K, GEMV_LOGITS));
   if (next_tok && m->samp_t > 0.f)  // the sampled token takes position T_b
     LAUNCH(launch_sample(logits, B, c.vocab, m->samp_t, m->samp_k, m->samp_seed, d_lens, 0, next_tok, s, pdl), 1);

@@ -30,6 +30,7 @@ RESIDUAL_STANDARD = 1
 RESIDUAL_PARALLEL = 2
 FLAG_DECODE_GRAPH = 1
 FLAG_NO_PDL = 2
+FLAG_ALL_LOGITS = 4
 
 # Entry points declared in include/ladder.h, with (restype, argtypes).
 _vp, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
@@ -303,17 +304,20 @@ class LadderModel:
         return lib().ladder_kv_seq_len(self._kv, b)
 
     # -- modes -----------------------------------------------------------
-    def set_mode(self, standard: bool = False, graph: bool = False, pdl: bool = True, parallel: bool = False):
+    def set_mode(self, standard: bool = False, graph: bool = False, pdl: bool = True, parallel: bool = False,
+                 all_logits: bool = False):
         """Residual schedule: as configured (default), every layer standard
         (``standard``), or every layer a parallel attention + MLP block
-        (``parallel``); decode launch flags."""
+        (``parallel``); decode launch flags; ``all_logits``: prefill returns the
+        logits of every packed position ([sum of lens, vocab])."""
         if standard and parallel:
             raise ValueError("standard and parallel are exclusive")
-        flags = (FLAG_DECODE_GRAPH if graph else 0) | (0 if pdl else FLAG_NO_PDL)
+        flags = (FLAG_DECODE_GRAPH if graph else 0) | (0 if pdl else FLAG_NO_PDL) | (FLAG_ALL_LOGITS if all_logits else 0)
         mode = RESIDUAL_STANDARD if standard else RESIDUAL_PARALLEL if parallel else RESIDUAL_CONFIG
         check(lib().ladder_set_mode(self._m, mode, flags))
         self._standard = standard
         self._parallel = parallel
+        self._all_logits = all_logits
 
     def set_sampling(self, temperature: float = 0.0, top_k: int = 0, seed: int = 0):
         """Next-token rule of prefill / decode_step: greedy (temperature <= 0) or
@@ -324,12 +328,15 @@ class LadderModel:
     # -- forward ---------------------------------------------------------
     def prefill(self, tokens: torch.Tensor, lens, logits: torch.Tensor | None = None,
                 next_tok: torch.Tensor | None = None, stream=None):
-        """tokens: device int32 packed prompts; lens: host list of lengths."""
+        """tokens: device int32 packed prompts; lens: host list of lengths.
+        Logits: [B, vocab] of each last position, or [sum of lens, vocab] of
+        every position when set_mode(all_logits=True)."""
         B = len(lens)
         hl = np.ascontiguousarray(lens, dtype=np.int32)
         dev = tokens.device
         if logits is None:
-            logits = torch.empty(B, self.dims["vocab"], dtype=torch.float32, device=dev)
+            rows = int(hl.sum()) if getattr(self, "_all_logits", False) else B
+            logits = torch.empty(rows, self.dims["vocab"], dtype=torch.float32, device=dev)
         if next_tok is None:
             next_tok = torch.empty(B, dtype=torch.int32, device=dev)
         check(lib().ladder_prefill(self._m, self._kv, tokens.data_ptr(), hl.ctypes.data_as(_pi32), B,

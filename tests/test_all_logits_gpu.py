@@ -1,0 +1,106 @@
+"""Prefill with the logits of every position (LADDER_FLAG_ALL_LOGITS).
+
+Every packed row against the oracle's all-position forward pass, and causality
+as a property that holds at any size: changing the token at position p leaves
+the logits of positions before p bitwise unchanged (each row of every prefill
+kernel depends only on its own inputs and on earlier positions, in a fixed
+order), and changes them from p on.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle.ladder_oracle as O
+from ladder_residual_transformer_gb300 import ladder, synth
+
+from gpu_common import compare_logits, gpu_weights, make_model, oracle_weights, packed, prompts_for, small_dims
+
+pytestmark = pytest.mark.gpu
+
+
+def prefill_all(model, prompts, graph=False):
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        model.reset()
+        model.set_mode(graph=graph, all_logits=True)
+        logits, tok = model.prefill(packed(prompts), [len(p) for p in prompts])
+        out = logits.cpu().numpy(), tok.cpu().numpy()
+    s.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("max_batch", [3, 2])
+def test_every_row_matches_the_oracle(max_batch):
+    """Ragged prompts (lm_head over 3 rows per launch: the batched projection
+    path; or 2: the per-row one), then a decode step on the filled cache."""
+    dims = small_dims()
+    lens = [5, 40, 17][:max_batch]
+    prompts = prompts_for(lens, dims["vocab"])
+    model = make_model(dims, gpu_weights(dims), max_batch=max_batch, max_seq=64, page_size=16)
+    g_all, g_tok = prefill_all(model, prompts)
+    assert g_all.shape == (sum(lens), dims["vocab"])
+    o_all = O.forward(dims, oracle_weights(dims), prompts, [O.SeqCache() for _ in lens], all_positions=True)
+    r = 0
+    for b, n in enumerate(lens):
+        compare_logits(g_all[r:r + n], o_all[b], f"sequence {b}")
+        assert g_tok[b] == O.argmax_lowest(g_all[r + n - 1])  # the device's own last row
+        r += n
+    # the cache is filled as in the ordinary prefill: one decode step matches the oracle
+    feed = np.array([7, 300, 11][:max_batch], dtype=np.int32)
+    lg, _ = model.decode_step(torch.from_numpy(feed).cuda())
+    caches = O.prefill(dims, oracle_weights(dims), prompts)[1]
+    compare_logits(lg.cpu().numpy(), O.decode_step(dims, oracle_weights(dims), feed, caches), "decode after all-row prefill")
+
+
+def test_flag_checks():
+    dims = small_dims()
+    model = make_model(dims, gpu_weights(dims), max_batch=2, max_seq=32, page_size=16)
+    model.set_sampling(0.8, 5, 1)
+    model.set_mode(all_logits=True)
+    with pytest.raises(ladder.LadderError) as e:
+        model.prefill(packed(prompts_for([4], dims["vocab"])), [4])
+    assert e.value.code == ladder.LADDER_ERR_UNSUPPORTED
+    assert model.seq_len(0) == 0
+    # without a next-token output (NULL), sampling settings do not matter
+    lg = torch.empty(4, dims["vocab"], device="cuda")
+    toks = packed(prompts_for([4], dims["vocab"]))
+    lens = np.array([4], dtype=np.int32)
+    ladder.check(ladder.lib().ladder_prefill(model._m, model._kv, toks.data_ptr(), lens.ctypes.data_as(ladder._pi32),
+                                             1, lg.data_ptr(), None, torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert model.seq_len(0) == 4 and np.isfinite(lg.cpu().numpy()).all()
+    assert ladder.lib().ladder_set_mode(model._m, 0, 8) == ladder.LADDER_ERR_INVALID
+
+
+def causality(dims, model, prompt, p):
+    a, _ = prefill_all(model, [prompt])
+    changed = prompt.copy()
+    changed[p] = (changed[p] + 1) % dims["vocab"]
+    b, _ = prefill_all(model, [changed])
+    assert np.array_equal(a[:p], b[:p]), "rows before the changed token moved"
+    assert not np.array_equal(a[p], b[p])
+    return a
+
+
+def test_causality_is_bitwise_tiny():
+    dims = small_dims()
+    model = make_model(dims, gpu_weights(dims), max_batch=1, max_seq=160, page_size=32)
+    prompt = prompts_for([150], dims["vocab"])[0]
+    for p in (0, 63, 128, 149):
+        causality(dims, model, prompt, p)
+
+
+@pytest.mark.slow
+def test_full_size_1p2b_every_row_and_causality():
+    """The 1.2B workload's 1024-token prompt: every row against the oracle, and
+    causality at position 700."""
+    dims = dict(synth.PRESETS["1.2b"])
+    gw = gpu_weights(dims)
+    prompt = prompts_for([1024], dims["vocab"])[0]
+    model = make_model(dims, gw, max_batch=1, max_seq=1024 + 256, max_prefill_tokens=1024)
+    g_all = causality(dims, model, prompt, 700)
+    del gw, model
+    torch.cuda.empty_cache()
+    o_all = O.forward(dims, O.synthetic_weights(dims), [prompt], [O.SeqCache()], all_positions=True)[0]
+    for r0 in range(0, 1024, 256):
+        compare_logits(g_all[r0:r0 + 256], o_all[r0:r0 + 256], f"1.2B rows {r0}..{r0 + 255}")

@@ -32,6 +32,23 @@ def test_library_exports_every_declared_entry_point():
     assert names == set(ladder._SIGNATURES)
 
 
+def test_binding_constants_match_the_header():
+    """Every enumerator of include/ladder.h that the binding mirrors has the same value."""
+    text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "ladder.h")).read(), flags=re.S)
+    enum = {k: int(v) for k, v in re.findall(r"\b(LADDER_[A-Z0-9_]+)\s*=\s*(-?\d+)", text)}
+    for name in ("OK", "ERR_INVALID", "ERR_CUDA", "ERR_CAPACITY", "ERR_UNSUPPORTED"):
+        assert getattr(ladder, "LADDER_" + name) == enum["LADDER_" + name], name
+    for name in ("CONFIG", "STANDARD", "PARALLEL"):
+        assert getattr(ladder, "RESIDUAL_" + name) == enum["LADDER_RESIDUAL_" + name], name
+    for name in ("DECODE_GRAPH", "NO_PDL", "ALL_LOGITS"):
+        assert getattr(ladder, "FLAG_" + name) == enum["LADDER_FLAG_" + name], name
+    for cls, v in ladder.PROBE_CLASSES.items():
+        key = "LADDER_PROBE_" + {"out": "OUT", "gateup": "GATEUP", "lmhead": "LMHEAD"}.get(cls, cls.upper())
+        assert enum[key] == v, cls
+    assert len(ladder.PROBE_CLASSES) == sum(k.startswith("LADDER_PROBE_") for k in enum)
+    assert ladder.DTYPES == {"bf16": enum["LADDER_DTYPE_BF16"], "fp16": enum["LADDER_DTYPE_F16"]}
+
+
 def cfg(**over):
     dims = dict(synth.PRESETS["tiny"])
     c = ladder.make_config(dims, max_batch=4, max_seq=256)

@@ -391,6 +391,19 @@ def test_host_and_device_errors(tiny):
         assert model.seq_len(0) == 32
         with pytest.raises(ladder.LadderError):
             model.decode_step(torch.zeros(3, dtype=torch.int32, device="cuda"))
+        # empty batches and empty prompts are rejected and leave the cache as it was
+        for call in (lambda: model.decode_step(torch.zeros(0, dtype=torch.int32, device="cuda")),
+                     lambda: model.prefill(torch.zeros(0, dtype=torch.int32, device="cuda"), [])):
+            with pytest.raises(ladder.LadderError) as e:
+                call()
+            assert e.value.code == ladder.LADDER_ERR_INVALID
+        model.reset()
+        with pytest.raises(ladder.LadderError) as e:
+            model.prefill(packed(prompts_for([4], dims["vocab"])), [4, 0])
+        assert e.value.code == ladder.LADDER_ERR_INVALID
+        assert model.seq_len(0) == 0 and model.seq_len(1) == 0
+        model.prefill(packed(prompts_for([31], dims["vocab"])), [31])
+        model.decode_step(tok)
     s.synchronize()
     assert model.seq_lens.cpu().tolist()[0] == 32
 
