@@ -38,6 +38,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic of the dominant kernel from one ncu capture, valid only while the
 # kernel source is unchanged (sha256 of the file that defines it).
+L2_BYTES = 129 * 10 ** 6  # GB300 L2 cache
 NCU_TRAFFIC = {  # profiles/gemv_gateup_1p2b_traffic.md (mean of the two captured launches)
     "source": "ladder_residual_transformer_gb300/csrc/decode_kernels.cu",
     "sha256": "9b1e41e127b124917a06d8b238fa1c5057abf915ac462157c3231eff74ea9e39",
@@ -250,7 +251,8 @@ def workload_config(args, dims):
                         f"{dims['n_q_heads']}q/{dims['n_kv_heads']}kv heads x {dims['head_dim']}, "
                         f"ffn {dims['ffn_dim']}, vocab {dims['vocab']}",
             "batch": args.batch, "prompt_tokens": args.prompt, "decode_steps": args.decode,
-            "l2": "inputs larger than L2 (all weights streamed every step)"}
+            "l2": ("inputs larger than L2 (all weights streamed every step)" if decode_step_bytes(dims, [0]) > L2_BYTES
+                   else "weights fit in L2 (a parity-size model, not a roofline workload)")}
 
 
 def run_ours(args, dims):

@@ -46,3 +46,29 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.max_over_ranks([3.0, 4.0], 1) == [3.0, 4.0]
     assert bench.sum_over_ranks([5.0], 1) == [5.0]
+
+
+def test_reference_arm_prints_one_json_line():
+    """bench.py --impl reference times the oracle on the host and prints the
+    contract's JSON line; the GPU arm without a GPU fails instead of falling back."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny", "--steps", "2",
+                        "--warmup", "1", "--ref-prompt", "16", "--ref-decode", "2"],
+                       cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    out = json.loads(lines[0])
+    assert out["impl"] == "reference" and out["unit"] == "tok/s" and out["value"] > 0
+    assert out["steps"] == 2 and out["warmup"] == 1 and out["higher_is_better"] is True
+    assert out["cpu_baseline"]["kind"] == "oracle" and out["cpu_baseline"]["value"] == out["value"]
+    assert out["e2e"] == {"value": out["value"], "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert "fit in L2" in out["config"]["l2"]
+    import torch
+    if not torch.cuda.is_available():
+        r = subprocess.run([sys.executable, "bench.py", "--workload", "tiny", "--steps", "1", "--warmup", "1",
+                            "--no-cpu-baseline"], cwd=root, capture_output=True, text=True, timeout=600)
+        assert r.returncode != 0 and not r.stdout.strip()
