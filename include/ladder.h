@@ -86,7 +86,7 @@ enum {
 /* Flags for ladder_set_mode. */
 enum {
   LADDER_FLAG_DECODE_GRAPH = 1, /* capture each decode step shape in a CUDA graph and replay it */
-  LADDER_FLAG_NO_PDL = 2,       /* launch decode kernels without programmatic dependent launch */
+  LADDER_FLAG_NO_PDL = 2,       /* launch prefill and decode kernels without programmatic dependent launch */
   LADDER_FLAG_ALL_LOGITS = 4    /* prefill writes the logits of every position (a debugging aid) */
 };
 
@@ -106,7 +106,9 @@ typedef struct {
   float rope_theta;
   float norm_eps;
   int32_t tie_embeddings;     /* 1: lm_head is the embedding table */
-  int32_t rope_interleaved;   /* must be 1 (pairs (2j, 2j+1)) */
+  int32_t rope_interleaved;   /* must be 1 (pairs (2j, 2j+1)); weights laid out for half-split
+                                 pairs (j, j + head_dim/2) need each head's W_q and W_k rows
+                                 reordered first (new row 2j = row j, 2j+1 = row j + head_dim/2) */
   int32_t shard_k;            /* 1 = off; 2, 4 or 8 = shard mode (see below) */
   int32_t page_size;          /* KV positions per page: 16, 32 or 64 */
   int32_t max_batch;          /* sequences per call, <= 64 */
