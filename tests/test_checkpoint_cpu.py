@@ -144,6 +144,13 @@ def test_dims_from_hf_config():
     assert d["n_kv_heads"] == 32 and d["head_dim"] == 64 and d["tie_embeddings"] == 1 and "rope_scaling" not in d
     d = C.dims_from_hf_config(dict(LLAMA31_8B, rope_scaling={"rope_type": "default"}), 32)
     assert "rope_scaling" not in d and d["n_standard_layers"] == 32
+    # a 16-layer, 2048-wide model with tied embeddings has the shapes of the 1.2B workload
+    small = dict(LLAMA31_8B, hidden_size=2048, num_hidden_layers=16, intermediate_size=8192, head_dim=64,
+                 tie_word_embeddings=True)
+    d = C.dims_from_hf_config(small, 0)
+    ref = synth.PRESETS["1.2b"]
+    assert all(d[k] == ref[k] for k in ("n_layers", "d_model", "n_q_heads", "n_kv_heads", "head_dim", "ffn_dim",
+                                        "vocab", "tie_embeddings"))
 
 
 @pytest.mark.parametrize("over,nstd", [({"hidden_act": "gelu"}, 0), ({"attention_bias": True}, 0),
