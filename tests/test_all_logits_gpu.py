@@ -104,3 +104,35 @@ def test_full_size_1p2b_every_row_and_causality():
     o_all = O.forward(dims, O.synthetic_weights(dims), [prompt], [O.SeqCache()], all_positions=True)[0]
     for r0 in range(0, 1024, 256):
         compare_logits(g_all[r0:r0 + 256], o_all[r0:r0 + 256], f"1.2B rows {r0}..{r0 + 255}")
+
+
+@pytest.mark.slow
+def test_full_size_8b_hybrid_batch_independence_and_causality():
+    """The 8B hybrid's prefill workload (4 x 4096 tokens, the launch shapes the
+    benchmark times): changing one token of sequence 2 leaves every row of the
+    other sequences, and the rows of sequence 2 before it, bitwise unchanged.
+    Compared on the device (the logits are 8.4 GB)."""
+    dims = dict(synth.PRESETS["8b-hybrid"])
+    n, B, p = 4096, 4, 3000
+    gw = gpu_weights(dims)
+    model = make_model(dims, gw, max_batch=B, max_seq=n, max_prefill_tokens=B * n)
+    prompts = prompts_for([n] * B, dims["vocab"])
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        model.set_mode(all_logits=True)
+        a, ta = model.prefill(packed(prompts), [n] * B)
+        prompts[2] = prompts[2].copy()
+        prompts[2][p] = (prompts[2][p] + 1) % dims["vocab"]
+        model.reset()
+        b, tb = model.prefill(packed(prompts), [n] * B)
+        same_others = all(torch.equal(a[q * n:(q + 1) * n], b[q * n:(q + 1) * n]) for q in (0, 1, 3))
+        same_before = torch.equal(a[2 * n:2 * n + p], b[2 * n:2 * n + p])
+        moved_at = not torch.equal(a[2 * n + p], b[2 * n + p])
+        finite = bool(torch.isfinite(a).all())
+        toks = ta.cpu().numpy(), tb.cpu().numpy()
+    s.synchronize()
+    assert finite
+    assert same_others, "a sequence's logits depend on another sequence's tokens"
+    assert same_before, "rows before the changed token moved"
+    assert moved_at
+    assert toks[0][[0, 1, 3]].tolist() == toks[1][[0, 1, 3]].tolist()
