@@ -131,6 +131,9 @@ def test_full_size_8b_hybrid_batch_independence_and_causality():
         finite = bool(torch.isfinite(a).all())
         toks = ta.cpu().numpy(), tb.cpu().numpy()
     s.synchronize()
+    model.close()
+    del a, b, gw, model
+    torch.cuda.empty_cache()
     assert finite
     assert same_others, "a sequence's logits depend on another sequence's tokens"
     assert same_before, "rows before the changed token moved"
