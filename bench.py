@@ -39,7 +39,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic of the dominant kernel from one ncu capture, valid only while the
 # kernel source is unchanged (sha256 of the file that defines it).
 L2_BYTES = 129 * 10 ** 6  # GB300 L2 cache
-NCU_TRAFFIC = {  # profiles/gemv_gateup_1p2b_traffic.md (mean of the two captured launches)
+NCU_TRAFFIC = {  # mean of the two captured launches
     "source": "ladder_residual_transformer_gb300/csrc/decode_kernels.cu",
     "sha256": "9b1e41e127b124917a06d8b238fa1c5057abf915ac462157c3231eff74ea9e39",
     "bytes_per_launch": 67253120,

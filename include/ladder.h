@@ -87,8 +87,21 @@ enum {
 enum {
   LADDER_FLAG_DECODE_GRAPH = 1, /* capture each decode step shape in a CUDA graph and replay it */
   LADDER_FLAG_NO_PDL = 2,       /* launch prefill and decode kernels without programmatic dependent launch */
-  LADDER_FLAG_ALL_LOGITS = 4    /* prefill writes the logits of every position (a debugging aid) */
+  LADDER_FLAG_ALL_LOGITS = 4,   /* prefill writes the logits of every position (a debugging aid) */
+  LADDER_FLAG_FAST_PREFILL = 8  /* prefill GEMM activations rounded once to 16 bits (see below) */
 };
+/* Prefill precision.  Decode projections read the fp32 stream directly.  The
+ * prefill projections are tensor-core GEMMs whose activation operand (the
+ * normalised rows into QKV and gate/up, the attention output into W_o, the
+ * SwiGLU output into W_down) is 16-bit.  By default each activation is held as
+ * a hi/lo pair, hi = its 16-bit rounding and lo = the rounding of what is
+ * left, and every GEMM multiplies both by the same weight tile: the
+ * activations enter with about 22 significant bits (fp16 storage) and the
+ * GEMMs do twice the tensor-core work.  LADDER_FLAG_FAST_PREFILL rounds them
+ * once instead (11 significant bits, half the work).  Rounding the
+ * activations once is within max-abs 3e-2 / relative L2 1e-2 of an fp32
+ * forward pass on shallow models, but on deep random-init models the
+ * rounding noise of 32 to 80 layers adds up to more than that. */
 
 /* Model dimensions and capacities.  All int32 fields must be positive unless
  * stated.  Shape rules: d_model, n_q_heads*head_dim and ffn_dim multiples of
@@ -257,7 +270,10 @@ int ladder_decode_step(ladder_model* m, ladder_kv* kv, const int32_t* tokens, in
                        float* logits, int32_t* next_tok, ladder_stream_t stream);
 
 /* Reads and clears the device error word (synchronises `stream`).  *code is 0
- * when no kernel reported a problem; 1 = a token id was outside [0, vocab). */
+ * when no kernel reported a problem, else an OR of: 1 = a token id was outside
+ * [0, vocab) (its row used a zero embedding); 2 = a pipeline wait ran out of
+ * time and the kernel stopped early; 4 = a projection produced inf or NaN (for
+ * example an activation beyond the 16-bit range of fp16 storage). */
 int ladder_get_device_error(ladder_model* m, ladder_stream_t stream, int32_t* code);
 
 /* Number of kernel launches the last prefill / decode call issued (a decode
@@ -331,12 +347,15 @@ int ladder_attention_decode(const float* q, const void* kv_layer, int32_t kv_dty
  * stall on an allocation).  The partials live in a file-scope device array of
  * LADDER_STATIC_SCRATCH_BYTES bytes that every GPU running this code keeps
  * until the process exits.  Calls whose partials need more than that fail with
- * LADDER_ERR_CAPACITY (need = 256-byte-aligned B*n_q_heads*nsplit*head_dim*4
- * plus B*n_q_heads*nsplit*8, nsplit = ceil((max_position+1)/128)).  The first
- * call on a device looks up the array's device address (cudaGetSymbolAddress)
- * with that device current; make that first call before any stream capture.
- * All calls share the one array: calls that can overlap on the GPU (on
- * different streams, or from different threads) race on it and must be
+ * LADDER_ERR_CAPACITY (need = ladder_attention_decode_scratch_bytes(B,
+ * n_q_heads, head_dim, max_position)).  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress) with that device current
+ * and keeps it for the life of the process; make that first call before any
+ * stream capture.  A device reset (cudaDeviceReset) unloads the library's
+ * device code and with it the array, so the kept address is no longer valid:
+ * do not call this entry point on a device after resetting it in the same
+ * process.  All calls share the one array: calls that can overlap on the GPU
+ * (on different streams, or from different threads) race on it and must be
  * serialised by the caller. */
 #define LADDER_STATIC_SCRATCH_BYTES (8u << 20)
 int ladder_attention_decode_noalloc(const float* q, const void* kv_layer, int32_t kv_dtype,

@@ -25,7 +25,6 @@ using namespace ladder;
 namespace {
 
 constexpr size_t kStaticScratchBytes = LADDER_STATIC_SCRATCH_BYTES;
-constexpr int kSplitLen = 128;  // keys per split, as in the scratch-taking entry point
 constexpr int kMaxDevices = 64;
 
 // Partials of the split attention: [B][n_q][nsplit][head_dim] fp32, then
@@ -52,8 +51,6 @@ int scratch_address(void** out) {
   return LADDER_OK;
 }
 
-size_t align256(size_t v) { return (v + 255) / 256 * 256; }
-
 }  // namespace
 
 extern "C" int ladder_attention_decode_noalloc(const float* q, const void* kv_layer, int32_t kv_dtype,
@@ -63,8 +60,8 @@ extern "C" int ladder_attention_decode_noalloc(const float* q, const void* kv_la
                                                int32_t max_position, float* out, ladder_stream_t stream) {
   if (B <= 0 || n_q_heads <= 0 || head_dim <= 0 || max_position < 0)
     return set_error(LADDER_ERR_INVALID, "B, n_q_heads, head_dim must be positive and max_position >= 0");
-  const size_t nsplit = ((size_t)max_position + 1 + kSplitLen - 1) / kSplitLen;
-  const size_t need = align256((size_t)B * n_q_heads * nsplit * head_dim * 4) + (size_t)B * n_q_heads * nsplit * 2 * 4;
+  // the same sizing rule as the scratch-taking entry point, from the one place that defines it
+  const size_t need = ladder_attention_decode_scratch_bytes(B, n_q_heads, head_dim, max_position);
   if (need > kStaticScratchBytes) {
     char msg[200];
     snprintf(msg, sizeof(msg),

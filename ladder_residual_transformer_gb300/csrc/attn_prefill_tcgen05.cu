@@ -349,12 +349,23 @@ __global__ void __launch_bounds__(FT_THREADS, 1)
         if (q < Tn) {
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = o[e + i] * inv;
             uint4 pk;
-            pk.x = C::pack(o[e] * inv, o[e + 1] * inv);
-            pk.y = C::pack(o[e + 2] * inv, o[e + 3] * inv);
-            pk.z = C::pack(o[e + 4] * inv, o[e + 5] * inv);
-            pk.w = C::pack(o[e + 6] * inv, o[e + 7] * inv);
+            pk.x = C::pack(v[0], v[1]);
+            pk.y = C::pack(v[2], v[3]);
+            pk.z = C::pack(v[4], v[5]);
+            pk.w = C::pack(v[6], v[7]);
             *reinterpret_cast<uint4*>(dst + c * 32 + e) = pk;
+            if (p.lo_off) {  // rounding remainders into the lo plane (hi/lo operand of the O projection)
+              uint4 pl;
+              pl.x = C::pack(v[0] - C::lo(pk.x), v[1] - C::hi(pk.x));
+              pl.y = C::pack(v[2] - C::lo(pk.y), v[3] - C::hi(pk.y));
+              pl.z = C::pack(v[4] - C::lo(pk.z), v[5] - C::hi(pk.z));
+              pl.w = C::pack(v[6] - C::lo(pk.w), v[7] - C::hi(pk.w));
+              *reinterpret_cast<uint4*>(dst + p.lo_off + c * 32 + e) = pl;
+            }
           }
         }
       }

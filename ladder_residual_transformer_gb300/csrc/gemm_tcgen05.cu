@@ -125,14 +125,20 @@ __device__ __forceinline__ void gemm_tile(int i, int m_tiles, uint32_t crank, in
   }
 }
 
-template <typename WT, int MODE, int BN, int KC, int PAIR>
+// WIDE = 1: A is a hi/lo pair of planes.  Each stage holds the hi and the lo
+// block of every A chunk (A_BYTES doubles, KC = 1), and each k step issues the
+// hi MMA and then the lo MMA against the same B tile, so the accumulator sums
+// W * hi + W * lo and the activations enter the product with about 22
+// significant bits instead of 11.
+template <typename WT, int MODE, int BN, int KC, int PAIR, int WIDE>
 __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_constant__ TcMaps maps,
                                                                 const GemmParams p, int m_tiles, int n_tiles,
                                                                 int* err) {
   using C = W16<WT>;
   constexpr int HALVES = BN / 128;
   constexpr int BK = 64 * KC;
-  constexpr int A_BYTES = KC * TC_CHUNK;   // 128 rows of A
+  static_assert(!WIDE || KC == 1, "hi/lo operands use one 64-wide chunk per stage");
+  constexpr int A_BYTES = KC * TC_CHUNK * (WIDE ? 2 : 1);   // 128 rows of A (hi and lo blocks when WIDE)
   constexpr int BH_BYTES = KC * TC_CHUNK;  // one 128-row half of B
   constexpr int HB = PAIR ? 1 : HALVES;  // B halves held by this CTA
   constexpr int STAGE = A_BYTES + HB * BH_BYTES;
@@ -217,13 +223,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
             // this CTA's A rows and B half r; both signal the leader's full barrier
             const uint32_t fb = smem_map_rank(&full[s], 0);
             if (leader) mbar_expect_tx(&full[s], 2 * STAGE);
-            tma_load_3d_pair(st, &maps.a, 0, m0, kb * KC, fb);
+            if (WIDE) tma_load_4d_pair(st, &maps.a, 0, m0, 0, kb, fb);
+            else tma_load_3d_pair(st, &maps.a, 0, m0, kb * KC, fb);
             if (crank == 0) tma_load_3d_pair(st + A_BYTES, &maps.b[map0], 0, row0, kb * KC, fb);
             else tma_load_3d_pair(st + A_BYTES, &maps.b[map1], 0, row1, kb * KC, fb);
             continue;
           }
           mbar_expect_tx(&full[s], STAGE);
-          tma_load_3d(st, &maps.a, 0, m0, kb * KC, &full[s]);
+          if (WIDE) tma_load_4d(st, &maps.a, 0, m0, 0, kb, &full[s]);
+          else tma_load_3d(st, &maps.a, 0, m0, kb * KC, &full[s]);
           tma_load_3d(st + A_BYTES, &maps.b[map0], 0, row0, kb * KC, &full[s]);
           if (HALVES == 2) tma_load_3d(st + A_BYTES + BH_BYTES, &maps.b[map1], 0, row1, kb * KC, &full[s]);
           // The CTAs of a tile column read the same weight boxes at about the same
@@ -280,13 +288,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-              for (int hh = 0; hh < MMAS; ++hh)
-                if (PAIR)
-                  umma_f16_pair(d, umma_desc(a_base + c * TC_CHUNK + kk * 32), umma_desc(b_base + c * TC_CHUNK + kk * 32),
-                                idesc, (kb | c | kk) != 0);
-                else
-                  umma_f16(d + hh * 128, umma_desc(a_base + c * TC_CHUNK + kk * 32),
-                           umma_desc(b_base + hh * BH_BYTES + c * TC_CHUNK + kk * 32), idesc, (kb | c | kk) != 0);
+              for (int w = 0; w <= WIDE; ++w) {  // w = 0: hi block (or the only one), 1: lo block
+                const uint32_t a_off = ((WIDE ? 2 : 1) * c + w) * TC_CHUNK + kk * 32;
+                const uint32_t accum = (kb | c | kk | w) != 0;
+#pragma unroll
+                for (int hh = 0; hh < MMAS; ++hh)
+                  if (PAIR)
+                    umma_f16_pair(d, umma_desc(a_base + a_off), umma_desc(b_base + c * TC_CHUNK + kk * 32), idesc,
+                                  accum);
+                  else
+                    umma_f16(d + hh * 128, umma_desc(a_base + a_off),
+                             umma_desc(b_base + hh * BH_BYTES + c * TC_CHUNK + kk * 32), idesc, accum);
+              }
           if (PAIR) umma_commit_pair(&empty[s], 3);
           else umma_commit(&empty[s]);
         }
@@ -361,19 +374,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
           float gv[32], uv[32];
           tmem_ld32(trow + c * 32, gv);
           tmem_ld32(trow + 128 + c * 32, uv);
-          uint32_t pk[16];
+          uint32_t pk[16], pl[16];
+          bool bad = false;
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            pk[j] = C::pack(silu_f(gv[2 * j]) * uv[2 * j], silu_f(gv[2 * j + 1]) * uv[2 * j + 1]);
-          // row lane, 64-byte rows, 16-byte chunk q at q ^ ((row >> 1) & 3) (64-byte swizzle)
+          for (int j = 0; j < 16; ++j) {
+            const float a0 = silu_f(gv[2 * j]) * uv[2 * j], a1 = silu_f(gv[2 * j + 1]) * uv[2 * j + 1];
+            pk[j] = C::pack(a0, a1);
+            bad |= mrow0 + lane < p.M && C::bad(pk[j]);  // rows past M hold padding
+            if (WIDE) pl[j] = C::pack(a0 - C::lo(pk[j]), a1 - C::hi(pk[j]));  // rounding remainders
+          }
+          if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(err, ERR_NONFINITE);
+          // row lane, 64-byte rows, 16-byte chunk q at q ^ ((row >> 1) & 3) (64-byte swizzle);
+          // the lo block (WIDE) is the second 2 KB of the buffer
           uint4* rowp = reinterpret_cast<uint4*>(buf + lane * 64);
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
+          for (int q = 0; q < 4; ++q) {
             rowp[q ^ ((lane >> 1) & 3)] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            if (WIDE)
+              rowp[128 + (q ^ ((lane >> 1) & 3))] = make_uint4(pl[4 * q], pl[4 * q + 1], pl[4 * q + 2], pl[4 * q + 3]);
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
             tma_store_2d(&maps.e_out, buf, tile_n * 128 + c * 32, mrow0);
+            if (WIDE) tma_store_2d(&maps.e_out, buf + 2048, tile_n * 128 + c * 32, p.lo_row + mrow0);
             bulk_commit();
           }
         }
@@ -392,6 +416,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
           tmem_ld32(trow + c * 32, v);
           // row lane of the block: 16-byte chunk q at q ^ (row & 7) (128-byte swizzle)
           float4* rowp = reinterpret_cast<float4*>(buf + lane * 32);
+          bool bad = false;
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             float4 xv = rowp[q ^ (lane & 7)];
@@ -399,8 +424,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
             xv.y += v[4 * q + 1];
             xv.z += v[4 * q + 2];
             xv.w += v[4 * q + 3];
+            bad |= mrow0 + lane < p.M && !(isfinite(xv.x) && isfinite(xv.y) && isfinite(xv.z) && isfinite(xv.w));
             rowp[q ^ (lane & 7)] = xv;
           }
+          if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(err, ERR_NONFINITE);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -464,13 +491,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
           WT* base = map == 0 ? static_cast<WT*>(p.out_h) + col
                               : static_cast<WT*>(p.kv.base) +
                                     ((long long)((map - 1) * p.kv.n_kv + head) * p.kv.page_size * hd + dim);
+          bool bad = false;
 #pragma unroll
           for (int r2 = 0; r2 < 16; ++r2) {
             const float r0 = a[2 * r2] * cs[r2] - a[2 * r2 + 1] * sn[r2];
             const float r1 = a[2 * r2] * sn[r2] + a[2 * r2 + 1] * cs[r2];
             const uint32_t pk = C::pack(r0, r1);
-            if (mrow0 + 2 * r2 + rsub < p.M) *reinterpret_cast<uint32_t*>(base + off[r2]) = pk;
+            const bool live = mrow0 + 2 * r2 + rsub < p.M;
+            bad |= live && C::bad(pk);
+            if (live) *reinterpret_cast<uint32_t*>(base + off[r2]) = pk;
           }
+          if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(err, ERR_NONFINITE);
         }
       }
       // hand the accumulator buffer back to the (leader's) MMA warp
@@ -541,8 +572,12 @@ bool make_tma_map(void* map_out, const void* base, uint64_t rows, uint64_t cols,
 
 // GEMM operand: row-major 16-bit [rows, cols] viewed as [cols / 64][rows][64]
 // (dimension order x = element in chunk, y = row, z = 64-element chunk), with a
-// box of 64 x 128 rows x KC chunks (KC = 1 and 2), 128-byte swizzle.
-bool make_tma_operand(TmaOperand* out, const void* base, uint64_t rows, uint64_t cols, int wdt) {
+// box of 64 x 128 rows x KC chunks (KC = 1 and 2), 128-byte swizzle.  With
+// `with_pair`, a second [rows, cols] matrix (the lo plane) follows the first
+// one, and `pair` views both as [cols / 64][2][rows][64] (x = element, y = row,
+// z = plane, w = chunk) with a box of 64 x 128 rows x 2 planes x 1 chunk: the
+// hi block lands first, the lo block 16 KB after it.
+bool make_tma_operand(TmaOperand* out, const void* base, uint64_t rows, uint64_t cols, int wdt, bool with_pair) {
   EncodeTiledFn fn = encode_fn();
   if (!fn || rows % 128 || cols % 128 || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
   const CUtensorMapDataType dt = wdt == WDT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -552,6 +587,17 @@ bool make_tma_operand(TmaOperand* out, const void* base, uint64_t rows, uint64_t
     cuuint32_t box[3] = {64, 128, (cuuint32_t)kc};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(&out->box[kc - 1], dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+  }
+  memcpy(&out->pair, &out->box[0], sizeof(CUtensorMap));
+  if (with_pair) {
+    cuuint64_t dims[4] = {64, rows, 2, cols / 64};
+    cuuint64_t strides[3] = {cols * 2, rows * cols * 2, 128};
+    cuuint32_t box[4] = {64, 128, 2, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(&out->pair, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
@@ -594,40 +640,45 @@ bool make_kv_tma_map(void* map_out, const void* base, uint64_t num_pages, int n_
   return r == CUDA_SUCCESS;
 }
 
-template <typename WT>
-static cudaError_t gemm_tc_configure_t() {
+template <typename WT, int WIDE>
+static cudaError_t gemm_tc_configure_w() {
+  constexpr int KN = WIDE ? 1 : 2;  // box depth of the 128-wide tiles
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 256, 1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 256, TC_PAIR_KC, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 128, 2, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_GATEUP, 256, 1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_GATEUP, 256, TC_PAIR_KC, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 256, 1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 256, TC_PAIR_KC, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
-  return cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 128, 2, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 256, 1, 0, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 256, TC_PAIR_KC, 1, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_QKV, 128, KN, 0, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_GATEUP, 256, 1, 0, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_GATEUP, 256, TC_PAIR_KC, 1, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 256, 1, 0, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  if ((e = cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 256, TC_PAIR_KC, 1, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM))) return e;
+  return cudaFuncSetAttribute(gemm_tc_kernel<WT, GEMM_RESID, 128, KN, 0, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
 }
 
 cudaError_t gemm_tc_configure() {
-  cudaError_t e = gemm_tc_configure_t<bf16>();
-  return e != cudaSuccess ? e : gemm_tc_configure_t<f16>();
+  cudaError_t e = gemm_tc_configure_w<bf16, 0>();
+  if (e == cudaSuccess) e = gemm_tc_configure_w<f16, 0>();
+  if (e == cudaSuccess) e = gemm_tc_configure_w<bf16, 1>();
+  if (e == cudaSuccess) e = gemm_tc_configure_w<f16, 1>();
+  return e;
 }
 
 // Tile width BN with its box depth: 256-wide tiles take 1-chunk boxes, 128-wide
-// 2-chunk boxes.  256-wide tiles with an even number of m tiles run as paired
+// 2-chunk boxes (1-chunk with hi/lo operands, whose stages carry two A blocks
+// per chunk).  256-wide tiles with an even number of m tiles run as paired
 // 256 x 256 tiles on clusters of two CTAs, as many clusters as can be resident.
-template <typename WT, int MODE, int BN>
+template <typename WT, int MODE, int BN, int WIDE>
 static cudaError_t gemm_tc_go(const TmaOperand* a, const TmaOperand* const* b, const void* const* e,
                               const GemmParams& p, int mt, int nt, int num_sms, int* err, cudaStream_t s, bool pdl) {
-  constexpr int KC = BN == 256 ? 1 : 2;
+  constexpr int KC = (BN == 256 || WIDE) ? 1 : 2;
   constexpr int BOX = (BN == 256 ? TC_PAIR_KC : KC) - 1;  // paired tiles use TC_PAIR_KC-chunk boxes
   TcMaps maps;
   memcpy(&maps.e_in, e[0] ? e[0] : &a->box[0], sizeof(CUtensorMap));
   memcpy(&maps.e_out, e[1] ? e[1] : &a->box[0], sizeof(CUtensorMap));
   if constexpr (BN == 256) {
     if (mt % 2 == 0) {
-      memcpy(&maps.a, &a->box[BOX], sizeof(CUtensorMap));
+      memcpy(&maps.a, WIDE ? &a->pair : &a->box[BOX], sizeof(CUtensorMap));
       for (int i = 0; i < 3; ++i) memcpy(&maps.b[i], &(b[i] ? b[i] : b[0])->box[BOX], sizeof(CUtensorMap));
-      auto kern = gemm_tc_kernel<WT, MODE, BN, TC_PAIR_KC, 1>;
+      auto kern = gemm_tc_kernel<WT, MODE, BN, TC_PAIR_KC, 1, WIDE>;
       cudaLaunchConfig_t cfg = {};
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -656,42 +707,47 @@ static cudaError_t gemm_tc_go(const TmaOperand* a, const TmaOperand* const* b, c
       return cudaLaunchKernelEx(&cfg, kern, maps, p, mt, nt, err);
     }
   }
-  memcpy(&maps.a, &a->box[KC - 1], sizeof(CUtensorMap));
+  memcpy(&maps.a, WIDE ? &a->pair : &a->box[KC - 1], sizeof(CUtensorMap));
   for (int i = 0; i < 3; ++i) memcpy(&maps.b[i], &(b[i] ? b[i] : b[0])->box[KC - 1], sizeof(CUtensorMap));
   const int total = mt * nt;
   const int grid = total < num_sms ? total : num_sms;
-  return launch_k(gemm_tc_kernel<WT, MODE, BN, KC, 0>, dim3(grid), dim3(TC_THREADS), (size_t)TC_SMEM, s, pdl, maps, p,
-                  mt, nt, err);
+  return launch_k(gemm_tc_kernel<WT, MODE, BN, KC, 0, WIDE>, dim3(grid), dim3(TC_THREADS), (size_t)TC_SMEM, s, pdl,
+                  maps, p, mt, nt, err);
 }
 
 // 256-wide tiles unless that leaves most SMs idle (narrow N at small M).
-template <typename WT>
+template <typename WT, int WIDE>
 static cudaError_t gemm_tc_dispatch(const TmaOperand* a, const TmaOperand* const* b, const void* const* e,
                                     const GemmParams& p, int mode, int mt, int num_sms, int* err, cudaStream_t s,
                                     bool pdl) {
-  if (mode == GEMM_GATEUP) return gemm_tc_go<WT, GEMM_GATEUP, 256>(a, b, e, p, mt, p.N / 128, num_sms, err, s, pdl);
+  if (mode == GEMM_GATEUP)
+    return gemm_tc_go<WT, GEMM_GATEUP, 256, WIDE>(a, b, e, p, mt, p.N / 128, num_sms, err, s, pdl);
   const int nt256 = (p.N + 255) / 256;
   const bool narrow = (long long)mt * nt256 * 4 < (long long)num_sms * 3;
   if (mode == GEMM_RESID) {
-    if (narrow) return gemm_tc_go<WT, GEMM_RESID, 128>(a, b, e, p, mt, (p.N + 127) / 128, num_sms, err, s, pdl);
-    return gemm_tc_go<WT, GEMM_RESID, 256>(a, b, e, p, mt, nt256, num_sms, err, s, pdl);
+    if (narrow) return gemm_tc_go<WT, GEMM_RESID, 128, WIDE>(a, b, e, p, mt, (p.N + 127) / 128, num_sms, err, s, pdl);
+    return gemm_tc_go<WT, GEMM_RESID, 256, WIDE>(a, b, e, p, mt, nt256, num_sms, err, s, pdl);
   }
-  if (narrow) return gemm_tc_go<WT, GEMM_QKV, 128>(a, b, e, p, mt, (p.N + 127) / 128, num_sms, err, s, pdl);
-  return gemm_tc_go<WT, GEMM_QKV, 256>(a, b, e, p, mt, nt256, num_sms, err, s, pdl);
+  if (narrow) return gemm_tc_go<WT, GEMM_QKV, 128, WIDE>(a, b, e, p, mt, (p.N + 127) / 128, num_sms, err, s, pdl);
+  return gemm_tc_go<WT, GEMM_QKV, 256, WIDE>(a, b, e, p, mt, nt256, num_sms, err, s, pdl);
 }
 
 cudaError_t launch_gemm_tc(const TmaOperand* a, const TmaOperand* b0, const TmaOperand* b1, const TmaOperand* b2,
                            const void* e_in, const void* e_out, const GemmParams& p, int mode, int wdt, int num_sms,
-                           int* err, cudaStream_t s, bool pdl) {
+                           int* err, cudaStream_t s, bool pdl, bool wide) {
   if (p.M <= 0) return cudaSuccess;
   // RESID reads and writes its rows through the epilogue maps, GATEUP writes through e_out
   if ((mode == GEMM_RESID && (!e_in || !e_out)) || (mode == GEMM_GATEUP && !e_out)) return cudaErrorInvalidValue;
   if (mode == GEMM_RESID && p.N % 256) return cudaErrorInvalidValue;  // every 32-column block of a tile exists
+  if (wide && mode == GEMM_GATEUP && p.lo_row <= 0) return cudaErrorInvalidValue;  // where the lo plane's rows start
   const TmaOperand* b[3] = {b0, b1, b2};
   const void* e[2] = {e_in, e_out};
   const int mt = (p.M + TC_BM - 1) / TC_BM;
-  return wdt == WDT_F16 ? gemm_tc_dispatch<f16>(a, b, e, p, mode, mt, num_sms, err, s, pdl)
-                        : gemm_tc_dispatch<bf16>(a, b, e, p, mode, mt, num_sms, err, s, pdl);
+  if (wide)
+    return wdt == WDT_F16 ? gemm_tc_dispatch<f16, 1>(a, b, e, p, mode, mt, num_sms, err, s, pdl)
+                          : gemm_tc_dispatch<bf16, 1>(a, b, e, p, mode, mt, num_sms, err, s, pdl);
+  return wdt == WDT_F16 ? gemm_tc_dispatch<f16, 0>(a, b, e, p, mode, mt, num_sms, err, s, pdl)
+                        : gemm_tc_dispatch<bf16, 0>(a, b, e, p, mode, mt, num_sms, err, s, pdl);
 }
 
 }  // namespace ladder

@@ -28,6 +28,10 @@ template <> struct W16<bf16> {
     __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&t);
   }
+  // either half of a packed pair is inf or NaN
+  static __device__ __forceinline__ bool bad(uint32_t v) {
+    return (v & 0x7f800000u) == 0x7f800000u || (v & 0x7f80u) == 0x7f80u;
+  }
   static constexpr uint32_t umma_fmt = 1;
 };
 template <> struct W16<f16> {
@@ -37,7 +41,18 @@ template <> struct W16<f16> {
     __half2 t = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&t);
   }
+  // either half of a packed pair is inf or NaN (overflow past 65504 included)
+  static __device__ __forceinline__ bool bad(uint32_t v) {
+    return (v & 0x7c000000u) == 0x7c000000u || (v & 0x7c00u) == 0x7c00u;
+  }
   static constexpr uint32_t umma_fmt = 0;
+};
+
+// Error-word bits set by the kernels (read back with ladder_get_device_error).
+enum ErrorBits {
+  ERR_TOKEN = 1,      // token id out of range (its row was computed from a zero embedding)
+  ERR_TIMEOUT = 2,    // a pipeline wait ran out of time; the kernel stopped early
+  ERR_NONFINITE = 4   // a projection produced inf or NaN (e.g. a value beyond the 16-bit range)
 };
 
 // ---------------------------------------------------------------------------
@@ -181,6 +196,7 @@ enum GemmMode { GEMM_QKV = 0, GEMM_GATEUP = 1, GEMM_RESID = 2 };
 struct GemmParams {
   int M, N, K;
   void* out_h;          // QKV: q [M][ldo]; GATEUP: act [M][ldo] (weight dtype)
+  int lo_row;           // GATEUP with hi/lo operands: first row of the lo plane in the e_out map (0: none)
   float* out_f;         // RESID: x_out [M][ldo]
   int ldo;
   const float* x_res;   // RESID
@@ -201,6 +217,7 @@ struct AttnPrefillParams {
   int n_q;
   float scale;
   void* out;            // [M][n_q * hd] in the weight dtype (operand of the O projection)
+  size_t lo_off;        // > 0: the rounding remainders go to out + lo_off (the lo plane)
 };
 
 // ---------------------------------------------------------------------------
@@ -238,17 +255,24 @@ cudaError_t launch_rope_tables(float* cos_t, float* sin_t, int max_seq, int hd, 
 
 // Prefill launches take `pdl` (programmatic dependent launch); every kernel
 // launched with it waits for the previous kernel before touching its data.
-cudaError_t launch_rmsnorm_rows(const float* x, int M, int d, const void* g, float eps, void* out, int wdt,
-                                cudaStream_t s, bool pdl = false);
+// lo_off > 0: the rounding remainder of each value (value minus its 16-bit
+// rounding, itself rounded to 16 bits) goes to out + lo_off (the lo plane).
+cudaError_t launch_rmsnorm_rows(const float* x, int M, int d, const void* g, float eps, void* out, size_t lo_off,
+                                int wdt, cudaStream_t s, bool pdl = false);
 // Tensor-core GEMM (tcgen05 + TMA).  Maps are CUtensorMap objects made by make_tma_map.
 // 2-D map of a row-major [rows, cols] 16-bit matrix, box 64 columns x 128 rows.
 bool make_tma_map(void* map_out, const void* base, uint64_t rows, uint64_t cols, int wdt);
 // GEMM operand: the same matrix as 3-D [cols / 64][rows][64], with boxes of
-// 128 rows x 1 and x 2 chunks (box[0], box[1]).
+// 128 rows x 1 and x 2 chunks (box[0], box[1]).  An activation operand held
+// as a hi/lo pair of planes (the hi matrix [rows][cols], then the lo matrix
+// right after it) also gets `pair`: a 4-D view [cols / 64][2][rows][64] whose
+// box of 128 rows x 2 planes x 1 chunk lands as the hi block, then the lo block.
 struct TmaOperand {
   CUtensorMap box[2];
+  CUtensorMap pair;
 };
-bool make_tma_operand(TmaOperand* out, const void* base, uint64_t rows, uint64_t cols, int wdt);
+bool make_tma_operand(TmaOperand* out, const void* base, uint64_t rows, uint64_t cols, int wdt,
+                      bool with_pair = false);
 // Epilogue block map (box 32 x 32): fp32 rows (elem_bytes 4) or weight-dtype rows (2).
 bool make_tma_map_epilogue(void* map_out, const void* base, uint64_t rows, uint64_t cols, int elem_bytes, int wdt);
 // One layer of the paged KV pool as a 3-D map (see gemm_tcgen05.cu).
@@ -256,9 +280,11 @@ bool make_kv_tma_map(void* map_out, const void* base, uint64_t num_pages, int n_
 cudaError_t gemm_tc_configure();
 // e_in / e_out: make_tma_map_epilogue maps of the residual rows and the output
 // rows (RESID, fp32) or of the SwiGLU output rows (GATEUP e_out, weight dtype).
+// wide: A is a hi/lo pair (a->pair); every k step multiplies both halves by
+// the same weight tile, so C = W * (hi + lo).
 cudaError_t launch_gemm_tc(const TmaOperand* a, const TmaOperand* b0, const TmaOperand* b1, const TmaOperand* b2,
                            const void* e_in, const void* e_out, const GemmParams& p, int mode, int wdt, int num_sms,
-                           int* err, cudaStream_t s, bool pdl = false);
+                           int* err, cudaStream_t s, bool pdl = false, bool wide = false);
 // Tensor-core causal attention for packed prefill rows (mma.sync, bf16 Q/K/V).
 // Prefill attention on tcgen05: q_map = make_tma_map of the query rows, kv_map =
 // make_kv_tma_map of the layer; head_dim 64 or 128.

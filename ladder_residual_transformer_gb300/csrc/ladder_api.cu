@@ -77,10 +77,12 @@ Plan make_plan(const ladder_config& c) {
     return o;
   };
   for (int i = 0; i < 3; ++i) p.x[i] = take(M * d * 4);
-  p.xn = take(Mp * d * 2);
+  // Prefill GEMM A operands: a hi plane [Mp][K] and a lo plane [Mp][K] (the
+  // 16-bit rounding remainders) right after it; decode reuses ao / act as fp32 rows.
+  p.xn = take(2 * Mp * d * 2);
   p.q = take(std::max(Mp * qd * 2, Bm * qd * 4));
-  p.ao = take(std::max(Mp * qd * 2, Bm * qd * 4));
-  p.act = take(std::max(Mp * f * 2, Bm * f * 4));
+  p.ao = take(std::max(2 * Mp * qd * 2, Bm * qd * 4));
+  p.act = take(std::max(2 * Mp * f * 2, Bm * f * 4));
   p.part_o = take(Bm * c.n_q_heads * (size_t)p.nsplit_max * c.head_dim * 4);
   p.part_ml = take(Bm * c.n_q_heads * (size_t)p.nsplit_max * 2 * 4);
   p.am_v = take(Bm * kArgmaxBlocks * 4);
@@ -390,14 +392,14 @@ int ladder_create(const ladder_config* cfg, const ladder_weights* w, void* works
     const uint64_t d = c.d_model, qd = (uint64_t)c.n_q_heads * c.head_dim, kvd = (uint64_t)c.n_kv_heads * c.head_dim;
     const uint64_t f = c.ffn_dim, Mp = plan.m_pad;
     const int wdt = c.weight_dtype;
-    bool ok = make_tma_operand(&m->map_xn, m->ws + plan.xn, Mp, d, wdt) &&
-              make_tma_operand(&m->map_ao, m->ws + plan.ao, Mp, qd, wdt) &&
-              make_tma_operand(&m->map_act, m->ws + plan.act, Mp, f, wdt) &&
+    bool ok = make_tma_operand(&m->map_xn, m->ws + plan.xn, Mp, d, wdt, true) &&
+              make_tma_operand(&m->map_ao, m->ws + plan.ao, Mp, qd, wdt, true) &&
+              make_tma_operand(&m->map_act, m->ws + plan.act, Mp, f, wdt, true) &&
               make_tma_map(&m->map_q, m->ws + plan.q, Mp, qd, wdt) &&
               make_tma_map_epilogue(&m->map_x[0], m->ws + plan.x[0], plan.m_max, d, 4, wdt) &&
               make_tma_map_epilogue(&m->map_x[1], m->ws + plan.x[1], plan.m_max, d, 4, wdt) &&
               make_tma_map_epilogue(&m->map_x[2], m->ws + plan.x[2], plan.m_max, d, 4, wdt) &&
-              make_tma_map_epilogue(&m->map_act_st, m->ws + plan.act, Mp, f, 2, wdt);
+              make_tma_map_epilogue(&m->map_act_st, m->ws + plan.act, 2 * Mp, f, 2, wdt);
     m->maps.resize(c.n_layers);
     for (int l = 0; ok && l < c.n_layers; ++l) {
       const LayerW& L = m->layers[l];
@@ -462,7 +464,7 @@ int ladder_set_mode(ladder_model* m, int residual_mode, int flags) {
   if (residual_mode != LADDER_RESIDUAL_CONFIG && residual_mode != LADDER_RESIDUAL_STANDARD &&
       residual_mode != LADDER_RESIDUAL_PARALLEL)
     return fail(LADDER_ERR_INVALID, "unknown residual mode %d", residual_mode);
-  if (flags & ~(LADDER_FLAG_DECODE_GRAPH | LADDER_FLAG_NO_PDL | LADDER_FLAG_ALL_LOGITS))
+  if (flags & ~(LADDER_FLAG_DECODE_GRAPH | LADDER_FLAG_NO_PDL | LADDER_FLAG_ALL_LOGITS | LADDER_FLAG_FAST_PREFILL))
     return fail(LADDER_ERR_INVALID, "unknown flags 0x%x", flags);
   if (residual_mode != m->residual_mode || flags != m->flags) m->drop_graphs();
   m->residual_mode = residual_mode;
@@ -1022,6 +1024,11 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
   // Every prefill kernel waits for its predecessor before touching memory, so
   // each one is launched early and its prologue overlaps the previous tail.
   const bool pdl = !(m->flags & LADDER_FLAG_NO_PDL);
+  // GEMM A operands as hi/lo pairs (the default) or rounded once (LADDER_FLAG_FAST_PREFILL).
+  const bool wide = !(m->flags & LADDER_FLAG_FAST_PREFILL);
+  const size_t Mp = P.m_pad;
+  const size_t lo_xn = wide ? Mp * d : 0, lo_ao = wide ? Mp * qd : 0;
+  const int lo_act = wide ? (int)Mp : 0;
 
   LAUNCH(launch_embed(tokens, M, m->embed, wdt, d, c.vocab, m->X(0), m->err(), s, pdl), 1);
   for (int l = 0; l < c.n_layers; ++l) {
@@ -1030,35 +1037,36 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
     const KvLayer kvl = kv->layer(l);
     {
       const int k = 2 * l + 1;
-      LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.attn_norm, c.norm_eps, xn, wdt, s, pdl), 1);
+      LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.attn_norm, c.norm_eps, xn, lo_xn, wdt, s, pdl), 1);
       GemmParams g{};
       g.M = M; g.N = qd + 2 * kvd; g.K = d;
       g.out_h = qb; g.ldo = qd; g.nq_hd = qd; g.nkv_hd = kvd;
       g.rope_cos = m->at<float>(P.rope_cos); g.rope_sin = m->at<float>(P.rope_sin);
       g.row_b = d_row_b; g.row_pos = d_row_pos; g.kv = kvl;
-      LAUNCH(launch_gemm_tc(&m->map_xn, &T.wq, &T.wk, &T.wv, nullptr, nullptr, g, GEMM_QKV, wdt, m->num_sms, m->err(), s, pdl), 1);
+      LAUNCH(launch_gemm_tc(&m->map_xn, &T.wq, &T.wk, &T.wv, nullptr, nullptr, g, GEMM_QKV, wdt, m->num_sms, m->err(), s,
+                            pdl, wide), 1);
 
       AttnPrefillParams a{};
       a.q = qb; a.kv = kvl; a.seq_start = d_start; a.seq_len = d_lens;
-      a.n_q = c.n_q_heads; a.scale = 1.0f / sqrtf((float)c.head_dim); a.out = aob;
+      a.n_q = c.n_q_heads; a.scale = 1.0f / sqrtf((float)c.head_dim); a.out = aob; a.lo_off = lo_ao;
       LAUNCH(launch_attn_prefill_tcgen05(&m->map_q, &kv->maps[l], a, c.head_dim, wdt, B, max_len, m->err(), s, pdl), 1);
 
       GemmParams o{};
       o.M = M; o.N = d; o.K = qd; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);
       LAUNCH(launch_gemm_tc(&m->map_ao, &T.wo, nullptr, nullptr, &m->map_x[(k - 1) % 3], &m->map_x[k % 3], o,
-                            GEMM_RESID, wdt, m->num_sms, m->err(), s, pdl), 1);
+                            GEMM_RESID, wdt, m->num_sms, m->err(), s, pdl, wide), 1);
     }
     {
       const int k = 2 * l + 2;
-      LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.mlp_norm, c.norm_eps, xn, wdt, s, pdl), 1);
+      LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.mlp_norm, c.norm_eps, xn, lo_xn, wdt, s, pdl), 1);
       GemmParams g{};
-      g.M = M; g.N = f; g.K = d; g.out_h = actb; g.ldo = f;
+      g.M = M; g.N = f; g.K = d; g.out_h = actb; g.ldo = f; g.lo_row = lo_act;
       LAUNCH(launch_gemm_tc(&m->map_xn, &T.gate, &T.up, nullptr, nullptr, &m->map_act_st, g, GEMM_GATEUP, wdt,
-                            m->num_sms, m->err(), s, pdl), 1);
+                            m->num_sms, m->err(), s, pdl, wide), 1);
       GemmParams o{};
       o.M = M; o.N = d; o.K = f; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);
       LAUNCH(launch_gemm_tc(&m->map_act, &T.down, nullptr, nullptr, &m->map_x[(k - 1) % 3], &m->map_x[k % 3], o,
-                            GEMM_RESID, wdt, m->num_sms, m->err(), s, pdl), 1);
+                            GEMM_RESID, wdt, m->num_sms, m->err(), s, pdl, wide), 1);
     }
   }
   GemvParams h{};

@@ -31,6 +31,7 @@ RESIDUAL_PARALLEL = 2
 FLAG_DECODE_GRAPH = 1
 FLAG_NO_PDL = 2
 FLAG_ALL_LOGITS = 4
+FLAG_FAST_PREFILL = 8
 
 # Entry points declared in include/ladder.h, with (restype, argtypes).
 _vp, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
@@ -305,19 +306,24 @@ class LadderModel:
 
     # -- modes -----------------------------------------------------------
     def set_mode(self, standard: bool = False, graph: bool = False, pdl: bool = True, parallel: bool = False,
-                 all_logits: bool = False):
+                 all_logits: bool = False, fast_prefill: bool = False):
         """Residual schedule: as configured (default), every layer standard
         (``standard``), or every layer a parallel attention + MLP block
         (``parallel``); decode launch flags; ``all_logits``: prefill returns the
-        logits of every packed position ([sum of lens, vocab])."""
+        logits of every packed position ([sum of lens, vocab]);
+        ``fast_prefill``: prefill GEMM activations rounded once to 16 bits
+        instead of carried as hi/lo pairs (half the tensor-core work, less
+        accurate on deep models; see LADDER_FLAG_FAST_PREFILL)."""
         if standard and parallel:
             raise ValueError("standard and parallel are exclusive")
         flags = (FLAG_DECODE_GRAPH if graph else 0) | (0 if pdl else FLAG_NO_PDL) | (FLAG_ALL_LOGITS if all_logits else 0)
+        flags |= FLAG_FAST_PREFILL if fast_prefill else 0
         mode = RESIDUAL_STANDARD if standard else RESIDUAL_PARALLEL if parallel else RESIDUAL_CONFIG
         check(lib().ladder_set_mode(self._m, mode, flags))
         self._standard = standard
         self._parallel = parallel
         self._all_logits = all_logits
+        self._fast_prefill = fast_prefill
 
     def set_sampling(self, temperature: float = 0.0, top_k: int = 0, seed: int = 0):
         """Next-token rule of prefill / decode_step: greedy (temperature <= 0) or

@@ -113,8 +113,9 @@ class OracleWeights:
     """Weights in the oracle's dtype, produced on demand by ``source(name, layer)``.
 
     ``source`` returns an array of the tensor's shape (any float dtype).  Layers
-    are kept after first use unless ``keep_layers`` is False, in which case each
-    ``layer(l)`` call produces them again (used for models larger than host RAM).
+    are kept after first use unless ``keep_layers`` is False, in which case only
+    the most recently used layer is kept and any other ``layer(l)`` call produces
+    its weights again (used for models larger than host RAM).
     """
 
     def __init__(self, dims: dict, source: Callable[[str, int], np.ndarray],
@@ -139,9 +140,10 @@ class OracleWeights:
     def layer(self, l: int) -> LayerWeights:
         if l in self._layers:
             return self._layers[l]
+        if not self._keep:
+            self._layers.clear()  # drop the previous layer before producing the next one
         lw = LayerWeights(**{k: self._get(k, l) for k in synth.LAYER_KINDS})
-        if self._keep:
-            self._layers[l] = lw
+        self._layers[l] = lw
         return lw
 
 

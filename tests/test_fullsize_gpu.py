@@ -1,32 +1,46 @@
-"""Full-size workloads on the GPU.
+"""Full-size workloads on the GPU against the oracle.
 
-8B hybrid (32 layers, lower 16 standard) against the oracle at full depth; the
-70B shapes (d_model 8192, 64 q / 8 kv heads of 128, SwiGLU 28672) with 4 of
-their 80 layers against the oracle; and the full 80-layer 70B model (141 GB of
-weights resident on the GPU) through properties that hold at any size: decode
-with the KV cache agrees with re-running prefill on the extended prompt, and
-repeated runs give identical logits.
+- 8B hybrid (32 layers, lower 16 standard) at full depth: prefill of two
+  prompts and two teacher-forced decode steps.
+- 8B full ladder in shard mode (k = 8 row/column shards per module, the
+  on-device reduce on the second stream): the ladder and the standard schedule
+  against the all-ladder and all-standard oracle.
+- 70B (80 layers, d_model 8192, 64 q / 8 kv heads of 128, SwiGLU 28672; 141 GB
+  of weights resident on the GPU): prefill and two decode steps at full depth
+  against the oracle, which regenerates one layer at a time so that host memory
+  stays bounded; and properties that hold at any size: decode with the KV cache
+  agrees with re-running prefill on the extended prompt, and repeated runs give
+  identical logits.
+
+The oracle's logits for a prefill of T tokens followed by decode steps fed
+tokens f_1, f_2 are the rows T - 1, T, T + 1 of one all-position forward pass
+over the prompt extended by f_1, f_2 (cached decode equals re-running prefill,
+a property the oracle's own tests pin).  That takes one pass over the weights
+instead of three.
+
+Every comparison is at the logit tolerance (max-abs 3e-2, relative L2 1e-2)
+with the default prefill, whose GEMM activations are hi/lo pairs.  Where the
+fast prefill (activations rounded once to 16 bits) runs too, its error is
+printed and required to be larger than the default's; at these depths it does
+not stay within max-abs 3e-2.
 """
-import json
-import os
-
 import numpy as np
 import pytest
 import torch
 
 import oracle.ladder_oracle as O
-from ladder_residual_transformer_gb300 import ladder, synth
+from ladder_residual_transformer_gb300 import synth
 
 from gpu_common import compare_logits, gpu_weights, make_model, packed, prompts_for
 
 pytestmark = pytest.mark.gpu
 
 
-def run_tf(model, prompts, feed, graph=True):
+def run_tf(model, prompts, feed, graph=True, fast_prefill=False, standard=False):
     s = torch.cuda.Stream()
     out = []
     with torch.cuda.stream(s):
-        model.set_mode(graph=graph)
+        model.set_mode(graph=graph, fast_prefill=fast_prefill, standard=standard)
         lg, _ = model.prefill(packed(prompts), [len(p) for p in prompts])
         out.append(lg.cpu().numpy())
         tok = torch.empty(len(prompts), dtype=torch.int32, device="cuda")
@@ -36,6 +50,26 @@ def run_tf(model, prompts, feed, graph=True):
             out.append(lg.cpu().numpy())
     s.synchronize()
     return np.stack(out)
+
+
+def oracle_tf(dims, W, prompts, feed):
+    """Oracle logits [steps + 1, B, V] of prefill + teacher-forced decode, from
+    one all-position forward pass per sequence over prompt + feed."""
+    S = feed.shape[1]
+    seqs = [np.concatenate([p, feed[b]]).astype(np.int32) for b, p in enumerate(prompts)]
+    rows = O.forward(dims, W, seqs, [O.SeqCache() for _ in seqs], all_positions=True)
+    out = np.empty((S + 1, len(prompts), dims["vocab"]), dtype=np.float32)
+    for b, p in enumerate(prompts):
+        out[:, b] = rows[b][len(p) - 1:]
+    return out
+
+
+def compare_steps(got, want, what):
+    return [compare_logits(got[s], want[s], f"{what} step {s}") for s in range(got.shape[0])]
+
+
+def rel_sum(got, want):
+    return sum(np.linalg.norm(got[s] - want[s]) / np.linalg.norm(want[s]) for s in range(got.shape[0]))
 
 
 def test_device_generator_matches_host_generator():
@@ -61,45 +95,74 @@ def test_full_size_8b_hybrid():
     gw = gpu_weights(dims)
     model = make_model(dims, gw, max_batch=2, max_seq=512, max_prefill_tokens=sum(lens))
     got = run_tf(model, prompts, feed)
+    model.reset()
+    fast = run_tf(model, prompts, feed, fast_prefill=True)
     model.close()
     del gw, model
     torch.cuda.empty_cache()
-    want, _ = O.teacher_forced_decode(dims, O.synthetic_weights(dims), prompts, feed)
-    # Relative L2 is held to 1e-2.  The max-abs bound is 3e-2, or 1.15x the error
-    # of an exactly rounded fp16-activation pipeline on these very inputs when
-    # that floor is higher (tests/golden/fp16_floor.py writes it from the oracle:
-    # 3.18e-2 for these 32 random layers, so no 16-bit implementation can meet 3e-2).
-    floor = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "fp16_floor_8b_hybrid.json")))
-    max_abs = max(3e-2, 1.15 * floor["max_abs"])
-    for s in range(3):
-        err = np.abs(got[s] - want[s]).max()
-        rel = np.linalg.norm(got[s] - want[s]) / np.linalg.norm(want[s])
-        print(f"8B hybrid step {s}: max-abs {err:.3e} rel-L2 {rel:.3e} (fp16 floor {floor['max_abs']:.3e})")
-        assert np.isfinite(got[s]).all()
-        assert err <= max_abs and rel <= 1e-2, (s, err, rel)
+    want = oracle_tf(dims, O.synthetic_weights(dims, keep_layers=False), prompts, feed)
+    er = compare_steps(got, want, "8B hybrid")
+    fe = max(float(np.abs(fast[s] - want[s]).max()) for s in range(3))
+    print(f"8B hybrid: max-abs {max(e for e, _ in er):.3e} rel-L2 {max(r for _, r in er):.3e}; "
+          f"fast prefill max-abs {fe:.3e}")
+    assert rel_sum(got, want) < rel_sum(fast, want)
 
 
 @pytest.mark.slow
-def test_70b_shapes_four_layers():
-    dims = dict(synth.PRESETS["70b"], n_layers=4)
-    lens = [64]
-    prompts = prompts_for(lens, dims["vocab"])
+def test_full_size_8b_ladder_shard_mode():
+    """Config of the shard-mode comparison: 8B shapes, every layer ladder,
+    k = 8 shards per module at decode (prefill is unsharded), batch 1; the
+    ladder schedule against the all-ladder oracle and the standard schedule
+    (every module waits for the previous module's reduce) against the
+    all-standard oracle."""
+    dims = dict(synth.PRESETS["8b-ladder"])
+    prompt = prompts_for([64], dims["vocab"])
     feed = synth.tokens(2, dims["vocab"], seed=synth.DECODE_SEED)[None, :]
     gw = gpu_weights(dims)
-    model = make_model(dims, gw, max_batch=1, max_seq=128, max_prefill_tokens=64)
-    got = run_tf(model, prompts, feed)
+    model = make_model(dims, gw, max_batch=1, max_seq=128, max_prefill_tokens=64, shard_k=8)
+    got_l = run_tf(model, prompt, feed)
+    model.reset()
+    got_s = run_tf(model, prompt, feed, standard=True)
     model.close()
     del gw, model
     torch.cuda.empty_cache()
-    want, _ = O.teacher_forced_decode(dims, O.synthetic_weights(dims), prompts, feed)
-    for s in range(3):
-        compare_logits(got[s], want[s], f"70B shapes step {s}")
+    W = O.synthetic_weights(dims, keep_layers=False)
+    compare_steps(got_l, oracle_tf(dims, W, prompt, feed), "8B ladder, shard k = 8")
+    std = dict(dims, n_standard_layers=dims["n_layers"])
+    compare_steps(got_s, oracle_tf(std, W, prompt, feed), "8B standard, shard k = 8")
+
+
+@pytest.fixture(scope="module")
+def weights_70b():
+    dims = dict(synth.PRESETS["70b"])
+    gw = gpu_weights(dims)
+    yield dims, gw
+    del gw
+    torch.cuda.empty_cache()
 
 
 @pytest.mark.slow
-def test_full_70b_cached_decode_agrees_with_prefill_and_is_deterministic():
-    dims = dict(synth.PRESETS["70b"])
-    gw = gpu_weights(dims)
+def test_full_size_70b_all_layers(weights_70b):
+    """All 80 layers: a 32-token prompt and two teacher-forced decode steps."""
+    dims, gw = weights_70b
+    prompt = prompts_for([32], dims["vocab"])
+    feed = synth.tokens(2, dims["vocab"], seed=synth.DECODE_SEED)[None, :]
+    model = make_model(dims, gw, max_batch=1, max_seq=64, max_prefill_tokens=64)
+    got = run_tf(model, prompt, feed)
+    model.reset()
+    fast = run_tf(model, prompt, feed, fast_prefill=True)
+    model.close()
+    want = oracle_tf(dims, O.synthetic_weights(dims, keep_layers=False), prompt, feed)
+    er = compare_steps(got, want, "70B")
+    fe = max(float(np.abs(fast[s] - want[s]).max()) for s in range(3))
+    print(f"70B: max-abs {max(e for e, _ in er):.3e} rel-L2 {max(r for _, r in er):.3e}; "
+          f"fast prefill max-abs {fe:.3e}")
+    assert rel_sum(got, want) < rel_sum(fast, want)
+
+
+@pytest.mark.slow
+def test_full_70b_cached_decode_agrees_with_prefill_and_is_deterministic(weights_70b):
+    dims, gw = weights_70b
     prompt = synth.tokens(34, dims["vocab"])
     model = make_model(dims, gw, max_batch=1, max_seq=64, max_prefill_tokens=64)
     feed = prompt[None, 32:34]

@@ -40,7 +40,7 @@ def test_binding_constants_match_the_header():
         assert getattr(ladder, "LADDER_" + name) == enum["LADDER_" + name], name
     for name in ("CONFIG", "STANDARD", "PARALLEL"):
         assert getattr(ladder, "RESIDUAL_" + name) == enum["LADDER_RESIDUAL_" + name], name
-    for name in ("DECODE_GRAPH", "NO_PDL", "ALL_LOGITS"):
+    for name in ("DECODE_GRAPH", "NO_PDL", "ALL_LOGITS", "FAST_PREFILL"):
         assert getattr(ladder, "FLAG_" + name) == enum["LADDER_FLAG_" + name], name
     for cls, v in ladder.PROBE_CLASSES.items():
         key = "LADDER_PROBE_" + {"out": "OUT", "gateup": "GATEUP", "lmhead": "LMHEAD"}.get(cls, cls.upper())

@@ -30,7 +30,8 @@ def run_teacher_forced(model, prompts, feed, graph=False, standard=None, paralle
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         model.set_mode(graph=graph, standard=getattr(model, "_standard", False) if standard is None else standard,
-                       parallel=getattr(model, "_parallel", False) if parallel is None else parallel)
+                       parallel=getattr(model, "_parallel", False) if parallel is None else parallel,
+                       fast_prefill=getattr(model, "_fast_prefill", False))
         logits, nxt = model.prefill(packed(prompts), [len(p) for p in prompts])
         out, toks = [logits.cpu().numpy()], [nxt.cpu().numpy()]
         tok_dev = torch.empty(len(prompts), dtype=torch.int32, device="cuda")
@@ -52,7 +53,8 @@ def test_tiny_greedy_tokens_and_logits(tiny):
     model = make_model(dims, gw, max_batch=1, max_seq=64)
     g_logits, g_toks = run_teacher_forced(model, prompts, o_toks[:, :8])
     errs = [compare_logits(g_logits[s], o_logits[s], f"step {s}")[0] for s in range(9)]
-    check_greedy(g_toks[:, 0], o_logits[:, 0], 2 * max(errs))
+    ties = check_greedy(g_toks[:, 0], o_logits[:, 0], 2 * max(errs))
+    print("steps decided by the near-tie rule:", ties)
     # free-running greedy generation on the device (token fed back without the host)
     model.reset()
     s = torch.cuda.Stream()
@@ -208,6 +210,46 @@ def test_prefill_repeats_bitwise():
         assert np.array_equal(r, g_logits)
 
 
+FAST_GEOMETRIES = {
+    # name: (dims overrides, prompt lengths, weight dtype)
+    "narrow ragged": (dict(d_model=512, n_q_heads=8, n_kv_heads=2, head_dim=64, ffn_dim=1024), [300, 150], "fp16"),
+    "paired 256x256": (dict(d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=2048), [2048, 2048],
+                       "fp16"),
+    "hd128 split K": (dict(d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=3072), [100, 257, 3],
+                      "fp16"),
+    "bf16": (dict(), [16, 70], "bf16"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FAST_GEOMETRIES))
+def test_prefill_precisions_match_oracle(name):
+    """Both prefill precisions on every GEMM tile shape (128-wide tiles with a
+    ragged last m tile, paired 256 x 256 tiles, 256-wide tiles with K in two
+    chunks) and on bf16 storage: each within the logit tolerance, the hi/lo
+    default strictly closer to the oracle than the once-rounded fast mode, and
+    the two not bitwise equal (the lo planes take part)."""
+    over, lens, dtype = FAST_GEOMETRIES[name]
+    dims = small_dims(vocab=2048, n_layers=2, n_standard_layers=0, **over)
+    ow = oracle_weights(dims)
+    prompts = prompts_for(lens, dims["vocab"])
+    feed = np.stack([synth.tokens(2, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(len(lens))])
+    model = make_model(dims, gpu_weights(dims, dtype=dtype), max_batch=len(lens), max_seq=max(lens) + 64,
+                       page_size=64 if max(lens) > 64 else 32)
+    got = {}
+    for fast in (False, True):
+        model._fast_prefill = fast
+        model.reset()
+        got[fast] = run_teacher_forced(model, prompts, feed, graph=True)[0]
+    model.close()
+    o_logits, _ = O.teacher_forced_decode(dims, ow, prompts, feed)
+    err = {}  # relative L2 error summed over the three steps
+    for fast in (False, True):
+        err[fast] = sum(compare_logits(got[fast][s], o_logits[s], f"{name} fast={fast} step {s}")[1] for s in range(3))
+    print(f"{name}: summed rel-L2 hi/lo {err[False]:.3e}, fast {err[True]:.3e}")
+    assert not np.array_equal(got[False], got[True])
+    assert err[False] < err[True]
+
+
 @pytest.mark.parametrize("B", [3, 4, 16, 21])
 def test_batched_decode_on_tensor_cores(B):
     """Decode batches of 3 rows and more run on the mma.sync projection in chunks
@@ -237,9 +279,11 @@ def test_ragged_batch_prefill_and_decode(tiny):
     model = make_model(dims, gw, max_batch=6, max_seq=96, page_size=32)
     g_logits, g_toks = run_teacher_forced(model, prompts, feed)
     o_logits, _ = O.teacher_forced_decode(dims, ow, prompts, feed)
+    errs = [compare_logits(g_logits[s], o_logits[s], f"step {s}")[0] for s in range(4)]
+    # every row of every step: the oracle's argmax unless its top-2 margin is
+    # inside twice the observed logit error (then a near-maximal candidate)
     for s in range(4):
-        compare_logits(g_logits[s], o_logits[s], f"step {s}")
-    assert (g_toks[0] == O.argmax_lowest(o_logits[0])).mean() >= 5 / 6
+        check_greedy(g_toks[s], o_logits[s], 2 * max(errs))
 
 
 @pytest.mark.parametrize("nstd,strict", [(1, 0), (1, 1), (3, 0)])
@@ -411,18 +455,31 @@ def test_host_and_device_errors(tiny):
 @pytest.mark.slow
 def test_full_size_1p2b_prefill_and_decode():
     """The 1.2B workload at its full prompt length, in the graph-replay launch
-    configuration the benchmark times, against the oracle on the same inputs."""
+    configuration the benchmark times, against the oracle on the same inputs,
+    with the prefill GEMM activations as hi/lo pairs (the default) and rounded
+    once (fast prefill): both within the logit tolerance at this depth."""
     dims = dict(synth.PRESETS["1.2b"])
     gw = gpu_weights(dims)
     prompts = prompts_for([1024], dims["vocab"])
     feed = synth.tokens(3, dims["vocab"], seed=synth.DECODE_SEED)[None, :]
     model = make_model(dims, gw, max_batch=1, max_seq=1024 + 256, max_prefill_tokens=1024)
-    g_logits, g_toks = run_teacher_forced(model, prompts, feed, graph=True)
+    runs = {}
+    for fast in (False, True):
+        model._fast_prefill = fast
+        model.reset()
+        runs[fast] = run_teacher_forced(model, prompts, feed, graph=True)
+    model.close()
     del gw, model
     torch.cuda.empty_cache()
     o_logits, _ = O.teacher_forced_decode(dims, O.synthetic_weights(dims), prompts, feed)
-    errs = [compare_logits(g_logits[s], o_logits[s], f"1.2B step {s}")[0] for s in range(4)]
-    check_greedy(g_toks[:, 0], o_logits[:, 0], 2 * max(errs))
+    rel = {}
+    for fast, (g_logits, g_toks) in runs.items():
+        er = [compare_logits(g_logits[s], o_logits[s], f"1.2B fast={fast} step {s}") for s in range(4)]
+        ties = check_greedy(g_toks[:, 0], o_logits[:, 0], 2 * max(e for e, _ in er))
+        rel[fast] = sum(r for _, r in er)
+        print(f"1.2B fast_prefill={fast}: max-abs {max(e for e, _ in er):.3e} rel-L2 {max(r for _, r in er):.3e}; "
+              f"steps decided by the near-tie rule: {ties}")
+    assert rel[False] < rel[True]  # the hi/lo operands are the more accurate prefill
 
 
 @pytest.mark.parametrize("k,standard,graph", [(2, False, False), (2, True, True), (4, False, True), (4, True, False)])
