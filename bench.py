@@ -1,18 +1,26 @@
 #!/usr/bin/env python3
 """Decode and prefill throughput of the Ladder Transformer forward pass on one GB300.
 
-Default workload: the 1.2B Ladder Transformer (16 ladder layers, d_model 2048,
-32 query / 8 KV heads of 64, SwiGLU 8192, vocab 128256, tied embeddings,
-random-init bf16 weights), batch 1, a 1024-token random prompt and 256 greedy
-decode steps.  One step = one prefill of the prompt plus the 256 decode steps,
-with the greedy token fed back on the device.  Every step streams the 2.47 GB
-of weights (more than the 129 MB L2), so no L2 flush is needed between steps.
+Headline workload: the 70B-shape Ladder Transformer (80 ladder layers, d_model
+8192, 64 query / 8 KV heads of 128, SwiGLU 28672, vocab 128256, random-init
+bf16-valued weights, 141 GB resident on the GPU), batch 1.  One step =
+  (a) an untimed 2048-token prefill that fills the KV cache,
+  (b) 64 greedy decode steps from context 2048 (timed: `value`, decode tok/s),
+  (c) a 512-token prefill from an empty cache (timed: `prefill`).
+Every decode step streams all 139 GB of weights and the KV cache (far more
+than the 129 MB L2), so no flush is needed between steps.
 
-Prints one JSON line.  `value` is decode tokens/s over all ranks; prefill
-tokens/s, the roofline of the dominant kernel, the end-to-end figure through
-the host API and the CPU oracle baseline ride along.
+The other workloads ride along as nested entries of the same line (`configs`),
+each timed the same way on its own model: the 1.2B ladder model (prompt 1024,
+256 decode steps; with the standard and parallel-block schedules on the same
+weights), the 8B hybrid (decode at batch 1 and 16 from context 2048; prefill
+of 4 x 4096 tokens), and the 8B full ladder in shard mode (k = 8; ladder vs
+standard schedule, batch 1 decode from context 2048).
+
+Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-nested]
 """
 from __future__ import annotations
 
@@ -35,15 +43,26 @@ from ladder_residual_transformer_gb300 import synth  # noqa: E402
 
 METRIC = "decode tok/s & % HBM roofline; prefill tok/s & % BF16 tensor peak (1 GB300)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-
-# DRAM traffic of the dominant kernel from one ncu capture, valid only while the
-# kernel source is unchanged (sha256 of the file that defines it).
+DTYPE = ("fp16 storage of the bf16-valued weights; fp16 tensor-core operands (prefill GEMM activations "
+         "as fp16 hi/lo pairs); fp32 accumulation and residual stream; fp16 KV cache")
 L2_BYTES = 129 * 10 ** 6  # GB300 L2 cache
-NCU_TRAFFIC = {  # mean of the two captured launches
-    "source": "ladder_residual_transformer_gb300/csrc/decode_kernels.cu",
-    "sha256": "9b1e41e127b124917a06d8b238fa1c5057abf915ac462157c3231eff74ea9e39",
-    "bytes_per_launch": 67253120,
+
+# What each workload's step runs.  ctx: decode starts from a prompt of this many
+# tokens (prefilled untimed); prefill: the timed prefill's prompt lengths.
+PLANS = {
+    "70b": {"decode": [{"batch": 1, "ctx": 2048, "steps": 64}], "prefill": [512]},
+    "1.2b": {"decode": [{"batch": 1, "ctx": 1024, "steps": 256}], "prefill": [1024], "schedules": True},
+    "8b-hybrid": {"decode": [{"batch": 1, "ctx": 2048, "steps": 128}, {"batch": 16, "ctx": 2048, "steps": 128}],
+                  "prefill": [4096] * 4},
+    "8b-ladder": {"decode": [{"batch": 1, "ctx": 2048, "steps": 128}], "prefill": [], "shard_k": 8},
+    "tiny": {"decode": [{"batch": 1, "ctx": 16, "steps": 8}], "prefill": [16]},
 }
+NESTED = ("1.2b", "8b-hybrid", "8b-ladder")
+
+# DRAM traffic of the dominant kernel (the decode gate/up GEMV) per launch at
+# each workload's shape, from one ncu capture, valid only while the kernel's
+# source file is unchanged (its sha256).
+NCU_TRAFFIC = {}
 
 
 # ---------------------------------------------------------------------------
@@ -188,24 +207,49 @@ def sum_over_ranks(values, world, device="cpu"):
 # ---------------------------------------------------------------------------
 # CPU oracle baseline (bounded sample of the same workload)
 # ---------------------------------------------------------------------------
-def oracle_sample(dims, prompt_len, decode_steps, W=None):
-    """Time the oracle on prefill of `prompt_len` tokens + `decode_steps` decode
-    steps of the same model; returns (prefill tok/s, decode tok/s, seconds)."""
+def sample_dims(dims, layers):
+    """The first `layers` layers of a workload (every layer has the same shapes)."""
+    out = dict(dims, n_layers=min(layers, dims["n_layers"]))
+    out["n_standard_layers"] = min(dims["n_standard_layers"], out["n_layers"])
+    return out
+
+
+def oracle_sample(dims, prompt_len, decode_steps, layers=None, W=None):
+    """Time the oracle on a prefill of `prompt_len` tokens and `decode_steps`
+    greedy decode steps of the workload cut to its first `layers` layers (all
+    when None; weights generated before timing), and scale the measured times
+    to the full depth by the ratio of algorithmic work: weight bytes per decode
+    step (the oracle's decode is a chain of matrix-vector products over fp32
+    weights) and flops per prefill.  Returns a dict with prefill / decode tok/s
+    at full depth, the seconds timed, and the weights for reuse."""
     import oracle.ladder_oracle as O
+    sd = sample_dims(dims, layers or dims["n_layers"])
     if W is None:
-        W = O.synthetic_weights(dims)
-        for l in range(dims["n_layers"]):
+        W = O.synthetic_weights(sd)
+        for l in range(sd["n_layers"]):
             W.layer(l)
         W.glob("embed"), W.glob("lm_head"), W.glob("final_norm")
-    prompt = [synth.tokens(prompt_len, dims["vocab"])]
+    prompt = [synth.tokens(prompt_len, sd["vocab"])]
     t0 = time.perf_counter()
-    logits, caches = O.prefill(dims, W, prompt)
+    logits, caches = O.prefill(sd, W, prompt)
     t1 = time.perf_counter()
     tok = O.argmax_lowest(logits)
     for _ in range(decode_steps):
-        tok = O.argmax_lowest(O.decode_step(dims, W, tok, caches))
+        tok = O.argmax_lowest(O.decode_step(sd, W, tok, caches))
     t2 = time.perf_counter()
-    return prompt_len / (t1 - t0), decode_steps / (t2 - t1), t2 - t0, W
+    dec_scale = (decode_step_bytes(dims, [prompt_len]) / decode_step_bytes(sd, [prompt_len]))
+    pre_scale = prefill_flops(dims, [prompt_len]) / prefill_flops(sd, [prompt_len])
+    return {"prefill_tok_s": prompt_len / ((t1 - t0) * pre_scale),
+            "decode_tok_s": decode_steps / ((t2 - t1) * dec_scale),
+            "seconds": t2 - t0, "layers": sd["n_layers"], "W": W}
+
+
+def sample_text(name, dims, r, prompt_len, decode_steps, threads):
+    cut = (f"its first {r['layers']} of {dims['n_layers']} layers (times scaled to full depth by the ratio of "
+           f"decode weight bytes and of prefill flops), " if r["layers"] < dims["n_layers"] else "")
+    return (f"{name}: the oracle (fp32 numpy) on {cut}a prefill of {prompt_len} tokens "
+            f"({r['prefill_tok_s']:.3g} tok/s) + {decode_steps} greedy decode steps, {threads} BLAS thread(s), "
+            f"{r['seconds']:.1f} s timed, weights generated before timing")
 
 
 def cpu_threads():
@@ -215,263 +259,367 @@ def cpu_threads():
     return os.cpu_count()
 
 
+def one_core_sample(name, prompt_len, decode_steps, layers):
+    """The same oracle sample in a child process limited to one BLAS thread."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", name, str(prompt_len),
+           str(decode_steps), str(layers)]
+    try:
+        out = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+        return json.loads(out.stdout.strip().splitlines()[-1])
+    except Exception as e:  # reported, not fatal: the GPU numbers stand on their own
+        return {"error": f"{type(e).__name__}: {e}"}
+
+
+# Bounded oracle samples: (prompt tokens, decode steps, layers) per workload.
+ORACLE_SAMPLES = {"70b": (32, 4, 4), "1.2b": (64, 4, 16), "8b-hybrid": (64, 4, 8), "8b-ladder": (64, 4, 8),
+                  "tiny": (16, 8, 2)}
+
+
+def cpu_baseline(name, dims):
+    prompt_len, decode_steps, layers = ORACLE_SAMPLES[name]
+    r = oracle_sample(dims, prompt_len, decode_steps, layers)
+    out = {"value": r["decode_tok_s"], "unit": "tok/s", "cores": cpu_threads(), "kind": "oracle",
+           "sample": sample_text(name, dims, r, prompt_len, decode_steps, cpu_threads()),
+           "prefill_tok_s": r["prefill_tok_s"]}
+    del r["W"]
+    # the 1.2B workload's oracle on one core, alongside
+    one = one_core_sample("1.2b", *ORACLE_SAMPLES["1.2b"])
+    if "error" not in one:
+        one["sample"] = sample_text("1.2b", synth.PRESETS["1.2b"], one, ORACLE_SAMPLES["1.2b"][0],
+                                    ORACLE_SAMPLES["1.2b"][1], 1)
+    out["one_core_1p2b"] = one
+    return out
+
+
 # ---------------------------------------------------------------------------
-# Arms
+# Reference arm: the oracle, timed as it stands on the host cores
 # ---------------------------------------------------------------------------
 def run_reference(args, dims):
     rank, world, _ = dist_env()
     if rank != 0:
         return None
+    prompt_len, decode_steps, layers = ORACLE_SAMPLES[args.workload]
     W = None
     for _ in range(args.warmup):
-        _, _, _, W = oracle_sample(dims, args.ref_prompt, args.ref_decode, W)
+        r = oracle_sample(dims, prompt_len, decode_steps, layers, W)
+        W = r["W"]
     pre, dec, secs = [], [], []
     for _ in range(args.steps):
-        p, d, s, W = oracle_sample(dims, args.ref_prompt, args.ref_decode, W)
-        pre.append(p)
-        dec.append(d)
-        secs.append(s)
-    value = args.ref_decode * args.steps / sum(args.ref_decode / d for d in dec)
-    sample = (f"{args.workload}: oracle prefill of {args.ref_prompt} tokens + {args.ref_decode} greedy decode "
-              f"steps per step (fp32 numpy, weights generated before timing)")
+        r = oracle_sample(dims, prompt_len, decode_steps, layers, W)
+        W = r["W"]
+        pre.append(r["prefill_tok_s"])
+        dec.append(r["decode_tok_s"])
+        secs.append(r["seconds"])
+    value = len(dec) / sum(1.0 / d for d in dec)  # decode tok/s over all timed steps
+    r["seconds"] = statistics.mean(secs)
+    r["prefill_tok_s"] = statistics.mean(pre)
+    sample = sample_text(args.workload, dims, r, prompt_len, decode_steps, cpu_threads())
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic", "config": workload_config(args, dims),
+        "data": "synthetic", "config": workload_config(args.workload, dims),
         "prefill": {"value": statistics.mean(pre), "unit": "tok/s"},
         "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cpu_threads(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
-def workload_config(args, dims):
-    return {"workload": f"{args.workload} Ladder Transformer ({dims['n_layers']} layers, "
-                        f"{dims['n_standard_layers']} standard), d_model {dims['d_model']}, "
-                        f"{dims['n_q_heads']}q/{dims['n_kv_heads']}kv heads x {dims['head_dim']}, "
-                        f"ffn {dims['ffn_dim']}, vocab {dims['vocab']}",
-            "batch": args.batch, "prompt_tokens": args.prompt, "decode_steps": args.decode,
-            "l2": ("inputs larger than L2 (all weights streamed every step)" if decode_step_bytes(dims, [0]) > L2_BYTES
-                   else "weights fit in L2 (a parity-size model, not a roofline workload)")}
+def workload_config(name, dims):
+    plan = PLANS[name]
+    cfg = {"workload": f"{name} Ladder Transformer ({dims['n_layers']} layers, "
+                       f"{dims['n_standard_layers']} standard), d_model {dims['d_model']}, "
+                       f"{dims['n_q_heads']}q/{dims['n_kv_heads']}kv heads x {dims['head_dim']}, "
+                       f"ffn {dims['ffn_dim']}, vocab {dims['vocab']}" +
+                       (f", shard mode k = {plan['shard_k']}" if plan.get("shard_k") else ""),
+           "decode": [dict(d) for d in plan["decode"]], "prefill_tokens": list(plan["prefill"]),
+           "l2": ("inputs larger than L2 (all weights streamed every step)" if decode_step_bytes(dims, [0]) > L2_BYTES
+                  else "weights fit in L2 (a parity-size model, not a roofline workload)")}
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+def measure_workload(name, dims, steps, warmup, args, peaks, dev, world, headline):
+    """Build the workload's model on the device and time its step (every phase
+    of PLANS[name]) `steps` times after `warmup` untimed steps."""
+    import torch
+    from ladder_residual_transformer_gb300 import ladder
+
+    plan = PLANS[name]
+    shard_k = plan.get("shard_k", 1) if args.shard_k is None else args.shard_k
+    phases = plan["decode"]
+    pre_lens = list(plan["prefill"])
+    max_batch = max([d["batch"] for d in phases] + [len(pre_lens)])
+    max_seq = max([d["ctx"] + d["steps"] + 1 for d in phases] + pre_lens)
+    max_pre = max([d["batch"] * d["ctx"] for d in phases] + [sum(pre_lens)])
+    weights = ladder.synthetic_weights(dims, device=dev)
+    model = ladder.LadderModel(dims, weights, max_batch=max_batch, max_seq=max_seq, max_prefill_tokens=max_pre,
+                               shard_k=shard_k)
+    stream = torch.cuda.Stream(device=dev)
+    # every input is resident on the device before any timing
+    dec_in = []
+    for d in phases:
+        prompts = [synth.tokens(d["ctx"], dims["vocab"], stream=b) for b in range(d["batch"])]
+        dec_in.append((prompts, torch.from_numpy(np.concatenate(prompts).astype(np.int32)).to(dev)))
+    pre_prompts = [synth.tokens(n, dims["vocab"], stream=b) for b, n in enumerate(pre_lens)]
+    pre_dev = torch.from_numpy(np.concatenate(pre_prompts).astype(np.int32)).to(dev) if pre_lens else None
+    tok = torch.zeros(max_batch, dtype=torch.int32, device=dev)
+    logits = torch.empty(max_batch, dims["vocab"], dtype=torch.float32, device=dev)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    def one_step(fast_prefill=False, decode=True, prefill=True, **mode):
+        """One pass over the phases; returns (decode ms per phase, prefill ms, launches)."""
+        launches, d_ev, p_ev = 0, [], None
+        model.set_mode(graph=not args.eager, pdl=not args.no_pdl, fast_prefill=fast_prefill, **mode)
+        for d, (prompts, pdev) in zip(phases if decode else [], dec_in):
+            B = d["batch"]
+            model.reset(stream)
+            model.prefill(pdev, [d["ctx"]] * B, logits[:B], tok[:B], stream)  # fills the context, untimed
+            e0, e1 = ev(), ev()
+            e0.record(stream)
+            for _ in range(d["steps"]):
+                model.decode_step(tok[:B], logits[:B], tok[:B], stream)
+                launches += model.last_launch_count()
+            e1.record(stream)
+            d_ev.append((e0, e1))
+        if pre_lens and prefill:
+            Bp = len(pre_lens)
+            model.reset(stream)
+            e0, e1 = ev(), ev()
+            e0.record(stream)
+            model.prefill(pre_dev, pre_lens, logits[:Bp], tok[:Bp], stream)
+            launches += model.last_launch_count()
+            e1.record(stream)
+            p_ev = (e0, e1)
+        stream.synchronize()
+        return ([a.elapsed_time(b) for a, b in d_ev], p_ev[0].elapsed_time(p_ev[1]) if p_ev else None, launches)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            one_step()
+        stream.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        clocks = ClockSampler(torch.cuda.current_device())
+        dec_ms = [[] for _ in phases]
+        pre_ms, launches = [], 0
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            d, p, n = one_step()
+            for i, v in enumerate(d):
+                dec_ms[i].append(v)
+            if p is not None:
+                pre_ms.append(p)
+            launches += n
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        barrier(world)
+        clk = clocks.stop()
+
+        # The prefill with its activations rounded once (LADDER_FLAG_FAST_PREFILL).
+        fast_ms = []
+        if pre_lens:
+            for i in range(warmup + min(steps, 5)):
+                _, p, _ = one_step(fast_prefill=True, decode=False)
+                if i >= warmup:
+                    fast_ms.append(p)
+
+        # Dominant kernel of decode: time each gate/up GEMV launch over one eager
+        # pass of the first decode phase.
+        d0 = phases[0]
+        model.set_mode(graph=False, pdl=not args.no_pdl)
+        model.reset(stream)
+        model.prefill(dec_in[0][1], [d0["ctx"]] * d0["batch"], logits[:d0["batch"]], tok[:d0["batch"]], stream)
+        model.probe_begin("gateup", d0["steps"] * dims["n_layers"])
+        for _ in range(d0["steps"]):
+            model.decode_step(tok[:d0["batch"]], logits[:d0["batch"]], tok[:d0["batch"]], stream)
+        n_probe, probe_ms = model.probe_end()
+        stream.synchronize()
+
+    out = {"config": workload_config(name, dims)}
+    # decode phases
+    out["decode"] = []
+    for d, ms in zip(phases, dec_ms):
+        tot = max_over_ranks([sum(ms)], world, dev)[0]
+        toks = sum_over_ranks([float(d["batch"] * d["steps"] * len(ms))], world, dev)[0]
+        bytes_step = statistics.mean(decode_step_bytes(dims, [d["ctx"] + i] * d["batch"]) for i in range(d["steps"]))
+        gbs = bytes_step * d["steps"] * len(ms) / (sum(ms) / 1e3) / 1e9
+        out["decode"].append({"batch": d["batch"], "ctx": d["ctx"], "steps": d["steps"],
+                              "tok_s": toks / (tot / 1e3), "ms_per_token": sum(ms) / (d["steps"] * len(ms)),
+                              "achieved_gbs": gbs, "peak_gbs": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
+                              "bytes_per_step": bytes_step})
+    if pre_ms:
+        pf = prefill_flops(dims, pre_lens)
+        tot = max_over_ranks([sum(pre_ms)], world, dev)[0]
+        toks = sum_over_ranks([float(sum(pre_lens) * len(pre_ms))], world, dev)[0]
+        tf = pf * len(pre_ms) / (sum(pre_ms) / 1e3) / 1e12
+        ftf = pf * len(fast_ms) / (sum(fast_ms) / 1e3) / 1e12 if fast_ms else None
+        out["prefill"] = {
+            "value": toks / (tot / 1e3), "unit": "tok/s", "ms": sum(pre_ms) / len(pre_ms), "tokens": pre_lens,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": tf / peaks["bf16_tflops"], "flops": pf,
+                         "note": "algorithmic flops (2 x rows x weights + causal attention + last-row lm_head); "
+                                 "the hi/lo activation operands issue twice the GEMM tensor-core work"},
+            "fast": {"ms": statistics.mean(fast_ms), "tok_s": sum(pre_lens) / (statistics.mean(fast_ms) / 1e3),
+                     "achieved_tflops": ftf, "frac": ftf / peaks["bf16_tflops"],
+                     "note": "LADDER_FLAG_FAST_PREFILL: activations rounded once to 16 bits"} if fast_ms else None}
+    gu_bytes = 2 * 2 * dims["ffn_dim"] * dims["d_model"]  # gate + up rows, 16-bit
+    gu_s = probe_ms / max(n_probe, 1) / 1e3
+    gu_gbs = gu_bytes / gu_s / 1e9 if gu_s > 0 else None
+    traffic = None
+    t = NCU_TRAFFIC.get(name)
+    if t and d0["batch"] == 1:
+        src = os.path.join(ROOT, t["source"])
+        if os.path.exists(src) and hashlib.sha256(open(src, "rb").read()).hexdigest() == t["sha256"]:
+            traffic = t["bytes_per_launch"]
+    out["roofline"] = {"bound": "hbm", "kernel": "decode gate/up GEMV (RMSNorm + SwiGLU fused)",
+                       "achieved": gu_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                       "frac": gu_gbs / peaks["hbm_gbs"] if gu_gbs else None, "traffic": traffic,
+                       "algorithmic_bytes_per_launch": gu_bytes, "launches_timed": n_probe,
+                       "timing": "CUDA events on the launching stream around each launch, one eager pass of the "
+                                 "first decode phase right after the timed region"}
+    out["clocks"] = clk
+    out["gpu_launches"] = launches
+    out["wall_s"] = wall
+    out["steps"], out["warmup"] = steps, warmup
+    out["ms_per_step"] = (sum(sum(m) for m in dec_ms) + sum(pre_ms)) / steps
+
+    # the same weights and kernels under the other residual schedules
+    ns = min(steps, 5)
+    if plan.get("schedules") and not args.no_schedules:
+        sch = {}
+        for label, mode in (("standard", {"standard": True}), ("parallel", {"parallel": True})):
+            d_all, p_all = [], []
+            for i in range(warmup + ns):
+                d, p, _ = one_step(**mode)
+                if i >= warmup:
+                    d_all.append(d[0])
+                    p_all.append(p)
+            sch[label] = {"decode_tok_s": phases[0]["batch"] * phases[0]["steps"] * ns / (sum(d_all) / 1e3),
+                          "prefill_ms": statistics.mean(p_all) if p_all[0] is not None else None}
+        sch["configured"] = {"decode_tok_s": out["decode"][0]["tok_s"] / world,
+                             "prefill_ms": out["prefill"]["ms"] if pre_ms else None}
+        sch["note"] = ("same weights and kernels; configured = the workload's ladder/hybrid schedule; standard = "
+                       "every layer standard; parallel = every layer a parallel attention + MLP block")
+        out["schedules"] = sch
+    if shard_k > 1 and not args.no_schedules:
+        d_all = []
+        for i in range(warmup + ns):
+            d, _, _ = one_step(prefill=False, standard=True)
+            if i >= warmup:
+                d_all.append(d[0])
+        out["shard"] = {"k": shard_k, "ladder_decode_tok_s": out["decode"][0]["tok_s"] / world,
+                        "standard_decode_tok_s": phases[0]["batch"] * phases[0]["steps"] * ns / (sum(d_all) / 1e3),
+                        "note": "same weights and kernels; standard = every module waits for the previous "
+                                "module's reduce; ladder = each module waits for the reduce two modules back"}
+
+    # end to end through the host API: host prompt in, host tokens out
+    if headline and not args.no_e2e:
+        prompts = dec_in[0][0]
+        reps = min(steps, 5)
+        with torch.cuda.stream(stream):
+            model.set_mode(graph=not args.eager, pdl=not args.no_pdl)
+            model.generate(prompts, d0["steps"], stream)
+            ts = []
+            for _ in range(reps):
+                t = time.perf_counter()
+                model.generate(prompts, d0["steps"], stream)
+                ts.append(time.perf_counter() - t)
+        tmax = max_over_ranks([sum(ts)], world, dev)[0]
+        gen = sum_over_ranks([float(d0["batch"] * d0["steps"] * reps)], world, dev)[0]
+        out["e2e"] = {"value": gen / tmax, "unit": "tok/s",
+                      "timed": f"generate(): pinned H2D of the {d0['ctx']}-token prompt, its prefill, "
+                               f"{d0['steps']} decode steps, D2H of the tokens; wall clock, prefill included",
+                      "h2d_bytes_per_step": 4 * d0["batch"] * d0["ctx"],
+                      "d2h_bytes_per_step": 4 * d0["batch"] * (d0["steps"] + 1)}
+    model.close()
+    del model, weights
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args, dims):
     import torch
-    from ladder_residual_transformer_gb300 import ladder
 
     rank, world, local = dist_env()
     dist_init(world, "nccl")
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
     peaks, peak_src = load_peaks()
-
-    weights = ladder.synthetic_weights(dims, device=dev)
-    B = args.batch
-    lens = [args.prompt] * B
-    shard_k = synth.RUNS[args.workload].get("shard_k", 1) if args.shard_k is None else args.shard_k
-    model = ladder.LadderModel(dims, weights, max_batch=B, max_seq=args.prompt + args.decode + 1,
-                               max_prefill_tokens=sum(lens), shard_k=shard_k)
-    prompts = [synth.tokens(n, dims["vocab"], stream=b) for b, n in enumerate(lens)]
-    prompt_dev = torch.from_numpy(np.concatenate(prompts).astype(np.int32)).to(dev)
-    stream = torch.cuda.Stream(device=dev)
-    tok = torch.empty(B, dtype=torch.int32, device=dev)
-    logits = torch.empty(B, dims["vocab"], dtype=torch.float32, device=dev)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-
-    def step(record=True):
-        model.reset(stream)
-        if record:
-            ev[0].record(stream)
-        model.prefill(prompt_dev, lens, logits, tok, stream)
-        n_pre = model.last_launch_count()
-        if record:
-            ev[1].record(stream)
-        n_dec = 0
-        for _ in range(args.decode):
-            model.decode_step(tok, logits, tok, stream)
-            n_dec += model.last_launch_count()
-        if record:
-            ev[2].record(stream)
-        return n_pre + n_dec
-
-    with torch.cuda.stream(stream):
-        model.set_mode(graph=not args.eager, pdl=not args.no_pdl)
-        for _ in range(args.warmup):
-            step(record=False)
-        stream.synchronize()
-        barrier(world)
-        torch.cuda.synchronize()
-        clocks = ClockSampler(local)
-        pre_ms, dec_ms, launches = [], [], 0
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            launches += step()
-            stream.synchronize()
-            pre_ms.append(ev[0].elapsed_time(ev[1]))
-            dec_ms.append(ev[1].elapsed_time(ev[2]))
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
-        barrier(world)
-        clk = clocks.stop()
-
-        # Dominant kernel: time each gate/up GEMV launch over one eager step's decode.
-        model.set_mode(graph=False, pdl=not args.no_pdl)
-        model.reset(stream)
-        model.prefill(prompt_dev, lens, logits, tok, stream)
-        model.probe_begin("gateup", args.decode * dims["n_layers"])
-        for _ in range(args.decode):
-            model.decode_step(tok, logits, tok, stream)
-        n_probe, probe_ms = model.probe_end()
-        stream.synchronize()
-
-    # The same weights and kernels under the other residual schedules (the pages'
-    # comparison: standard, where every module waits for the previous one, and
-    # the parallel-block model), each timed like the configured schedule above.
-    def time_schedule(**mode):
-        d_ms, p_ms = [], []
-        with torch.cuda.stream(stream):
-            model.set_mode(graph=not args.eager, pdl=not args.no_pdl, **mode)
-            for i in range(args.warmup + args.steps):
-                step(record=True)
-                stream.synchronize()
-                if i >= args.warmup:
-                    p_ms.append(ev[0].elapsed_time(ev[1]))
-                    d_ms.append(ev[1].elapsed_time(ev[2]))
-            model.set_mode(graph=not args.eager, pdl=not args.no_pdl)
-        return {"decode_tok_s": B * args.decode * len(d_ms) / (sum(d_ms) / 1e3),
-                "prefill_ms": sum(p_ms) / len(p_ms)}
-
-    schedules = None
-    shard = None
-    if not args.no_schedules:
-        schedules = {"configured": {"decode_tok_s": B * args.decode * args.steps / (sum(dec_ms) / 1e3),
-                                    "prefill_ms": sum(pre_ms) / len(pre_ms)},
-                     "standard": time_schedule(standard=True),
-                     "parallel": time_schedule(parallel=True),
-                     "note": "same weights and kernels; configured = the workload's ladder/hybrid schedule; "
-                             "standard = every layer standard; parallel = every layer a parallel "
-                             "attention + MLP block"}
-        if shard_k > 1:
-            shard = {"k": shard_k, "ladder_decode_tok_s": schedules["configured"]["decode_tok_s"],
-                     "standard_decode_tok_s": schedules["standard"]["decode_tok_s"],
-                     "note": "same weights and kernels; standard = every module waits for the previous "
-                             "module's reduce"}
-
-    tot_pre, tot_dec = sum(pre_ms), sum(dec_ms)
-    tot_pre, tot_dec = max_over_ranks([tot_pre, tot_dec], world, dev)
-    dec_tokens = sum_over_ranks([float(B * args.decode * args.steps)], world, dev)[0]
-    pre_tokens = sum_over_ranks([float(sum(lens) * args.steps)], world, dev)[0]
-    decode_tps = dec_tokens / (tot_dec / 1e3)
-    prefill_tps = pre_tokens / (tot_pre / 1e3)
-    ms_per_step = (tot_pre + tot_dec) / args.steps
-
-    # whole-decode and prefill rooflines
-    ctx0 = args.prompt
-    dec_bytes = sum(decode_step_bytes(dims, [ctx0 + i] * B) for i in range(args.decode))
-    dec_gbs = dec_bytes * args.steps / (sum(dec_ms) / 1e3) / 1e9
-    pf = prefill_flops(dims, lens)
-    pre_tf = pf * args.steps / (sum(pre_ms) / 1e3) / 1e12
-
-    gu_bytes = 2 * 2 * dims["ffn_dim"] * dims["d_model"]  # gate + up rows, bf16
-    gu_avg_s = probe_ms / max(n_probe, 1) / 1e3
-    gu_gbs = gu_bytes / gu_avg_s / 1e9 if gu_avg_s > 0 else None
-    traffic = None
-    if NCU_TRAFFIC and args.workload == "1.2b" and B == 1:
-        src = os.path.join(ROOT, NCU_TRAFFIC["source"])
-        if os.path.exists(src) and hashlib.sha256(open(src, "rb").read()).hexdigest() == NCU_TRAFFIC["sha256"]:
-            traffic = NCU_TRAFFIC["bytes_per_launch"]
-
-    # end to end through the host API: host prompt in, host tokens out
-    e2e = None
-    if not args.no_e2e:
-        with torch.cuda.stream(stream):
-            model.set_mode(graph=not args.eager, pdl=not args.no_pdl)
-            model.generate(prompts, args.decode, stream)
-            ts = []
-            for _ in range(args.steps):
-                t = time.perf_counter()
-                model.generate(prompts, args.decode, stream)
-                ts.append(time.perf_counter() - t)
-        tmax = max_over_ranks([sum(ts)], world, dev)[0]
-        e2e = {"value": dec_tokens / tmax, "unit": "tok/s",
-               "timed": "generate(): pinned H2D of the prompt, prefill, decode steps, D2H of the tokens; "
-                        "wall clock per step, prefill included",
-               "h2d_bytes_per_step": 4 * sum(lens), "d2h_bytes_per_step": 4 * B * (args.decode + 1)}
-
+    t_start = time.perf_counter()
+    head = measure_workload(args.workload, dims, args.steps, args.warmup, args, peaks, dev, world, headline=True)
+    nested = {}
+    if not args.no_nested and args.workload == "70b":
+        for name in NESTED:
+            try:
+                nested[name] = measure_workload(name, dict(synth.PRESETS[name]), min(args.steps, 5),
+                                                max(3, min(args.warmup, 3)), args, peaks, dev, world, headline=False)
+            except Exception as e:  # recorded in the line; the headline stands
+                nested[name] = {"error": f"{type(e).__name__}: {e}"}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        p_tps, d_tps, secs, _ = oracle_sample(dims, args.cpu_prompt, args.cpu_decode)
-        cpu = {"value": d_tps, "unit": "tok/s", "cores": cpu_threads(), "kind": "oracle",
-               "sample": f"{args.workload}: oracle prefill of {args.cpu_prompt} tokens "
-                         f"({p_tps:.1f} tok/s) + {args.cpu_decode} decode steps, fp32 numpy, "
-                         f"{secs:.1f} s timed",
-               "prefill_tok_s": p_tps}
-
+        cpu = cpu_baseline(args.workload, dims)
+    d0 = head["decode"][0]
+    plan = PLANS[args.workload]
     out = {
-        "metric": METRIC, "value": decode_tps, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init weights, random tokens)",
-        "config": dict(workload_config(args, dims), parallelism=f"replicas x{world}",
-                       decode_launch=("eager" if args.eager else "cuda graph") + (", no PDL" if args.no_pdl else ", PDL")),
-        "decode": {"tok_s": decode_tps, "achieved_gbs": dec_gbs, "peak_gbs": peaks["hbm_gbs"],
-                   "frac": dec_gbs / peaks["hbm_gbs"], "bytes_per_step": dec_bytes / args.decode},
-        "prefill": {"value": prefill_tps, "unit": "tok/s", "ms": tot_pre / args.steps,
-                    "roofline": {"bound": "tensor", "achieved": pre_tf, "peak": peaks["bf16_tflops"],
-                                 "unit": "TFLOP/s", "frac": pre_tf / peaks["bf16_tflops"], "flops": pf}},
-        "roofline": {"bound": "hbm", "kernel": "decode gate/up GEMV (RMSNorm + SwiGLU fused)",
-                     "achieved": gu_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": gu_gbs / peaks["hbm_gbs"] if gu_gbs else None, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": gu_bytes, "launches_timed": n_probe,
-                     "timing": "CUDA events on the launching stream around each launch, one eager "
-                               "step's decode right after the timed region"},
+        "metric": METRIC, "value": d0["tok_s"], "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": DTYPE, "data": "synthetic (random-init weights, random tokens)",
+        "config": dict(head["config"], batch=plan["decode"][0]["batch"], decode_ctx=plan["decode"][0]["ctx"],
+                       decode_steps=plan["decode"][0]["steps"], parallelism=f"replicas x{world}",
+                       decode_launch=("eager" if args.eager else "cuda graph") + (", no PDL" if args.no_pdl else ", PDL"),
+                       step=("untimed prefill of the decode context, timed decode steps, timed prefill of "
+                             "prefill_tokens from an empty cache")),
+        "decode": d0,
+        "prefill": head.get("prefill"),
+        "roofline": head["roofline"],
         "peaks": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'fallback 6.8 TB/s, 1.9 PF bf16'})",
-        "gpu_launches": launches, "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "shard": shard,
-        "schedules": schedules,
-        "wall_s": wall,
+        "gpu_launches": head["gpu_launches"], "clocks": head["clocks"], "e2e": head.get("e2e"),
+        "cpu_baseline": cpu,
+        "shard": head.get("shard"), "schedules": head.get("schedules"),
+        "configs": nested or None,
+        "wall_s": time.perf_counter() - t_start,
     }
-    if rank == 0:
-        return out
-    return None
+    if len(head["decode"]) > 1:
+        out["decode_phases"] = head["decode"]
+    return out if rank == 0 else None
 
 
 def main():
+    if len(sys.argv) > 1 and sys.argv[1] == "--oracle-sample":
+        # child process of one_core_sample: name prompt decode layers -> JSON
+        name, prompt_len, decode_steps, layers = sys.argv[2], int(sys.argv[3]), int(sys.argv[4]), int(sys.argv[5])
+        r = oracle_sample(dict(synth.PRESETS[name]), prompt_len, decode_steps, layers)
+        del r["W"]
+        print(json.dumps(dict(r, cores=1, unit="tok/s", value=r["decode_tok_s"], kind="oracle")))
+        return
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="1.2b", choices=sorted(synth.PRESETS))
-    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--workload", default="70b", choices=sorted(PLANS))
     ap.add_argument("--shard-k", type=int, default=None, help="shard mode k (default: the workload's)")
-    ap.add_argument("--prompt", type=int, default=None)
-    ap.add_argument("--decode", type=int, default=None)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-pdl", action="store_true", help="decode without programmatic dependent launch")
     ap.add_argument("--eager", action="store_true", help="decode without CUDA-graph replay")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-nested", action="store_true", help="time the named workload only")
     ap.add_argument("--layers", type=int, default=None,
                     help="cut the workload to this many layers (for kernel captures; the line names the count)")
     ap.add_argument("--no-schedules", action="store_true",
                     help="skip timing the standard and parallel-block schedules on the same weights")
-    ap.add_argument("--cpu-prompt", type=int, default=None, help="oracle sample prompt (default: the workload's)")
-    ap.add_argument("--cpu-decode", type=int, default=None, help="oracle sample decode steps (default: the workload's)")
-    ap.add_argument("--ref-prompt", type=int, default=64)
-    ap.add_argument("--ref-decode", type=int, default=4)
     args = ap.parse_args()
     dims = dict(synth.PRESETS[args.workload])
     if args.layers:
         # kernel captures on a shallow copy of the workload (every layer has the same shapes)
-        dims["n_layers"] = args.layers
-        dims["n_standard_layers"] = min(dims["n_standard_layers"], args.layers // 2)
-    run = synth.RUNS[args.workload]
-    if args.prompt is None:
-        args.prompt = run["prompt"]
-    if args.decode is None:
-        args.decode = run["decode_steps"]
-    if args.cpu_prompt is None:
-        args.cpu_prompt = args.prompt
-    if args.cpu_decode is None:
-        args.cpu_decode = args.decode
+        dims = sample_dims(dims, args.layers)
+        args.no_nested = True
     out = run_reference(args, dims) if args.impl == "reference" else run_ours(args, dims)
     if out is not None:
         print(json.dumps(out), flush=True)

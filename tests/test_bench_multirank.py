@@ -56,8 +56,7 @@ def test_reference_arm_prints_one_json_line():
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny", "--steps", "2",
-                        "--warmup", "1", "--ref-prompt", "16", "--ref-decode", "2"],
-                       cwd=root, capture_output=True, text=True, timeout=600)
+                        "--warmup", "1"], cwd=root, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.strip()]
     assert len(lines) == 1
@@ -72,3 +71,21 @@ def test_reference_arm_prints_one_json_line():
         r = subprocess.run([sys.executable, "bench.py", "--workload", "tiny", "--steps", "1", "--warmup", "1",
                             "--no-cpu-baseline"], cwd=root, capture_output=True, text=True, timeout=600)
         assert r.returncode != 0 and not r.stdout.strip()
+
+
+def test_oracle_sample_scales_a_cut_model_by_its_work():
+    """The bounded oracle sample of a deep model runs its first layers and
+    scales the times by the ratio of algorithmic work; on the full depth the
+    scale is 1; the one-thread child process reports the same fields."""
+    import bench
+    from ladder_residual_transformer_gb300 import synth
+    dims = dict(synth.PRESETS["tiny"], n_layers=4)
+    cut = bench.sample_dims(dims, 2)
+    assert cut["n_layers"] == 2 and cut["n_standard_layers"] == 0
+    r = bench.oracle_sample(dims, 8, 2, layers=2)
+    assert r["layers"] == 2 and r["decode_tok_s"] > 0 and r["prefill_tok_s"] > 0
+    assert bench.decode_step_bytes(dims, [8]) > bench.decode_step_bytes(cut, [8])
+    full = bench.oracle_sample(dims, 8, 2)
+    assert full["layers"] == 4
+    one = bench.one_core_sample("tiny", 8, 2, 2)
+    assert one["cores"] == 1 and one["layers"] == 2 and one["value"] > 0
