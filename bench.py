@@ -204,6 +204,14 @@ def sum_over_ranks(values, world, device="cpu"):
     return t.tolist()
 
 
+_T0 = time.perf_counter()
+
+
+def log(msg):
+    """Progress on stderr (the JSON line is the only stdout output)."""
+    print(f"[bench {time.perf_counter() - _T0:7.1f} s] {msg}", file=sys.stderr, flush=True)
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle baseline (bounded sample of the same workload)
 # ---------------------------------------------------------------------------
@@ -272,7 +280,7 @@ def one_core_sample(name, prompt_len, decode_steps, layers):
 
 
 # Bounded oracle samples: (prompt tokens, decode steps, layers) per workload.
-ORACLE_SAMPLES = {"70b": (32, 4, 4), "1.2b": (64, 4, 16), "8b-hybrid": (64, 4, 8), "8b-ladder": (64, 4, 8),
+ORACLE_SAMPLES = {"70b": (64, 24, 8), "1.2b": (128, 32, 16), "8b-hybrid": (64, 16, 8), "8b-ladder": (64, 16, 8),
                   "tiny": (16, 8, 2)}
 
 
@@ -355,9 +363,11 @@ def measure_workload(name, dims, steps, warmup, args, peaks, dev, world, headlin
     max_batch = max([d["batch"] for d in phases] + [len(pre_lens)])
     max_seq = max([d["ctx"] + d["steps"] + 1 for d in phases] + pre_lens)
     max_pre = max([d["batch"] * d["ctx"] for d in phases] + [sum(pre_lens)])
+    log(f"{name}: generating weights on the device")
     weights = ladder.synthetic_weights(dims, device=dev)
     model = ladder.LadderModel(dims, weights, max_batch=max_batch, max_seq=max_seq, max_prefill_tokens=max_pre,
                                shard_k=shard_k)
+    log(f"{name}: model ready")
     stream = torch.cuda.Stream(device=dev)
     # every input is resident on the device before any timing
     dec_in = []
@@ -400,8 +410,9 @@ def measure_workload(name, dims, steps, warmup, args, peaks, dev, world, headlin
         return ([a.elapsed_time(b) for a, b in d_ev], p_ev[0].elapsed_time(p_ev[1]) if p_ev else None, launches)
 
     with torch.cuda.stream(stream):
-        for _ in range(warmup):
+        for i in range(warmup):
             one_step()
+            log(f"{name}: warm-up step {i + 1}/{warmup}")
         stream.synchronize()
         barrier(world)
         torch.cuda.synchronize()
@@ -420,6 +431,7 @@ def measure_workload(name, dims, steps, warmup, args, peaks, dev, world, headlin
         wall = time.perf_counter() - t0
         barrier(world)
         clk = clocks.stop()
+        log(f"{name}: {steps} timed steps in {wall:.1f} s")
 
         # The prefill with its activations rounded once (LADDER_FLAG_FAST_PREFILL).
         fast_ms = []
@@ -489,6 +501,7 @@ def measure_workload(name, dims, steps, warmup, args, peaks, dev, world, headlin
     out["steps"], out["warmup"] = steps, warmup
     out["ms_per_step"] = (sum(sum(m) for m in dec_ms) + sum(pre_ms)) / steps
 
+    log(f"{name}: fast prefill and gate/up probe done")
     # the same weights and kernels under the other residual schedules
     ns = min(steps, 5)
     if plan.get("schedules") and not args.no_schedules:
@@ -540,6 +553,7 @@ def measure_workload(name, dims, steps, warmup, args, peaks, dev, world, headlin
     model.close()
     del model, weights
     torch.cuda.empty_cache()
+    log(f"{name}: done")
     return out
 
 
@@ -563,7 +577,9 @@ def run_ours(args, dims):
                 nested[name] = {"error": f"{type(e).__name__}: {e}"}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        log("oracle baseline on the host cores")
         cpu = cpu_baseline(args.workload, dims)
+        log("oracle baseline done")
     d0 = head["decode"][0]
     plan = PLANS[args.workload]
     out = {
