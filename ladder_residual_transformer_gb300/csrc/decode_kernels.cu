@@ -36,6 +36,72 @@ __global__ void embed_kernel(const int* __restrict__ tok, const WT* __restrict__
   }
 }
 
+// Prefill embedding with the RMSNorm outputs of the modules that read x_0 (see
+// NormOut): thread t holds 8 consecutive columns, so a 32-column chunk is four
+// neighbouring lanes, whose partial sums of squares meet by two shuffles (in a
+// fixed order); d is a multiple of 256, so every warp's lanes are all in or all
+// out of each pass.
+template <typename WT>
+__global__ void embed_norm_kernel(const int* __restrict__ tok, const WT* __restrict__ E, int d, int vocab,
+                                  float* __restrict__ x, const NormOut no, int* err) {
+  using C = W16<WT>;
+  pdl_trigger();
+  pdl_wait();
+  const int m = blockIdx.x;
+  const int t = tok[m];
+  const bool ok = (unsigned)t < (unsigned)vocab;
+  if (!ok && threadIdx.x == 0) atomicOr(err, ERR_TOKEN);
+  const WT* row = E + (size_t)(ok ? t : 0) * d;
+  float* out = x + (size_t)m * d;
+  for (int i = threadIdx.x * 8; i < d; i += blockDim.x * 8) {
+    const uint4 v = ok ? *reinterpret_cast<const uint4*>(row + i) : make_uint4(0, 0, 0, 0);
+    const float f[8] = {C::lo(v.x), C::hi(v.x), C::lo(v.y), C::hi(v.y), C::lo(v.z), C::hi(v.z), C::lo(v.w), C::hi(v.w)};
+    *reinterpret_cast<float4*>(out + i) = make_float4(f[0], f[1], f[2], f[3]);
+    *reinterpret_cast<float4*>(out + i + 4) = make_float4(f[4], f[5], f[6], f[7]);
+    if (!no.ss) continue;
+    float sq = ((f[0] * f[0] + f[1] * f[1]) + (f[2] * f[2] + f[3] * f[3])) +
+               ((f[4] * f[4] + f[5] * f[5]) + (f[6] * f[6] + f[7] * f[7]));
+    sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+    sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+    if ((threadIdx.x & 3) == 0) no.ss[(size_t)(i >> 5) * no.ld_ss + m] = sq;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      if (!no.u[k]) continue;
+      const uint4 gr = *reinterpret_cast<const uint4*>(static_cast<const WT*>(no.g[k]) + i);
+      const float g[8] = {C::lo(gr.x), C::hi(gr.x), C::lo(gr.y), C::hi(gr.y),
+                          C::lo(gr.z), C::hi(gr.z), C::lo(gr.w), C::hi(gr.w)};
+      float u[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) u[j] = f[j] * g[j];
+      uint4 hi;
+      hi.x = C::pack(u[0], u[1]);
+      hi.y = C::pack(u[2], u[3]);
+      hi.z = C::pack(u[4], u[5]);
+      hi.w = C::pack(u[6], u[7]);
+      WT* dst = static_cast<WT*>(no.u[k]) + (size_t)m * d + i;
+      *reinterpret_cast<uint4*>(dst) = hi;
+      if (no.u_lo) {
+        uint4 lo;
+        lo.x = C::pack(u[0] - C::lo(hi.x), u[1] - C::hi(hi.x));
+        lo.y = C::pack(u[2] - C::lo(hi.y), u[3] - C::hi(hi.y));
+        lo.z = C::pack(u[4] - C::lo(hi.z), u[5] - C::hi(hi.z));
+        lo.w = C::pack(u[6] - C::lo(hi.w), u[7] - C::hi(hi.w));
+        *reinterpret_cast<uint4*>(dst + no.u_lo) = lo;
+      }
+    }
+  }
+}
+
+cudaError_t launch_embed_norm(const int* tok, int M, const void* E, int wdt, int d, int vocab, float* x,
+                              const NormOut& no, int* err, cudaStream_t s, bool pdl) {
+  if (M <= 0) return cudaSuccess;
+  if (wdt == WDT_F16)
+    return launch_k(embed_norm_kernel<f16>, dim3(M), dim3(128), 0, s, pdl, tok, static_cast<const f16*>(E), d, vocab,
+                    x, no, err);
+  return launch_k(embed_norm_kernel<bf16>, dim3(M), dim3(128), 0, s, pdl, tok, static_cast<const bf16*>(E), d, vocab,
+                  x, no, err);
+}
+
 cudaError_t launch_embed(const int* tok, int M, const void* E, int wdt, int d, int vocab, float* x, int* err,
                          cudaStream_t s, bool pdl) {
   if (M <= 0) return cudaSuccess;

@@ -85,6 +85,70 @@ __device__ __forceinline__ bool b_half(const GemmParams& p, int tile_n, int h, i
   return false;
 }
 
+// RMSNorm row factor of row `row` for a reading GEMM: rsqrt(sum of the producer's
+// per-chunk sums of squares / K + eps), summed in a fixed order (four interleaved
+// partial sums, then a tree).
+__device__ __forceinline__ float row_rms_factor(const GemmParams& p, int row) {
+  if (row >= p.M) return 1.f;
+  const float* s = p.ss_in + row;
+  const size_t ld = (size_t)p.ld_ss;
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  int c = 0;
+  for (; c + 4 <= p.nss; c += 4) {
+    a0 += s[(size_t)c * ld];
+    a1 += s[(size_t)(c + 1) * ld];
+    a2 += s[(size_t)(c + 2) * ld];
+    a3 += s[(size_t)(c + 3) * ld];
+  }
+  for (; c < p.nss; ++c) a0 += s[(size_t)c * ld];
+  return rsqrtf(((a0 + a1) + (a2 + a3)) * p.inv_k + p.eps);
+}
+
+// The RMSNorm outputs of one 32-column chunk of a new stream row x (see NormOut):
+// its sum of squares, and x ⊙ g for each reading module as a 16-bit hi (and lo)
+// plane row segment.
+template <typename WT>
+__device__ __forceinline__ void norm_outputs(const NormOut& no, const float (&x)[32], int row, int col, int width) {
+  using C = W16<WT>;
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    s0 = fmaf(x[4 * j], x[4 * j], s0);
+    s1 = fmaf(x[4 * j + 1], x[4 * j + 1], s1);
+    s2 = fmaf(x[4 * j + 2], x[4 * j + 2], s2);
+    s3 = fmaf(x[4 * j + 3], x[4 * j + 3], s3);
+  }
+  no.ss[(size_t)(col >> 5) * no.ld_ss + row] = (s0 + s1) + (s2 + s3);
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    if (!no.u[k]) continue;
+    const uint4* gp = reinterpret_cast<const uint4*>(static_cast<const WT*>(no.g[k]) + col);
+    WT* dst = static_cast<WT*>(no.u[k]) + (size_t)row * width + col;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 gr = __ldg(gp + q);
+      const float u0 = x[8 * q] * C::lo(gr.x), u1 = x[8 * q + 1] * C::hi(gr.x);
+      const float u2 = x[8 * q + 2] * C::lo(gr.y), u3 = x[8 * q + 3] * C::hi(gr.y);
+      const float u4 = x[8 * q + 4] * C::lo(gr.z), u5 = x[8 * q + 5] * C::hi(gr.z);
+      const float u6 = x[8 * q + 6] * C::lo(gr.w), u7 = x[8 * q + 7] * C::hi(gr.w);
+      uint4 hi;
+      hi.x = C::pack(u0, u1);
+      hi.y = C::pack(u2, u3);
+      hi.z = C::pack(u4, u5);
+      hi.w = C::pack(u6, u7);
+      *reinterpret_cast<uint4*>(dst + 8 * q) = hi;
+      if (no.u_lo) {
+        uint4 lo;
+        lo.x = C::pack(u0 - C::lo(hi.x), u1 - C::hi(hi.x));
+        lo.y = C::pack(u2 - C::lo(hi.y), u3 - C::hi(hi.y));
+        lo.z = C::pack(u4 - C::lo(hi.z), u5 - C::hi(hi.z));
+        lo.w = C::pack(u6 - C::lo(hi.w), u7 - C::hi(hi.w));
+        *reinterpret_cast<uint4*>(dst + no.u_lo + 8 * q) = lo;
+      }
+    }
+  }
+}
+
 struct TcMaps {
   CUtensorMap a;
   CUtensorMap b[3];
@@ -328,6 +392,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
       int mt_, tile_n;
       gemm_tile<PAIR>(i, m_tiles, crank, mt_, tile_n);
       const int mrow0 = mt_ * TC_BM + warp * 32;
+      // RMSNorm factor of this lane's row (reading GEMMs), before the accumulator is awaited
+      const float rnorm = (MODE != GEMM_RESID && p.ss_in) ? row_rms_factor(p, mrow0 + lane) : 1.f;
       // Row metadata of this lane's row (QKV), fetched before the accumulator is
       // awaited: position and the element offset of its slot in the paged cache
       // (page base + slot * hd; the kv / head term is added per column).
@@ -374,6 +440,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
           float gv[32], uv[32];
           tmem_ld32(trow + c * 32, gv);
           tmem_ld32(trow + 128 + c * 32, uv);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            gv[j] *= rnorm;
+            uv[j] *= rnorm;
+          }
           uint32_t pk[16], pl[16];
           bool bad = false;
 #pragma unroll
@@ -426,6 +497,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
             xv.w += v[4 * q + 3];
             bad |= mrow0 + lane < p.M && !(isfinite(xv.x) && isfinite(xv.y) && isfinite(xv.z) && isfinite(xv.w));
             rowp[q ^ (lane & 7)] = xv;
+            v[4 * q] = xv.x;  // v now holds this lane's 32 new stream values
+            v[4 * q + 1] = xv.y;
+            v[4 * q + 2] = xv.z;
+            v[4 * q + 3] = xv.w;
           }
           if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(err, ERR_NONFINITE);
           fence_proxy_async_smem();
@@ -434,6 +509,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
             tma_store_2d(&maps.e_out, buf, tile_n * BN + c * 32, mrow0);
             bulk_commit();
           }
+          // the RMSNorm inputs of the modules that read this stream state
+          if (p.nout.ss && mrow0 + lane < p.M) norm_outputs<WT>(p.nout, v, mrow0 + lane, tile_n * BN + c * 32, p.N);
           if (c + 2 < NCH) {
             if (lane == 0) {
               bulk_wait_read_all();  // the store above has read the buffer
@@ -450,6 +527,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
           if (!b_half<GEMM_QKV, BN>(p, tile_n, c >> 2, map, row)) break;
           float v[32];
           tmem_ld32(trow + c * 32, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] *= rnorm;
           const int col = row + (c & 3) * 32 + cp;  // column inside its matrix (even: a RoPE pair)
           const int head = col / hd, dim = col % hd;
           // Rotation of each of this lane's 16 rows, all table loads in flight at

@@ -193,6 +193,23 @@ struct AttnDecodeParams {
 
 enum GemmMode { GEMM_QKV = 0, GEMM_GATEUP = 1, GEMM_RESID = 2 };
 
+// The RMSNorm of the prefill projections, split between the kernel that writes
+// a stream state x_j and the GEMMs of the modules that read it.  The producer
+// writes, per 32-column chunk c and row m, the partial sum of squares
+// ss[c * ld_ss + m], and for each reading module i the 16-bit operand
+// x ⊙ g_i (the hi plane at u[i]; with u_lo > 0 the rounding remainder in the
+// lo plane at u[i] + u_lo), rows of the state's width.  The reading GEMM scales
+// its accumulator row m by rsqrt(sum_c ss[c][m] / width + eps): the row factor
+// commutes with the contraction over the row, so the product equals the one
+// with the normalised row.
+struct NormOut {
+  float* ss;         // [width / 32][ld_ss] fp32, or nullptr (no reader)
+  int ld_ss;
+  void* u[2];        // operand bases of up to two readers (weight dtype), nullptr when absent
+  const void* g[2];  // their RMSNorm gains [width] (weight dtype)
+  size_t u_lo;       // element offset of the lo plane (0: hi plane only)
+};
+
 struct GemmParams {
   int M, N, K;
   void* out_h;          // QKV: q [M][ldo]; GATEUP: act [M][ldo] (weight dtype)
@@ -207,6 +224,13 @@ struct GemmParams {
   const int* row_b;     // sequence of packed row m
   const int* row_pos;   // position of packed row m
   KvLayer kv;
+  // QKV / GATEUP: the RMSNorm row factors from the producer's sums of squares
+  // (nss chunks of 32 columns, ld_ss rows apart; inv_k = 1 / K); nullptr: none.
+  const float* ss_in;
+  int nss, ld_ss;
+  float inv_k, eps;
+  // RESID: the operands and sums of squares for the modules that read x_out.
+  NormOut nout;
 };
 
 struct AttnPrefillParams {
@@ -225,6 +249,9 @@ struct AttnPrefillParams {
 // ---------------------------------------------------------------------------
 cudaError_t launch_embed(const int* tok, int M, const void* E, int wdt, int d, int vocab, float* x, int* err,
                          cudaStream_t s, bool pdl = false);
+// Prefill embedding: x_0 rows plus the RMSNorm outputs of the modules that read x_0.
+cudaError_t launch_embed_norm(const int* tok, int M, const void* E, int wdt, int d, int vocab, float* x,
+                              const NormOut& no, int* err, cudaStream_t s, bool pdl);
 cudaError_t launch_gemv(const GemvParams& p, int mode, int wdt, int num_sms, cudaStream_t s, bool pdl = false);
 cudaError_t gemv_configure();
 int gemv_chunk(int B, int K);
@@ -255,10 +282,6 @@ cudaError_t launch_rope_tables(float* cos_t, float* sin_t, int max_seq, int hd, 
 
 // Prefill launches take `pdl` (programmatic dependent launch); every kernel
 // launched with it waits for the previous kernel before touching its data.
-// lo_off > 0: the rounding remainder of each value (value minus its 16-bit
-// rounding, itself rounded to 16 bits) goes to out + lo_off (the lo plane).
-cudaError_t launch_rmsnorm_rows(const float* x, int M, int d, const void* g, float eps, void* out, size_t lo_off,
-                                int wdt, cudaStream_t s, bool pdl = false);
 // Tensor-core GEMM (tcgen05 + TMA).  Maps are CUtensorMap objects made by make_tma_map.
 // 2-D map of a row-major [rows, cols] 16-bit matrix, box 64 columns x 128 rows.
 bool make_tma_map(void* map_out, const void* base, uint64_t rows, uint64_t cols, int wdt);

@@ -55,7 +55,7 @@ constexpr int kArgmaxBlocks = 64;   // partial argmax blocks per sequence
 enum SplitKKind { SK_QKV = 0, SK_OUT = 1, SK_GATEUP = 2, SK_DOWN = 3, SK_LMHEAD = 4, SK_KINDS = 5 };
 
 struct Plan {
-  size_t x[3], xn, q, ao, act, part_o, part_ml, am_v, am_i, rope_cos, rope_sin, meta, xlast, err, shard;
+  size_t x[3], xn[2], ssq[3], q, ao, act, part_o, part_ml, am_v, am_i, rope_cos, rope_sin, meta, xlast, err, shard;
   size_t sk[SK_KINDS], sk_bytes[SK_KINDS];
   size_t total;
   int m_max, m_pad, nsplit_max;
@@ -79,7 +79,11 @@ Plan make_plan(const ladder_config& c) {
   for (int i = 0; i < 3; ++i) p.x[i] = take(M * d * 4);
   // Prefill GEMM A operands: a hi plane [Mp][K] and a lo plane [Mp][K] (the
   // 16-bit rounding remainders) right after it; decode reuses ao / act as fp32 rows.
-  p.xn = take(2 * Mp * d * 2);
+  // The normalised-row operands x ⊙ g come in two slots (module c uses slot c % 2,
+  // see ladder_prefill), and the per-chunk sums of squares of the stream states in
+  // three (state j uses slot j % 3), [d / 32][Mp] fp32.
+  for (int i = 0; i < 2; ++i) p.xn[i] = take(2 * Mp * d * 2);
+  for (int i = 0; i < 3; ++i) p.ssq[i] = take(d / 32 * Mp * 4);
   p.q = take(std::max(Mp * qd * 2, Bm * qd * 4));
   p.ao = take(std::max(2 * Mp * qd * 2, Bm * qd * 4));
   p.act = take(std::max(2 * Mp * f * 2, Bm * f * 4));
@@ -185,7 +189,7 @@ struct ladder_model {
   int wdt;  // weight dtype
   std::vector<LayerW> layers;
   std::vector<LayerMaps> maps;
-  TmaOperand map_xn, map_ao, map_act;  // activation operands, m_pad rows
+  TmaOperand map_xn[2], map_ao, map_act;  // activation operands, m_pad rows
   CUtensorMap map_q;  // rotated queries [m_pad][n_q * hd], the prefill attention operand
   CUtensorMap map_x[3];   // stream buffers [m_max][d] fp32, epilogue blocks (prefill residual GEMMs)
   CUtensorMap map_act_st; // SwiGLU rows [m_pad][ffn], epilogue blocks (prefill gate/up GEMM)
@@ -392,7 +396,8 @@ int ladder_create(const ladder_config* cfg, const ladder_weights* w, void* works
     const uint64_t d = c.d_model, qd = (uint64_t)c.n_q_heads * c.head_dim, kvd = (uint64_t)c.n_kv_heads * c.head_dim;
     const uint64_t f = c.ffn_dim, Mp = plan.m_pad;
     const int wdt = c.weight_dtype;
-    bool ok = make_tma_operand(&m->map_xn, m->ws + plan.xn, Mp, d, wdt, true) &&
+    bool ok = make_tma_operand(&m->map_xn[0], m->ws + plan.xn[0], Mp, d, wdt, true) &&
+              make_tma_operand(&m->map_xn[1], m->ws + plan.xn[1], Mp, d, wdt, true) &&
               make_tma_operand(&m->map_ao, m->ws + plan.ao, Mp, qd, wdt, true) &&
               make_tma_operand(&m->map_act, m->ws + plan.act, Mp, f, wdt, true) &&
               make_tma_map(&m->map_q, m->ws + plan.q, Mp, qd, wdt) &&
@@ -1017,7 +1022,6 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
 
   const int d = c.d_model, qd = c.n_q_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim, f = c.ffn_dim;
   const int wdt = m->wdt;
-  void* xn = m->ws + P.xn;    // normalised rows, weight dtype
   void* qb = m->ws + P.q;     // rotated queries, weight dtype
   void* aob = m->ws + P.ao;   // attention output, weight dtype
   void* actb = m->ws + P.act; // SwiGLU output, weight dtype
@@ -1027,24 +1031,57 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
   // GEMM A operands as hi/lo pairs (the default) or rounded once (LADDER_FLAG_FAST_PREFILL).
   const bool wide = !(m->flags & LADDER_FLAG_FAST_PREFILL);
   const size_t Mp = P.m_pad;
-  const size_t lo_xn = wide ? Mp * d : 0, lo_ao = wide ? Mp * qd : 0;
+  const size_t lo_ao = wide ? Mp * qd : 0;
   const int lo_act = wide ? (int)Mp : 0;
+  const int n_mod = 2 * c.n_layers;
 
-  LAUNCH(launch_embed(tokens, M, m->embed, wdt, d, c.vocab, m->X(0), m->err(), s, pdl), 1);
+  // RMSNorm split between the writer of each stream state x_j (the embedding, or
+  // a residual GEMM's epilogue) and the GEMMs of the modules that read it: the
+  // writer leaves x_j ⊙ g_c for each reading module c (slot c % 2) and the
+  // per-chunk sums of squares of x_j (slot j % 3); reading GEMM c scales its rows
+  // by rsqrt(mean(x_j^2) + eps).  Module c reads x_{input_index(c)}, one or two
+  // modules back, so at most two operands are pending at any time, and state j's
+  // sums are read by module j + 2 at the latest, before state j + 3 is written.
+  auto gain_of = [&](int k) -> const void* {
+    const LayerW& L = m->layers[(k - 1) / 2];
+    return (k & 1) ? L.attn_norm : L.mlp_norm;
+  };
+  auto norm_out = [&](int j) {
+    NormOut o{};
+    o.ld_ss = (int)Mp;
+    o.u_lo = wide ? Mp * d : 0;
+    int n = 0;
+    for (int k = j + 1; k <= j + 2 && k <= n_mod; ++k)
+      if (m->input_index(k) == j) {
+        o.u[n] = m->ws + P.xn[k % 2];
+        o.g[n] = gain_of(k);
+        ++n;
+      }
+    if (n) o.ss = m->at<float>(P.ssq[j % 3]);
+    return o;
+  };
+  auto reads_norm = [&](GemmParams& g, int k) {
+    g.ss_in = m->at<float>(P.ssq[m->input_index(k) % 3]);
+    g.nss = d / 32;
+    g.ld_ss = (int)Mp;
+    g.inv_k = 1.0f / (float)d;
+    g.eps = c.norm_eps;
+  };
+
+  LAUNCH(launch_embed_norm(tokens, M, m->embed, wdt, d, c.vocab, m->X(0), norm_out(0), m->err(), s, pdl), 1);
   for (int l = 0; l < c.n_layers; ++l) {
-    const LayerW& L = m->layers[l];
     const LayerMaps& T = m->maps[l];
     const KvLayer kvl = kv->layer(l);
     {
       const int k = 2 * l + 1;
-      LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.attn_norm, c.norm_eps, xn, lo_xn, wdt, s, pdl), 1);
       GemmParams g{};
       g.M = M; g.N = qd + 2 * kvd; g.K = d;
       g.out_h = qb; g.ldo = qd; g.nq_hd = qd; g.nkv_hd = kvd;
       g.rope_cos = m->at<float>(P.rope_cos); g.rope_sin = m->at<float>(P.rope_sin);
       g.row_b = d_row_b; g.row_pos = d_row_pos; g.kv = kvl;
-      LAUNCH(launch_gemm_tc(&m->map_xn, &T.wq, &T.wk, &T.wv, nullptr, nullptr, g, GEMM_QKV, wdt, m->num_sms, m->err(), s,
-                            pdl, wide), 1);
+      reads_norm(g, k);
+      LAUNCH(launch_gemm_tc(&m->map_xn[k % 2], &T.wq, &T.wk, &T.wv, nullptr, nullptr, g, GEMM_QKV, wdt, m->num_sms,
+                            m->err(), s, pdl, wide), 1);
 
       AttnPrefillParams a{};
       a.q = qb; a.kv = kvl; a.seq_start = d_start; a.seq_len = d_lens;
@@ -1053,18 +1090,20 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
 
       GemmParams o{};
       o.M = M; o.N = d; o.K = qd; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);
+      o.nout = norm_out(k);
       LAUNCH(launch_gemm_tc(&m->map_ao, &T.wo, nullptr, nullptr, &m->map_x[(k - 1) % 3], &m->map_x[k % 3], o,
                             GEMM_RESID, wdt, m->num_sms, m->err(), s, pdl, wide), 1);
     }
     {
       const int k = 2 * l + 2;
-      LAUNCH(launch_rmsnorm_rows(m->X(m->input_index(k)), M, d, L.mlp_norm, c.norm_eps, xn, lo_xn, wdt, s, pdl), 1);
       GemmParams g{};
       g.M = M; g.N = f; g.K = d; g.out_h = actb; g.ldo = f; g.lo_row = lo_act;
-      LAUNCH(launch_gemm_tc(&m->map_xn, &T.gate, &T.up, nullptr, nullptr, &m->map_act_st, g, GEMM_GATEUP, wdt,
+      reads_norm(g, k);
+      LAUNCH(launch_gemm_tc(&m->map_xn[k % 2], &T.gate, &T.up, nullptr, nullptr, &m->map_act_st, g, GEMM_GATEUP, wdt,
                             m->num_sms, m->err(), s, pdl, wide), 1);
       GemmParams o{};
       o.M = M; o.N = d; o.K = f; o.out_f = m->X(k); o.ldo = d; o.x_res = m->X(k - 1);
+      o.nout = norm_out(k);
       LAUNCH(launch_gemm_tc(&m->map_act, &T.down, nullptr, nullptr, &m->map_x[(k - 1) % 3], &m->map_x[k % 3], o,
                             GEMM_RESID, wdt, m->num_sms, m->err(), s, pdl, wide), 1);
     }
