@@ -37,10 +37,10 @@ __global__ void embed_kernel(const int* __restrict__ tok, const WT* __restrict__
 }
 
 // Prefill embedding with the RMSNorm outputs of the modules that read x_0 (see
-// NormOut): thread t holds 8 consecutive columns, so a 32-column chunk is four
-// neighbouring lanes, whose partial sums of squares meet by two shuffles (in a
-// fixed order); d is a multiple of 256, so every warp's lanes are all in or all
-// out of each pass.
+// NormOut): thread t holds 8 consecutive columns, so a 128-column entry of the
+// sums of squares is sixteen neighbouring lanes, whose partial sums meet by four
+// shuffles (in a fixed order); d is a multiple of 256, so every warp's lanes are
+// all in or all out of each pass.
 template <typename WT>
 __global__ void embed_norm_kernel(const int* __restrict__ tok, const WT* __restrict__ E, int d, int vocab,
                                   float* __restrict__ x, const NormOut no, int* err) {
@@ -63,7 +63,9 @@ __global__ void embed_norm_kernel(const int* __restrict__ tok, const WT* __restr
                ((f[4] * f[4] + f[5] * f[5]) + (f[6] * f[6] + f[7] * f[7]));
     sq += __shfl_xor_sync(0xffffffffu, sq, 1);
     sq += __shfl_xor_sync(0xffffffffu, sq, 2);
-    if ((threadIdx.x & 3) == 0) no.ss[(size_t)(i >> 5) * no.ld_ss + m] = sq;
+    sq += __shfl_xor_sync(0xffffffffu, sq, 4);
+    sq += __shfl_xor_sync(0xffffffffu, sq, 8);
+    if ((threadIdx.x & 15) == 0) no.ss[(size_t)(i >> 7) * no.ld_ss + m] = sq;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       if (!no.u[k]) continue;

@@ -86,29 +86,32 @@ __device__ __forceinline__ bool b_half(const GemmParams& p, int tile_n, int h, i
 }
 
 // RMSNorm row factor of row `row` for a reading GEMM: rsqrt(sum of the producer's
-// per-chunk sums of squares / K + eps), summed in a fixed order (four interleaved
-// partial sums, then a tree).
+// per-128-column sums of squares / K + eps), summed in a fixed order (eight
+// interleaved partial sums whose loads are all in flight at once, then a tree).
 __device__ __forceinline__ float row_rms_factor(const GemmParams& p, int row) {
   if (row >= p.M) return 1.f;
   const float* s = p.ss_in + row;
   const size_t ld = (size_t)p.ld_ss;
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   int c = 0;
-  for (; c + 4 <= p.nss; c += 4) {
-    a0 += s[(size_t)c * ld];
-    a1 += s[(size_t)(c + 1) * ld];
-    a2 += s[(size_t)(c + 2) * ld];
-    a3 += s[(size_t)(c + 3) * ld];
+  for (; c + 8 <= p.nss; c += 8) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = __ldg(s + (size_t)(c + j) * ld);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a[j] += v[j];
   }
-  for (; c < p.nss; ++c) a0 += s[(size_t)c * ld];
-  return rsqrtf(((a0 + a1) + (a2 + a3)) * p.inv_k + p.eps);
+  for (; c < p.nss; ++c) a[c & 7] += __ldg(s + (size_t)c * ld);
+  const float t = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+  return rsqrtf(t * p.inv_k + p.eps);
 }
 
 // The RMSNorm outputs of one 32-column chunk of a new stream row x (see NormOut):
-// its sum of squares, and x ⊙ g for each reading module as a 16-bit hi (and lo)
-// plane row segment.
+// x ⊙ g for each reading module as a 16-bit hi (and lo) plane row segment.
+// Returns the chunk's sum of squares (the caller adds four chunks per 128-column
+// entry of no.ss).
 template <typename WT>
-__device__ __forceinline__ void norm_outputs(const NormOut& no, const float (&x)[32], int row, int col, int width) {
+__device__ __forceinline__ float norm_outputs(const NormOut& no, const float (&x)[32], int row, int col, int width) {
   using C = W16<WT>;
   float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
@@ -118,7 +121,6 @@ __device__ __forceinline__ void norm_outputs(const NormOut& no, const float (&x)
     s2 = fmaf(x[4 * j + 2], x[4 * j + 2], s2);
     s3 = fmaf(x[4 * j + 3], x[4 * j + 3], s3);
   }
-  no.ss[(size_t)(col >> 5) * no.ld_ss + row] = (s0 + s1) + (s2 + s3);
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     if (!no.u[k]) continue;
@@ -147,6 +149,7 @@ __device__ __forceinline__ void norm_outputs(const NormOut& no, const float (&x)
       }
     }
   }
+  return (s0 + s1) + (s2 + s3);
 }
 
 struct TcMaps {
@@ -473,6 +476,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
           }
         }
       } else if (MODE == GEMM_RESID) {
+        float sq128 = 0.f;  // sum of squares of this row's current 128 columns
         for (int c = 0; c < NCH; ++c) {
           const int bi = c & 1;
           float* buf = reinterpret_cast<float*>(ewarp + bi * 4096);
@@ -510,7 +514,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
             bulk_commit();
           }
           // the RMSNorm inputs of the modules that read this stream state
-          if (p.nout.ss && mrow0 + lane < p.M) norm_outputs<WT>(p.nout, v, mrow0 + lane, tile_n * BN + c * 32, p.N);
+          if (p.nout.ss && mrow0 + lane < p.M) {
+            sq128 += norm_outputs<WT>(p.nout, v, mrow0 + lane, tile_n * BN + c * 32, p.N);
+            if ((c & 3) == 3) {
+              p.nout.ss[(size_t)((tile_n * BN + c * 32) >> 7) * p.nout.ld_ss + mrow0 + lane] = sq128;
+              sq128 = 0.f;
+            }
+          }
           if (c + 2 < NCH) {
             if (lane == 0) {
               bulk_wait_read_all();  // the store above has read the buffer

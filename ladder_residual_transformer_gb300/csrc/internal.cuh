@@ -195,7 +195,7 @@ enum GemmMode { GEMM_QKV = 0, GEMM_GATEUP = 1, GEMM_RESID = 2 };
 
 // The RMSNorm of the prefill projections, split between the kernel that writes
 // a stream state x_j and the GEMMs of the modules that read it.  The producer
-// writes, per 32-column chunk c and row m, the partial sum of squares
+// writes, per 128-column block c and row m, the partial sum of squares
 // ss[c * ld_ss + m], and for each reading module i the 16-bit operand
 // x ⊙ g_i (the hi plane at u[i]; with u_lo > 0 the rounding remainder in the
 // lo plane at u[i] + u_lo), rows of the state's width.  The reading GEMM scales
@@ -203,7 +203,7 @@ enum GemmMode { GEMM_QKV = 0, GEMM_GATEUP = 1, GEMM_RESID = 2 };
 // commutes with the contraction over the row, so the product equals the one
 // with the normalised row.
 struct NormOut {
-  float* ss;         // [width / 32][ld_ss] fp32, or nullptr (no reader)
+  float* ss;         // [width / 128][ld_ss] fp32, or nullptr (no reader)
   int ld_ss;
   void* u[2];        // operand bases of up to two readers (weight dtype), nullptr when absent
   const void* g[2];  // their RMSNorm gains [width] (weight dtype)
@@ -225,7 +225,7 @@ struct GemmParams {
   const int* row_pos;   // position of packed row m
   KvLayer kv;
   // QKV / GATEUP: the RMSNorm row factors from the producer's sums of squares
-  // (nss chunks of 32 columns, ld_ss rows apart; inv_k = 1 / K); nullptr: none.
+  // (nss blocks of 128 columns, ld_ss rows apart; inv_k = 1 / K); nullptr: none.
   const float* ss_in;
   int nss, ld_ss;
   float inv_k, eps;

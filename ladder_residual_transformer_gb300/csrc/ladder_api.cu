@@ -81,9 +81,9 @@ Plan make_plan(const ladder_config& c) {
   // 16-bit rounding remainders) right after it; decode reuses ao / act as fp32 rows.
   // The normalised-row operands x ⊙ g come in two slots (module c uses slot c % 2,
   // see ladder_prefill), and the per-chunk sums of squares of the stream states in
-  // three (state j uses slot j % 3), [d / 32][Mp] fp32.
+  // three (state j uses slot j % 3), [d / 128][Mp] fp32.
   for (int i = 0; i < 2; ++i) p.xn[i] = take(2 * Mp * d * 2);
-  for (int i = 0; i < 3; ++i) p.ssq[i] = take(d / 32 * Mp * 4);
+  for (int i = 0; i < 3; ++i) p.ssq[i] = take(d / 128 * Mp * 4);
   p.q = take(std::max(Mp * qd * 2, Bm * qd * 4));
   p.ao = take(std::max(2 * Mp * qd * 2, Bm * qd * 4));
   p.act = take(std::max(2 * Mp * f * 2, Bm * f * 4));
@@ -1062,7 +1062,7 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
   };
   auto reads_norm = [&](GemmParams& g, int k) {
     g.ss_in = m->at<float>(P.ssq[m->input_index(k) % 3]);
-    g.nss = d / 32;
+    g.nss = d / 128;
     g.ld_ss = (int)Mp;
     g.inv_k = 1.0f / (float)d;
     g.eps = c.norm_eps;
