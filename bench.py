@@ -62,7 +62,12 @@ NESTED = ("1.2b", "8b-hybrid", "8b-ladder")
 # DRAM traffic of the dominant kernel (the decode gate/up GEMV) per launch at
 # each workload's shape, from one ncu capture, valid only while the kernel's
 # source file is unchanged (its sha256).
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    "70b": {"source": "ladder_residual_transformer_gb300/csrc/gemv.cu",
+            "sha256": "eca339879ed533e5f8ec3517da5ba19a2fb832314b1bcfb90059fe2ab776134c",
+            # mean of three captured launches: 939.62 MB read + 1.09 MB written
+            "bytes_per_launch": 940716971},
+}
 
 
 # ---------------------------------------------------------------------------
