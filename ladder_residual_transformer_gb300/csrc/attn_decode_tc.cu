@@ -74,64 +74,6 @@ __device__ __forceinline__ uint32_t ad_swz(int key, int dim) {
   return (uint32_t)((dim >> 6) * AD_BLK + key * 128 + ((((dim & 63) >> 3) ^ (key & 7)) << 4) + ((dim & 7) << 1));
 }
 
-// The last split of (sequence b, kv head kvh) to finish merges the partials of
-// the group's G query heads into p.out, with the combine step's arithmetic and
-// order: M = max over splits of m_s, L = sum w_s l_s, out = sum w_s o_s / L with
-// w_s = exp(m_s - M), splits in ascending order.  Every split of the group
-// takes part in the count (a failed one too), so the counter always returns to
-// zero.
-template <int HD>
-__device__ void ad_merge_if_last(const AttnDecodeParams& p, int b, int kvh, int G, int ctx) {
-  __shared__ int s_last;
-  const int tid = threadIdx.x;
-  __threadfence();  // this split's partials are visible before it is counted
-  __syncthreads();
-  int* cnt = p.count + (size_t)b * p.kv.n_kv + kvh;
-  const int ns = min((ctx + AD_KEYS - 1) / AD_KEYS, p.nsplit);
-  if (tid == 0) s_last = atomicAdd(cnt, 1) == ns - 1;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (tid == 0) *cnt = 0;  // ready for the next launch
-  constexpr int CB = 16;
-  for (int i = tid; i < G * HD; i += AD_THREADS) {
-    const int g = i / HD, d = i % HD;
-    const int h = kvh * G + g;
-    const size_t base = ((size_t)b * p.n_q + h) * p.nsplit;
-    float M = -INFINITY, L = 0.f, acc = 0.f;
-    if (ns <= CB) {  // every partial requested at once
-      float m[CB], l[CB], o[CB];
-#pragma unroll
-      for (int s = 0; s < CB; ++s) {
-        if (s < ns) {
-          m[s] = __ldcg(p.part_ml + (base + s) * 2);
-          l[s] = __ldcg(p.part_ml + (base + s) * 2 + 1);
-          o[s] = __ldcg(p.part_o + (base + s) * HD + d);
-        }
-      }
-#pragma unroll
-      for (int s = 0; s < CB; ++s)
-        if (s < ns) M = fmaxf(M, m[s]);
-#pragma unroll
-      for (int s = 0; s < CB; ++s) {
-        if (s < ns) {
-          const float w = __expf(m[s] - M);
-          L += w * l[s];
-          acc += w * o[s];
-        }
-      }
-    } else {
-      for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(p.part_ml + (base + s) * 2));
-      for (int s = 0; s < ns; ++s) {
-        const float w = __expf(__ldcg(p.part_ml + (base + s) * 2) - M);
-        L += w * __ldcg(p.part_ml + (base + s) * 2 + 1);
-        acc += w * __ldcg(p.part_o + (base + s) * HD + d);
-      }
-    }
-    p.out[(size_t)b * p.n_q * HD + (size_t)h * HD + d] = acc / L;
-  }
-}
-
 template <typename T, int HD>
 __global__ void __launch_bounds__(AD_THREADS) attn_decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map,
                                                                    const AttnDecodeParams p, int* err) {
@@ -195,7 +137,6 @@ __global__ void __launch_bounds__(AD_THREADS) attn_decode_tc_kernel(const __grid
   __syncthreads();
   if (!__syncthreads_and(ok)) {
     if (tid == 0) atomicOr(err, 2);
-    if (p.count != nullptr) ad_merge_if_last<HD>(p, b, kvh, G, ctx);
     return;
   }
   const uint32_t kbase = smem_u32(smem + L::K_OFF), vbase = smem_u32(smem + L::V_OFF);
@@ -278,7 +219,6 @@ __global__ void __launch_bounds__(AD_THREADS) attn_decode_tc_kernel(const __grid
       p.part_ml[idx * 2 + 1] = red_l[g] + red_l[8 + g] + red_l[16 + g] + red_l[24 + g];
     }
   }
-  if (p.count != nullptr) ad_merge_if_last<HD>(p, b, kvh, G, ctx);
 }
 
 size_t attn_decode_tc_smem(int hd) { return hd == 64 ? AdCfg<64>::SMEM : AdCfg<128>::SMEM; }
@@ -310,7 +250,7 @@ cudaError_t launch_attn_decode_tc(const void* kv_map, const AttnDecodeParams& p,
   else
     e = hd == 64 ? launch_k(attn_decode_tc_kernel<bf16, 64>, grid, dim3(AD_THREADS), (size_t)AdCfg<64>::SMEM, s, pdl, map, p, err)
                  : launch_k(attn_decode_tc_kernel<bf16, 128>, grid, dim3(AD_THREADS), (size_t)AdCfg<128>::SMEM, s, pdl, map, p, err);
-  if (e != cudaSuccess || p.count != nullptr) return e;
+  if (e != cudaSuccess) return e;
   return launch_attn_combine(p, B, hd, s, pdl);
 }
 

@@ -189,10 +189,6 @@ struct AttnDecodeParams {
   float* part_o;        // [B][n_q][nsplit][hd]
   float* part_ml;       // [B][n_q][nsplit][2]
   float* out;           // [B][n_q * hd]
-  // [B][n_kv] split counters, zero between launches: the last split of each
-  // (sequence, kv head) to finish merges the partials into `out` (tensor-core
-  // kernel only); nullptr: a separate combine launch merges them.
-  int* count;
 };
 
 enum GemmMode { GEMM_QKV = 0, GEMM_GATEUP = 1, GEMM_RESID = 2 };

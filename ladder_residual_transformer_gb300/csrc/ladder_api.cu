@@ -55,7 +55,7 @@ constexpr int kArgmaxBlocks = 64;   // partial argmax blocks per sequence
 enum SplitKKind { SK_QKV = 0, SK_OUT = 1, SK_GATEUP = 2, SK_DOWN = 3, SK_LMHEAD = 4, SK_KINDS = 5 };
 
 struct Plan {
-  size_t x[3], xn[2], ssq[3], q, ao, act, part_o, part_ml, att_count, am_v, am_i, rope_cos, rope_sin, meta, xlast, err, shard;
+  size_t x[3], xn[2], ssq[3], q, ao, act, part_o, part_ml, am_v, am_i, rope_cos, rope_sin, meta, xlast, err, shard;
   size_t sk[SK_KINDS], sk_bytes[SK_KINDS];
   size_t total;
   int m_max, m_pad, nsplit_max;
@@ -89,7 +89,6 @@ Plan make_plan(const ladder_config& c) {
   p.act = take(std::max(2 * Mp * f * 2, Bm * f * 4));
   p.part_o = take(Bm * c.n_q_heads * (size_t)p.nsplit_max * c.head_dim * 4);
   p.part_ml = take(Bm * c.n_q_heads * (size_t)p.nsplit_max * 2 * 4);
-  p.att_count = take(Bm * c.n_kv_heads * 4);  // decode-attention split counters (zero between launches)
   p.am_v = take(Bm * kArgmaxBlocks * 4);
   p.am_i = take(Bm * kArgmaxBlocks * 4);
   p.rope_cos = take((size_t)c.max_seq * (c.head_dim / 2) * 4);
@@ -436,7 +435,6 @@ int ladder_create(const ladder_config* cfg, const ladder_weights* w, void* works
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_fork, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ev_part, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaMemsetAsync(m->err(), 0, 256, stream);
-  if (e == cudaSuccess) e = cudaMemsetAsync(m->ws + plan.att_count, 0, (size_t)cfg->max_batch * cfg->n_kv_heads * 4, stream);
   for (int i = 0; i < SK_KINDS && e == cudaSuccess; ++i)
     if (plan.sk_bytes[i]) e = cudaMemsetAsync(m->ws + plan.sk[i], 0, plan.sk_bytes[i], stream);
   if (e == cudaSuccess)
@@ -754,9 +752,8 @@ int enqueue_decode_shard(ladder_model* m, ladder_kv* kv, const int32_t* tokens, 
       a.q = q; a.kv = kvl; a.seq_lens = kv->seq_lens; a.n_q = c.n_q_heads; a.split_len = kSplitLen;
       a.nsplit = nsplit; a.scale = 1.0f / sqrtf((float)c.head_dim);
       a.part_o = m->at<float>(P.part_o); a.part_ml = m->at<float>(P.part_ml); a.out = ao;
-      a.count = m->at<int>(P.att_count);
       auto pa = m->probe_start(LADDER_PROBE_ATTN, s);
-      LAUNCH(launch_attn_decode_tc(&kv->maps[l], a, B, c.n_kv_heads, c.head_dim, m->wdt, m->err(), s, pdl), 1);
+      LAUNCH(launch_attn_decode_tc(&kv->maps[l], a, B, c.n_kv_heads, c.head_dim, m->wdt, m->err(), s, pdl), 2);
       m->probe_stop(pa, s);
       o.x = ao; o.ldx = qd; o.K = qd / ksh; o.kfull = qd; o.ldw = qd; o.w0 = L.wo;
     } else {  // MLP module
@@ -864,9 +861,8 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       a.q = q; a.kv = kvl; a.seq_lens = kv->seq_lens; a.n_q = c.n_q_heads; a.split_len = kSplitLen;
       a.nsplit = nsplit; a.scale = 1.0f / sqrtf((float)c.head_dim);
       a.part_o = m->at<float>(P.part_o); a.part_ml = m->at<float>(P.part_ml); a.out = ao;
-      a.count = m->at<int>(P.att_count);
       pe = m->probe_start(LADDER_PROBE_ATTN, s);
-      LAUNCH(launch_attn_decode_tc(&kv->maps[l], a, B, c.n_kv_heads, c.head_dim, m->wdt, m->err(), s, pdl), 1);
+      LAUNCH(launch_attn_decode_tc(&kv->maps[l], a, B, c.n_kv_heads, c.head_dim, m->wdt, m->err(), s, pdl), 2);
       m->probe_stop(pe, s);
 
       if ((rc = use(k - 1, 0))) return rc;
