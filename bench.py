@@ -284,9 +284,13 @@ def one_core_sample(name, prompt_len, decode_steps, layers):
         return {"error": f"{type(e).__name__}: {e}"}
 
 
-# Bounded oracle samples: (prompt tokens, decode steps, layers) per workload.
+# Bounded oracle samples: (prompt tokens, decode steps, layers) per workload: the
+# CPU baseline of our arm (one sample of about 10-20 s), and the per-step sample of
+# the reference arm (small, so that 20 timed steps stay within a few minutes).
 ORACLE_SAMPLES = {"70b": (64, 24, 8), "1.2b": (128, 32, 16), "8b-hybrid": (64, 16, 8), "8b-ladder": (64, 16, 8),
                   "tiny": (16, 8, 2)}
+REF_SAMPLES = {"70b": (32, 8, 4), "1.2b": (64, 8, 16), "8b-hybrid": (32, 8, 4), "8b-ladder": (32, 8, 4),
+               "tiny": (16, 8, 2)}
 
 
 def cpu_baseline(name, dims):
@@ -296,12 +300,13 @@ def cpu_baseline(name, dims):
            "sample": sample_text(name, dims, r, prompt_len, decode_steps, cpu_threads()),
            "prefill_tok_s": r["prefill_tok_s"]}
     del r["W"]
-    # the 1.2B workload's oracle on one core, alongside
-    one = one_core_sample("1.2b", *ORACLE_SAMPLES["1.2b"])
-    if "error" not in one:
-        one["sample"] = sample_text("1.2b", synth.PRESETS["1.2b"], one, ORACLE_SAMPLES["1.2b"][0],
-                                    ORACLE_SAMPLES["1.2b"][1], 1)
-    out["one_core_1p2b"] = one
+    # the tiny and 1.2B workloads' oracle on one core, alongside
+    for small, key in (("tiny", "one_core_tiny"), ("1.2b", "one_core_1p2b")):
+        one = one_core_sample(small, *ORACLE_SAMPLES[small])
+        if "error" not in one:
+            one["sample"] = sample_text(small, synth.PRESETS[small], one, ORACLE_SAMPLES[small][0],
+                                        ORACLE_SAMPLES[small][1], 1)
+        out[key] = one
     return out
 
 
@@ -312,7 +317,7 @@ def run_reference(args, dims):
     rank, world, _ = dist_env()
     if rank != 0:
         return None
-    prompt_len, decode_steps, layers = ORACLE_SAMPLES[args.workload]
+    prompt_len, decode_steps, layers = REF_SAMPLES[args.workload]
     W = None
     for _ in range(args.warmup):
         r = oracle_sample(dims, prompt_len, decode_steps, layers, W)

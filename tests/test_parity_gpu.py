@@ -452,6 +452,33 @@ def test_host_and_device_errors(tiny):
     assert model.seq_lens.cpu().tolist()[0] == 32
 
 
+def test_non_finite_projection_output_is_flagged():
+    """A prefill whose SwiGLU activations leave the fp16 range (gate and up
+    weights of layer 0 scaled by 2^14, still finite fp16 weights) reports bit 4
+    of the device error word; the same model with bf16 storage (no overflow)
+    reports nothing."""
+    dims = small_dims()
+
+    def scale(name, layer, bits):
+        if layer != 0 or name not in ("w_gate", "w_up"):
+            return bits
+        f = (bits.astype(np.uint32) << 16).view(np.float32) * np.float32(2.0 ** 14)  # exact: a power of two
+        return (f.view(np.uint32) >> 16).astype(np.uint16)
+
+    prompts = prompts_for([24], dims["vocab"])
+    codes = {}
+    for dtype in ("fp16", "bf16"):
+        model = make_model(dims, gpu_weights(dims, transform=scale, dtype=dtype), max_batch=1, max_seq=32,
+                           page_size=16)
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            model.prefill(packed(prompts), [24])
+            codes[dtype] = model.device_error(s)
+        model.close()
+    assert codes["fp16"] & 4, codes
+    assert codes["bf16"] == 0, codes
+
+
 @pytest.mark.slow
 def test_full_size_1p2b_prefill_and_decode():
     """The 1.2B workload at its full prompt length, in the graph-replay launch
