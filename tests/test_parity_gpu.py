@@ -271,6 +271,30 @@ def test_batched_decode_on_tensor_cores(B):
         check_greedy(g_toks[s_], o_logits[s_], 6e-2)
 
 
+def test_maximum_batch_and_full_capacity():
+    """The largest batch the library takes (64 sequences: four 16-row chunks of
+    the batched projection, 64 prefill segments of ragged lengths from 1 to 126),
+    decode to the last position each sequence's pages hold, against the oracle;
+    one step more is refused before any launch."""
+    dims = small_dims()
+    B, cap = 64, 128
+    lens = [1 + (37 * b) % 126 for b in range(B)]  # at most cap - 2, so two decode steps fit
+    lens[0], lens[1] = cap - 2, 1  # one sequence ends exactly at its capacity
+    prompts = prompts_for(lens, dims["vocab"])
+    feed = np.stack([synth.tokens(2, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(B)])
+    model = make_model(dims, gpu_weights(dims), max_batch=B, max_seq=cap, page_size=32,
+                       max_prefill_tokens=sum(lens))
+    g_logits, _ = run_teacher_forced(model, prompts, feed, graph=True)
+    o_logits, _ = O.teacher_forced_decode(dims, oracle_weights(dims), prompts, feed)
+    for s_ in range(3):
+        compare_logits(g_logits[s_], o_logits[s_], f"B=64 step {s_}")
+    assert model.seq_len(0) == cap
+    with pytest.raises(ladder.LadderError) as e:
+        model.decode_step(torch.zeros(B, dtype=torch.int32, device="cuda"))
+    assert e.value.code == ladder.LADDER_ERR_CAPACITY
+    model.close()
+
+
 def test_ragged_batch_prefill_and_decode(tiny):
     dims, gw, ow = tiny
     lens = [5, 70, 33, 1, 64, 17]
