@@ -45,6 +45,8 @@ METRIC = "decode tok/s & % HBM roofline; prefill tok/s & % BF16 tensor peak (1 G
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DTYPE = ("fp16 storage of the bf16-valued weights; fp16 tensor-core operands (prefill GEMM activations "
          "as fp16 hi/lo pairs); fp32 accumulation and residual stream; fp16 KV cache")
+DTYPE_BF16 = ("bf16 weights; bf16 tensor-core operands (prefill GEMM activations as bf16 hi/lo pairs); fp32 "
+              "accumulation and residual stream; bf16 KV cache")
 L2_BYTES = 129 * 10 ** 6  # GB300 L2 cache
 
 # What each workload's step runs.  ctx: decode starts from a prompt of this many
@@ -56,8 +58,16 @@ PLANS = {
                   "prefill": [4096] * 4},
     "8b-ladder": {"decode": [{"batch": 1, "ctx": 2048, "steps": 128}], "prefill": [], "shard_k": 8},
     "tiny": {"decode": [{"batch": 1, "ctx": 16, "steps": 8}], "prefill": [16]},
+    # the 1.2B workload with bf16 storage: bf16 weights, KV cache and tensor-core operands
+    "1.2b-bf16": {"preset": "1.2b", "dtype": "bf16", "decode": [{"batch": 1, "ctx": 1024, "steps": 256}],
+                  "prefill": [1024]},
 }
-NESTED = ("1.2b", "8b-hybrid", "8b-ladder")
+NESTED = ("1.2b", "1.2b-bf16", "8b-hybrid", "8b-ladder")
+
+
+def plan_dims(name):
+    """Model dimensions of a workload (its preset's)."""
+    return dict(synth.PRESETS[PLANS[name].get("preset", name)])
 
 # DRAM traffic of the dominant kernel (the decode gate/up GEMV) per launch at
 # each workload's shape, from one ncu capture, valid only while the kernel's
@@ -288,9 +298,9 @@ def one_core_sample(name, prompt_len, decode_steps, layers):
 # CPU baseline of our arm (one sample of about 10-20 s), and the per-step sample of
 # the reference arm (small, so that 20 timed steps stay within a few minutes).
 ORACLE_SAMPLES = {"70b": (64, 24, 8), "1.2b": (128, 32, 16), "8b-hybrid": (64, 16, 8), "8b-ladder": (64, 16, 8),
-                  "tiny": (16, 8, 2)}
+                  "tiny": (16, 8, 2), "1.2b-bf16": (128, 32, 16)}
 REF_SAMPLES = {"70b": (32, 8, 4), "1.2b": (64, 8, 16), "8b-hybrid": (32, 8, 4), "8b-ladder": (32, 8, 4),
-               "tiny": (16, 8, 2)}
+               "tiny": (16, 8, 2), "1.2b-bf16": (64, 8, 16)}
 
 
 def cpu_baseline(name, dims):
@@ -350,7 +360,8 @@ def workload_config(name, dims):
                        f"{dims['n_standard_layers']} standard), d_model {dims['d_model']}, "
                        f"{dims['n_q_heads']}q/{dims['n_kv_heads']}kv heads x {dims['head_dim']}, "
                        f"ffn {dims['ffn_dim']}, vocab {dims['vocab']}" +
-                       (f", shard mode k = {plan['shard_k']}" if plan.get("shard_k") else ""),
+                       (f", shard mode k = {plan['shard_k']}" if plan.get("shard_k") else "") +
+                       (f", {plan['dtype']} weights, KV cache and tensor-core operands" if plan.get("dtype") else ""),
            "decode": [dict(d) for d in plan["decode"]], "prefill_tokens": list(plan["prefill"]),
            "l2": ("inputs larger than L2 (all weights streamed every step)" if decode_step_bytes(dims, [0]) > L2_BYTES
                   else "weights fit in L2 (a parity-size model, not a roofline workload)")}
@@ -374,7 +385,7 @@ def measure_workload(name, dims, steps, warmup, args, peaks, dev, world, headlin
     max_seq = max([d["ctx"] + d["steps"] + 1 for d in phases] + pre_lens)
     max_pre = max([d["batch"] * d["ctx"] for d in phases] + [sum(pre_lens)])
     log(f"{name}: generating weights on the device")
-    weights = ladder.synthetic_weights(dims, device=dev)
+    weights = ladder.synthetic_weights(dims, device=dev, dtype=plan.get("dtype", "fp16"))
     model = ladder.LadderModel(dims, weights, max_batch=max_batch, max_seq=max_seq, max_prefill_tokens=max_pre,
                                shard_k=shard_k)
     log(f"{name}: model ready")
@@ -581,7 +592,7 @@ def run_ours(args, dims):
     if not args.no_nested and args.workload == "70b":
         for name in NESTED:
             try:
-                nested[name] = measure_workload(name, dict(synth.PRESETS[name]), min(args.steps, 5),
+                nested[name] = measure_workload(name, plan_dims(name), min(args.steps, 5),
                                                 max(3, min(args.warmup, 3)), args, peaks, dev, world, headline=False)
             except Exception as e:  # recorded in the line; the headline stands
                 nested[name] = {"error": f"{type(e).__name__}: {e}"}
@@ -595,7 +606,8 @@ def run_ours(args, dims):
     out = {
         "metric": METRIC, "value": d0["tok_s"], "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": DTYPE, "data": "synthetic (random-init weights, random tokens)",
+        "vs_baseline": None, "dtype": DTYPE_BF16 if plan.get("dtype") == "bf16" else DTYPE,
+        "data": "synthetic (random-init weights, random tokens)",
         "config": dict(head["config"], batch=plan["decode"][0]["batch"], decode_ctx=plan["decode"][0]["ctx"],
                        decode_steps=plan["decode"][0]["steps"], parallelism=f"replicas x{world}",
                        decode_launch=("eager" if args.eager else "cuda graph") + (", no PDL" if args.no_pdl else ", PDL"),
@@ -641,7 +653,7 @@ def main():
     ap.add_argument("--no-schedules", action="store_true",
                     help="skip timing the standard and parallel-block schedules on the same weights")
     args = ap.parse_args()
-    dims = dict(synth.PRESETS[args.workload])
+    dims = plan_dims(args.workload)
     if args.layers:
         # kernel captures on a shallow copy of the workload (every layer has the same shapes)
         dims = sample_dims(dims, args.layers)

@@ -533,6 +533,28 @@ def test_full_size_1p2b_prefill_and_decode():
     assert rel[False] < rel[True]  # the hi/lo operands are the more accurate prefill
 
 
+@pytest.mark.slow
+def test_full_size_1p2b_bf16_storage():
+    """The 1.2B workload with bf16 storage (weights, KV cache and the prefill's
+    hi/lo tensor-core operands in bf16), the configuration of the bench's bf16
+    arm: its full prompt and three decode steps in the graph configuration,
+    against the oracle on the same bf16-valued weights."""
+    dims = dict(synth.PRESETS["1.2b"])
+    prompts = prompts_for([1024], dims["vocab"])
+    feed = synth.tokens(3, dims["vocab"], seed=synth.DECODE_SEED)[None, :]
+    model = make_model(dims, gpu_weights(dims, dtype="bf16"), max_batch=1, max_seq=1024 + 256,
+                       max_prefill_tokens=1024)
+    g_logits, g_toks = run_teacher_forced(model, prompts, feed, graph=True)
+    model.close()
+    del model
+    torch.cuda.empty_cache()
+    o_logits, _ = O.teacher_forced_decode(dims, O.synthetic_weights(dims), prompts, feed)
+    er = [compare_logits(g_logits[s], o_logits[s], f"1.2B bf16 step {s}") for s in range(4)]
+    ties = check_greedy(g_toks[:, 0], o_logits[:, 0], 2 * max(e for e, _ in er))
+    print(f"1.2B bf16 storage: max-abs {max(e for e, _ in er):.3e} rel-L2 {max(r for _, r in er):.3e}; "
+          f"steps decided by the near-tie rule: {ties}")
+
+
 @pytest.mark.parametrize("k,standard,graph", [(2, False, False), (2, True, True), (4, False, True), (4, True, False)])
 def test_shard_mode_matches_oracle(k, standard, graph):
     """Shard mode: row-parallel partial sums reduced on a second stream (ladder or standard schedule)."""
