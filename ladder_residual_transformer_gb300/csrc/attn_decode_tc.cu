@@ -238,7 +238,7 @@ cudaError_t attn_decode_tc_configure() {
 }
 
 cudaError_t launch_attn_decode_tc(const void* kv_map, const AttnDecodeParams& p, int B, int n_kv, int hd, int wdt,
-                                  int* err, cudaStream_t s, bool pdl) {
+                                  int* err, cudaStream_t s, bool pdl, bool pdl_combine) {
   if (p.split_len != AD_KEYS || (hd != 64 && hd != 128) || p.n_q / n_kv > 8) return cudaErrorInvalidValue;
   CUtensorMap map;
   memcpy(&map, kv_map, sizeof(map));
@@ -251,7 +251,7 @@ cudaError_t launch_attn_decode_tc(const void* kv_map, const AttnDecodeParams& p,
     e = hd == 64 ? launch_k(attn_decode_tc_kernel<bf16, 64>, grid, dim3(AD_THREADS), (size_t)AdCfg<64>::SMEM, s, pdl, map, p, err)
                  : launch_k(attn_decode_tc_kernel<bf16, 128>, grid, dim3(AD_THREADS), (size_t)AdCfg<128>::SMEM, s, pdl, map, p, err);
   if (e != cudaSuccess) return e;
-  return launch_attn_combine(p, B, hd, s, pdl);
+  return launch_attn_combine(p, B, hd, s, pdl_combine);
 }
 
 }  // namespace ladder

@@ -262,10 +262,11 @@ cudaError_t launch_attn_decode(const AttnDecodeParams& p, int B, int n_kv, int h
 cudaError_t launch_attn_combine(const AttnDecodeParams& p, int B, int hd, cudaStream_t s, bool pdl);
 // Decode attention on the tensor cores (mma.sync), K/V pages through the layer's
 // KV pool map (make_kv_tma_map); split_len 128, head_dim 64 or 128, up to 8 query
-// heads per KV head.  Launches the split kernel and the combine step.
+// heads per KV head.  Launches the split kernel (programmatic dependent launch
+// when `pdl`) and the combine step (when `pdl_combine`).
 cudaError_t attn_decode_tc_configure();
 cudaError_t launch_attn_decode_tc(const void* kv_map, const AttnDecodeParams& p, int B, int n_kv, int hd, int wdt,
-                                  int* err, cudaStream_t s, bool pdl);
+                                  int* err, cudaStream_t s, bool pdl, bool pdl_combine);
 // Temperature / top-k sampling of the next token (sample.cu); row b draws with
 // position pos[b] + pos_off.  temperature must be > 0.
 cudaError_t launch_sample(const float* logits, int B, int V, float temperature, int top_k, uint64_t seed,

@@ -49,6 +49,8 @@ namespace {
 
 constexpr int kSplitLen = 128;      // keys per decode-attention split
 constexpr int kArgmaxBlocks = 64;   // partial argmax blocks per sequence
+// Largest decode projection (weight bytes) launched with programmatic dependent launch.
+constexpr size_t kPdlMaxWeightBytes = (size_t)128 << 20;
 
 // Split-K workspace of the batched decode projections (B > 2), one region per
 // projection kind so that the two decode streams never share one.
@@ -753,7 +755,7 @@ int enqueue_decode_shard(ladder_model* m, ladder_kv* kv, const int32_t* tokens, 
       a.nsplit = nsplit; a.scale = 1.0f / sqrtf((float)c.head_dim);
       a.part_o = m->at<float>(P.part_o); a.part_ml = m->at<float>(P.part_ml); a.out = ao;
       auto pa = m->probe_start(LADDER_PROBE_ATTN, s);
-      LAUNCH(launch_attn_decode_tc(&kv->maps[l], a, B, c.n_kv_heads, c.head_dim, m->wdt, m->err(), s, pdl), 2);
+      LAUNCH(launch_attn_decode_tc(&kv->maps[l], a, B, c.n_kv_heads, c.head_dim, m->wdt, m->err(), s, pdl, pdl), 2);
       m->probe_stop(pa, s);
       o.x = ao; o.ldx = qd; o.K = qd / ksh; o.kfull = qd; o.ldw = qd; o.w0 = L.wo;
     } else {  // MLP module
@@ -813,6 +815,20 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
                    : m->residual_mode == LADDER_RESIDUAL_PARALLEL ? 0
                                                                   : c.n_standard_layers;
   const bool pdl = !(m->flags & LADDER_FLAG_NO_PDL);
+  // Programmatic dependent launch lets a kernel's blocks become resident while
+  // the previous kernel of its stream finishes, which hides a short kernel's
+  // ramp.  Behind a long kernel (a projection of more than kPdlMaxWeightBytes
+  // of weights) those blocks would wait on SM slots that the other ladder
+  // stream's kernels need, and a long kernel's own blocks would crowd the
+  // other stream; so a kernel launches early only when it is short and so is
+  // its predecessor.
+  bool long_prev[2] = {false, false};  // per stream: the last kernel was a long projection
+  auto early = [&](int si, size_t weight_bytes) {
+    return pdl && !long_prev[si] && weight_bytes <= kPdlMaxWeightBytes;
+  };
+  auto ran = [&](int si, size_t weight_bytes) { long_prev[si] = weight_bytes > kPdlMaxWeightBytes; };
+  const size_t wb_qkv = (size_t)(qd + 2 * kvd) * d * 2, wb_o = (size_t)qd * d * 2;
+  const size_t wb_gu = (size_t)2 * f * d * 2, wb_down = (size_t)f * d * 2, wb_lm = (size_t)c.vocab * d * 2;
   cudaStream_t streams[2] = {s, m->aux};
   int writer[3] = {0, 0, 0};  // stream index that last wrote each buffer
   bool forked = false;
@@ -834,7 +850,8 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
   };
   int rc;
 
-  LAUNCH(launch_embed(tokens, B, m->embed, m->wdt, d, c.vocab, m->X(0), m->err(), s, pdl), 1);
+  LAUNCH(launch_embed(tokens, B, m->embed, m->wdt, d, c.vocab, m->X(0), m->err(), s, early(0, 0)), 1);
+  ran(0, 0);
   if ((rc = wrote(0, 0))) return rc;
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerW& L = m->layers[l];
@@ -854,7 +871,8 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       auto pe = m->probe_start(LADDER_PROBE_QKV, s);
       g.err = m->err();
       m->splitk(g, SK_QKV);
-      LAUNCH(launch_gemv(g, GEMV_QKV, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, g.K, GEMV_QKV));
+      LAUNCH(launch_gemv(g, GEMV_QKV, m->wdt, m->num_sms, s, early(0, wb_qkv)), gemv_launch_count(B, g.K, GEMV_QKV));
+      ran(0, wb_qkv);
       m->probe_stop(pe, s);
 
       AttnDecodeParams a{};
@@ -862,7 +880,13 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       a.nsplit = nsplit; a.scale = 1.0f / sqrtf((float)c.head_dim);
       a.part_o = m->at<float>(P.part_o); a.part_ml = m->at<float>(P.part_ml); a.out = ao;
       pe = m->probe_start(LADDER_PROBE_ATTN, s);
-      LAUNCH(launch_attn_decode_tc(&kv->maps[l], a, B, c.n_kv_heads, c.head_dim, m->wdt, m->err(), s, pdl), 2);
+      // the split kernel reads the K/V of every split (its size for the rule
+      // above); the combine launches early only when the split kernel did
+      const size_t kv_bytes = (size_t)B * nsplit * kSplitLen * kvd * 2 * 2;
+      const bool attn_early = early(0, kv_bytes);
+      LAUNCH(launch_attn_decode_tc(&kv->maps[l], a, B, c.n_kv_heads, c.head_dim, m->wdt, m->err(), s, attn_early,
+                                   attn_early), 2);
+      ran(0, kv_bytes);
       m->probe_stop(pe, s);
 
       if ((rc = use(k - 1, 0))) return rc;
@@ -872,7 +896,8 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       pe = m->probe_start(LADDER_PROBE_OUT, s);
       o.err = m->err();
       m->splitk(o, SK_OUT);
-      LAUNCH(launch_gemv(o, GEMV_RESID, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, o.K, GEMV_RESID));
+      LAUNCH(launch_gemv(o, GEMV_RESID, m->wdt, m->num_sms, s, early(0, wb_o)), gemv_launch_count(B, o.K, GEMV_RESID));
+      ran(0, wb_o);
       m->probe_stop(pe, s);
       if ((rc = wrote(k, 0))) return rc;
     }
@@ -888,7 +913,8 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       auto pe = m->probe_start(LADDER_PROBE_GATEUP, ms);
       g.err = m->err();
       m->splitk(g, SK_GATEUP);
-      LAUNCH(launch_gemv(g, GEMV_GATEUP, m->wdt, m->num_sms, ms, pdl), gemv_launch_count(B, g.K, GEMV_GATEUP));
+      LAUNCH(launch_gemv(g, GEMV_GATEUP, m->wdt, m->num_sms, ms, early(mlp_stream, wb_gu)), gemv_launch_count(B, g.K, GEMV_GATEUP));
+      ran(mlp_stream, wb_gu);
       m->probe_stop(pe, ms);
 
       if ((rc = use(k - 1, mlp_stream))) return rc;
@@ -898,7 +924,8 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       pe = m->probe_start(LADDER_PROBE_DOWN, ms);
       o.err = m->err();
       m->splitk(o, SK_DOWN);
-      LAUNCH(launch_gemv(o, GEMV_RESID, m->wdt, m->num_sms, ms, pdl), gemv_launch_count(B, o.K, GEMV_RESID));
+      LAUNCH(launch_gemv(o, GEMV_RESID, m->wdt, m->num_sms, ms, early(mlp_stream, wb_down)), gemv_launch_count(B, o.K, GEMV_RESID));
+      ran(mlp_stream, wb_down);
       m->probe_stop(pe, ms);
       if ((rc = wrote(k, mlp_stream))) return rc;
     }
@@ -910,12 +937,13 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
   auto pe = m->probe_start(LADDER_PROBE_LMHEAD, s);
   h.err = m->err();
   m->splitk(h, SK_LMHEAD);
-  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s, pdl), gemv_launch_count(B, h.K, GEMV_LOGITS));
+  LAUNCH(launch_gemv(h, GEMV_LOGITS, m->wdt, m->num_sms, s, early(0, wb_lm)), gemv_launch_count(B, h.K, GEMV_LOGITS));
+  ran(0, wb_lm);
   m->probe_stop(pe, s);
   if (next_tok && m->samp_t > 0.f)  // the sampled token takes position seq_lens[b] + 1
-    LAUNCH(launch_sample(logits, B, c.vocab, m->samp_t, m->samp_k, m->samp_seed, kv->seq_lens, 1, next_tok, s, pdl), 1);
+    LAUNCH(launch_sample(logits, B, c.vocab, m->samp_t, m->samp_k, m->samp_seed, kv->seq_lens, 1, next_tok, s, early(0, 0)), 1);
   else if (next_tok)
-    LAUNCH(launch_argmax(logits, B, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i), kArgmaxBlocks, next_tok, s, pdl), 2);
+    LAUNCH(launch_argmax(logits, B, c.vocab, m->at<float>(P.am_v), m->at<int>(P.am_i), kArgmaxBlocks, next_tok, s, early(0, 0)), 2);
   LAUNCH(launch_advance(kv->seq_lens, B, s, pdl), 1);
   return LADDER_OK;
 }
