@@ -609,7 +609,89 @@ static cudaError_t set_gemv_attrs() {
   return cudaFuncSetAttribute(gemv_kernel<WT, BT, GEMV_LOGITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
+// Residency of the CUDA-core GEMV instantiations: the CTAs per SM that their
+// registers and threads allow, and their static shared memory; with the SM's
+// shared memory and the per-CTA reservation.  Read once, from gemv_configure
+// (model creation), never inside a stream capture.
+struct GemvResidency {
+  int ctas[2][3][5] = {};         // [weight dtype][batch tile 1, 2, 4][mode]
+  int static_smem[2][3][5] = {};
+  int smem_per_sm = 0;
+  int smem_reserved = 0;
+};
+
+template <typename WT, int BT>
+static void gemv_residency_row(GemvResidency& r, int w, int b) {
+  const void* f[5] = {(const void*)gemv_kernel<WT, BT, GEMV_QKV>, (const void*)gemv_kernel<WT, BT, GEMV_GATEUP>,
+                      (const void*)gemv_kernel<WT, BT, GEMV_RESID>, (const void*)gemv_kernel<WT, BT, GEMV_LOGITS>,
+                      (const void*)gemv_kernel<WT, BT, GEMV_PARTIAL>};
+  for (int m = 0; m < 5; ++m) {
+    int n = 0;
+    cudaFuncAttributes a{};
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f[m], GEMV_THREADS, 0) == cudaSuccess &&
+        cudaFuncGetAttributes(&a, f[m]) == cudaSuccess) {
+      r.ctas[w][b][m] = n;
+      r.static_smem[w][b][m] = (int)a.sharedSizeBytes;
+    } else {
+      (void)cudaGetLastError();  // leave the rule off for this kernel (ctas = 0)
+    }
+  }
+}
+
+static const GemvResidency& gemv_residency() {
+  static const GemvResidency r = [] {
+    GemvResidency t;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&t.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&t.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) {
+      (void)cudaGetLastError();
+      t.smem_per_sm = 0;
+      return t;
+    }
+    gemv_residency_row<bf16, 1>(t, WDT_BF16, 0);
+    gemv_residency_row<bf16, 2>(t, WDT_BF16, 1);
+    gemv_residency_row<bf16, 4>(t, WDT_BF16, 2);
+    gemv_residency_row<f16, 1>(t, WDT_F16, 0);
+    gemv_residency_row<f16, 2>(t, WDT_F16, 1);
+    gemv_residency_row<f16, 4>(t, WDT_F16, 2);
+    return t;
+  }();
+  return r;
+}
+
+// Staged chunk length of a projection whose rows take several chunks (ks = 1,
+// 8 tasks per CTA).  When the launch's CTAs would not all be resident at once,
+// the chunks are shortened (equal lengths, multiples of 256) until they are:
+// a second wave of a few CTAs, alone on their SMs, streams its rows at a
+// fraction of the bandwidth.  The 70B down projection (K = 28672) took 64 KB
+// chunks, 3 CTAs per SM and 512 CTAs in 1.12 waves (104.5 us per launch,
+// serialised); 3 chunks of 9728 columns give 4 CTAs per SM (registers) in one
+// wave: 70B decode step 22.64 -> 20.82 ms.  Chunk boundaries at multiples of
+// 256 leave each lane's columns and the order of its products unchanged, so the
+// result is bit-identical.
+static int gemv_fit_chunk(const GemvParams& p, int bt, int mode, int wdt, int num_sms) {
+  const GemvResidency& r = gemv_residency();
+  const int w = wdt == WDT_F16 ? WDT_F16 : WDT_BF16, b = bt == 1 ? 0 : (bt == 2 ? 1 : 2);
+  const int cap = r.ctas[w][b][mode];
+  if (cap <= 0 || r.smem_per_sm <= 0) return p.kc;
+  long long grid = (p.n_tasks + GEMV_WARPS - 1) / GEMV_WARPS;
+  if (grid > (long long)num_sms * 8) grid = (long long)num_sms * 8;  // launch_gemv's cap
+  int kc = p.kc;
+  int nch = (p.kfull + kc - 1) / kc;
+  while (kc > 2048) {
+    const int per_cta = bt * kc * (int)sizeof(float) + r.static_smem[w][b][mode] + r.smem_reserved;
+    int fit = r.smem_per_sm / per_cta;
+    if (fit > cap) fit = cap;
+    if ((long long)fit * num_sms >= grid) break;
+    ++nch;
+    kc = ((p.kfull + nch - 1) / nch + 255) / 256 * 256;
+  }
+  return kc;
+}
+
 cudaError_t gemv_configure() {
+  (void)gemv_residency();
   cudaError_t e;
   if ((e = set_gemv_attrs<bf16, 1>())) return e;
   if ((e = set_gemv_attrs<bf16, 2>())) return e;
@@ -686,6 +768,7 @@ cudaError_t launch_gemv(const GemvParams& p0, int mode, int wdt, int num_sms, cu
     }
     p.kc = gemv_chunk(p.B, p.kfull);
     if (mode == GEMV_PARTIAL && p.kc < p.kfull) return cudaErrorInvalidValue;  // shard partials stage one chunk
+    if (p.kc < p.kfull) p.kc = gemv_fit_chunk(p, bt, mode, wdt, num_sms);
     const size_t smem = (size_t)bt * p.kc * sizeof(float);
     // K split: the smallest that gives at least 1.5 CTAs per SM (more warps in
     // flight for short, wide matrices) while each slice stays a multiple of 256.
