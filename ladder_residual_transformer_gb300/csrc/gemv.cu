@@ -173,8 +173,9 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
         r0 = W0 + (size_t)(2 * task0) * K;
         r1 = r0 + K;
       }
-      const int kb = ks_ > 1 ? (warp % ks_) * (K / ks_) : 0;
-      const int ke_all = ks_ > 1 ? kb + K / ks_ : K;
+      const int span0 = (p.kc >= p.kfull ? K : p.kc) / ks_;  // the warp's slice of the first staged chunk
+      const int kb = ks_ > 1 ? (warp % ks_) * span0 : 0;
+      const int ke_all = ks_ > 1 ? kb + span0 : K;
       const int ke = one_round ? ke_all : min(ke_all, kb + GEMV_PF_HEAD);
       // one 128-byte line (64 elements) per lane per step
       for (int k = kb + lane * 64; k < ke; k += 32 * 64) {
@@ -221,7 +222,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
   const int rounds = (p.n_tasks + total_slots - 1) / total_slots;
   const int KF = p.kfull;  // length of the staged input rows
   const bool single_chunk = p.kc >= KF;
-  const int kspan = K / ks;  // single chunk when ks > 1
+  const int kspan = K / ks;  // the warp's slice of a single staged chunk
   __shared__ float s_part[GEMV_WARPS][2][BT];
 
   for (int r = 0; r < rounds; ++r) {
@@ -269,8 +270,9 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
         // which are single-chunk).
         const WT* p0 = row0 + k0;
         const WT* p1 = row1 + k0;
-        const int kb = ks > 1 ? kslice * kspan : 0;
-        const int ke = ks > 1 ? kb + kspan : (MODE == GEMV_PARTIAL ? K : kc);
+        const int ksl = single_chunk ? kspan : kc / ks;  // rows staged in chunks: a slice of each chunk
+        const int kb = ks > 1 ? kslice * ksl : 0;
+        const int ke = ks > 1 ? kb + ksl : (MODE == GEMV_PARTIAL ? K : kc);
         int k = kb + lane * 8;
         for (; k + 768 < ke; k += 1024) {
           uint4 wa[4], wb[4];
@@ -660,34 +662,34 @@ static const GemvResidency& gemv_residency() {
   return r;
 }
 
-// Staged chunk length of a projection whose rows take several chunks (ks = 1,
-// 8 tasks per CTA).  When the launch's CTAs would not all be resident at once,
-// the chunks are shortened (equal lengths, multiples of 256) until they are:
-// a second wave of a few CTAs, alone on their SMs, streams its rows at a
-// fraction of the bandwidth.  The 70B down projection (K = 28672) took 64 KB
-// chunks, 3 CTAs per SM and 512 CTAs in 1.12 waves (104.5 us per launch,
-// serialised); 3 chunks of 9728 columns give 4 CTAs per SM (registers) in one
-// wave: 70B decode step 22.64 -> 20.82 ms.  Chunk boundaries at multiples of
-// 256 leave each lane's columns and the order of its products unchanged, so the
-// result is bit-identical.
-static int gemv_fit_chunk(const GemvParams& p, int bt, int mode, int wdt, int num_sms) {
+// Longest staged chunk -- at most kc_max columns, a multiple of `align`, the row
+// cut into equal chunks -- with which a launch of `grid` CTAs is resident at
+// once (one wave); 0 when no chunk of at least 2048 columns gives that.  A
+// second wave of a few CTAs, alone on their SMs, streams its rows at a fraction
+// of the bandwidth.  Chunk boundaries at multiples of 256 leave each lane's
+// columns and the order of its products unchanged.
+static int gemv_wave_chunk(int kfull, int kc_max, int align, long long grid, int bt, int mode, int wdt,
+                           int num_sms) {
   const GemvResidency& r = gemv_residency();
   const int w = wdt == WDT_F16 ? WDT_F16 : WDT_BF16, b = bt == 1 ? 0 : (bt == 2 ? 1 : 2);
   const int cap = r.ctas[w][b][mode];
-  if (cap <= 0 || r.smem_per_sm <= 0) return p.kc;
-  long long grid = (p.n_tasks + GEMV_WARPS - 1) / GEMV_WARPS;
-  if (grid > (long long)num_sms * 8) grid = (long long)num_sms * 8;  // launch_gemv's cap
-  int kc = p.kc;
-  int nch = (p.kfull + kc - 1) / kc;
-  while (kc > 2048) {
+  if (cap <= 0 || r.smem_per_sm <= 0 || kfull % align) return 0;
+  kc_max -= kc_max % align;
+  if (kc_max <= 0) return 0;
+  for (int nch = (kfull + kc_max - 1) / kc_max;; ++nch) {
+    const int kc = ((kfull + nch - 1) / nch + align - 1) / align * align;
+    if (kc < 2048) return 0;
     const int per_cta = bt * kc * (int)sizeof(float) + r.static_smem[w][b][mode] + r.smem_reserved;
     int fit = r.smem_per_sm / per_cta;
     if (fit > cap) fit = cap;
-    if ((long long)fit * num_sms >= grid) break;
-    ++nch;
-    kc = ((p.kfull + nch - 1) / nch + 255) / 256 * 256;
+    if ((long long)fit * num_sms >= grid) return kc;
   }
-  return kc;
+}
+
+static long long gemv_grid(int n_tasks, int ks, int num_sms) {
+  const int tpc = GEMV_WARPS / ks;
+  const long long g = (n_tasks + tpc - 1) / tpc;
+  return g < (long long)num_sms * 8 ? g : (long long)num_sms * 8;
 }
 
 cudaError_t gemv_configure() {
@@ -768,8 +770,6 @@ cudaError_t launch_gemv(const GemvParams& p0, int mode, int wdt, int num_sms, cu
     }
     p.kc = gemv_chunk(p.B, p.kfull);
     if (mode == GEMV_PARTIAL && p.kc < p.kfull) return cudaErrorInvalidValue;  // shard partials stage one chunk
-    if (p.kc < p.kfull) p.kc = gemv_fit_chunk(p, bt, mode, wdt, num_sms);
-    const size_t smem = (size_t)bt * p.kc * sizeof(float);
     // K split: the smallest that gives at least 1.5 CTAs per SM (more warps in
     // flight for short, wide matrices) while each slice stays a multiple of 256.
     // Residual projections (O, down: few outputs, long rows) split K at least
@@ -786,6 +786,35 @@ cudaError_t launch_gemv(const GemvParams& p0, int mode, int wdt, int num_sms, cu
       // runs once per task; measured 0.8% faster on the 1.2B step than K split 2)
       if (mode == GEMV_QKV) p.ks = 1;
     }
+    // Rows longer than one chunk (70B down projection, K = 28672): chunks short
+    // enough for one wave.  64 KB chunks gave 3 CTAs per SM and 512 CTAs in 1.12
+    // waves (104.5 us per launch, serialised); 3 chunks of 9728 columns give 4
+    // CTAs per SM (registers) in one wave: 70B decode step 22.64 -> 20.59 ms,
+    // logits bit-identical.
+    if (p.kc < p.kfull) {
+      const int kc = gemv_wave_chunk(p.kfull, p.kc, 256, gemv_grid(p.n_tasks, 1, num_sms), bt, mode, wdt, num_sms);
+      if (kc) p.kc = kc;
+    }
+    // Residual projections (O, down): the largest K split of 4, 2 or 1 whose
+    // launch fits one wave, staging the rows in chunks where that raises the
+    // CTAs per SM; when none does, the split chosen above.  8B: O at K split 2
+    // (512 CTAs, was 1024 in 1.68 waves), down at K split 2 in two chunks of
+    // 7168 (was 1024 CTAs in 2.25 waves at 3 per SM); 70B O at no split (512
+    // CTAs, was 1216 in two waves).  Decode step, graph, context 2048: 8B hybrid
+    // B = 1 3057 -> 2908 us, B = 2 4228 -> 3759 us, 70B 20.87 -> 20.78 ms; the
+    // 1.2B launches already fitted (unchanged).
+    if (mode == GEMV_RESID) {
+      for (int ks = 4; ks >= 1; ks /= 2) {
+        const int kc = gemv_wave_chunk(p.kfull, gemv_chunk(p.B, p.kfull), 256 * ks, gemv_grid(p.n_tasks, ks, num_sms),
+                                       bt, mode, wdt, num_sms);
+        if (kc) {
+          p.ks = ks;
+          p.kc = kc;
+          break;
+        }
+      }
+    }
+    const size_t smem = (size_t)bt * p.kc * sizeof(float);
     const int tpc = GEMV_WARPS / p.ks;
     int grid = (p.n_tasks + tpc - 1) / tpc;
     const int cap = num_sms * 8;
