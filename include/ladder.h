@@ -153,7 +153,9 @@ typedef struct {
  * fixed order 0..k-1, to the residual.  A ladder module does not wait for the
  * previous module's reduce, so the reduce overlaps its GEMVs; a standard
  * module waits for it.  Requires n_q_heads, n_kv_heads divisible by k and
- * n_q_heads*head_dim/k, ffn_dim/k multiples of 256.  Prefill is unsharded (the
+ * n_q_heads*head_dim/k, ffn_dim/k multiples of 256, ffn_dim/k at most 16384
+ * (a decode GEMV of 2 rows: 8192; of 3 or 4 rows: 4096, else the decode step
+ * returns LADDER_ERR_CUDA).  Prefill is unsharded (the
  * same function, up to fp32 reassociation). */
 
 /* Storage types.  bf16-valued weights convert to fp16 exactly when

@@ -153,7 +153,8 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
   {
     const int ks_ = p.ks;
     const int task0 = blockIdx.x * (GEMV_WARPS / ks_) + warp / ks_;
-    const bool one_round = p.kc >= p.kfull && (long long)gridDim.x * (GEMV_WARPS / ks_) >= p.n_tasks;
+    const bool one_round =
+        (MODE == GEMV_PARTIAL || p.kc >= p.kfull) && (long long)gridDim.x * (GEMV_WARPS / ks_) >= p.n_tasks;
     if (task0 < p.n_tasks) {
       const WT* r0;
       const WT* r1;
@@ -220,7 +221,10 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
   const int slot = warp / ks, kslice = warp % ks;
   const int total_slots = gridDim.x * tpc;
   const int rounds = (p.n_tasks + total_slots - 1) / total_slots;
-  const int KF = p.kfull;  // length of the staged input rows
+  // Length of the staged input rows: the whole row, or for shard partials the
+  // K-slice of one shard (a CTA's tasks in one round share a shard: its tasks
+  // per round divide the shard's task count).
+  const int KF = MODE == GEMV_PARTIAL ? K : p.kfull;
   const bool single_chunk = p.kc >= KF;
   const int kspan = K / ks;  // the warp's slice of a single staged chunk
   __shared__ float s_part[GEMV_WARPS][2][BT];
@@ -235,6 +239,10 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
     int local = 0, kind = 0;  // QKV: kind 0 = q, 1 = k, 2 = v; local = row inside its matrix
     int koff = 0;             // PARTIAL: first input element of the task's shard
     if (active) gemv_task_rows<WT, MODE>(p, task, row0, row1, kind, local, koff);
+    // PARTIAL: the shard whose slice this round stages (every CTA stages one,
+    // active or not, so that all threads reach the barriers)
+    int xoff = 0;
+    if (MODE == GEMV_PARTIAL) xoff = (min(r * total_slots + blockIdx.x * tpc, p.n_tasks - 1) / p.shard_tasks) * K;
 
     float a0[BT], a1[BT];
 #pragma unroll
@@ -242,13 +250,13 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
 
     for (int k0 = 0; k0 < KF; k0 += p.kc) {
       const int kc = min(p.kc, KF - k0);
-      if (!single_chunk || r == 0) {
+      if (!single_chunk || r == 0 || MODE == GEMV_PARTIAL) {
         __syncthreads();
         // Stage the (normalised) input chunk in the two-plane layout.
         for (int i = tid * 4; i < kc; i += GEMV_THREADS * 4) {
           float4 gv = make_float4(1.f, 1.f, 1.f, 1.f);
           if (g != nullptr) {
-            const uint2 graw = *reinterpret_cast<const uint2*>(g + k0 + i);
+            const uint2 graw = *reinterpret_cast<const uint2*>(g + xoff + k0 + i);
             gv = make_float4(C::lo(graw.x), C::hi(graw.x), C::lo(graw.y), C::hi(graw.y));
           }
           const int dst = ((i & 4) ? (kc >> 1) : 0) + ((i >> 3) << 2);
@@ -256,7 +264,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
           for (int b = 0; b < BT; ++b) {
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
             if (b < p.B) {
-              v = *reinterpret_cast<const float4*>(p.x + (size_t)b * p.ldx + k0 + i);
+              v = *reinterpret_cast<const float4*>(p.x + (size_t)b * p.ldx + xoff + k0 + i);
               const float sc = (p.g != nullptr) ? s_rms[b] : 1.f;
               v.x *= sc * gv.x; v.y *= sc * gv.y; v.z *= sc * gv.z; v.w *= sc * gv.w;
             }
@@ -266,13 +274,13 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
         __syncthreads();
       }
       if (active) {
-        // Weights: row + k0 + k; staged input: element koff + k (koff = 0 but for shard partials,
-        // which are single-chunk).
+        // Weights: row + k0 + k (a shard's rows start at its slice); staged
+        // input: element k of the chunk (of the shard's slice).
         const WT* p0 = row0 + k0;
         const WT* p1 = row1 + k0;
         const int ksl = single_chunk ? kspan : kc / ks;  // rows staged in chunks: a slice of each chunk
         const int kb = ks > 1 ? kslice * ksl : 0;
-        const int ke = ks > 1 ? kb + ksl : (MODE == GEMV_PARTIAL ? K : kc);
+        const int ke = ks > 1 ? kb + ksl : kc;
         int k = kb + lane * 8;
         for (; k + 768 < ke; k += 1024) {
           uint4 wa[4], wb[4];
@@ -283,15 +291,15 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_kernel(const GemvParams p) 
           }
 #pragma unroll
           for (int s = 0; s < 4; ++s) {
-            gemv_fma<WT, BT>(wa[s], u, kc, koff + k + 256 * s, a0);
-            gemv_fma<WT, BT>(wb[s], u, kc, koff + k + 256 * s, a1);
+            gemv_fma<WT, BT>(wa[s], u, kc, k + 256 * s, a0);
+            gemv_fma<WT, BT>(wb[s], u, kc, k + 256 * s, a1);
           }
         }
         for (; k < ke; k += 256) {
           const uint4 wa = ld_stream_u4(p0 + k);
           const uint4 wb = ld_stream_u4(p1 + k);
-          gemv_fma<WT, BT>(wa, u, kc, koff + k, a0);
-          gemv_fma<WT, BT>(wb, u, kc, koff + k, a1);
+          gemv_fma<WT, BT>(wa, u, kc, k, a0);
+          gemv_fma<WT, BT>(wb, u, kc, k, a1);
         }
       }
     }
@@ -768,15 +776,16 @@ cudaError_t launch_gemv(const GemvParams& p0, int mode, int wdt, int num_sms, cu
       p.ldw = p.K;
       p.shard_tasks = p.n_tasks;
     }
-    p.kc = gemv_chunk(p.B, p.kfull);
-    if (mode == GEMV_PARTIAL && p.kc < p.kfull) return cudaErrorInvalidValue;  // shard partials stage one chunk
+    // Shard partials stage one shard's K-slice of the row (one chunk).
+    p.kc = mode == GEMV_PARTIAL ? p.K : gemv_chunk(p.B, p.kfull);
+    if (mode == GEMV_PARTIAL && p.kc > gemv_chunk(p.B, p.K)) return cudaErrorInvalidValue;
     // K split: the smallest that gives at least 1.5 CTAs per SM (more warps in
     // flight for short, wide matrices) while each slice stays a multiple of 256.
     // Residual projections (O, down: few outputs, long rows) split K at least
     // 4 ways (measured on the 1.2B and 8B decode steps: 1.2% and 4.8% faster
     // than the 1.5-CTAs-per-SM rule alone); QKV never splits.
     p.ks = 1;
-    if (p.kc >= p.kfull) {
+    if (p.kc >= p.kfull || mode == GEMV_PARTIAL) {
       while (p.ks < GEMV_WARPS && (long long)p.n_tasks * p.ks < (long long)num_sms * 12 &&
              (p.K / (2 * p.ks)) % 256 == 0)
         p.ks *= 2;
@@ -791,7 +800,7 @@ cudaError_t launch_gemv(const GemvParams& p0, int mode, int wdt, int num_sms, cu
     // waves (104.5 us per launch, serialised); 3 chunks of 9728 columns give 4
     // CTAs per SM (registers) in one wave: 70B decode step 22.64 -> 20.59 ms,
     // logits bit-identical.
-    if (p.kc < p.kfull) {
+    if (p.kc < p.kfull && mode != GEMV_PARTIAL) {
       const int kc = gemv_wave_chunk(p.kfull, p.kc, 256, gemv_grid(p.n_tasks, 1, num_sms), bt, mode, wdt, num_sms);
       if (kc) p.kc = kc;
     }

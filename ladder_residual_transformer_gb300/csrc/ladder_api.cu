@@ -147,8 +147,8 @@ int validate_config(const ladder_config* c) {
       return fail(LADDER_ERR_INVALID, "shard_k=%d must divide n_q_heads and n_kv_heads", k);
     if ((c->n_q_heads * c->head_dim / k) % 256 || (c->ffn_dim / k) % 256 || c->ffn_dim % k)
       return fail(LADDER_ERR_UNSUPPORTED, "shard_k=%d: per-shard O and down depths must be multiples of 256", k);
-    if ((size_t)c->ffn_dim * 4 > 64 * 1024)
-      return fail(LADDER_ERR_UNSUPPORTED, "shard mode stages whole ffn rows: ffn_dim <= 16384 required");
+    if ((size_t)(c->ffn_dim / k) * 4 > 64 * 1024)
+      return fail(LADDER_ERR_UNSUPPORTED, "shard mode stages one shard's slice of a row: ffn_dim/shard_k <= 16384 required");
   }
   if (c->page_size != 16 && c->page_size != 32 && c->page_size != 64)
     return fail(LADDER_ERR_INVALID, "page_size=%d must be 16, 32 or 64", c->page_size);
@@ -231,7 +231,7 @@ struct ladder_model {
   int* err() { return at<int>(plan.err); }
 
   // Point a batched decode projection at its split-K region (no-op when the
-  // model was created for at most 4 rows).
+  // model was created for at most 2 rows).
   void splitk(GemvParams& g, int kind) {
     if (!plan.sk_bytes[kind]) return;
     const GemvSplitK sk = gemv_splitk_shape(g.n_tasks, g.K);

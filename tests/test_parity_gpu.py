@@ -578,6 +578,23 @@ def test_shard_mode_matches_oracle(k, standard, graph):
         compare_logits(g_logits[s_], o_logits[s_], f"shard k={k} standard={standard} step {s_}")
 
 
+@pytest.mark.parametrize("k,ffn,B", [(2, 10240, 2), (4, 4096, 4)])
+def test_shard_mode_batches_and_wide_ffn(k, ffn, B):
+    """Shard mode with the row-parallel partials of 2 rows over a 10240-wide ffn
+    (each CTA stages one shard's 5120-column slice of a row: the whole rows would
+    not fit its staging buffer) and of 4 rows (batch tile 4), ragged prompts."""
+    dims = small_dims(d_model=1024, n_q_heads=8, n_kv_heads=4, head_dim=128, ffn_dim=ffn, vocab=2048)
+    gw, ow = gpu_weights(dims), oracle_weights(dims)
+    lens = [40, 9, 23, 1][:B]
+    prompts = prompts_for(lens, dims["vocab"])
+    feed = np.stack([synth.tokens(4, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(B)])
+    model = make_model(dims, gw, max_batch=B, max_seq=64, page_size=32, shard_k=k)
+    g_logits, _ = run_teacher_forced(model, prompts, feed, graph=True)
+    o_logits, _ = O.teacher_forced_decode(dims, ow, prompts, feed)
+    for s_ in range(5):
+        compare_logits(g_logits[s_], o_logits[s_], f"shard k={k} ffn={ffn} B={B} step {s_}")
+
+
 def test_shard_config_is_validated():
     dims = small_dims(d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=3072, vocab=2048)
     gw = gpu_weights(dims)
