@@ -568,23 +568,118 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_splitk_kernel(const GemvPar
     }
 }
 
+// Residency of the decode projection kernels: the CTAs per SM that their
+// registers and threads allow, and their static shared memory; with the SM's
+// shared memory and the per-CTA reservation.  Read once, from gemv_configure
+// (model creation), never inside a stream capture.
+struct GemvResidency {
+  int ctas[2][3][5] = {};         // GEMV: [weight dtype][batch tile 1, 2, 4][mode]
+  int static_smem[2][3][5] = {};
+  int mma_ctas[2][4] = {};        // split-K projection: [weight dtype][mode]
+  int mma_static_smem[2][4] = {};
+  int smem_per_sm = 0;
+  int smem_reserved = 0;
+};
+
+static void residency_of(const void* fn, int& ctas, int& static_smem) {
+  int n = 0;
+  cudaFuncAttributes a{};
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, GEMV_THREADS, 0) == cudaSuccess &&
+      cudaFuncGetAttributes(&a, fn) == cudaSuccess) {
+    ctas = n;
+    static_smem = (int)a.sharedSizeBytes;
+  } else {
+    (void)cudaGetLastError();  // leave the rules that use it off for this kernel (ctas = 0)
+  }
+}
+
+template <typename WT>
+static void gemv_mma_residency_row(GemvResidency& r, int w) {
+  const void* f[4] = {(const void*)gemv_splitk_kernel<WT, GEMV_QKV>, (const void*)gemv_splitk_kernel<WT, GEMV_GATEUP>,
+                      (const void*)gemv_splitk_kernel<WT, GEMV_RESID>, (const void*)gemv_splitk_kernel<WT, GEMV_LOGITS>};
+  for (int m = 0; m < 4; ++m) residency_of(f[m], r.mma_ctas[w][m], r.mma_static_smem[w][m]);
+}
+
+template <typename WT, int BT>
+static void gemv_residency_row(GemvResidency& r, int w, int b) {
+  const void* f[5] = {(const void*)gemv_kernel<WT, BT, GEMV_QKV>, (const void*)gemv_kernel<WT, BT, GEMV_GATEUP>,
+                      (const void*)gemv_kernel<WT, BT, GEMV_RESID>, (const void*)gemv_kernel<WT, BT, GEMV_LOGITS>,
+                      (const void*)gemv_kernel<WT, BT, GEMV_PARTIAL>};
+  for (int m = 0; m < 5; ++m) residency_of(f[m], r.ctas[w][b][m], r.static_smem[w][b][m]);
+}
+
+static const GemvResidency& gemv_residency() {
+  static const GemvResidency r = [] {
+    GemvResidency t;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&t.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&t.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) {
+      (void)cudaGetLastError();
+      t.smem_per_sm = 0;
+      return t;
+    }
+    gemv_residency_row<bf16, 1>(t, WDT_BF16, 0);
+    gemv_residency_row<bf16, 2>(t, WDT_BF16, 1);
+    gemv_residency_row<bf16, 4>(t, WDT_BF16, 2);
+    gemv_residency_row<f16, 1>(t, WDT_F16, 0);
+    gemv_residency_row<f16, 2>(t, WDT_F16, 1);
+    gemv_residency_row<f16, 4>(t, WDT_F16, 2);
+    gemv_mma_residency_row<bf16>(t, WDT_BF16);
+    gemv_mma_residency_row<f16>(t, WDT_F16);
+    return t;
+  }();
+  return r;
+}
+
+// Shared-memory carveout of one launch: the smallest share of the SM's unified
+// memory that holds the CTAs per SM the launch can use (its grid over the SMs,
+// at most `cap`, what registers and threads allow), so that the rest serves as
+// L1 for the weight loads in flight; -1 (the driver's choice) when unknown.
+// Measured on the batched projection (8B hybrid, 16 rows, context 2048): the
+// 132 KB configuration (3 CTAs per SM) 5090 -> 4910 us per step against the
+// driver's choice; 68 KB (2 CTAs) 5250 us; all shared memory 6100 us.
+static int carveout_for(long long grid, size_t smem, int static_smem, int cap, int num_sms) {
+  const GemvResidency& r = gemv_residency();
+  if (cap <= 0 || r.smem_per_sm <= 0 || num_sms <= 0) return -1;
+  long long want = (grid + num_sms - 1) / num_sms;
+  if (want > cap) want = cap;
+  if (want < 1) want = 1;
+  const long long need = want * ((long long)smem + static_smem + r.smem_reserved);
+  const long long pct = (need * 100 + r.smem_per_sm - 1) / r.smem_per_sm;
+  return pct > 100 ? 100 : (int)pct;
+}
+
+static int gemv_carveout(int grid, size_t smem, int bt, int mode, int wdt, int num_sms) {
+  const GemvResidency& r = gemv_residency();
+  const int w = wdt == WDT_F16 ? WDT_F16 : WDT_BF16, b = bt == 1 ? 0 : (bt == 2 ? 1 : 2);
+  return carveout_for(grid, smem, r.static_smem[w][b][mode], r.ctas[w][b][mode], num_sms);
+}
+
 template <typename WT>
 static cudaError_t set_gemv_mma_attrs() {
   const int bytes = 16 * (GM_KL_MAX + 8) * 2;
+  const void* fns[4] = {(const void*)gemv_splitk_kernel<WT, GEMV_QKV>, (const void*)gemv_splitk_kernel<WT, GEMV_GATEUP>,
+                        (const void*)gemv_splitk_kernel<WT, GEMV_RESID>, (const void*)gemv_splitk_kernel<WT, GEMV_LOGITS>};
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(gemv_splitk_kernel<WT, GEMV_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
-  if ((e = cudaFuncSetAttribute(gemv_splitk_kernel<WT, GEMV_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
-  if ((e = cudaFuncSetAttribute(gemv_splitk_kernel<WT, GEMV_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
-  return cudaFuncSetAttribute(gemv_splitk_kernel<WT, GEMV_LOGITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  for (const void* fn : fns)
+    if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
+  return cudaSuccess;
 }
 
 // Rows b0 .. b0 + 15 (at most) of a batched projection on the tensor cores.
-static cudaError_t launch_gemv_mma(GemvParams p, int mode, int wdt, cudaStream_t s, bool pdl) {
+static cudaError_t launch_gemv_mma(GemvParams p, int mode, int wdt, int num_sms, cudaStream_t s, bool pdl) {
   if (p.sk_part == nullptr || p.sk_ss == nullptr || p.sk_count == nullptr) return cudaErrorInvalidValue;
   const GemvSplitK sk = gemv_splitk_shape(p.n_tasks, p.K);
   const dim3 grid(sk.n_groups, sk.ksplit), block(GEMV_THREADS);
   const size_t smem = (size_t)16 * (sk.kl + 8) * 2;
-  auto go = [&](auto kern) { return launch_k(kern, grid, block, smem, s, pdl, p, sk.ksplit, sk.kl); };
+  int co = -1;
+  if (p.carve) {
+    const GemvResidency& r = gemv_residency();
+    const int w = wdt == WDT_F16 ? WDT_F16 : WDT_BF16, m = mode < 4 ? mode : GEMV_LOGITS;
+    co = carveout_for((long long)grid.x * grid.y, smem, r.mma_static_smem[w][m], r.mma_ctas[w][m], num_sms);
+  }
+  auto go = [&](auto kern) { return launch_k_carveout(kern, grid, block, smem, s, pdl, co, p, sk.ksplit, sk.kl); };
   if (wdt == WDT_F16) {
     switch (mode) {
       case GEMV_QKV: return go(gemv_splitk_kernel<f16, GEMV_QKV>);
@@ -617,57 +712,6 @@ static cudaError_t set_gemv_attrs() {
   if ((e = cudaFuncSetAttribute(gemv_kernel<WT, BT, GEMV_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
   if ((e = cudaFuncSetAttribute(gemv_kernel<WT, BT, GEMV_PARTIAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
   return cudaFuncSetAttribute(gemv_kernel<WT, BT, GEMV_LOGITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-}
-
-// Residency of the CUDA-core GEMV instantiations: the CTAs per SM that their
-// registers and threads allow, and their static shared memory; with the SM's
-// shared memory and the per-CTA reservation.  Read once, from gemv_configure
-// (model creation), never inside a stream capture.
-struct GemvResidency {
-  int ctas[2][3][5] = {};         // [weight dtype][batch tile 1, 2, 4][mode]
-  int static_smem[2][3][5] = {};
-  int smem_per_sm = 0;
-  int smem_reserved = 0;
-};
-
-template <typename WT, int BT>
-static void gemv_residency_row(GemvResidency& r, int w, int b) {
-  const void* f[5] = {(const void*)gemv_kernel<WT, BT, GEMV_QKV>, (const void*)gemv_kernel<WT, BT, GEMV_GATEUP>,
-                      (const void*)gemv_kernel<WT, BT, GEMV_RESID>, (const void*)gemv_kernel<WT, BT, GEMV_LOGITS>,
-                      (const void*)gemv_kernel<WT, BT, GEMV_PARTIAL>};
-  for (int m = 0; m < 5; ++m) {
-    int n = 0;
-    cudaFuncAttributes a{};
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f[m], GEMV_THREADS, 0) == cudaSuccess &&
-        cudaFuncGetAttributes(&a, f[m]) == cudaSuccess) {
-      r.ctas[w][b][m] = n;
-      r.static_smem[w][b][m] = (int)a.sharedSizeBytes;
-    } else {
-      (void)cudaGetLastError();  // leave the rule off for this kernel (ctas = 0)
-    }
-  }
-}
-
-static const GemvResidency& gemv_residency() {
-  static const GemvResidency r = [] {
-    GemvResidency t;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&t.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&t.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) {
-      (void)cudaGetLastError();
-      t.smem_per_sm = 0;
-      return t;
-    }
-    gemv_residency_row<bf16, 1>(t, WDT_BF16, 0);
-    gemv_residency_row<bf16, 2>(t, WDT_BF16, 1);
-    gemv_residency_row<bf16, 4>(t, WDT_BF16, 2);
-    gemv_residency_row<f16, 1>(t, WDT_F16, 0);
-    gemv_residency_row<f16, 2>(t, WDT_F16, 1);
-    gemv_residency_row<f16, 4>(t, WDT_F16, 2);
-    return t;
-  }();
-  return r;
 }
 
 // Longest staged chunk -- at most kc_max columns, a multiple of `align`, the row
@@ -714,23 +758,24 @@ cudaError_t gemv_configure() {
 }
 
 template <typename WT, int BT>
-static cudaError_t gemv_dispatch(const GemvParams& p, int mode, int grid, size_t smem, cudaStream_t s, bool pdl) {
+static cudaError_t gemv_dispatch(const GemvParams& p, int mode, int grid, size_t smem, cudaStream_t s, bool pdl,
+                                 int co) {
   const dim3 g(grid), b(GEMV_THREADS);
   switch (mode) {
-    case GEMV_QKV: return launch_k(gemv_kernel<WT, BT, GEMV_QKV>, g, b, smem, s, pdl, p);
-    case GEMV_GATEUP: return launch_k(gemv_kernel<WT, BT, GEMV_GATEUP>, g, b, smem, s, pdl, p);
-    case GEMV_RESID: return launch_k(gemv_kernel<WT, BT, GEMV_RESID>, g, b, smem, s, pdl, p);
-    case GEMV_PARTIAL: return launch_k(gemv_kernel<WT, BT, GEMV_PARTIAL>, g, b, smem, s, pdl, p);
-    default: return launch_k(gemv_kernel<WT, BT, GEMV_LOGITS>, g, b, smem, s, pdl, p);
+    case GEMV_QKV: return launch_k_carveout(gemv_kernel<WT, BT, GEMV_QKV>, g, b, smem, s, pdl, co, p);
+    case GEMV_GATEUP: return launch_k_carveout(gemv_kernel<WT, BT, GEMV_GATEUP>, g, b, smem, s, pdl, co, p);
+    case GEMV_RESID: return launch_k_carveout(gemv_kernel<WT, BT, GEMV_RESID>, g, b, smem, s, pdl, co, p);
+    case GEMV_PARTIAL: return launch_k_carveout(gemv_kernel<WT, BT, GEMV_PARTIAL>, g, b, smem, s, pdl, co, p);
+    default: return launch_k_carveout(gemv_kernel<WT, BT, GEMV_LOGITS>, g, b, smem, s, pdl, co, p);
   }
 }
 
 template <typename WT>
 static cudaError_t gemv_dispatch_bt(const GemvParams& p, int bt, int mode, int grid, size_t smem, cudaStream_t s,
-                                    bool pdl) {
-  if (bt == 1) return gemv_dispatch<WT, 1>(p, mode, grid, smem, s, pdl);
-  if (bt == 2) return gemv_dispatch<WT, 2>(p, mode, grid, smem, s, pdl);
-  return gemv_dispatch<WT, 4>(p, mode, grid, smem, s, pdl);
+                                    bool pdl, int co) {
+  if (bt == 1) return gemv_dispatch<WT, 1>(p, mode, grid, smem, s, pdl, co);
+  if (bt == 2) return gemv_dispatch<WT, 2>(p, mode, grid, smem, s, pdl, co);
+  return gemv_dispatch<WT, 4>(p, mode, grid, smem, s, pdl, co);
 }
 
 // Batches of 1..4 rows run on the CUDA-core GEMV; larger batches run on the
@@ -757,7 +802,7 @@ cudaError_t launch_gemv(const GemvParams& p0, int mode, int wdt, int num_sms, cu
       p.kfull = p.K;
       p.ldw = p.K;
       p.shard_tasks = p.n_tasks;
-      cudaError_t e = launch_gemv_mma(p, mode, wdt, s, pdl);
+      cudaError_t e = launch_gemv_mma(p, mode, wdt, num_sms, s, pdl);
       if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -828,8 +873,9 @@ cudaError_t launch_gemv(const GemvParams& p0, int mode, int wdt, int num_sms, cu
     int grid = (p.n_tasks + tpc - 1) / tpc;
     const int cap = num_sms * 8;
     if (grid > cap) grid = cap;
-    cudaError_t e = wdt == WDT_F16 ? gemv_dispatch_bt<f16>(p, bt, mode, grid, smem, s, pdl)
-                                   : gemv_dispatch_bt<bf16>(p, bt, mode, grid, smem, s, pdl);
+    const int co = p.carve ? gemv_carveout(grid, smem, bt, mode, wdt, num_sms) : -1;
+    cudaError_t e = wdt == WDT_F16 ? gemv_dispatch_bt<f16>(p, bt, mode, grid, smem, s, pdl, co)
+                                   : gemv_dispatch_bt<bf16>(p, bt, mode, grid, smem, s, pdl, co);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -113,6 +113,34 @@ inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// launch_k with a preferred shared-memory carveout for this launch (percent of
+// the SM's maximum shared memory; the rest of the unified memory is L1; a
+// negative value leaves the choice to the driver).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k_carveout(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                     bool pdl, int carveout_pct, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (carveout_pct >= 0) {
+    attr[n].id = cudaLaunchAttributePreferredSharedMemoryCarveout;
+    attr[n].val.sharedMemCarveout = (unsigned)carveout_pct;
+    ++n;
+  }
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // ---------------------------------------------------------------------------
 // Kernel parameter blocks
 // ---------------------------------------------------------------------------
@@ -147,8 +175,9 @@ struct GemvParams {
   const void* w2;    // QKV: wv
   int n_tasks;       // row pairs (QKV, RESID, LOGITS) or rows (GATEUP)
   int kc;            // K chunk staged in shared memory (multiple of 256)
-  int ks;            // warps that split one task's K range (1, 2, 4, 8; > 1 only with a single chunk)
+  int ks;            // warps that split one task's K range (1, 2, 4, 8; with chunked rows, of each chunk)
   int* err;          // device error word
+  int carve;         // 1: the launch asks for the smallest shared-memory carveout holding its CTAs
   // Row-parallel shard partials (GEMV_PARTIAL): K is one shard's depth, kfull
   // the whole input row, ldw the weight row stride; task t is row pair
   // t % shard_tasks of shard t / shard_tasks.  Other modes: kfull = ldw = K.

@@ -51,6 +51,8 @@ constexpr int kSplitLen = 128;      // keys per decode-attention split
 constexpr int kArgmaxBlocks = 64;   // partial argmax blocks per sequence
 // Largest decode projection (weight bytes) launched with programmatic dependent launch.
 constexpr size_t kPdlMaxWeightBytes = (size_t)128 << 20;
+// Decode carveout rule (see ladder_model::gemv_carve): 8.4 MB (1.2B) off, 33.5 MB (8B) on.
+constexpr size_t kCarveoutMinWeightBytes = (size_t)16 << 20;
 
 // Split-K workspace of the batched decode projections (B > 2), one region per
 // projection kind so that the two decode streams never share one.
@@ -198,6 +200,16 @@ struct ladder_model {
   char* ws;
   Plan plan;
   int num_sms;
+  // Decode projections ask, launch by launch, for the smallest shared-memory
+  // carveout that holds their CTAs (the rest of the SM's unified memory is L1
+  // for the weight loads in flight) when the model's smallest projection has
+  // at least kCarveoutMinWeightBytes of weights; else the driver chooses.
+  // Measured on the graph decode step (context 2048): 8B hybrid B = 1 2914 ->
+  // 2828 us, shard mode (k = 8) 3221 -> 3176 us, 70B unchanged; 1.2B (8.4 MB O
+  // projection) 587 -> 600 us with every launch, 617 us with only those of at
+  // least 32 MB -- its short launches of the two ladder streams share SMs, which
+  // launches of different carveouts cannot.
+  bool gemv_carve = false;
   int residual_mode = LADDER_RESIDUAL_CONFIG;
   int flags = 0;
   // next-token rule: greedy when samp_t <= 0, else temperature / top-k sampling
@@ -424,6 +436,16 @@ int ladder_create(const ladder_config* cfg, const ladder_weights* w, void* works
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  {
+    const ladder_config& c = *cfg;
+    const size_t d = c.d_model, qd = (size_t)c.n_q_heads * c.head_dim, kvd = (size_t)c.n_kv_heads * c.head_dim;
+    const size_t f = c.ffn_dim;
+    size_t smallest = d * (qd + 2 * kvd);  // elements of the QKV, O, gate/up and down weights
+    if (qd * d < smallest) smallest = qd * d;
+    if (2 * d * f < smallest) smallest = 2 * d * f;
+    if (d * f < smallest) smallest = d * f;
+    m->gemv_carve = smallest * 2 >= kCarveoutMinWeightBytes;
+  }
   if (e == cudaSuccess) e = gemv_configure();
   if (e == cudaSuccess) e = gemm_tc_configure();
   if (e == cudaSuccess) e = attn_prefill_tcgen05_configure();
@@ -742,9 +764,11 @@ int enqueue_decode_shard(ladder_model* m, ladder_kv* kv, const int32_t* tokens, 
     if ((rc = use(j))) return rc;
     float* pk = part + (size_t)(k & 1) * part_stride;
     GemvParams o{};
+    o.carve = m->gemv_carve;
     if (k & 1) {  // attention module
       const KvLayer kvl = kv->layer(l);
       GemvParams g{};
+      g.carve = m->gemv_carve;
       g.x = m->X(j); g.ldx = d; g.g = L.attn_norm; g.eps = c.norm_eps; g.B = B; g.K = d;
       g.w0 = L.wq; g.w1 = L.wk; g.w2 = L.wv; g.n_tasks = (qd + 2 * kvd) / 2;
       g.out = q; g.ldo = qd; g.nq_hd = qd; g.nkv_hd = kvd;
@@ -764,6 +788,7 @@ int enqueue_decode_shard(ladder_model* m, ladder_kv* kv, const int32_t* tokens, 
       o.x = ao; o.ldx = qd; o.K = qd / ksh; o.kfull = qd; o.ldw = qd; o.w0 = L.wo;
     } else {  // MLP module
       GemvParams g{};
+      g.carve = m->gemv_carve;
       g.x = m->X(j); g.ldx = d; g.g = L.mlp_norm; g.eps = c.norm_eps; g.B = B; g.K = d;
       g.w0 = L.w_gate; g.w1 = L.w_up; g.n_tasks = f; g.out = act; g.ldo = f; g.err = m->err();
       auto pe = m->probe_start(LADDER_PROBE_GATEUP, s);
@@ -790,6 +815,7 @@ int enqueue_decode_shard(ladder_model* m, ladder_kv* kv, const int32_t* tokens, 
   }
   if ((rc = use(2 * c.n_layers))) return rc;
   GemvParams h{};
+  h.carve = m->gemv_carve;
   h.x = m->X(2 * c.n_layers); h.ldx = d; h.g = m->final_norm; h.eps = c.norm_eps; h.B = B; h.K = d;
   h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.out = logits; h.ldo = c.vocab; h.err = m->err();
   m->splitk(h, SK_LMHEAD);
@@ -867,6 +893,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       const int j = m->input_index(k);
       if ((rc = use(j, 0))) return rc;
       GemvParams g{};
+      g.carve = m->gemv_carve;
       g.x = m->X(j); g.ldx = d; g.g = L.attn_norm; g.eps = c.norm_eps; g.B = B; g.K = d;
       g.w0 = L.wq; g.w1 = L.wk; g.w2 = L.wv; g.n_tasks = (qd + 2 * kvd) / 2;
       g.out = q; g.ldo = qd; g.nq_hd = qd; g.nkv_hd = kvd;
@@ -895,6 +922,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
 
       if ((rc = use(k - 1, 0))) return rc;
       GemvParams o{};
+      o.carve = m->gemv_carve;
       o.x = ao; o.ldx = qd; o.g = nullptr; o.B = B; o.K = qd; o.w0 = L.wo; o.n_tasks = d / 2;
       o.out = m->X(k); o.ldo = d; o.x_res = m->X(k - 1); o.ldr = d;
       pe = m->probe_start(LADDER_PROBE_OUT, s);
@@ -912,6 +940,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       cudaStream_t ms = streams[mlp_stream];
       if ((rc = use(j, mlp_stream))) return rc;
       GemvParams g{};
+      g.carve = m->gemv_carve;
       g.x = m->X(j); g.ldx = d; g.g = L.mlp_norm; g.eps = c.norm_eps; g.B = B; g.K = d;
       g.w0 = L.w_gate; g.w1 = L.w_up; g.n_tasks = f; g.out = act; g.ldo = f;
       auto pe = m->probe_start(LADDER_PROBE_GATEUP, ms);
@@ -923,6 +952,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
 
       if ((rc = use(k - 1, mlp_stream))) return rc;
       GemvParams o{};
+      o.carve = m->gemv_carve;
       o.x = act; o.ldx = f; o.g = nullptr; o.B = B; o.K = f; o.w0 = L.w_down; o.n_tasks = d / 2;
       o.out = m->X(k); o.ldo = d; o.x_res = m->X(k - 1); o.ldr = d;
       pe = m->probe_start(LADDER_PROBE_DOWN, ms);
@@ -936,6 +966,7 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
   }
   if ((rc = use(2 * c.n_layers, 0))) return rc;
   GemvParams h{};
+  h.carve = m->gemv_carve;
   h.x = m->X(2 * c.n_layers); h.ldx = d; h.g = m->final_norm; h.eps = c.norm_eps; h.B = B; h.K = d;
   h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.out = logits; h.ldo = c.vocab;
   auto pe = m->probe_start(LADDER_PROBE_LMHEAD, s);
@@ -1141,6 +1172,7 @@ extern "C" int ladder_prefill(ladder_model* m, ladder_kv* kv, const int32_t* tok
     }
   }
   GemvParams h{};
+  h.carve = m->gemv_carve;
   h.ldx = d; h.g = m->final_norm; h.eps = c.norm_eps; h.K = d;
   h.w0 = m->lm_head; h.n_tasks = c.vocab / 2; h.ldo = c.vocab;
   h.err = m->err();
