@@ -107,7 +107,8 @@ def test_bf16_batched_decode_on_tensor_cores():
 
 @pytest.mark.parametrize("graph", [False, True])
 def test_medium_head_dim_128_and_split_k(graph):
-    """head_dim 128 in both attention kernels; the down projection (K = 3072) streams in two chunks."""
+    """head_dim 128 in both attention kernels; at 3 rows the projections take the split-K
+    tensor-core path (the down projection's K = 3072 in three slices)."""
     dims = small_dims(d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=3072, vocab=2048,
                       n_layers=2, n_standard_layers=0)
     gw, ow = gpu_weights(dims), oracle_weights(dims)
@@ -119,6 +120,25 @@ def test_medium_head_dim_128_and_split_k(graph):
     o_logits, _ = O.teacher_forced_decode(dims, ow, prompts, feed)
     for s_ in range(4):
         compare_logits(g_logits[s_], o_logits[s_], f"medium step {s_}")
+
+
+@pytest.mark.parametrize("B", [1, 2])
+def test_decode_rows_longer_than_one_staged_chunk(B):
+    """Decode projections whose rows exceed the GEMV's staging buffer (ffn 20480 > 16384
+    columns per batch row): the down projection stages its rows in chunks and splits K
+    across warps within each chunk (B = 1: 2 chunks of 10240, K split 4; B = 2: 4 chunks
+    of 5120, the launch shapes that fit one wave)."""
+    dims = small_dims(d_model=1024, n_q_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=20480, vocab=2048,
+                      n_layers=2, n_standard_layers=0)
+    gw, ow = gpu_weights(dims), oracle_weights(dims)
+    lens = [37, 5][:B]
+    prompts = prompts_for(lens, dims["vocab"])
+    feed = np.stack([synth.tokens(3, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(B)])
+    model = make_model(dims, gw, max_batch=B, max_seq=64, page_size=32)
+    g_logits, _ = run_teacher_forced(model, prompts, feed, graph=True)
+    o_logits, _ = O.teacher_forced_decode(dims, ow, prompts, feed)
+    for s_ in range(4):
+        compare_logits(g_logits[s_], o_logits[s_], f"long rows B={B} step {s_}")
 
 
 def test_kv_cache_layout_is_bit_exact(tiny):
