@@ -274,8 +274,10 @@ int ladder_decode_step(ladder_model* m, ladder_kv* kv, const int32_t* tokens, in
 /* Reads and clears the device error word (synchronises `stream`).  *code is 0
  * when no kernel reported a problem, else an OR of: 1 = a token id was outside
  * [0, vocab) (its row used a zero embedding); 2 = a pipeline wait ran out of
- * time and the kernel stopped early; 4 = a projection produced inf or NaN (for
- * example an activation beyond the 16-bit range of fp16 storage). */
+ * time and the kernel stopped early; 4 = a projection produced inf or NaN in a
+ * 16-bit output (for example an activation beyond the range of fp16 storage):
+ * the prefill GEMMs' 16-bit operands and cache writes, and the decode
+ * projection's K/V cache write. */
 int ladder_get_device_error(ladder_model* m, ladder_stream_t stream, int32_t* code);
 
 /* Number of kernel launches the last prefill / decode call issued (a decode

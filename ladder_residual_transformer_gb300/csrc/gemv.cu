@@ -107,7 +107,9 @@ __device__ __forceinline__ void gemv_store(const GemvParams& p, int task, int b,
     } else {
       const int head = local / hd, dim = local % hd;
       WT* dst = static_cast<WT*>(p.kv.base) + p.kv.slot(b, pos, kind - 1, head) + dim;
-      *reinterpret_cast<uint32_t*>(dst) = C::pack(r0, r1);
+      const uint32_t pk = C::pack(r0, r1);
+      *reinterpret_cast<uint32_t*>(dst) = pk;
+      if (C::bad(pk) && p.err != nullptr) atomicOr(p.err, ERR_NONFINITE);  // beyond the 16-bit range
     }
   } else if (MODE == GEMV_GATEUP) {
     p.out[(size_t)b * p.ldo + task] = silu_f(v0) * v1;

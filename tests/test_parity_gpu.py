@@ -523,6 +523,36 @@ def test_non_finite_projection_output_is_flagged():
     assert codes["bf16"] == 0, codes
 
 
+def test_non_finite_decode_kv_write_is_flagged():
+    """A decode step whose new K values leave the fp16 range (the K projection of
+    layer 0 scaled by 2^18, still finite fp16 weights) reports bit 4 of the device
+    error word from the decode projection's cache write (the prefill's own flags
+    are read, and so cleared, first); the same model with bf16 storage reports
+    nothing."""
+    dims = small_dims()
+
+    def scale(name, layer, bits):
+        if layer != 0 or name != "wk":
+            return bits
+        f = (bits.astype(np.uint32) << 16).view(np.float32) * np.float32(2.0 ** 18)  # exact: a power of two
+        return (f.view(np.uint32) >> 16).astype(np.uint16)
+
+    prompts = prompts_for([24], dims["vocab"])
+    codes = {}
+    for dtype in ("fp16", "bf16"):
+        model = make_model(dims, gpu_weights(dims, transform=scale, dtype=dtype), max_batch=1, max_seq=32,
+                           page_size=16)
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            _, nt = model.prefill(packed(prompts), [24])
+            model.device_error(s)
+            model.decode_step(nt)
+            codes[dtype] = model.device_error(s)
+        model.close()
+    assert codes["fp16"] & 4, codes
+    assert codes["bf16"] == 0, codes
+
+
 @pytest.mark.slow
 def test_full_size_1p2b_prefill_and_decode():
     """The 1.2B workload at its full prompt length, in the graph-replay launch
