@@ -1,7 +1,8 @@
 """Full-size workloads on the GPU against the oracle.
 
 - 8B hybrid (32 layers, lower 16 standard) at full depth: prefill of two
-  prompts and two teacher-forced decode steps.
+  prompts and two teacher-forced decode steps; and 16 rows decoded together (the
+  batched tensor-core projections), three of them against the oracle.
 - 8B full ladder in shard mode (k = 8 row/column shards per module, the
   on-device reduce on the second stream): the ladder and the standard schedule
   against the all-ladder and all-standard oracle.
@@ -106,6 +107,28 @@ def test_full_size_8b_hybrid():
     print(f"8B hybrid: max-abs {max(e for e, _ in er):.3e} rel-L2 {max(r for _, r in er):.3e}; "
           f"fast prefill max-abs {fe:.3e}")
     assert rel_sum(got, want) < rel_sum(fast, want)
+
+
+@pytest.mark.slow
+def test_full_size_8b_hybrid_16_rows():
+    """The batched decode of the 8B hybrid at 16 rows, the launch configuration the
+    benchmark times (the split-K tensor-core projections, each launch with its
+    shared-memory carveout), at full depth: 16 ragged prompts and two teacher-forced
+    decode steps; sequences 0, 7 and 15 against the oracle."""
+    dims = dict(synth.PRESETS["8b-hybrid"])
+    lens = [40, 17, 64, 9, 33, 1, 58, 25, 12, 47, 5, 61, 30, 19, 52, 36]
+    prompts = prompts_for(lens, dims["vocab"])
+    feed = np.stack([synth.tokens(2, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(16)])
+    gw = gpu_weights(dims)
+    model = make_model(dims, gw, max_batch=16, max_seq=128, max_prefill_tokens=sum(lens))
+    got = run_tf(model, prompts, feed)
+    model.close()
+    del gw, model
+    torch.cuda.empty_cache()
+    pick = [0, 7, 15]
+    want = oracle_tf(dims, O.synthetic_weights(dims, keep_layers=False), [prompts[b] for b in pick], feed[pick])
+    er = compare_steps(got[:, pick], want, "8B hybrid, 16 rows")
+    print(f"8B hybrid, 16 rows: max-abs {max(e for e, _ in er):.3e} rel-L2 {max(r for _, r in er):.3e}")
 
 
 @pytest.mark.slow
