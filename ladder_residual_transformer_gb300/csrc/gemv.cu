@@ -638,9 +638,9 @@ static const GemvResidency& gemv_residency() {
 // memory that holds the CTAs per SM the launch can use (its grid over the SMs,
 // at most `cap`, what registers and threads allow), so that the rest serves as
 // L1 for the weight loads in flight; -1 (the driver's choice) when unknown.
-// Measured on the batched projection (8B hybrid, 16 rows, context 2048): the
-// 132 KB configuration (3 CTAs per SM) 5090 -> 4910 us per step against the
-// driver's choice; 68 KB (2 CTAs) 5250 us; all shared memory 6100 us.
+// Measured on the batched projection (8B hybrid, 16 rows, context 2048): this
+// request (45%, 3 CTAs per SM) 5090 -> 4930 us per step against the driver's
+// choice; 50% 4910 us; 30% (2 CTAs) 5250 us; all shared memory 6100 us.
 static int carveout_for(long long grid, size_t smem, int static_smem, int cap, int num_sms) {
   const GemvResidency& r = gemv_residency();
   if (cap <= 0 || r.smem_per_sm <= 0 || num_sms <= 0) return -1;
