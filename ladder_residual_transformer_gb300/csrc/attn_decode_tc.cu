@@ -5,12 +5,16 @@
 // TMA copies of the split's K and V pages (3-D map of the pool, 128-byte
 // swizzle: [64-dim block][key][64 dims]); the G = n_q / n_kv query heads of the
 // group, pre-scaled by scale * log2(e), sit as rows 0..G-1 of a 16-row 16-bit
-// tile.  Warp w computes S = Q K^T for keys 32w..32w+31 with mma.sync m16n8k16
-// (K fragments by ldmatrix from the swizzled tile), the row maxima and sums are
-// combined across the warps through shared memory, P (16-bit) is written to
-// shared memory, and warp w computes O = P V for a quarter of the head
-// dimensions (V fragments by ldmatrix.trans).  Keys past the context are masked
-// in S and their V rows zeroed.  The per-split partials (unnormalised O, max in
+// tile, and their rounding remainders (also 16-bit) as rows 8..8+G-1: the MMA's
+// idle padding rows carry the lo half of a hi/lo pair, so S = Q_hi K^T + Q_lo
+// K^T is a sum of two accumulator rows that one thread already holds (about 22
+// significant bits of q at no extra tensor-core work; G <= 8).  Warp w computes
+// S = Q K^T for keys 32w..32w+31 with mma.sync m16n8k16 (K fragments by
+// ldmatrix from the swizzled tile), the row maxima and sums are combined across
+// the warps through shared memory, P is written to shared memory as the same
+// hi/lo row pair, and warp w computes O = P V for a quarter of the head
+// dimensions (V fragments by ldmatrix.trans), adding the two rows of each pair.
+// Keys past the context are masked in S and their V rows zeroed.  The per-split partials (unnormalised O, max in
 // natural-log units, sum) feed the same combine kernel as attn_decode_kernel.
 // Every wait is bounded (bit 1 of the error word on expiry).
 #include "internal.cuh"
@@ -118,14 +122,18 @@ __global__ void __launch_bounds__(AD_THREADS) attn_decode_tc_kernel(const __grid
       }
     }
   }
-  // 2. Queries of the group (rows 0..G-1, pre-scaled for exp2), rows G..15 zero.
+  // 2. Queries of the group, pre-scaled for exp2: rows 0..G-1 the 16-bit values
+  //    (hi), rows 8..8+G-1 their rounding remainders (lo), other rows zero.
   const float qs = p.scale * 1.4426950408889634f;
   const float* qg = p.q + (size_t)b * p.n_q * HD + (size_t)kvh * G * HD;
-  for (int i = tid; i < 16 * (HD / 2); i += AD_THREADS) {
+  for (int i = tid; i < 8 * (HD / 2); i += AD_THREADS) {
     const int r = i / (HD / 2), d2 = (i % (HD / 2)) * 2;
     float2 v = make_float2(0.f, 0.f);
     if (r < G) v = *reinterpret_cast<const float2*>(qg + r * HD + d2);
-    *reinterpret_cast<uint32_t*>(sQ + r * L::LDQ + d2) = C::pack(v.x * qs, v.y * qs);
+    const float a = v.x * qs, c = v.y * qs;
+    const uint32_t hi = C::pack(a, c);
+    *reinterpret_cast<uint32_t*>(sQ + r * L::LDQ + d2) = hi;
+    *reinterpret_cast<uint32_t*>(sQ + (r + 8) * L::LDQ + d2) = C::pack(a - C::lo(hi), c - C::hi(hi));
   }
   const bool ok = mbar_wait(bar, 0, AD_WAIT_LIMIT);
   // keys past the context: zero their V rows (they meet P = 0)
@@ -161,13 +169,15 @@ __global__ void __launch_bounds__(AD_THREADS) attn_decode_tc_kernel(const __grid
       ad_mma<T>(s[j + 1], a0, a1, a2, a3, b2, b3);
     }
   }
-  // rows g (thread holds keys warp*32 + j*8 + 2 t4 + {0,1}); rows g + 8 are padding
+  // row g of S (thread holds keys warp*32 + j*8 + 2 t4 + {0,1}) = accumulator
+  // row g (q hi) + row g + 8 (q lo)
   float mx = -INFINITY;
 #pragma unroll
   for (int j = 0; j < 4; ++j)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int key = warp * 32 + j * 8 + 2 * t4 + e;
+      s[j][e] += s[j][e + 2];
       if (key >= n) s[j][e] = -INFINITY;
       mx = fmaxf(mx, s[j][e]);
     }
@@ -181,9 +191,11 @@ __global__ void __launch_bounds__(AD_THREADS) attn_decode_tc_kernel(const __grid
   for (int j = 0; j < 4; ++j) {
     const float p0 = exp2f(s[j][0] - m), p1 = exp2f(s[j][1] - m);
     sum += p0 + p1;
-    *reinterpret_cast<uint32_t*>(sP + g * L::LDP + warp * 32 + j * 8 + 2 * t4) = C::pack(p0, p1);
-    // rows 8..15 of P are zero
-    *reinterpret_cast<uint32_t*>(sP + (g + 8) * L::LDP + warp * 32 + j * 8 + 2 * t4) = 0u;
+    // row g: P rounded to 16 bits (hi); row g + 8: the rounding remainders (lo)
+    const uint32_t hi = C::pack(p0, p1);
+    *reinterpret_cast<uint32_t*>(sP + g * L::LDP + warp * 32 + j * 8 + 2 * t4) = hi;
+    *reinterpret_cast<uint32_t*>(sP + (g + 8) * L::LDP + warp * 32 + j * 8 + 2 * t4) =
+        C::pack(p0 - C::lo(hi), p1 - C::hi(hi));
   }
   sum += __shfl_xor_sync(0xffffffffu, sum, 1);
   sum += __shfl_xor_sync(0xffffffffu, sum, 2);
@@ -212,8 +224,9 @@ __global__ void __launch_bounds__(AD_THREADS) attn_decode_tc_kernel(const __grid
   if (g < G) {
     const size_t idx = ((size_t)b * p.n_q + (size_t)kvh * G + g) * p.nsplit + split;
 #pragma unroll
-    for (int j = 0; j < NT; ++j)
-      *reinterpret_cast<float2*>(p.part_o + idx * HD + d0 + j * 8 + 2 * t4) = make_float2(o[j][0], o[j][1]);
+    for (int j = 0; j < NT; ++j)  // row g (P hi) + row g + 8 (P lo)
+      *reinterpret_cast<float2*>(p.part_o + idx * HD + d0 + j * 8 + 2 * t4) =
+          make_float2(o[j][0] + o[j][2], o[j][1] + o[j][3]);
     if (warp == 0 && t4 == 0) {
       p.part_ml[idx * 2] = m * 0.6931471805599453f;
       p.part_ml[idx * 2 + 1] = red_l[g] + red_l[8 + g] + red_l[16 + g] + red_l[24 + g];
