@@ -118,14 +118,14 @@ def test_full_size_8b_hybrid_batch_independence_and_causality():
     against the oracle's forward pass of that sequence, and changing one token
     of sequence 2 leaves every row of the other sequences, and the rows of
     sequence 2 before it, bitwise unchanged.  Compared on the device (the
-    logits are 8.4 GB).  Then two teacher-forced decode steps of the 4 rows from
+    logits are 8.4 GB).  Then four teacher-forced decode steps of the 4 rows from
     context 4096; sequence 0's logits against the oracle's."""
     dims = dict(synth.PRESETS["8b-hybrid"])
     n, B, p = 4096, 4, 3000
     gw = gpu_weights(dims)
-    model = make_model(dims, gw, max_batch=B, max_seq=n + 4, max_prefill_tokens=B * n)
+    model = make_model(dims, gw, max_batch=B, max_seq=n + 8, max_prefill_tokens=B * n)
     prompts = prompts_for([n] * B, dims["vocab"])
-    feed = np.stack([synth.tokens(2, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(B)])
+    feed = np.stack([synth.tokens(4, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(B)])
     seq0 = prompts[0]
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
@@ -157,10 +157,10 @@ def test_full_size_8b_hybrid_batch_independence_and_causality():
     assert moved_at
     assert toks[0][[0, 1, 3]].tolist() == toks[1][[0, 1, 3]].tolist()
     # the oracle's stream for sequence 0 alone (sequences are independent, as shown
-    # above), extended by its two fed tokens: rows n and n + 1 are the decode steps'
+    # above), extended by its fed tokens: rows n .. n + 3 are the decode steps'
     # logits (cached decode equals re-running the forward pass)
     W = O.synthetic_weights(dims, keep_layers=False)
-    rows = SAMPLED_ROWS + [n, n + 1]
+    rows = SAMPLED_ROWS + [n + i for i in range(feed.shape[1])]
     _, hist = O.forward(dims, W, [np.concatenate([seq0, feed[0]]).astype(np.int32)], [O.SeqCache()],
                         return_stream=True)
     xl = hist[0][2 * dims["n_layers"]][rows]
@@ -168,5 +168,5 @@ def test_full_size_8b_hybrid_batch_independence_and_causality():
     want = O.rmsnorm(xl, W.glob("final_norm"), dims["norm_eps"]) @ W.glob("lm_head").T
     for i, r in enumerate(SAMPLED_ROWS):
         compare_logits(sampled[i], want[i], f"8B hybrid 4 x 4096 prefill, sequence 0 row {r}")
-    for i in range(2):
+    for i in range(feed.shape[1]):
         compare_logits(dec[i], want[len(SAMPLED_ROWS) + i], f"8B hybrid, 4 rows from context 4096, decode step {i + 1}")

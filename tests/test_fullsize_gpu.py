@@ -5,8 +5,9 @@
   contexts of 1133-2048 tokens (the batched tensor-core projections), the longest
   and the shortest against the oracle.
 - 8B full ladder in shard mode (k = 8 row/column shards per module, the
-  on-device reduce on the second stream): the ladder and the standard schedule
-  against the all-ladder and all-standard oracle.
+  on-device reduce on the second stream), four decode steps from context 2048:
+  the ladder and the standard schedule against the all-ladder and all-standard
+  oracle.
 - 70B (80 layers, d_model 8192, 64 q / 8 kv heads of 128, SwiGLU 28672; 141 GB
   of weights resident on the GPU): the 512-token prefill and four decode steps at
   full depth against the oracle, which regenerates one layer at a time so that host memory
@@ -115,12 +116,12 @@ def test_full_size_8b_hybrid_16_rows():
     """The batched decode of the 8B hybrid at 16 rows from contexts near 2048 (the
     benchmark's batch-16 configuration: the split-K tensor-core projections, each
     launch with its shared-memory carveout) at full depth: 16 ragged prompts of
-    1133-2048 tokens and two teacher-forced decode steps; the longest and the
+    1133-2048 tokens and four teacher-forced decode steps; the longest and the
     shortest sequence against the oracle."""
     dims = dict(synth.PRESETS["8b-hybrid"])
     lens = [2048 - 61 * i for i in range(16)]
     prompts = prompts_for(lens, dims["vocab"])
-    feed = np.stack([synth.tokens(2, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(16)])
+    feed = np.stack([synth.tokens(4, dims["vocab"], seed=synth.DECODE_SEED, stream=b) for b in range(16)])
     gw = gpu_weights(dims)
     model = make_model(dims, gw, max_batch=16, max_seq=2048 + 8, max_prefill_tokens=sum(lens))
     got = run_tf(model, prompts, feed)
@@ -137,15 +138,15 @@ def test_full_size_8b_hybrid_16_rows():
 @pytest.mark.slow
 def test_full_size_8b_ladder_shard_mode():
     """Config of the shard-mode comparison: 8B shapes, every layer ladder,
-    k = 8 shards per module at decode (prefill is unsharded), batch 1; the
-    ladder schedule against the all-ladder oracle and the standard schedule
-    (every module waits for the previous module's reduce) against the
-    all-standard oracle."""
+    k = 8 shards per module at decode (prefill is unsharded), batch 1, four
+    decode steps from context 2048 (the benchmark's); the ladder schedule
+    against the all-ladder oracle and the standard schedule (every module waits
+    for the previous module's reduce) against the all-standard oracle."""
     dims = dict(synth.PRESETS["8b-ladder"])
-    prompt = prompts_for([64], dims["vocab"])
-    feed = synth.tokens(2, dims["vocab"], seed=synth.DECODE_SEED)[None, :]
+    prompt = prompts_for([2048], dims["vocab"])
+    feed = synth.tokens(4, dims["vocab"], seed=synth.DECODE_SEED)[None, :]
     gw = gpu_weights(dims)
-    model = make_model(dims, gw, max_batch=1, max_seq=128, max_prefill_tokens=64, shard_k=8)
+    model = make_model(dims, gw, max_batch=1, max_seq=2048 + 8, max_prefill_tokens=2048, shard_k=8)
     got_l = run_tf(model, prompt, feed)
     model.reset()
     got_s = run_tf(model, prompt, feed, standard=True)
