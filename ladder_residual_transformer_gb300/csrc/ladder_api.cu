@@ -51,6 +51,7 @@ constexpr int kSplitLen = 128;      // keys per decode-attention split
 constexpr int kArgmaxBlocks = 64;   // partial argmax blocks per sequence
 // Largest decode projection (weight bytes) launched with programmatic dependent launch.
 constexpr size_t kPdlMaxWeightBytes = (size_t)128 << 20;
+constexpr size_t kPdlMaxMlpWeightBytes = (size_t)256 << 20;  // the MLP chain's limit at one or two rows
 // Decode carveout rule (see ladder_model::gemv_carve): 8.4 MB (1.2B) off, 33.5 MB (8B) on.
 constexpr size_t kCarveoutMinWeightBytes = (size_t)16 << 20;
 
@@ -851,12 +852,22 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
   // of weights) those blocks would wait on SM slots that the other ladder
   // stream's kernels need, and a long kernel's own blocks would crowd the
   // other stream; so a kernel launches early only when it is short and so is
-  // its predecessor.
+  // its predecessor.  The MLP chain (gate/up -> down, one chain across the
+  // layers: the step's critical path) counts as short up to kPdlMaxMlpWeightBytes
+  // at one or two rows: 8B hybrid B = 1 2828 -> 2763 us, 70B and 1.2B unchanged
+  // (their MLP projections are above or below both limits); the attention
+  // chain keeps the lower limit, since its early blocks hold SM slots the MLP
+  // chain needs (the 70B's O projection, 134 MB, launched early: 20.72 ->
+  // 21.67 ms).  Batched rows keep the lower limit for both (8B at 16 rows
+  // within noise, 4960 vs 4998 us).
   bool long_prev[2] = {false, false};  // per stream: the last kernel was a long projection
-  auto early = [&](int si, size_t weight_bytes) {
-    return pdl && !long_prev[si] && weight_bytes <= kPdlMaxWeightBytes;
+  auto early = [&](int si, size_t weight_bytes, size_t lim = kPdlMaxWeightBytes) {
+    return pdl && !long_prev[si] && weight_bytes <= lim;
   };
-  auto ran = [&](int si, size_t weight_bytes) { long_prev[si] = weight_bytes > kPdlMaxWeightBytes; };
+  auto ran = [&](int si, size_t weight_bytes, size_t lim = kPdlMaxWeightBytes) {
+    long_prev[si] = weight_bytes > lim;
+  };
+  const size_t mlp_lim = B <= 2 ? kPdlMaxMlpWeightBytes : kPdlMaxWeightBytes;
   const size_t wb_qkv = (size_t)(qd + 2 * kvd) * d * 2, wb_o = (size_t)qd * d * 2;
   const size_t wb_gu = (size_t)2 * f * d * 2, wb_down = (size_t)f * d * 2, wb_lm = (size_t)c.vocab * d * 2;
   cudaStream_t streams[2] = {s, m->aux};
@@ -946,8 +957,8 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       auto pe = m->probe_start(LADDER_PROBE_GATEUP, ms);
       g.err = m->err();
       m->splitk(g, SK_GATEUP);
-      LAUNCH(launch_gemv(g, GEMV_GATEUP, m->wdt, m->num_sms, ms, early(mlp_stream, wb_gu)), gemv_launch_count(B, g.K, GEMV_GATEUP));
-      ran(mlp_stream, wb_gu);
+      LAUNCH(launch_gemv(g, GEMV_GATEUP, m->wdt, m->num_sms, ms, early(mlp_stream, wb_gu, mlp_lim)), gemv_launch_count(B, g.K, GEMV_GATEUP));
+      ran(mlp_stream, wb_gu, mlp_lim);
       m->probe_stop(pe, ms);
 
       if ((rc = use(k - 1, mlp_stream))) return rc;
@@ -958,8 +969,8 @@ int enqueue_decode(ladder_model* m, ladder_kv* kv, const int32_t* tokens, int B,
       pe = m->probe_start(LADDER_PROBE_DOWN, ms);
       o.err = m->err();
       m->splitk(o, SK_DOWN);
-      LAUNCH(launch_gemv(o, GEMV_RESID, m->wdt, m->num_sms, ms, early(mlp_stream, wb_down)), gemv_launch_count(B, o.K, GEMV_RESID));
-      ran(mlp_stream, wb_down);
+      LAUNCH(launch_gemv(o, GEMV_RESID, m->wdt, m->num_sms, ms, early(mlp_stream, wb_down, mlp_lim)), gemv_launch_count(B, o.K, GEMV_RESID));
+      ran(mlp_stream, wb_down, mlp_lim);
       m->probe_stop(pe, ms);
       if ((rc = wrote(k, mlp_stream))) return rc;
     }
